@@ -1,0 +1,9 @@
+"""CPU f64 oracle of the blr layer: test infrastructure only (see blr_oracle)."""
+from .blr_oracle import (  # noqa: F401
+    backward,
+    forward,
+    pack_signs,
+    rel_err,
+    unpack_signs,
+    words_per_row,
+)

@@ -1,0 +1,162 @@
+"""CPU f64 oracle of the binary low-rank (blr) linear layer.
+
+TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH. Only the test suite,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference leg may
+import or call this module. The GPU library never routes through it, and the
+two share no code: this file has its own bitmap unpacking, its own packing and
+its own arithmetic.
+
+Source: ``train_mm.rs`` of cortiq-engine 0.8.21 (docs.rs source view). Every
+function below cites the part of that page it restates:
+
+* module documentation, formula block: the layer
+  W_hat = diag(h) . S_U . diag(l) . S_V^T . diag(g) and its six
+  forward/backward formulas;
+* the ``expand`` kernel's comment: the sign-bitmap convention
+  ``[rows][ceil(r/32)]`` u32, bit j of word w is rank 32w+j, a set bit is +1;
+* the test helper ``pack_bits``: a sign is packed as 1 iff its value is > 0;
+* the test ``blr_layer_matches_host``: the per-token f64 host loop this oracle
+  vectorises, and the normwise relative error metric.
+
+Precision: inputs are f32 on the page; they are widened to f64 here and every
+step runs in f64. There is no staging, no f16 and no scaling in the oracle: the
+method reaches the formulas' exact value up to rounding order, so the oracle is
+that definition written out. Matrix products use ``numpy.matmul`` as a library
+primitive, one product per formula, with no blocking, fusion or reordering.
+
+Parity is pinned (see ``tests/test_oracle.py``) by: a brute-force dense W_hat
+built element by element; central finite differences of L = <dy, y> for
+dg, dl, dh and dx (exact, since L is linear in each); Euler identities; a
+hand-written golden bitmap fixture; one-hot l; and integer popcount sums.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "words_per_row",
+    "unpack_signs",
+    "pack_signs",
+    "forward",
+    "backward",
+    "rel_err",
+]
+
+
+def words_per_row(r: int) -> int:
+    """Number of u32 words per bitmap row: ceil(r / 32) (``expand`` kernel comment)."""
+    return (int(r) + 31) // 32
+
+
+def unpack_signs(bits: np.ndarray, rows: int, r: int) -> np.ndarray:
+    """Sign bitmap -> dense +-1 matrix [rows][r] in f64.
+
+    train_mm.rs, ``expand`` kernel comment: the bitmap is ``[rows][words]``
+    u32 with words = ceil(r/32); bit j of word w is rank 32w+j; a set bit is
+    +1 and a clear bit is -1. Bits of the last word at ranks >= r are ignored.
+    """
+    w = words_per_row(r)
+    bits = np.asarray(bits, dtype=np.uint32).reshape(rows, w)
+    out = np.empty((rows, r), dtype=np.float64)
+    for k in range(r):
+        word = bits[:, k // 32]
+        bit = (word >> np.uint32(k % 32)) & np.uint32(1)
+        out[:, k] = np.where(bit == 1, 1.0, -1.0)
+    return out
+
+
+def pack_signs(src: np.ndarray) -> np.ndarray:
+    """Dense values [rows][r] -> sign bitmap [rows][ceil(r/32)] u32.
+
+    train_mm.rs, test helper ``pack_bits``: bit (row, k) is set iff
+    src[row, k] > 0. Zero, -0.0 and NaN therefore pack as -1. Unused high
+    bits of the last word are written 0.
+    """
+    src = np.asarray(src)
+    rows, r = src.shape
+    w = words_per_row(r)
+    out = np.zeros((rows, w), dtype=np.uint32)
+    positive = src > 0
+    for k in range(r):
+        out[:, k // 32] |= positive[:, k].astype(np.uint32) << np.uint32(k % 32)
+    return out
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def forward(x, bits_u, bits_v, g, l, h, y_prior=None) -> dict:
+    """blr forward in f64.
+
+    train_mm.rs, module documentation (forward row of the formula block):
+        a = (x (.) g) . S_V        x [M][d_in], S_V [d_in][r]
+        c = (a (.) l) . S_U^T      S_U [d_out][r]
+        y (+)= h (.) c             y [M][d_out]
+    The page's ``Blr`` is "m x n" with m = d_out and n = d_in; S_U is expanded
+    from ``bits_u`` over d_out rows and S_V from ``bits_v`` over d_in rows.
+    ``y_prior`` given = accumulate mode (the page's later paths), else y is
+    overwritten (its first path).
+
+    Returns a dict with y, a and c (f64).
+    """
+    x = _f64(x)
+    g, l, h = _f64(g), _f64(l), _f64(h)
+    M, d_in = x.shape
+    d_out, r = h.shape[0], l.shape[0]
+    s_u = unpack_signs(bits_u, d_out, r)
+    s_v = unpack_signs(bits_v, d_in, r)
+    a = np.matmul(x * g[None, :], s_v)           # [M][r]
+    c = np.matmul(a * l[None, :], s_u.T)         # [M][d_out]
+    y = h[None, :] * c
+    if y_prior is not None:
+        y = _f64(y_prior) + y
+    return {"y": y, "a": a, "c": c}
+
+
+def backward(x, dy, bits_u, bits_v, g, l, h, dx_prior=None) -> dict:
+    """blr backward in f64.
+
+    train_mm.rs, module documentation (backward rows of the formula block):
+        dh  = sum over tokens of dy (.) c
+        db  = (dy (.) h) . S_U
+        dl  = sum over tokens of a (.) db
+        dx' = (db (.) l) . S_V^T
+        dg  = sum over tokens of x (.) dx'
+        dx (+)= g (.) dx'
+    a and c are the forward's intermediates on the same x and parameters,
+    recomputed here. ``dx_prior`` given = accumulate mode, else overwrite.
+    The gradients dh, dl, dg are returned as this call's contribution; the GPU
+    library adds them into caller vectors, so a test adds any prior itself.
+
+    Returns a dict with dx, dg, dl, dh, db and dxp (f64).
+    """
+    x, dy = _f64(x), _f64(dy)
+    g, l, h = _f64(g), _f64(l), _f64(h)
+    fw = forward(x, bits_u, bits_v, g, l, h)
+    a, c = fw["a"], fw["c"]
+    M, d_in = x.shape
+    d_out, r = h.shape[0], l.shape[0]
+    s_u = unpack_signs(bits_u, d_out, r)
+    s_v = unpack_signs(bits_v, d_in, r)
+    dh = np.sum(dy * c, axis=0)
+    db = np.matmul(dy * h[None, :], s_u)         # [M][r]
+    dl = np.sum(a * db, axis=0)
+    dxp = np.matmul(db * l[None, :], s_v.T)      # [M][d_in]
+    dg = np.sum(x * dxp, axis=0)
+    dx = g[None, :] * dxp
+    if dx_prior is not None:
+        dx = _f64(dx_prior) + dx
+    return {"dx": dx, "dg": dg, "dl": dl, "dh": dh, "db": db, "dxp": dxp}
+
+
+def rel_err(got, want) -> float:
+    """Normwise relative error sqrt(sum (got-want)^2 / max(sum want^2, 1e-30)).
+
+    train_mm.rs, test ``blr_layer_matches_host`` (its ``rel`` closure).
+    """
+    got = _f64(got).ravel()
+    want = _f64(want).ravel()
+    num = float(np.sum((got - want) ** 2))
+    den = max(float(np.sum(want * want)), 1e-30)
+    return float(np.sqrt(num / den))

@@ -1,0 +1,320 @@
+"""Pins of the CPU f64 oracle against facts fixed outside the oracle itself.
+
+Each pin uses an independent route to the same number: hand-written fixtures of
+the page's bit convention and pack rule, a dense W_hat built element by element
+with plain loops, central finite differences of L = <dy, y> (exact here because
+L is linear in each of g, l, h and x), Euler identities, one-hot l, and integer
+popcount sums. The planted-mistake tests check that each pin actually catches
+the kind of error it is meant to (a flipped bit order, a dropped factor, a
+transposed operand, a wrong sign).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from binary_rank_linear_gb300 import workloads as wl
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------- fixtures --
+def _read_convention(golden_dir):
+    rows, r = [], None
+    with open(os.path.join(golden_dir, "bitmap_convention.txt")) as f:
+        lines = [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+    words = None
+    for ln in lines:
+        key, _, rest = ln.partition(" ")
+        if key == "r":
+            r = int(rest)
+        elif key == "row":
+            words = [int(w, 16) for w in rest.split()]
+        elif key == "signs":
+            rows.append((words, [1.0 if ch == "+" else -1.0 for ch in rest]))
+    return r, rows
+
+
+def _read_pack(golden_dir):
+    cases, vals = [], None
+    with open(os.path.join(golden_dir, "pack_rule.txt")) as f:
+        for ln in f:
+            ln = ln.strip()
+            if not ln or ln.startswith("#"):
+                continue
+            key, _, rest = ln.partition(" ")
+            if key == "values":
+                vals = [float(v) for v in rest.split()]
+            elif key == "words":
+                cases.append((vals, [int(w, 16) for w in rest.split()]))
+    return cases
+
+
+def _tiny(seed=0, M=3, d_in=6, d_out=5, r=40):
+    rng = np.random.default_rng(seed)
+    su = np.where(rng.random((d_out, r)) < 0.5, 1.0, -1.0).astype(np.float32)
+    sv = np.where(rng.random((d_in, r)) < 0.5, 1.0, -1.0).astype(np.float32)
+    return {
+        "x": rng.standard_normal((M, d_in)).astype(np.float32),
+        "dy": rng.standard_normal((M, d_out)).astype(np.float32),
+        "su": su, "sv": sv,
+        "bu": oracle.pack_signs(su), "bv": oracle.pack_signs(sv),
+        "g": (1 + 0.3 * rng.standard_normal(d_in)).astype(np.float32),
+        "h": (1 + 0.3 * rng.standard_normal(d_out)).astype(np.float32),
+        "l": rng.uniform(0.1, 1.0, r).astype(np.float32),
+    }
+
+
+def _dense_w_loops(su, sv, g, l, h):
+    """W_hat[i][j] = h_i g_j sum_k S_U[i,k] l_k S_V[j,k], element by element."""
+    d_out, r = su.shape
+    d_in = sv.shape[0]
+    w = [[0.0] * d_in for _ in range(d_out)]
+    for i in range(d_out):
+        for j in range(d_in):
+            acc = 0.0
+            for k in range(r):
+                acc += float(su[i][k]) * float(l[k]) * float(sv[j][k])
+            w[i][j] = float(h[i]) * acc * float(g[j])
+    return w
+
+
+def _bruteforce_y_dx(t, W):
+    x, dy = t["x"].astype(np.float64), t["dy"].astype(np.float64)
+    M, d_in = x.shape
+    d_out = dy.shape[1]
+    y = np.zeros((M, d_out))
+    dx = np.zeros((M, d_in))
+    for m in range(M):
+        for i in range(d_out):
+            y[m, i] = sum(W[i][j] * x[m, j] for j in range(d_in))
+        for j in range(d_in):
+            dx[m, j] = sum(dy[m, i] * W[i][j] for i in range(d_out))
+    return y, dx
+
+
+# ------------------------------------------------------- bitmap convention --
+def test_unpack_matches_golden_convention(golden_dir):
+    r, rows = _read_convention(golden_dir)
+    bits = np.array([w for w, _ in rows], dtype=np.uint32)
+    want = np.array([s for _, s in rows])
+    got = oracle.unpack_signs(bits, len(rows), r)
+    assert got.shape == want.shape
+    assert np.array_equal(got, want)
+
+
+def test_pack_matches_golden_rule(golden_dir):
+    for vals, words in _read_pack(golden_dir):
+        got = oracle.pack_signs(np.array([vals], dtype=np.float32))
+        assert got.dtype == np.uint32
+        assert [int(w) for w in got[0]] == words
+
+
+@pytest.mark.parametrize("rows,r", [(7, 64), (5, 40), (3, 32), (9, 1), (4, 95)])
+def test_pack_unpack_roundtrip(rows, r):
+    rng = np.random.default_rng(rows * 100 + r)
+    s = np.where(rng.random((rows, r)) < 0.5, 1.0, -1.0)
+    bits = oracle.pack_signs(s)
+    assert bits.shape == (rows, oracle.words_per_row(r))
+    assert np.array_equal(oracle.unpack_signs(bits, rows, r), s)
+    # unused high bits of the last word are written 0
+    if r % 32:
+        assert np.all(bits[:, -1] >> np.uint32(r % 32) == 0)
+
+
+def test_unpack_ignores_bits_past_r():
+    bits = np.array([[0xFFFFFFFF, 0xFFFFFF00]], dtype=np.uint32)
+    s = oracle.unpack_signs(bits, 1, 40)
+    assert np.all(s[0, :32] == 1.0) and np.all(s[0, 32:] == -1.0)
+
+
+# -------------------------------------------------------- forward/backward --
+@pytest.mark.parametrize("seed", [0, 1])
+def test_forward_backward_match_bruteforce_dense(seed):
+    t = _tiny(seed)
+    W = _dense_w_loops(t["su"], t["sv"], t["g"], t["l"], t["h"])
+    y_bf, dx_bf = _bruteforce_y_dx(t, W)
+    fw = oracle.forward(t["x"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    assert np.allclose(fw["y"], y_bf, rtol=1e-12, atol=1e-12)
+    assert np.allclose(bw["dx"], dx_bf, rtol=1e-12, atol=1e-12)
+
+
+def _loss(t, g=None, l=None, h=None, x=None):
+    y = oracle.forward(t["x"] if x is None else x, t["bu"], t["bv"],
+                       t["g"] if g is None else g, t["l"] if l is None else l,
+                       t["h"] if h is None else h)["y"]
+    return float(np.sum(t["dy"].astype(np.float64) * y))
+
+
+@pytest.mark.parametrize("seed", [2, 3])
+def test_gradients_match_central_differences(seed):
+    """L = <dy, y> is linear in each of g, l, h, x: the central difference is exact."""
+    t = _tiny(seed)
+    bw = oracle.backward(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    eps = 0.25
+    for name, key in (("g", "dg"), ("l", "dl"), ("h", "dh")):
+        base = t[name].astype(np.float64)
+        fd = np.empty_like(base)
+        for i in range(base.size):
+            p, m = base.copy(), base.copy()
+            p[i] += eps
+            m[i] -= eps
+            fd[i] = (_loss(t, **{name: p}) - _loss(t, **{name: m})) / (2 * eps)
+        assert np.allclose(bw[key], fd, rtol=1e-10, atol=1e-10), name
+    x = t["x"].astype(np.float64)
+    fdx = np.empty_like(x)
+    for idx in np.ndindex(*x.shape):
+        p, m = x.copy(), x.copy()
+        p[idx] += eps
+        m[idx] -= eps
+        fdx[idx] = (_loss(t, x=p) - _loss(t, x=m)) / (2 * eps)
+    assert np.allclose(bw["dx"], fdx, rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_euler_identities(name):
+    """y is homogeneous of degree 1 in each of h, l, g and x, so
+    <dh,h> = <dl,l> = <dg,g> = <dx,x> = <dy,y> (single path, overwrite mode)."""
+    w = wl.WORKLOADS[name].with_shape(M=64)
+    t = wl.make_inputs(w)
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    fw = oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    ref = float(np.sum(t["dy"].astype(np.float64) * fw["y"]))
+    for vec, par in ((bw["dh"], t["h"]), (bw["dl"], t["l"]), (bw["dg"], t["g"])):
+        assert math.isclose(float(np.dot(vec, par.astype(np.float64))), ref, rel_tol=1e-9)
+    assert math.isclose(float(np.sum(bw["dx"] * t["x"].astype(np.float64))), ref, rel_tol=1e-9)
+
+
+@pytest.mark.parametrize("k", [0, 31, 32, 39])
+def test_one_hot_l_isolates_rank(k):
+    """l = e_k gives W_hat = (h . S_U[:,k]) (g . S_V[:,k])^T: one bit per row of
+    each bitmap, so the bit-to-rank mapping is pinned."""
+    t = _tiny(5, M=4, d_in=7, d_out=6, r=40)
+    l = np.zeros(40, dtype=np.float32)
+    l[k] = 1.0
+    fw = oracle.forward(t["x"], t["bu"], t["bv"], t["g"], l, t["h"])
+    # bit (row, k) read straight from the packed words
+    bit_u = np.array([(int(t["bu"][i][k // 32]) >> (k % 32)) & 1 for i in range(6)])
+    bit_v = np.array([(int(t["bv"][j][k // 32]) >> (k % 32)) & 1 for j in range(7)])
+    su_k = 2.0 * bit_u - 1.0
+    sv_k = 2.0 * bit_v - 1.0
+    coef = t["x"].astype(np.float64) @ (t["g"].astype(np.float64) * sv_k)
+    want = coef[:, None] * (t["h"].astype(np.float64) * su_k)[None, :]
+    assert np.allclose(fw["y"], want, rtol=1e-12, atol=1e-12)
+
+
+def test_popcount_integer_sums():
+    """x = 1, g = 1: a_k = 2 * (number of +1 in column k of S_V) - d_in, an integer."""
+    d_in, r = 50, 70
+    rng = np.random.default_rng(11)
+    bv = rng.integers(0, 2**32, size=(d_in, 3), dtype=np.uint64).astype(np.uint32)
+    bu = rng.integers(0, 2**32, size=(4, 3), dtype=np.uint64).astype(np.uint32)
+    fw = oracle.forward(np.ones((2, d_in), np.float32), bu, bv, np.ones(d_in, np.float32),
+                        np.ones(r, np.float32), np.ones(4, np.float32))
+    for k in range(r):
+        ones = sum(bin(int(bv[j][k // 32]))[2:].zfill(32)[::-1][k % 32] == "1" for j in range(d_in))
+        assert fw["a"][0, k] == 2 * ones - d_in
+        assert fw["a"][1, k] == 2 * ones - d_in
+
+
+def test_accumulate_mode_adds_prior():
+    t = _tiny(7)
+    y0 = np.full((3, 5), 0.75)
+    dx0 = np.full((3, 6), -1.25)
+    a = oracle.forward(t["x"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    b = oracle.forward(t["x"], t["bu"], t["bv"], t["g"], t["l"], t["h"], y_prior=y0)
+    assert np.array_equal(b["y"], a["y"] + y0)
+    c = oracle.backward(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    d = oracle.backward(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"], dx_prior=dx0)
+    assert np.array_equal(d["dx"], c["dx"] + dx0)
+
+
+def test_rel_err_metric():
+    assert oracle.rel_err([1.0, 2.0], [1.0, 2.0]) == 0.0
+    assert math.isclose(oracle.rel_err([3.0, 4.0], [0.0, 0.0]), math.sqrt(25 / 1e-30))
+    assert math.isclose(oracle.rel_err([1.1, 0.0], [1.0, 0.0]), 0.1, rel_tol=1e-12)
+
+
+def test_pages_case_two_paths_pinned():
+    """The page's own two-path test shape (d_out 256, d_in 384, r 128, 70 tokens),
+    checked path by path against the dense brute force on a token subset."""
+    for path in (0, 1):
+        t = wl.pages_case(path)
+        bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+        fw = oracle.forward(t["x"][:2], bu, bv, t["g"], t["l"], t["h"])
+        W = (t["h"].astype(np.float64)[:, None]
+             * ((t["su"].astype(np.float64) * t["l"].astype(np.float64)[None, :])
+                @ t["sv"].astype(np.float64).T)
+             * t["g"].astype(np.float64)[None, :])
+        # spot-check entries of W against the element-by-element definition
+        for (i, j) in [(0, 0), (17, 300), (255, 383)]:
+            ref = sum(float(t["su"][i][k]) * float(t["l"][k]) * float(t["sv"][j][k]) for k in range(128))
+            assert math.isclose(W[i, j], float(t["h"][i]) * ref * float(t["g"][j]), rel_tol=1e-12)
+        assert np.allclose(fw["y"], t["x"][:2].astype(np.float64) @ W.T, rtol=1e-10, atol=1e-12)
+
+
+# -------------------------------------------------------- planted mistakes --
+def _mutant_unpack_reversed(bits, rows, r):
+    w = oracle.words_per_row(r)
+    bits = np.asarray(bits, dtype=np.uint32).reshape(rows, w)
+    out = np.empty((rows, r))
+    for k in range(r):
+        out[:, k] = np.where((bits[:, k // 32] >> np.uint32(31 - k % 32)) & 1, 1.0, -1.0)
+    return out
+
+
+def test_planted_bit_order_mistake_is_caught(golden_dir, monkeypatch):
+    from oracle import blr_oracle
+    r, rows = _read_convention(golden_dir)
+    bits = np.array([w for w, _ in rows], dtype=np.uint32)
+    want = np.array([s for _, s in rows])
+    monkeypatch.setattr(blr_oracle, "unpack_signs", _mutant_unpack_reversed)
+    assert not np.array_equal(blr_oracle.unpack_signs(bits, len(rows), r), want)
+
+
+@pytest.mark.parametrize("mutant", ["drop_l", "permuted_u_rows", "sign_dh"])
+def test_planted_formula_mistakes_are_caught(mutant, monkeypatch):
+    from oracle import blr_oracle
+    t = _tiny(9, M=3, d_in=6, d_out=6, r=40)
+    real_matmul = np.matmul
+    if mutant == "drop_l":
+        orig = blr_oracle.forward
+
+        def fwd(x, bu, bv, g, l, h, y_prior=None):
+            return orig(x, bu, bv, g, np.ones_like(l), h, y_prior)
+        monkeypatch.setattr(blr_oracle, "forward", fwd)
+        W = _dense_w_loops(t["su"], t["sv"], t["g"], t["l"], t["h"])
+        y_bf, _ = _bruteforce_y_dx(t, W)
+        y = blr_oracle.forward(t["x"], t["bu"], t["bv"], t["g"], t["l"], t["h"])["y"]
+        assert not np.allclose(y, y_bf, rtol=1e-6)
+    elif mutant == "permuted_u_rows":
+        # a wrong row index of S_U (rows reversed) in the backward's db product
+        calls = {"n": 0}
+
+        def mm(a, b):
+            calls["n"] += 1
+            if calls["n"] == 3:          # third product of backward = db
+                return real_matmul(a, b[::-1])
+            return real_matmul(a, b)
+        monkeypatch.setattr(blr_oracle.np, "matmul", mm)
+        bw = blr_oracle.backward(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+        monkeypatch.setattr(blr_oracle.np, "matmul", real_matmul)
+        W = _dense_w_loops(t["su"], t["sv"], t["g"], t["l"], t["h"])
+        _, dx_bf = _bruteforce_y_dx(t, W)
+        assert not np.allclose(bw["dx"], dx_bf, rtol=1e-6)
+    else:
+        bw = blr_oracle.backward(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+        eps = 0.25
+        base = t["h"].astype(np.float64)
+        fd = np.empty_like(base)
+        for i in range(base.size):
+            p, m = base.copy(), base.copy()
+            p[i] += eps
+            m[i] -= eps
+            fd[i] = (_loss(t, h=p) - _loss(t, h=m)) / (2 * eps)
+        assert np.allclose(bw["dh"], fd, rtol=1e-10)
+        assert not np.allclose(-bw["dh"], fd, rtol=1e-6)
