@@ -1,0 +1,407 @@
+"""Benchmark of the blr layer's forward+backward step on GB300.
+
+One step = blr_forward + blr_backward over one batch of synthetic tokens (every
+kernel of the hot path). Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload small]
+  python bench.py --impl reference ...     # the CPU f64 oracle as the reference arm
+
+Timing: W untimed warm-up steps, then K timed steps between a barrier and
+cudaDeviceSynchronize on both sides, measured with CUDA events on the launch
+stream; max over ranks. L2 (129 MB) is defeated by rotating independent
+input/output/workspace sets whose total exceeds twice the L2 size. Kernel-level
+durations for the roofline come from the library's event trace over a second
+timed pass of the same K steps. Multi-GPU: every rank runs its own batch
+(weak scaling); the path needs no collective inside a step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "blr fwd+bwd tokens/sec and TFLOP/s (% of GB300 f16 tensor peak / % HBM BW)"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------- per-kernel work ----
+def kernel_work(name: str, M: int, d_in: int, d_out: int, r: int):
+    """Algorithmic (flops, bytes) of one launch of a kernel of the step.
+
+    Bytes count each tensor the kernel must read or write once (f32 = 4 B,
+    staged f16 = 2 B, bitmaps d*r/8 B); FLOP counts 2 per multiply-add of the
+    sign products.
+    """
+    bits_u = d_out * r / 8
+    bits_v = d_in * r / 8
+    if name == "fwd_prologue":
+        return 0.0, 4.0 * M * d_in + 2.0 * M * d_in + 2 * (bits_u + bits_v)
+    if name == "gemm_fwd1":
+        return 2.0 * M * r * d_in, 2.0 * M * d_in + bits_v + 4.0 * M * r + 2.0 * M * r
+    if name == "gemm_fwd2":
+        return 2.0 * M * r * d_out, 2.0 * M * r + bits_u + 4.0 * M * d_out + 2.0 * M * d_out
+    if name == "bwd_prologue":
+        return 0.0, 4.0 * M * d_out + 2.0 * M * d_out + 2.0 * M * d_out + 2 * (bits_u + bits_v)
+    if name == "gemm_bwd1":
+        return 2.0 * M * r * d_out, 2.0 * M * d_out + bits_u + 4.0 * M * r + 2.0 * M * r
+    if name == "gemm_bwd2":
+        return 2.0 * M * r * d_in, 2.0 * M * r + bits_v + 4.0 * M * d_in + 4.0 * M * d_in
+    if name == "reduce_partials":
+        return 0.0, 4.0 * (d_in + d_out + r) * 2
+    return 0.0, 0.0
+
+
+# --------------------------------------------------------------- clocks -----
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- CPU oracle ------
+def cpu_oracle_rate(w, budget_s: float = 12.0, max_reps: int = 50):
+    """tokens/s of the CPU f64 oracle (as it stands) on the workload's batch,
+    repeated until ``budget_s`` seconds of CPU work have run. For workloads
+    whose batch would exceed the budget, a prefix of the tokens is used."""
+    import oracle
+    from binary_rank_linear_gb300 import workloads as wl
+
+    sample_M = w.M
+    # keep one oracle pass in the seconds range: ~4 f64 GEMMs of 2*M*r*d each
+    per_token = 4.0 * w.r * (w.d_in + w.d_out)
+    while sample_M > 64 and per_token * sample_M > 3e11:
+        sample_M //= 2
+    t = wl.make_inputs(w.with_shape(M=sample_M))
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
+        oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", cores)))
+    return {
+        "value": reps * sample_M / el,
+        "unit": "tokens/s",
+        "cores": min(cores, threads),
+        "kind": "oracle",
+        "sample": f"{reps} x (forward+backward of {sample_M} tokens of {w.name}) in {el:.1f} s, numpy f64",
+    }
+
+
+# ------------------------------------------------------------ GPU arm -------
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import binary_rank_linear_gb300 as blr
+    from binary_rank_linear_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = wl.WORKLOADS[args.workload]
+    M, d_in, d_out, r = w.M, w.d_in, w.d_out, w.r
+    t = wl.make_inputs(w)
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    g, l, h = d(t["g"]), d(t["l"]), d(t["h"])
+    bu, bv = blr.pack_signs(d(t["su"])), blr.pack_signs(d(t["sv"]))
+    x0, dy0 = d(t["x"]), d(t["dy"])
+    ws_bytes = blr.workspace_bytes(M, d_in, d_out, r)
+    set_bytes = 4 * M * (2 * d_in + 2 * d_out) + ws_bytes
+    nsets = max(1, min(64, -(-2 * L2_BYTES // set_bytes) + 1))
+    sets = []
+    for _ in range(nsets):
+        sets.append({
+            "x": x0.clone(), "dy": dy0.clone(),
+            "y": torch.empty(M, d_out, device=dev), "dx": torch.empty(M, d_in, device=dev),
+            "ws": torch.empty(ws_bytes, dtype=torch.uint8, device=dev),
+        })
+    dg = torch.zeros(d_in, device=dev)
+    dl = torch.zeros(r, device=dev)
+    dh = torch.zeros(d_out, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = sets[i % nsets]
+        blr.forward(s["x"], bu, bv, g, l, h, s["y"], s["ws"])
+        blr.backward(s["x"], s["dy"], bu, bv, g, l, h, s["dx"], dg, dl, dh, s["ws"])
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    def barrier():
+        if dist:
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        step(i)
+    status = blr.check_status(sets[0]["ws"])
+    if status:
+        raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    # second timed pass with the per-kernel event trace
+    blr.trace_begin(capacity=16 * args.steps)
+    barrier()
+    for i in range(args.steps):
+        step(i)
+    barrier()
+    trace = blr.trace_end()
+    clk = clocks.stop()
+    for s in sets:
+        st = blr.check_status(s["ws"])
+        if st:
+            raise RuntimeError(f"device status {st:#x}")
+
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    per = {}
+    for name, kms in trace:
+        per.setdefault(name, []).append(kms)
+    launches_per_step = len(trace) / max(1, args.steps)
+    peaks, peak_src = _peaks()
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    kernels = {}
+    for name, lst in per.items():
+        avg = sum(lst) / len(lst)
+        fl, by = kernel_work(name, M, d_in, d_out, r)
+        kernels[name] = {"avg_us": avg * 1e3, "share": sum(lst) / sum(sum(v) for v in per.values()),
+                         "tflops": fl / (avg * 1e-3) / 1e12, "gbs": by / (avg * 1e-3) / 1e9}
+    dom = max(per, key=lambda n: sum(per[n]))
+    fl, by = kernel_work(dom, M, d_in, d_out, r)
+    avg_s = kernels[dom]["avg_us"] * 1e-6
+    t_tc, t_hbm = fl / (tc_peak * 1e12), by / (hbm_peak * 1e9)
+    if t_tc >= t_hbm:
+        roof = {"bound": "tensor", "achieved": fl / avg_s / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": by / avg_s / 1e9, "peak": hbm_peak, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json: bf16 burst, f16 assumed equal)" \
+        if peak_src == "measured" else "fallback"
+    roof["traffic"] = None
+
+    # end-to-end: host buffers through the public API, copies inside the timed region
+    xh = torch.from_numpy(t["x"]).pin_memory()
+    dyh = torch.from_numpy(t["dy"]).pin_memory()
+    yh = torch.empty(M, d_out).pin_memory()
+    dxh = torch.empty(M, d_in).pin_memory()
+    gh = torch.empty(d_in + r + d_out).pin_memory()
+    s0 = sets[0]
+
+    def e2e_step():
+        s0["x"].copy_(xh, non_blocking=True)
+        s0["dy"].copy_(dyh, non_blocking=True)
+        blr.forward(s0["x"], bu, bv, g, l, h, s0["y"], s0["ws"])
+        blr.backward(s0["x"], s0["dy"], bu, bv, g, l, h, s0["dx"], dg, dl, dh, s0["ws"])
+        yh.copy_(s0["y"], non_blocking=True)
+        dxh.copy_(s0["dx"], non_blocking=True)
+        gh[:d_in].copy_(dg, non_blocking=True)
+        gh[d_in:d_in + r].copy_(dl, non_blocking=True)
+        gh[d_in + r:].copy_(dh, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    barrier()
+    e2e_ms = f0.elapsed_time(f1)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    value = world * M * args.steps / (ms * 1e-3)
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{w.name}: {w.note}",
+            "M": M, "d_in": d_in, "d_out": d_out, "r": r,
+            "mode": "overwrite y/dx, dynamic per-token gradient scale",
+            "l2": f"{nsets} rotating input/output/workspace sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)",
+        },
+        "tflops": world * w.flops * args.steps / (ms * 1e-3) / 1e12,
+        "tensor_frac": (world * w.flops * args.steps / (ms * 1e-3) / 1e12) / tc_peak,
+        "hbm_frac": (w.canonical_bytes * args.steps / (ms * 1e-3) / 1e9) / hbm_peak,
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "clocks": clk,
+        "e2e": {"value": world * M * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 4 * M * (d_in + d_out),
+                "d2h_bytes_per_step": 4 * (M * (d_in + d_out) + d_in + r + d_out)},
+    }
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="blr", choices=["blr", "reference"])
+    ap.add_argument("--workload", default="small")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    from binary_rank_linear_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        budget = 10.0
+        t0 = time.perf_counter()
+        for _ in range(args.warmup):
+            pass
+        per_step = []
+        base = None
+        for _ in range(args.steps):
+            base = cpu_oracle_rate(w, budget_s=min(budget, 120.0 / max(1, args.steps)), max_reps=1)
+            per_step.append(base["value"])
+        value = statistics.median(per_step)
+        el = time.perf_counter() - t0
+        base["value"] = value
+        out = {
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.M / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"{w.name}: {w.note}", "M": w.M, "d_in": w.d_in,
+                                            "d_out": w.d_out, "r": w.r},
+            "cpu_baseline": base,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": el,
+        }
+        print(json.dumps(out))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_oracle_rate(w)
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,29 @@
+"""GB300-native (sm_103a) binary low-rank (blr) linear layer, forward and backward.
+
+The compute path is the CUDA library ``_lib/libblr.so`` (C ABI in
+``include/blr.h``); this package is its thin Python binding plus the seeded
+synthetic workloads used by the tests and the benchmark.
+"""
+from ._binding import (  # noqa: F401
+    BLR_ERR_ALIGN,
+    BLR_ERR_ARG,
+    BLR_ERR_CUDA,
+    BLR_ERR_DEVICE_CHECK,
+    BLR_ERR_SHAPE,
+    BLR_ERR_STATE,
+    BLR_ERR_UNSUPPORTED_DEVICE,
+    BLR_ERR_WORKSPACE,
+    BLR_OK,
+    BlrError,
+    alloc_workspace,
+    backward,
+    check_status,
+    forward,
+    load,
+    pack_signs,
+    trace_begin,
+    trace_end,
+    unpack_signs,
+    words_per_row,
+    workspace_bytes,
+)

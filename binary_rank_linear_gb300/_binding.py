@@ -1,0 +1,191 @@
+"""ctypes binding of libblr.so: the C ABI of include/blr.h with the same names.
+
+Argument marshalling only: torch tensors are checked for device, dtype, shape
+and contiguity, their data pointers and the current CUDA stream are passed to
+the library, and negative status codes become ``BlrError``. Every step of the
+layer runs in the library's CUDA kernels; if the library is missing this module
+raises instead of computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB
+
+BLR_OK = 0
+BLR_ERR_ARG = -1
+BLR_ERR_SHAPE = -2
+BLR_ERR_ALIGN = -3
+BLR_ERR_WORKSPACE = -4
+BLR_ERR_STATE = -5
+BLR_ERR_CUDA = -6
+BLR_ERR_DEVICE_CHECK = -7
+BLR_ERR_UNSUPPORTED_DEVICE = -8
+
+_lib = None
+
+
+class BlrError(RuntimeError):
+    """A negative status returned by the blr library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = load().blr_status_string(code).decode()
+        super().__init__(f"{where}: {msg} (status {code})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libblr.so from the package tree (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise RuntimeError(
+            f"{LIB} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.blr_workspace_bytes.argtypes = [I, I, I, I]
+    lib.blr_workspace_bytes.restype = Z
+    lib.blr_pack_signs.argtypes = [P, P, I, I, P]
+    lib.blr_unpack_signs.argtypes = [P, P, I, I, P]
+    lib.blr_forward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, Z, P]
+    lib.blr_backward.argtypes = [P, P, P, P, P, P, P, P, I, P, P, P, F, I, I, I, I, P, Z, P]
+    lib.blr_check_status.argtypes = [P, Z, P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.blr_status_string.argtypes = [I]
+    lib.blr_status_string.restype = ctypes.c_char_p
+    lib.blr_trace_begin.argtypes = [I]
+    lib.blr_trace_read.argtypes = [I, ctypes.POINTER(ctypes.c_float)]
+    lib.blr_trace_read.restype = ctypes.c_char_p
+    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_check_status",
+              "blr_trace_begin", "blr_trace_end", "blr_trace_count"):
+        getattr(lib, f).restype = I
+    _lib = lib
+    return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor, name: str, dtype, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _check(code: int, where: str) -> None:
+    if code != BLR_OK:
+        raise BlrError(code, where)
+
+
+def words_per_row(r: int) -> int:
+    return (r + 31) // 32
+
+
+def workspace_bytes(M: int, d_in: int, d_out: int, r: int) -> int:
+    return int(load().blr_workspace_bytes(M, d_in, d_out, r))
+
+
+def alloc_workspace(M: int, d_in: int, d_out: int, r: int, device=None) -> torch.Tensor:
+    """A caller-owned workspace for one layer instance (torch owns the memory)."""
+    n = workspace_bytes(M, d_in, d_out, r)
+    if n == 0:
+        raise BlrError(BLR_ERR_SHAPE, "workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def pack_signs(src: torch.Tensor, bits: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """bits[rows][ceil(r/32)] (int32 storage of u32 words) from src[rows][r] f32."""
+    rows, r = src.shape
+    if bits is None:
+        bits = torch.empty(rows, words_per_row(r), dtype=torch.int32, device=src.device)
+    _check(load().blr_pack_signs(_ptr(src, "src", torch.float32), _ptr(bits, "bits", torch.int32,
+                                 (rows, words_per_row(r))), rows, r, _stream(stream)), "blr_pack_signs")
+    return bits
+
+
+def unpack_signs(bits: torch.Tensor, r: int, dst: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """+-1 f16 [rows][r] from a bitmap, through the GEMMs' expansion code."""
+    rows = bits.shape[0]
+    if dst is None:
+        dst = torch.empty(rows, r, dtype=torch.float16, device=bits.device)
+    _check(load().blr_unpack_signs(_ptr(bits, "bits", torch.int32, (rows, words_per_row(r))),
+                                   _ptr(dst, "dst", torch.float16, (rows, r)), rows, r, _stream(stream)),
+           "blr_unpack_signs")
+    return dst
+
+
+def forward(x, bits_u, bits_v, g, l, h, y, ws, accumulate: bool = False, stream=None) -> torch.Tensor:
+    """y (+)= h.c with a = (x.g) S_V, c = (a.l) S_U^T; the tape goes to ``ws``."""
+    M, d_in = x.shape
+    d_out, r = h.shape[0], l.shape[0]
+    w = words_per_row(r)
+    code = load().blr_forward(
+        _ptr(x, "x", torch.float32, (M, d_in)), _ptr(bits_u, "bits_u", torch.int32, (d_out, w)),
+        _ptr(bits_v, "bits_v", torch.int32, (d_in, w)), _ptr(g, "g", torch.float32, (d_in,)),
+        _ptr(l, "l", torch.float32, (r,)), _ptr(h, "h", torch.float32, (d_out,)),
+        _ptr(y, "y", torch.float32, (M, d_out)), int(bool(accumulate)), M, d_in, d_out, r,
+        _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check(code, "blr_forward")
+    return y
+
+
+def backward(x, dy, bits_u, bits_v, g, l, h, dx, dg, dl, dh, ws, gscale: float = 0.0,
+             accumulate: bool = False, stream=None) -> torch.Tensor:
+    """dx (+)= g.dx'; dg, dl, dh += their token sums (the last forward's tape in ``ws``)."""
+    M, d_in = x.shape
+    d_out, r = h.shape[0], l.shape[0]
+    w = words_per_row(r)
+    code = load().blr_backward(
+        _ptr(x, "x", torch.float32, (M, d_in)), _ptr(dy, "dy", torch.float32, (M, d_out)),
+        _ptr(bits_u, "bits_u", torch.int32, (d_out, w)), _ptr(bits_v, "bits_v", torch.int32, (d_in, w)),
+        _ptr(g, "g", torch.float32, (d_in,)), _ptr(l, "l", torch.float32, (r,)),
+        _ptr(h, "h", torch.float32, (d_out,)), _ptr(dx, "dx", torch.float32, (M, d_in)),
+        int(bool(accumulate)), _ptr(dg, "dg", torch.float32, (d_in,)), _ptr(dl, "dl", torch.float32, (r,)),
+        _ptr(dh, "dh", torch.float32, (d_out,)), float(gscale), M, d_in, d_out, r,
+        _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check(code, "blr_backward")
+    return dx
+
+
+def check_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the workspace's device status word (0 = no failure)."""
+    code = ctypes.c_uint32(0)
+    rc = load().blr_check_status(_ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream), ctypes.byref(code))
+    if rc not in (BLR_OK, BLR_ERR_DEVICE_CHECK):
+        raise BlrError(rc, "blr_check_status")
+    return int(code.value)
+
+
+def trace_begin(capacity: int = 64) -> None:
+    _check(load().blr_trace_begin(capacity), "blr_trace_begin")
+
+
+def trace_end() -> list:
+    """Stop tracing; return [(kernel name, ms), ...] for the kernels recorded."""
+    lib = load()
+    lib.blr_trace_end()
+    out = []
+    for i in range(lib.blr_trace_count()):
+        ms = ctypes.c_float(0.0)
+        name = lib.blr_trace_read(i, ctypes.byref(ms))
+        if name is None:
+            raise BlrError(BLR_ERR_CUDA, "blr_trace_read")
+        out.append((name.decode(), float(ms.value)))
+    return out

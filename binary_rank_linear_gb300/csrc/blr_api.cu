@@ -1,0 +1,459 @@
+// Host side of the blr C ABI (include/blr.h): argument and shape checks,
+// workspace layout, TMA descriptors, GEMM tile choice and the launch sequence
+// of the forward and backward passes on the caller's stream.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/blr.h"
+#include "blr_kernels.h"
+
+namespace blr {
+cudaError_t launch_gemm_fwd(int epi, int bn, const CUtensorMap &tmap_a, const GemmArgs &args, int grid,
+                            cudaStream_t s);
+cudaError_t launch_gemm_bwd(int epi, int bn, const CUtensorMap &tmap_a, const GemmArgs &args, int grid,
+                            cudaStream_t s);
+
+// ------------------------------------------------------------ tracing ------
+namespace {
+struct TraceState {
+    bool on = false;
+    int cap = 0;
+    int n = 0;
+    std::vector<cudaEvent_t> ev;
+    std::vector<const char *> names;
+};
+thread_local TraceState g_trace;
+}  // namespace
+
+void trace_before(const char *name, cudaStream_t stream) {
+    TraceState &t = g_trace;
+    if (!t.on || t.n >= t.cap) return;
+    t.names[t.n] = name;
+    cudaEventRecord(t.ev[2 * t.n], stream);
+}
+
+void trace_after(cudaStream_t stream) {
+    TraceState &t = g_trace;
+    if (!t.on || t.n >= t.cap) return;
+    cudaEventRecord(t.ev[2 * t.n + 1], stream);
+    ++t.n;
+}
+
+cudaError_t launch_gemm(int epi, int bn, const CUtensorMap &tmap_a, const GemmArgs &args, int grid,
+                        cudaStream_t s) {
+    static const char *names[4] = {"gemm_fwd1", "gemm_fwd2", "gemm_bwd1", "gemm_bwd2"};
+    trace_before(names[epi & 3], s);
+    cudaError_t e = (epi == kEpiFwd1 || epi == kEpiFwd2) ? launch_gemm_fwd(epi, bn, tmap_a, args, grid, s)
+                                                          : launch_gemm_bwd(epi, bn, tmap_a, args, grid, s);
+    trace_after(s);
+    return e;
+}
+
+// ------------------------------------------------------- device checks ------
+namespace {
+struct DevInfo {
+    bool init = false;
+    bool supported = false;
+    int sms = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+int device_info(int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BLR_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.init) {
+        int maj = 0, min = 0, n = 0;
+        if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return BLR_ERR_CUDA;
+        d.supported = (maj == 10 && min == 3);
+        d.sms = n;
+        d.init = true;
+    }
+    if (!d.supported) return BLR_ERR_UNSUPPORTED_DEVICE;
+    *sms = d.sms;
+    return BLR_OK;
+}
+
+// ------------------------------------------------------------- TMA ---------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// f16 activation operand [rows][K], box 64 (K) x 128 (rows), 128-byte swizzle;
+// rows past `rows` and columns past K read as zero.
+bool make_tmap_act16(CUtensorMap *m, const void *base, int rows, int K) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ layout --------
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+    size_t header, bp_f1, bp_f2, bp_b1, bp_b2, act16, a32, act16b, c16, s_inv, sig, sig_inv, part_dh, part_dl,
+        part_dg, total;
+    int rows_dh, rows_dl, rows_dg;
+};
+
+bool shape_ok(int M, int d_in, int d_out, int r) {
+    auto dim_ok = [](int d) { return d >= 64 && d <= 65536 && d % 32 == 0; };
+    return M >= 1 && M <= (1 << 28) && dim_ok(d_in) && dim_ok(d_out) && dim_ok(r);
+}
+
+Layout make_layout(int M, int d_in, int d_out, int r) {
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += align_up(bytes, 256);
+        return o;
+    };
+    const size_t m = (size_t)M;
+    const size_t m_tiles = (m + 127) / 128;
+    L.header = take(256);
+    L.bp_f1 = take((size_t)((d_in + 63) / 64) * r * 8);   // forward 1: N = r, K = d_in
+    L.bp_f2 = take((size_t)((r + 63) / 64) * d_out * 8);  // forward 2: N = d_out, K = r
+    L.bp_b1 = take((size_t)((d_out + 63) / 64) * r * 8);  // backward 1: N = r, K = d_out
+    L.bp_b2 = take((size_t)((r + 63) / 64) * d_in * 8);   // backward 2: N = d_in, K = r
+    L.act16 = take(m * (size_t)(d_in > d_out ? d_in : d_out) * 2);
+    L.a32 = take(m * r * 4);
+    L.act16b = take(m * r * 2);
+    L.c16 = take(m * d_out * 2);
+    L.s_inv = take(m * 4);
+    L.sig = take(m * 4);
+    L.sig_inv = take(m * 4);
+    L.rows_dh = stage_dy_blocks(M, d_out);
+    L.rows_dl = (int)(m_tiles * 4);
+    L.rows_dg = (int)(m_tiles * 4);
+    L.part_dh = take((size_t)L.rows_dh * d_out * 4);
+    L.part_dl = take((size_t)L.rows_dl * r * 4);
+    L.part_dg = take((size_t)L.rows_dg * d_in * 4);
+    L.total = off;
+    return L;
+}
+
+// Feature tile width: the widest of 256/128/64/32 that divides N, narrowed
+// while the grid would leave SMs idle.
+int pick_bn(int M, int N, int sms) {
+    const long long m_tiles = (M + 127) / 128;
+    int bn = 256;
+    while (bn > 32 && N % bn != 0) bn /= 2;
+    while (bn > 32 && m_tiles * (N / bn) < sms && N % (bn / 2) == 0) bn /= 2;
+    return bn;
+}
+
+int gemm_grid(int M, int N, int bn, int sms) {
+    const long long tiles = (long long)((M + 127) / 128) * (N / bn);
+    return (int)(tiles < sms ? tiles : sms);
+}
+
+// ------------------------------------------------------------ tape ---------
+struct Tape {
+    int M, d_in, d_out, r;
+};
+std::mutex g_tape_mu;
+std::unordered_map<const void *, Tape> g_tapes;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool fault_injected(const char *site) {
+    const char *f = std::getenv("BLR_FAULT");
+    return f && std::strcmp(f, site) == 0;
+}
+
+bool pow2_positive(float v) {
+    if (!(v > 0.0f) || !std::isfinite(v)) return false;
+    int e;
+    return std::frexp(v, &e) == 0.5f;
+}
+}  // namespace
+}  // namespace blr
+
+using namespace blr;
+
+extern "C" {
+
+size_t blr_workspace_bytes(int M, int d_in, int d_out, int r) {
+    if (!shape_ok(M, d_in, d_out, r)) return 0;
+    return make_layout(M, d_in, d_out, r).total;
+}
+
+int blr_pack_signs(const float *src, uint32_t *bits, int rows, int r, blr_stream_t stream) {
+    if (!src || !bits) return BLR_ERR_ARG;
+    if (rows < 1 || r < 1) return BLR_ERR_SHAPE;
+    if (!aligned16(src) || !aligned16(bits)) return BLR_ERR_ALIGN;
+    int sms;
+    int st = device_info(&sms);
+    if (st != BLR_OK) return st;
+    if (fault_injected("pack")) return BLR_ERR_CUDA;
+    return launch_pack_signs(src, bits, rows, r, (cudaStream_t)stream) == cudaSuccess ? BLR_OK : BLR_ERR_CUDA;
+}
+
+int blr_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, int r, blr_stream_t stream) {
+    if (!bits || !dst) return BLR_ERR_ARG;
+    if (rows < 1 || r < 1) return BLR_ERR_SHAPE;
+    if (!aligned16(bits) || !aligned16(dst)) return BLR_ERR_ALIGN;
+    int sms;
+    int st = device_info(&sms);
+    if (st != BLR_OK) return st;
+    if (fault_injected("unpack")) return BLR_ERR_CUDA;
+    return launch_unpack_signs(bits, dst, rows, r, (cudaStream_t)stream) == cudaSuccess ? BLR_OK : BLR_ERR_CUDA;
+}
+
+int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, const float *g, const float *l,
+                const float *h, float *y, int accumulate_y, int M, int d_in, int d_out, int r, void *ws,
+                size_t ws_bytes, blr_stream_t stream) {
+    if (!x || !bits_u || !bits_v || !g || !l || !h || !y || !ws) return BLR_ERR_ARG;
+    if (accumulate_y != 0 && accumulate_y != 1) return BLR_ERR_ARG;
+    if (!shape_ok(M, d_in, d_out, r)) return BLR_ERR_SHAPE;
+    const void *ptrs[] = {x, bits_u, bits_v, g, l, h, y, ws};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return BLR_ERR_ALIGN;
+    const Layout L = make_layout(M, d_in, d_out, r);
+    if (ws_bytes < L.total) return BLR_ERR_WORKSPACE;
+    int sms;
+    int st = device_info(&sms);
+    if (st != BLR_OK) return st;
+    if (fault_injected("forward")) return BLR_ERR_CUDA;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    char *w = static_cast<char *>(ws);
+    uint32_t *status = reinterpret_cast<uint32_t *>(w + L.header);
+    uint32_t *bp_f1 = reinterpret_cast<uint32_t *>(w + L.bp_f1);
+    uint32_t *bp_f2 = reinterpret_cast<uint32_t *>(w + L.bp_f2);
+    uint16_t *x16 = reinterpret_cast<uint16_t *>(w + L.act16);
+    float *a32 = reinterpret_cast<float *>(w + L.a32);
+    uint16_t *al16 = reinterpret_cast<uint16_t *>(w + L.act16b);
+    uint16_t *c16 = reinterpret_cast<uint16_t *>(w + L.c16);
+
+    CUtensorMap tm_x, tm_a;
+    if (!make_tmap_act16(&tm_x, x16, M, d_in) || !make_tmap_act16(&tm_a, al16, M, r)) return BLR_ERR_CUDA;
+
+    // a new forward starts a new tape: forget the old one first
+    {
+        std::lock_guard<std::mutex> lk(g_tape_mu);
+        g_tapes.erase(ws);
+    }
+    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return BLR_ERR_CUDA;
+    // S_V [d_in][r/32] has its bits along r: the first product needs them along d_in
+    SignPrep pv{bits_v, bp_f1, r, d_in, 1};
+    SignPrep pu{bits_u, bp_f2, d_out, r, 0};
+    if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    GemmArgs f1{};
+    f1.M = M;
+    f1.N = r;
+    f1.K = d_in;
+    f1.bsign = bp_f1;
+    f1.out32 = a32;
+    f1.out16 = al16;
+    f1.colv = l;
+    f1.status = status;
+    const int bn1 = pick_bn(M, r, sms);
+    if (launch_gemm(kEpiFwd1, bn1, tm_x, f1, gemm_grid(M, r, bn1, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    GemmArgs f2{};
+    f2.M = M;
+    f2.N = d_out;
+    f2.K = r;
+    f2.bsign = bp_f2;
+    f2.out32 = y;
+    f2.out16 = c16;
+    f2.colv = h;
+    f2.accumulate = accumulate_y;
+    f2.status = status;
+    const int bn2 = pick_bn(M, d_out, sms);
+    if (launch_gemm(kEpiFwd2, bn2, tm_a, f2, gemm_grid(M, d_out, bn2, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    std::lock_guard<std::mutex> lk(g_tape_mu);
+    g_tapes[ws] = Tape{M, d_in, d_out, r};
+    return BLR_OK;
+}
+
+int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const uint32_t *bits_v, const float *g,
+                 const float *l, const float *h, float *dx, int accumulate_dx, float *dg, float *dl, float *dh,
+                 float gscale, int M, int d_in, int d_out, int r, void *ws, size_t ws_bytes, blr_stream_t stream) {
+    if (!x || !dy || !bits_u || !bits_v || !g || !l || !h || !dx || !dg || !dl || !dh || !ws) return BLR_ERR_ARG;
+    if (accumulate_dx != 0 && accumulate_dx != 1) return BLR_ERR_ARG;
+    if (std::isnan(gscale) || (gscale > 0.0f && !pow2_positive(gscale))) return BLR_ERR_ARG;
+    if (!shape_ok(M, d_in, d_out, r)) return BLR_ERR_SHAPE;
+    const void *ptrs[] = {x, dy, bits_u, bits_v, g, l, h, dx, dg, dl, dh, ws};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return BLR_ERR_ALIGN;
+    const Layout L = make_layout(M, d_in, d_out, r);
+    if (ws_bytes < L.total) return BLR_ERR_WORKSPACE;
+    {
+        std::lock_guard<std::mutex> lk(g_tape_mu);
+        auto it = g_tapes.find(ws);
+        if (it == g_tapes.end() || it->second.M != M || it->second.d_in != d_in || it->second.d_out != d_out ||
+            it->second.r != r)
+            return BLR_ERR_STATE;
+    }
+    int sms;
+    int st = device_info(&sms);
+    if (st != BLR_OK) return st;
+    if (fault_injected("backward")) return BLR_ERR_CUDA;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    char *w = static_cast<char *>(ws);
+    uint32_t *status = reinterpret_cast<uint32_t *>(w + L.header);
+    uint32_t *bp_b1 = reinterpret_cast<uint32_t *>(w + L.bp_b1);
+    uint32_t *bp_b2 = reinterpret_cast<uint32_t *>(w + L.bp_b2);
+    uint16_t *dy16 = reinterpret_cast<uint16_t *>(w + L.act16);
+    const float *a32 = reinterpret_cast<const float *>(w + L.a32);
+    uint16_t *db16 = reinterpret_cast<uint16_t *>(w + L.act16b);
+    const uint16_t *c16 = reinterpret_cast<const uint16_t *>(w + L.c16);
+    float *s_inv = reinterpret_cast<float *>(w + L.s_inv);
+    float *sig = reinterpret_cast<float *>(w + L.sig);
+    float *sig_inv = reinterpret_cast<float *>(w + L.sig_inv);
+    float *part_dh = reinterpret_cast<float *>(w + L.part_dh);
+    float *part_dl = reinterpret_cast<float *>(w + L.part_dl);
+    float *part_dg = reinterpret_cast<float *>(w + L.part_dg);
+
+    CUtensorMap tm_dy, tm_db;
+    if (!make_tmap_act16(&tm_dy, dy16, M, d_out) || !make_tmap_act16(&tm_db, db16, M, r)) return BLR_ERR_CUDA;
+
+    // S_U [d_out][r/32] has its bits along r: the first product needs them along d_out
+    SignPrep pu{bits_u, bp_b1, r, d_out, 1};
+    SignPrep pv{bits_v, bp_b2, d_in, r, 0};
+    StageDyArgs sa{};
+    sa.dy = dy;
+    sa.h = h;
+    sa.c16 = c16;
+    sa.l = l;
+    sa.dy16 = dy16;
+    sa.s_inv = s_inv;
+    sa.sig = sig;
+    sa.sig_inv = sig_inv;
+    sa.part_dh = part_dh;
+    sa.gscale = gscale;
+    sa.M = M;
+    sa.d_out = d_out;
+    sa.r = r;
+    if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    GemmArgs b1{};
+    b1.M = M;
+    b1.N = r;
+    b1.K = d_out;
+    b1.bsign = bp_b1;
+    b1.out16 = db16;
+    b1.colv = l;
+    b1.aux = a32;
+    b1.row_inv = s_inv;
+    b1.row_scale = sig;
+    b1.part = part_dl;
+    b1.status = status;
+    const int bn1 = pick_bn(M, r, sms);
+    if (launch_gemm(kEpiBwd1, bn1, tm_dy, b1, gemm_grid(M, r, bn1, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    GemmArgs b2{};
+    b2.M = M;
+    b2.N = d_in;
+    b2.K = r;
+    b2.bsign = bp_b2;
+    b2.out32 = dx;
+    b2.colv = g;
+    b2.aux = x;
+    b2.row_inv = sig_inv;
+    b2.part = part_dg;
+    b2.accumulate = accumulate_dx;
+    b2.status = status;
+    const int bn2 = pick_bn(M, d_in, sms);
+    if (launch_gemm(kEpiBwd2, bn2, tm_db, b2, gemm_grid(M, d_in, bn2, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    ReduceSeg sh{part_dh, dh, L.rows_dh, d_out};
+    ReduceSeg sl{part_dl, dl, L.rows_dl, r};
+    ReduceSeg sg{part_dg, dg, L.rows_dg, d_in};
+    if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
+    return BLR_OK;
+}
+
+int blr_check_status(const void *ws, size_t ws_bytes, blr_stream_t stream, uint32_t *device_code) {
+    if (!ws || ws_bytes < 256) return BLR_ERR_ARG;
+    uint32_t code = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&code, ws, sizeof(code), cudaMemcpyDeviceToHost, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (device_code) *device_code = code;
+    return code ? BLR_ERR_DEVICE_CHECK : BLR_OK;
+}
+
+const char *blr_status_string(int status) {
+    switch (status) {
+        case BLR_OK: return "ok";
+        case BLR_ERR_ARG: return "invalid argument";
+        case BLR_ERR_SHAPE: return "shape rule violated (M >= 1; d_in, d_out, r multiples of 32 in [64, 65536])";
+        case BLR_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case BLR_ERR_WORKSPACE: return "workspace too small";
+        case BLR_ERR_STATE: return "backward without a matching forward on this workspace";
+        case BLR_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case BLR_ERR_DEVICE_CHECK: return "a kernel recorded a failure in the workspace status word";
+        case BLR_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3";
+        default: return "unknown status";
+    }
+}
+
+int blr_trace_begin(int capacity) {
+    if (capacity < 1) return BLR_ERR_ARG;
+    TraceState &t = g_trace;
+    while ((int)t.ev.size() < 2 * capacity) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return BLR_ERR_CUDA;
+        t.ev.push_back(e);
+    }
+    t.names.assign(capacity, nullptr);
+    t.cap = capacity;
+    t.n = 0;
+    t.on = true;
+    return BLR_OK;
+}
+
+int blr_trace_end(void) {
+    g_trace.on = false;
+    return BLR_OK;
+}
+
+int blr_trace_count(void) { return g_trace.n; }
+
+const char *blr_trace_read(int i, float *ms) {
+    TraceState &t = g_trace;
+    if (i < 0 || i >= t.n) return nullptr;
+    if (cudaEventSynchronize(t.ev[2 * i + 1]) != cudaSuccess) return nullptr;
+    float v = 0.0f;
+    if (cudaEventElapsedTime(&v, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess) return nullptr;
+    if (ms) *ms = v;
+    return t.names[i];
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+/*
+ * blr.h - C ABI of the GB300 (sm_103a) binary low-rank linear layer.
+ *
+ * The layer (train_mm.rs, cortiq-engine 0.8.21, module documentation) is
+ *
+ *     W_hat = diag(h) . S_U . diag(l) . S_V^T . diag(g)
+ *
+ * with S_U [d_out x r] and S_V [d_in x r] sign matrices held as 1-bit bitmaps,
+ * and g [d_in], l [r], h [d_out] f32 vectors. Its forward and backward passes
+ * (same page, formula block) are
+ *
+ *     forward   a = (x.g) S_V         c = (a.l) S_U^T      y (+)= h.c
+ *     backward  dh = sum_t dy.c       db = (dy.h) S_U      dl = sum_t a.db
+ *               dx' = (db.l) S_V^T    dg = sum_t x.dx'     dx (+)= g.dx'
+ *
+ * where "." is the elementwise product broadcast along tokens and sum_t sums
+ * over tokens.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layouts are row-major and unpadded: x, dx [M][d_in]; y, dy [M][d_out]
+ *    f32. Token counts need not be multiples of anything; the library pads
+ *    internally (the page pads activation rows to 128).
+ *  - Sign bitmaps (train_mm.rs, comment of the `expand` kernel): bits_u is
+ *    [d_out][ceil(r/32)] u32 and bits_v is [d_in][ceil(r/32)] u32; bit j of
+ *    word w is rank 32w+j; a set bit is +1, a clear bit -1.
+ *  - Every data pointer is a DEVICE pointer owned by the caller and must be
+ *    16-byte aligned. The library never allocates, frees or synchronises on
+ *    the hot path; work is queued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and returns before it runs.
+ *  - Shape rule: M >= 1; d_in, d_out, r multiples of 32 and >= 64.
+ *  - Numerics: operands are staged to f16 (round to nearest even), products
+ *    accumulate in f32 on the tensor cores, outputs are f32. The forward
+ *    stages x.g and a.l unscaled, so |x.g| and |a.l| must stay below 65504.
+ *    The backward stages dy.h and db.l under powers of two (see
+ *    blr_backward) that the epilogues divide back out exactly.
+ *  - Return value: BLR_OK (0) or a negative BLR_ERR_* code. Argument errors
+ *    are reported before anything is queued. Device-side failures (a bounded
+ *    wait inside a kernel that ran out) do not fault the GPU: the kernel
+ *    records a code in the workspace status word and returns; read it with
+ *    blr_check_status().
+ *  - Calls are thread-safe as long as concurrent calls use distinct
+ *    workspaces.
+ *  - The device must be compute capability 10.3 (GB300); there is no other
+ *    code path and no CPU fallback.
+ */
+#ifndef BLR_H_
+#define BLR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define BLR_API __attribute__((visibility("default")))
+#else
+#define BLR_API
+#endif
+
+/* ABI-identical to cudaStream_t; declared here so that this header needs no
+ * CUDA header. */
+typedef struct CUstream_st *blr_stream_t;
+
+enum {
+    BLR_OK = 0,
+    BLR_ERR_ARG = -1,                /* null pointer, bad flag, gscale not a power of two */
+    BLR_ERR_SHAPE = -2,              /* shape rule violated */
+    BLR_ERR_ALIGN = -3,              /* a pointer is not 16-byte aligned */
+    BLR_ERR_WORKSPACE = -4,          /* ws_bytes < blr_workspace_bytes(...) */
+    BLR_ERR_STATE = -5,              /* backward without a matching forward on this workspace */
+    BLR_ERR_CUDA = -6,               /* a CUDA runtime/driver call or a launch failed */
+    BLR_ERR_DEVICE_CHECK = -7,       /* a kernel recorded a failure in the status word */
+    BLR_ERR_UNSUPPORTED_DEVICE = -8  /* current device is not compute capability 10.3 */
+};
+
+/* Bytes of caller-owned device workspace that one layer instance needs for a
+ * forward+backward at this shape. The workspace holds the forward's tape (a in
+ * f32 [M][r], c in f16 [M][d_out]) for the backward, the f16 staged operands,
+ * the re-laid-out sign bitmaps, the per-tile partial sums of dh/dl/dg and a
+ * 256-byte header whose first word is the device status. Returns 0 if the
+ * shape breaks the shape rule. Pure host arithmetic; needs no GPU. */
+BLR_API size_t blr_workspace_bytes(int M, int d_in, int d_out, int r);
+
+/* Pack signs into a bitmap (train_mm.rs, test helper `pack_bits`).
+ *   src  [rows][r] f32, device.
+ *   bits [rows][ceil(r/32)] u32, device, written in full: bit (row, k) is 1
+ *        iff src[row][k] > 0 (so 0, -0 and NaN give -1); unused high bits of
+ *        the last word are 0.
+ * rows >= 1, r >= 1. Bit-exact. */
+BLR_API int blr_pack_signs(const float *src, uint32_t *bits, int rows, int r, blr_stream_t stream);
+
+/* Expand a bitmap into +-1 f16 (train_mm.rs, `expand` kernel), through the
+ * same device expansion code the GEMMs use for their shared-memory operand
+ * tiles. For tests: the GEMMs never write dense planes.
+ *   bits [rows][ceil(r/32)] u32, device.
+ *   dst  [rows][r] f16 bit patterns (0x3C00 = +1, 0xBC00 = -1), device.
+ * rows >= 1, r >= 1. Bit-exact. */
+BLR_API int blr_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, int r, blr_stream_t stream);
+
+/* Forward pass (train_mm.rs, `blr_forward` and the formula block).
+ *   x [M][d_in] f32 in; bits_u [d_out][ceil(r/32)], bits_v [d_in][ceil(r/32)];
+ *   g [d_in], l [r], h [d_out] f32 in.
+ *   y [M][d_out] f32 out: y = h.c when accumulate_y == 0 (the page's first
+ *     path), y += h.c when accumulate_y == 1 (its later paths).
+ *   ws / ws_bytes: workspace of at least blr_workspace_bytes(M, d_in, d_out, r)
+ *     bytes; it receives the tape that blr_backward consumes, so it must not
+ *     be shared with another layer between the forward and its backward.
+ * Errors: BLR_ERR_ARG (null pointer, accumulate_y not 0/1), BLR_ERR_SHAPE,
+ *   BLR_ERR_ALIGN, BLR_ERR_WORKSPACE, BLR_ERR_UNSUPPORTED_DEVICE, BLR_ERR_CUDA. */
+BLR_API int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v,
+                const float *g, const float *l, const float *h,
+                float *y, int accumulate_y,
+                int M, int d_in, int d_out, int r,
+                void *ws, size_t ws_bytes, blr_stream_t stream);
+
+/* Backward pass (train_mm.rs, `blr_backward` and the formula block). Must
+ * follow blr_forward on the same workspace, shape, x and parameters.
+ *   x [M][d_in], dy [M][d_out] f32 in; bitmaps and g, l, h as in the forward.
+ *   dx [M][d_in] f32 out: dx = g.dx' (accumulate_dx == 0) or dx += g.dx' (1).
+ *   dg [d_in], dl [r], dh [d_out] f32: ALWAYS accumulated (+=), like the
+ *     page's column sums, in a fixed order (deterministic).
+ *   gscale > 0: the page's semantics: dy.h and db.l are staged times gscale,
+ *     which must be a power of two.
+ *   gscale <= 0: dynamic per-token powers of two: token t's dy.h is staged
+ *     times s_t = 2^(14 - ceil(log2 max_i |dy_ti h_i|)), and its db.l times
+ *     the largest power of two that keeps the L1 bound of db_t.l under 2^15,
+ *     which keeps gradients out of the f16 subnormals and never overflows.
+ * Errors: as blr_forward, plus BLR_ERR_STATE when no forward of this shape
+ *   preceded it on `ws` and BLR_ERR_ARG when gscale is positive but not a
+ *   power of two. */
+BLR_API int blr_backward(const float *x, const float *dy,
+                 const uint32_t *bits_u, const uint32_t *bits_v,
+                 const float *g, const float *l, const float *h,
+                 float *dx, int accumulate_dx,
+                 float *dg, float *dl, float *dh,
+                 float gscale,
+                 int M, int d_in, int d_out, int r,
+                 void *ws, size_t ws_bytes, blr_stream_t stream);
+
+/* Synchronises `stream` and reads the workspace's device status word.
+ * Returns BLR_OK if no kernel recorded a failure since the last blr_forward
+ * on this workspace, BLR_ERR_DEVICE_CHECK if one did (the code is written to
+ * *device_code when it is not NULL), BLR_ERR_CUDA if the stream reports an
+ * error. This call blocks; it is meant for tests and diagnostics. */
+BLR_API int blr_check_status(const void *ws, size_t ws_bytes, blr_stream_t stream, uint32_t *device_code);
+
+/* Static description of a status code. Never NULL. */
+BLR_API const char *blr_status_string(int status);
+
+/* Kernel-level timing for benchmarks. blr_trace_begin(capacity) makes every
+ * following blr_forward/blr_backward on this thread bracket each kernel it
+ * launches with a pair of CUDA events recorded on the launch stream, up to
+ * `capacity` kernels; blr_trace_end() stops recording. blr_trace_count()
+ * returns the number of kernels recorded; blr_trace_read(i, &ms) synchronises
+ * on kernel i's end event and returns its name, with its duration in
+ * milliseconds in *ms (NULL if i is out of range). The events are created
+ * once, on the first blr_trace_begin. Off by default; no effect on results. */
+BLR_API int blr_trace_begin(int capacity);
+BLR_API int blr_trace_end(void);
+BLR_API int blr_trace_count(void);
+BLR_API const char *blr_trace_read(int i, float *ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BLR_H_ */

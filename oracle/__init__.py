@@ -1,6 +1,7 @@
 """CPU f64 oracle of the blr layer: test infrastructure only (see blr_oracle)."""
 from .blr_oracle import (  # noqa: F401
     backward,
+    backward_sampled,
     forward,
     pack_signs,
     rel_err,

@@ -39,6 +39,7 @@ __all__ = [
     "pack_signs",
     "forward",
     "backward",
+    "backward_sampled",
     "rel_err",
 ]
 
@@ -148,6 +149,35 @@ def backward(x, dy, bits_u, bits_v, g, l, h, dx_prior=None) -> dict:
     if dx_prior is not None:
         dx = _f64(dx_prior) + dx
     return {"dx": dx, "dg": dg, "dl": dl, "dh": dh, "db": db, "dxp": dxp}
+
+
+def backward_sampled(x, dy, bits_u, bits_v, g, l, h, cols_h, cols_g) -> dict:
+    """dl in full, and dh and dg at the given output columns, in f64.
+
+    The same backward formulas (train_mm.rs, module documentation), evaluated
+    only where asked: dh_i needs c[:, i] = (a (.) l) . S_U[i, :]^T, and dg_j
+    needs dx'[:, j] = (db (.) l) . S_V[j, :]^T, so restricting the sign
+    matrices to the sampled rows restricts the products to those columns.
+    a and db are computed in full (both are token-by-rank). This lets full-size
+    workloads be checked against exact values at a fraction of the cost.
+
+    Returns a dict with dl [r], dh [len(cols_h)], dg [len(cols_g)].
+    """
+    x, dy = _f64(x), _f64(dy)
+    g, l, h = _f64(g), _f64(l), _f64(h)
+    d_in, d_out, r = x.shape[1], h.shape[0], l.shape[0]
+    s_u = unpack_signs(bits_u, d_out, r)
+    s_v = unpack_signs(bits_v, d_in, r)
+    cols_h = np.asarray(cols_h, dtype=np.int64)
+    cols_g = np.asarray(cols_g, dtype=np.int64)
+    a = np.matmul(x * g[None, :], s_v)
+    db = np.matmul(dy * h[None, :], s_u)
+    dl = np.sum(a * db, axis=0)
+    c_cols = np.matmul(a * l[None, :], s_u[cols_h].T)
+    dh = np.sum(dy[:, cols_h] * c_cols, axis=0)
+    dxp_cols = np.matmul(db * l[None, :], s_v[cols_g].T)
+    dg = np.sum(x[:, cols_g] * dxp_cols, axis=0)
+    return {"dl": dl, "dh": dh, "dg": dg}
 
 
 def rel_err(got, want) -> float:

@@ -1,0 +1,120 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/blr.h declares, and rejects bad arguments before touching the device.
+
+The pointers passed here are never dereferenced: every call below fails its
+host-side checks (or is pure host arithmetic) before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from binary_rank_linear_gb300 import _build
+    _build.build()
+    import binary_rank_linear_gb300 as blr
+    return blr.load()
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "blr.h")).read()
+    return sorted(set(re.findall(r"BLR_API\s+[\w\s\*]+?\b(blr_\w+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    names = _declared_symbols()
+    for n in ("blr_forward", "blr_backward", "blr_pack_signs", "blr_workspace_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_symbols()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(0, -9, -1):
+        s = lib.blr_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.blr_status_string(-100) == b"unknown status"
+
+
+def test_workspace_bytes_shape_rule(lib):
+    assert lib.blr_workspace_bytes(128, 256, 256, 64) > 0
+    assert lib.blr_workspace_bytes(0, 256, 256, 64) == 0       # M >= 1
+    assert lib.blr_workspace_bytes(128, 48, 256, 64) == 0      # d_in >= 64
+    assert lib.blr_workspace_bytes(128, 256, 100, 64) == 0     # multiple of 32
+    assert lib.blr_workspace_bytes(128, 256, 256, 65568) == 0  # <= 65536
+    small = lib.blr_workspace_bytes(2048, 1024, 1024, 256)
+    assert lib.blr_workspace_bytes(2049, 1024, 1024, 256) > small
+    # tape alone: a f32 [M][r] + c f16 [M][d_out]
+    assert small > 2048 * 256 * 4 + 2048 * 1024 * 2
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced
+
+
+def _fwd(lib, **over):
+    a = dict(x=FAKE, bu=FAKE, bv=FAKE, g=FAKE, l=FAKE, h=FAKE, y=FAKE, acc=0, M=64, di=128, do=128, r=64,
+             ws=FAKE, wsb=1 << 40, s=None)
+    a.update(over)
+    return lib.blr_forward(a["x"], a["bu"], a["bv"], a["g"], a["l"], a["h"], a["y"], a["acc"], a["M"], a["di"],
+                           a["do"], a["r"], a["ws"], a["wsb"], a["s"])
+
+
+def _bwd(lib, **over):
+    a = dict(x=FAKE, dy=FAKE, bu=FAKE, bv=FAKE, g=FAKE, l=FAKE, h=FAKE, dx=FAKE, acc=0, dg=FAKE, dl=FAKE,
+             dh=FAKE, gs=0.0, M=64, di=128, do=128, r=64, ws=FAKE + 4096, wsb=1 << 40, s=None)
+    a.update(over)
+    return lib.blr_backward(a["x"], a["dy"], a["bu"], a["bv"], a["g"], a["l"], a["h"], a["dx"], a["acc"],
+                            a["dg"], a["dl"], a["dh"], a["gs"], a["M"], a["di"], a["do"], a["r"], a["ws"],
+                            a["wsb"], a["s"])
+
+
+def test_forward_argument_errors(lib):
+    import binary_rank_linear_gb300 as blr
+    assert _fwd(lib, x=None) == blr.BLR_ERR_ARG
+    assert _fwd(lib, acc=2) == blr.BLR_ERR_ARG
+    assert _fwd(lib, M=0) == blr.BLR_ERR_SHAPE
+    assert _fwd(lib, r=40) == blr.BLR_ERR_SHAPE
+    assert _fwd(lib, y=FAKE + 4) == blr.BLR_ERR_ALIGN
+    assert _fwd(lib, wsb=1000) == blr.BLR_ERR_WORKSPACE
+
+
+def test_backward_argument_errors(lib):
+    import binary_rank_linear_gb300 as blr
+    assert _bwd(lib, dh=None) == blr.BLR_ERR_ARG
+    assert _bwd(lib, gs=3.0) == blr.BLR_ERR_ARG          # not a power of two
+    assert _bwd(lib, gs=float("nan")) == blr.BLR_ERR_ARG
+    assert _bwd(lib, acc=-1) == blr.BLR_ERR_ARG
+    assert _bwd(lib, do=70) == blr.BLR_ERR_SHAPE
+    assert _bwd(lib, dx=FAKE + 8) == blr.BLR_ERR_ALIGN
+    assert _bwd(lib, wsb=64) == blr.BLR_ERR_WORKSPACE
+    # no forward ever ran on this workspace
+    assert _bwd(lib) == blr.BLR_ERR_STATE
+    assert _bwd(lib, gs=1024.0) == blr.BLR_ERR_STATE
+
+
+def test_pack_argument_errors(lib):
+    import binary_rank_linear_gb300 as blr
+    assert lib.blr_pack_signs(None, FAKE, 4, 64, None) == blr.BLR_ERR_ARG
+    assert lib.blr_pack_signs(FAKE, FAKE, 0, 64, None) == blr.BLR_ERR_SHAPE
+    assert lib.blr_pack_signs(FAKE + 4, FAKE, 4, 64, None) == blr.BLR_ERR_ALIGN
+    assert lib.blr_unpack_signs(FAKE, None, 4, 64, None) == blr.BLR_ERR_ARG
+    assert lib.blr_unpack_signs(FAKE, FAKE, 4, 0, None) == blr.BLR_ERR_SHAPE
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    """No silent fallback: a missing library is an error, not another code path."""
+    from binary_rank_linear_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _binding.load()

@@ -1,0 +1,251 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU f64 oracle.
+
+Tolerances (normwise relative error, the page's metric): y and dx <= 2e-3;
+dh, dl and dg <= 5e-3. Sign packing and expansion are bit-exact. On the
+integer grid (x, dy in {-1, 0, 1}, g = h = 1, l a power of two) every f16
+operand and every f32 partial sum is exact, so y and dx must match the oracle
+bit for bit; that pins the bit-to-rank mappings and the GEMM data layout.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from binary_rank_linear_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 2e-3
+TOL_GRAD = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import binary_rank_linear_gb300 as blr
+    blr.load()
+
+
+def _run(*a, **k):
+    from blr_gpu_run import run_layer
+    return run_layer(*a, **k)
+
+
+def _check_against_oracle(t, out, gscale_note="", y_prior=None, dx_prior=None, grad_prior=None):
+    bu = oracle.pack_signs(t["su"])
+    bv = oracle.pack_signs(t["sv"])
+    assert np.array_equal(out["bu"], bu) and np.array_equal(out["bv"], bv)
+    fw = oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"], y_prior=y_prior)
+    errs = {"y": oracle.rel_err(out["y"], fw["y"])}
+    if "dx" in out:
+        bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"], dx_prior=dx_prior)
+        errs["dx"] = oracle.rel_err(out["dx"], bw["dx"])
+        for k in ("dh", "dl", "dg"):
+            want = bw[k] + (grad_prior[k] if grad_prior is not None else 0.0)
+            errs[k] = oracle.rel_err(out[k], want)
+    assert out["status"] == 0, f"device status {out['status']:#x}"
+    for k, e in errs.items():
+        tol = TOL_OUT if k in ("y", "dx") else TOL_GRAD
+        assert np.isfinite(e) and e <= tol, f"{k}: rel err {e:.3e} > {tol} {gscale_note} {errs}"
+    return errs
+
+
+# --------------------------------------------------------- bit-exact parts --
+@pytest.mark.parametrize("rows,r", [(1, 64), (37, 40), (300, 256), (513, 95), (64, 1024)])
+def test_pack_signs_bit_exact(rows, r):
+    import binary_rank_linear_gb300 as blr
+    rng = np.random.default_rng(rows + r)
+    src = rng.standard_normal((rows, r)).astype(np.float32)
+    src[rng.random((rows, r)) < 0.05] = 0.0
+    src[rng.random((rows, r)) < 0.02] = -0.0
+    src[rng.random((rows, r)) < 0.02] = np.nan
+    src[0, 0] = np.inf
+    got = blr.pack_signs(torch.from_numpy(src).cuda()).cpu().numpy().view(np.uint32)
+    assert np.array_equal(got, oracle.pack_signs(src))
+
+
+@pytest.mark.parametrize("rows,r", [(3, 40), (129, 64), (50, 1024), (7, 95)])
+def test_unpack_signs_bit_exact(rows, r):
+    import binary_rank_linear_gb300 as blr
+    rng = np.random.default_rng(7 * rows + r)
+    bits = rng.integers(0, 2**32, size=(rows, (r + 31) // 32), dtype=np.uint64).astype(np.uint32)
+    got = blr.unpack_signs(torch.from_numpy(bits.view(np.int32)).cuda(), r).cpu().numpy().view(np.uint16)
+    want = np.where(oracle.unpack_signs(bits, rows, r) > 0, 0x3C00, 0xBC00).astype(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def _integer_grid(M, d_in, d_out, r, seed, one_hot=None):
+    rng = np.random.default_rng(seed)
+    t = {
+        "x": rng.integers(-1, 2, size=(M, d_in)).astype(np.float32),
+        "dy": rng.integers(-1, 2, size=(M, d_out)).astype(np.float32),
+        "su": np.where(rng.random((d_out, r)) < 0.5, 1.0, -1.0).astype(np.float32),
+        "sv": np.where(rng.random((d_in, r)) < 0.5, 1.0, -1.0).astype(np.float32),
+        "g": np.ones(d_in, np.float32),
+        "h": np.ones(d_out, np.float32),
+    }
+    if one_hot is None:
+        t["l"] = rng.choice(np.array([0.5, 1.0, 2.0], np.float32), size=r)
+    else:
+        t["l"] = np.zeros(r, np.float32)
+        t["l"][one_hot] = 1.0
+    return t
+
+
+@pytest.mark.parametrize("M,d_in,d_out,r", [(128, 128, 128, 64), (200, 96, 160, 96), (70, 256, 64, 128)])
+def test_integer_grid_bit_exact(M, d_in, d_out, r):
+    t = _integer_grid(M, d_in, d_out, r, seed=M + r)
+    out = _run(t, gscale=1.0)
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    fw = oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    assert out["status"] == 0
+    assert np.array_equal(out["y"], fw["y"].astype(np.float32))
+    assert np.array_equal(out["dx"], bw["dx"].astype(np.float32))
+    assert oracle.rel_err(out["dl"], bw["dl"]) == 0.0
+
+
+@pytest.mark.parametrize("k", [0, 31, 32, 63, 95])
+def test_one_hot_rank_bit_exact(k):
+    """l = e_k: every output depends on bit k of each bitmap row only."""
+    M, d_in, d_out, r = 130, 160, 96, 96
+    t = _integer_grid(M, d_in, d_out, r, seed=100 + k, one_hot=k)
+    out = _run(t, gscale=1.0)
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    fw = oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    assert np.array_equal(out["y"], fw["y"].astype(np.float32))
+    assert np.array_equal(out["dx"], bw["dx"].astype(np.float32))
+    for key in ("dh", "dl", "dg"):
+        assert np.array_equal(out[key], bw[key].astype(np.float32)), key
+
+
+# ------------------------------------------------------ tolerance parity ---
+SHAPES = [
+    # name, M, d_in, d_out, r : several tiles, ragged tails, half k-steps (K % 64 == 32)
+    ("tiny", 128, 256, 256, 64),
+    ("small", 300, 320, 448, 96),
+    ("small", 257, 352, 192, 160),
+    ("attn", 513, 512, 640, 256),
+    ("ragged", 1, 128, 128, 64),
+    ("ragged", 127, 256, 512, 128),
+    ("ragged", 129, 192, 96, 64),
+]
+
+
+@pytest.mark.parametrize("name,M,d_in,d_out,r", SHAPES)
+@pytest.mark.parametrize("gscale", [0.0, 1024.0])
+def test_parity_shapes(name, M, d_in, d_out, r, gscale):
+    t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    if name == "ragged" and gscale > 0:
+        gscale = 2.0 ** 30  # the dy ~ 1e-7 workload needs a large fixed scale
+    out = _run(t, gscale=gscale)
+    _check_against_oracle(t, out, f"(gscale {gscale})")
+
+
+def test_accumulate_modes():
+    w = wl.WORKLOADS["small"].with_shape(M=200, d_in=256, d_out=320, r=128)
+    t = wl.make_inputs(w, with_priors=True)
+    rng = np.random.default_rng(5)
+    grad_prior = {"dg": rng.standard_normal(256).astype(np.float32),
+                  "dl": rng.standard_normal(128).astype(np.float32),
+                  "dh": rng.standard_normal(320).astype(np.float32)}
+    out = _run(t, y_prior=t["y_prior"], dx_prior=t["dx_prior"], grad_prior=grad_prior)
+    _check_against_oracle(t, out, y_prior=t["y_prior"], dx_prior=t["dx_prior"], grad_prior=grad_prior)
+
+
+def test_pages_two_path_case():
+    """The page's own test: two paths summed (path 0 overwrites, path 1
+    accumulates), d_out 256, d_in 384, r 128, 70 tokens, gscale 1024."""
+    from blr_gpu_run import run_layer
+    p0, p1 = wl.pages_case(0), wl.pages_case(1)
+    o0 = run_layer(p0, gscale=1024.0)
+    o1 = run_layer(p1, gscale=1024.0, y_prior=o0["y"], dx_prior=o0["dx"])
+    want_y = np.zeros((70, 256))
+    want_dx = np.zeros((70, 384))
+    for p, o in ((p0, o0), (p1, o1)):
+        bu, bv = oracle.pack_signs(p["su"]), oracle.pack_signs(p["sv"])
+        want_y += oracle.forward(p["x"], bu, bv, p["g"], p["l"], p["h"])["y"]
+        bw = oracle.backward(p["x"], p["dy"], bu, bv, p["g"], p["l"], p["h"])
+        want_dx += bw["dx"]
+        for k in ("dh", "dl", "dg"):
+            assert oracle.rel_err(o[k], bw[k]) <= 3e-3, k
+    assert oracle.rel_err(o1["y"], want_y) <= 2e-3
+    assert oracle.rel_err(o1["dx"], want_dx) <= 2e-3
+
+
+def test_outputs_stay_in_bounds():
+    """Rows past M of y and dx are never written (poisoned guard rows survive)."""
+    import binary_rank_linear_gb300 as blr
+    from blr_gpu_run import to_dev
+    M, d_in, d_out, r = 70, 256, 192, 64
+    t = wl.make_inputs(wl.WORKLOADS["tiny"].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    ybuf = torch.full((M + 3, d_out), 12345.0, device="cuda")
+    dxbuf = torch.full((M + 3, d_in), -777.0, device="cuda")
+    x, dy = to_dev(t["x"]), to_dev(t["dy"])
+    g, l, h = to_dev(t["g"]), to_dev(t["l"]), to_dev(t["h"])
+    bu, bv = blr.pack_signs(to_dev(t["su"])), blr.pack_signs(to_dev(t["sv"]))
+    ws = blr.alloc_workspace(M, d_in, d_out, r)
+    blr.forward(x, bu, bv, g, l, h, ybuf[:M], ws)
+    dg, dl, dh = torch.zeros(d_in, device="cuda"), torch.zeros(r, device="cuda"), torch.zeros(d_out, device="cuda")
+    blr.backward(x, dy, bu, bv, g, l, h, dxbuf[:M], dg, dl, dh, ws)
+    assert blr.check_status(ws) == 0
+    assert torch.all(ybuf[M:] == 12345.0) and torch.all(dxbuf[M:] == -777.0)
+    assert torch.isfinite(ybuf[:M]).all() and torch.isfinite(dxbuf[:M]).all()
+
+
+def test_deterministic():
+    w = wl.WORKLOADS["small"].with_shape(M=300, d_in=256, d_out=256, r=128)
+    t = wl.make_inputs(w)
+    a, b = _run(t), _run(t)
+    for k in ("y", "dx", "dh", "dl", "dg"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_backward_without_forward_is_rejected():
+    import binary_rank_linear_gb300 as blr
+    M, d_in, d_out, r = 16, 64, 64, 64
+    z = lambda *s: torch.zeros(*s, device="cuda")  # noqa: E731
+    bits = torch.zeros(64, 2, dtype=torch.int32, device="cuda")
+    ws = blr.alloc_workspace(M, d_in, d_out, r)
+    with pytest.raises(blr.BlrError) as e:
+        blr.backward(z(M, d_in), z(M, d_out), bits, bits, z(d_in), z(r), z(d_out), z(M, d_in),
+                     z(d_in), z(r), z(d_out), ws)
+    assert e.value.code == blr.BLR_ERR_STATE
+
+
+# ------------------------------------------------------- full workloads ----
+FULL = ["tiny", "small", "attn", "ragged", "mlp_up", "mlp_down"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    """The workloads at full size, in the launch configuration the benchmark
+    times: y and dx on sampled tokens, dl in full and dh, dg on sampled
+    columns against exact oracle values; the Euler identities on everything."""
+    w = wl.WORKLOADS[name]
+    t = wl.make_inputs(w)
+    out = _run(t)
+    assert out["status"] == 0
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    assert np.array_equal(out["bu"], bu) and np.array_equal(out["bv"], bv)
+    rng = np.random.default_rng(w.wid)
+    rows = np.unique(np.concatenate([[0, w.M - 1], rng.choice(w.M, size=min(w.M, 40), replace=False)]))
+    fw = oracle.forward(t["x"][rows], bu, bv, t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"][rows], t["dy"][rows], bu, bv, t["g"], t["l"], t["h"])
+    assert oracle.rel_err(out["y"][rows], fw["y"]) <= TOL_OUT
+    assert oracle.rel_err(out["dx"][rows], bw["dx"]) <= TOL_OUT
+    ch = np.unique(np.concatenate([[0, w.d_out - 1], rng.choice(w.d_out, size=min(w.d_out, 64), replace=False)]))
+    cg = np.unique(np.concatenate([[0, w.d_in - 1], rng.choice(w.d_in, size=min(w.d_in, 64), replace=False)]))
+    smp = oracle.backward_sampled(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"], ch, cg)
+    assert oracle.rel_err(out["dl"], smp["dl"]) <= TOL_GRAD
+    assert oracle.rel_err(out["dh"][ch], smp["dh"]) <= TOL_GRAD
+    assert oracle.rel_err(out["dg"][cg], smp["dg"]) <= TOL_GRAD
+    # Euler identities: <dh,h> = <dl,l> = <dg,g> = <dx,x> = <dy,y>
+    ref = float(np.sum(t["dy"].astype(np.float64) * out["y"].astype(np.float64)))
+    for vec, par in ((out["dh"], t["h"]), (out["dl"], t["l"]), (out["dg"], t["g"])):
+        got = float(np.dot(vec.astype(np.float64), par.astype(np.float64)))
+        assert abs(got - ref) <= TOL_GRAD * abs(ref) + 1e-30
+    got = float(np.sum(out["dx"].astype(np.float64) * t["x"].astype(np.float64)))
+    assert abs(got - ref) <= TOL_GRAD * abs(ref)

@@ -318,3 +318,16 @@ def test_planted_formula_mistakes_are_caught(mutant, monkeypatch):
             fd[i] = (_loss(t, h=p) - _loss(t, h=m)) / (2 * eps)
         assert np.allclose(bw["dh"], fd, rtol=1e-10)
         assert not np.allclose(-bw["dh"], fd, rtol=1e-6)
+
+
+def test_sampled_backward_matches_full():
+    """The column-sampled evaluation equals the full backward at those columns."""
+    w = wl.WORKLOADS["small"].with_shape(M=96, d_in=128, d_out=160, r=64)
+    t = wl.make_inputs(w)
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    full = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    ch, cg = [0, 7, 159, 80], [127, 3, 64]
+    smp = oracle.backward_sampled(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"], ch, cg)
+    assert np.allclose(smp["dl"], full["dl"], rtol=1e-12, atol=1e-14)
+    assert np.allclose(smp["dh"], full["dh"][ch], rtol=1e-12, atol=1e-14)
+    assert np.allclose(smp["dg"], full["dg"][cg], rtol=1e-12, atol=1e-14)
