@@ -10,8 +10,10 @@ Timing: W untimed warm-up steps, then K timed steps between a barrier and
 cudaDeviceSynchronize on both sides, measured with CUDA events on the launch
 stream; max over ranks. L2 (129 MB) is defeated by rotating independent
 input/output/workspace sets whose total exceeds twice the L2 size. Kernel-level
-durations for the roofline come from the library's event trace over a second
-timed pass of the same K steps. Multi-GPU: every rank runs its own batch
+durations for the roofline come from the library's event trace over an eager
+pass of the same K steps. Steps are timed as CUDA-graph replays (one graph
+per buffer set, captured from the same library calls), so host launch cost is
+not in the device time; the end-to-end number keeps every host call. Multi-GPU: every rank runs its own batch
 (weak scaling); the path needs no collective inside a step.
 """
 from __future__ import annotations
@@ -210,11 +212,25 @@ def run_gpu(args, rank, world, local_rank):
             tdist.barrier()
         torch.cuda.synchronize()
 
-    for i in range(args.warmup):
+    for i in range(max(args.warmup, nsets)):
         step(i)
     status = blr.check_status(sets[0]["ws"])
     if status:
         raise RuntimeError(f"device status {status:#x} after warm-up")
+
+    # one CUDA graph per buffer set: a step is replayed with no host launch cost
+    graphs = []
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        for i in range(nsets):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=cap):
+                step(i)
+            graphs.append(gr)
+    stream.wait_stream(cap)
+    for i in range(args.warmup):
+        graphs[i % nsets].replay()
 
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -223,13 +239,19 @@ def run_gpu(args, rank, world, local_rank):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        step(i)
+        graphs[i % nsets].replay()
     e1.record(stream)
     barrier()
     ms = e0.elapsed_time(e1)
-    # second timed pass with the per-kernel event trace
-    blr.trace_begin(capacity=16 * args.steps)
+    # kernel-level durations: an eager pass of the same steps with the library's
+    # event trace, queued behind a GPU sleep so that host launch gaps do not
+    # land inside any kernel's bracket
+    t0 = time.perf_counter()
+    step(0)
+    host_step_s = time.perf_counter() - t0
     barrier()
+    blr.trace_begin(capacity=16 * args.steps)
+    torch.cuda._sleep(int(min(4e9, 2.5e9 * host_step_s * (args.steps + 2))))
     for i in range(args.steps):
         step(i)
     barrier()

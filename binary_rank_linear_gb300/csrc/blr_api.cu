@@ -12,10 +12,10 @@
 #include "blr_kernels.h"
 
 namespace blr {
-cudaError_t launch_gemm_fwd(int epi, int bn, const CUtensorMap &tmap_a, const GemmArgs &args, int grid,
-                            cudaStream_t s);
-cudaError_t launch_gemm_bwd(int epi, int bn, const CUtensorMap &tmap_a, const GemmArgs &args, int grid,
-                            cudaStream_t s);
+cudaError_t launch_gemm_fwd(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps,
+                            const GemmArgs &args, int grid, cudaStream_t s);
+cudaError_t launch_gemm_bwd(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps,
+                            const GemmArgs &args, int grid, cudaStream_t s);
 
 // ------------------------------------------------------------ tracing ------
 namespace {
@@ -43,12 +43,12 @@ void trace_after(cudaStream_t stream) {
     ++t.n;
 }
 
-cudaError_t launch_gemm(int epi, int bn, const CUtensorMap &tmap_a, const GemmArgs &args, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args,
+                        int grid, cudaStream_t s) {
     static const char *names[4] = {"gemm_fwd1", "gemm_fwd2", "gemm_bwd1", "gemm_bwd2"};
     trace_before(names[epi & 3], s);
-    cudaError_t e = (epi == kEpiFwd1 || epi == kEpiFwd2) ? launch_gemm_fwd(epi, bn, tmap_a, args, grid, s)
-                                                          : launch_gemm_bwd(epi, bn, tmap_a, args, grid, s);
+    cudaError_t e = (epi == kEpiFwd1 || epi == kEpiFwd2) ? launch_gemm_fwd(epi, bn, tmap_a, emaps, args, grid, s)
+                                                          : launch_gemm_bwd(epi, bn, tmap_a, emaps, args, grid, s);
     trace_after(s);
     return e;
 }
@@ -116,6 +116,22 @@ bool make_tmap_act16(CUtensorMap *m, const void *base, int rows, int K) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D [rows][cols] map with a 32 x 32 box (f32 with the 128-byte swizzle, f16
+// with the 64-byte swizzle): the epilogue chunks of the wide products.
+bool make_tmap_chunk(CUtensorMap *m, const void *base, int rows, int cols, bool f16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t esz = f16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              f16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ layout --------
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -126,8 +142,8 @@ struct Layout {
 };
 
 bool shape_ok(int M, int d_in, int d_out, int r) {
-    auto dim_ok = [](int d) { return d >= 64 && d <= 65536 && d % 32 == 0; };
-    return M >= 1 && M <= (1 << 28) && dim_ok(d_in) && dim_ok(d_out) && dim_ok(r);
+    auto dim_ok = [](int d, int hi) { return d >= 64 && d <= hi && d % 32 == 0; };
+    return M >= 1 && M <= (1 << 28) && dim_ok(d_in, 65536) && dim_ok(d_out, 32768) && dim_ok(r, 65536);
 }
 
 Layout make_layout(int M, int d_in, int d_out, int r) {
@@ -258,17 +274,20 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
 
     CUtensorMap tm_x, tm_a;
     if (!make_tmap_act16(&tm_x, x16, M, d_in) || !make_tmap_act16(&tm_a, al16, M, r)) return BLR_ERR_CUDA;
+    EpiMaps em_none{}, em_f2{};
+    if (!make_tmap_chunk(&em_f2.out32, y, M, d_out, false) || !make_tmap_chunk(&em_f2.out16, c16, M, d_out, true))
+        return BLR_ERR_CUDA;
+    em_f2.in32 = em_f2.out32;
 
     // a new forward starts a new tape: forget the old one first
     {
         std::lock_guard<std::mutex> lk(g_tape_mu);
         g_tapes.erase(ws);
     }
-    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return BLR_ERR_CUDA;
     // S_V [d_in][r/32] has its bits along r: the first product needs them along d_in
     SignPrep pv{bits_v, bp_f1, r, d_in, 1};
     SignPrep pu{bits_u, bp_f2, d_out, r, 0};
-    if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, status, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs f1{};
     f1.M = M;
@@ -280,7 +299,8 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f1.colv = l;
     f1.status = status;
     const int bn1 = pick_bn(M, r, sms);
-    if (launch_gemm(kEpiFwd1, bn1, tm_x, f1, gemm_grid(M, r, bn1, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiFwd1, bn1, tm_x, em_none, f1, gemm_grid(M, r, bn1, sms), s) != cudaSuccess)
+        return BLR_ERR_CUDA;
 
     GemmArgs f2{};
     f2.M = M;
@@ -293,7 +313,8 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f2.accumulate = accumulate_y;
     f2.status = status;
     const int bn2 = pick_bn(M, d_out, sms);
-    if (launch_gemm(kEpiFwd2, bn2, tm_a, f2, gemm_grid(M, d_out, bn2, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiFwd2, bn2, tm_a, em_f2, f2, gemm_grid(M, d_out, bn2, sms), s) != cudaSuccess)
+        return BLR_ERR_CUDA;
 
     std::lock_guard<std::mutex> lk(g_tape_mu);
     g_tapes[ws] = Tape{M, d_in, d_out, r};
@@ -342,6 +363,9 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
 
     CUtensorMap tm_dy, tm_db;
     if (!make_tmap_act16(&tm_dy, dy16, M, d_out) || !make_tmap_act16(&tm_db, db16, M, r)) return BLR_ERR_CUDA;
+    EpiMaps em_none{}, em_b2{};
+    if (!make_tmap_chunk(&em_b2.out32, dx, M, d_in, false) || !make_tmap_chunk(&em_b2.in32, x, M, d_in, false))
+        return BLR_ERR_CUDA;
 
     // S_U [d_out][r/32] has its bits along r: the first product needs them along d_out
     SignPrep pu{bits_u, bp_b1, r, d_out, 1};
@@ -360,6 +384,8 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     sa.M = M;
     sa.d_out = d_out;
     sa.r = r;
+    int rows_dh = 0;
+    sa.rows_used = &rows_dh;
     if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs b1{};
@@ -375,7 +401,8 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b1.part = part_dl;
     b1.status = status;
     const int bn1 = pick_bn(M, r, sms);
-    if (launch_gemm(kEpiBwd1, bn1, tm_dy, b1, gemm_grid(M, r, bn1, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd1, bn1, tm_dy, em_none, b1, gemm_grid(M, r, bn1, sms), s) != cudaSuccess)
+        return BLR_ERR_CUDA;
 
     GemmArgs b2{};
     b2.M = M;
@@ -390,9 +417,10 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b2.accumulate = accumulate_dx;
     b2.status = status;
     const int bn2 = pick_bn(M, d_in, sms);
-    if (launch_gemm(kEpiBwd2, bn2, tm_db, b2, gemm_grid(M, d_in, bn2, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd2, bn2, tm_db, em_b2, b2, gemm_grid(M, d_in, bn2, sms), s) != cudaSuccess)
+        return BLR_ERR_CUDA;
 
-    ReduceSeg sh{part_dh, dh, L.rows_dh, d_out};
+    ReduceSeg sh{part_dh, dh, rows_dh, d_out};
     ReduceSeg sl{part_dl, dl, L.rows_dl, r};
     ReduceSeg sg{part_dg, dg, L.rows_dg, d_in};
     if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
@@ -413,7 +441,7 @@ const char *blr_status_string(int status) {
     switch (status) {
         case BLR_OK: return "ok";
         case BLR_ERR_ARG: return "invalid argument";
-        case BLR_ERR_SHAPE: return "shape rule violated (M >= 1; d_in, d_out, r multiples of 32 in [64, 65536])";
+        case BLR_ERR_SHAPE: return "shape rule violated (M >= 1; d_in, d_out, r multiples of 32, >= 64; d_out <= 32768, d_in, r <= 65536)";
         case BLR_ERR_ALIGN: return "pointer not 16-byte aligned";
         case BLR_ERR_WORKSPACE: return "workspace too small";
         case BLR_ERR_STATE: return "backward without a matching forward on this workspace";

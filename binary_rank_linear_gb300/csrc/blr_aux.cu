@@ -12,6 +12,7 @@ namespace blr {
 // is 1 iff src[row][k] > 0. One warp per output word; lane j votes for rank
 // 32w+j of the row.
 __global__ void pack_signs_kernel(const float *__restrict__ src, uint32_t *__restrict__ bits, int rows, int r) {
+    pdl_wait();
     const int words = (r + 31) / 32;
     const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
     const int lane = threadIdx.x & 31;
@@ -31,6 +32,7 @@ __global__ void pack_signs_kernel(const float *__restrict__ src, uint32_t *__res
 // pair-ready transform and pair expansion the GEMM expanders use.
 __global__ void unpack_signs_kernel(const uint32_t *__restrict__ bits, uint16_t *__restrict__ dst, int rows,
                                     int r) {
+    pdl_wait();
     const int words = (r + 31) / 32;
     const long long total = (long long)rows * words;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -111,7 +113,10 @@ __device__ void stage_x_run(const float *__restrict__ x, const float *__restrict
 }
 
 __global__ void __launch_bounds__(256) fwd_prologue_kernel(SignPrep p0, SignPrep p1, const float *x, const float *g,
-                                                           uint16_t *x16, int M, int d_in) {
+                                                           uint16_t *x16, int M, int d_in, uint32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
     const int b0 = prep_blocks(p0, blockDim.x);
     const int b1 = prep_blocks(p1, blockDim.x);
     const int b = blockIdx.x;
@@ -127,27 +132,38 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(SignPrep p0, SignPrep
 // =========================================================== stage dy ======
 // Backward staging (train_mm.rs, `blr_backward`: cvt of dy with the column
 // factor h under the gradient scale, and `colsum_prod` of dy and c for dh).
-// A block of 1024 threads owns whole token rows; `tpr` threads share a row
-// and a block works on 1024/tpr rows at a time. Per row t:
-//   s_t     = gscale, or 2^(14 - ceil(log2 max_i |dy_ti h_i|))  (1 if the max is 0)
+// A block of 512 threads owns whole token rows: `tpr` threads share a row and
+// the block works on 512/tpr rows at a time, visiting rows in a grid-stride
+// loop. Per row t (one joint block reduction of the pair (max, sum)):
+//   A_t     = max_i |dy_ti h_i|,  L_t = sum_i |dy_ti h_i|
+//   s_t     = gscale, or 2^(14 - ceil(log2 A_t))   (1 if A_t is 0 or not finite)
 //   dy16_t  = f16(dy_t . h . s_t)
-//   sigma_t = gscale, or s_t * 2^(15 - ceil(log2(L1_t * max|l|))) with
-//             L1_t = sum_i |dy16_ti|, which bounds |db_t . l . sigma_t| by 2^15
-// and the block accumulates sum_t dy_ti c_ti into one partial row of dh.
-constexpr int kStageThreads = 1024;
-constexpr int kStageRowsPerBlock = 32;
+//   sigma_t = gscale, or 2^(15 - ceil(log2(L_t max_k |l_k|)))
+// sigma_t scales the staged db.l in the next product. Since
+// |db_tk| = |sum_i dy16_ti S_ik| / s_t <= L_t (1 + 2^-11), every staged value
+// |db_tk l_k sigma_t| stays below 2^15 (1 + 2^-11), under the f16 maximum
+// 65504 whatever the data, while sigma_t is as large as that bound allows.
+// The block accumulates sum_t dy_ti c_ti for its rows in shared memory and
+// writes one partial row of dh.
+constexpr int kStageThreads = 512;
+constexpr int kStageMaxBlocks = 2 * 160;  // partial rows reserved per call
 
 __host__ __device__ inline int stage_tpr(int d_out) {
-    const int G = d_out / 4;
+    const int G = d_out / 4;  // float4 groups per row
     int t = 32;
-    while (t * 2 <= G / 4 && t < kStageThreads) t *= 2;
+    while (t * 8 < G && t < kStageThreads) t *= 2;  // at most 8 groups per thread when possible
     return t;
+}
+
+__host__ __device__ inline int stage_gpt(int d_out) {
+    const int tpr = stage_tpr(d_out);
+    return (d_out / 4 + tpr - 1) / tpr;
 }
 
 int stage_dy_blocks(int M, int d_out) {
     const int rb = kStageThreads / stage_tpr(d_out);
-    const int rows = rb > kStageRowsPerBlock ? rb : kStageRowsPerBlock;
-    return (M + rows - 1) / rows;
+    const int batches = (M + rb - 1) / rb;
+    return batches < kStageMaxBlocks ? batches : kStageMaxBlocks;
 }
 
 // ceil(log2(v)) for finite v > 0.
@@ -162,108 +178,96 @@ __device__ __forceinline__ float pow2i(int e) {
     return __int_as_float((e + 127) << 23);
 }
 
-// Reduce `v` over the `tpr` consecutive threads sharing a row (tpr >= 32, a
-// power of two). Every thread of the block must call it.
-template <bool kMax>
-__device__ __forceinline__ float row_reduce(float v, float *red, int tpr) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float u = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        v = kMax ? fmaxf(v, u) : v + u;
-    }
-    const int warp = threadIdx.x / 32;
-    if ((threadIdx.x & 31) == 0) red[warp] = v;
-    __syncthreads();
-    const int wpr = tpr / 32;
-    const int first = (threadIdx.x / tpr) * wpr;
-    float r = red[first];
-    for (int i = 1; i < wpr; ++i) r = kMax ? fmaxf(r, red[first + i]) : r + red[first + i];
-    __syncthreads();
-    return r;
-}
-
 template <int GPT>
-__device__ void stage_dy_run(const StageDyArgs &a, int block, float *smem) {
-    float *red = smem;             // [32]
-    float *dh_red = smem + 32;     // [d_out]
+__device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float *smem) {
     const int tpr = stage_tpr(a.d_out);
     const int rb_n = kStageThreads / tpr;
-    const int rows_per_block = rb_n > kStageRowsPerBlock ? rb_n : kStageRowsPerBlock;
+    const int wpr = tpr / 32;  // warps per row
     const int rb = threadIdx.x / tpr;
     const int ti = threadIdx.x % tpr;
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
     const int G = a.d_out / 4;
-    const int row0 = block * rows_per_block;
-    const int row_end = min(row0 + rows_per_block, a.M);
+    float2 *red = reinterpret_cast<float2 *>(smem);      // [2][16 warps]
+    float4 *dh_s = reinterpret_cast<float4 *>(smem + 64);  // [rb_n][G]
     const bool dynamic = !(a.gscale > 0.0f);
 
     float lmax = 0.0f;
     if (dynamic) {
-        for (int k = threadIdx.x; k < a.r; k += blockDim.x) lmax = fmaxf(lmax, fabsf(__ldg(a.l + k)));
-        lmax = row_reduce<true>(lmax, red, kStageThreads < 1024 ? kStageThreads : 1024);
+        for (int k = lane; k < a.r; k += 32) lmax = fmaxf(lmax, fabsf(__ldg(a.l + k)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
     }
 
     const float4 *dy4 = reinterpret_cast<const float4 *>(a.dy);
     const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
     const uint2 *c4 = reinterpret_cast<const uint2 *>(a.c16);
     uint2 *o4 = reinterpret_cast<uint2 *>(a.dy16);
-
-    float4 acc[GPT];
 #pragma unroll
-    for (int g = 0; g < GPT; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < GPT; ++g) {
+        const int col = g * tpr + ti;
+        if (col < G) dh_s[rb * G + col] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 
-    for (int base = row0; base < row_end; base += rb_n) {
-        const int t = base + rb;
-        const bool valid = t < row_end;
-        float s = a.gscale;
-        if (dynamic) {
-            float amax = 0.0f;
+    const int batches = (a.M + rb_n - 1) / rb_n;
+    int buf = 0;
+    for (int bt = block; bt < batches; bt += nblocks, buf ^= 1) {
+        const int t = bt * rb_n + rb;
+        const bool valid = t < a.M;
+        float4 v[GPT];
+        float amax = 0.0f, l1 = 0.0f;
 #pragma unroll
-            for (int g = 0; g < GPT; ++g) {
-                const int col = g * tpr + ti;
-                if (valid && col < G) {
-                    const float4 v = __ldg(dy4 + (long long)t * G + col);
-                    const float4 f = __ldg(h4 + col);
-                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x * f.x), fabsf(v.y * f.y)),
-                                             fmaxf(fabsf(v.z * f.z), fabsf(v.w * f.w))));
-                }
+        for (int g = 0; g < GPT; ++g) {
+            const int col = g * tpr + ti;
+            v[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (valid && col < G) {
+                const long long idx = (long long)t * G + col;
+                const float4 d = __ldcs(dy4 + idx);
+                const uint2 cw = __ldcs(c4 + idx);
+                const float4 f = __ldg(h4 + col);
+                v[g] = make_float4(d.x * f.x, d.y * f.y, d.z * f.z, d.w * f.w);
+                const float2 c0 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.x));
+                const float2 c1 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.y));
+                float4 acc = dh_s[rb * G + col];
+                acc.x += d.x * c0.x;
+                acc.y += d.y * c0.y;
+                acc.z += d.z * c1.x;
+                acc.w += d.w * c1.y;
+                dh_s[rb * G + col] = acc;
+                const float4 q = make_float4(fabsf(v[g].x), fabsf(v[g].y), fabsf(v[g].z), fabsf(v[g].w));
+                amax = fmaxf(amax, fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w)));
+                l1 += (q.x + q.y) + (q.z + q.w);
             }
-            amax = row_reduce<true>(amax, red, tpr);
-            s = (amax > 0.0f && amax <= 3.402823466e38f) ? pow2i(14 - ceil_log2_pos(amax)) : 1.0f;
         }
-        float l1 = 0.0f;
+        float s = a.gscale, sig = a.gscale;
+        if (dynamic) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+            }
+            if (lane == 0) red[buf * 16 + warp] = make_float2(amax, l1);
+            __syncthreads();
+            float2 r = red[buf * 16 + rb * wpr];
+            for (int i = 1; i < wpr; ++i) {
+                const float2 o = red[buf * 16 + rb * wpr + i];
+                r.x = fmaxf(r.x, o.x);
+                r.y += o.y;
+            }
+            const bool fin = r.x > 0.0f && r.x <= 3.402823466e38f;
+            s = fin ? pow2i(14 - ceil_log2_pos(r.x)) : 1.0f;
+            sig = s;
+            const float bound = r.y * lmax;  // bound on |db_t . l|, unscaled
+            if (fin && bound > 0.0f && bound <= 3.402823466e38f) sig = pow2i(15 - ceil_log2_pos(bound));
+        }
 #pragma unroll
         for (int g = 0; g < GPT; ++g) {
             const int col = g * tpr + ti;
             if (valid && col < G) {
-                const long long idx = (long long)t * G + col;
-                const float4 v = __ldg(dy4 + idx);
-                const float4 f = __ldg(h4 + col);
                 uint2 st;
-                st.x = pack_half2(v.x * f.x * s, v.y * f.y * s);
-                st.y = pack_half2(v.z * f.z * s, v.w * f.w * s);
-                o4[idx] = st;
-                const __half2 s0 = *reinterpret_cast<const __half2 *>(&st.x);
-                const __half2 s1 = *reinterpret_cast<const __half2 *>(&st.y);
-                const float2 q0 = __half22float2(s0), q1 = __half22float2(s1);
-                l1 += fabsf(q0.x) + fabsf(q0.y) + fabsf(q1.x) + fabsf(q1.y);
-                const uint2 cw = __ldg(c4 + idx);
-                const float2 c0 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.x));
-                const float2 c1 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.y));
-                acc[g].x += v.x * c0.x;
-                acc[g].y += v.y * c0.y;
-                acc[g].z += v.z * c1.x;
-                acc[g].w += v.w * c1.y;
-            }
-        }
-        float sig = a.gscale;
-        if (dynamic) {
-            l1 = row_reduce<false>(l1, red, tpr);
-            const float bound = l1 * lmax;
-            sig = s;
-            if (bound > 0.0f && bound <= 3.402823466e38f) {
-                int e_s;
-                frexpf(s, &e_s);  // s = 0.5 * 2^e_s
-                sig = pow2i((e_s - 1) + 15 - ceil_log2_pos(bound));
+                st.x = pack_half2(v[g].x * s, v[g].y * s);
+                st.y = pack_half2(v[g].z * s, v[g].w * s);
+                __stcs(o4 + (long long)t * G + col, st);
             }
         }
         if (valid && ti == 0) {
@@ -272,41 +276,31 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, float *smem) {
             a.sig_inv[t] = 1.0f / sig;
         }
     }
-
-    // combine the row groups' dh sums in a fixed order, then store the block's partial row
-    for (int q = 0; q < rb_n; ++q) {
-        if (rb == q) {
-#pragma unroll
-            for (int g = 0; g < GPT; ++g) {
-                const int col = g * tpr + ti;
-                if (col < G) {
-                    float4 *d = reinterpret_cast<float4 *>(dh_red) + col;
-                    if (q == 0) {
-                        *d = acc[g];
-                    } else {
-                        float4 o = *d;
-                        o.x += acc[g].x;
-                        o.y += acc[g].y;
-                        o.z += acc[g].z;
-                        o.w += acc[g].w;
-                        *d = o;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
+    __syncthreads();
+    // fixed-order combine of the row groups' dh sums into the block's partial row
     float4 *dst = reinterpret_cast<float4 *>(a.part_dh + (long long)block * a.d_out);
-    for (int col = threadIdx.x; col < G; col += blockDim.x) dst[col] = reinterpret_cast<float4 *>(dh_red)[col];
+    for (int col = threadIdx.x; col < G; col += kStageThreads) {
+        float4 acc = dh_s[col];
+        for (int q = 1; q < rb_n; ++q) {
+            const float4 o = dh_s[q * G + col];
+            acc.x += o.x;
+            acc.y += o.y;
+            acc.z += o.z;
+            acc.w += o.w;
+        }
+        dst[col] = acc;
+    }
 }
 
 template <int GPT>
-__global__ void __launch_bounds__(kStageThreads, 1)
+__global__ void __launch_bounds__(kStageThreads, (GPT <= 8 ? 2 : 1))
     bwd_prologue_kernel(SignPrep p0, SignPrep p1, StageDyArgs a, int stage_blocks) {
     extern __shared__ __align__(16) float smem_f[];
+    pdl_wait();
+    pdl_launch_dependents();
     const int b = blockIdx.x;
     if (b < stage_blocks) {
-        stage_dy_run<GPT>(a, b, smem_f);
+        stage_dy_run<GPT>(a, b, stage_blocks, smem_f);
         return;
     }
     const int b0 = prep_blocks(p0, blockDim.x);
@@ -319,23 +313,38 @@ __global__ void __launch_bounds__(kStageThreads, 1)
 }
 
 // ============================================================== reduce =====
-__global__ void reduce_partials_kernel(ReduceSeg a, ReduceSeg b, ReduceSeg c) {
-    const long long total = (long long)a.n + b.n + c.n;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const float *part;
-        float *out;
-        int rows, n, f;
-        if (i < a.n) {
-            part = a.part, out = a.out, rows = a.rows, n = a.n, f = (int)i;
-        } else if (i < (long long)a.n + b.n) {
-            part = b.part, out = b.out, rows = b.rows, n = b.n, f = (int)(i - a.n);
-        } else {
-            part = c.part, out = c.out, rows = c.rows, n = c.n, f = (int)(i - a.n - b.n);
-        }
-        float acc = 0.0f;
-        for (int p = 0; p < rows; ++p) acc += part[(long long)p * n + f];
-        out[f] += acc;
+// out[f] += sum_p part[p][f]. A block of 8 warps owns 32 consecutive columns
+// of one segment; warp w sums rows w, w+8, ... and the eight warp sums are
+// added in warp order, so the result does not depend on scheduling.
+__global__ void __launch_bounds__(256) reduce_partials_kernel(ReduceSeg a, ReduceSeg b, ReduceSeg c) {
+    __shared__ float red[8][32];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int nba = (a.n + 31) / 32, nbb = (b.n + 31) / 32;
+    const float *part;
+    float *out;
+    int rows, n, col0;
+    if ((int)blockIdx.x < nba) {
+        part = a.part, out = a.out, rows = a.rows, n = a.n, col0 = blockIdx.x * 32;
+    } else if ((int)blockIdx.x < nba + nbb) {
+        part = b.part, out = b.out, rows = b.rows, n = b.n, col0 = (blockIdx.x - nba) * 32;
+    } else {
+        part = c.part, out = c.out, rows = c.rows, n = c.n, col0 = (blockIdx.x - nba - nbb) * 32;
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int col = col0 + lane;
+    float acc = 0.0f;
+    if (col < n) {
+#pragma unroll 4
+        for (int p = w; p < rows; p += 8) acc += __ldcs(part + (long long)p * n + col);
+    }
+    red[w][lane] = acc;
+    __syncthreads();
+    if (w == 0 && col < n) {
+        float t = red[0][lane];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) t += red[i][lane];
+        out[col] += t;
     }
 }
 
@@ -350,17 +359,17 @@ static int grid_for(long long items, int per_block, int cap = 1 << 20) {
 cudaError_t launch_pack_signs(const float *src, uint32_t *bits, int rows, int r, cudaStream_t s) {
     const long long words = (long long)rows * ((r + 31) / 32);
     trace_before("pack_signs", s);
-    pack_signs_kernel<<<grid_for(words, 8, 65535), 256, 0, s>>>(src, bits, rows, r);
+    cudaError_t e = launch_k(pack_signs_kernel, dim3(grid_for(words, 8, 65535)), dim3(256), 0, s, src, bits, rows, r);
     trace_after(s);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, int r, cudaStream_t s) {
     const long long words = (long long)rows * ((r + 31) / 32);
     trace_before("unpack_signs", s);
-    unpack_signs_kernel<<<grid_for(words, 256, 65535), 256, 0, s>>>(bits, dst, rows, r);
+    cudaError_t e = launch_k(unpack_signs_kernel, dim3(grid_for(words, 256, 65535)), dim3(256), 0, s, bits, dst, rows, r);
     trace_after(s);
-    return cudaGetLastError();
+    return e;
 }
 
 static int host_prep_blocks(const SignPrep &p, int threads) {
@@ -373,47 +382,90 @@ static int host_prep_blocks(const SignPrep &p, int threads) {
 }
 
 cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
-                                int d_in, cudaStream_t s) {
+                                int d_in, uint32_t *status, cudaStream_t s) {
+    static bool prepared = false;
+    if (!prepared) {
+        cudaError_t e = prepare_kernel(fwd_prologue_kernel, 0);
+        if (e != cudaSuccess) return e;
+        prepared = true;
+    }
     const int b0 = host_prep_blocks(p0, 256), b1 = host_prep_blocks(p1, 256);
     const long long groups = (long long)M * (d_in / 4);
     int bs = grid_for(groups, 256 * 4, 152 * 16);
     trace_before("fwd_prologue", s);
-    fwd_prologue_kernel<<<b0 + b1 + bs, 256, 0, s>>>(p0, p1, x, g, x16, M, d_in);
+    cudaError_t e = launch_k(fwd_prologue_kernel, dim3(b0 + b1 + bs), dim3(256), 0, s, p0, p1, x, g, x16, M, d_in, status);
     trace_after(s);
-    return cudaGetLastError();
+    return e;
 }
 
 template <int GPT>
 static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
-    const int sb = stage_dy_blocks(a.M, a.d_out);
+    const int tpr = stage_tpr(a.d_out);
+    const int rb_n = kStageThreads / tpr;
+    const size_t smem = (64 + (size_t)rb_n * a.d_out) * sizeof(float);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = prepare_kernel(bwd_prologue_kernel<GPT>, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    // blocks per SM for this shared-memory size, queried once per size
+    static int cached_smem[8] = {0}, cached_per_sm[8] = {0}, cached_sms = 0;
+    int per_sm = 0;
+    for (int i = 0; i < 8; ++i)
+        if (cached_smem[i] == (int)smem) per_sm = cached_per_sm[i];
+    if (per_sm == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&cached_sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_prologue_kernel<GPT>, kStageThreads, smem);
+        if (per_sm < 1) per_sm = 1;
+        for (int i = 0; i < 8; ++i)
+            if (cached_smem[i] == 0) {
+                cached_smem[i] = (int)smem;
+                cached_per_sm[i] = per_sm;
+                break;
+            }
+    }
+    const int sms = cached_sms;
+    int sb = stage_dy_blocks(a.M, a.d_out);
+    if (sb > per_sm * sms) sb = per_sm * sms;
     const int b0 = host_prep_blocks(p0, kStageThreads), b1 = host_prep_blocks(p1, kStageThreads);
-    const size_t smem = (32 + (size_t)a.d_out) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(bwd_prologue_kernel<GPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
     trace_before("bwd_prologue", s);
-    bwd_prologue_kernel<GPT><<<sb + b0 + b1, kStageThreads, smem, s>>>(p0, p1, a, sb);
+    cudaError_t e = launch_k(bwd_prologue_kernel<GPT>, dim3(sb + b0 + b1), dim3(kStageThreads), smem, s, p0, p1, a, sb);
     trace_after(s);
-    return cudaGetLastError();
+    if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
+    return e;
 }
 
 cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
-    const int tpr = stage_tpr(a.d_out);
-    const int gpt = (a.d_out / 4 + tpr - 1) / tpr;
-    if (gpt <= 1) return launch_bwd_prologue_t<1>(p0, p1, a, s);
-    if (gpt <= 2) return launch_bwd_prologue_t<2>(p0, p1, a, s);
-    if (gpt <= 4) return launch_bwd_prologue_t<4>(p0, p1, a, s);
-    if (gpt <= 8) return launch_bwd_prologue_t<8>(p0, p1, a, s);
-    if (gpt <= 16) return launch_bwd_prologue_t<16>(p0, p1, a, s);
+    switch (stage_gpt(a.d_out)) {
+        case 1: return launch_bwd_prologue_t<1>(p0, p1, a, s);
+        case 2: return launch_bwd_prologue_t<2>(p0, p1, a, s);
+        case 3:
+        case 4: return launch_bwd_prologue_t<4>(p0, p1, a, s);
+        case 5:
+        case 6:
+        case 7:
+        case 8: return launch_bwd_prologue_t<8>(p0, p1, a, s);
+        default: break;
+    }
+    if (stage_gpt(a.d_out) <= 16) return launch_bwd_prologue_t<16>(p0, p1, a, s);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaStream_t s) {
-    const long long total = (long long)a.n + b.n + c.n;
+    const int blocks = (a.n + 31) / 32 + (b.n + 31) / 32 + (c.n + 31) / 32;
+    static bool prepared = false;
+    if (!prepared) {
+        cudaError_t e = prepare_kernel(reduce_partials_kernel, 0);
+        if (e != cudaSuccess) return e;
+        prepared = true;
+    }
     trace_before("reduce_partials", s);
-    reduce_partials_kernel<<<grid_for(total, 256, 4096), 256, 0, s>>>(a, b, c);
+    cudaError_t e = launch_k(reduce_partials_kernel, dim3(blocks), dim3(256), 0, s, a, b, c);
     trace_after(s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace blr

@@ -5,20 +5,31 @@
 // for one 128-token x BN-feature tile at a time, with a fused epilogue per
 // pass. The activation operand is an f16 matrix [M][K] brought in by TMA
 // (128-byte swizzle, box 64 x 128). The sign operand is never stored as a
-// dense matrix anywhere: expander warps read the pair-ready bitmap words and
-// write +-1 f16 straight into the shared-memory operand tile, in the same
-// 128-byte-swizzled K-major layout TMA produces. One thread issues the MMAs;
-// the accumulators live in TMEM, double-buffered so that the epilogue of one
-// tile overlaps the main loop of the next.
+// dense matrix anywhere: the TMA producer bulk-copies each k-step's
+// pair-ready bitmap words (BN x 8 bytes) next to the activation tile, and
+// expander warps turn them into +-1 f16 straight in a shared-memory operand
+// tile, in the same 128-byte-swizzled K-major layout TMA produces. One thread
+// issues the MMAs; the accumulators live in TMEM, double-buffered so that the
+// epilogue of one tile overlaps the main loop of the next.
+//
+// Two rings feed the MMAs: a deep "A ring" (activation tile + bitmap words,
+// filled by TMA, so that load latency is hidden) and a shallow "B ring" of
+// expanded sign tiles (filled by the expanders from the A ring's words).
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-5 sign expanders, warps 6-9 epilogue (warp w reads TMEM
 // lanes 32*(w%4) .. +31, i.e. tokens 32*(w%4) .. +31 of the tile).
 //
+// Epilogues: the two products with a wide output (c and dx', N = d_out or
+// d_in, K = r) stage each 32 x 32 output chunk in per-warp shared memory and
+// write it with TMA stores; their input chunks (x for dg, y for accumulation)
+// arrive by TMA into the same buffers, double-buffered. The two products with
+// a narrow output (a and db, N = r) write straight from registers.
+//
 // Every wait is bounded (blr_device.cuh): a wait that runs out sets the
 // shared abort flag and a status bit, the other roles leave their loops, the
-// TMA producer drains its in-flight loads, the MMA issuer drains its MMAs, and
-// the CTA frees its TMEM and returns.
+// TMA producer drains its in-flight loads, the epilogue drains its copies,
+// the MMA issuer drains its MMAs, and the CTA frees its TMEM and returns.
 #pragma once
 
 #include "blr_device.cuh"
@@ -36,16 +47,28 @@ constexpr int kNumExpWarps = 4;
 constexpr int kWarpEpi0 = 6;
 constexpr int kNumEpiWarps = 4;
 
-template <int BN>
+template <int BN, int EPI>
 struct GemmShape {
-    static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = BN * kBK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStagesRaw = (192 * 1024) / kStageBytes;
-    static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
+    static constexpr bool kTmaEpi = (EPI == kEpiFwd2 || EPI == kEpiBwd2);
+    static constexpr int kABytes = kBM * kBK * 2;  // activation tile
+    static constexpr int kBitsBytes = BN * 8;      // bitmap words of one k-step
+    static constexpr int kBBytes = BN * kBK * 2;   // expanded sign tile
+    static constexpr int kEpiF32 = 32 * 32 * 4;
+    static constexpr int kEpiF16 = (EPI == kEpiFwd2) ? 32 * 32 * 2 : 0;
+    static constexpr int kEpiBuf = kEpiF32 + kEpiF16;
+    static constexpr int kEpiBytes = kTmaEpi ? kNumEpiWarps * 2 * kEpiBuf : 0;
+    static constexpr int kBudget = 205 * 1024 - kEpiBytes;
+    static constexpr int kNB = kTmaEpi ? 2 : (BN >= 128 ? 3 : 4);
+    static constexpr int kNARaw = (kBudget - kNB * kBBytes) / (kABytes + kBitsBytes);
+    static constexpr int kNA = kNARaw > 8 ? 8 : kNARaw;
     static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr int kBarBytes = (3 * kStages + 5) * 8;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + 16;
+    static constexpr int kBitsRegion = ((kNA * kBitsBytes + 1023) / 1024) * 1024;
+    static constexpr int kNumBars = 2 * kNA + 2 * kNB + 4 + 1 + kNumEpiWarps * 2;
+    static constexpr int kSmemBytes =
+        1024 + kNA * kABytes + kNB * kBBytes + kEpiBytes + kBitsRegion + kNumBars * 8 + 16;
+    static_assert(kNA >= 2, "activation ring too shallow");
+    static_assert(kBitsBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 // Sum of p[j] over the 32 lanes of the warp, returned in lane j (a
@@ -70,11 +93,18 @@ __device__ __forceinline__ void fail_status(const GemmArgs &a, volatile int *abo
     atomicOr(a.status, code);
 }
 
-// Epilogue of one 32-column chunk. f[] = accumulator of token t (this
-// thread's TMEM lane), columns col0 .. col0+31.
+// Byte offset of 16-byte chunk c of row `row` in a box with 128-byte rows in
+// the 128-byte swizzle (the layout TMA reads and writes).
+__device__ __forceinline__ int sw128_off(int row, int c) { return row * 128 + ((c ^ (row & 7)) << 4); }
+// Same for 64-byte rows and the 64-byte swizzle.
+__device__ __forceinline__ int sw64_off(int row, int c) { return row * 64 + ((c ^ ((row >> 1) & 3)) << 4); }
+
+// Epilogue of one 32-column chunk of a narrow-output product (N = r), written
+// straight from registers. f[] = accumulator of token t (this thread's TMEM
+// lane), columns col0 .. col0+31.
 template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs &a, float (&f)[32], long long t, bool valid, int col0,
-                                               int part_row, float row_inv, float row_scale) {
+__device__ __forceinline__ void epilogue_chunk_direct(const GemmArgs &a, float (&f)[32], long long t, bool valid,
+                                                      int col0, int part_row, float row_inv, float row_scale) {
     const long long rowoff = t * (long long)a.N + col0;
     const float4 *cv = reinterpret_cast<const float4 *>(a.colv + col0);
     if constexpr (EPI == kEpiFwd1) {
@@ -94,31 +124,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &a, float (&f)[32]
 #pragma unroll
             for (int j = 0; j < 4; ++j) d16[j] = make_uint4(hp[4 * j], hp[4 * j + 1], hp[4 * j + 2], hp[4 * j + 3]);
         }
-    } else if constexpr (EPI == kEpiFwd2) {
-        // y (+)= h.c, and c saved in f16 for dh
-        if (valid) {
-            float4 *d = reinterpret_cast<float4 *>(a.out32 + rowoff);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 hv = __ldg(cv + j);
-                float4 y = make_float4(hv.x * f[4 * j], hv.y * f[4 * j + 1], hv.z * f[4 * j + 2], hv.w * f[4 * j + 3]);
-                if (a.accumulate) {
-                    const float4 o = d[j];
-                    y.x += o.x;
-                    y.y += o.y;
-                    y.z += o.z;
-                    y.w += o.w;
-                }
-                d[j] = y;
-            }
-            uint4 *d16 = reinterpret_cast<uint4 *>(a.out16 + rowoff);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                d16[j] = make_uint4(pack_half2(f[8 * j], f[8 * j + 1]), pack_half2(f[8 * j + 2], f[8 * j + 3]),
-                                    pack_half2(f[8 * j + 4], f[8 * j + 5]), pack_half2(f[8 * j + 6], f[8 * j + 7]));
-            }
-        }
-    } else if constexpr (EPI == kEpiBwd1) {
+    } else {
         // db = acc / s_t; dl partial sum_t a.db; db.l staged under sigma_t
         float p[32];
         uint32_t hp[16];
@@ -143,14 +149,50 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &a, float (&f)[32]
         }
         const float s = warp_column_sums(p);
         a.part[(long long)part_row * a.N + col0 + (threadIdx.x & 31)] = s;
+    }
+}
+
+// Epilogue of one 32-column chunk of a wide-output product, through the
+// warp's shared-memory chunk buffer `buf` (f32 part in the 128-byte swizzle;
+// for the forward an f16 part at +4096 in the 64-byte swizzle). When `has_in`
+// the f32 part already holds the chunk's input (x for the backward, y for an
+// accumulating forward); outputs overwrite the buffer in place.
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk_smem(const GemmArgs &a, float (&f)[32], uint8_t *buf, long long t,
+                                                    bool valid, int col0, int part_row, float row_inv,
+                                                    bool has_in) {
+    const int row = threadIdx.x & 31;
+    const float4 *cv = reinterpret_cast<const float4 *>(a.colv + col0);
+    if constexpr (EPI == kEpiFwd2) {
+        // y (+)= h.c, c saved in f16
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 hv = __ldg(cv + j);
+            float4 y = make_float4(hv.x * f[4 * j], hv.y * f[4 * j + 1], hv.z * f[4 * j + 2], hv.w * f[4 * j + 3]);
+            float4 *slot = reinterpret_cast<float4 *>(buf + sw128_off(row, j));
+            if (has_in) {
+                const float4 o = *slot;
+                y.x += o.x;
+                y.y += o.y;
+                y.z += o.z;
+                y.w += o.w;
+            }
+            *slot = y;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            *reinterpret_cast<uint4 *>(buf + 4096 + sw64_off(row, j)) =
+                make_uint4(pack_half2(f[8 * j], f[8 * j + 1]), pack_half2(f[8 * j + 2], f[8 * j + 3]),
+                           pack_half2(f[8 * j + 4], f[8 * j + 5]), pack_half2(f[8 * j + 6], f[8 * j + 7]));
+        }
     } else {
         // dx' = acc / sigma_t; dg partial sum_t x.dx'; dx (+)= g.dx'
         float p[32];
-        const float4 *xp = reinterpret_cast<const float4 *>(a.aux + rowoff);
-        float4 *d = reinterpret_cast<float4 *>(a.out32 + rowoff);
+        const long long rowoff = t * (long long)a.N + col0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float4 xv = valid ? __ldg(xp + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 *slot = reinterpret_cast<float4 *>(buf + sw128_off(row, j));
+            const float4 xv = *slot;  // rows past M arrive as zeros
             const float4 gv = __ldg(cv + j);
             const float d0 = f[4 * j] * row_inv, d1 = f[4 * j + 1] * row_inv;
             const float d2 = f[4 * j + 2] * row_inv, d3 = f[4 * j + 3] * row_inv;
@@ -158,17 +200,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &a, float (&f)[32]
             p[4 * j + 1] = xv.y * d1;
             p[4 * j + 2] = xv.z * d2;
             p[4 * j + 3] = xv.w * d3;
-            if (valid) {
-                float4 o = make_float4(gv.x * d0, gv.y * d1, gv.z * d2, gv.w * d3);
-                if (a.accumulate) {
-                    const float4 old = d[j];
-                    o.x += old.x;
-                    o.y += old.y;
-                    o.z += old.z;
-                    o.w += old.w;
-                }
-                d[j] = o;
+            float4 o = make_float4(gv.x * d0, gv.y * d1, gv.z * d2, gv.w * d3);
+            if (a.accumulate && valid) {
+                const float4 old = *reinterpret_cast<const float4 *>(a.out32 + rowoff + 4 * j);
+                o.x += old.x;
+                o.y += old.y;
+                o.z += old.z;
+                o.w += old.w;
             }
+            *slot = o;
         }
         const float s = warp_column_sums(p);
         a.part[(long long)part_row * a.N + col0 + (threadIdx.x & 31)] = s;
@@ -177,20 +217,26 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs &a, float (&f)[32]
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs args) {
-    using S = GemmShape<BN>;
+    blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ EpiMaps emaps,
+                    const GemmArgs args) {
+    using S = GemmShape<BN, EPI>;
+    constexpr int NA = S::kNA, NB = S::kNB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + S::kStages * S::kABytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + S::kStages * S::kBBytes);
+    uint8_t *sA = smem;                                                 // [NA][kABytes]
+    uint8_t *sB = sA + NA * S::kABytes;                                 // [NB][kBBytes]
+    uint8_t *sE = sB + NB * S::kBBytes;                                 // [4 warps][2][kEpiBuf]
+    uint32_t *sBits = reinterpret_cast<uint32_t *>(sE + S::kEpiBytes);  // [NA][BN*2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sBits) + S::kBitsRegion);
     uint64_t *full_a = bars;
-    uint64_t *full_b = bars + S::kStages;
-    uint64_t *empty = bars + 2 * S::kStages;
-    uint64_t *tmem_full = bars + 3 * S::kStages;
+    uint64_t *empty_a = full_a + NA;
+    uint64_t *full_b = empty_a + NA;
+    uint64_t *empty_b = full_b + NB;
+    uint64_t *tmem_full = empty_b + NB;
     uint64_t *tmem_empty = tmem_full + 2;
     uint64_t *drain_bar = tmem_full + 4;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain_bar + 1);
+    uint64_t *eload = drain_bar + 1;  // [4 warps][2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(eload + kNumEpiWarps * 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32;
@@ -202,20 +248,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int num_kb = (args.K + kBK - 1) / kBK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S::kStages; ++s) {
+        for (int s = 0; s < NA; ++s) {
             mbar_init(&full_a[s], 1);
+            mbar_init(&empty_a[s], 1);
+        }
+        for (int s = 0; s < NB; ++s) {
             mbar_init(&full_b[s], kNumExpWarps);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty_b[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tmem_full[i], 1);
             mbar_init(&tmem_empty[i], kNumEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        for (int i = 0; i < kNumEpiWarps * 2; ++i) mbar_init(&eload[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == kWarpTma && lane == 0) tma_prefetch_desc(&tmap_a);
+    if constexpr (S::kTmaEpi) {
+        if (warp == kWarpEpi0 && lane == 0) {
+            tma_prefetch_desc(&emaps.out32);
+            tma_prefetch_desc(&emaps.in32);
+            if constexpr (EPI == kEpiFwd2) tma_prefetch_desc(&emaps.out16);
+        }
+    }
     if (warp == kWarpMma) {
         tmem_alloc(tmem_slot, S::kTmemCols);
         tmem_relinquish();
@@ -224,32 +281,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // setup above overlaps the previous kernel; global memory only after this
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == kWarpTma) {
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0, issued = 0, parity = 0;
+            int sa = 0;
+            uint32_t pa = 0, issued = 0, parity = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 const int m0 = (tile / n_tiles) * kBM;
+                const int n0 = (tile % n_tiles) * BN;
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                    if (!mbar_wait(&empty_a[sa], pa ^ 1u, abort_flag)) {
                         fail_status(args, abort_flag, kStTimeoutTma);
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full_a[stage], S::kABytes);
-                    tma_load_2d(sA + stage * S::kABytes, &tmap_a, &full_a[stage], kb * kBK, m0);
-                    issued |= 1u << stage;
-                    parity = (parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == S::kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    mbar_arrive_expect_tx(&full_a[sa], S::kABytes + S::kBitsBytes);
+                    tma_load_2d(sA + sa * S::kABytes, &tmap_a, &full_a[sa], kb * kBK, m0);
+                    bulk_load(sBits + sa * (S::kBitsBytes / 4), args.bsign + ((size_t)kb * N + n0) * 2,
+                              S::kBitsBytes, &full_a[sa]);
+                    issued |= 1u << sa;
+                    parity = (parity & ~(1u << sa)) | (pa << sa);
+                    if (++sa == NA) {
+                        sa = 0;
+                        pa ^= 1u;
                     }
                 }
             }
             // drain: every load issued must have landed before the CTA exits
-            for (int s = 0; s < S::kStages; ++s) {
+            for (int s = 0; s < NA; ++s) {
                 if (((issued >> s) & 1u) && !mbar_wait(&full_a[s], (parity >> s) & 1u, abort_flag, false))
                     atomicOr(args.status, kStTimeoutDrain);
             }
@@ -258,8 +321,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             constexpr uint32_t idesc = umma_idesc_f16_f32(kBM, BN);
-            int stage = 0;
-            uint32_t phase = 0;
+            int sa = 0, sb = 0;
+            uint32_t pa = 0, pb = 0;
             bool ok = true;
             int local = 0;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
@@ -272,24 +335,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&full_a[stage], phase, abort_flag) || !mbar_wait(&full_b[stage], phase, abort_flag)) {
+                    if (!mbar_wait(&full_a[sa], pa, abort_flag) || !mbar_wait(&full_b[sb], pb, abort_flag)) {
                         fail_status(args, abort_flag, kStTimeoutMma);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = umma_sdesc_sw128(smem_u32(sA + stage * S::kABytes));
-                    const uint64_t bdesc = umma_sdesc_sw128(smem_u32(sB + stage * S::kBBytes));
+                    const uint64_t adesc = umma_sdesc_sw128(smem_u32(sA + sa * S::kABytes));
+                    const uint64_t bdesc = umma_sdesc_sw128(smem_u32(sB + sb * S::kBBytes));
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
                         // advance 16 f16 (32 bytes) along K inside the swizzled rows
                         umma_f16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
                                  (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    umma_commit(&empty[stage]);
-                    if (++stage == S::kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    umma_commit(&empty_a[sa]);
+                    umma_commit(&empty_b[sb]);
+                    if (++sa == NA) {
+                        sa = 0;
+                        pa ^= 1u;
+                    }
+                    if (++sb == NB) {
+                        sb = 0;
+                        pb ^= 1u;
                     }
                 }
                 if (!ok) break;
@@ -305,33 +373,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         constexpr int kUnits = BN * 2;  // (operand row, word) pairs per k-step
         constexpr int kUpt = (kUnits + 127) / 128;
         const int e = threadIdx.x - kWarpExp0 * 32;
-        int stage = 0;
-        uint32_t phase = 0;
+        int sa = 0, sb = 0;
+        uint32_t pa = 0, pb = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const int n0 = (tile % n_tiles) * BN;
             for (int kb = 0; kb < num_kb; ++kb) {
-                const uint32_t *src = args.bsign + ((size_t)kb * N + n0) * 2;
-                uint32_t wv[kUpt];
-#pragma unroll
-                for (int i = 0; i < kUpt; ++i) {
-                    const int u = e + 128 * i;
-                    wv[i] = (u < kUnits) ? __ldg(src + u) : 0u;
-                }
-                const bool got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+                const bool got =
+                    mbar_wait(&full_a[sa], pa, abort_flag) && mbar_wait(&empty_b[sb], pb ^ 1u, abort_flag);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     if (lane == 0) fail_status(args, abort_flag, kStTimeoutExpand);
                     ok = false;
                     break;
                 }
-                uint8_t *tile_b = sB + stage * S::kBBytes;
+                const uint32_t *bits = sBits + sa * (S::kBitsBytes / 4);
+                uint8_t *tile_b = sB + sb * S::kBBytes;
 #pragma unroll
                 for (int i = 0; i < kUpt; ++i) {
                     const int u = e + 128 * i;
                     if (u < kUnits) {
                         const int row = u >> 1;
                         const int w = u & 1;
-                        const uint32_t p = wv[i];
+                        const uint32_t p = bits[u];
                         uint8_t *rowp = tile_b + row * 128;
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -344,29 +406,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full_b[stage]);
-                if (++stage == S::kStages) {
-                    stage = 0;
-                    phase ^= 1u;
+                if (lane == 0) mbar_arrive(&full_b[sb]);
+                if (++sa == NA) {
+                    sa = 0;
+                    pa ^= 1u;
+                }
+                if (++sb == NB) {
+                    sb = 0;
+                    pb ^= 1u;
                 }
             }
         }
     } else {
         // ---- epilogue ------------------------------------------------------
         const int q = warp & 3;
+        constexpr int kChunks = BN / 32;
+        uint8_t *ebuf = sE + (warp - kWarpEpi0) * 2 * S::kEpiBuf;
+        uint64_t *ebar = eload + (warp - kWarpEpi0) * 2;
+        const bool has_in = (EPI == kEpiBwd2) || (EPI == kEpiFwd2 && args.accumulate);
+        uint32_t ephase = 0u;   // bit b: phase of buffer b's next input load
+        uint32_t pending = 0u;  // bit b: an input load in flight into buffer b (lane 0's view)
+        int gch = 0;                       // running chunk count: buffer = gch & 1
         int local = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
             const int acc = local & 1;
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
             const int mt = tile / n_tiles;
             const int n0 = (tile % n_tiles) * BN;
+            const int row0 = mt * kBM + q * 32;
+            if constexpr (S::kTmaEpi) {
+                // this tile's first two input chunks, once the buffers' last stores have read them
+                if (has_in && lane == 0) {
+                    bulk_wait_group_read<0>();
+                    for (int c = 0; c < 2 && c < kChunks; ++c) {
+                        const int b = (gch + c) & 1;
+                        mbar_arrive_expect_tx(&ebar[b], S::kEpiF32);
+                        tma_load_2d(ebuf + b * S::kEpiBuf, &emaps.in32, &ebar[b], n0 + 32 * c, row0);
+                        pending |= 1u << b;
+                    }
+                }
+            }
             const bool got = mbar_wait(&tmem_full[acc], acc_phase, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, got)) {
                 if (lane == 0) fail_status(args, abort_flag, kStTimeoutEpi);
+                ok = false;
                 break;
             }
             tc_fence_after();
-            const long long t = (long long)mt * kBM + q * 32 + lane;
+            const long long t = (long long)row0 + lane;
             const bool valid = t < M;
             float row_inv = 1.0f, row_scale = 1.0f;
             if constexpr (EPI == kEpiBwd1 || EPI == kEpiBwd2) {
@@ -377,11 +465,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             const int part_row = mt * 4 + q;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = 0; ch < kChunks; ++ch, ++gch) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + ch * 32), v);
                 tmem_wait_ld();
-                if (ch == BN / 32 - 1) {
+                if (ch == kChunks - 1) {
                     // accumulator fully read: hand it back to the MMA issuer
                     tc_fence_before();
                     __syncwarp();
@@ -390,8 +478,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 float f[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-                epilogue_chunk<EPI>(args, f, t, valid, n0 + ch * 32, part_row, row_inv, row_scale);
+                if constexpr (S::kTmaEpi) {
+                    const int b = gch & 1;
+                    uint8_t *buf = ebuf + b * S::kEpiBuf;
+                    if (has_in) {
+                        const bool in_ok = mbar_wait(&ebar[b], (ephase >> b) & 1u, abort_flag);
+                        ephase ^= 1u << b;
+                        pending &= ~(1u << b);
+                        if (!__all_sync(0xFFFFFFFFu, in_ok)) {
+                            if (lane == 0) fail_status(args, abort_flag, kStTimeoutEpi);
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        // the store that last used this buffer must have read it
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                    }
+                    epilogue_chunk_smem<EPI>(args, f, buf, t, valid, n0 + ch * 32, part_row, row_inv, has_in);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&emaps.out32, buf, n0 + ch * 32, row0);
+                        if constexpr (EPI == kEpiFwd2) tma_store_2d(&emaps.out16, buf + 4096, n0 + ch * 32, row0);
+                        bulk_commit_group();
+                        if (has_in && ch + 2 < kChunks) {
+                            // chunk ch+2 uses this buffer again: load it once the store has read it
+                            bulk_wait_group_read<0>();
+                            mbar_arrive_expect_tx(&ebar[b], S::kEpiF32);
+                            tma_load_2d(buf, &emaps.in32, &ebar[b], n0 + 32 * (ch + 2), row0);
+                            pending |= 1u << b;
+                        }
+                    }
+                    __syncwarp();
+                } else {
+                    epilogue_chunk_direct<EPI>(args, f, t, valid, n0 + ch * 32, part_row, row_inv, row_scale);
+                }
             }
+        }
+        if constexpr (S::kTmaEpi) {
+            // drain: stores complete, and input loads issued but not consumed have landed
+            if (lane == 0) {
+                bulk_wait_group_all();
+                for (int b = 0; b < 2; ++b)
+                    if (((pending >> b) & 1u) && !mbar_wait(&ebar[b], (ephase >> b) & 1u, abort_flag, false))
+                        atomicOr(args.status, kStTimeoutDrain);
+            }
+            __syncwarp();
         }
     }
 
@@ -402,23 +535,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <int BN, int EPI>
-cudaError_t launch_gemm_t(const CUtensorMap &tmap_a, const GemmArgs &args, int grid, cudaStream_t s) {
-    using S = GemmShape<BN>;
-    static_assert(S::kSmemBytes <= 227 * 1024, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(blr_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    blr_gemm_kernel<BN, EPI><<<grid, kGemmThreads, S::kSmemBytes, s>>>(tmap_a, args);
-    return cudaGetLastError();
+cudaError_t launch_gemm_t(const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args, int grid,
+                          cudaStream_t s) {
+    using S = GemmShape<BN, EPI>;
+    static bool attr_set = false;  // set once, outside any later stream capture
+    if (!attr_set) {
+        cudaError_t e = prepare_kernel(blr_gemm_kernel<BN, EPI>, S::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch_k(blr_gemm_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), S::kSmemBytes, s, tmap_a, emaps,
+                    args);
 }
 
 template <int EPI>
-cudaError_t launch_gemm_epi(int bn, const CUtensorMap &tmap_a, const GemmArgs &args, int grid, cudaStream_t s) {
+cudaError_t launch_gemm_epi(int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args,
+                            int grid, cudaStream_t s) {
     switch (bn) {
-        case 32: return launch_gemm_t<32, EPI>(tmap_a, args, grid, s);
-        case 64: return launch_gemm_t<64, EPI>(tmap_a, args, grid, s);
-        case 128: return launch_gemm_t<128, EPI>(tmap_a, args, grid, s);
-        case 256: return launch_gemm_t<256, EPI>(tmap_a, args, grid, s);
+        case 32: return launch_gemm_t<32, EPI>(tmap_a, emaps, args, grid, s);
+        case 64: return launch_gemm_t<64, EPI>(tmap_a, emaps, args, grid, s);
+        case 128: return launch_gemm_t<128, EPI>(tmap_a, emaps, args, grid, s);
+        case 256: return launch_gemm_t<256, EPI>(tmap_a, emaps, args, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }

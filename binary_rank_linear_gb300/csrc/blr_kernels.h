@@ -10,6 +10,33 @@
 
 namespace blr {
 
+// Launch with programmatic stream serialization (see pdl_wait in
+// blr_device.cuh) and the maximum shared-memory carveout, so that consecutive
+// kernels of a pass overlap their setup and never reconfigure L1/shared
+// memory between each other.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Sets the maximum dynamic shared memory and the carveout of `kernel` once.
+template <typename... KArgs>
+cudaError_t prepare_kernel(void (*kernel)(KArgs...), int max_dyn_smem) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+}
+
 // Optional per-kernel event tracing (see blr_trace_begin in blr.h).
 void trace_before(const char *name, cudaStream_t stream);
 void trace_after(cudaStream_t stream);
@@ -30,9 +57,10 @@ struct SignPrep {
     int kind;  // 0 direct, 1 transpose
 };
 
-// Forward prologue, one launch: re-lay two bitmaps and stage x16 = f16(x.g).
+// Forward prologue, one launch: clear the device status word, re-lay two
+// bitmaps and stage x16 = f16(x.g).
 cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
-                                int d_in, cudaStream_t s);
+                                int d_in, uint32_t *status, cudaStream_t s);
 
 // Backward prologue, two parts in one launch: re-lay two bitmaps, and stage
 // dy16 = f16(dy.h.s_t) with per-token scales, dh partials and sigma_t.
@@ -45,11 +73,12 @@ struct StageDyArgs {
     float *s_inv;          // [M] out: 1/s_t
     float *sig;            // [M] out: sigma_t (scale of db.l)
     float *sig_inv;        // [M] out: 1/sigma_t
-    float *part_dh;        // [rows_blocks][d_out] out
+    float *part_dh;        // [stage_dy_blocks(M, d_out)][d_out] out
     float gscale;          // > 0 fixed, <= 0 dynamic
     int M, d_out, r;
+    int *rows_used;        // host out: dh partial rows the launch wrote
 };
-int stage_dy_blocks(int M, int d_out);  // number of dh partial rows
+int stage_dy_blocks(int M, int d_out);  // dh partial rows reserved in the workspace
 cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s);
 
 // out[f] += sum_p part[p][f] over three independent segments, fixed order.
@@ -80,10 +109,17 @@ struct GemmArgs {
     uint32_t *status;        // device status word
 };
 
+// Extra TMA descriptors of the wide-output products (c and dx'); unused by
+// the other two.
+struct EpiMaps {
+    CUtensorMap out32;  // f32 [M][N], box 32 x 32, 128-byte swizzle (y or dx)
+    CUtensorMap out16;  // f16 [M][N], box 32 x 32, 64-byte swizzle (c)
+    CUtensorMap in32;   // f32 [M][N], box 32 x 32, 128-byte swizzle (x, or y to accumulate)
+};
+
 // `tmap_a`: the f16 activation operand [M][K], box 64 x 128, 128-B swizzle.
 // bn: 32, 64, 128 or 256 (must divide N). grid: number of persistent CTAs.
-cudaError_t launch_gemm(int epi, int bn, const CUtensorMap &tmap_a, const GemmArgs &args, int grid,
-                        cudaStream_t s);
-int gemm_smem_bytes(int bn);
+cudaError_t launch_gemm(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args,
+                        int grid, cudaStream_t s);
 
 }  // namespace blr

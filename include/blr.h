@@ -28,7 +28,9 @@
  *    16-byte aligned. The library never allocates, frees or synchronises on
  *    the hot path; work is queued on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and returns before it runs.
- *  - Shape rule: M >= 1; d_in, d_out, r multiples of 32 and >= 64.
+ *  - Shape rule: M >= 1; d_in, d_out, r multiples of 32 and >= 64;
+ *    d_out <= 32768 (one token row of dy is staged by one thread block);
+ *    d_in, r <= 65536.
  *  - Numerics: operands are staged to f16 (round to nearest even), products
  *    accumulate in f32 on the tensor cores, outputs are f32. The forward
  *    stages x.g and a.l unscaled, so |x.g| and |a.l| must stay below 65504.

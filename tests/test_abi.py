@@ -51,7 +51,9 @@ def test_workspace_bytes_shape_rule(lib):
     assert lib.blr_workspace_bytes(0, 256, 256, 64) == 0       # M >= 1
     assert lib.blr_workspace_bytes(128, 48, 256, 64) == 0      # d_in >= 64
     assert lib.blr_workspace_bytes(128, 256, 100, 64) == 0     # multiple of 32
-    assert lib.blr_workspace_bytes(128, 256, 256, 65568) == 0  # <= 65536
+    assert lib.blr_workspace_bytes(128, 256, 256, 65568) == 0  # r <= 65536
+    assert lib.blr_workspace_bytes(128, 256, 32800, 64) == 0   # d_out <= 32768
+    assert lib.blr_workspace_bytes(128, 65536, 32768, 64) > 0
     small = lib.blr_workspace_bytes(2048, 1024, 1024, 256)
     assert lib.blr_workspace_bytes(2049, 1024, 1024, 256) > small
     # tape alone: a f32 [M][r] + c f16 [M][d_out]
