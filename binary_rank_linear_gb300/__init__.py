@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     backward,
     check_status,
     forward,
+    forward_noalloc,
     load,
     pack_signs,
     trace_begin,

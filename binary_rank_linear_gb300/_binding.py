@@ -189,3 +189,28 @@ def trace_end() -> list:
             raise BlrError(BLR_ERR_CUDA, "blr_trace_read")
         out.append((name.decode(), float(ms.value)))
     return out
+
+
+def forward_noalloc(x, bits_u, bits_v, g, l, h, y, accumulate: bool = False, stream=None) -> torch.Tensor:
+    """blr_forward_noalloc: the forward pass for callers that cannot allocate device memory.
+
+    Same inputs and output as ``forward`` but no workspace: the library uses a
+    fixed scratch array in its own device memory (BLR_NOALLOC_SCRATCH_BYTES =
+    16 MiB, held by every GPU that loads the library). The first call on a
+    device looks up that array's address, so make it before any stream
+    capture. Calls share the array: calls that overlap on the GPU race.
+    """
+    lib = load()
+    fn = lib.blr_forward_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
+    fn.restype = I
+    M, d_in = x.shape
+    d_out, r = h.shape[0], l.shape[0]
+    w = words_per_row(r)
+    code = fn(_ptr(x, "x", torch.float32, (M, d_in)), _ptr(bits_u, "bits_u", torch.int32, (d_out, w)),
+              _ptr(bits_v, "bits_v", torch.int32, (d_in, w)), _ptr(g, "g", torch.float32, (d_in,)),
+              _ptr(l, "l", torch.float32, (r,)), _ptr(h, "h", torch.float32, (d_out,)),
+              _ptr(y, "y", torch.float32, (M, d_out)), int(bool(accumulate)), M, d_in, d_out, r, _stream(stream))
+    _check(code, "blr_forward_noalloc")
+    return y

@@ -1,0 +1,196 @@
+// blr_forward_noalloc: the blr forward pass for callers that cannot allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc or any allocator: a plugin running inside
+// a host application that owns every device allocation and forbids raw
+// allocations, or a real-time inference loop with a fixed memory budget that
+// must never enter an allocator. They cannot provide the caller-owned
+// workspace that blr_forward needs. This entry point takes the same inputs and
+// output and uses a fixed scratch array in the library's own device memory
+// instead (BLR_NOALLOC_SCRATCH_BYTES; every GPU that loads the library keeps it
+// until the process exits).
+//
+// It runs the same kernels as blr_forward, with their workspace pointers taken
+// from that array. The host needs the array's device address: the first call
+// on each device looks it up with cudaGetSymbolAddress (with that device
+// current) and caches it, so that first call should be made before any stream
+// capture. All calls share the one array and it keeps the last call's
+// contents; the kernels clear what must start at zero (the status word), and
+// calls that overlap on the GPU race on the array.
+#include <mutex>
+
+#include "../../include/blr.h"
+#include "blr_kernels.h"
+
+namespace blr {
+namespace {
+
+// The scratch array. Host code must not take its address with `&`: on the
+// host the name is a stand-in, not a device address.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[BLR_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_na_mu;
+void *g_na_ptr[64];
+int g_na_sms[64];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn na_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool na_tmap(CUtensorMap *m, const void *base, int rows, int cols, int box_cols, int box_rows, bool f16,
+             CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = na_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t esz = f16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t na_align(size_t v) { return (v + 255) / 256 * 256; }
+
+int na_pick_bn(int M, int N, int sms) {
+    const long long m_tiles = (M + 127) / 128;
+    int bn = 256;
+    while (bn > 32 && N % bn != 0) bn /= 2;
+    while (bn > 32 && m_tiles * (N / bn) < sms && N % (bn / 2) == 0) bn /= 2;
+    return bn;
+}
+
+int na_grid(int M, int N, int bn, int sms) {
+    const long long tiles = (long long)((M + 127) / 128) * (N / bn);
+    return (int)(tiles < sms ? tiles : sms);
+}
+
+// Device address of the scratch array on the current device (looked up once
+// per device), its SM count, and whether the device is supported.
+int na_setup(void **ptr, int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BLR_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    if (!g_na_ptr[dev]) {
+        int maj = 0, min = 0, n = 0;
+        if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return BLR_ERR_CUDA;
+        if (maj != 10 || min != 3) return BLR_ERR_UNSUPPORTED_DEVICE;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return BLR_ERR_CUDA;
+        g_na_ptr[dev] = p;
+        g_na_sms[dev] = n;
+    }
+    *ptr = g_na_ptr[dev];
+    *sms = g_na_sms[dev];
+    return BLR_OK;
+}
+
+// Scratch bytes a forward of this shape needs (0 if the shape is invalid).
+size_t na_scratch_bytes(int M, int d_in, int d_out, int r) {
+    if (M < 1 || d_in < 64 || d_out < 64 || r < 64 || d_in % 32 || d_out % 32 || r % 32 || d_in > 65536 ||
+        d_out > 32768 || r > 65536)
+        return 0;
+    const size_t m = (size_t)M;
+    return na_align(256) + na_align((size_t)((d_in + 63) / 64) * r * 8) + na_align((size_t)((r + 63) / 64) * d_out * 8) +
+           na_align(m * d_in * 2) + na_align(m * r * 4) + na_align(m * r * 2) + na_align(m * d_out * 2);
+}
+
+}  // namespace
+}  // namespace blr
+
+using namespace blr;
+
+extern "C" int blr_forward_noalloc(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, const float *g,
+                                   const float *l, const float *h, float *y, int accumulate_y, int M, int d_in,
+                                   int d_out, int r, blr_stream_t stream) {
+    if (!x || !bits_u || !bits_v || !g || !l || !h || !y) return BLR_ERR_ARG;
+    if (accumulate_y != 0 && accumulate_y != 1) return BLR_ERR_ARG;
+    const size_t need = na_scratch_bytes(M, d_in, d_out, r);
+    if (need == 0) return BLR_ERR_SHAPE;
+    const void *ptrs[] = {x, bits_u, bits_v, g, l, h, y};
+    for (const void *p : ptrs)
+        if (reinterpret_cast<uintptr_t>(p) & 15u) return BLR_ERR_ALIGN;
+    // the shape must fit the fixed scratch array: no allocation happens here
+    if (need > (size_t)BLR_NOALLOC_SCRATCH_BYTES) return BLR_ERR_WORKSPACE;
+
+    void *base = nullptr;
+    int sms = 0;
+    int st = na_setup(&base, &sms);
+    if (st != BLR_OK) return st;
+
+    // scratch layout: status header, two re-laid bitmaps, x16, a (f32), a.l (f16), c (f16)
+    char *w = static_cast<char *>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += na_align(bytes);
+        return w + o;
+    };
+    const size_t m = (size_t)M;
+    uint32_t *status = reinterpret_cast<uint32_t *>(take(256));
+    uint32_t *bp_f1 = reinterpret_cast<uint32_t *>(take((size_t)((d_in + 63) / 64) * r * 8));
+    uint32_t *bp_f2 = reinterpret_cast<uint32_t *>(take((size_t)((r + 63) / 64) * d_out * 8));
+    uint16_t *x16 = reinterpret_cast<uint16_t *>(take(m * d_in * 2));
+    float *a32 = reinterpret_cast<float *>(take(m * r * 4));
+    uint16_t *al16 = reinterpret_cast<uint16_t *>(take(m * r * 2));
+    uint16_t *c16 = reinterpret_cast<uint16_t *>(take(m * d_out * 2));
+
+    CUtensorMap tm_x, tm_a;
+    EpiMaps em_none{}, em_f2{};
+    if (!na_tmap(&tm_x, x16, M, d_in, 64, 128, true, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !na_tmap(&tm_a, al16, M, r, 64, 128, true, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !na_tmap(&em_f2.out32, y, M, d_out, 32, 32, false, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !na_tmap(&em_f2.out16, c16, M, d_out, 32, 32, true, CU_TENSOR_MAP_SWIZZLE_64B))
+        return BLR_ERR_CUDA;
+    em_f2.in32 = em_f2.out32;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    SignPrep pv{bits_v, bp_f1, r, d_in, 1};
+    SignPrep pu{bits_u, bp_f2, d_out, r, 0};
+    if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, status, s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    GemmArgs f1{};
+    f1.M = M;
+    f1.N = r;
+    f1.K = d_in;
+    f1.bsign = bp_f1;
+    f1.out32 = a32;
+    f1.out16 = al16;
+    f1.colv = l;
+    f1.status = status;
+    const int bn1 = na_pick_bn(M, r, sms);
+    if (launch_gemm(kEpiFwd1, bn1, tm_x, em_none, f1, na_grid(M, r, bn1, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    GemmArgs f2{};
+    f2.M = M;
+    f2.N = d_out;
+    f2.K = r;
+    f2.bsign = bp_f2;
+    f2.out32 = y;
+    f2.out16 = c16;
+    f2.colv = h;
+    f2.accumulate = accumulate_y;
+    f2.status = status;
+    const int bn2 = na_pick_bn(M, d_out, sms);
+    if (launch_gemm(kEpiFwd2, bn2, tm_a, em_f2, f2, na_grid(M, d_out, bn2, sms), s) != cudaSuccess)
+        return BLR_ERR_CUDA;
+    return BLR_OK;
+}

@@ -165,6 +165,33 @@ BLR_API int blr_trace_end(void);
 BLR_API int blr_trace_count(void);
 BLR_API const char *blr_trace_read(int i, float *ms);
 
+/* Size in bytes of the fixed scratch array behind blr_forward_noalloc. */
+#define BLR_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* Forward pass for callers that cannot allocate device memory. The pages have
+ * no counterpart: this is a library convenience. Some callers cannot call
+ * cudaMalloc or any allocator, for instance a plugin inside a host application
+ * that owns every device allocation, or a real-time inference loop with a
+ * fixed memory budget, so they cannot provide blr_forward's workspace.
+ * Arguments, layouts and results are those of blr_forward without `ws`: the
+ * scratch is a fixed array of BLR_NOALLOC_SCRATCH_BYTES in the library's own
+ * device memory, held by every GPU that loads the library until exit. No
+ * allocation happens in this call.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array, which keeps the last call's contents; the
+ *    kernels clear what must start at zero. Calls that overlap on the GPU
+ *    (other streams, other threads) race on the array: serialise them.
+ *  - The tape it leaves is not usable by blr_backward.
+ * Errors: as blr_forward; BLR_ERR_WORKSPACE when the shape needs more scratch
+ *   than BLR_NOALLOC_SCRATCH_BYTES (roughly M*(2 d_in + 6 r + 2 d_out) bytes
+ *   plus the re-laid bitmaps). */
+BLR_API int blr_forward_noalloc(const float *x, const uint32_t *bits_u, const uint32_t *bits_v,
+                                const float *g, const float *l, const float *h,
+                                float *y, int accumulate_y,
+                                int M, int d_in, int d_out, int r, blr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
