@@ -155,12 +155,15 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
         return o;
     };
     const size_t m = (size_t)M;
-    const size_t m_tiles = (m + 127) / 128;
     L.header = take(256);
-    L.bp_f1 = take((size_t)((d_in + 63) / 64) * r * 8);   // forward 1: N = r, K = d_in
-    L.bp_f2 = take((size_t)((r + 63) / 64) * d_out * 8);  // forward 2: N = d_out, K = r
-    L.bp_b1 = take((size_t)((d_out + 63) / 64) * r * 8);  // backward 1: N = r, K = d_out
-    L.bp_b2 = take((size_t)((r + 63) / 64) * d_in * 8);   // backward 2: N = d_in, K = r
+    // re-laid bitmaps, [K blocks of 64, padded to an even count][N][2] u32: the
+    // CTA-pair GEMMs consume two blocks per k-step (the pad block is never
+    // multiplied by anything but zero activations)
+    auto kblocks = [](int K) { return (size_t)((K + 127) / 128) * 2; };
+    L.bp_f1 = take(kblocks(d_in) * r * 8);   // forward 1: N = r, K = d_in
+    L.bp_f2 = take(kblocks(r) * d_out * 8);  // forward 2: N = d_out, K = r
+    L.bp_b1 = take(kblocks(d_out) * r * 8);  // backward 1: N = r, K = d_out
+    L.bp_b2 = take(kblocks(r) * d_in * 8);   // backward 2: N = d_in, K = r
     L.act16 = take(m * (size_t)(d_in > d_out ? d_in : d_out) * 2);
     L.a32 = take(m * r * 4);
     L.act16b = take(m * r * 2);
@@ -169,8 +172,9 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     L.sig = take(m * 4);
     L.sig_inv = take(m * 4);
     L.rows_dh = stage_dy_blocks(M, d_out);
-    L.rows_dl = (int)(m_tiles * 4);
-    L.rows_dg = (int)(m_tiles * 4);
+    // four partial rows per 128-token tile; tiles counted in 256-token pairs
+    L.rows_dl = (int)(((m + 255) / 256) * 8);
+    L.rows_dg = L.rows_dl;
     L.part_dh = take((size_t)L.rows_dh * d_out * 4);
     L.part_dl = take((size_t)L.rows_dl * r * 4);
     L.part_dg = take((size_t)L.rows_dg * d_in * 4);
@@ -191,6 +195,28 @@ int pick_bn(int M, int N, int sms) {
 int gemm_grid(int M, int N, int bn, int sms) {
     const long long tiles = (long long)((M + 127) / 128) * (N / bn);
     return (int)(tiles < sms ? tiles : sms);
+}
+
+// GEMM launch plan: CTA pairs (tcgen05 cta_group::2, 256-token x 256-feature
+// tiles) for the narrow-output products when there are enough such tiles to
+// give every pair of SMs one; otherwise one CTA per 128-token tile with
+// pick_bn's width. (Measured on GB300: pairs gain a few percent on the long-K,
+// narrow-output products and lose on the wide-output ones, whose TMA
+// epilogues leave the pair too few pipeline stages.)
+struct GemmPlan {
+    int bn;          // > 0 single-CTA tile width; -256 CTA pairs
+    int grid;        // CTAs
+    int part_rows;   // partial-sum rows the epilogue writes (4 per 128-token tile)
+};
+
+GemmPlan plan_gemm(int M, int N, int sms, bool wide_output) {
+    const long long pair_tiles = (long long)((M + 255) / 256) * (N / 256);
+    if (!wide_output && N % 256 == 0 && M > 128 && pair_tiles >= sms / 2) {
+        const long long pairs = pair_tiles < sms / 2 ? pair_tiles : sms / 2;
+        return GemmPlan{-256, (int)(2 * pairs), (int)(((M + 255) / 256) * 8)};
+    }
+    const int bn = pick_bn(M, N, sms);
+    return GemmPlan{bn, gemm_grid(M, N, bn, sms), (int)(((M + 127) / 128) * 4)};
 }
 
 // ------------------------------------------------------------ tape ---------
@@ -298,9 +324,8 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f1.out16 = al16;
     f1.colv = l;
     f1.status = status;
-    const int bn1 = pick_bn(M, r, sms);
-    if (launch_gemm(kEpiFwd1, bn1, tm_x, em_none, f1, gemm_grid(M, r, bn1, sms), s) != cudaSuccess)
-        return BLR_ERR_CUDA;
+    const GemmPlan p1 = plan_gemm(M, r, sms, false);
+    if (launch_gemm(kEpiFwd1, p1.bn, tm_x, em_none, f1, p1.grid, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs f2{};
     f2.M = M;
@@ -312,9 +337,8 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f2.colv = h;
     f2.accumulate = accumulate_y;
     f2.status = status;
-    const int bn2 = pick_bn(M, d_out, sms);
-    if (launch_gemm(kEpiFwd2, bn2, tm_a, em_f2, f2, gemm_grid(M, d_out, bn2, sms), s) != cudaSuccess)
-        return BLR_ERR_CUDA;
+    const GemmPlan p2 = plan_gemm(M, d_out, sms, true);
+    if (launch_gemm(kEpiFwd2, p2.bn, tm_a, em_f2, f2, p2.grid, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     std::lock_guard<std::mutex> lk(g_tape_mu);
     g_tapes[ws] = Tape{M, d_in, d_out, r};
@@ -400,9 +424,8 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b1.row_scale = sig;
     b1.part = part_dl;
     b1.status = status;
-    const int bn1 = pick_bn(M, r, sms);
-    if (launch_gemm(kEpiBwd1, bn1, tm_dy, em_none, b1, gemm_grid(M, r, bn1, sms), s) != cudaSuccess)
-        return BLR_ERR_CUDA;
+    const GemmPlan p1 = plan_gemm(M, r, sms, false);
+    if (launch_gemm(kEpiBwd1, p1.bn, tm_dy, em_none, b1, p1.grid, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs b2{};
     b2.M = M;
@@ -416,13 +439,12 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b2.part = part_dg;
     b2.accumulate = accumulate_dx;
     b2.status = status;
-    const int bn2 = pick_bn(M, d_in, sms);
-    if (launch_gemm(kEpiBwd2, bn2, tm_db, em_b2, b2, gemm_grid(M, d_in, bn2, sms), s) != cudaSuccess)
-        return BLR_ERR_CUDA;
+    const GemmPlan p2 = plan_gemm(M, d_in, sms, true);
+    if (launch_gemm(kEpiBwd2, p2.bn, tm_db, em_b2, b2, p2.grid, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     ReduceSeg sh{part_dh, dh, rows_dh, d_out};
-    ReduceSeg sl{part_dl, dl, L.rows_dl, r};
-    ReduceSeg sg{part_dg, dg, L.rows_dg, d_in};
+    ReduceSeg sl{part_dl, dl, p1.part_rows, r};
+    ReduceSeg sg{part_dg, dg, p2.part_rows, d_in};
     if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
     return BLR_OK;
 }

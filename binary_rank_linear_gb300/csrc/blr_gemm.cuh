@@ -16,9 +16,15 @@
 // filled by TMA, so that load latency is hidden) and a shallow "B ring" of
 // expanded sign tiles (filled by the expanders from the A ring's words).
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-5 sign expanders, warps 6-9 epilogue (warp w reads TMEM
+// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-9 sign expanders, warps 10-13 epilogue (warp w reads TMEM
 // lanes 32*(w%4) .. +31, i.e. tokens 32*(w%4) .. +31 of the tile).
+//
+// Per k-step the MMA issuer waits on one barrier (full_b: the expanders
+// finished the sign tile; they had waited for the stage's activation tile
+// and bitmap words on full_a, so full_b implies full_a) and commits once
+// (empty_a). An expander reuses sign slot i % NB once the MMAs of k-step
+// i - NB completed, which is the completion of empty_a for that k-step.
 //
 // Epilogues: the two products with a wide output (c and dx', N = d_out or
 // d_in, K = r) stage each 32 x 32 output chunk in per-warp shared memory and
@@ -39,36 +45,47 @@ namespace blr {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kGemmThreads = 320;
+constexpr int kGemmThreads = 448;
 constexpr int kWarpTma = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpExp0 = 2;
-constexpr int kNumExpWarps = 4;
-constexpr int kWarpEpi0 = 6;
+constexpr int kNumExpWarps = 8;
+constexpr int kWarpEpi0 = 10;
 constexpr int kNumEpiWarps = 4;
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 struct GemmShape {
     static constexpr bool kTmaEpi = (EPI == kEpiFwd2 || EPI == kEpiBwd2);
-    static constexpr int kABytes = kBM * kBK * 2;  // activation tile
-    static constexpr int kBitsBytes = BN * 8;      // bitmap words of one k-step
-    static constexpr int kBBytes = BN * kBK * 2;   // expanded sign tile
+    static constexpr int kKB = PAIR ? 2 : 1;            // 64-wide K blocks per k-step
+    static constexpr int kStepK = kKB * kBK;            // K per k-step
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;   // sign-tile rows this CTA expands
+    static constexpr int kABlock = kBM * kBK * 2;       // one 128 x 64 activation box
+    static constexpr int kABytes = kKB * kABlock;       // activation tile of a k-step
+    static constexpr int kBitsBlock = kBRows * 8;       // bitmap words of one 64-wide block
+    static constexpr int kBitsBytes = kKB * kBitsBlock;
+    static constexpr int kBBlock = kBRows * kBK * 2;    // one 64-wide block of the sign tile
+    static constexpr int kBBytes = kKB * kBBlock;       // expanded sign tile (this CTA's rows)
     static constexpr int kEpiF32 = 32 * 32 * 4;
     static constexpr int kEpiF16 = (EPI == kEpiFwd2) ? 32 * 32 * 2 : 0;
     static constexpr int kEpiBuf = kEpiF32 + kEpiF16;
     static constexpr int kEpiBytes = kTmaEpi ? kNumEpiWarps * 2 * kEpiBuf : 0;
-    static constexpr int kBudget = 205 * 1024 - kEpiBytes;
-    static constexpr int kNB = kTmaEpi ? 2 : (BN >= 128 ? 3 : 4);
+    static constexpr int kBudget = (PAIR ? 220 : 205) * 1024 - kEpiBytes;
+    static constexpr int kNB = kTmaEpi ? 2 : (PAIR ? 3 : (kBRows >= 128 ? 3 : 4));
     static constexpr int kNARaw = (kBudget - kNB * kBBytes) / (kABytes + kBitsBytes);
     static constexpr int kNA = kNARaw > 8 ? 8 : kNARaw;
     static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
     static constexpr int kBitsRegion = ((kNA * kBitsBytes + 1023) / 1024) * 1024;
-    static constexpr int kNumBars = 2 * kNA + 2 * kNB + 4 + 1 + kNumEpiWarps * 2;
+    static constexpr int kNumBars = 2 * kNA + kNB + 4 + 1 + kNumEpiWarps * 2;
     static constexpr int kSmemBytes =
         1024 + kNA * kABytes + kNB * kBBytes + kEpiBytes + kBitsRegion + kNumBars * 8 + 16;
     static_assert(kNA >= 2, "activation ring too shallow");
+    // an expander frees sign slot i % NB by waiting on the activation slot of
+    // k-step i - NB; that wait is unambiguous only if the activation ring is at
+    // least as deep as the sign ring
+    static_assert(kNA >= kNB, "activation ring must be at least as deep as the sign ring");
     static_assert(kBitsBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(!PAIR || BN >= 64, "a pair splits the sign tile in two halves of >= 32 rows");
 };
 
 // Sum of p[j] over the 32 lanes of the warp, returned in lane j (a
@@ -215,11 +232,23 @@ __device__ __forceinline__ void epilogue_chunk_smem(const GemmArgs &a, float (&f
     }
 }
 
-template <int BN, int EPI>
+// PAIR = false: one CTA per 128-token tile (tcgen05 cta_group::1).
+// PAIR = true: a cluster of two CTAs per 256-token tile (cta_group::2). Each
+// CTA loads its own 128 activation rows and expands half of the sign tile;
+// the leader (rank 0) issues the M=256 MMAs, which read both CTAs' shared
+// memory and write each CTA's TMEM. Within each CTA the producer, expanders
+// and epilogue signal local barriers only; the peer's MMA warp waits until a
+// k-step's sign half is in place (which follows its activation tile) and then
+// makes the one cluster-scope arrival on the leader's full_b (a cluster-scope
+// release costs a memory barrier, so it is paid once per k-step, not per
+// warp). The peer's epilogue warps release their TMEM half to the leader
+// remotely, once per tile. The leader's commits are multicast to both CTAs'
+// barriers.
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ EpiMaps emaps,
                     const GemmArgs args) {
-    using S = GemmShape<BN, EPI>;
+    using S = GemmShape<BN, EPI, PAIR>;
     constexpr int NA = S::kNA, NB = S::kNB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -231,8 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t *full_a = bars;
     uint64_t *empty_a = full_a + NA;
     uint64_t *full_b = empty_a + NA;
-    uint64_t *empty_b = full_b + NB;
-    uint64_t *tmem_full = empty_b + NB;
+    uint64_t *tmem_full = full_b + NB;
     uint64_t *tmem_empty = tmem_full + 2;
     uint64_t *drain_bar = tmem_full + 4;
     uint64_t *eload = drain_bar + 1;  // [4 warps][2]
@@ -242,23 +270,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     const int M = args.M, N = args.N;
-    const int m_tiles = (M + kBM - 1) / kBM;
+    constexpr int kUnitRows = PAIR ? 2 * kBM : kBM;  // token rows per tile
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // tile worker (CTA or pair)
+    const int num_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int m_tiles = (M + kUnitRows - 1) / kUnitRows;
     const int n_tiles = N / BN;
     const int num_tiles = m_tiles * n_tiles;
-    const int num_kb = (args.K + kBK - 1) / kBK;
+    const int num_kb = (args.K + S::kStepK - 1) / S::kStepK;  // k-steps per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NA; ++s) {
             mbar_init(&full_a[s], 1);
             mbar_init(&empty_a[s], 1);
         }
-        for (int s = 0; s < NB; ++s) {
-            mbar_init(&full_b[s], kNumExpWarps);
-            mbar_init(&empty_b[s], 1);
-        }
+        for (int s = 0; s < NB; ++s) mbar_init(&full_b[s], (PAIR && leader) ? kNumExpWarps + 1 : kNumExpWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tmem_full[i], 1);
-            mbar_init(&tmem_empty[i], kNumEpiWarps);
+            mbar_init(&tmem_empty[i], PAIR ? 2 * kNumEpiWarps : kNumEpiWarps);
         }
         mbar_init(drain_bar, 1);
         for (int i = 0; i < kNumEpiWarps * 2; ++i) mbar_init(&eload[i], 1);
@@ -273,14 +303,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if constexpr (EPI == kEpiFwd2) tma_prefetch_desc(&emaps.out16);
         }
     }
-    if (warp == kWarpMma) {
-        tmem_alloc(tmem_slot, S::kTmemCols);
-        tmem_relinquish();
+    if constexpr (PAIR) {
+        cluster_sync();  // both CTAs' barriers exist before any remote arrival
+        if (warp == kWarpMma) {
+            tmem_alloc_pair(tmem_slot, S::kTmemCols);
+            tmem_relinquish_pair();
+        }
+    } else {
+        if (warp == kWarpMma) {
+            tmem_alloc(tmem_slot, S::kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the leader's copy of a barrier, as a cluster address (PAIR only)
+    auto leader_bar = [&](uint64_t *bar) -> uint32_t { return mapa_shared(smem_u32(bar), 0); };
     // setup above overlaps the previous kernel; global memory only after this
     pdl_wait();
     pdl_launch_dependents();
@@ -290,9 +330,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int sa = 0;
             uint32_t pa = 0, issued = 0, parity = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile / n_tiles) * kBM;
-                const int n0 = (tile % n_tiles) * BN;
+            for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
+                const int m0 = (tile / n_tiles) * kUnitRows + (int)rank * kBM;
+                const int nb0 = (tile % n_tiles) * BN + (int)rank * S::kBRows;  // this CTA's sign rows
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&empty_a[sa], pa ^ 1u, abort_flag)) {
                         fail_status(args, abort_flag, kStTimeoutTma);
@@ -300,9 +340,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&full_a[sa], S::kABytes + S::kBitsBytes);
-                    tma_load_2d(sA + sa * S::kABytes, &tmap_a, &full_a[sa], kb * kBK, m0);
-                    bulk_load(sBits + sa * (S::kBitsBytes / 4), args.bsign + ((size_t)kb * N + n0) * 2,
-                              S::kBitsBytes, &full_a[sa]);
+#pragma unroll
+                    for (int kk = 0; kk < S::kKB; ++kk) {
+                        const int blk = kb * S::kKB + kk;  // 64-wide K block (the bitmap layout pads to kKB)
+                        tma_load_2d(sA + sa * S::kABytes + kk * S::kABlock, &tmap_a, &full_a[sa], blk * kBK, m0);
+                        bulk_load(sBits + sa * (S::kBitsBytes / 4) + kk * (S::kBitsBlock / 4),
+                                  args.bsign + ((size_t)blk * N + nb0) * 2, S::kBitsBlock, &full_a[sa]);
+                    }
                     issued |= 1u << sa;
                     parity = (parity & ~(1u << sa)) | (pa << sa);
                     if (++sa == NA) {
@@ -319,38 +363,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_f16_f32(kBM, BN);
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = umma_idesc_f16_f32(PAIR ? 2 * kBM : kBM, BN);
             int sa = 0, sb = 0;
             uint32_t pa = 0, pb = 0;
             bool ok = true;
             int local = 0;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+            for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++local) {
                 const int acc = local & 1;
                 const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-                if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag)) {
+                const bool got = PAIR ? mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1u, abort_flag)
+                                      : mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag);
+                if (!got) {
                     fail_status(args, abort_flag, kStTimeoutMma);
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&full_a[sa], pa, abort_flag) || !mbar_wait(&full_b[sb], pb, abort_flag)) {
+                    const bool ready = PAIR ? mbar_wait_cluster(&full_b[sb], pb, abort_flag)
+                                            : mbar_wait(&full_b[sb], pb, abort_flag);
+                    if (!ready) {
                         fail_status(args, abort_flag, kStTimeoutMma);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = umma_sdesc_sw128(smem_u32(sA + sa * S::kABytes));
-                    const uint64_t bdesc = umma_sdesc_sw128(smem_u32(sB + sb * S::kBBytes));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // advance 16 f16 (32 bytes) along K inside the swizzled rows
-                        umma_f16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
-                                 (kb > 0 || k > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < S::kKB; ++kk) {
+                        const uint64_t adesc = umma_sdesc_sw128(smem_u32(sA + sa * S::kABytes + kk * S::kABlock));
+                        const uint64_t bdesc = umma_sdesc_sw128(smem_u32(sB + sb * S::kBBytes + kk * S::kBBlock));
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            // advance 16 f16 (32 bytes) along K inside the swizzled rows
+                            const uint32_t acc_in = (kb > 0 || kk > 0 || k > 0) ? 1u : 0u;
+                            if constexpr (PAIR)
+                                umma_f16_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
+                                              acc_in);
+                            else
+                                umma_f16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc, acc_in);
+                        }
                     }
-                    umma_commit(&empty_a[sa]);
-                    umma_commit(&empty_b[sb]);
+                    if constexpr (PAIR)
+                        umma_commit_pair_multicast(&empty_a[sa], 3);
+                    else
+                        umma_commit(&empty_a[sa]);
                     if (++sa == NA) {
                         sa = 0;
                         pa ^= 1u;
@@ -361,25 +418,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit(&tmem_full[acc]);
+                if constexpr (PAIR)
+                    umma_commit_pair_multicast(&tmem_full[acc], 3);
+                else
+                    umma_commit(&tmem_full[acc]);
             }
             // drain: no MMA may still be running when TMEM is freed
-            umma_commit(drain_bar);
+            if constexpr (PAIR)
+                umma_commit_pair_multicast(drain_bar, 1);
+            else
+                umma_commit(drain_bar);
             if (!mbar_wait(drain_bar, 0, abort_flag, false)) atomicOr(args.status, kStTimeoutDrain);
+        } else if (PAIR && lane == 0) {
+            // the peer's MMA warp: once a k-step's sign half is in this CTA's
+            // shared memory (after its activation tile), one arrival on the leader
+            int sb = 0;
+            uint32_t pb = 0;
+            bool ok = true;
+            for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&full_b[sb], pb, abort_flag)) {
+                        fail_status(args, abort_flag, kStTimeoutMma);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_remote(leader_bar(&full_b[sb]));
+                    if (++sb == NB) {
+                        sb = 0;
+                        pb ^= 1u;
+                    }
+                }
+            }
         }
         __syncwarp();
     } else if (warp < kWarpEpi0) {
         // ---- sign expanders: bitmap words -> +-1 f16 operand tile --------
-        constexpr int kUnits = BN * 2;  // (operand row, word) pairs per k-step
-        constexpr int kUpt = (kUnits + 127) / 128;
+        constexpr int kUnits = S::kBRows * 2 * S::kKB;  // (operand row, word) pairs per k-step
+        constexpr int kExpThreads = kNumExpWarps * 32;
+        constexpr int kUpt = (kUnits + kExpThreads - 1) / kExpThreads;
         const int e = threadIdx.x - kWarpExp0 * 32;
         int sa = 0, sb = 0;
-        uint32_t pa = 0, pb = 0;
+        uint32_t pa = 0;
+        int lag = -NB;              // k-step whose MMAs must have freed this sign slot
+        int ls = 0;                 // its activation slot
+        uint32_t lp = 0;            // and that slot's phase parity
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
             for (int kb = 0; kb < num_kb; ++kb) {
-                const bool got =
-                    mbar_wait(&full_a[sa], pa, abort_flag) && mbar_wait(&empty_b[sb], pb ^ 1u, abort_flag);
+                bool got = mbar_wait(&full_a[sa], pa, abort_flag);
+                if (got && lag >= 0) got = mbar_wait(&empty_a[ls], lp, abort_flag);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     if (lane == 0) fail_status(args, abort_flag, kStTimeoutExpand);
                     ok = false;
@@ -389,18 +476,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 uint8_t *tile_b = sB + sb * S::kBBytes;
 #pragma unroll
                 for (int i = 0; i < kUpt; ++i) {
-                    const int u = e + 128 * i;
+                    const int u = e + kExpThreads * i;
                     if (u < kUnits) {
-                        const int row = u >> 1;
-                        const int w = u & 1;
+                        const int kk = u / (S::kBRows * 2);  // 64-wide block
+                        const int v = u - kk * (S::kBRows * 2);
+                        const int row = v >> 1;
+                        const int w = v & 1;
                         const uint32_t p = bits[u];
-                        uint8_t *rowp = tile_b + row * 128;
+                        uint8_t *rowp = tile_b + kk * S::kBBlock + row * 128;
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint4 v = make_uint4(sign_pair(p, 4 * j), sign_pair(p, 4 * j + 1),
-                                                       sign_pair(p, 4 * j + 2), sign_pair(p, 4 * j + 3));
+                            const uint4 q4 = make_uint4(sign_pair(p, 4 * j), sign_pair(p, 4 * j + 1),
+                                                        sign_pair(p, 4 * j + 2), sign_pair(p, 4 * j + 3));
                             const int chunk = (4 * w + j) ^ (row & 7);
-                            *reinterpret_cast<uint4 *>(rowp + chunk * 16) = v;
+                            *reinterpret_cast<uint4 *>(rowp + chunk * 16) = q4;
                         }
                     }
                 }
@@ -411,9 +500,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     sa = 0;
                     pa ^= 1u;
                 }
-                if (++sb == NB) {
-                    sb = 0;
-                    pb ^= 1u;
+                if (++sb == NB) sb = 0;
+                if (++lag > 0) {
+                    if (++ls == NA) {
+                        ls = 0;
+                        lp ^= 1u;
+                    }
                 }
             }
         }
@@ -429,10 +521,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int gch = 0;                       // running chunk count: buffer = gch & 1
         int local = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++local) {
             const int acc = local & 1;
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
-            const int mt = tile / n_tiles;
+            const int mt = (tile / n_tiles) * (PAIR ? 2 : 1) + (int)rank;  // 128-row tile index
             const int n0 = (tile % n_tiles) * BN;
             const int row0 = mt * kBM + q * 32;
             if constexpr (S::kTmaEpi) {
@@ -473,7 +565,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // accumulator fully read: hand it back to the MMA issuer
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_remote(leader_bar(&tmem_empty[acc]));
+                        else
+                            mbar_arrive(&tmem_empty[acc]);
+                    }
                 }
                 float f[32];
 #pragma unroll
@@ -529,33 +626,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == kWarpMma) tmem_dealloc(tmem_base, S::kTmemCols);
+    if constexpr (PAIR) {
+        // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it
+        cluster_sync();
+        tc_fence_after();
+        if (warp == kWarpMma) tmem_dealloc_pair(tmem_base, S::kTmemCols);
+    } else {
+        __syncthreads();
+        tc_fence_after();
+        if (warp == kWarpMma) tmem_dealloc(tmem_base, S::kTmemCols);
+    }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 cudaError_t launch_gemm_t(const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args, int grid,
                           cudaStream_t s) {
-    using S = GemmShape<BN, EPI>;
+    using S = GemmShape<BN, EPI, PAIR>;
     static bool attr_set = false;  // set once, outside any later stream capture
     if (!attr_set) {
-        cudaError_t e = prepare_kernel(blr_gemm_kernel<BN, EPI>, S::kSmemBytes);
+        cudaError_t e = prepare_kernel(blr_gemm_kernel<BN, EPI, PAIR>, S::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_k(blr_gemm_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), S::kSmemBytes, s, tmap_a, emaps,
-                    args);
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kGemmThreads);
+        cfg.dynamicSmemBytes = S::kSmemBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, blr_gemm_kernel<BN, EPI, PAIR>, tmap_a, emaps, args);
+    } else {
+        return launch_k(blr_gemm_kernel<BN, EPI, PAIR>, dim3(grid), dim3(kGemmThreads), S::kSmemBytes, s, tmap_a,
+                        emaps, args);
+    }
 }
 
+// bn > 0: one CTA per 128-token tile of width bn; bn < 0: CTA pairs, tiles of
+// 256 tokens x |bn| features (|bn| = 128 or 256). `grid` counts CTAs (even for
+// pairs).
 template <int EPI>
 cudaError_t launch_gemm_epi(int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args,
                             int grid, cudaStream_t s) {
     switch (bn) {
-        case 32: return launch_gemm_t<32, EPI>(tmap_a, emaps, args, grid, s);
-        case 64: return launch_gemm_t<64, EPI>(tmap_a, emaps, args, grid, s);
-        case 128: return launch_gemm_t<128, EPI>(tmap_a, emaps, args, grid, s);
-        case 256: return launch_gemm_t<256, EPI>(tmap_a, emaps, args, grid, s);
+        case 32: return launch_gemm_t<32, EPI, false>(tmap_a, emaps, args, grid, s);
+        case 64: return launch_gemm_t<64, EPI, false>(tmap_a, emaps, args, grid, s);
+        case 128: return launch_gemm_t<128, EPI, false>(tmap_a, emaps, args, grid, s);
+        case 256: return launch_gemm_t<256, EPI, false>(tmap_a, emaps, args, grid, s);
+        case -128: return launch_gemm_t<128, EPI, true>(tmap_a, emaps, args, grid, s);
+        case -256: return launch_gemm_t<256, EPI, true>(tmap_a, emaps, args, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -131,6 +131,9 @@ SHAPES = [
     ("ragged", 1, 128, 128, 64),
     ("ragged", 127, 256, 512, 128),
     ("ragged", 129, 192, 96, 64),
+    # enough 256 x 256 tiles for the CTA-pair GEMMs of the narrow outputs, ragged
+    # M, and a reduction length (d_out = 1568) that ends in a partial k-step
+    ("attn", 4600, 1024, 1568, 1280),
 ]
 
 
