@@ -12,10 +12,10 @@
 #include "blr_kernels.h"
 
 namespace blr {
-cudaError_t launch_gemm_fwd(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps,
-                            const GemmArgs &args, int grid, cudaStream_t s);
-cudaError_t launch_gemm_bwd(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps,
-                            const GemmArgs &args, int grid, cudaStream_t s);
+cudaError_t launch_gemm_fwd(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args,
+                            cudaStream_t s);
+cudaError_t launch_gemm_bwd(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args,
+                            cudaStream_t s);
 
 // ------------------------------------------------------------ tracing ------
 namespace {
@@ -43,12 +43,11 @@ void trace_after(cudaStream_t stream) {
     ++t.n;
 }
 
-cudaError_t launch_gemm(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args,
-                        int grid, cudaStream_t s) {
+cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s) {
     static const char *names[4] = {"gemm_fwd1", "gemm_fwd2", "gemm_bwd1", "gemm_bwd2"};
     trace_before(names[epi & 3], s);
-    cudaError_t e = (epi == kEpiFwd1 || epi == kEpiFwd2) ? launch_gemm_fwd(epi, bn, tmap_a, emaps, args, grid, s)
-                                                          : launch_gemm_bwd(epi, bn, tmap_a, emaps, args, grid, s);
+    cudaError_t e = (epi == kEpiFwd1 || epi == kEpiFwd2) ? launch_gemm_fwd(epi, plan, maps, args, s)
+                                                          : launch_gemm_bwd(epi, plan, maps, args, s);
     trace_after(s);
     return e;
 }
@@ -102,22 +101,23 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// f16 activation operand [rows][K], box 64 (K) x 128 (rows), 128-byte swizzle;
+// f16 activation operand [rows][K], box 64 (K) x box_rows, 128-byte swizzle;
 // rows past `rows` and columns past K read as zero.
-bool make_tmap_act16(CUtensorMap *m, const void *base, int rows, int K) {
+bool make_tmap_act16(CUtensorMap *m, const void *base, int rows, int K, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D [rows][cols] map with a 32 x 32 box (f32 with the 128-byte swizzle, f16
-// with the 64-byte swizzle): the epilogue chunks of the wide products.
+// [rows][cols] f32 or f16 with a 32 x 32 box, no swizzle: the epilogue's
+// chunks (32 tokens x 32 features); loads read zeros out of range and stores
+// are clipped to it.
 bool make_tmap_chunk(CUtensorMap *m, const void *base, int rows, int cols, bool f16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -127,9 +127,8 @@ bool make_tmap_chunk(CUtensorMap *m, const void *base, int rows, int cols, bool 
     cuuint32_t box[2] = {32, 32};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base),
-              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              f16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------ layout --------
@@ -156,14 +155,14 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     };
     const size_t m = (size_t)M;
     L.header = take(256);
-    // re-laid bitmaps, [K blocks of 64, padded to an even count][N][2] u32: the
-    // CTA-pair GEMMs consume two blocks per k-step (the pad block is never
-    // multiplied by anything but zero activations)
+    // re-laid bitmaps, [K blocks of 64, two per 128-deep k-step][sign_rows(N)][2]
+    // u32 (pad blocks and rows are never multiplied by anything but zero
+    // activations, or never stored)
     auto kblocks = [](int K) { return (size_t)((K + 127) / 128) * 2; };
-    L.bp_f1 = take(kblocks(d_in) * r * 8);   // forward 1: N = r, K = d_in
-    L.bp_f2 = take(kblocks(r) * d_out * 8);  // forward 2: N = d_out, K = r
-    L.bp_b1 = take(kblocks(d_out) * r * 8);  // backward 1: N = r, K = d_out
-    L.bp_b2 = take(kblocks(r) * d_in * 8);   // backward 2: N = d_in, K = r
+    L.bp_f1 = take(kblocks(d_in) * sign_rows(r) * 8);   // forward 1: N = r, K = d_in
+    L.bp_f2 = take(kblocks(r) * sign_rows(d_out) * 8);  // forward 2: N = d_out, K = r
+    L.bp_b1 = take(kblocks(d_out) * sign_rows(r) * 8);  // backward 1: N = r, K = d_out
+    L.bp_b2 = take(kblocks(r) * sign_rows(d_in) * 8);   // backward 2: N = d_in, K = r
     L.act16 = take(m * (size_t)(d_in > d_out ? d_in : d_out) * 2);
     L.a32 = take(m * r * 4);
     L.act16b = take(m * r * 2);
@@ -172,51 +171,14 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     L.sig = take(m * 4);
     L.sig_inv = take(m * 4);
     L.rows_dh = stage_dy_blocks(M, d_out);
-    // four partial rows per 128-token tile; tiles counted in 256-token pairs
-    L.rows_dl = (int)(((m + 255) / 256) * 8);
+    // one partial row per 128-token tile
+    L.rows_dl = (int)((m + 127) / 128);
     L.rows_dg = L.rows_dl;
     L.part_dh = take((size_t)L.rows_dh * d_out * 4);
     L.part_dl = take((size_t)L.rows_dl * r * 4);
     L.part_dg = take((size_t)L.rows_dg * d_in * 4);
     L.total = off;
     return L;
-}
-
-// Feature tile width: the widest of 256/128/64/32 that divides N, narrowed
-// while the grid would leave SMs idle.
-int pick_bn(int M, int N, int sms) {
-    const long long m_tiles = (M + 127) / 128;
-    int bn = 256;
-    while (bn > 32 && N % bn != 0) bn /= 2;
-    while (bn > 32 && m_tiles * (N / bn) < sms && N % (bn / 2) == 0) bn /= 2;
-    return bn;
-}
-
-int gemm_grid(int M, int N, int bn, int sms) {
-    const long long tiles = (long long)((M + 127) / 128) * (N / bn);
-    return (int)(tiles < sms ? tiles : sms);
-}
-
-// GEMM launch plan: CTA pairs (tcgen05 cta_group::2, 256-token x 256-feature
-// tiles) for the narrow-output products when there are enough such tiles to
-// give every pair of SMs one; otherwise one CTA per 128-token tile with
-// pick_bn's width. (Measured on GB300: pairs gain a few percent on the long-K,
-// narrow-output products and lose on the wide-output ones, whose TMA
-// epilogues leave the pair too few pipeline stages.)
-struct GemmPlan {
-    int bn;          // > 0 single-CTA tile width; -256 CTA pairs
-    int grid;        // CTAs
-    int part_rows;   // partial-sum rows the epilogue writes (4 per 128-token tile)
-};
-
-GemmPlan plan_gemm(int M, int N, int sms, bool wide_output) {
-    const long long pair_tiles = (long long)((M + 255) / 256) * (N / 256);
-    if (!wide_output && N % 256 == 0 && M > 128 && pair_tiles >= sms / 2) {
-        const long long pairs = pair_tiles < sms / 2 ? pair_tiles : sms / 2;
-        return GemmPlan{-256, (int)(2 * pairs), (int)(((M + 255) / 256) * 8)};
-    }
-    const int bn = pick_bn(M, N, sms);
-    return GemmPlan{bn, gemm_grid(M, N, bn, sms), (int)(((M + 127) / 128) * 4)};
 }
 
 // ------------------------------------------------------------ tape ---------
@@ -239,6 +201,36 @@ bool pow2_positive(float v) {
     return std::frexp(v, &e) == 0.5f;
 }
 }  // namespace
+}  // namespace blr
+
+namespace blr {
+
+// Tiles of 128 features (256 for a CTA pair) x BT tokens. CTA pairs whenever
+// there are at least as many pair tiles as pairs of SMs, with the token tile
+// (160 or 192: MMAs of N >= 160 run at full rate) that needs the fewest
+// token-rounds of the persistent grid; otherwise single CTAs with 128-token
+// tiles, for more tiles in flight on small problems.
+GemmPlan plan_gemm(int M, int N, int sms) {
+    const int pairs = sms / 2;
+    const long long fp = (N + 255) / 256;
+    GemmPlan best{false, 0, 0, 0};
+    long long best_cost = 0;
+    for (int bt : {192, 160}) {
+        const long long t_tiles = (M + bt - 1) / bt;
+        const long long tiles = t_tiles * fp;
+        if (tiles < pairs) continue;
+        const long long cost = ((tiles + pairs - 1) / pairs) * bt;  // rounds x MMA time per tile
+        if (best.bt == 0 || cost < best_cost) {
+            best = GemmPlan{true, bt, 2 * pairs, (int)t_tiles};
+            best_cost = cost;
+        }
+    }
+    if (best.bt != 0) return best;
+    const long long t_tiles = (M + 127) / 128;
+    const long long tiles = t_tiles * ((N + 127) / 128);
+    return GemmPlan{false, 128, (int)(tiles < sms ? tiles : sms), (int)t_tiles};
+}
+
 }  // namespace blr
 
 using namespace blr;
@@ -298,12 +290,15 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     uint16_t *al16 = reinterpret_cast<uint16_t *>(w + L.act16b);
     uint16_t *c16 = reinterpret_cast<uint16_t *>(w + L.c16);
 
-    CUtensorMap tm_x, tm_a;
-    if (!make_tmap_act16(&tm_x, x16, M, d_in) || !make_tmap_act16(&tm_a, al16, M, r)) return BLR_ERR_CUDA;
-    EpiMaps em_none{}, em_f2{};
-    if (!make_tmap_chunk(&em_f2.out32, y, M, d_out, false) || !make_tmap_chunk(&em_f2.out16, c16, M, d_out, true))
+    const GemmPlan p1 = plan_gemm(M, r, sms);
+    const GemmPlan p2 = plan_gemm(M, d_out, sms);
+    GemmMaps m1{}, m2{};
+    if (!make_tmap_act16(&m1.act, x16, M, d_in, p1.pair ? p1.bt / 2 : p1.bt) ||
+        !make_tmap_chunk(&m1.out32, a32, M, r, false) || !make_tmap_chunk(&m1.out16, al16, M, r, true) ||
+        !make_tmap_act16(&m2.act, al16, M, r, p2.pair ? p2.bt / 2 : p2.bt) ||
+        !make_tmap_chunk(&m2.in32, y, M, d_out, false) || !make_tmap_chunk(&m2.out32, y, M, d_out, false) ||
+        !make_tmap_chunk(&m2.out16, c16, M, d_out, true))
         return BLR_ERR_CUDA;
-    em_f2.in32 = em_f2.out32;
 
     // a new forward starts a new tape: forget the old one first
     {
@@ -311,34 +306,34 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
         g_tapes.erase(ws);
     }
     // S_V [d_in][r/32] has its bits along r: the first product needs them along d_in
-    SignPrep pv{bits_v, bp_f1, r, d_in, 1};
-    SignPrep pu{bits_u, bp_f2, d_out, r, 0};
+    SignPrep pv{bits_v, bp_f1, r, d_in, 1, sign_rows(r)};
+    SignPrep pu{bits_u, bp_f2, d_out, r, 0, sign_rows(d_out)};
     if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, status, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs f1{};
     f1.M = M;
     f1.N = r;
     f1.K = d_in;
+    f1.Ns = sign_rows(r);
     f1.bsign = bp_f1;
     f1.out32 = a32;
     f1.out16 = al16;
     f1.colv = l;
     f1.status = status;
-    const GemmPlan p1 = plan_gemm(M, r, sms, false);
-    if (launch_gemm(kEpiFwd1, p1.bn, tm_x, em_none, f1, p1.grid, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiFwd1, p1, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs f2{};
     f2.M = M;
     f2.N = d_out;
     f2.K = r;
+    f2.Ns = sign_rows(d_out);
     f2.bsign = bp_f2;
     f2.out32 = y;
     f2.out16 = c16;
     f2.colv = h;
     f2.accumulate = accumulate_y;
     f2.status = status;
-    const GemmPlan p2 = plan_gemm(M, d_out, sms, true);
-    if (launch_gemm(kEpiFwd2, p2.bn, tm_a, em_f2, f2, p2.grid, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     std::lock_guard<std::mutex> lk(g_tape_mu);
     g_tapes[ws] = Tape{M, d_in, d_out, r};
@@ -385,15 +380,18 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     float *part_dl = reinterpret_cast<float *>(w + L.part_dl);
     float *part_dg = reinterpret_cast<float *>(w + L.part_dg);
 
-    CUtensorMap tm_dy, tm_db;
-    if (!make_tmap_act16(&tm_dy, dy16, M, d_out) || !make_tmap_act16(&tm_db, db16, M, r)) return BLR_ERR_CUDA;
-    EpiMaps em_none{}, em_b2{};
-    if (!make_tmap_chunk(&em_b2.out32, dx, M, d_in, false) || !make_tmap_chunk(&em_b2.in32, x, M, d_in, false))
+    const GemmPlan p1 = plan_gemm(M, r, sms);
+    const GemmPlan p2 = plan_gemm(M, d_in, sms);
+    GemmMaps m1{}, m2{};
+    if (!make_tmap_act16(&m1.act, dy16, M, d_out, p1.pair ? p1.bt / 2 : p1.bt) ||
+        !make_tmap_chunk(&m1.in32, a32, M, r, false) || !make_tmap_chunk(&m1.out16, db16, M, r, true) ||
+        !make_tmap_act16(&m2.act, db16, M, r, p2.pair ? p2.bt / 2 : p2.bt) ||
+        !make_tmap_chunk(&m2.in32, x, M, d_in, false) || !make_tmap_chunk(&m2.out32, dx, M, d_in, false))
         return BLR_ERR_CUDA;
 
     // S_U [d_out][r/32] has its bits along r: the first product needs them along d_out
-    SignPrep pu{bits_u, bp_b1, r, d_out, 1};
-    SignPrep pv{bits_v, bp_b2, d_in, r, 0};
+    SignPrep pu{bits_u, bp_b1, r, d_out, 1, sign_rows(r)};
+    SignPrep pv{bits_v, bp_b2, d_in, r, 0, sign_rows(d_in)};
     StageDyArgs sa{};
     sa.dy = dy;
     sa.h = h;
@@ -416,31 +414,29 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b1.M = M;
     b1.N = r;
     b1.K = d_out;
+    b1.Ns = sign_rows(r);
     b1.bsign = bp_b1;
     b1.out16 = db16;
     b1.colv = l;
-    b1.aux = a32;
     b1.row_inv = s_inv;
     b1.row_scale = sig;
     b1.part = part_dl;
     b1.status = status;
-    const GemmPlan p1 = plan_gemm(M, r, sms, false);
-    if (launch_gemm(kEpiBwd1, p1.bn, tm_dy, em_none, b1, p1.grid, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs b2{};
     b2.M = M;
     b2.N = d_in;
     b2.K = r;
+    b2.Ns = sign_rows(d_in);
     b2.bsign = bp_b2;
     b2.out32 = dx;
     b2.colv = g;
-    b2.aux = x;
     b2.row_inv = sig_inv;
     b2.part = part_dg;
     b2.accumulate = accumulate_dx;
     b2.status = status;
-    const GemmPlan p2 = plan_gemm(M, d_in, sms, true);
-    if (launch_gemm(kEpiBwd2, p2.bn, tm_db, em_b2, b2, p2.grid, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     ReduceSeg sh{part_dh, dh, rows_dh, d_out};
     ReduceSeg sl{part_dl, dl, p1.part_rows, r};

@@ -51,37 +51,42 @@ __global__ void unpack_signs_kernel(const uint32_t *__restrict__ bits, uint16_t 
 }
 
 // ============================================ bitmap re-layout (prep) ======
-// Destination order [ks][n][2] u32: word (n, 2ks + w) covers reduction
-// indices 64ks + 32w .. +31 of operand row n, pair-ready.
-__device__ __forceinline__ int prep_blocks(const SignPrep &p, int threads) {
+// Destination order [kb][n][2] u32 (kb < 2 ceil(K/128), n < Ns): word
+// (n, 2kb + w) covers reduction indices 64kb + 32w .. +31 of operand row n,
+// pair-ready. Rows past N and words past K are written from an all-zero word.
+__host__ __device__ __forceinline__ int prep_kwords(int K) { return 4 * ((K + 127) / 128); }
+
+__host__ __device__ __forceinline__ int prep_blocks(const SignPrep &p, int threads) {
     if (p.kind == 0) {
-        const long long units = (long long)p.N * 2 * ((p.K + 63) / 64);
+        const long long units = (long long)p.Ns * prep_kwords(p.K);
         return (int)((units + threads - 1) / threads);
     }
-    const long long warps = (long long)(p.K / 32) * (p.N / 32);
+    const long long warps = (long long)prep_kwords(p.K) * (p.Ns / 32);
     return (int)((warps + threads / 32 - 1) / (threads / 32));
 }
 
 __device__ void prep_run(const SignPrep &p, int block, int threads) {
+    const int kw_total = prep_kwords(p.K);
     if (p.kind == 0) {
         // direct: src [N][K/32]
         const int words = p.K / 32;
-        const int kw_total = 2 * ((p.K + 63) / 64);
         const long long u = (long long)block * threads + threadIdx.x;
-        if (u >= (long long)p.N * kw_total) return;
-        const int n = (int)(u % p.N);
-        const int kw = (int)(u / p.N);
-        const uint32_t w = kw < words ? p.src[(long long)n * words + kw] : 0u;
-        p.dst[((long long)(kw >> 1) * p.N + n) * 2 + (kw & 1)] = sign_word_pair_ready(w);
+        if (u >= (long long)p.Ns * kw_total) return;
+        const int n = (int)(u % p.Ns);
+        const int kw = (int)(u / p.Ns);
+        const uint32_t w = (kw < words && n < p.N) ? p.src[(long long)n * words + kw] : 0u;
+        p.dst[((long long)(kw >> 1) * p.Ns + n) * 2 + (kw & 1)] = sign_word_pair_ready(w);
     } else {
         // transpose: src [K][N/32]; one warp per 32 x 32 bit block.
         const int nwords = p.N / 32;
+        const int nwords_s = p.Ns / 32;
         const long long wi = (long long)block * (threads / 32) + threadIdx.x / 32;
-        if (wi >= (long long)(p.K / 32) * nwords) return;
-        const int kw = (int)(wi / nwords);
-        const int nw = (int)(wi % nwords);
+        if (wi >= (long long)kw_total * nwords_s) return;
+        const int kw = (int)(wi / nwords_s);
+        const int nw = (int)(wi % nwords_s);
         const int lane = threadIdx.x & 31;
-        const uint32_t mine = p.src[(long long)(32 * kw + lane) * nwords + nw];
+        const bool in = kw < p.K / 32 && nw < nwords;
+        const uint32_t mine = in ? p.src[(long long)(32 * kw + lane) * nwords + nw] : 0u;
         uint32_t keep = 0;
 #pragma unroll
         for (int b = 0; b < 32; ++b) {
@@ -89,7 +94,7 @@ __device__ void prep_run(const SignPrep &p, int block, int threads) {
             if (lane == b) keep = col;
         }
         const int n = 32 * nw + lane;
-        p.dst[((long long)(kw >> 1) * p.N + n) * 2 + (kw & 1)] = sign_word_pair_ready(keep);
+        p.dst[((long long)(kw >> 1) * p.Ns + n) * 2 + (kw & 1)] = sign_word_pair_ready(keep);
     }
 }
 
@@ -372,15 +377,6 @@ cudaError_t launch_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, i
     return e;
 }
 
-static int host_prep_blocks(const SignPrep &p, int threads) {
-    if (p.kind == 0) {
-        const long long units = (long long)p.N * 2 * ((p.K + 63) / 64);
-        return (int)((units + threads - 1) / threads);
-    }
-    const long long warps = (long long)(p.K / 32) * (p.N / 32);
-    return (int)((warps + threads / 32 - 1) / (threads / 32));
-}
-
 cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
                                 int d_in, uint32_t *status, cudaStream_t s) {
     static bool prepared = false;
@@ -389,7 +385,7 @@ cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const 
         if (e != cudaSuccess) return e;
         prepared = true;
     }
-    const int b0 = host_prep_blocks(p0, 256), b1 = host_prep_blocks(p1, 256);
+    const int b0 = prep_blocks(p0, 256), b1 = prep_blocks(p1, 256);
     const long long groups = (long long)M * (d_in / 4);
     int bs = grid_for(groups, 256 * 4, 152 * 16);
     trace_before("fwd_prologue", s);
@@ -430,7 +426,7 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
     const int sms = cached_sms;
     int sb = stage_dy_blocks(a.M, a.d_out);
     if (sb > per_sm * sms) sb = per_sm * sms;
-    const int b0 = host_prep_blocks(p0, kStageThreads), b1 = host_prep_blocks(p1, kStageThreads);
+    const int b0 = prep_blocks(p0, kStageThreads), b1 = prep_blocks(p1, kStageThreads);
     trace_before("bwd_prologue", s);
     cudaError_t e = launch_k(bwd_prologue_kernel<GPT>, dim3(sb + b0 + b1), dim3(kStageThreads), smem, s, p0, p1, a, sb);
     trace_after(s);

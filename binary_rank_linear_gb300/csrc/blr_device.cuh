@@ -81,12 +81,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same condition. Measured on GB300 with tcgen05
+// MMAs in flight from the testing thread: a satisfied test_wait leaves the
+// tensor pipe busy, while a satisfied try_wait (acquire) stalls the thread
+// for about 160 cycles, longer than the pipe's queue of issued MMAs lasts.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase of `bar` with parity `parity` has completed. Gives up
 // (returns false) after kWaitLimitNs, or early when *abort_flag is set and
 // `honour_abort` is true.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort_flag,
                                           bool honour_abort = true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -111,36 +127,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t ra
     return r;
 }
 
-// Arrive once on an mbarrier of another CTA of the cluster (cluster address).
+// Arrive once on an mbarrier of another CTA of the cluster (cluster address),
+// with release at CTA scope, the form cluster barriers commonly use: the
+// data it announces (tensor-memory stores completed by tcgen05.wait::st,
+// TMA loads completed on the sender's own barrier) is complete before the
+// arrival leaves. Measured on GB300: about 6 cycles for the sender, against
+// 300-1400 cycles for a release at cluster scope, which waits for a
+// cluster-wide memory fence and limited a once-per-k-step forwarder to one
+// k-step per ~1200 cycles.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// As mbar_wait, with cluster-scope acquire (for barriers that receive
-// arrivals from the peer CTA).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, const volatile int *abort_flag,
-                                                  bool honour_abort = true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((i & 31u) == 0) {
-            if (honour_abort && *abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-        }
-    }
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Whole-cluster barrier (every thread of every CTA of the cluster).
@@ -261,6 +257,33 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem desc]^T: the A operand (M rows, 16 K
+// values per instruction) is read from tensor memory, lane m = row m, two f16
+// per 32-bit column (K index 2c in the low half of column c, 2c+1 in the high
+// half); B comes from shared memory as in umma_f16.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// CTA-pair form of umma_f16_ts (issued by the leader): A rows 0-127 from the
+// leader's TMEM and rows 128-255 from the peer's, at the same column address;
+// B's N rows are split in halves between the two CTAs' shared memory.
+__device__ __forceinline__ void umma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` at the same shared-memory offset in every CTA of
 // `cta_mask` when the pair's MMAs issued so far have completed.
 __device__ __forceinline__ void umma_commit_pair_multicast(uint64_t *bar, uint16_t cta_mask) {
@@ -319,7 +342,40 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)
         : "r"(taddr));
 }
 
+#define BLR_TMEM_ST32_INS(v)                                                                                   \
+    "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), \
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),           \
+        "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),            \
+        "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+
+// Each thread of the warp writes 32 consecutive 32-bit columns of its own
+// TMEM lane (lane = 32 * (warp % 4) + lane id, encoded in taddr's high half).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        BLR_TMEM_ST32_INS(v)
+        : "memory");
+}
+
+// Wait until this thread's tcgen05.st writes have completed.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+#define BLR_TMEM_REG32_INOUT(v)                                                                                \
+    "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), \
+        "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), \
+        "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),             \
+        "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+
+// tcgen05.wait::ld that names the destination registers of the load it waits
+// for: the compiler then cannot move a read of them above the wait (the load
+// writes them asynchronously, which the compiler does not know).
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&v)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : BLR_TMEM_REG32_INOUT(v)::"memory");
+}
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

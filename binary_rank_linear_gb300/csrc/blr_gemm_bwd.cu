@@ -4,10 +4,9 @@
 
 namespace blr {
 
-cudaError_t launch_gemm_bwd(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args,
-                            int grid, cudaStream_t s) {
-    if (epi == kEpiBwd1) return launch_gemm_epi<kEpiBwd1>(bn, tmap_a, emaps, args, grid, s);
-    if (epi == kEpiBwd2) return launch_gemm_epi<kEpiBwd2>(bn, tmap_a, emaps, args, grid, s);
+cudaError_t launch_gemm_bwd(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s) {
+    if (epi == kEpiBwd1) return launch_gemm_epi<kEpiBwd1>(plan, maps, args, s);
+    if (epi == kEpiBwd2) return launch_gemm_epi<kEpiBwd2>(plan, maps, args, s);
     return cudaErrorInvalidValue;
 }
 

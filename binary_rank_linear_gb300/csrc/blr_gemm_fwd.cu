@@ -4,10 +4,9 @@
 
 namespace blr {
 
-cudaError_t launch_gemm_fwd(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args,
-                            int grid, cudaStream_t s) {
-    if (epi == kEpiFwd1) return launch_gemm_epi<kEpiFwd1>(bn, tmap_a, emaps, args, grid, s);
-    if (epi == kEpiFwd2) return launch_gemm_epi<kEpiFwd2>(bn, tmap_a, emaps, args, grid, s);
+cudaError_t launch_gemm_fwd(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s) {
+    if (epi == kEpiFwd1) return launch_gemm_epi<kEpiFwd1>(plan, maps, args, s);
+    if (epi == kEpiFwd2) return launch_gemm_epi<kEpiFwd2>(plan, maps, args, s);
     return cudaErrorInvalidValue;
 }
 

@@ -46,7 +46,9 @@ cudaError_t launch_pack_signs(const float *src, uint32_t *bits, int rows, int r,
 cudaError_t launch_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, int r, cudaStream_t s);
 
 // Re-layout of one bitmap into the GEMM's "pair-ready" operand order
-// [ceil(K/64)][N][2] u32 (see sign_word_pair_ready):
+// [2 ceil(K/128)][Ns][2] u32 (see sign_word_pair_ready); rows N .. Ns-1 and
+// words past K are written as all -1 signs (they only ever meet zero
+// activations or are never stored):
 //  - kind 0 ("direct"): src is [N][K/32], bits already run along K;
 //  - kind 1 ("transpose"): src is [K][N/32], bits run along N.
 struct SignPrep {
@@ -55,6 +57,7 @@ struct SignPrep {
     int N;     // operand rows (output features)
     int K;     // reduction length
     int kind;  // 0 direct, 1 transpose
+    int Ns;    // destination row stride, sign_rows(N)
 };
 
 // Forward prologue, one launch: clear the device status word, re-lay two
@@ -95,31 +98,46 @@ enum GemmEpi : int { kEpiFwd1 = 0, kEpiFwd2 = 1, kEpiBwd1 = 2, kEpiBwd2 = 3 };
 
 struct GemmArgs {
     int M;                   // tokens
-    int N;                   // features = operand rows of the sign matrix
+    int N;                   // features = rows of the sign operand
     int K;                   // reduction length
-    const uint32_t *bsign;   // pair-ready bitmap [ceil(K/64)][N][2]
+    int Ns;                  // row stride of the re-laid bitmap (N rounded up to 256)
+    const uint32_t *bsign;   // pair-ready bitmap [2 ceil(K/128)][Ns][2]
     float *out32;            // FWD1 a-tape, FWD2 y, BWD2 dx   [M][N]
     uint16_t *out16;         // FWD1 a.l, FWD2 c, BWD1 db.l.sigma (f16 bits) [M][N]
     const float *colv;       // per-feature factor: FWD1 l, FWD2 h, BWD1 l, BWD2 g
-    const float *aux;        // BWD1 a-tape, BWD2 x   [M][N]
     const float *row_inv;    // BWD1 1/s_t, BWD2 1/sigma_t  [M]
     const float *row_scale;  // BWD1 sigma_t  [M]
-    float *part;             // BWD1 dl partials, BWD2 dg partials  [ceil(M/128)][N]
+    float *part;             // BWD1 dl partials, BWD2 dg partials  [token tiles][N]
     int accumulate;          // FWD2 y +=, BWD2 dx +=
     uint32_t *status;        // device status word
 };
 
-// Extra TMA descriptors of the wide-output products (c and dx'); unused by
-// the other two.
-struct EpiMaps {
-    CUtensorMap out32;  // f32 [M][N], box 32 x 32, 128-byte swizzle (y or dx)
-    CUtensorMap out16;  // f16 [M][N], box 32 x 32, 64-byte swizzle (c)
-    CUtensorMap in32;   // f32 [M][N], box 32 x 32, 128-byte swizzle (x, or y to accumulate)
+// Rows of the re-laid bitmap of a product with N features (a multiple of the
+// widest feature tile, so that tile loads stay inside the buffer).
+inline int sign_rows(int N) { return (N + 255) / 256 * 256; }
+
+// TMA descriptors of one GEMM launch. act: the f16 activation operand [M][K],
+// box 64 x (BT/2 for CTA pairs, BT otherwise), 128-byte swizzle. The
+// epilogue's chunk maps are [M][N] with a 32 x 32 box and no swizzle: in32
+// the f32 input (a-tape for db, x for dx', y when c accumulates into it),
+// out32 / out16 the f32 and f16 outputs (a and a.l, y and c, -, dx and -).
+// Maps a product does not use are left zero.
+struct GemmMaps {
+    CUtensorMap act, in32, out32, out16;
 };
 
-// `tmap_a`: the f16 activation operand [M][K], box 64 x 128, 128-B swizzle.
-// bn: 32, 64, 128 or 256 (must divide N). grid: number of persistent CTAs.
-cudaError_t launch_gemm(int epi, int bn, const CUtensorMap &tmap_a, const EpiMaps &emaps, const GemmArgs &args,
-                        int grid, cudaStream_t s);
+// Tile plan of one GEMM launch: CTA pairs (tcgen05 cta_group::2) with 160 or
+// 192 tokens per tile, or single CTAs with 128; grid = persistent CTAs (even
+// for pairs); part_rows = token tiles = partial-sum rows the epilogue writes.
+struct GemmPlan {
+    bool pair;
+    int bt;
+    int grid;
+    int part_rows;
+};
+
+GemmPlan plan_gemm(int M, int N, int sms);
+
+cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
 
 }  // namespace blr

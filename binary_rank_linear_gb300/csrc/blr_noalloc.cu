@@ -67,19 +67,6 @@ bool na_tmap(CUtensorMap *m, const void *base, int rows, int cols, int box_cols,
 
 size_t na_align(size_t v) { return (v + 255) / 256 * 256; }
 
-int na_pick_bn(int M, int N, int sms) {
-    const long long m_tiles = (M + 127) / 128;
-    int bn = 256;
-    while (bn > 32 && N % bn != 0) bn /= 2;
-    while (bn > 32 && m_tiles * (N / bn) < sms && N % (bn / 2) == 0) bn /= 2;
-    return bn;
-}
-
-int na_grid(int M, int N, int bn, int sms) {
-    const long long tiles = (long long)((M + 127) / 128) * (N / bn);
-    return (int)(tiles < sms ? tiles : sms);
-}
-
 // Device address of the scratch array on the current device (looked up once
 // per device), its SM count, and whether the device is supported.
 int na_setup(void **ptr, int *sms) {
@@ -109,7 +96,8 @@ size_t na_scratch_bytes(int M, int d_in, int d_out, int r) {
         d_out > 32768 || r > 65536)
         return 0;
     const size_t m = (size_t)M;
-    return na_align(256) + na_align((size_t)((d_in + 63) / 64) * r * 8) + na_align((size_t)((r + 63) / 64) * d_out * 8) +
+    return na_align(256) + na_align((size_t)((d_in + 127) / 128) * 2 * sign_rows(r) * 8) +
+           na_align((size_t)((r + 127) / 128) * 2 * sign_rows(d_out) * 8) +
            na_align(m * d_in * 2) + na_align(m * r * 4) + na_align(m * r * 2) + na_align(m * d_out * 2);
 }
 
@@ -146,51 +134,53 @@ extern "C" int blr_forward_noalloc(const float *x, const uint32_t *bits_u, const
     };
     const size_t m = (size_t)M;
     uint32_t *status = reinterpret_cast<uint32_t *>(take(256));
-    uint32_t *bp_f1 = reinterpret_cast<uint32_t *>(take((size_t)((d_in + 63) / 64) * r * 8));
-    uint32_t *bp_f2 = reinterpret_cast<uint32_t *>(take((size_t)((r + 63) / 64) * d_out * 8));
+    uint32_t *bp_f1 = reinterpret_cast<uint32_t *>(take((size_t)((d_in + 127) / 128) * 2 * sign_rows(r) * 8));
+    uint32_t *bp_f2 = reinterpret_cast<uint32_t *>(take((size_t)((r + 127) / 128) * 2 * sign_rows(d_out) * 8));
     uint16_t *x16 = reinterpret_cast<uint16_t *>(take(m * d_in * 2));
     float *a32 = reinterpret_cast<float *>(take(m * r * 4));
     uint16_t *al16 = reinterpret_cast<uint16_t *>(take(m * r * 2));
     uint16_t *c16 = reinterpret_cast<uint16_t *>(take(m * d_out * 2));
 
-    CUtensorMap tm_x, tm_a;
-    EpiMaps em_none{}, em_f2{};
-    if (!na_tmap(&tm_x, x16, M, d_in, 64, 128, true, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !na_tmap(&tm_a, al16, M, r, 64, 128, true, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !na_tmap(&em_f2.out32, y, M, d_out, 32, 32, false, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !na_tmap(&em_f2.out16, c16, M, d_out, 32, 32, true, CU_TENSOR_MAP_SWIZZLE_64B))
+    // the same tile plans as blr_forward
+    const GemmPlan p1 = plan_gemm(M, r, sms);
+    const GemmPlan p2 = plan_gemm(M, d_out, sms);
+    GemmMaps m1{}, m2{};
+    const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (!na_tmap(&m1.act, x16, M, d_in, 64, p1.pair ? p1.bt / 2 : p1.bt, true, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !na_tmap(&m1.out32, a32, M, r, 32, 32, false, none) || !na_tmap(&m1.out16, al16, M, r, 32, 32, true, none) ||
+        !na_tmap(&m2.act, al16, M, r, 64, p2.pair ? p2.bt / 2 : p2.bt, true, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !na_tmap(&m2.in32, y, M, d_out, 32, 32, false, none) || !na_tmap(&m2.out32, y, M, d_out, 32, 32, false, none) ||
+        !na_tmap(&m2.out16, c16, M, d_out, 32, 32, true, none))
         return BLR_ERR_CUDA;
-    em_f2.in32 = em_f2.out32;
 
     cudaStream_t s = (cudaStream_t)stream;
-    SignPrep pv{bits_v, bp_f1, r, d_in, 1};
-    SignPrep pu{bits_u, bp_f2, d_out, r, 0};
+    SignPrep pv{bits_v, bp_f1, r, d_in, 1, sign_rows(r)};
+    SignPrep pu{bits_u, bp_f2, d_out, r, 0, sign_rows(d_out)};
     if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, status, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs f1{};
     f1.M = M;
     f1.N = r;
     f1.K = d_in;
+    f1.Ns = sign_rows(r);
     f1.bsign = bp_f1;
     f1.out32 = a32;
     f1.out16 = al16;
     f1.colv = l;
     f1.status = status;
-    const int bn1 = na_pick_bn(M, r, sms);
-    if (launch_gemm(kEpiFwd1, bn1, tm_x, em_none, f1, na_grid(M, r, bn1, sms), s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiFwd1, p1, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs f2{};
     f2.M = M;
     f2.N = d_out;
     f2.K = r;
+    f2.Ns = sign_rows(d_out);
     f2.bsign = bp_f2;
     f2.out32 = y;
     f2.out16 = c16;
     f2.colv = h;
     f2.accumulate = accumulate_y;
     f2.status = status;
-    const int bn2 = na_pick_bn(M, d_out, sms);
-    if (launch_gemm(kEpiFwd2, bn2, tm_a, em_f2, f2, na_grid(M, d_out, bn2, sms), s) != cudaSuccess)
-        return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) return BLR_ERR_CUDA;
     return BLR_OK;
 }
