@@ -44,9 +44,9 @@
 // CTA pairs (tcgen05 cta_group::2): the leader issues M=256 MMAs reading A
 // from both CTAs' TMEM (rows 0-127 leader, 128-255 peer) and B from both
 // CTAs' shared memory (tokens 0 .. BT/2-1 leader, the rest peer); each CTA's
-// TMEM receives its 128 feature rows of the accumulator. The peer's MMA warp
-// forwards each k-step's readiness to the leader with one remote arrival; the
-// leader's commits are multicast to both CTAs.
+// TMEM receives its 128 feature rows of the accumulator. The peer's expander
+// warps arrive on the leader's full_s directly (remote arrivals); the leader's
+// commits are multicast to both CTAs.
 //
 // Every wait is bounded (blr_device.cuh): a wait that runs out sets the
 // shared abort flag and a status bit, the other roles leave their loops, the
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&full_b[s], 1);
             mbar_init(&empty_b[s], 1);
         }
-        for (int s = 0; s < NS; ++s) mbar_init(&full_s[s], (PAIR && leader) ? kNumExpWarps + 1 : kNumExpWarps);
+        for (int s = 0; s < NS; ++s) mbar_init(&full_s[s], PAIR ? 2 * kNumExpWarps : kNumExpWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tmem_full[i], 1);
             mbar_init(&tmem_empty[i], PAIR ? 2 * kNumEpiWarps : kNumEpiWarps);
@@ -242,6 +242,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == kWarpMma) {
         if (lane == 0 && leader) {
             constexpr uint32_t idesc = umma_idesc_f16_f32(PAIR ? 2 * kFM : kFM, BT);
+            // descriptors and TMEM addresses advance by constants per k-step, so
+            // the issuer's path between two k-steps stays a handful of instructions
+            const uint64_t bdesc0 = umma_sdesc_sw128(smem_u32(sB));
+            constexpr uint64_t kDescStage = S::kBBytes >> 4, kDescBlock = S::kBBlock >> 4;
+            const uint32_t sign0 = tmem_base + (uint32_t)S::kSignCol0;
             int sa = 0, sb = 0;
             uint32_t pa = 0;
             bool ok = true;
@@ -251,13 +256,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
                 // (the peer's arrivals on tmem_empty and full_s are released at CTA
                 // scope, see mbar_arrive_remote; they are awaited at CTA scope too)
-                const bool got = mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag);
-                if (!got) {
+                if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag)) {
                     fail_status(args, abort_flag, kStTimeoutMma);
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * S::kAccCols);
+                uint32_t acc_in = 0u;  // the tile's first MMA overwrites the accumulator
                 for (int ks = 0; ks < num_ks; ++ks) {
                     if (!mbar_wait(&full_s[sa], pa, abort_flag)) {
                         fail_status(args, abort_flag, kStTimeoutMma);
@@ -265,19 +270,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_tmem = tmem_base + (uint32_t)(S::kSignCol0 + sa * kSignCols);
+                    const uint32_t a_tmem = sign0 + (uint32_t)(sa * kSignCols);
+                    const uint64_t bdesc = bdesc0 + (uint64_t)sb * kDescStage;
 #pragma unroll
                     for (int kk = 0; kk < kKB; ++kk) {
-                        const uint64_t bdesc = umma_sdesc_sw128(smem_u32(sB + sb * S::kBBytes + kk * S::kBBlock));
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k) {
                             // 16 K values per MMA: 8 TMEM columns of A, 32 bytes along B's swizzled rows
-                            const uint32_t acc_in = (ks > 0 || kk > 0 || k > 0) ? 1u : 0u;
                             const uint32_t a_k = a_tmem + (uint32_t)(kk * (kBK / 2) + k * 8);
+                            const uint64_t b_k = bdesc + (uint64_t)kk * kDescBlock + (uint64_t)(2 * k);
                             if constexpr (PAIR)
-                                umma_f16_ts_pair(d_tmem, a_k, bdesc + (uint64_t)(2 * k), idesc, acc_in);
+                                umma_f16_ts_pair(d_tmem, a_k, b_k, idesc, acc_in);
                             else
-                                umma_f16_ts(d_tmem, a_k, bdesc + (uint64_t)(2 * k), idesc, acc_in);
+                                umma_f16_ts(d_tmem, a_k, b_k, idesc, acc_in);
+                            acc_in = 1u;
                         }
                     }
                     if constexpr (PAIR)
@@ -302,26 +308,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             else
                 umma_commit(drain_bar);
             if (!mbar_wait(drain_bar, 0, abort_flag, false)) atomicOr(args.status, kStTimeoutDrain);
-        } else if (PAIR && lane == 0) {
-            // the peer's MMA warp: once a k-step's sign rows are in this CTA's
-            // TMEM (after its activation tile landed), one arrival on the leader
-            int sa = 0;
-            uint32_t pa = 0;
-            bool ok = true;
-            for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
-                for (int ks = 0; ks < num_ks; ++ks) {
-                    if (!mbar_wait(&full_s[sa], pa, abort_flag)) {
-                        fail_status(args, abort_flag, kStTimeoutMma);
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_remote(leader_bar(&full_s[sa]));
-                    if (++sa == NS) {
-                        sa = 0;
-                        pa ^= 1u;
-                    }
-                }
-            }
         }
         __syncwarp();
     } else if (warp < kWarpEpi0) {
@@ -362,7 +348,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full_s[sa]);
+                if (lane == 0) {
+                    // the leader's MMAs read both CTAs' stages: the peer's warps
+                    // arrive on the leader's barrier directly
+                    if (PAIR && !leader)
+                        mbar_arrive_remote(leader_bar(&full_s[sa]));
+                    else
+                        mbar_arrive(&full_s[sa]);
+                }
                 if (++sb == NB) {
                     sb = 0;
                     pb ^= 1u;
