@@ -37,6 +37,35 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources and the C header (what a kernel's DRAM
+    traffic depends on), so that stored ncu counters can be matched to them."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "binary_rank_linear_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    with open(os.path.join(ROOT, "include", "blr.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()
+
+
+def stored_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+    `kernel` on `workload` from the committed ncu summary profiles/traffic.json,
+    or None when there is none or the kernels changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha256") != kernel_source_hash():
+        return None
+    v = d.get("bytes_per_launch", {}).get(workload, {}).get(kernel)
+    return float(v) if v is not None else None
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -292,7 +321,7 @@ def run_gpu(args, rank, world, local_rank):
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json: bf16 burst, f16 assumed equal)" \
         if peak_src == "measured" else "fallback"
-    roof["traffic"] = None
+    roof["traffic"] = stored_traffic(args.workload, dom)
 
     # end-to-end: host buffers through the public API, copies inside the timed region
     xh = torch.from_numpy(t["x"]).pin_memory()
