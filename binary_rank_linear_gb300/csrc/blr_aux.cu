@@ -65,6 +65,21 @@ __host__ __device__ __forceinline__ int prep_blocks(const SignPrep &p, int threa
     return (int)((warps + threads / 32 - 1) / (threads / 32));
 }
 
+__device__ void prep_run(const SignPrep &p, int block, int threads);
+
+// This block's share of the two re-layouts: virtual prep blocks block,
+// block + nblocks, ... (done first by every block of a prologue, so that the
+// re-layout never runs as a tail after the staging).
+__device__ void prep_share(const SignPrep &p0, const SignPrep &p1, int block, int nblocks) {
+    const int b0 = prep_blocks(p0, blockDim.x), b1 = prep_blocks(p1, blockDim.x);
+    for (int v = block; v < b0 + b1; v += nblocks) {
+        if (v < b0)
+            prep_run(p0, v, blockDim.x);
+        else
+            prep_run(p1, v - b0, blockDim.x);
+    }
+}
+
 __device__ void prep_run(const SignPrep &p, int block, int threads) {
     const int kw_total = prep_kwords(p.K);
     if (p.kind == 0) {
@@ -100,20 +115,47 @@ __device__ void prep_run(const SignPrep &p, int block, int threads) {
 
 // ============================================================ stage x ======
 // train_mm.rs, `cvt_col` staging: x16 = f16(x . g), forward unscaled.
+// A thread walks float4 groups (row-major [M][d_in/4]) with a grid stride,
+// four groups per round (four loads in flight); row and column advance by
+// precomputed steps, so the loop does no division.
 __device__ void stage_x_run(const float *__restrict__ x, const float *__restrict__ g, uint16_t *__restrict__ x16,
                             int M, int d_in, int block, int nblocks) {
-    const long long groups = (long long)M * (d_in / 4);
     const int g4n = d_in / 4;
+    const long long groups = (long long)M * g4n;
+    const long long stride = (long long)nblocks * blockDim.x;  // groups between a thread's consecutive visits
+    const int step_col = (int)(stride % g4n);
     const float4 *x4 = reinterpret_cast<const float4 *>(x);
     const float4 *gg = reinterpret_cast<const float4 *>(g);
     uint2 *o = reinterpret_cast<uint2 *>(x16);
-    for (long long i = (long long)block * blockDim.x + threadIdx.x; i < groups; i += (long long)nblocks * blockDim.x) {
-        const float4 v = __ldcs(x4 + i);
-        const float4 f = __ldg(gg + (int)(i % g4n));
-        uint2 out;
-        out.x = pack_half2(v.x * f.x, v.y * f.y);
-        out.y = pack_half2(v.z * f.z, v.w * f.w);
-        o[i] = out;
+    long long i = (long long)block * blockDim.x + threadIdx.x;
+    int col = (int)(i % g4n);
+    constexpr int kU = 8;
+    for (; i < groups; i += kU * stride) {
+        float4 v[kU], f[kU];
+        long long idx[kU];
+        long long ii = i;
+        int cc = col;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            idx[u] = ii;
+            if (ii < groups) {
+                v[u] = __ldcs(x4 + ii);
+                f[u] = __ldg(gg + cc);
+            }
+            ii += stride;
+            cc += step_col;
+            if (cc >= g4n) cc -= g4n;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (idx[u] < groups) {
+                uint2 out;
+                out.x = pack_half2(v[u].x * f[u].x, v[u].y * f[u].y);
+                out.y = pack_half2(v[u].z * f[u].z, v[u].w * f[u].w);
+                o[idx[u]] = out;
+            }
+        }
+        col = cc;
     }
 }
 
@@ -122,16 +164,8 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(SignPrep p0, SignPrep
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
-    const int b0 = prep_blocks(p0, blockDim.x);
-    const int b1 = prep_blocks(p1, blockDim.x);
-    const int b = blockIdx.x;
-    if (b < b0) {
-        prep_run(p0, b, blockDim.x);
-    } else if (b < b0 + b1) {
-        prep_run(p1, b - b0, blockDim.x);
-    } else {
-        stage_x_run(x, g, x16, M, d_in, b - b0 - b1, gridDim.x - b0 - b1);
-    }
+    prep_share(p0, p1, blockIdx.x, gridDim.x);
+    stage_x_run(x, g, x16, M, d_in, blockIdx.x, gridDim.x);
 }
 
 // =========================================================== stage dy ======
@@ -215,8 +249,19 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
     }
 
     const int batches = (a.M + rb_n - 1) / rb_n;
+    // the block reduces and stores a batch before it loads the next one: the
+    // next batch's rows of dy and c are prefetched into L2 meanwhile
+    auto prefetch_batch = [&](int bt) {
+        if (threadIdx.x != 0 || bt >= batches) return;
+        const int r0 = bt * rb_n;
+        const int nr = a.M - r0 < rb_n ? a.M - r0 : rb_n;
+        bulk_prefetch_l2(a.dy + (size_t)r0 * a.d_out, (uint32_t)((size_t)nr * a.d_out * 4));
+        bulk_prefetch_l2(a.c16 + (size_t)r0 * a.d_out, (uint32_t)((size_t)nr * a.d_out * 2));
+    };
+    prefetch_batch(block);
     int buf = 0;
     for (int bt = block; bt < batches; bt += nblocks, buf ^= 1) {
+        prefetch_batch(bt + nblocks);
         const int t = bt * rb_n + rb;
         const bool valid = t < a.M;
         float4 v[GPT];
@@ -303,18 +348,8 @@ __global__ void __launch_bounds__(kStageThreads, (GPT <= 8 ? 2 : 1))
     extern __shared__ __align__(16) float smem_f[];
     pdl_wait();
     pdl_launch_dependents();
-    const int b = blockIdx.x;
-    if (b < stage_blocks) {
-        stage_dy_run<GPT>(a, b, stage_blocks, smem_f);
-        return;
-    }
-    const int b0 = prep_blocks(p0, blockDim.x);
-    const int rest = b - stage_blocks;
-    if (rest < b0) {
-        prep_run(p0, rest, blockDim.x);
-    } else {
-        prep_run(p1, rest - b0, blockDim.x);
-    }
+    prep_share(p0, p1, blockIdx.x, stage_blocks);
+    stage_dy_run<GPT>(a, blockIdx.x, stage_blocks, smem_f);
 }
 
 // ============================================================== reduce =====
@@ -385,11 +420,20 @@ cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const 
         if (e != cudaSuccess) return e;
         prepared = true;
     }
-    const int b0 = prep_blocks(p0, 256), b1 = prep_blocks(p1, 256);
+    // one wave of persistent blocks (each does its share of the re-layouts, then
+    // grid-strides over x), but no more blocks than 8-group shares of x
+    static int wave = 0;
+    if (wave == 0) {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_prologue_kernel, 256, 0);
+        wave = (per_sm < 1 ? 1 : per_sm) * sms;
+    }
     const long long groups = (long long)M * (d_in / 4);
-    int bs = grid_for(groups, 256 * 4, 152 * 16);
+    const int bs = grid_for(groups, 256 * 8, wave);
     trace_before("fwd_prologue", s);
-    cudaError_t e = launch_k(fwd_prologue_kernel, dim3(b0 + b1 + bs), dim3(256), 0, s, p0, p1, x, g, x16, M, d_in, status);
+    cudaError_t e = launch_k(fwd_prologue_kernel, dim3(bs), dim3(256), 0, s, p0, p1, x, g, x16, M, d_in, status);
     trace_after(s);
     return e;
 }
@@ -426,9 +470,8 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
     const int sms = cached_sms;
     int sb = stage_dy_blocks(a.M, a.d_out);
     if (sb > per_sm * sms) sb = per_sm * sms;
-    const int b0 = prep_blocks(p0, kStageThreads), b1 = prep_blocks(p1, kStageThreads);
     trace_before("bwd_prologue", s);
-    cudaError_t e = launch_k(bwd_prologue_kernel<GPT>, dim3(sb + b0 + b1), dim3(kStageThreads), smem, s, p0, p1, a, sb);
+    cudaError_t e = launch_k(bwd_prologue_kernel<GPT>, dim3(sb), dim3(kStageThreads), smem, s, p0, p1, a, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;

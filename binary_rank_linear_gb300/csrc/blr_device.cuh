@@ -191,6 +191,13 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         : "memory");
 }
 
+// Asynchronous prefetch of [gsrc, gsrc + bytes) into L2 (16-byte aligned,
+// size a multiple of 16); nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
