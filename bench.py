@@ -99,6 +99,13 @@ def kernel_work(name: str, M: int, d_in: int, d_out: int, r: int):
         return 2.0 * M * r * d_in, 2.0 * M * r + bits_v + 4.0 * M * d_in + 4.0 * M * d_in
     if name == "reduce_partials":
         return 0.0, 4.0 * (d_in + d_out + r) * 2
+    if name == "small_fwd":  # fused forward of the small-M path
+        parts = [kernel_work(n, M, d_in, d_out, r) for n in ("fwd_prologue", "gemm_fwd1", "gemm_fwd2")]
+        return sum(p[0] for p in parts), 4.0 * M * d_in + 4.0 * M * r + 2.0 * M * r + 6.0 * M * d_out + bits_u + bits_v
+    if name == "small_bwd":  # fused backward of the small-M path
+        parts = [kernel_work(n, M, d_in, d_out, r) for n in ("gemm_bwd1", "gemm_bwd2")]
+        return (sum(p[0] for p in parts),
+                4.0 * M * d_out + 2.0 * M * d_out + 4.0 * M * r + 2.0 * M * r + 8.0 * M * d_in + bits_u + bits_v)
     return 0.0, 0.0
 
 

@@ -231,6 +231,22 @@ GemmPlan plan_gemm(int M, int N, int sms) {
     return GemmPlan{false, 128, (int)(tiles < sms ? tiles : sms), (int)t_tiles};
 }
 
+// Grid of the fused small-M kernels: enough CTAs for the larger GEMM phase's
+// tiles (at least 16, for the staging phases), at most one per SM.
+int small_grid(const GemmPlan &p1, int N1, const GemmPlan &p2, int N2, int M, int sms) {
+    const int t = (M + 127) / 128;
+    int tiles = t * ((N1 + 127) / 128);
+    const int t2 = t * ((N2 + 127) / 128);
+    if (t2 > tiles) tiles = t2;
+    if (tiles < 16) tiles = 16;
+    (void)p1;
+    (void)p2;
+    return tiles < sms ? tiles : sms;
+}
+
+// Word of the workspace header used as the fused kernels' grid-barrier counter.
+constexpr size_t kGridBarOffset = 64;
+
 }  // namespace blr
 
 using namespace blr;
@@ -308,7 +324,6 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     // S_V [d_in][r/32] has its bits along r: the first product needs them along d_in
     SignPrep pv{bits_v, bp_f1, r, d_in, 1, sign_rows(r)};
     SignPrep pu{bits_u, bp_f2, d_out, r, 0, sign_rows(d_out)};
-    if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, status, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs f1{};
     f1.M = M;
@@ -320,7 +335,6 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f1.out16 = al16;
     f1.colv = l;
     f1.status = status;
-    if (launch_gemm(kEpiFwd1, p1, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs f2{};
     f2.M = M;
@@ -333,7 +347,18 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f2.colv = h;
     f2.accumulate = accumulate_y;
     f2.status = status;
-    if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) return BLR_ERR_CUDA;
+
+    if (!p1.pair && !p2.pair) {
+        // small problem: the whole pass as one fused cooperative kernel
+        SmallFwdArgs fa{pv, pu, x, g, x16, M, d_in, status,
+                        reinterpret_cast<unsigned int *>(w + L.header + kGridBarOffset), f1, f2};
+        if (launch_small_fwd(m1, m2, fa, small_grid(p1, r, p2, d_out, M, sms), s) != cudaSuccess)
+            return BLR_ERR_CUDA;
+    } else {
+        if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, status, s) != cudaSuccess) return BLR_ERR_CUDA;
+        if (launch_gemm(kEpiFwd1, p1, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
+        if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) return BLR_ERR_CUDA;
+    }
 
     std::lock_guard<std::mutex> lk(g_tape_mu);
     g_tapes[ws] = Tape{M, d_in, d_out, r};
@@ -408,7 +433,6 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     sa.r = r;
     int rows_dh = 0;
     sa.rows_used = &rows_dh;
-    if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs b1{};
     b1.M = M;
@@ -422,7 +446,6 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b1.row_scale = sig;
     b1.part = part_dl;
     b1.status = status;
-    if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
 
     GemmArgs b2{};
     b2.M = M;
@@ -436,11 +459,29 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b2.part = part_dg;
     b2.accumulate = accumulate_dx;
     b2.status = status;
-    if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) return BLR_ERR_CUDA;
 
-    ReduceSeg sh{part_dh, dh, rows_dh, d_out};
     ReduceSeg sl{part_dl, dl, p1.part_rows, r};
     ReduceSeg sg{part_dg, dg, p2.part_rows, d_in};
+    if (!p1.pair && !p2.pair && small_bwd_fits(d_out)) {
+        // small problem: the whole pass as one fused cooperative kernel
+        SmallBwdArgs ba{};
+        ba.pu = pu;
+        ba.pv = pv;
+        ba.sd = sa;
+        ba.gbar = reinterpret_cast<unsigned int *>(w + L.header + kGridBarOffset);
+        ba.b1 = b1;
+        ba.b2 = b2;
+        ba.rh = ReduceSeg{part_dh, dh, 0, d_out};
+        ba.rl = sl;
+        ba.rg = sg;
+        if (launch_small_bwd(m1, m2, ba, small_grid(p1, r, p2, d_in, M, sms), L.rows_dh, s) != cudaSuccess)
+            return BLR_ERR_CUDA;
+        return BLR_OK;
+    }
+    if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) return BLR_ERR_CUDA;
+    ReduceSeg sh{part_dh, dh, rows_dh, d_out};
     if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
     return BLR_OK;
 }

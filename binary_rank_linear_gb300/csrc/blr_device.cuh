@@ -19,6 +19,7 @@ enum : uint32_t {
     kStTimeoutEpi = 1u << 3,     // epilogue: accumulator never ready
     kStTimeoutDrain = 1u << 4,   // teardown: in-flight copies or MMAs never drained
     kStBadLaunch = 1u << 5,      // launch geometry inconsistent with the kernel
+    kStTimeoutGrid = 1u << 6,    // fused small-M kernel: a grid barrier never completed
 };
 
 // A bounded wait gives up after this much wall time (ns). Normal waits in
@@ -53,6 +54,12 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // --------------------------------------------------------------- mbarrier ---
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Invalidate a barrier no thread or copy will touch again, so that its
+// memory may be reused (or the barrier initialised again).
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void fence_mbar_init() {

@@ -74,6 +74,7 @@ constexpr int kWarpExp0 = 2;
 constexpr int kNumExpWarps = 8;
 constexpr int kWarpEpi0 = 10;
 constexpr int kNumEpiWarps = 4;
+constexpr int kCtlBytes = 1024;   // shared-memory control block ahead of a phase's layout
 static_assert(kNumExpWarps == 4 * kKB, "one expander warp per (lane quarter, 64-wide block)");
 
 template <int EPI, bool PAIR, int BT>
@@ -102,7 +103,8 @@ struct GemmShape {
     static constexpr int kNS = kNSMax < kNB ? kNSMax : kNB;  // sign stages in TMEM
     static constexpr int kNumBars = 2 * kNB + kNS + 2 + 2 + 1 + kNumEpiWarps * kNE;
     static_assert(kNE >= 4, "prefetch distance of at least two chunks");
-    static constexpr int kSmemBytes = 1024 + kNB * kBBytes + kEpiBytes + kNB * kBitsBytes + kNumBars * 8 + 16;
+    static constexpr int kPhaseBytes = kNB * kBBytes + kEpiBytes + kNB * kBitsBytes + kNumBars * 8;
+    static constexpr int kSmemBytes = 1024 + kCtlBytes + kPhaseBytes;  // alignment slack, control block, phase
     static_assert(BT % 32 == 0 && BT >= 64 && BT <= 256 && (!PAIR || BT % 16 == 0), "token tile");
     static_assert(kTokRows % 8 == 0, "activation boxes hold whole 8-row swizzle groups");
     static_assert(kNS >= 2, "at least two sign stages");
@@ -115,6 +117,54 @@ struct GemmShape {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
+// Shared-memory control block at the (1024-aligned) start of dynamic shared
+// memory; a GEMM phase's own layout starts kCtlBytes after it.
+struct GemmCtl {
+    uint32_t tmem_slot;  // TMEM base address written by tcgen05.alloc
+    int abort_flag;      // set by any role whose bounded wait ran out
+};
+static_assert(sizeof(GemmCtl) <= kCtlBytes, "control block");
+
+// Shared-memory layout of one GEMM phase (from a 1024-aligned base).
+template <int EPI, bool PAIR, int BT>
+struct GemmLayout {
+    using S = GemmShape<EPI, PAIR, BT>;
+    uint8_t *sB;       // [NB][kBBytes] activation tiles
+    uint8_t *sE;       // [4 warps][kNE][slot] epilogue chunks
+    uint32_t *sBits;   // [NB][2][128][2] bitmap words
+    uint64_t *full_b, *empty_b, *full_s, *tmem_full, *tmem_empty, *drain_bar, *eload;
+    __device__ explicit GemmLayout(uint8_t *base) {
+        sB = base;
+        sE = sB + S::kNB * S::kBBytes;
+        sBits = reinterpret_cast<uint32_t *>(sE + S::kEpiBytes);
+        full_b = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sBits) + S::kNB * S::kBitsBytes);
+        empty_b = full_b + S::kNB;
+        full_s = empty_b + S::kNB;
+        tmem_full = full_s + S::kNS;
+        tmem_empty = tmem_full + 2;
+        drain_bar = tmem_empty + 2;
+        eload = drain_bar + 1;  // [4 warps][kNE]
+    }
+    // one thread: initialise every barrier of the phase
+    __device__ void init_barriers() const {
+        for (int s = 0; s < S::kNB; ++s) {
+            mbar_init(&full_b[s], 1);
+            mbar_init(&empty_b[s], 1);
+        }
+        for (int s = 0; s < S::kNS; ++s) mbar_init(&full_s[s], PAIR ? 2 * kNumExpWarps : kNumExpWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tmem_full[i], 1);
+            mbar_init(&tmem_empty[i], PAIR ? 2 * kNumEpiWarps : kNumEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        for (int i = 0; i < kNumEpiWarps * S::kNE; ++i) mbar_init(&eload[i], 1);
+    }
+    // one thread, once every role of the phase has finished with the barriers
+    __device__ void inval_barriers() const {
+        for (uint64_t *b = full_b; b < eload + kNumEpiWarps * S::kNE; ++b) mbar_inval(b);
+    }
+};
+
 __device__ __forceinline__ void fail_status(const GemmArgs &a, volatile int *abort_flag, uint32_t code) {
     *abort_flag = 1;
     atomicOr(a.status, code);
@@ -122,84 +172,34 @@ __device__ __forceinline__ void fail_status(const GemmArgs &a, volatile int *abo
 
 __device__ __forceinline__ uint16_t f16_bits(float v) { return __half_as_ushort(__float2half_rn(v)); }
 
+// The four roles of one GEMM phase over the tiles unit, unit + num_units, ...
+// (a CTA, or a CTA pair, per unit). Barriers must be initialised (and, for a
+// pair, both CTAs' barriers visible) and TMEM allocated before the call; on
+// return every load, MMA and store the phase issued has completed.
 template <int EPI, bool PAIR, int BT>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ CUtensorMap tmap_in,
-                    const __grid_constant__ CUtensorMap tmap_out32, const __grid_constant__ CUtensorMap tmap_out16,
-                    const GemmArgs args) {
+__device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, const CUtensorMap &tmap_act,
+                                           const CUtensorMap &tmap_in, const CUtensorMap &tmap_out32,
+                                           const CUtensorMap &tmap_out16, const GemmArgs &args,
+                                           uint32_t tmem_base, volatile int *abort_flag, int unit, int num_units) {
     using S = GemmShape<EPI, PAIR, BT>;
     constexpr int NB = S::kNB, NS = S::kNS, kChunks = S::kChunks, kNE = S::kNE;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sB = smem;                                                  // [NB][kBBytes]
-    uint8_t *sE = sB + NB * S::kBBytes;                                  // [4 warps][kNE][slot]
-    uint32_t *sBits = reinterpret_cast<uint32_t *>(sE + S::kEpiBytes);  // [NB][2][128][2]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sBits) + NB * S::kBitsBytes);
-    uint64_t *full_b = bars;
-    uint64_t *empty_b = full_b + NB;
-    uint64_t *full_s = empty_b + NB;
-    uint64_t *tmem_full = full_s + NS;
-    uint64_t *tmem_empty = tmem_full + 2;
-    uint64_t *drain_bar = tmem_empty + 2;
-    uint64_t *eload = drain_bar + 1;  // [4 warps][kNE]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(eload + kNumEpiWarps * kNE);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
+    uint8_t *sB = L.sB;
+    uint8_t *sE = L.sE;
+    uint32_t *sBits = L.sBits;
+    uint64_t *full_b = L.full_b, *empty_b = L.empty_b, *full_s = L.full_s, *tmem_full = L.tmem_full,
+             *tmem_empty = L.tmem_empty, *drain_bar = L.drain_bar, *eload = L.eload;
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     const int M = args.M, N = args.N;
     constexpr int kUnitF = PAIR ? 2 * kFM : kFM;  // features per tile
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
-    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // tile worker (CTA or pair)
-    const int num_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     const int f_tiles = (N + kUnitF - 1) / kUnitF;
     const int t_tiles = (M + BT - 1) / BT;
     const int num_tiles = f_tiles * t_tiles;  // feature tile varies fastest: neighbours share activations
     const int num_ks = (args.K + kStepK - 1) / kStepK;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NB; ++s) {
-            mbar_init(&full_b[s], 1);
-            mbar_init(&empty_b[s], 1);
-        }
-        for (int s = 0; s < NS; ++s) mbar_init(&full_s[s], PAIR ? 2 * kNumExpWarps : kNumExpWarps);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&tmem_full[i], 1);
-            mbar_init(&tmem_empty[i], PAIR ? 2 * kNumEpiWarps : kNumEpiWarps);
-        }
-        mbar_init(drain_bar, 1);
-        for (int i = 0; i < kNumEpiWarps * kNE; ++i) mbar_init(&eload[i], 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == kWarpTma && lane == 0) tma_prefetch_desc(&tmap_act);
-    if (warp == kWarpEpi0 && lane == 0) {
-        if (EPI != kEpiFwd1) tma_prefetch_desc(&tmap_in);
-        if (S::kHas32) tma_prefetch_desc(&tmap_out32);
-        if (S::kHas16) tma_prefetch_desc(&tmap_out16);
-    }
-    if constexpr (PAIR) {
-        cluster_sync();  // both CTAs' barriers exist before any remote arrival
-        if (warp == kWarpMma) {
-            tmem_alloc_pair(tmem_slot, kTmemCols);
-            tmem_relinquish_pair();
-        }
-    } else {
-        if (warp == kWarpMma) {
-            tmem_alloc(tmem_slot, kTmemCols);
-            tmem_relinquish();
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
     // the leader's copy of a barrier, as a cluster address (PAIR only)
     auto leader_bar = [&](uint64_t *bar) -> uint32_t { return mapa_shared(smem_u32(bar), 0); };
-    // setup above overlaps the previous kernel; global memory only after this
-    pdl_wait();
-    pdl_launch_dependents();
 
     if (warp == kWarpTma) {
         if (lane == 0) {
@@ -541,6 +541,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
     }
 
+}
+
+// Prefetch of a phase's tensor-map descriptors (TMA and epilogue lanes).
+template <int EPI, bool PAIR, int BT>
+__device__ __forceinline__ void gemm_prefetch_maps(const CUtensorMap &tmap_act, const CUtensorMap &tmap_in,
+                                                   const CUtensorMap &tmap_out32, const CUtensorMap &tmap_out16) {
+    using S = GemmShape<EPI, PAIR, BT>;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    if (warp == kWarpTma && lane == 0) tma_prefetch_desc(&tmap_act);
+    if (warp == kWarpEpi0 && lane == 0) {
+        if (EPI != kEpiFwd1) tma_prefetch_desc(&tmap_in);
+        if (S::kHas32) tma_prefetch_desc(&tmap_out32);
+        if (S::kHas16) tma_prefetch_desc(&tmap_out16);
+    }
+}
+
+__device__ __forceinline__ uint8_t *smem_base_1024() {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+}
+
+template <int EPI, bool PAIR, int BT>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ CUtensorMap tmap_in,
+                    const __grid_constant__ CUtensorMap tmap_out32, const __grid_constant__ CUtensorMap tmap_out16,
+                    const GemmArgs args) {
+    uint8_t *smem = smem_base_1024();
+    GemmCtl *ctl = reinterpret_cast<GemmCtl *>(smem);
+    const GemmLayout<EPI, PAIR, BT> L(smem + kCtlBytes);
+    const int warp = threadIdx.x / 32;
+    if (threadIdx.x == 0) {
+        L.init_barriers();
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    gemm_prefetch_maps<EPI, PAIR, BT>(tmap_act, tmap_in, tmap_out32, tmap_out16);
+    if constexpr (PAIR) {
+        cluster_sync();  // both CTAs' barriers exist before any remote arrival
+        if (warp == kWarpMma) {
+            tmem_alloc_pair(&ctl->tmem_slot, kTmemCols);
+            tmem_relinquish_pair();
+        }
+    } else {
+        if (warp == kWarpMma) {
+            tmem_alloc(&ctl->tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_slot;
+    // setup above overlaps the previous kernel; global memory only after this
+    pdl_wait();
+    pdl_launch_dependents();
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // tile worker (CTA or pair)
+    const int num_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    gemm_roles<EPI, PAIR, BT>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
+                              reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units);
     tc_fence_before();
     if constexpr (PAIR) {
         // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it

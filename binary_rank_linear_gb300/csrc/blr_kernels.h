@@ -140,4 +140,37 @@ GemmPlan plan_gemm(int M, int N, int sms);
 
 cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
 
+// ---- fused small-M path (blr_small.cu) ---------------------------------------
+// One cooperative launch (grid = one CTA per SM) per pass; the GEMM phases use
+// single-CTA 128-token tiles (plans with pair = false, bt = 128). `gbar` is a
+// grid-barrier counter in the workspace header, zeroed by the launcher.
+struct SmallFwdArgs {
+    SignPrep pv, pu;    // re-layouts of S_V (a-product) and S_U (c-product)
+    const float *x, *g;
+    uint16_t *x16;
+    int M, d_in;
+    uint32_t *status;
+    unsigned int *gbar;
+    GemmArgs f1, f2;    // the a- and c-products
+};
+
+struct SmallBwdArgs {
+    SignPrep pu, pv;    // re-layouts of S_U (db-product) and S_V (dx'-product)
+    StageDyArgs sd;     // dy staging (its part_dh has stage_blocks rows)
+    int stage_tpr;      // threads per token row in the staging (power of two <= 256); set by the launcher
+    int stage_nthr;     // staging threads per CTA (a multiple of stage_tpr); set by the launcher
+    int stage_blocks;   // CTAs that stage (dh partial rows written); set by the launcher
+    unsigned int *gbar;
+    GemmArgs b1, b2;    // the db- and dx'-products
+    ReduceSeg rh, rl, rg;
+};
+
+cudaError_t launch_small_fwd(const GemmMaps &m1, const GemmMaps &m2, const SmallFwdArgs &a, int grid,
+                             cudaStream_t s);
+// The launcher fills in the staging geometry and rh.rows (dh partial rows:
+// at most rows_dh_reserved, the rows the workspace holds).
+cudaError_t launch_small_bwd(const GemmMaps &m1, const GemmMaps &m2, SmallBwdArgs a, int grid, int rows_dh_reserved,
+                             cudaStream_t s);
+bool small_bwd_fits(int d_out);  // the fused backward stages rows of d_out floats
+
 }  // namespace blr

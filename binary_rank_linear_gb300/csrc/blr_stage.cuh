@@ -1,0 +1,336 @@
+// Bandwidth stages of the blr layer as device functions, shared by the
+// stand-alone prologue kernels (blr_aux.cu) and the fused small-M kernels
+// (blr_small.cu): bitmap re-layout, x staging, dy staging with the dh sums,
+// and the fixed-order reduction of per-tile partial sums.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "blr_device.cuh"
+#include "blr_kernels.h"
+
+namespace blr {
+
+// ============================================ bitmap re-layout (prep) ======
+// Destination order [kb][n][2] u32 (kb < 2 ceil(K/128), n < Ns): word
+// (n, 2kb + w) covers reduction indices 64kb + 32w .. +31 of operand row n,
+// pair-ready. Rows past N and words past K are written from an all-zero word.
+__host__ __device__ __forceinline__ int prep_kwords(int K) { return 4 * ((K + 127) / 128); }
+
+__host__ __device__ __forceinline__ int prep_blocks(const SignPrep &p, int threads) {
+    if (p.kind == 0) {
+        const long long units = (long long)p.Ns * prep_kwords(p.K);
+        return (int)((units + threads - 1) / threads);
+    }
+    const long long warps = (long long)prep_kwords(p.K) * (p.Ns / 32);
+    return (int)((warps + threads / 32 - 1) / (threads / 32));
+}
+
+__device__ inline void prep_run(const SignPrep &p, int block, int threads);
+
+// This block's share of the two re-layouts: virtual prep blocks block,
+// block + nblocks, ... (done first by every block of a prologue, so that the
+// re-layout never runs as a tail after the staging).
+__device__ inline void prep_share(const SignPrep &p0, const SignPrep &p1, int block, int nblocks) {
+    const int b0 = prep_blocks(p0, blockDim.x), b1 = prep_blocks(p1, blockDim.x);
+    for (int v = block; v < b0 + b1; v += nblocks) {
+        if (v < b0)
+            prep_run(p0, v, blockDim.x);
+        else
+            prep_run(p1, v - b0, blockDim.x);
+    }
+}
+
+__device__ inline void prep_run(const SignPrep &p, int block, int threads) {
+    const int kw_total = prep_kwords(p.K);
+    if (p.kind == 0) {
+        // direct: src [N][K/32]
+        const int words = p.K / 32;
+        const long long u = (long long)block * threads + threadIdx.x;
+        if (u >= (long long)p.Ns * kw_total) return;
+        const int n = (int)(u % p.Ns);
+        const int kw = (int)(u / p.Ns);
+        const uint32_t w = (kw < words && n < p.N) ? p.src[(long long)n * words + kw] : 0u;
+        p.dst[((long long)(kw >> 1) * p.Ns + n) * 2 + (kw & 1)] = sign_word_pair_ready(w);
+    } else {
+        // transpose: src [K][N/32]; one warp per 32 x 32 bit block.
+        const int nwords = p.N / 32;
+        const int nwords_s = p.Ns / 32;
+        const long long wi = (long long)block * (threads / 32) + threadIdx.x / 32;
+        if (wi >= (long long)kw_total * nwords_s) return;
+        const int kw = (int)(wi / nwords_s);
+        const int nw = (int)(wi % nwords_s);
+        const int lane = threadIdx.x & 31;
+        const bool in = kw < p.K / 32 && nw < nwords;
+        const uint32_t mine = in ? p.src[(long long)(32 * kw + lane) * nwords + nw] : 0u;
+        uint32_t keep = 0;
+#pragma unroll
+        for (int b = 0; b < 32; ++b) {
+            const uint32_t col = __ballot_sync(0xFFFFFFFFu, (mine >> b) & 1u);
+            if (lane == b) keep = col;
+        }
+        const int n = 32 * nw + lane;
+        p.dst[((long long)(kw >> 1) * p.Ns + n) * 2 + (kw & 1)] = sign_word_pair_ready(keep);
+    }
+}
+
+// ============================================================ stage x ======
+// train_mm.rs, `cvt_col` staging: x16 = f16(x . g), forward unscaled.
+// A thread walks float4 groups (row-major [M][d_in/4]) with a grid stride,
+// four groups per round (four loads in flight); row and column advance by
+// precomputed steps, so the loop does no division.
+__device__ inline void stage_x_run(const float *__restrict__ x, const float *__restrict__ g, uint16_t *__restrict__ x16,
+                            int M, int d_in, int block, int nblocks) {
+    const int g4n = d_in / 4;
+    const long long groups = (long long)M * g4n;
+    const long long stride = (long long)nblocks * blockDim.x;  // groups between a thread's consecutive visits
+    const int step_col = (int)(stride % g4n);
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    const float4 *gg = reinterpret_cast<const float4 *>(g);
+    uint2 *o = reinterpret_cast<uint2 *>(x16);
+    long long i = (long long)block * blockDim.x + threadIdx.x;
+    int col = (int)(i % g4n);
+    constexpr int kU = 8;
+    for (; i < groups; i += kU * stride) {
+        float4 v[kU], f[kU];
+        long long idx[kU];
+        long long ii = i;
+        int cc = col;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            idx[u] = ii;
+            if (ii < groups) {
+                v[u] = __ldcs(x4 + ii);
+                f[u] = __ldg(gg + cc);
+            }
+            ii += stride;
+            cc += step_col;
+            if (cc >= g4n) cc -= g4n;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (idx[u] < groups) {
+                uint2 out;
+                out.x = pack_half2(v[u].x * f[u].x, v[u].y * f[u].y);
+                out.y = pack_half2(v[u].z * f[u].z, v[u].w * f[u].w);
+                o[idx[u]] = out;
+            }
+        }
+        col = cc;
+    }
+}
+
+// =========================================================== stage dy ======
+// Backward staging (train_mm.rs, `blr_backward`: cvt of dy with the column
+// factor h under the gradient scale, and `colsum_prod` of dy and c for dh).
+// The first `nthr` threads of a block own whole token rows: `tpr` threads
+// share a row and the block works on nthr/tpr rows at a time, visiting rows
+// in a grid-stride loop (the other threads of the block only keep step with
+// its barriers). Per row t (one joint block reduction of the pair (max, sum)):
+//   A_t     = max_i |dy_ti h_i|,  L_t = sum_i |dy_ti h_i|
+//   s_t     = gscale, or 2^(14 - ceil(log2 A_t))   (1 if A_t is 0 or not finite)
+//   dy16_t  = f16(dy_t . h . s_t)
+//   sigma_t = gscale, or 2^(15 - ceil(log2(L_t max_k |l_k|)))
+// sigma_t scales the staged db.l in the next product. Since
+// |db_tk| = |sum_i dy16_ti S_ik| / s_t <= L_t (1 + 2^-11), every staged value
+// |db_tk l_k sigma_t| stays below 2^15 (1 + 2^-11), under the f16 maximum
+// 65504 whatever the data, while sigma_t is as large as that bound allows.
+// The block accumulates sum_t dy_ti c_ti for its rows in shared memory and
+// writes one partial row of dh.
+constexpr int kStageThreads = 512;
+constexpr int kStageMaxBlocks = 2 * 160;  // partial rows reserved per call
+
+__host__ __device__ inline int stage_tpr(int d_out) {
+    const int G = d_out / 4;  // float4 groups per row
+    int t = 32;
+    while (t * 8 < G && t < kStageThreads) t *= 2;  // at most 8 groups per thread when possible
+    return t;
+}
+
+__host__ __device__ inline int stage_gpt(int d_out) {
+    const int tpr = stage_tpr(d_out);
+    return (d_out / 4 + tpr - 1) / tpr;
+}
+
+// ceil(log2(v)) for finite v > 0.
+__device__ __forceinline__ int ceil_log2_pos(float v) {
+    int e;
+    const float m = frexpf(v, &e);  // v = m * 2^e, m in [0.5, 1)
+    return (m == 0.5f) ? e - 1 : e;
+}
+
+__device__ __forceinline__ float pow2i(int e) {
+    e = e < -126 ? -126 : (e > 127 ? 127 : e);
+    return __int_as_float((e + 127) << 23);
+}
+
+// Shared memory stage_dy_run needs (floats) for `tpr` threads per row.
+__host__ __device__ inline size_t stage_dy_smem_bytes(int d_out, int tpr, int nthr) {
+    return (64 + (size_t)(nthr / tpr) * d_out) * sizeof(float);
+}
+
+template <int GPT>
+__device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float *smem, int tpr, int nthr) {
+    const int rb_n = nthr / tpr;
+    const int wpr = tpr / 32;  // warps per row
+    const bool active = (int)threadIdx.x < nthr;
+    const int rb = active ? (int)threadIdx.x / tpr : 0;
+    const int ti = threadIdx.x % tpr;
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int G = a.d_out / 4;
+    float2 *red = reinterpret_cast<float2 *>(smem);      // [2][16 warps]
+    float4 *dh_s = reinterpret_cast<float4 *>(smem + 64);  // [rb_n][G]
+    const bool dynamic = !(a.gscale > 0.0f);
+
+    float lmax = 0.0f;
+    if (dynamic) {
+        for (int k = lane; k < a.r; k += 32) lmax = fmaxf(lmax, fabsf(__ldg(a.l + k)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+    }
+
+    const float4 *dy4 = reinterpret_cast<const float4 *>(a.dy);
+    const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
+    const uint2 *c4 = reinterpret_cast<const uint2 *>(a.c16);
+    uint2 *o4 = reinterpret_cast<uint2 *>(a.dy16);
+#pragma unroll
+    for (int g = 0; g < GPT; ++g) {
+        const int col = g * tpr + ti;
+        if (active && col < G) dh_s[rb * G + col] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    const int batches = (a.M + rb_n - 1) / rb_n;
+    // the block reduces and stores a batch before it loads the next one: the
+    // next batch's rows of dy and c are prefetched into L2 meanwhile
+    auto prefetch_batch = [&](int bt) {
+        if (threadIdx.x != 0 || bt >= batches) return;
+        const int r0 = bt * rb_n;
+        const int nr = a.M - r0 < rb_n ? a.M - r0 : rb_n;
+        bulk_prefetch_l2(a.dy + (size_t)r0 * a.d_out, (uint32_t)((size_t)nr * a.d_out * 4));
+        bulk_prefetch_l2(a.c16 + (size_t)r0 * a.d_out, (uint32_t)((size_t)nr * a.d_out * 2));
+    };
+    prefetch_batch(block);
+    int buf = 0;
+    for (int bt = block; bt < batches; bt += nblocks, buf ^= 1) {
+        prefetch_batch(bt + nblocks);
+        const int t = bt * rb_n + rb;
+        const bool valid = active && t < a.M;
+        float4 v[GPT];
+        float amax = 0.0f, l1 = 0.0f;
+#pragma unroll
+        for (int g = 0; g < GPT; ++g) {
+            const int col = g * tpr + ti;
+            v[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (valid && col < G) {
+                const long long idx = (long long)t * G + col;
+                const float4 d = __ldcs(dy4 + idx);
+                const uint2 cw = __ldcs(c4 + idx);
+                const float4 f = __ldg(h4 + col);
+                v[g] = make_float4(d.x * f.x, d.y * f.y, d.z * f.z, d.w * f.w);
+                const float2 c0 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.x));
+                const float2 c1 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.y));
+                float4 acc = dh_s[rb * G + col];
+                acc.x += d.x * c0.x;
+                acc.y += d.y * c0.y;
+                acc.z += d.z * c1.x;
+                acc.w += d.w * c1.y;
+                dh_s[rb * G + col] = acc;
+                const float4 q = make_float4(fabsf(v[g].x), fabsf(v[g].y), fabsf(v[g].z), fabsf(v[g].w));
+                amax = fmaxf(amax, fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w)));
+                l1 += (q.x + q.y) + (q.z + q.w);
+            }
+        }
+        float s = a.gscale, sig = a.gscale;
+        if (dynamic) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+            }
+            if (lane == 0 && active) red[buf * 16 + warp] = make_float2(amax, l1);
+            __syncthreads();
+            float2 r = red[buf * 16 + rb * wpr];
+            for (int i = 1; i < wpr; ++i) {
+                const float2 o = red[buf * 16 + rb * wpr + i];
+                r.x = fmaxf(r.x, o.x);
+                r.y += o.y;
+            }
+            const bool fin = r.x > 0.0f && r.x <= 3.402823466e38f;
+            s = fin ? pow2i(14 - ceil_log2_pos(r.x)) : 1.0f;
+            sig = s;
+            const float bound = r.y * lmax;  // bound on |db_t . l|, unscaled
+            if (fin && bound > 0.0f && bound <= 3.402823466e38f) sig = pow2i(15 - ceil_log2_pos(bound));
+        }
+#pragma unroll
+        for (int g = 0; g < GPT; ++g) {
+            const int col = g * tpr + ti;
+            if (valid && col < G) {
+                uint2 st;
+                st.x = pack_half2(v[g].x * s, v[g].y * s);
+                st.y = pack_half2(v[g].z * s, v[g].w * s);
+                __stcs(o4 + (long long)t * G + col, st);
+            }
+        }
+        if (valid && ti == 0) {
+            a.s_inv[t] = 1.0f / s;
+            a.sig[t] = sig;
+            a.sig_inv[t] = 1.0f / sig;
+        }
+    }
+    __syncthreads();
+    // fixed-order combine of the row groups' dh sums into the block's partial row
+    float4 *dst = reinterpret_cast<float4 *>(a.part_dh + (long long)block * a.d_out);
+    for (int col = threadIdx.x; col < G; col += blockDim.x) {
+        float4 acc = dh_s[col];
+        for (int q = 1; q < rb_n; ++q) {
+            const float4 o = dh_s[q * G + col];
+            acc.x += o.x;
+            acc.y += o.y;
+            acc.z += o.z;
+            acc.w += o.w;
+        }
+        dst[col] = acc;
+    }
+}
+
+// ============================================================== reduce =====
+// out[f] += sum_p part[p][f] over three segments, 32 columns per work item:
+// warp w of the block sums rows w, w + nwarps, ... and the warp sums are
+// added in warp order, so the result depends only on the block size. `red`
+// is nwarps x 32 floats of shared memory.
+__device__ __forceinline__ void reduce_partials_run(const ReduceSeg &a, const ReduceSeg &b, const ReduceSeg &c,
+                                                    int block, int nblocks, float *red) {
+    const int nba = (a.n + 31) / 32, nbb = (b.n + 31) / 32, nbc = (c.n + 31) / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int item = block; item < nba + nbb + nbc; item += nblocks) {
+        // the segment's fields by value (selecting a parameter by reference
+        // would copy the parameters to local memory)
+        const float *part;
+        float *out;
+        int rows, n, col0;
+        if (item < nba) {
+            part = a.part, out = a.out, rows = a.rows, n = a.n, col0 = 32 * item;
+        } else if (item < nba + nbb) {
+            part = b.part, out = b.out, rows = b.rows, n = b.n, col0 = 32 * (item - nba);
+        } else {
+            part = c.part, out = c.out, rows = c.rows, n = c.n, col0 = 32 * (item - nba - nbb);
+        }
+        const int col = col0 + lane;
+        float acc = 0.0f;
+        if (col < n) {
+#pragma unroll 4
+            for (int p = w; p < rows; p += nwarps) acc += __ldcs(part + (long long)p * n + col);
+        }
+        red[w * 32 + lane] = acc;
+        __syncthreads();
+        if (w == 0 && col < n) {
+            float t = red[lane];
+            for (int i = 1; i < nwarps; ++i) t += red[i * 32 + lane];
+            out[col] += t;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace blr

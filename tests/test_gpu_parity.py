@@ -134,6 +134,9 @@ SHAPES = [
     # enough 256 x 256 tiles for the CTA-pair GEMMs of the narrow outputs, ragged
     # M, and a reduction length (d_out = 1568) that ends in a partial k-step
     ("attn", 4600, 1024, 1568, 1280),
+    # small M with a wide output: the fused small-M forward, then the general
+    # backward (its dy rows are too wide for the fused staging)
+    ("small", 200, 128, 9216, 64),
 ]
 
 
