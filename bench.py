@@ -382,6 +382,7 @@ def run_gpu(args, rank, world, local_rank):
             "workload": f"{w.name}: {w.note}",
             "M": M, "d_in": d_in, "d_out": d_out, "r": r,
             "mode": "overwrite y/dx, dynamic per-token gradient scale",
+            "small_path": args.small_path,
             "l2": f"{nsets} rotating input/output/workspace sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)",
         },
         "tflops": world * w.flops * args.steps / (ms * 1e-3) / 1e12,
@@ -406,9 +407,13 @@ def main():
     ap.add_argument("--impl", default="blr", choices=["blr", "reference"])
     ap.add_argument("--workload", default="small")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small-path", default="general", choices=["general", "fused"],
+                    help="kernels for small problems: stand-alone (default) or the fused cooperative pair")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.small_path == "fused":
+        os.environ["BLR_SMALL_PATH"] = "fused"  # read by the library at each call
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

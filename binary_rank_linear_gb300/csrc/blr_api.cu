@@ -247,6 +247,15 @@ int small_grid(const GemmPlan &p1, int N1, const GemmPlan &p2, int N2, int M, in
 // Word of the workspace header used as the fused kernels' grid-barrier counter.
 constexpr size_t kGridBarOffset = 64;
 
+// The fused small-M kernels (blr_small.cu) are used for small problems only
+// when BLR_SMALL_PATH=fused is set: measured on GB300 they match the
+// stand-alone kernels on per-kernel time but lose under CUDA-graph replay,
+// where the stand-alone kernels overlap each other's setup and tails.
+bool fused_small_enabled() {
+    const char *v = std::getenv("BLR_SMALL_PATH");
+    return v && std::strcmp(v, "fused") == 0;
+}
+
 }  // namespace blr
 
 using namespace blr;
@@ -348,7 +357,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f2.accumulate = accumulate_y;
     f2.status = status;
 
-    if (!p1.pair && !p2.pair) {
+    if (!p1.pair && !p2.pair && fused_small_enabled()) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallFwdArgs fa{pv, pu, x, g, x16, M, d_in, status,
                         reinterpret_cast<unsigned int *>(w + L.header + kGridBarOffset), f1, f2};
@@ -462,7 +471,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
 
     ReduceSeg sl{part_dl, dl, p1.part_rows, r};
     ReduceSeg sg{part_dg, dg, p2.part_rows, d_in};
-    if (!p1.pair && !p2.pair && small_bwd_fits(d_out)) {
+    if (!p1.pair && !p2.pair && small_bwd_fits(d_out) && fused_small_enabled()) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallBwdArgs ba{};
         ba.pu = pu;

@@ -260,3 +260,13 @@ def test_full_size_workload(name):
         v64, p64 = vec.astype(np.float64).ravel(), par.astype(np.float64).ravel()
         got = float(np.dot(v64, p64))
         assert abs(got - ref) <= tol * np.linalg.norm(v64) * np.linalg.norm(p64) + ref_slack
+
+
+@pytest.mark.parametrize("name,M,d_in,d_out,r", [("tiny", 128, 256, 256, 64), ("small", 300, 320, 448, 96),
+                                                 ("small", 2048, 1024, 1024, 256), ("ragged", 129, 192, 96, 64)])
+def test_fused_small_path(monkeypatch, name, M, d_in, d_out, r):
+    """The fused small-M kernels (one cooperative kernel per pass) against the oracle."""
+    monkeypatch.setenv("BLR_SMALL_PATH", "fused")
+    t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    out = _run(t, gscale=0.0)
+    _check_against_oracle(t, out, "(fused small-M path)")
