@@ -171,9 +171,9 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     L.sig = take(m * 4);
     L.sig_inv = take(m * 4);
     L.rows_dh = stage_dy_blocks(M, d_out);
-    // one partial row per 128-token tile
-    L.rows_dl = (int)((m + 127) / 128);
-    L.rows_dg = L.rows_dl;
+    // partial rows per token tile (tiles of at least 128 tokens)
+    L.rows_dl = (int)((m + 127) / 128) * epi_part_rows_per_tile(kEpiBwd1);
+    L.rows_dg = (int)((m + 127) / 128) * epi_part_rows_per_tile(kEpiBwd2);
     L.part_dh = take((size_t)L.rows_dh * d_out * 4);
     L.part_dl = take((size_t)L.rows_dl * r * 4);
     L.part_dg = take((size_t)L.rows_dg * d_in * 4);
@@ -469,8 +469,8 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b2.accumulate = accumulate_dx;
     b2.status = status;
 
-    ReduceSeg sl{part_dl, dl, p1.part_rows, r};
-    ReduceSeg sg{part_dg, dg, p2.part_rows, d_in};
+    ReduceSeg sl{part_dl, dl, p1.part_rows * epi_part_rows_per_tile(kEpiBwd1), r};
+    ReduceSeg sg{part_dg, dg, p2.part_rows * epi_part_rows_per_tile(kEpiBwd2), d_in};
     if (!p1.pair && !p2.pair && small_bwd_fits(d_out) && fused_small_enabled()) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallBwdArgs ba{};

@@ -166,7 +166,7 @@ template <int GPT>
 static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
     const int tpr = stage_tpr(a.d_out);
     const int rb_n = kStageThreads / tpr;
-    const size_t smem = (64 + (size_t)rb_n * a.d_out) * sizeof(float);
+    const size_t smem = stage_dy_smem_bytes(a.d_out, tpr, rb_n * tpr);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = prepare_kernel(bwd_prologue_kernel<GPT>, 200 * 1024);

@@ -67,13 +67,13 @@ constexpr int kKB = 2;            // 64-wide blocks per k-step
 constexpr int kStepK = kKB * kBK;  // K per k-step (one MMA-issuer wait and one commit)
 constexpr int kSignCols = kStepK / 2;  // TMEM columns of one sign stage
 constexpr int kTmemCols = 512;
-constexpr int kGemmThreads = 448;
 constexpr int kWarpTma = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpExp0 = 2;
 constexpr int kNumExpWarps = 8;
 constexpr int kWarpEpi0 = 10;
-constexpr int kNumEpiWarps = 4;
+__host__ __device__ constexpr int gemm_threads(int epi) { return (kWarpEpi0 + epi_warps(epi)) * 32; }
+constexpr int kGemmThreads = (kWarpEpi0 + 8) * 32;  // the fused small-M kernels' block (every phase fits)
 constexpr int kCtlBytes = 1024;   // shared-memory control block ahead of a phase's layout
 static_assert(kNumExpWarps == 4 * kKB, "one expander warp per (lane quarter, 64-wide block)");
 
@@ -87,22 +87,25 @@ struct GemmShape {
     static constexpr int kBBytes = kKB * kBBlock;          // activation tile of a k-step
     static constexpr int kBitsBlock = kFM * 8;             // bitmap words of 128 rows, one block
     static constexpr int kBitsBytes = kKB * kBitsBlock;
+    static constexpr int kEW = epi_warps(EPI);             // epilogue warps
+    static constexpr int kSplit = kEW / 4;                 // epilogue warps per TMEM lane quarter
+    static constexpr int kThreads = gemm_threads(EPI);
     static constexpr bool kHas16 = EPI != kEpiBwd2;        // f16 output: a.l, c, db.l
     static constexpr bool kHas32 = EPI != kEpiBwd1;        // f32 output: a, y, dx
     static constexpr int kSlot32 = 32 * 32 * 4;            // f32 chunk: input, then output in place
     static constexpr int kSlotBytes = kSlot32 + (kHas16 ? 32 * 32 * 2 : 0);
-    // chunk slots per epilogue warp; inputs are prefetched kNE - 2 chunks ahead
-    // (a slot is free once the store of the chunk two before has read it). dx'
-    // streams x in and dx out at HBM rate, which takes ~6 chunks in flight
-    static constexpr int kNE = EPI == kEpiBwd2 ? 8 : 4;
-    static constexpr int kEpiBytes = kNumEpiWarps * kNE * kSlotBytes;
+    // chunk slots per epilogue warp; inputs are prefetched kNE - 2 of the
+    // warp's chunks ahead (a slot is free once the store of the warp's chunk two
+    // before has read it). dx' streams x in and dx out at HBM rate
+    static constexpr int kNE = EPI == kEpiBwd2 ? 4 : (kSplit == 2 ? 2 : 4);
+    static constexpr int kEpiBytes = kEW * kNE * kSlotBytes;
     static constexpr int kBudget = 221 * 1024 - kEpiBytes;
     static constexpr int kNBRaw = kBudget / (kBBytes + kBitsBytes);
     static constexpr int kNB = kNBRaw > 10 ? 10 : kNBRaw;
     static constexpr int kNSMax = (kTmemCols - 2 * BT) / kSignCols;
     static constexpr int kNS = kNSMax < kNB ? kNSMax : kNB;  // sign stages in TMEM
-    static constexpr int kNumBars = 2 * kNB + kNS + 2 + 2 + 1 + kNumEpiWarps * kNE;
-    static_assert(kNE >= 4, "prefetch distance of at least two chunks");
+    static constexpr int kNumBars = 2 * kNB + kNS + 2 + 2 + 1 + kEW * kNE;
+    static_assert(kNE >= 2, "double-buffered chunk staging");
     static constexpr int kPhaseBytes = kNB * kBBytes + kEpiBytes + kNB * kBitsBytes + kNumBars * 8;
     static constexpr int kSmemBytes = 1024 + kCtlBytes + kPhaseBytes;  // alignment slack, control block, phase
     static_assert(BT % 32 == 0 && BT >= 64 && BT <= 256 && (!PAIR || BT % 16 == 0), "token tile");
@@ -143,7 +146,7 @@ struct GemmLayout {
         tmem_full = full_s + S::kNS;
         tmem_empty = tmem_full + 2;
         drain_bar = tmem_empty + 2;
-        eload = drain_bar + 1;  // [4 warps][kNE]
+        eload = drain_bar + 1;  // [epilogue warps][kNE]
     }
     // one thread: initialise every barrier of the phase
     __device__ void init_barriers() const {
@@ -154,14 +157,14 @@ struct GemmLayout {
         for (int s = 0; s < S::kNS; ++s) mbar_init(&full_s[s], PAIR ? 2 * kNumExpWarps : kNumExpWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tmem_full[i], 1);
-            mbar_init(&tmem_empty[i], PAIR ? 2 * kNumEpiWarps : kNumEpiWarps);
+            mbar_init(&tmem_empty[i], PAIR ? 2 * S::kEW : S::kEW);
         }
         mbar_init(drain_bar, 1);
-        for (int i = 0; i < kNumEpiWarps * S::kNE; ++i) mbar_init(&eload[i], 1);
+        for (int i = 0; i < S::kEW * S::kNE; ++i) mbar_init(&eload[i], 1);
     }
     // one thread, once every role of the phase has finished with the barriers
     __device__ void inval_barriers() const {
-        for (uint64_t *b = full_b; b < eload + kNumEpiWarps * S::kNE; ++b) mbar_inval(b);
+        for (uint64_t *b = full_b; b < eload + S::kEW * S::kNE; ++b) mbar_inval(b);
     }
 };
 
@@ -369,22 +372,28 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
                 }
             }
         }
-    } else {
+    } else if (warp < kWarpEpi0 + S::kEW) {
         // ---- epilogue: thread = one feature of the tile, BT tokens ----------
+        // With two warps per lane quarter (kSplit = 2), the warp `half` takes
+        // the tile's chunks half, half + 2, ...; g counts the warp's own chunks.
+        constexpr int kSplit = S::kSplit;
+        constexpr int kMaxNc = (kChunks + kSplit - 1) / kSplit;  // chunks per tile of the busier warp
         const int q = warp & 3;
         const int ew = warp - kWarpEpi0;
+        const int half = ew / 4;
+        const int nc = (kChunks - half + kSplit - 1) / kSplit;  // this warp's chunks per tile
         uint8_t *slots = sE + ew * kNE * S::kSlotBytes;
         uint64_t *ebar = eload + ew * kNE;
         const bool has_in = (EPI == kEpiBwd1) || (EPI == kEpiBwd2) || (EPI == kEpiFwd2 && args.accumulate);
         uint32_t pending = 0u;  // lane 0: slots with an input load not yet waited on
         uint32_t ppar = 0u;     // and that load's phase parity
-        // chunk g = (local tile g / kChunks, chunk g % kChunks): its 32 features and first token
+        // the warp's chunk g: local tile g / nc, chunk half + kSplit * (g % nc)
         auto chunk_at = [&](int g, int &fq, int &tok) -> bool {
-            const int lt = g / kChunks;
+            const int lt = g / nc;
             const int tile = unit + lt * num_units;
             if (tile >= num_tiles) return false;
             fq = (tile % f_tiles) * kUnitF + (int)rank * kFM + q * 32;
-            tok = (tile / f_tiles) * BT + 32 * (g - lt * kChunks);
+            tok = (tile / f_tiles) * BT + 32 * (half + kSplit * (g - lt * nc));
             return true;
         };
         auto load_chunk = [&](int g) {  // lane 0
@@ -409,14 +418,15 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
             const int fq = (tile % f_tiles) * kUnitF + (int)rank * kFM + q * 32;  // this warp's 32 features
             const int f = fq + lane;
             const int t0 = tt * BT;
-            // per-token scales of the whole tile (lane l: token t0 + 32c + l),
-            // fetched before the accumulator is ready
-            float ri_t[kChunks], rs_t[kChunks];
+            // per-token scales of this warp's chunks (lane l: token 32c + l of
+            // the tile), fetched before the accumulator is ready
+            float ri_t[kMaxNc], rs_t[kMaxNc];
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                const int tl = t0 + 32 * c + lane;
-                ri_t[c] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && tl < M ? __ldg(args.row_inv + tl) : 0.0f;
-                rs_t[c] = (EPI == kEpiBwd1) && tl < M ? __ldg(args.row_scale + tl) : 0.0f;
+            for (int i = 0; i < kMaxNc; ++i) {
+                const int tl = t0 + 32 * (half + kSplit * i) + lane;
+                const bool use = i < nc && tl < M;
+                ri_t[i] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && use ? __ldg(args.row_inv + tl) : 0.0f;
+                rs_t[i] = (EPI == kEpiBwd1) && use ? __ldg(args.row_scale + tl) : 0.0f;
             }
             const bool fvalid = f < N;
             const float cf = fvalid ? __ldg(args.colv + f) : 0.0f;
@@ -429,20 +439,29 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
             tc_fence_after();
             float psum = 0.0f;
             const uint32_t acc_addr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * S::kAccCols);
-            // accumulator columns come in two register sets: chunk c+1 is loaded
-            // from TMEM while chunk c is processed
+            // One warp per quarter: accumulator columns come in two register
+            // sets, the next chunk loaded from TMEM while the current one is
+            // processed. Two warps per quarter overlap each other instead (one
+            // register set keeps them within the 96 registers their 18 warps allow).
             uint32_t va[32], vb[32];
-            tmem_ld_32x32b_x32(acc_addr, va);
+            if constexpr (kSplit == 1) tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * half), va);
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c, ++g) {
-                uint32_t(&v)[32] = (c & 1) ? vb : va;
-                uint32_t(&vn)[32] = (c & 1) ? va : vb;
-                tmem_wait_ld_regs(v);
-                if (c + 1 < kChunks) {
-                    tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * (c + 1)), vn);
+            for (int i = 0; i < kMaxNc; ++i) {
+                if (i >= nc) break;
+                const int c = half + kSplit * i;  // chunk of the tile
+                uint32_t(&v)[32] = (kSplit == 1 && (i & 1)) ? vb : va;
+                uint32_t(&vn)[32] = (kSplit == 1 && (i & 1)) ? va : vb;
+                if constexpr (kSplit == 1) {
+                    tmem_wait_ld_regs(v);
+                    if (i + 1 < nc) tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * (c + kSplit)), vn);
                 } else {
-                    // accumulator fully read: hand it back to the MMA issuer
-                    tmem_wait_ld_regs(vn);
+                    tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * c), v);
+                    tmem_wait_ld_regs(v);
+                }
+                if (i + 1 == nc) {
+                    // this warp's part of the accumulator is read: one arrival
+                    // of the kEW (per CTA) that hand it back to the MMA issuer
+                    if constexpr (kSplit == 1) tmem_wait_ld_regs(vn);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -453,8 +472,8 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
                     }
                 }
                 if (lane == 0) {
-                    // the slot of chunk g + kNE - 2 was last stored from by chunk g-2:
-                    // all stores but the newest (chunk g-1) have finished reading
+                    // the slot of the warp's chunk g + kNE - 2 was last stored from by
+                    // its chunk g-2: all stores but the newest (g-1) have read theirs
                     bulk_wait_group_read<1>();
                     if (has_in) load_chunk(g + kNE - 2);
                 }
@@ -495,8 +514,8 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
                     // db = acc / s_t; dl partial sum_t a.db; db.l staged under sigma_t
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float ri = __shfl_sync(0xFFFFFFFFu, ri_t[c], j);
-                        const float rs = __shfl_sync(0xFFFFFFFFu, rs_t[c], j);
+                        const float ri = __shfl_sync(0xFFFFFFFFu, ri_t[i], j);
+                        const float rs = __shfl_sync(0xFFFFFFFFu, rs_t[i], j);
                         const float db = __uint_as_float(v[j]) * ri;
                         psum += s32[j * 32 + lane] * db;
                         s16[j * 32 + lane] = f16_bits(db * cf * rs);
@@ -505,7 +524,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
                     // dx' = acc / sigma_t; dg partial sum_t x.dx'; dx (+)= g.dx'
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float ri = __shfl_sync(0xFFFFFFFFu, ri_t[c], j);
+                        const float ri = __shfl_sync(0xFFFFFFFFu, ri_t[i], j);
                         const float dxp = __uint_as_float(v[j]) * ri;
                         psum += s32[j * 32 + lane] * dxp;
                         s32[j * 32 + lane] = cf * dxp;
@@ -525,10 +544,12 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
                     if constexpr (S::kHas16) tma_store_2d(&tmap_out16, s16, fq, tc);
                 }
                 if (lane == 0) bulk_commit_group();
+                ++g;
             }
             if (!ok) break;
             if constexpr (EPI == kEpiBwd1 || EPI == kEpiBwd2) {
-                if (fvalid) args.part[(size_t)tt * N + f] = psum;
+                // one partial row per (token tile, warp of the quarter)
+                if (fvalid) args.part[((size_t)tt * kSplit + half) * N + f] = psum;
             }
         }
         // drain: stores complete, and input loads issued but not consumed have landed
@@ -563,7 +584,7 @@ __device__ __forceinline__ uint8_t *smem_base_1024() {
 }
 
 template <int EPI, bool PAIR, int BT>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(EPI), 1)
     blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ CUtensorMap tmap_in,
                     const __grid_constant__ CUtensorMap tmap_out32, const __grid_constant__ CUtensorMap tmap_out16,
                     const GemmArgs args) {
@@ -624,7 +645,7 @@ cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(S::kThreads);
     cfg.dynamicSmemBytes = S::kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];

@@ -96,6 +96,15 @@ cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaSt
 // ---- tcgen05 GEMMs --------------------------------------------------------
 enum GemmEpi : int { kEpiFwd1 = 0, kEpiFwd2 = 1, kEpiBwd1 = 2, kEpiBwd2 = 3 };
 
+// Epilogue warps of a product's GEMM: one per TMEM lane quarter, or two
+// (taking alternate chunks) for dx', whose epilogue (x in, dx out) outlasts its
+// short main loop. Measured on GB300, two warps per quarter also shortened the
+// c-product's epilogue only for K <= 512 and lengthened it otherwise (18 warps
+// cap every role at 96 registers). Each epilogue warp writes its own row of
+// token partial sums, so dx' has two partial rows per token tile.
+__host__ __device__ constexpr int epi_warps(int epi) { return epi == kEpiBwd2 ? 8 : 4; }
+__host__ __device__ constexpr int epi_part_rows_per_tile(int epi) { return epi_warps(epi) / 4; }
+
 struct GemmArgs {
     int M;                   // tokens
     int N;                   // features = rows of the sign operand
@@ -128,7 +137,8 @@ struct GemmMaps {
 
 // Tile plan of one GEMM launch: CTA pairs (tcgen05 cta_group::2) with 160 or
 // 192 tokens per tile, or single CTAs with 128; grid = persistent CTAs (even
-// for pairs); part_rows = token tiles = partial-sum rows the epilogue writes.
+// for pairs); part_rows = token tiles (the epilogue writes
+// epi_part_rows_per_tile rows of partial sums per token tile).
 struct GemmPlan {
     bool pair;
     int bt;

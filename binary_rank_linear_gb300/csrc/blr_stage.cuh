@@ -138,6 +138,9 @@ __device__ inline void stage_x_run(const float *__restrict__ x, const float *__r
 // The block accumulates sum_t dy_ti c_ti for its rows in shared memory and
 // writes one partial row of dh.
 constexpr int kStageThreads = 512;
+// floats of the staging's shared reduction buffer: float2 [2][32 warps], for
+// blocks of up to 1024 threads (the dh row sums follow it)
+constexpr int kStageRedFloats = 2 * 32 * 2;
 constexpr int kStageMaxBlocks = 2 * 160;  // partial rows reserved per call
 
 __host__ __device__ inline int stage_tpr(int d_out) {
@@ -166,7 +169,7 @@ __device__ __forceinline__ float pow2i(int e) {
 
 // Shared memory stage_dy_run needs (floats) for `tpr` threads per row.
 __host__ __device__ inline size_t stage_dy_smem_bytes(int d_out, int tpr, int nthr) {
-    return (64 + (size_t)(nthr / tpr) * d_out) * sizeof(float);
+    return (kStageRedFloats + (size_t)(nthr / tpr) * d_out) * sizeof(float);
 }
 
 template <int GPT>
@@ -179,8 +182,8 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     const int G = a.d_out / 4;
-    float2 *red = reinterpret_cast<float2 *>(smem);      // [2][16 warps]
-    float4 *dh_s = reinterpret_cast<float4 *>(smem + 64);  // [rb_n][G]
+    float2 *red = reinterpret_cast<float2 *>(smem);                    // [2][32 warps]
+    float4 *dh_s = reinterpret_cast<float4 *>(smem + kStageRedFloats);  // [rb_n][G]
     const bool dynamic = !(a.gscale > 0.0f);
 
     float lmax = 0.0f;
@@ -248,11 +251,11 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
                 amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
                 l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
             }
-            if (lane == 0 && active) red[buf * 16 + warp] = make_float2(amax, l1);
+            if (lane == 0 && active) red[buf * 32 + warp] = make_float2(amax, l1);
             __syncthreads();
-            float2 r = red[buf * 16 + rb * wpr];
+            float2 r = red[buf * 32 + rb * wpr];
             for (int i = 1; i < wpr; ++i) {
-                const float2 o = red[buf * 16 + rb * wpr + i];
+                const float2 o = red[buf * 32 + rb * wpr + i];
                 r.x = fmaxf(r.x, o.x);
                 r.y += o.y;
             }
