@@ -5,6 +5,7 @@ from .blr_oracle import (  # noqa: F401
     forward,
     pack_signs,
     rel_err,
+    sign_grads,
     unpack_signs,
     words_per_row,
 )

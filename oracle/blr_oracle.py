@@ -16,7 +16,10 @@ function below cites the part of that page it restates:
   ``[rows][ceil(r/32)]`` u32, bit j of word w is rank 32w+j, a set bit is +1;
 * the test helper ``pack_bits``: a sign is packed as 1 iff its value is > 0;
 * the test ``blr_layer_matches_host``: the per-token f64 host loop this oracle
-  vectorises, and the normwise relative error metric.
+  vectorises, and the normwise relative error metric;
+* ``blr_backward``'s documentation and the test helper ``host_sign_grads``:
+  the sign gradients G_U = diag(h) dy^T a diag(l) and
+  G_V = diag(g) x^T b diag(l), b the backward's db.
 
 Precision: inputs are f32 on the page; they are widened to f64 here and every
 step runs in f64. There is no staging, no f16 and no scaling in the oracle: the
@@ -40,6 +43,7 @@ __all__ = [
     "forward",
     "backward",
     "backward_sampled",
+    "sign_grads",
     "rel_err",
 ]
 
@@ -178,6 +182,31 @@ def backward_sampled(x, dy, bits_u, bits_v, g, l, h, cols_h, cols_g) -> dict:
     dxp_cols = np.matmul(db * l[None, :], s_v[cols_g].T)
     dg = np.sum(x[:, cols_g] * dxp_cols, axis=0)
     return {"dl": dl, "dh": dh, "dg": dg}
+
+
+def sign_grads(x, dy, bits_u, bits_v, g, l, h) -> dict:
+    """Sign gradients of the layer in f64.
+
+    train_mm.rs, ``blr_backward`` documentation and the test helper
+    ``host_sign_grads``:
+        a = (x (.) g) . S_V,  b = (dy (.) h) . S_U            [M][r]
+        G_U[i][k] = h_i l_k sum_t dy[t][i] a[t][k]           [d_out][r]
+        G_V[j][k] = g_j l_k sum_t x[t][j]  b[t][k]           [d_in][r]
+    i.e. G_U = diag(h) dy^T a diag(l) and G_V = diag(g) x^T b diag(l). With
+    L = <dy, y> these are dL/dS_U and dL/dS_V (L is linear in each sign).
+
+    Returns a dict with gu [d_out][r] and gv [d_in][r] (f64).
+    """
+    x, dy = _f64(x), _f64(dy)
+    g, l, h = _f64(g), _f64(l), _f64(h)
+    d_in, d_out, r = x.shape[1], h.shape[0], l.shape[0]
+    s_u = unpack_signs(bits_u, d_out, r)
+    s_v = unpack_signs(bits_v, d_in, r)
+    a = np.matmul(x * g[None, :], s_v)
+    b = np.matmul(dy * h[None, :], s_u)
+    gu = h[:, None] * np.matmul(dy.T, a) * l[None, :]
+    gv = g[:, None] * np.matmul(x.T, b) * l[None, :]
+    return {"gu": gu, "gv": gv}
 
 
 def rel_err(got, want) -> float:

@@ -331,3 +331,84 @@ def test_sampled_backward_matches_full():
     assert np.allclose(smp["dl"], full["dl"], rtol=1e-12, atol=1e-14)
     assert np.allclose(smp["dh"], full["dh"][ch], rtol=1e-12, atol=1e-14)
     assert np.allclose(smp["dg"], full["dg"][cg], rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------------- sign gradients --
+def _flip_bit(bits, rows, r, i, k):
+    """Copy of a bitmap with the sign of (row i, rank k) flipped (bit k%32 of word k//32)."""
+    w = oracle.words_per_row(r)
+    out = np.array(bits, dtype=np.uint32).reshape(rows, w).copy()
+    out[i, k // 32] ^= np.uint32(1 << (k % 32))
+    return out
+
+
+@pytest.mark.parametrize("seed", [5, 6])
+def test_sign_grads_flip_identity(seed):
+    """L = <dy, y> is linear in every single sign, so flipping S[i,k] (value s)
+    changes L by exactly -2 s G[i,k]; checked for every sign of a tiny layer
+    by re-running the forward with the flipped bitmap."""
+    t = _tiny(seed, M=4, d_in=5, d_out=6, r=36)
+    sg = oracle.sign_grads(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    l0 = _loss(t)
+    d_in, d_out, r = 5, 6, 36
+    for side, rows, key, gkey in (("u", d_out, "bu", "gu"), ("v", d_in, "bv", "gv")):
+        signs = t["su"] if side == "u" else t["sv"]
+        for i in range(rows):
+            for k in range(r):
+                flipped = dict(t)
+                flipped[key] = _flip_bit(t[key], rows, r, i, k)
+                dl = _loss(flipped) - l0
+                want = -2.0 * float(signs[i, k]) * sg[gkey][i, k]
+                assert abs(dl - want) <= 1e-9 * (1.0 + abs(want)), (side, i, k, dl, want)
+
+
+def test_sign_grads_trace_identity():
+    """sum_i S_U[i,k] G_U[i,k] = sum_j S_V[j,k] G_V[j,k] = l_k dl_k: both equal
+    l_k sum_t a_tk b_tk, which ties the sign gradients to the backward's dl."""
+    t = _tiny(7, M=5, d_in=9, d_out=7, r=40)
+    sg = oracle.sign_grads(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    want = t["l"].astype(np.float64) * bw["dl"]
+    assert np.allclose(np.sum(t["su"] * sg["gu"], axis=0), want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(np.sum(t["sv"] * sg["gv"], axis=0), want, rtol=1e-12, atol=1e-12)
+
+
+def test_sign_grads_match_loops():
+    """The sign gradients against the pages' per-element host formula, written
+    as plain Python loops (no matrix products)."""
+    t = _tiny(8, M=3, d_in=4, d_out=5, r=33)
+    sg = oracle.sign_grads(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    x, dy = t["x"].astype(np.float64), t["dy"].astype(np.float64)
+    M, d_in = x.shape
+    d_out, r = t["su"].shape
+    a = [[sum(x[m, j] * float(t["g"][j]) * float(t["sv"][j, k]) for j in range(d_in)) for k in range(r)]
+         for m in range(M)]
+    b = [[sum(dy[m, i] * float(t["h"][i]) * float(t["su"][i, k]) for i in range(d_out)) for k in range(r)]
+         for m in range(M)]
+    for k in range(r):
+        for i in range(d_out):
+            want = float(t["h"][i]) * float(t["l"][k]) * sum(dy[m, i] * a[m][k] for m in range(M))
+            assert math.isclose(sg["gu"][i, k], want, rel_tol=1e-12, abs_tol=1e-12)
+        for j in range(d_in):
+            want = float(t["g"][j]) * float(t["l"][k]) * sum(x[m, j] * b[m][k] for m in range(M))
+            assert math.isclose(sg["gv"][j, k], want, rel_tol=1e-12, abs_tol=1e-12)
+
+
+@pytest.mark.parametrize("mutant", ["swap_hg", "drop_l", "transpose_b"])
+def test_planted_sign_grad_mistakes_are_caught(mutant, monkeypatch):
+    """Plausible mistakes in sign_grads fail the flip identity."""
+    real = oracle.sign_grads
+
+    def broken(x, dy, bu, bv, g, l, h):
+        out = real(x, dy, bu, bv, g, l, h)
+        if mutant == "swap_hg":
+            out["gu"] = out["gu"] / np.asarray(h, np.float64)[:, None] * np.mean(g)
+        elif mutant == "drop_l":
+            out["gv"] = out["gv"] / np.asarray(l, np.float64)[None, :]
+        else:
+            out["gu"] = out["gu"][::-1].copy()
+        return out
+
+    monkeypatch.setattr(oracle, "sign_grads", broken)
+    with pytest.raises(AssertionError):
+        test_sign_grads_flip_identity(5)
