@@ -6,6 +6,7 @@ from .blr_oracle import (  # noqa: F401
     pack_signs,
     rel_err,
     sign_grads,
+    sign_grads_sampled,
     unpack_signs,
     words_per_row,
 )

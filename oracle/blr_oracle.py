@@ -209,6 +209,31 @@ def sign_grads(x, dy, bits_u, bits_v, g, l, h) -> dict:
     return {"gu": gu, "gv": gv}
 
 
+def sign_grads_sampled(x, dy, bits_u, bits_v, g, l, h, rows_u, rows_v) -> dict:
+    """G_U at the given rows of S_U and G_V at the given rows of S_V, in f64.
+
+    The sign_grads formulas (train_mm.rs, ``blr_backward`` documentation and
+    the test helper ``host_sign_grads``) restricted to rows: G_U[i, :] needs
+    only dy[:, i], and G_V[j, :] only x[:, j]; a and b are token-by-rank and
+    computed in full. For checking full-size workloads at a fraction of the
+    cost.
+
+    Returns a dict with gu [len(rows_u)][r] and gv [len(rows_v)][r].
+    """
+    x, dy = _f64(x), _f64(dy)
+    g, l, h = _f64(g), _f64(l), _f64(h)
+    d_in, d_out, r = x.shape[1], h.shape[0], l.shape[0]
+    s_u = unpack_signs(bits_u, d_out, r)
+    s_v = unpack_signs(bits_v, d_in, r)
+    rows_u = np.asarray(rows_u, dtype=np.int64)
+    rows_v = np.asarray(rows_v, dtype=np.int64)
+    a = np.matmul(x * g[None, :], s_v)
+    b = np.matmul(dy * h[None, :], s_u)
+    gu = h[rows_u, None] * np.matmul(dy[:, rows_u].T, a) * l[None, :]
+    gv = g[rows_v, None] * np.matmul(x[:, rows_v].T, b) * l[None, :]
+    return {"gu": gu, "gv": gv}
+
+
 def rel_err(got, want) -> float:
     """Normwise relative error sqrt(sum (got-want)^2 / max(sum want^2, 1e-30)).
 

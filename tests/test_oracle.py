@@ -412,3 +412,14 @@ def test_planted_sign_grad_mistakes_are_caught(mutant, monkeypatch):
     monkeypatch.setattr(oracle, "sign_grads", broken)
     with pytest.raises(AssertionError):
         test_sign_grads_flip_identity(5)
+
+
+def test_sign_grads_sampled_rows():
+    """The row-sampled sign gradients equal those rows of the full ones (which
+    the flip identity pins), including repeated and edge rows."""
+    t = _tiny(9, M=6, d_in=11, d_out=13, r=40)
+    full = oracle.sign_grads(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"])
+    ru, rv = np.array([0, 5, 5, 12]), np.array([10, 0, 3])
+    smp = oracle.sign_grads_sampled(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"], ru, rv)
+    assert np.allclose(smp["gu"], full["gu"][ru], rtol=1e-13, atol=1e-13)
+    assert np.allclose(smp["gv"], full["gv"][rv], rtol=1e-13, atol=1e-13)
