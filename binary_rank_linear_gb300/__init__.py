@@ -1,4 +1,4 @@
-"""GB300-native (sm_103a) binary low-rank (blr) linear layer, forward and backward.
+"""GB300-native (sm_103a) binary low-rank (blr) linear layer: forward, backward and sign gradients.
 
 The compute path is the CUDA library ``_lib/libblr.so`` (C ABI in
 ``include/blr.h``); this package is its thin Python binding plus the seeded
@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     BLR_ERR_WORKSPACE,
     BLR_OK,
     BlrError,
+    alloc_sign_workspace,
     alloc_workspace,
     backward,
     check_status,
@@ -22,6 +23,8 @@ from ._binding import (  # noqa: F401
     forward_noalloc,
     load,
     pack_signs,
+    sign_grads,
+    sign_workspace_bytes,
     trace_begin,
     trace_end,
     unpack_signs,

@@ -54,13 +54,16 @@ def load() -> ctypes.CDLL:
     lib.blr_unpack_signs.argtypes = [P, P, I, I, P]
     lib.blr_forward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, Z, P]
     lib.blr_backward.argtypes = [P, P, P, P, P, P, P, P, I, P, P, P, F, I, I, I, I, P, Z, P]
+    lib.blr_sign_workspace_bytes.argtypes = [I, I, I, I]
+    lib.blr_sign_workspace_bytes.restype = Z
+    lib.blr_sign_grads.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, Z, P]
     lib.blr_check_status.argtypes = [P, Z, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.blr_status_string.argtypes = [I]
     lib.blr_status_string.restype = ctypes.c_char_p
     lib.blr_trace_begin.argtypes = [I]
     lib.blr_trace_read.argtypes = [I, ctypes.POINTER(ctypes.c_float)]
     lib.blr_trace_read.restype = ctypes.c_char_p
-    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_check_status",
+    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_sign_grads", "blr_check_status",
               "blr_trace_begin", "blr_trace_end", "blr_trace_count"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -162,6 +165,32 @@ def backward(x, dy, bits_u, bits_v, g, l, h, dx, dg, dl, dh, ws, gscale: float =
         _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
     _check(code, "blr_backward")
     return dx
+
+
+def sign_workspace_bytes(M: int, d_in: int, d_out: int, r: int) -> int:
+    return int(load().blr_sign_workspace_bytes(M, d_in, d_out, r))
+
+
+def alloc_sign_workspace(M: int, d_in: int, d_out: int, r: int, device=None) -> torch.Tensor:
+    """The second, caller-owned workspace of ``sign_grads`` (transposed f16 operands)."""
+    n = sign_workspace_bytes(M, d_in, d_out, r)
+    if n == 0:
+        raise BlrError(BLR_ERR_SHAPE, "sign_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def sign_grads(x, g, l, gu, gv, ws, sws, accumulate: bool = False, stream=None):
+    """G_U = diag(h) dy^T a diag(l) -> gu [d_out][r], G_V = diag(g) x^T db diag(l) -> gv [d_in][r],
+    from the tape of the last forward/backward pair on ``ws``."""
+    M, d_in = x.shape
+    d_out, r = gu.shape
+    code = load().blr_sign_grads(
+        _ptr(x, "x", torch.float32, (M, d_in)), _ptr(g, "g", torch.float32, (d_in,)),
+        _ptr(l, "l", torch.float32, (r,)), _ptr(gu, "gu", torch.float32, (d_out, r)),
+        _ptr(gv, "gv", torch.float32, (d_in, r)), int(bool(accumulate)), M, d_in, d_out, r,
+        _ptr(ws, "ws", torch.uint8), ws.numel(), _ptr(sws, "sws", torch.uint8), sws.numel(), _stream(stream))
+    _check(code, "blr_sign_grads")
+    return gu, gv
 
 
 def check_status(ws: torch.Tensor, stream=None) -> int:

@@ -131,12 +131,26 @@ bool make_tmap_chunk(CUtensorMap *m, const void *base, int rows, int cols, bool 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows][cols] f32 with a 32 x 32 box and 128-byte swizzle (the sign
+// gradients' output chunks); stores are clipped to the extent.
+bool make_tmap_out_sw128(CUtensorMap *m, void *base, int rows, int cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ layout --------
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-    size_t header, bp_f1, bp_f2, bp_b1, bp_b2, act16, a32, act16b, c16, s_inv, sig, sig_inv, part_dh, part_dl,
-        part_dg, total;
+    size_t header, bp_f1, bp_f2, bp_b1, bp_b2, x16, dy16, a32, al16, db16, c16, s_inv, sig, sig_inv, blkmax,
+        part_dh, part_dl, part_dg, total;
     int rows_dh, rows_dl, rows_dg;
 };
 
@@ -163,14 +177,19 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     L.bp_f2 = take(kblocks(r) * sign_rows(d_out) * 8);  // forward 2: N = d_out, K = r
     L.bp_b1 = take(kblocks(d_out) * sign_rows(r) * 8);  // backward 1: N = r, K = d_out
     L.bp_b2 = take(kblocks(r) * sign_rows(d_in) * 8);   // backward 2: N = d_in, K = r
-    L.act16 = take(m * (size_t)(d_in > d_out ? d_in : d_out) * 2);
+    // the f16 staging of all four products stays in place after the pass
+    // (the sign-gradient products read x16, dy16, al16 and db16 again)
+    L.x16 = take(m * d_in * 2);
+    L.dy16 = take(m * d_out * 2);
     L.a32 = take(m * r * 4);
-    L.act16b = take(m * r * 2);
+    L.al16 = take(m * r * 2);
+    L.db16 = take(m * r * 2);
     L.c16 = take(m * d_out * 2);
     L.s_inv = take(m * 4);
     L.sig = take(m * 4);
     L.sig_inv = take(m * 4);
     L.rows_dh = stage_dy_blocks(M, d_out);
+    L.blkmax = take((size_t)L.rows_dh * 8);
     // partial rows per token tile (tiles of at least 128 tokens)
     L.rows_dl = (int)((m + 127) / 128) * epi_part_rows_per_tile(kEpiBwd1);
     L.rows_dg = (int)((m + 127) / 128) * epi_part_rows_per_tile(kEpiBwd2);
@@ -181,12 +200,45 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     return L;
 }
 
+// Second workspace of blr_sign_grads: header (the two scale maxima), then the
+// rank-side operands rescaled to one gradient scale, bu and bv [M][r] f16.
+struct SignLayout {
+    size_t header, bu, bv, total;
+};
+
+SignLayout make_sign_layout(int M, int r) {
+    SignLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += align_up(bytes, 256);
+        return o;
+    };
+    L.header = take(256);
+    L.bu = take((size_t)M * r * 2);
+    L.bv = take((size_t)M * r * 2);
+    L.total = off;
+    return L;
+}
+
 // ------------------------------------------------------------ tape ---------
 struct Tape {
     int M, d_in, d_out, r;
+    bool backward_done;  // a blr_backward has run on this tape (its staged dy and db are in the workspace)
+    float gscale;        // that backward's gradient scale (<= 0: dynamic per-token scales)
+    int stage_blocks;    // its staging blocks (entries of the per-block scale maxima)
 };
 std::mutex g_tape_mu;
 std::unordered_map<const void *, Tape> g_tapes;
+
+void mark_backward_done(const void *ws, float gscale, int stage_blocks) {
+    std::lock_guard<std::mutex> lk(g_tape_mu);
+    auto it = g_tapes.find(ws);
+    if (it == g_tapes.end()) return;
+    it->second.backward_done = true;
+    it->second.gscale = gscale;
+    it->second.stage_blocks = stage_blocks;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -310,9 +362,9 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     uint32_t *status = reinterpret_cast<uint32_t *>(w + L.header);
     uint32_t *bp_f1 = reinterpret_cast<uint32_t *>(w + L.bp_f1);
     uint32_t *bp_f2 = reinterpret_cast<uint32_t *>(w + L.bp_f2);
-    uint16_t *x16 = reinterpret_cast<uint16_t *>(w + L.act16);
+    uint16_t *x16 = reinterpret_cast<uint16_t *>(w + L.x16);
     float *a32 = reinterpret_cast<float *>(w + L.a32);
-    uint16_t *al16 = reinterpret_cast<uint16_t *>(w + L.act16b);
+    uint16_t *al16 = reinterpret_cast<uint16_t *>(w + L.al16);
     uint16_t *c16 = reinterpret_cast<uint16_t *>(w + L.c16);
 
     const GemmPlan p1 = plan_gemm(M, r, sms);
@@ -370,7 +422,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     }
 
     std::lock_guard<std::mutex> lk(g_tape_mu);
-    g_tapes[ws] = Tape{M, d_in, d_out, r};
+    g_tapes[ws] = Tape{M, d_in, d_out, r, false, 0.0f, 0};
     return BLR_OK;
 }
 
@@ -403,9 +455,9 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     uint32_t *status = reinterpret_cast<uint32_t *>(w + L.header);
     uint32_t *bp_b1 = reinterpret_cast<uint32_t *>(w + L.bp_b1);
     uint32_t *bp_b2 = reinterpret_cast<uint32_t *>(w + L.bp_b2);
-    uint16_t *dy16 = reinterpret_cast<uint16_t *>(w + L.act16);
+    uint16_t *dy16 = reinterpret_cast<uint16_t *>(w + L.dy16);
     const float *a32 = reinterpret_cast<const float *>(w + L.a32);
-    uint16_t *db16 = reinterpret_cast<uint16_t *>(w + L.act16b);
+    uint16_t *db16 = reinterpret_cast<uint16_t *>(w + L.db16);
     const uint16_t *c16 = reinterpret_cast<const uint16_t *>(w + L.c16);
     float *s_inv = reinterpret_cast<float *>(w + L.s_inv);
     float *sig = reinterpret_cast<float *>(w + L.sig);
@@ -436,6 +488,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     sa.sig = sig;
     sa.sig_inv = sig_inv;
     sa.part_dh = part_dh;
+    sa.blkmax = reinterpret_cast<float2 *>(w + L.blkmax);
     sa.gscale = gscale;
     sa.M = M;
     sa.d_out = d_out;
@@ -485,6 +538,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
         ba.rg = sg;
         if (launch_small_bwd(m1, m2, ba, small_grid(p1, r, p2, d_in, M, sms), L.rows_dh, s) != cudaSuccess)
             return BLR_ERR_CUDA;
+        mark_backward_done(ws, gscale, rows_dh);
         return BLR_OK;
     }
     if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
@@ -492,7 +546,88 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) return BLR_ERR_CUDA;
     ReduceSeg sh{part_dh, dh, rows_dh, d_out};
     if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
+    mark_backward_done(ws, gscale, rows_dh);
     return BLR_OK;
+}
+
+size_t blr_sign_workspace_bytes(int M, int d_in, int d_out, int r) {
+    if (!shape_ok(M, d_in, d_out, r)) return 0;
+    return make_sign_layout(M, r).total;
+}
+
+int blr_sign_grads(const float *x, const float *g, const float *l, float *gu, float *gv, int accumulate, int M, int d_in,
+                   int d_out, int r, const void *ws, size_t ws_bytes, void *sws, size_t sws_bytes,
+                   blr_stream_t stream) {
+    if (!x || !g || !l || !gu || !gv || !ws || !sws) return BLR_ERR_ARG;
+    if (accumulate != 0 && accumulate != 1) return BLR_ERR_ARG;
+    if (!shape_ok(M, d_in, d_out, r)) return BLR_ERR_SHAPE;
+    const void *ptrs[] = {x, g, l, gu, gv, ws, sws};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return BLR_ERR_ALIGN;
+    const Layout L = make_layout(M, d_in, d_out, r);
+    const SignLayout SL = make_sign_layout(M, r);
+    if (ws_bytes < L.total || sws_bytes < SL.total) return BLR_ERR_WORKSPACE;
+    Tape tape{};
+    {
+        std::lock_guard<std::mutex> lk(g_tape_mu);
+        auto it = g_tapes.find(ws);
+        if (it == g_tapes.end() || !it->second.backward_done || it->second.M != M || it->second.d_in != d_in ||
+            it->second.d_out != d_out || it->second.r != r)
+            return BLR_ERR_STATE;
+        tape = it->second;
+    }
+    int sms;
+    int st = device_info(&sms);
+    if (st != BLR_OK) return st;
+    if (fault_injected("sign")) return BLR_ERR_CUDA;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    char *w = static_cast<char *>(const_cast<void *>(ws));
+    char *sw = static_cast<char *>(sws);
+    const uint16_t *x16 = reinterpret_cast<const uint16_t *>(w + L.x16);
+    const uint16_t *dy16 = reinterpret_cast<const uint16_t *>(w + L.dy16);
+    const uint16_t *al16 = reinterpret_cast<const uint16_t *>(w + L.al16);
+    const uint16_t *db16 = reinterpret_cast<const uint16_t *>(w + L.db16);
+
+    SignGemmLaunch gl{};
+    gl.F[0] = d_out;
+    gl.F[1] = d_in;
+    gl.out[0] = gu;
+    gl.out[1] = gv;
+    gl.M = M;
+    gl.r = r;
+    gl.accumulate = accumulate;
+    gl.status = reinterpret_cast<uint32_t *>(w + L.header);
+    gl.sms = sms;
+    const uint16_t *bu = al16, *bv = db16;
+    if (tape.gscale > 0.0f) {
+        // one scale for every token: the staged a.l and db.l serve as they are
+        gl.scale[0] = gl.scale[1] = 1.0f / tape.gscale;
+    } else {
+        SignRescaleArgs ra{};
+        ra.al16 = al16;
+        ra.db16 = db16;
+        ra.s_inv = reinterpret_cast<const float *>(w + L.s_inv);
+        ra.sig_inv = reinterpret_cast<const float *>(w + L.sig_inv);
+        ra.blkmax = reinterpret_cast<const float2 *>(w + L.blkmax);
+        ra.nblk = tape.stage_blocks;
+        ra.M = M;
+        ra.r = r;
+        ra.bu = reinterpret_cast<uint16_t *>(sw + SL.bu);
+        ra.bv = reinterpret_cast<uint16_t *>(sw + SL.bv);
+        ra.gmax = reinterpret_cast<float *>(sw + SL.header);
+        if (launch_sign_rescale(ra, sms, s) != cudaSuccess) return BLR_ERR_CUDA;
+        bu = ra.bu;
+        bv = ra.bv;
+        gl.scale[0] = gl.scale[1] = 1.0f;
+        gl.dscale[0] = ra.gmax;
+        gl.dscale[1] = ra.gmax + 1;
+    }
+    if (!make_tmap_act16(&gl.maps.a[0], dy16, M, d_out, 64) || !make_tmap_act16(&gl.maps.b[0], bu, M, r, 64) ||
+        !make_tmap_act16(&gl.maps.a[1], x16, M, d_in, 64) || !make_tmap_act16(&gl.maps.b[1], bv, M, r, 64) ||
+        !make_tmap_out_sw128(&gl.maps.o[0], gu, d_out, r) || !make_tmap_out_sw128(&gl.maps.o[1], gv, d_in, r))
+        return BLR_ERR_CUDA;
+    return launch_sign_gemm(gl, s) == cudaSuccess ? BLR_OK : BLR_ERR_CUDA;
 }
 
 int blr_check_status(const void *ws, size_t ws_bytes, blr_stream_t stream, uint32_t *device_code) {

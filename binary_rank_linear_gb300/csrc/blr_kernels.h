@@ -77,6 +77,8 @@ struct StageDyArgs {
     float *sig;            // [M] out: sigma_t (scale of db.l)
     float *sig_inv;        // [M] out: 1/sigma_t
     float *part_dh;        // [stage_dy_blocks(M, d_out)][d_out] out
+    float2 *blkmax;        // [stage blocks] out: per block (max 1/s_t, max 1/sigma_t) over its rows with
+                           // nonzero finite dy.h (0 if none); the sign-gradient products rescale by them
     float gscale;          // > 0 fixed, <= 0 dynamic
     int M, d_out, r;
     int *rows_used;        // host out: dh partial rows the launch wrote
@@ -182,5 +184,47 @@ cudaError_t launch_small_fwd(const GemmMaps &m1, const GemmMaps &m2, const Small
 cudaError_t launch_small_bwd(const GemmMaps &m1, const GemmMaps &m2, SmallBwdArgs a, int grid, int rows_dh_reserved,
                              cudaStream_t s);
 bool small_bwd_fits(int d_out);  // the fused backward stages rows of d_out floats
+
+// ---- sign gradients (blr_sign.cu) -------------------------------------------
+// TMA descriptors of the sign-gradient products, [0] = G_U, [1] = G_V, all
+// token-major as the path stores them (K = tokens is the outer dimension, so
+// both MMA operands are MN-major):
+// a = dy16 / x16 [M][F] f16 (box 64 features x 64 tokens, 128-byte swizzle),
+// b = the rank-side operand [M][r] f16 (box 64 ranks x 64 tokens, same),
+// o = gu / gv [F][r] f32 (box 32 x 32, 128-byte swizzle).
+struct SignGemmMaps {
+    CUtensorMap a[2], b[2], o[2];
+};
+
+// Rank tile of the sign-gradient products: 256 when r >= 256, else 128.
+inline int sign_bn(int r) { return r >= 256 ? 256 : 128; }
+
+// Dynamic gradient scale: rescale the rank-side operands to one scale each,
+//   bu[t][k] = al16[t][k] * (1/s_t) / max_t (1/s_t)
+//   bv[t][k] = db16[t][k] * (1/sigma_t) / max_t (1/sigma_t)
+// (powers of two <= 1), maxima from the staging's per-block maxima; gmax[0..1]
+// receives the two maxima (a zero maximum, all dy zero, counts as 1).
+struct SignRescaleArgs {
+    const uint16_t *al16, *db16;   // [M][r]
+    const float *s_inv, *sig_inv;  // [M]
+    const float2 *blkmax;          // [nblk]
+    int nblk, M, r;
+    uint16_t *bu, *bv;             // [M][r] out
+    float *gmax;                   // [2] out
+};
+cudaError_t launch_sign_rescale(const SignRescaleArgs &a, int sms, cudaStream_t s);
+
+// G = scale * dscale (if given) * sum_t A[t][f] B[t][k], overwritten or added.
+struct SignGemmLaunch {
+    SignGemmMaps maps;
+    int F[2];                      // d_out, d_in
+    float scale[2];
+    const float *dscale[2];        // device scalars or null
+    float *out[2];                 // gu, gv
+    int M, r, accumulate;
+    uint32_t *status;
+    int sms;
+};
+cudaError_t launch_sign_gemm(const SignGemmLaunch &L, cudaStream_t s);
 
 }  // namespace blr

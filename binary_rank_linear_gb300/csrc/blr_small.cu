@@ -214,6 +214,7 @@ cudaError_t launch_small_bwd(const GemmMaps &m1, const GemmMaps &m2, SmallBwdArg
     a.stage_nthr = (kGemmThreads / a.stage_tpr) * a.stage_tpr;
     a.stage_blocks = grid < rows_dh_reserved ? grid : rows_dh_reserved;
     a.rh.rows = a.stage_blocks;
+    if (a.sd.rows_used) *a.sd.rows_used = a.stage_blocks;
     const int gpt = (a.sd.d_out / 4 + a.stage_tpr - 1) / a.stage_tpr;
     if (gpt <= 2) return launch_small_bwd_t<2>(m1, m2, a, grid, s);
     if (gpt <= 8) return launch_small_bwd_t<8>(m1, m2, a, grid, s);

@@ -136,7 +136,9 @@ __device__ inline void stage_x_run(const float *__restrict__ x, const float *__r
 // |db_tk l_k sigma_t| stays below 2^15 (1 + 2^-11), under the f16 maximum
 // 65504 whatever the data, while sigma_t is as large as that bound allows.
 // The block accumulates sum_t dy_ti c_ti for its rows in shared memory and
-// writes one partial row of dh.
+// writes one partial row of dh, and the largest 1/s_t and 1/sigma_t of its
+// rows with nonzero finite A_t (rows of zeros carry no gradient, and their
+// scale 1 must not set the common scale of the sign-gradient products).
 constexpr int kStageThreads = 512;
 // floats of the staging's shared reduction buffer: float2 [2][32 warps], for
 // blocks of up to 1024 threads (the dh row sums follow it)
@@ -215,6 +217,7 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
     };
     prefetch_batch(block);
     int buf = 0;
+    float2 mx = make_float2(0.0f, 0.0f);  // this thread's rows: max 1/s_t, max 1/sigma_t
     for (int bt = block; bt < batches; bt += nblocks, buf ^= 1) {
         prefetch_batch(bt + nblocks);
         const int t = bt * rb_n + rb;
@@ -245,6 +248,7 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
             }
         }
         float s = a.gscale, sig = a.gscale;
+        bool counts = true;  // the row takes part in the block's maxima
         if (dynamic) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -260,6 +264,7 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
                 r.y += o.y;
             }
             const bool fin = r.x > 0.0f && r.x <= 3.402823466e38f;
+            counts = fin;
             s = fin ? pow2i(14 - ceil_log2_pos(r.x)) : 1.0f;
             sig = s;
             const float bound = r.y * lmax;  // bound on |db_t . l|, unscaled
@@ -279,9 +284,24 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
             a.s_inv[t] = 1.0f / s;
             a.sig[t] = sig;
             a.sig_inv[t] = 1.0f / sig;
+            if (counts) mx = make_float2(fmaxf(mx.x, 1.0f / s), fmaxf(mx.y, 1.0f / sig));
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx.x = fmaxf(mx.x, __shfl_xor_sync(0xFFFFFFFFu, mx.x, o));
+        mx.y = fmaxf(mx.y, __shfl_xor_sync(0xFFFFFFFFu, mx.y, o));
+    }
+    __syncthreads();  // every read of red in the loop is done
+    if (lane == 0) red[warp] = mx;
     __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 1; i < (int)(blockDim.x >> 5); ++i) {
+            mx.x = fmaxf(mx.x, red[i].x);
+            mx.y = fmaxf(mx.y, red[i].y);
+        }
+        a.blkmax[block] = mx;
+    }
     // fixed-order combine of the row groups' dh sums into the block's partial row
     float4 *dst = reinterpret_cast<float4 *>(a.part_dh + (long long)block * a.d_out);
     for (int col = threadIdx.x; col < G; col += blockDim.x) {

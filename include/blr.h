@@ -142,6 +142,46 @@ BLR_API int blr_backward(const float *x, const float *dy,
                  int M, int d_in, int d_out, int r,
                  void *ws, size_t ws_bytes, blr_stream_t stream);
 
+/* Bytes of the second workspace blr_sign_grads needs for this shape (0 when
+ * the shape violates the shape rule): the rank-side f16 operands rescaled to
+ * one gradient scale, 4*M*r bytes plus a 256-byte header. */
+BLR_API size_t blr_sign_workspace_bytes(int M, int d_in, int d_out, int r);
+
+/* Sign gradients of the layer (train_mm.rs, blr_backward documentation, and
+ * its test helper host_sign_grads):
+ *
+ *     G_U = diag(h) . dy^T . a . diag(l)      gu [d_out][r] f32
+ *     G_V = diag(g) . x^T  . b . diag(l)      gv [d_in][r]  f32
+ *
+ * with a = (x.g) S_V the forward's product and b = (dy.h) S_U the backward's
+ * db. With L = <dy, y> these are dL/dS_U and dL/dS_V. The pages form them
+ * inside the backward ("with sign"); here they are a separate call after
+ * blr_backward on the same workspace `ws`, whose tape it reads: a (forward),
+ * and the backward's staged f16 dy.h and db.l with their per-token powers of
+ * two. So dy, h and the bitmaps are not arguments; x, g and l must be the
+ * ones of that forward/backward pair.
+ *  - Operands: the pass's own f16 staging, token-major as it is (the tensor
+ *    cores read it as MN-major tiles; nothing is transposed): dy.h with x.g
+ *    on the feature side, a.l and db.l on the rank side. With a fixed
+ *    gscale every token shares one scale and the products are divided by
+ *    it. With dynamic per-token scales, a.l and db.l are first rescaled
+ *    into `sws` (caller-owned, blr_sign_workspace_bytes(...) bytes,
+ *    16-byte aligned) by 1/s_t / max_t(1/s_t) and 1/sigma_t /
+ *    max_t(1/sigma_t), over the tokens with a nonzero gradient: powers of
+ *    two <= 1, exact unless a value falls into the f16 subnormals (tokens
+ *    whose gradient is far below the largest). The products accumulate in
+ *    f32 on the tensor cores and the common scales are divided back out.
+ *  - accumulate = 0 overwrites gu and gv, 1 adds to them.
+ * Errors: as blr_backward; BLR_ERR_STATE when no blr_backward of this shape
+ *   has run on `ws` since its last blr_forward; BLR_ERR_WORKSPACE when
+ *   ws_bytes or sws_bytes is short. Kernel-side failures go to the status
+ *   word of `ws` (blr_check_status). */
+BLR_API int blr_sign_grads(const float *x, const float *g, const float *l,
+                           float *gu, float *gv, int accumulate,
+                           int M, int d_in, int d_out, int r,
+                           const void *ws, size_t ws_bytes, void *sws, size_t sws_bytes,
+                           blr_stream_t stream);
+
 /* Synchronises `stream` and reads the workspace's device status word.
  * Returns BLR_OK if no kernel recorded a failure since the last blr_forward
  * on this workspace, BLR_ERR_DEVICE_CHECK if one did (the code is written to

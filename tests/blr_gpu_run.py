@@ -13,8 +13,9 @@ def to_dev(a, dtype=torch.float32):
     return torch.from_numpy(np.ascontiguousarray(a)).to(device="cuda", dtype=dtype)
 
 
-def run_layer(t, gscale=0.0, y_prior=None, dx_prior=None, grad_prior=None, ws=None, backward=True):
-    """Forward (+ backward) of one path. Priors given = accumulate mode."""
+def run_layer(t, gscale=0.0, y_prior=None, dx_prior=None, grad_prior=None, ws=None, backward=True, sign=False,
+              sign_prior=None):
+    """Forward (+ backward, + sign gradients) of one path. Priors given = accumulate mode."""
     x, dy = to_dev(t["x"]), to_dev(t["dy"]) if backward else None
     M, d_in = t["x"].shape
     d_out, r = t["su"].shape
@@ -36,6 +37,15 @@ def run_layer(t, gscale=0.0, y_prior=None, dx_prior=None, grad_prior=None, ws=No
             dh = torch.zeros(d_out, device="cuda")
         blr.backward(x, dy, bu, bv, g, l, h, dx, dg, dl, dh, ws, gscale=gscale, accumulate=dx_prior is not None)
         out.update(dx=dx, dg=dg, dl=dl, dh=dh)
+        if sign:
+            sws = blr.alloc_sign_workspace(M, d_in, d_out, r)
+            if sign_prior is not None:
+                gu, gv = to_dev(sign_prior["gu"]), to_dev(sign_prior["gv"])
+            else:
+                gu = torch.full((d_out, r), float("nan"), device="cuda")
+                gv = torch.full((d_in, r), float("nan"), device="cuda")
+            blr.sign_grads(x, g, l, gu, gv, ws, sws, accumulate=sign_prior is not None)
+            out.update(gu=gu, gv=gv)
     out["status"] = blr.check_status(ws)
     host = {}
     for k, v in out.items():

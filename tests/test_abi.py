@@ -56,8 +56,9 @@ def test_workspace_bytes_shape_rule(lib):
     assert lib.blr_workspace_bytes(128, 65536, 32768, 64) > 0
     small = lib.blr_workspace_bytes(2048, 1024, 1024, 256)
     assert lib.blr_workspace_bytes(2049, 1024, 1024, 256) > small
-    # tape alone: a f32 [M][r] + c f16 [M][d_out]
-    assert small > 2048 * 256 * 4 + 2048 * 1024 * 2
+    # tape alone: a f32 [M][r] + c f16 [M][d_out], and the four f16 stagings
+    # x.g, dy.h, a.l, db.l kept side by side
+    assert small > 2048 * 256 * 4 + 2048 * 1024 * 2 + 2048 * (1024 + 1024 + 256 + 256) * 2
 
 
 FAKE = 1 << 20  # 16-byte aligned, never dereferenced
@@ -102,6 +103,38 @@ def test_backward_argument_errors(lib):
     # no forward ever ran on this workspace
     assert _bwd(lib) == blr.BLR_ERR_STATE
     assert _bwd(lib, gs=1024.0) == blr.BLR_ERR_STATE
+
+
+def _sign(lib, **over):
+    a = dict(x=FAKE, g=FAKE, l=FAKE, gu=FAKE, gv=FAKE, acc=0, M=64, di=128, do=128, r=64, ws=FAKE + 8192,
+             wsb=1 << 40, sws=FAKE, swsb=1 << 40, s=None)
+    a.update(over)
+    return lib.blr_sign_grads(a["x"], a["g"], a["l"], a["gu"], a["gv"], a["acc"], a["M"], a["di"], a["do"], a["r"],
+                              a["ws"], a["wsb"], a["sws"], a["swsb"], a["s"])
+
+
+def test_sign_workspace_bytes(lib):
+    assert lib.blr_sign_workspace_bytes(0, 256, 256, 64) == 0
+    assert lib.blr_sign_workspace_bytes(128, 256, 100, 64) == 0
+    # two rescaled rank-side f16 operands [M][r] plus a header
+    n = lib.blr_sign_workspace_bytes(70, 384, 256, 128)
+    assert 2 * 70 * 128 * 2 <= n < 2 * 70 * 128 * 2 + 2048
+    assert lib.blr_sign_workspace_bytes(71, 384, 256, 128) > n
+    assert lib.blr_sign_workspace_bytes(70, 4096, 4096, 128) == n
+
+
+def test_sign_grads_argument_errors(lib):
+    import binary_rank_linear_gb300 as blr
+    assert _sign(lib, gu=None) == blr.BLR_ERR_ARG
+    assert _sign(lib, sws=None) == blr.BLR_ERR_ARG
+    assert _sign(lib, acc=3) == blr.BLR_ERR_ARG
+    assert _sign(lib, r=48) == blr.BLR_ERR_SHAPE
+    assert _sign(lib, gv=FAKE + 4) == blr.BLR_ERR_ALIGN
+    assert _sign(lib, sws=FAKE + 2) == blr.BLR_ERR_ALIGN
+    assert _sign(lib, wsb=64) == blr.BLR_ERR_WORKSPACE
+    assert _sign(lib, swsb=64) == blr.BLR_ERR_WORKSPACE
+    # no forward/backward ever ran on this workspace
+    assert _sign(lib) == blr.BLR_ERR_STATE
 
 
 def test_pack_argument_errors(lib):
