@@ -166,6 +166,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------ rank aggregation ---
+def max_over_ranks(v: float, device="cpu") -> float:
+    """The largest of every rank's `v` (the job's time is its slowest rank's);
+    `v` itself when no process group is up."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank processes its own batch each step
+    (weak scaling), over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / (ms * 1e-3)
+
+
 # ---------------------------------------------------------- CPU oracle ------
 def cpu_oracle_rate(w, budget_s: float = 12.0, max_reps: int = 50):
     """tokens/s of the CPU f64 oracle (as it stands) on the workload's batch,
@@ -298,10 +317,7 @@ def run_gpu(args, rank, world, local_rank):
         if st:
             raise RuntimeError(f"device status {st:#x}")
 
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dev)
 
     per = {}
     for name, kms in trace:
@@ -329,6 +345,9 @@ def run_gpu(args, rank, world, local_rank):
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json: bf16 burst, f16 assumed equal)" \
         if peak_src == "measured" else "fallback"
     roof["traffic"] = stored_traffic(args.workload, dom)
+
+    sign = measure_sign_grads(blr, sets, g, l, args.steps, tc_peak, M, d_in, d_out, r, dev) \
+        if not args.no_sign else None
 
     # end-to-end: host buffers through the public API, copies inside the timed region
     xh = torch.from_numpy(t["x"]).pin_memory()
@@ -359,12 +378,9 @@ def run_gpu(args, rank, world, local_rank):
     f1.record(stream)
     barrier()
     e2e_ms = f0.elapsed_time(f1)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
-    value = world * M * args.steps / (ms * 1e-3)
+    value = job_tokens_per_s(world, M, args.steps, ms)
     result = {
         "metric": METRIC,
         "value": value,
@@ -392,11 +408,59 @@ def run_gpu(args, rank, world, local_rank):
         "kernels": kernels,
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clk,
-        "e2e": {"value": world * M * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, M, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": 4 * M * (d_in + d_out),
                 "d2h_bytes_per_step": 4 * (M * (d_in + d_out) + d_in + r + d_out)},
     }
+    if sign is not None:
+        result["sign_grads"] = sign
     return result
+
+
+def measure_sign_grads(blr, sets, g, l, steps, tc_peak, M, d_in, d_out, r, dev):
+    """The sign gradients G_U, G_V (blr_sign_grads) after the step: a call of
+    their own, outside the step's time. Each call reads the tape of one of the
+    rotating buffer sets (every set holds a forward+backward by now)."""
+    import torch
+    sws = blr.alloc_sign_workspace(M, d_in, d_out, r, device=dev)
+    gu = torch.empty(d_out, r, device=dev)
+    gv = torch.empty(d_in, r, device=dev)
+    n = len(sets)
+    stream = torch.cuda.current_stream()
+
+    def call(i):
+        s = sets[i % n]
+        blr.sign_grads(s["x"], g, l, gu, gv, s["ws"], sws)
+
+    for i in range(max(3, n)):
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    blr.trace_begin(capacity=4 * steps)
+    for i in range(steps):
+        call(i)
+    torch.cuda.synchronize()
+    per = {}
+    for name, kms in blr.trace_end():
+        per.setdefault(name, []).append(kms)
+    flops = 2.0 * M * r * (d_in + d_out)
+    gem = per.get("sign_gemm", [float("nan")])
+    g_ms = sum(gem) / len(gem)
+    return {
+        "what": "G_U = diag(h) dy^T a diag(l), G_V = diag(g) x^T db diag(l) after the step (not in its time)",
+        "us_per_call": ms * 1e3,
+        "tflops": flops / (ms * 1e-3) / 1e12,
+        "kernels": {k: {"avg_us": 1e3 * sum(v) / len(v)} for k, v in per.items()},
+        "roofline": {"bound": "tensor", "kernel": "sign_gemm", "achieved": flops / (g_ms * 1e-3) / 1e12,
+                     "peak": tc_peak, "unit": "TFLOP/s", "frac": flops / (g_ms * 1e-3) / 1e12 / tc_peak},
+        "gpu_launches_per_call": len(sum(per.values(), [])) / steps,
+    }
 
 
 def main():
@@ -407,6 +471,7 @@ def main():
     ap.add_argument("--impl", default="blr", choices=["blr", "reference"])
     ap.add_argument("--workload", default="small")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sign", action="store_true", help="skip the sign-gradient measurement")
     ap.add_argument("--small-path", default="general", choices=["general", "fused"],
                     help="kernels for small problems: stand-alone (default) or the fused cooperative pair")
     args = ap.parse_args()
