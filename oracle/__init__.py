@@ -1,5 +1,6 @@
 """CPU f64 oracle of the blr layer: test infrastructure only (see blr_oracle)."""
 from .blr_oracle import (  # noqa: F401
+    adam_step,
     backward,
     backward_sampled,
     forward,

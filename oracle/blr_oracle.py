@@ -19,7 +19,10 @@ function below cites the part of that page it restates:
   vectorises, and the normwise relative error metric;
 * ``blr_backward``'s documentation and the test helper ``host_sign_grads``:
   the sign gradients G_U = diag(h) dy^T a diag(l) and
-  G_V = diag(g) x^T b diag(l), b the backward's db.
+  G_V = diag(g) x^T b diag(l), b the backward's db;
+* the WGSL ``adam`` kernel and its Rust wrapper ``adam``: one Adam step (no
+  weight decay) with an optional frozen-entry mask, a gradient multiplier and
+  optional steps relative to the parameter's magnitude.
 
 Precision: inputs are f32 on the page; they are widened to f64 here and every
 step runs in f64. There is no staging, no f16 and no scaling in the oracle: the
@@ -44,6 +47,8 @@ __all__ = [
     "backward",
     "backward_sampled",
     "sign_grads",
+    "sign_grads_sampled",
+    "adam_step",
     "rel_err",
 ]
 
@@ -232,6 +237,37 @@ def sign_grads_sampled(x, dy, bits_u, bits_v, g, l, h, rows_u, rows_v) -> dict:
     gu = h[rows_u, None] * np.matmul(dy[:, rows_u].T, a) * l[None, :]
     gv = g[rows_v, None] * np.matmul(x[:, rows_v].T, b) * l[None, :]
     return {"gu": gu, "gv": gv}
+
+
+def adam_step(w, grad, m1, m2, lr, step, b1, b2, eps, mask=None, gmul=1.0, rel=0.0) -> dict:
+    """One Adam update, elementwise, in f64.
+
+    train_mm.rs, WGSL ``adam`` kernel and its wrapper ``adam``. Entries whose
+    mask value is exactly 0 are frozen (nothing changes). For every other
+    entry, with t = step (1-based):
+        gr = grad * gmul
+        m1 <- b1 m1 + (1 - b1) gr
+        m2 <- b2 m2 + (1 - b2) gr^2
+        st = lr * (m1 / (1 - b1^t)) / (sqrt(m2 / (1 - b2^t)) + eps)
+        w  <- w - st * max(|w|, rel)   if rel > 0 (relative step, floored)
+        w  <- w - st                   otherwise
+    Returns a dict with the new w, m1, m2 (f64).
+    """
+    w, grad, m1, m2 = _f64(w), _f64(grad), _f64(m1), _f64(m2)
+    t = float(step)
+    gr = grad * float(gmul)
+    n1 = b1 * m1 + (1.0 - b1) * gr
+    n2 = b2 * m2 + (1.0 - b2) * gr * gr
+    mh = n1 / (1.0 - b1 ** t)
+    vh = n2 / (1.0 - b2 ** t)
+    st = lr * mh / (np.sqrt(vh) + eps)
+    nw = w - st * np.maximum(np.abs(w), rel) if rel > 0 else w - st
+    if mask is not None:
+        live = _f64(mask) != 0.0
+        nw = np.where(live, nw, w)
+        n1 = np.where(live, n1, m1)
+        n2 = np.where(live, n2, m2)
+    return {"w": nw, "m1": n1, "m2": n2}
 
 
 def rel_err(got, want) -> float:

@@ -423,3 +423,102 @@ def test_sign_grads_sampled_rows():
     smp = oracle.sign_grads_sampled(t["x"], t["dy"], t["bu"], t["bv"], t["g"], t["l"], t["h"], ru, rv)
     assert np.allclose(smp["gu"], full["gu"][ru], rtol=1e-13, atol=1e-13)
     assert np.allclose(smp["gv"], full["gv"][rv], rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ Adam ---
+def _adam_inputs(seed, n=257):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal(n), rng.standard_normal(n) * 1e-2,
+            rng.standard_normal(n) * 1e-3, np.abs(rng.standard_normal(n)) * 1e-4)
+
+
+def test_adam_matches_torch():
+    """No mask, gmul 1, absolute steps: the textbook Adam (torch.optim.Adam, no
+    weight decay, eps added to the bias-corrected root), run for several steps
+    on the same gradients in f64."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    n, lr, b1, b2, eps = 300, 3e-3, 0.9, 0.999, 1e-8
+    w0 = rng.standard_normal(n)
+    grads = [rng.standard_normal(n) * 10.0 ** rng.uniform(-4, 0) for _ in range(6)]
+    p = torch.nn.Parameter(torch.tensor(w0, dtype=torch.float64))
+    opt = torch.optim.Adam([p], lr=lr, betas=(b1, b2), eps=eps)
+    w, m1, m2 = w0.copy(), np.zeros(n), np.zeros(n)
+    for step, gvec in enumerate(grads, start=1):
+        p.grad = torch.tensor(gvec, dtype=torch.float64)
+        opt.step()
+        o = oracle.adam_step(w, gvec, m1, m2, lr, step, b1, b2, eps)
+        w, m1, m2 = o["w"], o["m1"], o["m2"]
+        assert np.allclose(w, p.detach().numpy(), rtol=1e-13, atol=1e-15), step
+        st = opt.state[p]
+        assert np.allclose(m1, st["exp_avg"].numpy(), rtol=1e-13, atol=0)
+        assert np.allclose(m2, st["exp_avg_sq"].numpy(), rtol=1e-13, atol=0)
+
+
+def test_adam_first_step_closed_form():
+    """From zero moments the first bias-corrected moments are gr and gr^2, so the
+    step is lr * gr / (|gr| + eps), for any betas."""
+    w, g, _, _ = _adam_inputs(3)
+    for b1, b2, gmul in ((0.9, 0.999, 1.0), (0.5, 0.9, 0.25), (0.0, 0.0, 4.0)):
+        o = oracle.adam_step(w, g, np.zeros_like(w), np.zeros_like(w), 1e-2, 1, b1, b2, 1e-6, gmul=gmul)
+        gr = g * gmul
+        assert np.allclose(o["w"], w - 1e-2 * gr / (np.abs(gr) + 1e-6), rtol=1e-14, atol=1e-16)
+        assert np.allclose(o["m1"], (1 - b1) * gr, rtol=1e-15, atol=0)
+        assert np.allclose(o["m2"], (1 - b2) * gr * gr, rtol=1e-15, atol=0)
+
+
+def test_adam_constant_gradient_closed_form():
+    """A constant gradient c from zero moments: both bias-corrected moments are
+    exactly c and c^2 at every step, so every step moves by lr*c/(|c|+eps)."""
+    rng = np.random.default_rng(4)
+    c = rng.standard_normal(50)
+    w0 = rng.standard_normal(50)
+    w, m1, m2 = w0.copy(), np.zeros(50), np.zeros(50)
+    for step in range(1, 8):
+        o = oracle.adam_step(w, c, m1, m2, 1e-3, step, 0.8, 0.95, 1e-7)
+        w, m1, m2 = o["w"], o["m1"], o["m2"]
+        assert np.allclose(w, w0 - step * 1e-3 * c / (np.abs(c) + 1e-7), rtol=1e-12, atol=1e-14)
+
+
+def test_adam_mask_and_relative_step():
+    """Mask 0 freezes an entry (w and both moments); relative steps equal the
+    absolute step times max(|w|, floor)."""
+    w, g, m1, m2 = _adam_inputs(5)
+    mask = (np.arange(w.size) % 3 != 0).astype(np.float64)
+    args = (1e-3, 5, 0.9, 0.99, 1e-8)
+    full = oracle.adam_step(w, g, m1, m2, *args)
+    msk = oracle.adam_step(w, g, m1, m2, *args, mask=mask)
+    live = mask != 0
+    for k, before in (("w", w), ("m1", m1), ("m2", m2)):
+        assert np.array_equal(msk[k][~live], before[~live])
+        assert np.array_equal(msk[k][live], full[k][live])
+    st = w - full["w"]
+    relw = oracle.adam_step(w, g, m1, m2, *args, rel=0.5)["w"]
+    # both differences cancel against |w| ~ 1, so about 12 digits survive
+    assert np.allclose(w - relw, st * np.maximum(np.abs(w), 0.5), rtol=1e-9, atol=1e-16)
+
+
+@pytest.mark.parametrize("mutant", ["no_bias_correction", "eps_inside_sqrt", "mask_ignored"])
+def test_planted_adam_mistakes_are_caught(mutant, monkeypatch):
+    real = oracle.adam_step
+
+    def broken(w, grad, m1, m2, lr, step, b1, b2, eps, mask=None, gmul=1.0, rel=0.0):
+        if mutant == "no_bias_correction" and step > 1:
+            o = real(w, grad, m1, m2, lr, 1, 0.0, 0.0, eps, mask=mask, gmul=gmul, rel=rel)
+            o["m1"], o["m2"] = real(w, grad, m1, m2, lr, step, b1, b2, eps)["m1"], real(
+                w, grad, m1, m2, lr, step, b1, b2, eps)["m2"]
+            return o
+        if mutant == "eps_inside_sqrt":
+            o = real(w, grad, m1, m2, lr, step, b1, b2, 0.0, mask=mask, gmul=gmul, rel=rel)
+            n1 = b1 * np.asarray(m1) + (1 - b1) * np.asarray(grad) * gmul
+            n2 = b2 * np.asarray(m2) + (1 - b2) * (np.asarray(grad) * gmul) ** 2
+            st = lr * (n1 / (1 - b1 ** step)) / np.sqrt(n2 / (1 - b2 ** step) + eps)
+            o["w"] = np.asarray(w, np.float64) - st
+            return o
+        return real(w, grad, m1, m2, lr, step, b1, b2, eps, mask=None, gmul=gmul, rel=rel)
+
+    monkeypatch.setattr(oracle, "adam_step", broken)
+    with pytest.raises(AssertionError):
+        test_adam_matches_torch()
+        test_adam_first_step_closed_form()
+        test_adam_mask_and_relative_step()
