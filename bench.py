@@ -348,6 +348,7 @@ def run_gpu(args, rank, world, local_rank):
 
     sign = measure_sign_grads(blr, sets, g, l, args.steps, tc_peak, M, d_in, d_out, r, dev) \
         if not args.no_sign else None
+    adam = measure_adam(blr, torch.cat([dg, dl, dh]), args.steps, hbm_peak, dev)
 
     # end-to-end: host buffers through the public API, copies inside the timed region
     xh = torch.from_numpy(t["x"]).pin_memory()
@@ -414,7 +415,50 @@ def run_gpu(args, rank, world, local_rank):
     }
     if sign is not None:
         result["sign_grads"] = sign
+    result["adam"] = adam
     return result
+
+
+def measure_adam(blr, grad, steps, hbm_peak, dev):
+    """One Adam step (blr_adam) over the layer's vectors g | l | h as one
+    contiguous array, with this step's dg | dl | dh as the gradient; a call of
+    its own after the step."""
+    import torch
+    n = grad.numel()
+    w = torch.ones(n, device=dev)
+    m1 = torch.zeros(n, device=dev)
+    m2 = torch.zeros(n, device=dev)
+    for i in range(3):
+        blr.adam(w, grad, m1, m2, step=i + 1, lr=1e-4)
+    us = 1e3 * time_queued(lambda i: blr.adam(w, grad, m1, m2, step=i + 4, lr=1e-4), steps)
+    by = 28.0 * n  # w, grad, m1, m2 read; w, m1, m2 written (f32)
+    return {"what": "Adam step of g | l | h (d_in + r + d_out parameters) after the step (not in its time)",
+            "n": n, "us_per_call": us,
+            "roofline": {"bound": "hbm", "achieved": by / (us * 1e-6) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": by / (us * 1e-6) / 1e9 / hbm_peak},
+            "note": "a few hundred KB per call: bound by launch and latency, not bandwidth"}
+
+
+def time_queued(fn, steps):
+    """Device milliseconds per call of `fn` (which queues GPU work on the
+    current stream): all calls are queued behind a GPU sleep that outlasts
+    their host-side launch cost, then bracketed by two CUDA events, so host
+    launch latency stays outside the measurement."""
+    import torch
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    fn(0)
+    torch.cuda.synchronize()
+    host_s = time.perf_counter() - t0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(min(4e9, 2.5e9 * host_s * (steps + 2))))
+    e0.record(stream)
+    for i in range(steps):
+        fn(i + 1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
 
 
 def measure_sign_grads(blr, sets, g, l, steps, tc_peak, M, d_in, d_out, r, dev):
@@ -426,7 +470,6 @@ def measure_sign_grads(blr, sets, g, l, steps, tc_peak, M, d_in, d_out, r, dev):
     gu = torch.empty(d_out, r, device=dev)
     gv = torch.empty(d_in, r, device=dev)
     n = len(sets)
-    stream = torch.cuda.current_stream()
 
     def call(i):
         s = sets[i % n]
@@ -434,18 +477,9 @@ def measure_sign_grads(blr, sets, g, l, steps, tc_peak, M, d_in, d_out, r, dev):
 
     for i in range(max(3, n)):
         call(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(steps):
-        call(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    ms = time_queued(call, steps)
     blr.trace_begin(capacity=4 * steps)
-    for i in range(steps):
-        call(i)
-    torch.cuda.synchronize()
+    time_queued(call, steps)  # the trace brackets each kernel of the queued calls
     per = {}
     for name, kms in blr.trace_end():
         per.setdefault(name, []).append(kms)
@@ -459,7 +493,7 @@ def measure_sign_grads(blr, sets, g, l, steps, tc_peak, M, d_in, d_out, r, dev):
         "kernels": {k: {"avg_us": 1e3 * sum(v) / len(v)} for k, v in per.items()},
         "roofline": {"bound": "tensor", "kernel": "sign_gemm", "achieved": flops / (g_ms * 1e-3) / 1e12,
                      "peak": tc_peak, "unit": "TFLOP/s", "frac": flops / (g_ms * 1e-3) / 1e12 / tc_peak},
-        "gpu_launches_per_call": len(sum(per.values(), [])) / steps,
+        "gpu_launches_per_call": len(sum(per.values(), [])) / (steps + 1),
     }
 
 

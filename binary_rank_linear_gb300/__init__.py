@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     BLR_ERR_WORKSPACE,
     BLR_OK,
     BlrError,
+    adam,
     alloc_sign_workspace,
     alloc_workspace,
     backward,

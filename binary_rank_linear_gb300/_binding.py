@@ -57,13 +57,14 @@ def load() -> ctypes.CDLL:
     lib.blr_sign_workspace_bytes.argtypes = [I, I, I, I]
     lib.blr_sign_workspace_bytes.restype = Z
     lib.blr_sign_grads.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, Z, P]
+    lib.blr_adam.argtypes = [P, P, P, P, P, I, I, F, F, F, F, F, F, P]
     lib.blr_check_status.argtypes = [P, Z, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.blr_status_string.argtypes = [I]
     lib.blr_status_string.restype = ctypes.c_char_p
     lib.blr_trace_begin.argtypes = [I]
     lib.blr_trace_read.argtypes = [I, ctypes.POINTER(ctypes.c_float)]
     lib.blr_trace_read.restype = ctypes.c_char_p
-    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_sign_grads", "blr_check_status",
+    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_sign_grads", "blr_adam", "blr_check_status",
               "blr_trace_begin", "blr_trace_end", "blr_trace_count"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -191,6 +192,19 @@ def sign_grads(x, g, l, gu, gv, ws, sws, accumulate: bool = False, stream=None):
         _ptr(ws, "ws", torch.uint8), ws.numel(), _ptr(sws, "sws", torch.uint8), sws.numel(), _stream(stream))
     _check(code, "blr_sign_grads")
     return gu, gv
+
+
+def adam(w, grad, m1, m2, step: int, lr: float, b1: float = 0.9, b2: float = 0.999, eps: float = 1e-8,
+         mask=None, gmul: float = 1.0, rel: float = 0.0, stream=None):
+    """One Adam step in place on w, m1, m2 (f32 [n] CUDA tensors); mask 0 freezes an entry."""
+    n = w.numel()
+    shape = tuple(w.shape)
+    code = load().blr_adam(
+        _ptr(w, "w", torch.float32), _ptr(grad, "grad", torch.float32, shape), _ptr(m1, "m1", torch.float32, shape),
+        _ptr(m2, "m2", torch.float32, shape), _ptr(mask, "mask", torch.float32, shape) if mask is not None else None,
+        n, int(step), float(lr), float(b1), float(b2), float(eps), float(gmul), float(rel), _stream(stream))
+    _check(code, "blr_adam")
+    return w
 
 
 def check_status(ws: torch.Tensor, stream=None) -> int:

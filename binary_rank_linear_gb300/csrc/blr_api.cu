@@ -630,6 +630,40 @@ int blr_sign_grads(const float *x, const float *g, const float *l, float *gu, fl
     return launch_sign_gemm(gl, s) == cudaSuccess ? BLR_OK : BLR_ERR_CUDA;
 }
 
+int blr_adam(float *w, const float *grad, float *m1, float *m2, const float *mask, int n, int step, float lr,
+             float b1, float b2, float eps, float gmul, float rel, blr_stream_t stream) {
+    if (!w || !grad || !m1 || !m2) return BLR_ERR_ARG;
+    if (n < 0) return BLR_ERR_SHAPE;
+    if (step < 1 || !std::isfinite(lr) || !std::isfinite(gmul) || std::isnan(rel) || !std::isfinite(eps) ||
+        eps < 0.0f || !(b1 >= 0.0f && b1 < 1.0f) || !(b2 >= 0.0f && b2 < 1.0f))
+        return BLR_ERR_ARG;
+    const void *ptrs[] = {w, grad, m1, m2, mask};
+    for (const void *p : ptrs)
+        if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0) return BLR_ERR_ALIGN;
+    if (n == 0) return BLR_OK;
+    int sms;
+    int st = device_info(&sms);
+    if (st != BLR_OK) return st;
+    if (fault_injected("adam")) return BLR_ERR_CUDA;
+    AdamArgs a{};
+    a.w = w;
+    a.grad = grad;
+    a.m1 = m1;
+    a.m2 = m2;
+    a.mask = mask;
+    a.n = n;
+    a.lr = lr;
+    a.b1 = b1;
+    a.b2 = b2;
+    a.eps = eps;
+    a.gmul = gmul;
+    a.rel = rel;
+    a.bc1 = (float)(1.0 - std::pow((double)b1, (double)step));
+    a.bc2 = (float)(1.0 - std::pow((double)b2, (double)step));
+    if (!(a.bc1 > 0.0f) || !(a.bc2 > 0.0f)) return BLR_ERR_ARG;
+    return launch_adam(a, sms, (cudaStream_t)stream) == cudaSuccess ? BLR_OK : BLR_ERR_CUDA;
+}
+
 int blr_check_status(const void *ws, size_t ws_bytes, blr_stream_t stream, uint32_t *device_code) {
     if (!ws || ws_bytes < 256) return BLR_ERR_ARG;
     uint32_t code = 0;

@@ -227,4 +227,16 @@ struct SignGemmLaunch {
 };
 cudaError_t launch_sign_gemm(const SignGemmLaunch &L, cudaStream_t s);
 
+// ---- Adam (blr_adam.cu) -------------------------------------------------------
+struct AdamArgs {
+    float *w;             // [n] parameters, updated
+    const float *grad;    // [n]
+    float *m1, *m2;       // [n] first and second moments, updated
+    const float *mask;    // [n] or null; 0 = frozen entry
+    long long n;
+    float lr, b1, b2, eps, gmul, rel;
+    float bc1, bc2;       // 1 - b1^t, 1 - b2^t
+};
+cudaError_t launch_adam(const AdamArgs &a, int sms, cudaStream_t s);
+
 }  // namespace blr

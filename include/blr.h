@@ -182,6 +182,28 @@ BLR_API int blr_sign_grads(const float *x, const float *g, const float *l,
                            const void *ws, size_t ws_bytes, void *sws, size_t sws_bytes,
                            blr_stream_t stream);
 
+/* One Adam step over n parameters (train_mm.rs, WGSL adam kernel and its
+ * wrapper adam), meant for the layer's vectors g, l and h (for instance kept
+ * as one contiguous [d_in + r + d_out] array with its gradient dg | dl | dh):
+ *
+ *     gr = grad * gmul
+ *     m1 = b1 m1 + (1 - b1) gr,   m2 = b2 m2 + (1 - b2) gr^2
+ *     st = lr (m1 / (1 - b1^step)) / (sqrt(m2 / (1 - b2^step)) + eps)
+ *     w -= st * max(|w|, rel)   if rel > 0 (steps relative to |w|, floored at rel)
+ *     w -= st                   otherwise
+ *
+ * f32 arithmetic as on the page; the bias corrections are formed on the host.
+ *  - w, m1, m2 [n] f32 device, updated in place; grad [n] f32 device;
+ *    mask [n] f32 device or NULL: entries with mask exactly 0 are frozen (w,
+ *    m1 and m2 unchanged). No weight decay. step >= 1 counts updates from 1.
+ *  - Pointers need 4-byte alignment; n = 0 is a no-op.
+ * Errors: BLR_ERR_ARG (null pointer, step < 1, b1 or b2 outside [0, 1), eps
+ *   negative or not finite, lr or gmul not finite, rel NaN), BLR_ERR_SHAPE
+ *   (n < 0), BLR_ERR_ALIGN, BLR_ERR_UNSUPPORTED_DEVICE, BLR_ERR_CUDA. */
+BLR_API int blr_adam(float *w, const float *grad, float *m1, float *m2, const float *mask,
+                     int n, int step, float lr, float b1, float b2, float eps,
+                     float gmul, float rel, blr_stream_t stream);
+
 /* Synchronises `stream` and reads the workspace's device status word.
  * Returns BLR_OK if no kernel recorded a failure since the last blr_forward
  * on this workspace, BLR_ERR_DEVICE_CHECK if one did (the code is written to

@@ -137,6 +137,29 @@ def test_sign_grads_argument_errors(lib):
     assert _sign(lib) == blr.BLR_ERR_STATE
 
 
+def _adam(lib, **over):
+    a = dict(w=FAKE, g=FAKE, m1=FAKE, m2=FAKE, mask=None, n=16, step=1, lr=1e-3, b1=0.9, b2=0.999, eps=1e-8,
+             gmul=1.0, rel=0.0, s=None)
+    a.update(over)
+    return lib.blr_adam(a["w"], a["g"], a["m1"], a["m2"], a["mask"], a["n"], a["step"], a["lr"], a["b1"], a["b2"],
+                        a["eps"], a["gmul"], a["rel"], a["s"])
+
+
+def test_adam_argument_errors(lib):
+    import binary_rank_linear_gb300 as blr
+    assert _adam(lib, m2=None) == blr.BLR_ERR_ARG
+    assert _adam(lib, step=0) == blr.BLR_ERR_ARG
+    assert _adam(lib, b1=1.0) == blr.BLR_ERR_ARG
+    assert _adam(lib, b2=-0.1) == blr.BLR_ERR_ARG
+    assert _adam(lib, eps=-1e-8) == blr.BLR_ERR_ARG
+    assert _adam(lib, lr=float("inf")) == blr.BLR_ERR_ARG
+    assert _adam(lib, rel=float("nan")) == blr.BLR_ERR_ARG
+    assert _adam(lib, n=-1) == blr.BLR_ERR_SHAPE
+    assert _adam(lib, w=FAKE + 2) == blr.BLR_ERR_ALIGN
+    assert _adam(lib, mask=FAKE + 1) == blr.BLR_ERR_ALIGN
+    assert _adam(lib, n=0) == blr.BLR_OK  # nothing to do, nothing queued
+
+
 def test_pack_argument_errors(lib):
     import binary_rank_linear_gb300 as blr
     assert lib.blr_pack_signs(None, FAKE, 4, 64, None) == blr.BLR_ERR_ARG
