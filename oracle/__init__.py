@@ -5,6 +5,7 @@ from .blr_oracle import (  # noqa: F401
     backward_sampled,
     forward,
     pack_signs,
+    plane_linear,
     rel_err,
     sign_grads,
     sign_grads_sampled,

@@ -22,7 +22,9 @@ function below cites the part of that page it restates:
   G_V = diag(g) x^T b diag(l), b the backward's db;
 * the WGSL ``adam`` kernel and its Rust wrapper ``adam``: one Adam step (no
   weight decay) with an optional frozen-entry mask, a gradient multiplier and
-  optional steps relative to the parameter's magnitude.
+  optional steps relative to the parameter's magnitude;
+* ``plane_linear`` and ``mm``: a dense frozen linear y = x . plane^T through
+  the f16 staging, or its transpose (input gradient) y = x . plane.
 
 Precision: inputs are f32 on the page; they are widened to f64 here and every
 step runs in f64. There is no staging, no f16 and no scaling in the oracle: the
@@ -49,6 +51,7 @@ __all__ = [
     "sign_grads",
     "sign_grads_sampled",
     "adam_step",
+    "plane_linear",
     "rel_err",
 ]
 
@@ -268,6 +271,21 @@ def adam_step(w, grad, m1, m2, lr, step, b1, b2, eps, mask=None, gmul=1.0, rel=0
         n1 = np.where(live, n1, m1)
         n2 = np.where(live, n2, m2)
     return {"w": nw, "m1": n1, "m2": n2}
+
+
+def plane_linear(x, plane, transpose=False, y_prior=None) -> np.ndarray:
+    """A dense frozen linear in f64.
+
+    train_mm.rs, ``plane_linear`` (staging ``cvt`` of x under ``scale``, then
+    ``mm`` with output scale 1/scale) and ``mm`` (out[m][n] = act[m][k] .
+    plane[n][k]^T): y = (x s) plane^T / s = x plane^T, the scale cancelling
+    exactly; with ``transpose`` (the input gradient through the same plane),
+    y = x plane. ``plane`` holds f16 values (given as any float array).
+    ``y_prior`` adds the result to it (accumulate mode).
+    """
+    x, p = _f64(x), _f64(plane)
+    y = np.matmul(x, p) if transpose else np.matmul(x, p.T)
+    return y if y_prior is None else _f64(y_prior) + y
 
 
 def rel_err(got, want) -> float:

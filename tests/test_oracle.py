@@ -522,3 +522,56 @@ def test_planted_adam_mistakes_are_caught(mutant, monkeypatch):
         test_adam_matches_torch()
         test_adam_first_step_closed_form()
         test_adam_mask_and_relative_step()
+
+
+# ---------------------------------------------------------- plane_linear ---
+def _plane_case(seed, ntok=5, n=7, k=6):
+    rng = np.random.default_rng(seed)
+    plane = rng.standard_normal((n, k)).astype(np.float16)
+    return rng.standard_normal((ntok, k)), rng.standard_normal((ntok, n)), plane
+
+
+def test_plane_linear_loops():
+    """y[t][i] = sum_j x[t][j] plane[i][j] and its transpose, as plain loops."""
+    x, u, p = _plane_case(1)
+    y = oracle.plane_linear(x, p)
+    yt = oracle.plane_linear(u, p, transpose=True)
+    for t in range(x.shape[0]):
+        for i in range(p.shape[0]):
+            assert math.isclose(y[t, i], sum(x[t, j] * float(p[i, j]) for j in range(p.shape[1])),
+                                rel_tol=1e-13, abs_tol=1e-13)
+        for j in range(p.shape[1]):
+            assert math.isclose(yt[t, j], sum(u[t, i] * float(p[i, j]) for i in range(p.shape[0])),
+                                rel_tol=1e-13, abs_tol=1e-13)
+
+
+def test_plane_linear_adjoint_and_library():
+    """<x P^T, u> = <x, u P> (the transpose is the adjoint, which pins which
+    index is contracted), and the forward equals torch's linear in f64."""
+    torch = pytest.importorskip("torch")
+    x, u, p = _plane_case(2, ntok=9, n=13, k=11)
+    y = oracle.plane_linear(x, p)
+    yt = oracle.plane_linear(u, p, transpose=True)
+    assert math.isclose(float(np.sum(y * u)), float(np.sum(x * yt)), rel_tol=1e-12)
+    lib = torch.nn.functional.linear(torch.tensor(x), torch.tensor(p.astype(np.float64))).numpy()
+    assert np.allclose(y, lib, rtol=1e-13, atol=1e-13)
+    prior = np.ones_like(y)
+    assert np.allclose(oracle.plane_linear(x, p, y_prior=prior), y + 1.0, rtol=1e-15, atol=1e-15)
+
+
+@pytest.mark.parametrize("mutant", ["no_transpose", "transposed_plane"])
+def test_planted_plane_mistakes_are_caught(mutant, monkeypatch):
+    real = oracle.plane_linear
+
+    def broken(x, plane, transpose=False, y_prior=None):
+        if mutant == "no_transpose" and transpose:
+            return real(x, np.asarray(plane).T, transpose=False, y_prior=y_prior)[:, ::-1]
+        if mutant == "transposed_plane":
+            q = np.asarray(plane, np.float64).copy()
+            q[0, 1], q[1, 0] = q[1, 0], q[0, 1]
+            return real(x, q, transpose=transpose, y_prior=y_prior)
+        return real(x, plane, transpose=transpose, y_prior=y_prior)
+
+    monkeypatch.setattr(oracle, "plane_linear", broken)
+    with pytest.raises(AssertionError):
+        test_plane_linear_loops()
