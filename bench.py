@@ -349,6 +349,7 @@ def run_gpu(args, rank, world, local_rank):
     sign = measure_sign_grads(blr, sets, g, l, args.steps, tc_peak, M, d_in, d_out, r, dev) \
         if not args.no_sign else None
     adam = measure_adam(blr, torch.cat([dg, dl, dh]), args.steps, hbm_peak, dev)
+    plane = measure_plane(blr, sets[0], args.steps, tc_peak, M, d_in, d_out, dev) if not args.no_plane else None
 
     # end-to-end: host buffers through the public API, copies inside the timed region
     xh = torch.from_numpy(t["x"]).pin_memory()
@@ -416,7 +417,40 @@ def run_gpu(args, rank, world, local_rank):
     if sign is not None:
         result["sign_grads"] = sign
     result["adam"] = adam
+    if plane is not None:
+        result["plane_linear"] = plane
     return result
+
+
+def measure_plane(blr, s, steps, tc_peak, M, d_in, d_out, dev):
+    """plane_linear (blr_plane_linear) on the workload's shape as a dense
+    frozen f16 linear: y = x P^T with P [d_out][d_in], and its transpose
+    dx = dy P; calls of their own after the step (they reuse the step's x, y,
+    dy, dx buffers)."""
+    import torch
+    gen = torch.Generator(device=dev).manual_seed(5)
+    P = (torch.randn(d_out, d_in, device=dev, generator=gen) * 0.02).half()
+    ws = blr.alloc_plane_workspace(M, d_out, d_in, device=dev)
+    flops = 2.0 * M * d_in * d_out
+    out = {"what": "dense frozen f16 linear on the workload's shape (not in the step's time)"}
+    for name, x, y, tr in (("forward", s["x"], s["y"], False), ("transpose", s["dy"], s["dx"], True)):
+        def call(i, x=x, y=y, tr=tr):
+            blr.plane_linear(x, P, y, ws, transpose=tr)
+        for i in range(3):
+            call(i)
+        blr.trace_begin(capacity=4 * steps)
+        ms = time_queued(call, steps)
+        per = {}
+        for kname, kms in blr.trace_end():
+            per.setdefault(kname, []).append(kms)
+        gem = per.get("plane_gemm", [float("nan")])
+        g_ms = sum(gem) / len(gem)
+        out[name] = {"us_per_call": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12,
+                     "kernels": {k: {"avg_us": 1e3 * sum(v) / len(v)} for k, v in per.items()},
+                     "roofline": {"bound": "tensor", "kernel": "plane_gemm",
+                                  "achieved": flops / (g_ms * 1e-3) / 1e12, "peak": tc_peak, "unit": "TFLOP/s",
+                                  "frac": flops / (g_ms * 1e-3) / 1e12 / tc_peak}}
+    return out
 
 
 def measure_adam(blr, grad, steps, hbm_peak, dev):
@@ -506,6 +540,7 @@ def main():
     ap.add_argument("--workload", default="small")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sign", action="store_true", help="skip the sign-gradient measurement")
+    ap.add_argument("--no-plane", action="store_true", help="skip the plane_linear measurement")
     ap.add_argument("--small-path", default="general", choices=["general", "fused"],
                     help="kernels for small problems: stand-alone (default) or the fused cooperative pair")
     args = ap.parse_args()

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     BLR_OK,
     BlrError,
     adam,
+    alloc_plane_workspace,
     alloc_sign_workspace,
     alloc_workspace,
     backward,
@@ -24,6 +25,8 @@ from ._binding import (  # noqa: F401
     forward_noalloc,
     load,
     pack_signs,
+    plane_linear,
+    plane_workspace_bytes,
     sign_grads,
     sign_workspace_bytes,
     trace_begin,

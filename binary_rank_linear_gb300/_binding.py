@@ -58,13 +58,16 @@ def load() -> ctypes.CDLL:
     lib.blr_sign_workspace_bytes.restype = Z
     lib.blr_sign_grads.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, Z, P]
     lib.blr_adam.argtypes = [P, P, P, P, P, I, I, F, F, F, F, F, F, P]
+    lib.blr_plane_workspace_bytes.argtypes = [I, I, I]
+    lib.blr_plane_workspace_bytes.restype = Z
+    lib.blr_plane_linear.argtypes = [P, P, P, I, I, F, I, I, I, P, Z, P]
     lib.blr_check_status.argtypes = [P, Z, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.blr_status_string.argtypes = [I]
     lib.blr_status_string.restype = ctypes.c_char_p
     lib.blr_trace_begin.argtypes = [I]
     lib.blr_trace_read.argtypes = [I, ctypes.POINTER(ctypes.c_float)]
     lib.blr_trace_read.restype = ctypes.c_char_p
-    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_sign_grads", "blr_adam", "blr_check_status",
+    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_sign_grads", "blr_adam", "blr_plane_linear", "blr_check_status",
               "blr_trace_begin", "blr_trace_end", "blr_trace_count"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -192,6 +195,31 @@ def sign_grads(x, g, l, gu, gv, ws, sws, accumulate: bool = False, stream=None):
         _ptr(ws, "ws", torch.uint8), ws.numel(), _ptr(sws, "sws", torch.uint8), sws.numel(), _stream(stream))
     _check(code, "blr_sign_grads")
     return gu, gv
+
+
+def plane_workspace_bytes(ntok: int, n: int, k: int) -> int:
+    return int(load().blr_plane_workspace_bytes(ntok, n, k))
+
+
+def alloc_plane_workspace(ntok: int, n: int, k: int, device=None) -> torch.Tensor:
+    nb = plane_workspace_bytes(ntok, n, k)
+    if nb == 0:
+        raise BlrError(BLR_ERR_SHAPE, "plane_workspace_bytes")
+    return torch.empty(nb, dtype=torch.uint8, device=device or "cuda")
+
+
+def plane_linear(x, plane, y, ws, transpose: bool = False, accumulate: bool = False, scale: float = 1.0,
+                 stream=None) -> torch.Tensor:
+    """y (+)= x plane^T (x [ntok][k]) or, with transpose, y (+)= x plane (x [ntok][n]); plane [n][k] f16."""
+    n, k = plane.shape
+    ntok = x.shape[0]
+    kin, nout = (n, k) if transpose else (k, n)
+    code = load().blr_plane_linear(
+        _ptr(x, "x", torch.float32, (ntok, kin)), _ptr(plane, "plane", torch.float16, (n, k)),
+        _ptr(y, "y", torch.float32, (ntok, nout)), int(bool(transpose)), int(bool(accumulate)), float(scale),
+        ntok, n, k, _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check(code, "blr_plane_linear")
+    return y
 
 
 def adam(w, grad, m1, m2, step: int, lr: float, b1: float = 0.9, b2: float = 0.999, eps: float = 1e-8,

@@ -240,6 +240,11 @@ void mark_backward_done(const void *ws, float gscale, int stage_blocks) {
     it->second.stage_blocks = stage_blocks;
 }
 
+bool plane_shape_ok(int ntok, int n, int k) {
+    auto dim_ok = [](int d) { return d >= 32 && d <= 65536 && d % 32 == 0; };
+    return ntok >= 1 && ntok <= (1 << 28) && dim_ok(n) && dim_ok(k);
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool fault_injected(const char *site) {
@@ -589,13 +594,14 @@ int blr_sign_grads(const float *x, const float *g, const float *l, float *gu, fl
     const uint16_t *al16 = reinterpret_cast<const uint16_t *>(w + L.al16);
     const uint16_t *db16 = reinterpret_cast<const uint16_t *>(w + L.db16);
 
-    SignGemmLaunch gl{};
+    DenseGemmLaunch gl{};
     gl.F[0] = d_out;
     gl.F[1] = d_in;
     gl.out[0] = gu;
     gl.out[1] = gv;
-    gl.M = M;
-    gl.r = r;
+    gl.R = r;
+    gl.K = M;  // the products sum over tokens
+    gl.a_mn = gl.b_mn = true;
     gl.accumulate = accumulate;
     gl.status = reinterpret_cast<uint32_t *>(w + L.header);
     gl.sms = sms;
@@ -627,7 +633,54 @@ int blr_sign_grads(const float *x, const float *g, const float *l, float *gu, fl
         !make_tmap_act16(&gl.maps.a[1], x16, M, d_in, 64) || !make_tmap_act16(&gl.maps.b[1], bv, M, r, 64) ||
         !make_tmap_out_sw128(&gl.maps.o[0], gu, d_out, r) || !make_tmap_out_sw128(&gl.maps.o[1], gv, d_in, r))
         return BLR_ERR_CUDA;
-    return launch_sign_gemm(gl, s) == cudaSuccess ? BLR_OK : BLR_ERR_CUDA;
+    return launch_dense_gemm(gl, "sign_gemm", s) == cudaSuccess ? BLR_OK : BLR_ERR_CUDA;
+}
+
+size_t blr_plane_workspace_bytes(int ntok, int n, int k) {
+    if (!plane_shape_ok(ntok, n, k)) return 0;
+    return 256 + align_up((size_t)ntok * (size_t)(n > k ? n : k) * 2, 256);
+}
+
+int blr_plane_linear(const float *x, const uint16_t *plane, float *y, int transpose, int accumulate, float scale,
+                     int ntok, int n, int k, void *ws, size_t ws_bytes, blr_stream_t stream) {
+    if (!x || !plane || !y || !ws) return BLR_ERR_ARG;
+    if ((transpose != 0 && transpose != 1) || (accumulate != 0 && accumulate != 1)) return BLR_ERR_ARG;
+    if (!pow2_positive(scale)) return BLR_ERR_ARG;
+    if (!plane_shape_ok(ntok, n, k)) return BLR_ERR_SHAPE;
+    const void *ptrs[] = {x, plane, y, ws};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return BLR_ERR_ALIGN;
+    if (ws_bytes < blr_plane_workspace_bytes(ntok, n, k)) return BLR_ERR_WORKSPACE;
+    int sms;
+    int st = device_info(&sms);
+    if (st != BLR_OK) return st;
+    if (fault_injected("plane")) return BLR_ERR_CUDA;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    char *w = static_cast<char *>(ws);
+    uint32_t *status = reinterpret_cast<uint32_t *>(w);
+    uint16_t *act16 = reinterpret_cast<uint16_t *>(w + 256);
+    // forward: x [ntok][k] -> y [ntok][n] = x plane^T; transpose: x [ntok][n] -> y [ntok][k] = x plane
+    const int kin = transpose ? n : k, nout = transpose ? k : n;
+    if (launch_plane_stage(x, act16, (long long)ntok * kin, scale, status, sms, s) != cudaSuccess) return BLR_ERR_CUDA;
+    DenseGemmLaunch gl{};
+    gl.F[0] = ntok;
+    gl.F[1] = 0;
+    gl.scale[0] = 1.0f / scale;
+    gl.out[0] = y;
+    gl.R = nout;
+    gl.K = kin;
+    gl.accumulate = accumulate;
+    gl.a_mn = false;           // act16 rows are K-vectors
+    gl.b_mn = transpose != 0;  // plane rows are K-vectors (forward) or N-vectors (transpose)
+    gl.status = status;
+    gl.sms = sms;
+    const bool ok = make_tmap_act16(&gl.maps.a[0], act16, ntok, kin, 128) &&
+                    (transpose ? make_tmap_act16(&gl.maps.b[0], plane, n, k, 64)
+                               : make_tmap_act16(&gl.maps.b[0], plane, n, k, dense_bn(nout))) &&
+                    make_tmap_out_sw128(&gl.maps.o[0], y, ntok, nout);
+    if (!ok) return BLR_ERR_CUDA;
+    return launch_dense_gemm(gl, "plane_gemm", s) == cudaSuccess ? BLR_OK : BLR_ERR_CUDA;
 }
 
 int blr_adam(float *w, const float *grad, float *m1, float *m2, const float *mask, int n, int step, float lr,

@@ -186,18 +186,37 @@ cudaError_t launch_small_bwd(const GemmMaps &m1, const GemmMaps &m2, SmallBwdArg
 bool small_bwd_fits(int d_out);  // the fused backward stages rows of d_out floats
 
 // ---- sign gradients (blr_sign.cu) -------------------------------------------
-// TMA descriptors of the sign-gradient products, [0] = G_U, [1] = G_V, all
-// token-major as the path stores them (K = tokens is the outer dimension, so
-// both MMA operands are MN-major):
-// a = dy16 / x16 [M][F] f16 (box 64 features x 64 tokens, 128-byte swizzle),
-// b = the rank-side operand [M][r] f16 (box 64 ranks x 64 tokens, same),
-// o = gu / gv [F][r] f32 (box 32 x 32, 128-byte swizzle).
-struct SignGemmMaps {
+// ---- dense tensor-core products (blr_dense.cu) --------------------------------
+// TMA descriptors of up to two products, [0] and [1]:
+// a = the M-side operand: MN-major [K][F] (box 64 rows x 64 K) or K-major
+//     [F][K] (box 64 K x 128 rows), f16, 128-byte swizzle;
+// b = the N-side operand: MN-major [K][R] (box 64 x 64) or K-major [R][K]
+//     (box 64 K x BN rows), f16, 128-byte swizzle;
+// o = the f32 output [F][R] (box 32 x 32, 128-byte swizzle).
+struct DenseGemmMaps {
     CUtensorMap a[2], b[2], o[2];
 };
 
-// Rank tile of the sign-gradient products: 256 when r >= 256, else 128.
-inline int sign_bn(int r) { return r >= 256 ? 256 : 128; }
+// Column tile of the dense products: 256 when R >= 256, else 128.
+inline int dense_bn(int R) { return R >= 256 ? 256 : 128; }
+
+// out_j = scale_j * dscale_j (if given) * sum_k A_j B_j, overwritten or added.
+struct DenseGemmLaunch {
+    DenseGemmMaps maps;
+    int F[2];                      // rows of each product (F[1] = 0: one product)
+    float scale[2];
+    const float *dscale[2];        // device scalars or null
+    float *out[2];
+    int R, K, accumulate;
+    bool a_mn, b_mn;               // operand majorness (A MN-major needs B MN-major)
+    uint32_t *status;
+    int sms;
+};
+cudaError_t launch_dense_gemm(const DenseGemmLaunch &L, const char *name, cudaStream_t s);
+
+// ---- sign gradients (blr_sign.cu) -------------------------------------------
+// G_U = dense product of dy16 [M][d_out] and the rank-side operand [M][r], G_V
+// of x16 [M][d_in] and [M][r]: K = tokens, both operands MN-major.
 
 // Dynamic gradient scale: rescale the rank-side operands to one scale each,
 //   bu[t][k] = al16[t][k] * (1/s_t) / max_t (1/s_t)
@@ -214,18 +233,11 @@ struct SignRescaleArgs {
 };
 cudaError_t launch_sign_rescale(const SignRescaleArgs &a, int sms, cudaStream_t s);
 
-// G = scale * dscale (if given) * sum_t A[t][f] B[t][k], overwritten or added.
-struct SignGemmLaunch {
-    SignGemmMaps maps;
-    int F[2];                      // d_out, d_in
-    float scale[2];
-    const float *dscale[2];        // device scalars or null
-    float *out[2];                 // gu, gv
-    int M, r, accumulate;
-    uint32_t *status;
-    int sms;
-};
-cudaError_t launch_sign_gemm(const SignGemmLaunch &L, cudaStream_t s);
+
+// ---- plane_linear (blr_plane.cu) ----------------------------------------------
+// act16 = f16(x * scale) over n values (n a multiple of 8); clears *status.
+cudaError_t launch_plane_stage(const float *x, uint16_t *act16, long long n, float scale, uint32_t *status, int sms,
+                               cudaStream_t s);
 
 // ---- Adam (blr_adam.cu) -------------------------------------------------------
 struct AdamArgs {

@@ -182,6 +182,36 @@ BLR_API int blr_sign_grads(const float *x, const float *g, const float *l,
                            const void *ws, size_t ws_bytes, void *sws, size_t sws_bytes,
                            blr_stream_t stream);
 
+/* Bytes of the workspace blr_plane_linear needs (0 when the shape violates
+ * its rule): a 256-byte header (word 0: device status) and the f16 staging
+ * of x, ntok * max(n, k) * 2 bytes. */
+BLR_API size_t blr_plane_workspace_bytes(int ntok, int n, int k);
+
+/* A dense frozen f16 linear (train_mm.rs, plane_linear and mm):
+ *
+ *   transpose = 0:  y [ntok][n] (+)= (f16(x * scale) . plane^T) / scale,  x [ntok][k]
+ *   transpose = 1:  y [ntok][k] (+)= (f16(x * scale) . plane)   / scale,  x [ntok][n]
+ *
+ * plane [n][k] f16 (IEEE binary16 bits, row-major) is the same array in both
+ * directions: the transpose (the input gradient through the plane) reads it
+ * as MN-major tiles, nothing is transposed in memory. x is staged once into
+ * `ws` as f16(x * scale), round to nearest even; the product accumulates in
+ * f32 on the tensor cores and is multiplied by 1/scale.
+ *  - scale: a positive power of two (the page's caller-chosen scale, 1 for a
+ *    forward, a gradient scale for the input gradient); |x * scale| must stay
+ *    below 65504 (f16 range), and values below 2^-14 lose precision.
+ *  - accumulate = 0 overwrites y, 1 adds to it.
+ *  - Shape rule: ntok >= 1; n and k multiples of 32 in [32, 65536].
+ *  - All pointers device, caller-owned, 16-byte aligned.
+ * Errors: BLR_ERR_ARG (null pointer, flag not 0/1, scale not a positive power
+ *   of two), BLR_ERR_SHAPE, BLR_ERR_ALIGN, BLR_ERR_WORKSPACE,
+ *   BLR_ERR_UNSUPPORTED_DEVICE, BLR_ERR_CUDA; kernel-side failures go to the
+ *   status word of `ws` (blr_check_status). */
+BLR_API int blr_plane_linear(const float *x, const uint16_t *plane, float *y,
+                             int transpose, int accumulate, float scale,
+                             int ntok, int n, int k,
+                             void *ws, size_t ws_bytes, blr_stream_t stream);
+
 /* One Adam step over n parameters (train_mm.rs, WGSL adam kernel and its
  * wrapper adam), meant for the layer's vectors g, l and h (for instance kept
  * as one contiguous [d_in + r + d_out] array with its gradient dg | dl | dh):

@@ -160,6 +160,28 @@ def test_adam_argument_errors(lib):
     assert _adam(lib, n=0) == blr.BLR_OK  # nothing to do, nothing queued
 
 
+def _plane(lib, **over):
+    a = dict(x=FAKE, p=FAKE, y=FAKE, tr=0, acc=0, scale=1.0, ntok=64, n=128, k=96, ws=FAKE, wsb=1 << 40, s=None)
+    a.update(over)
+    return lib.blr_plane_linear(a["x"], a["p"], a["y"], a["tr"], a["acc"], a["scale"], a["ntok"], a["n"], a["k"],
+                                a["ws"], a["wsb"], a["s"])
+
+
+def test_plane_linear_argument_errors(lib):
+    import binary_rank_linear_gb300 as blr
+    assert lib.blr_plane_workspace_bytes(70, 128, 96) == 256 + ((70 * 128 * 2 + 255) // 256) * 256
+    assert lib.blr_plane_workspace_bytes(0, 128, 96) == 0
+    assert lib.blr_plane_workspace_bytes(8, 100, 96) == 0
+    assert _plane(lib, p=None) == blr.BLR_ERR_ARG
+    assert _plane(lib, tr=2) == blr.BLR_ERR_ARG
+    assert _plane(lib, scale=3.0) == blr.BLR_ERR_ARG
+    assert _plane(lib, scale=0.0) == blr.BLR_ERR_ARG
+    assert _plane(lib, k=48) == blr.BLR_ERR_SHAPE
+    assert _plane(lib, ntok=0) == blr.BLR_ERR_SHAPE
+    assert _plane(lib, y=FAKE + 8) == blr.BLR_ERR_ALIGN
+    assert _plane(lib, wsb=512) == blr.BLR_ERR_WORKSPACE
+
+
 def test_pack_argument_errors(lib):
     import binary_rank_linear_gb300 as blr
     assert lib.blr_pack_signs(None, FAKE, 4, 64, None) == blr.BLR_ERR_ARG
