@@ -149,8 +149,8 @@ bool make_tmap_out_sw128(CUtensorMap *m, void *base, int rows, int cols) {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-    size_t header, bp_f1, bp_f2, bp_b1, bp_b2, x16, dy16, a32, al16, db16, c16, s_inv, sig, sig_inv, blkmax,
-        part_dh, part_dl, part_dg, total;
+    size_t header, bp_f1, bp_f2, bp_b1, bp_b2, plane_u, plane_v, x16, dy16, a32, al16, db16, c16, s_inv, sig,
+        sig_inv, blkmax, part_dh, part_dl, part_dg, total;
     int rows_dh, rows_dl, rows_dg;
 };
 
@@ -177,6 +177,9 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     L.bp_f2 = take(kblocks(r) * sign_rows(d_out) * 8);  // forward 2: N = d_out, K = r
     L.bp_b1 = take(kblocks(d_out) * sign_rows(r) * 8);  // backward 1: N = r, K = d_out
     L.bp_b2 = take(kblocks(r) * sign_rows(d_in) * 8);   // backward 2: N = d_in, K = r
+    // +-1 f16 sign planes in the bitmaps' own [rows][r] order (plane-mode GEMMs)
+    L.plane_u = take((size_t)d_out * r * 2);
+    L.plane_v = take((size_t)d_in * r * 2);
     // the f16 staging of all four products stays in place after the pass
     // (the sign-gradient products read x16, dy16, al16 and db16 again)
     L.x16 = take(m * d_in * 2);
@@ -288,6 +291,34 @@ GemmPlan plan_gemm(int M, int N, int sms) {
     return GemmPlan{false, 128, (int)(tiles < sms ? tiles : sms), (int)t_tiles};
 }
 
+// Plane-mode tiles: CTA pairs of 256 features x 256 tokens (each CTA loads
+// half the tokens, which halves the activation bytes a k-step brings per SM)
+// when there are at least as many pair tiles as pairs of SMs, single CTAs of
+// 128 x 128 otherwise. Measured on GB300, 256 tokens beat 192 and 160 on every
+// workload although they leave more of the last round idle.
+GemmPlan plan_gemm_plane(int M, int N, int sms) {
+    const int pairs = sms / 2;
+    const long long t_tiles = (M + 255) / 256;
+    const long long tiles = t_tiles * ((N + 255) / 256);
+    if (tiles >= pairs) return GemmPlan{true, 256, 2 * pairs, (int)t_tiles, true};
+    const long long s_tiles = (M + 127) / 128;
+    const long long stiles = s_tiles * ((N + 127) / 128);
+    return GemmPlan{false, 128, (int)(stiles < sms ? stiles : sms), (int)s_tiles, true};
+}
+
+// Where the general path's GEMMs take the sign operand from: bitmap words
+// expanded into TMEM (default), or +-1 f16 planes read by TMA when
+// BLR_SIGN_SRC=plane. Measured on GB300: kernel by kernel (serialised, event
+// trace) the planes win every product of the passes whose widths are both at
+// most 4096 (attention-sized layer: 12 us of 395) and lose on 12288- and
+// 32768-wide ones; but timed as CUDA-graph replays, where consecutive kernels
+// overlap their setup and tails, the attention-sized step took 393 us with
+// planes against 381 with the TMEM expansion, and the small one 62.4 both ways.
+bool plane_mode() {
+    const char *v = std::getenv("BLR_SIGN_SRC");
+    return v && std::strcmp(v, "plane") == 0;
+}
+
 // Grid of the fused small-M kernels: enough CTAs for the larger GEMM phase's
 // tiles (at least 16, for the staging phases), at most one per SM.
 int small_grid(const GemmPlan &p1, int N1, const GemmPlan &p2, int N2, int M, int sms) {
@@ -372,9 +403,19 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     uint16_t *al16 = reinterpret_cast<uint16_t *>(w + L.al16);
     uint16_t *c16 = reinterpret_cast<uint16_t *>(w + L.c16);
 
-    const GemmPlan p1 = plan_gemm(M, r, sms);
-    const GemmPlan p2 = plan_gemm(M, d_out, sms);
+    uint16_t *plane_u = reinterpret_cast<uint16_t *>(w + L.plane_u);
+    uint16_t *plane_v = reinterpret_cast<uint16_t *>(w + L.plane_v);
+    // the TMEM-expansion tiles decide what counts as a small problem (fused path)
+    const GemmPlan q1 = plan_gemm(M, r, sms);
+    const GemmPlan q2 = plan_gemm(M, d_out, sms);
+    const bool fused = !q1.pair && !q2.pair && fused_small_enabled();
+    const bool planes = !fused && plane_mode();
+    const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : q1;
+    const GemmPlan p2 = planes ? plan_gemm_plane(M, d_out, sms) : q2;
     GemmMaps m1{}, m2{};
+    // a-product: S_V [d_in][r] read MN-major; c-product: S_U [d_out][r] read K-major
+    if (planes && (!make_tmap_act16(&m1.sgn, plane_v, d_in, r, 64) || !make_tmap_act16(&m2.sgn, plane_u, d_out, r, 128)))
+        return BLR_ERR_CUDA;
     if (!make_tmap_act16(&m1.act, x16, M, d_in, p1.pair ? p1.bt / 2 : p1.bt) ||
         !make_tmap_chunk(&m1.out32, a32, M, r, false) || !make_tmap_chunk(&m1.out16, al16, M, r, true) ||
         !make_tmap_act16(&m2.act, al16, M, r, p2.pair ? p2.bt / 2 : p2.bt) ||
@@ -390,6 +431,11 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     // S_V [d_in][r/32] has its bits along r: the first product needs them along d_in
     SignPrep pv{bits_v, bp_f1, r, d_in, 1, sign_rows(r)};
     SignPrep pu{bits_u, bp_f2, d_out, r, 0, sign_rows(d_out)};
+    if (planes) {
+        // both products read +-1 f16 planes in the bitmaps' own order
+        pv = SignPrep{bits_v, reinterpret_cast<uint32_t *>(plane_v), d_in, r, 2, 0};
+        pu = SignPrep{bits_u, reinterpret_cast<uint32_t *>(plane_u), d_out, r, 2, 0};
+    }
 
     GemmArgs f1{};
     f1.M = M;
@@ -414,7 +460,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f2.accumulate = accumulate_y;
     f2.status = status;
 
-    if (!p1.pair && !p2.pair && fused_small_enabled()) {
+    if (fused) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallFwdArgs fa{pv, pu, x, g, x16, M, d_in, status,
                         reinterpret_cast<unsigned int *>(w + L.header + kGridBarOffset), f1, f2};
@@ -471,9 +517,18 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     float *part_dl = reinterpret_cast<float *>(w + L.part_dl);
     float *part_dg = reinterpret_cast<float *>(w + L.part_dg);
 
-    const GemmPlan p1 = plan_gemm(M, r, sms);
-    const GemmPlan p2 = plan_gemm(M, d_in, sms);
+    uint16_t *plane_u = reinterpret_cast<uint16_t *>(w + L.plane_u);
+    uint16_t *plane_v = reinterpret_cast<uint16_t *>(w + L.plane_v);
+    const GemmPlan q1 = plan_gemm(M, r, sms);
+    const GemmPlan q2 = plan_gemm(M, d_in, sms);
+    const bool fused = !q1.pair && !q2.pair && small_bwd_fits(d_out) && fused_small_enabled();
+    const bool planes = !fused && plane_mode();
+    const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : q1;
+    const GemmPlan p2 = planes ? plan_gemm_plane(M, d_in, sms) : q2;
     GemmMaps m1{}, m2{};
+    // db-product: S_U [d_out][r] read MN-major; dx'-product: S_V [d_in][r] read K-major
+    if (planes && (!make_tmap_act16(&m1.sgn, plane_u, d_out, r, 64) || !make_tmap_act16(&m2.sgn, plane_v, d_in, r, 128)))
+        return BLR_ERR_CUDA;
     if (!make_tmap_act16(&m1.act, dy16, M, d_out, p1.pair ? p1.bt / 2 : p1.bt) ||
         !make_tmap_chunk(&m1.in32, a32, M, r, false) || !make_tmap_chunk(&m1.out16, db16, M, r, true) ||
         !make_tmap_act16(&m2.act, db16, M, r, p2.pair ? p2.bt / 2 : p2.bt) ||
@@ -483,6 +538,10 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     // S_U [d_out][r/32] has its bits along r: the first product needs them along d_out
     SignPrep pu{bits_u, bp_b1, r, d_out, 1, sign_rows(r)};
     SignPrep pv{bits_v, bp_b2, d_in, r, 0, sign_rows(d_in)};
+    if (planes) {
+        pu = SignPrep{bits_u, reinterpret_cast<uint32_t *>(plane_u), d_out, r, 2, 0};
+        pv = SignPrep{bits_v, reinterpret_cast<uint32_t *>(plane_v), d_in, r, 2, 0};
+    }
     StageDyArgs sa{};
     sa.dy = dy;
     sa.h = h;
@@ -529,7 +588,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
 
     ReduceSeg sl{part_dl, dl, p1.part_rows * epi_part_rows_per_tile(kEpiBwd1), r};
     ReduceSeg sg{part_dg, dg, p2.part_rows * epi_part_rows_per_tile(kEpiBwd2), d_in};
-    if (!p1.pair && !p2.pair && small_bwd_fits(d_out) && fused_small_enabled()) {
+    if (fused) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallBwdArgs ba{};
         ba.pu = pu;

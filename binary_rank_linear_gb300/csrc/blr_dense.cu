@@ -42,7 +42,6 @@ struct DenseGemmArgs {
 
 constexpr int kSgThreads = 192;
 constexpr int kSgEpi0 = 2;
-constexpr uint32_t kMnBlockBytes = 64 * 64 * 2;
 
 template <int BN>
 struct DenseGemmShape {
@@ -57,25 +56,6 @@ struct DenseGemmShape {
     static_assert(kNB >= 2, "pipeline depth");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
-
-// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle
-// layout (fields as in umma_sdesc_sw128): leading byte offset = stride of the
-// 64-element blocks along M or N, stride byte offset = stride of the 8-row
-// groups along K.
-__device__ __forceinline__ uint64_t umma_sdesc_sw128_mn(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(kMnBlockBytes >> 4) << 16;
-    d |= static_cast<uint64_t>(1024u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
-    d |= static_cast<uint64_t>(2u) << 61;
-    return d;
-}
-
-// Instruction descriptor with A and/or B MN-major (transpose bits 15, 16).
-__host__ __device__ constexpr uint32_t umma_idesc_f16_f32_major(int m, int n, bool a_mn, bool b_mn) {
-    return umma_idesc_f16_f32(m, n) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
-}
 
 // Descriptor of an operand tile and its per-MMA advance (16 K values).
 template <bool MN>

@@ -339,6 +339,29 @@ __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Bytes of one 64 x 64 f16 block of an MN-major operand tile (the 8 KB
+// stride between its 64-element blocks along M or N).
+constexpr uint32_t kMnBlockBytes = 64 * 64 * 2;
+
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle
+// layout (fields as in umma_sdesc_sw128): leading byte offset = stride of the
+// 64-element blocks along M or N, stride byte offset = stride of the 8-row
+// groups along K.
+__device__ __forceinline__ uint64_t umma_sdesc_sw128_mn(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(kMnBlockBytes >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Instruction descriptor with A and/or B MN-major (transpose bits 15, 16).
+__host__ __device__ constexpr uint32_t umma_idesc_f16_f32_major(int m, int n, bool a_mn, bool b_mn) {
+    return umma_idesc_f16_f32(m, n) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
+}
+
 #define BLR_TMEM_LD32_OUTS(v)                                                                                  \
     "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), \
         "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), \

@@ -77,19 +77,34 @@ constexpr int kGemmThreads = (kWarpEpi0 + 8) * 32;  // the fused small-M kernels
 constexpr int kCtlBytes = 1024;   // shared-memory control block ahead of a phase's layout
 static_assert(kNumExpWarps == 4 * kKB, "one expander warp per (lane quarter, 64-wide block)");
 
-template <int EPI, bool PAIR, int BT>
+// PLANE selects where the sign operand comes from: false, bitmap words
+// expanded into TMEM by expander warps (above); true, a +-1 f16 sign plane
+// in global memory (written once per pass by the prologue, L2-resident) read
+// by TMA like the activations, so both MMA operands come from shared memory
+// and no expander warps exist. Plane mode takes one 64-deep block per k-step,
+// and the plane tile is K-major (the c- and dx'-products: plane rows are the
+// features) or MN-major (the a- and db-products: plane rows run along K). In
+// a CTA pair each CTA loads its own 128 plane rows and half the tokens, and
+// the peer's MMA warp, idle otherwise, forwards each stage's arrival to the
+// leader (full_p) once the peer's loads have landed.
+template <int EPI, bool PAIR, int BT, bool PLANE = false>
 struct GemmShape {
+    static constexpr int kKBm = PLANE ? 1 : kKB;           // 64-wide blocks per k-step
+    static constexpr int kStepKm = kKBm * kBK;             // K per k-step
+    static constexpr int kEpi0 = PLANE ? 2 : kWarpEpi0;    // first epilogue warp
+    static constexpr bool kPlaneMN = EPI == kEpiFwd1 || EPI == kEpiBwd1;  // plane rows run along K
     static constexpr int kAccCols = BT;                    // TMEM columns of one accumulator
     static constexpr int kSignCol0 = 2 * BT;               // first sign-stage column
     static constexpr int kChunks = BT / 32;                // epilogue chunks per tile
     static constexpr int kTokRows = PAIR ? BT / 2 : BT;    // activation rows this CTA loads per tile
     static constexpr int kBBlock = kTokRows * kBK * 2;     // one 64-wide activation box
-    static constexpr int kBBytes = kKB * kBBlock;          // activation tile of a k-step
+    static constexpr int kBBytes = kKBm * kBBlock;         // activation tile of a k-step
     static constexpr int kBitsBlock = kFM * 8;             // bitmap words of 128 rows, one block
-    static constexpr int kBitsBytes = kKB * kBitsBlock;
+    static constexpr int kABlock = kFM * kBK * 2;          // plane tile of 128 rows x 64 K (PLANE)
+    static constexpr int kBitsBytes = PLANE ? kABlock : kKB * kBitsBlock;  // per stage: words or plane tile
     static constexpr int kEW = epi_warps(EPI);             // epilogue warps
     static constexpr int kSplit = kEW / 4;                 // epilogue warps per TMEM lane quarter
-    static constexpr int kThreads = gemm_threads(EPI);
+    static constexpr int kThreads = (kEpi0 + kEW) * 32;
     static constexpr bool kHas16 = EPI != kEpiBwd2;        // f16 output: a.l, c, db.l
     static constexpr bool kHas32 = EPI != kEpiBwd1;        // f32 output: a, y, dx
     static constexpr int kSlot32 = 32 * 32 * 4;            // f32 chunk: input, then output in place
@@ -97,20 +112,24 @@ struct GemmShape {
     // chunk slots per epilogue warp; inputs are prefetched kNE - 2 of the
     // warp's chunks ahead (a slot is free once the store of the warp's chunk two
     // before has read it). dx' streams x in and dx out at HBM rate
-    static constexpr int kNE = EPI == kEpiBwd2 ? 4 : (kSplit == 2 ? 2 : 4);
+    // (plane mode leaves more room to the operand ring, which measured faster
+    // than deeper chunk buffering: no input prefetch but for dx')
+    static constexpr int kNE = PLANE ? (EPI == kEpiBwd2 ? 3 : 2)
+                                     : (EPI == kEpiBwd2 ? 4 : (kSplit == 2 ? 2 : 4));
     static constexpr int kEpiBytes = kEW * kNE * kSlotBytes;
-    static constexpr int kBudget = 221 * 1024 - kEpiBytes;
+    static constexpr int kBudget = (PLANE ? 224 : 221) * 1024 - kEpiBytes;
     static constexpr int kNBRaw = kBudget / (kBBytes + kBitsBytes);
     static constexpr int kNB = kNBRaw > 10 ? 10 : kNBRaw;
     static constexpr int kNSMax = (kTmemCols - 2 * BT) / kSignCols;
-    static constexpr int kNS = kNSMax < kNB ? kNSMax : kNB;  // sign stages in TMEM
-    static constexpr int kNumBars = 2 * kNB + kNS + 2 + 2 + 1 + kEW * kNE;
+    static constexpr int kNS = PLANE ? 0 : (kNSMax < kNB ? kNSMax : kNB);  // sign stages in TMEM
+    static constexpr int kNumBars = 2 * kNB + kNS + 2 + 2 + 1 + kEW * kNE + (PLANE && PAIR ? kNB : 0);
     static_assert(kNE >= 2, "double-buffered chunk staging");
     static constexpr int kPhaseBytes = kNB * kBBytes + kEpiBytes + kNB * kBitsBytes + kNumBars * 8;
     static constexpr int kSmemBytes = 1024 + kCtlBytes + kPhaseBytes;  // alignment slack, control block, phase
     static_assert(BT % 32 == 0 && BT >= 64 && BT <= 256 && (!PAIR || BT % 16 == 0), "token tile");
     static_assert(kTokRows % 8 == 0, "activation boxes hold whole 8-row swizzle groups");
-    static_assert(kNS >= 2, "at least two sign stages");
+    static_assert(PLANE || kNS >= 2, "at least two sign stages");
+    static_assert(kNB >= 2, "at least two operand stages");
     // an expander frees sign stage i % NS by waiting on the activation slot of
     // k-step i - NS; that wait is unambiguous only if the activation ring is at
     // least as deep as the sign ring
@@ -129,13 +148,13 @@ struct GemmCtl {
 static_assert(sizeof(GemmCtl) <= kCtlBytes, "control block");
 
 // Shared-memory layout of one GEMM phase (from a 1024-aligned base).
-template <int EPI, bool PAIR, int BT>
+template <int EPI, bool PAIR, int BT, bool PLANE = false>
 struct GemmLayout {
-    using S = GemmShape<EPI, PAIR, BT>;
+    using S = GemmShape<EPI, PAIR, BT, PLANE>;
     uint8_t *sB;       // [NB][kBBytes] activation tiles
     uint8_t *sE;       // [4 warps][kNE][slot] epilogue chunks
-    uint32_t *sBits;   // [NB][2][128][2] bitmap words
-    uint64_t *full_b, *empty_b, *full_s, *tmem_full, *tmem_empty, *drain_bar, *eload;
+    uint32_t *sBits;   // [NB][2][128][2] bitmap words, or [NB][plane tile] (PLANE)
+    uint64_t *full_b, *empty_b, *full_s, *tmem_full, *tmem_empty, *drain_bar, *eload, *full_p;
     __device__ explicit GemmLayout(uint8_t *base) {
         sB = base;
         sE = sB + S::kNB * S::kBBytes;
@@ -147,6 +166,7 @@ struct GemmLayout {
         tmem_empty = tmem_full + 2;
         drain_bar = tmem_empty + 2;
         eload = drain_bar + 1;  // [epilogue warps][kNE]
+        full_p = eload + S::kEW * S::kNE;  // [NB] (plane pairs: the peer's stage has landed)
     }
     // one thread: initialise every barrier of the phase
     __device__ void init_barriers() const {
@@ -161,10 +181,12 @@ struct GemmLayout {
         }
         mbar_init(drain_bar, 1);
         for (int i = 0; i < S::kEW * S::kNE; ++i) mbar_init(&eload[i], 1);
+        if (PLANE && PAIR)
+            for (int s = 0; s < S::kNB; ++s) mbar_init(&full_p[s], 1);
     }
     // one thread, once every role of the phase has finished with the barriers
     __device__ void inval_barriers() const {
-        for (uint64_t *b = full_b; b < eload + S::kEW * S::kNE; ++b) mbar_inval(b);
+        for (uint64_t *b = full_b; b < eload + S::kEW * S::kNE + (PLANE && PAIR ? S::kNB : 0); ++b) mbar_inval(b);
     }
 };
 
@@ -179,12 +201,14 @@ __device__ __forceinline__ uint16_t f16_bits(float v) { return __half_as_ushort(
 // (a CTA, or a CTA pair, per unit). Barriers must be initialised (and, for a
 // pair, both CTAs' barriers visible) and TMEM allocated before the call; on
 // return every load, MMA and store the phase issued has completed.
-template <int EPI, bool PAIR, int BT>
-__device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, const CUtensorMap &tmap_act,
+template <int EPI, bool PAIR, int BT, bool PLANE = false>
+__device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE> &L, const CUtensorMap &tmap_act,
                                            const CUtensorMap &tmap_in, const CUtensorMap &tmap_out32,
                                            const CUtensorMap &tmap_out16, const GemmArgs &args,
-                                           uint32_t tmem_base, volatile int *abort_flag, int unit, int num_units) {
-    using S = GemmShape<EPI, PAIR, BT>;
+                                           uint32_t tmem_base, volatile int *abort_flag, int unit, int num_units,
+                                           const CUtensorMap *tmap_sgn = nullptr) {
+    using S = GemmShape<EPI, PAIR, BT, PLANE>;
+    constexpr int kKB = S::kKBm, kStepK = S::kStepKm, kWarpEpi0 = S::kEpi0;
     constexpr int NB = S::kNB, NS = S::kNS, kChunks = S::kChunks, kNE = S::kNE;
     uint8_t *sB = L.sB;
     uint8_t *sE = L.sE;
@@ -219,13 +243,30 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
                         break;
                     }
                     mbar_arrive_expect_tx(&full_b[sb], S::kBBytes + S::kBitsBytes);
+                    if constexpr (PLANE) {
+                        // one 64-deep block: the activation box and the plane tile
+                        // (rows and K past the plane's extent read zero)
+                        const int k0 = ks * kBK;
+                        uint8_t *sa = reinterpret_cast<uint8_t *>(sBits) + sb * S::kBitsBytes;
+                        tma_load_2d(sB + sb * S::kBBytes, &tmap_act, &full_b[sb], k0, t0);
+                        if constexpr (S::kPlaneMN) {
+                            // plane [K][N]: two 64-feature blocks of 64 K rows
+                            tma_load_2d(sa, tmap_sgn, &full_b[sb], f0, k0);
+                            tma_load_2d(sa + S::kABlock / 2, tmap_sgn, &full_b[sb], f0 + 64, k0);
+                        } else {
+                            // plane [N][K]: 128 feature rows of 64 K
+                            tma_load_2d(sa, tmap_sgn, &full_b[sb], k0, f0);
+                        }
+                    } else {
 #pragma unroll
-                    for (int kk = 0; kk < kKB; ++kk) {
-                        // 64-wide K block; blocks past K read zero activations (and padded words)
-                        const int blk = ks * kKB + kk;
-                        tma_load_2d(sB + sb * S::kBBytes + kk * S::kBBlock, &tmap_act, &full_b[sb], blk * kBK, t0);
-                        bulk_load(sBits + sb * (S::kBitsBytes / 4) + kk * (S::kBitsBlock / 4),
-                                  args.bsign + ((size_t)blk * args.Ns + f0) * 2, S::kBitsBlock, &full_b[sb]);
+                        for (int kk = 0; kk < kKB; ++kk) {
+                            // 64-wide K block; blocks past K read zero activations (and padded words)
+                            const int blk = ks * kKB + kk;
+                            tma_load_2d(sB + sb * S::kBBytes + kk * S::kBBlock, &tmap_act, &full_b[sb], blk * kBK,
+                                        t0);
+                            bulk_load(sBits + sb * (S::kBitsBytes / 4) + kk * (S::kBitsBlock / 4),
+                                      args.bsign + ((size_t)blk * args.Ns + f0) * 2, S::kBitsBlock, &full_b[sb]);
+                        }
                     }
                     issued |= 1u << sb;
                     parity = (parity & ~(1u << sb)) | (pb << sb);
@@ -239,6 +280,90 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
             for (int s = 0; s < NB; ++s) {
                 if (((issued >> s) & 1u) && !mbar_wait(&full_b[s], (parity >> s) & 1u, abort_flag, false))
                     atomicOr(args.status, kStTimeoutDrain);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma && PLANE) {
+        if constexpr (PLANE) {
+            if (lane == 0 && leader) {
+                // both operands in shared memory: 4 MMAs (K = 16 each) per 64-deep block
+                constexpr uint32_t idesc = umma_idesc_f16_f32_major(PAIR ? 2 * kFM : kFM, BT, S::kPlaneMN, false);
+                constexpr uint64_t kAdvA = S::kPlaneMN ? (2048u >> 4) : (32u >> 4);
+                const uint64_t bdesc0 = umma_sdesc_sw128(smem_u32(sB));
+                const uint32_t abase = smem_u32(sBits);
+                int sb = 0;
+                uint32_t pb = 0;
+                bool ok = true;
+                int local = 0;
+                for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++local) {
+                    const int acc = local & 1;
+                    const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
+                    if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag)) {
+                        fail_status(args, abort_flag, kStTimeoutMma);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * S::kAccCols);
+                    uint32_t acc_in = 0u;
+                    for (int ks = 0; ks < num_ks; ++ks) {
+                        bool got = mbar_wait(&full_b[sb], pb, abort_flag);
+                        if (PAIR && got) got = mbar_wait(&L.full_p[sb], pb, abort_flag);
+                        if (!got) {
+                            fail_status(args, abort_flag, kStTimeoutMma);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = abase + (uint32_t)(sb * S::kBitsBytes);
+                        const uint64_t adesc = S::kPlaneMN ? umma_sdesc_sw128_mn(a_addr) : umma_sdesc_sw128(a_addr);
+                        const uint64_t bdesc = bdesc0 + (uint64_t)sb * (S::kBBytes >> 4);
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            if constexpr (PAIR)
+                                umma_f16_pair(d_tmem, adesc + kAdvA * k, bdesc + (uint64_t)(2 * k), idesc, acc_in);
+                            else
+                                umma_f16(d_tmem, adesc + kAdvA * k, bdesc + (uint64_t)(2 * k), idesc, acc_in);
+                            acc_in = 1u;
+                        }
+                        if constexpr (PAIR)
+                            umma_commit_pair_multicast(&empty_b[sb], 3);
+                        else
+                            umma_commit(&empty_b[sb]);
+                        if (++sb == NB) {
+                            sb = 0;
+                            pb ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    if constexpr (PAIR)
+                        umma_commit_pair_multicast(&tmem_full[acc], 3);
+                    else
+                        umma_commit(&tmem_full[acc]);
+                }
+                if constexpr (PAIR)
+                    umma_commit_pair_multicast(drain_bar, 1);
+                else
+                    umma_commit(drain_bar);
+                if (!mbar_wait(drain_bar, 0, abort_flag, false)) atomicOr(args.status, kStTimeoutDrain);
+            } else if (PAIR && lane == 0) {
+                // peer: forward each stage's landing (its own full_b) to the leader's full_p
+                int sb = 0;
+                uint32_t pb = 0;
+                bool ok = true;
+                for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
+                    for (int ks = 0; ks < num_ks; ++ks) {
+                        if (!mbar_wait(&full_b[sb], pb, abort_flag)) {
+                            fail_status(args, abort_flag, kStTimeoutMma);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_remote(leader_bar(&L.full_p[sb]));
+                        if (++sb == NB) {
+                            sb = 0;
+                            pb ^= 1u;
+                        }
+                    }
+                }
             }
         }
         __syncwarp();
@@ -314,6 +439,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
         }
         __syncwarp();
     } else if (warp < kWarpEpi0) {
+      if constexpr (!PLANE) {
         // ---- sign expanders: bitmap words -> +-1 f16 A operand in TMEM -----
         const int quarter = warp & 3;
         const int kk = (warp - kWarpExp0) / 4;  // which 64-wide block of the k-step
@@ -372,6 +498,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
                 }
             }
         }
+      }
     } else if (warp < kWarpEpi0 + S::kEW) {
         // ---- epilogue: thread = one feature of the tile, BT tokens ----------
         // With two warps per lane quarter (kSplit = 2), the warp `half` takes
@@ -565,13 +692,17 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT> &L, c
 }
 
 // Prefetch of a phase's tensor-map descriptors (TMA and epilogue lanes).
-template <int EPI, bool PAIR, int BT>
+template <int EPI, bool PAIR, int BT, bool PLANE = false>
 __device__ __forceinline__ void gemm_prefetch_maps(const CUtensorMap &tmap_act, const CUtensorMap &tmap_in,
-                                                   const CUtensorMap &tmap_out32, const CUtensorMap &tmap_out16) {
-    using S = GemmShape<EPI, PAIR, BT>;
+                                                   const CUtensorMap &tmap_out32, const CUtensorMap &tmap_out16,
+                                                   const CUtensorMap *tmap_sgn = nullptr) {
+    using S = GemmShape<EPI, PAIR, BT, PLANE>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    if (warp == kWarpTma && lane == 0) tma_prefetch_desc(&tmap_act);
-    if (warp == kWarpEpi0 && lane == 0) {
+    if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_desc(&tmap_act);
+        if (PLANE) tma_prefetch_desc(tmap_sgn);
+    }
+    if (warp == S::kEpi0 && lane == 0) {
         if (EPI != kEpiFwd1) tma_prefetch_desc(&tmap_in);
         if (S::kHas32) tma_prefetch_desc(&tmap_out32);
         if (S::kHas16) tma_prefetch_desc(&tmap_out16);
@@ -583,21 +714,21 @@ __device__ __forceinline__ uint8_t *smem_base_1024() {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 }
 
-template <int EPI, bool PAIR, int BT>
-__global__ void __launch_bounds__(gemm_threads(EPI), 1)
+template <int EPI, bool PAIR, int BT, bool PLANE>
+__global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE>::kThreads, 1)
     blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ CUtensorMap tmap_in,
                     const __grid_constant__ CUtensorMap tmap_out32, const __grid_constant__ CUtensorMap tmap_out16,
-                    const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmap_sgn, const GemmArgs args) {
     uint8_t *smem = smem_base_1024();
     GemmCtl *ctl = reinterpret_cast<GemmCtl *>(smem);
-    const GemmLayout<EPI, PAIR, BT> L(smem + kCtlBytes);
+    const GemmLayout<EPI, PAIR, BT, PLANE> L(smem + kCtlBytes);
     const int warp = threadIdx.x / 32;
     if (threadIdx.x == 0) {
         L.init_barriers();
         ctl->abort_flag = 0;
         fence_mbar_init();
     }
-    gemm_prefetch_maps<EPI, PAIR, BT>(tmap_act, tmap_in, tmap_out32, tmap_out16);
+    gemm_prefetch_maps<EPI, PAIR, BT, PLANE>(tmap_act, tmap_in, tmap_out32, tmap_out16, &tmap_sgn);
     if constexpr (PAIR) {
         cluster_sync();  // both CTAs' barriers exist before any remote arrival
         if (warp == kWarpMma) {
@@ -619,8 +750,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     pdl_launch_dependents();
     const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // tile worker (CTA or pair)
     const int num_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-    gemm_roles<EPI, PAIR, BT>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
-                              reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units);
+    gemm_roles<EPI, PAIR, BT, PLANE>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
+                                     reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units, &tmap_sgn);
     tc_fence_before();
     if constexpr (PAIR) {
         // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it
@@ -634,12 +765,12 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     }
 }
 
-template <int EPI, bool PAIR, int BT>
+template <int EPI, bool PAIR, int BT, bool PLANE = false>
 cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, cudaStream_t s) {
-    using S = GemmShape<EPI, PAIR, BT>;
+    using S = GemmShape<EPI, PAIR, BT, PLANE>;
     static bool attr_set = false;  // set once, outside any later stream capture
     if (!attr_set) {
-        cudaError_t e = prepare_kernel(blr_gemm_kernel<EPI, PAIR, BT>, S::kSmemBytes);
+        cudaError_t e = prepare_kernel(blr_gemm_kernel<EPI, PAIR, BT, PLANE>, S::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -657,14 +788,19 @@ cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = PAIR ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, blr_gemm_kernel<EPI, PAIR, BT>, maps.act, maps.in32, maps.out32, maps.out16,
-                              args);
+    return cudaLaunchKernelEx(&cfg, blr_gemm_kernel<EPI, PAIR, BT, PLANE>, maps.act, maps.in32, maps.out32,
+                              maps.out16, maps.sgn, args);
 }
 
 // Tile configurations: CTA pairs with 160 or 192 tokens per tile, single CTAs
 // with 128.
 template <int EPI>
 cudaError_t launch_gemm_epi(const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s) {
+    if (plan.plane) {
+        if (plan.pair && plan.bt == 256) return launch_gemm_t<EPI, true, 256, true>(maps, args, plan.grid, s);
+        if (!plan.pair && plan.bt == 128) return launch_gemm_t<EPI, false, 128, true>(maps, args, plan.grid, s);
+        return cudaErrorInvalidValue;
+    }
     if (plan.pair && plan.bt == 192) return launch_gemm_t<EPI, true, 192>(maps, args, plan.grid, s);
     if (plan.pair && plan.bt == 160) return launch_gemm_t<EPI, true, 160>(maps, args, plan.grid, s);
     if (!plan.pair && plan.bt == 128) return launch_gemm_t<EPI, false, 128>(maps, args, plan.grid, s);

@@ -51,12 +51,14 @@ cudaError_t launch_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, i
 // activations or are never stored):
 //  - kind 0 ("direct"): src is [N][K/32], bits already run along K;
 //  - kind 1 ("transpose"): src is [K][N/32], bits run along N.
+//  - kind 2 ("plane"): src is [N][K/32] with K = r, dst the +-1 f16 plane
+//    [N][K] (as u32 pairs) that plane-mode GEMMs read by TMA; Ns unused.
 struct SignPrep {
     const uint32_t *src;
     uint32_t *dst;
-    int N;     // operand rows (output features)
-    int K;     // reduction length
-    int kind;  // 0 direct, 1 transpose
+    int N;     // operand rows (output features; plane: bitmap rows)
+    int K;     // reduction length (plane: r)
+    int kind;  // 0 direct, 1 transpose, 2 plane
     int Ns;    // destination row stride, sign_rows(N)
 };
 
@@ -133,22 +135,29 @@ inline int sign_rows(int N) { return (N + 255) / 256 * 256; }
 // the f32 input (a-tape for db, x for dx', y when c accumulates into it),
 // out32 / out16 the f32 and f16 outputs (a and a.l, y and c, -, dx and -).
 // Maps a product does not use are left zero.
+// sgn: the sign plane of a plane-mode GEMM, f16 with 128-byte swizzle: for
+// the a- and db-products [K][N] read MN-major (box 64 features x 64 K), for
+// the c- and dx'-products [N][K] read K-major (box 64 K x 128 features).
 struct GemmMaps {
-    CUtensorMap act, in32, out32, out16;
+    CUtensorMap act, in32, out32, out16, sgn;
 };
 
 // Tile plan of one GEMM launch: CTA pairs (tcgen05 cta_group::2) with 160 or
 // 192 tokens per tile, or single CTAs with 128; grid = persistent CTAs (even
 // for pairs); part_rows = token tiles (the epilogue writes
 // epi_part_rows_per_tile rows of partial sums per token tile).
+// plane = true: the sign operand is a +-1 f16 plane read by TMA (single CTAs,
+// bt = 128, 192 or 256); false: bitmap words expanded into TMEM.
 struct GemmPlan {
     bool pair;
     int bt;
     int grid;
     int part_rows;
+    bool plane;
 };
 
-GemmPlan plan_gemm(int M, int N, int sms);
+GemmPlan plan_gemm(int M, int N, int sms);        // TMEM-expansion tiles
+GemmPlan plan_gemm_plane(int M, int N, int sms);  // plane tiles
 
 cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
 

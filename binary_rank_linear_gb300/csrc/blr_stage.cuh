@@ -18,6 +18,10 @@ namespace blr {
 __host__ __device__ __forceinline__ int prep_kwords(int K) { return 4 * ((K + 127) / 128); }
 
 __host__ __device__ __forceinline__ int prep_blocks(const SignPrep &p, int threads) {
+    if (p.kind == 2) {
+        const long long words = (long long)p.N * (p.K / 32);
+        return (int)((words + threads - 1) / threads);
+    }
     if (p.kind == 0) {
         const long long units = (long long)p.Ns * prep_kwords(p.K);
         return (int)((units + threads - 1) / threads);
@@ -42,6 +46,20 @@ __device__ inline void prep_share(const SignPrep &p0, const SignPrep &p1, int bl
 }
 
 __device__ inline void prep_run(const SignPrep &p, int block, int threads) {
+    if (p.kind == 2) {
+        // plane: one bitmap word -> 32 f16 signs (64 bytes) of its row, through
+        // the pair-ready transform and pair expansion of the TMEM expanders
+        const int words = p.K / 32;
+        const long long u = (long long)block * threads + threadIdx.x;
+        if (u >= (long long)p.N * words) return;
+        const uint32_t w = sign_word_pair_ready(p.src[u]);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.dst + u * 16);  // row n, ranks 32(u % words) ..
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(sign_pair(w, 4 * i), sign_pair(w, 4 * i + 1), sign_pair(w, 4 * i + 2),
+                                sign_pair(w, 4 * i + 3));
+        return;
+    }
     const int kw_total = prep_kwords(p.K);
     if (p.kind == 0) {
         // direct: src [N][K/32]

@@ -270,3 +270,29 @@ def test_fused_small_path(monkeypatch, name, M, d_in, d_out, r):
     t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     out = _run(t, gscale=0.0)
     _check_against_oracle(t, out, "(fused small-M path)")
+
+
+@pytest.mark.parametrize("src", ["plane", "tmem"])
+@pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 4600, 1024, 1568, 1280),
+                                                 ("ragged", 2100, 640, 4224, 256), ("small", 200, 128, 9216, 64)])
+def test_sign_source_modes(monkeypatch, src, name, M, d_in, d_out, r):
+    """Both sources of the sign operand (+-1 f16 planes read by TMA, or bitmap
+    words expanded into TMEM), each forced on single-CTA and CTA-pair tiles."""
+    monkeypatch.setenv("BLR_SIGN_SRC", src)
+    t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    out = _run(t, gscale=0.0)
+    _check_against_oracle(t, out, f"(sign source {src})")
+
+
+@pytest.mark.parametrize("src", ["plane", "tmem"])
+def test_sign_source_integer_grid_bit_exact(monkeypatch, src):
+    monkeypatch.setenv("BLR_SIGN_SRC", src)
+    M, d_in, d_out, r = 2100, 512, 4096, 160  # CTA-pair tiles in both forms
+    t = _integer_grid(M, d_in, d_out, r, seed=77)
+    out = _run(t, gscale=1.0)
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    fw = oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    assert out["status"] == 0
+    assert np.array_equal(out["y"], fw["y"].astype(np.float32))
+    assert np.array_equal(out["dx"], bw["dx"].astype(np.float32))
