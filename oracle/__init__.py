@@ -2,8 +2,10 @@
 from .blr_oracle import (  # noqa: F401
     adam_step,
     backward,
+    backward_paths,
     backward_sampled,
     forward,
+    forward_paths,
     pack_signs,
     plane_linear,
     rel_err,

@@ -24,7 +24,10 @@ function below cites the part of that page it restates:
   weight decay) with an optional frozen-entry mask, a gradient multiplier and
   optional steps relative to the parameter's magnitude;
 * ``plane_linear`` and ``mm``: a dense frozen linear y = x . plane^T through
-  the f16 staging, or its transpose (input gradient) y = x . plane.
+  the f16 staging, or its transpose (input gradient) y = x . plane;
+* ``Blr`` (a layer is y = sum_p W_hat_p x over its paths) and ``blr_forward``
+  / ``blr_backward``'s path loops: path 0 overwrites y and dx, later paths
+  add, and each path keeps its own dh, dl, dg.
 
 Precision: inputs are f32 on the page; they are widened to f64 here and every
 step runs in f64. There is no staging, no f16 and no scaling in the oracle: the
@@ -52,6 +55,8 @@ __all__ = [
     "sign_grads_sampled",
     "adam_step",
     "plane_linear",
+    "forward_paths",
+    "backward_paths",
     "rel_err",
 ]
 
@@ -286,6 +291,33 @@ def plane_linear(x, plane, transpose=False, y_prior=None) -> np.ndarray:
     x, p = _f64(x), _f64(plane)
     y = np.matmul(x, p) if transpose else np.matmul(x, p.T)
     return y if y_prior is None else _f64(y_prior) + y
+
+
+def forward_paths(x, paths, y_prior=None) -> dict:
+    """A multi-path layer y = sum_p W_hat_p x, in f64.
+
+    train_mm.rs, ``Blr`` and ``blr_forward`` (its loop over paths: path 0
+    overwrites y, later paths add). ``paths`` is a list of dicts with keys
+    bu, bv (bitmaps), g, l, h. Returns y and the per-path forward dicts.
+    """
+    outs = [forward(x, p["bu"], p["bv"], p["g"], p["l"], p["h"]) for p in paths]
+    y = sum(o["y"] for o in outs)
+    if y_prior is not None:
+        y = _f64(y_prior) + y
+    return {"y": y, "paths": outs}
+
+
+def backward_paths(x, dy, paths, dx_prior=None) -> dict:
+    """Backward of a multi-path layer, in f64.
+
+    train_mm.rs, ``blr_backward``'s loop over paths: dx = sum_p dx_p (path 0
+    overwrites, later paths add) and each path's own dh, dl, dg.
+    """
+    outs = [backward(x, dy, p["bu"], p["bv"], p["g"], p["l"], p["h"]) for p in paths]
+    dx = sum(o["dx"] for o in outs)
+    if dx_prior is not None:
+        dx = _f64(dx_prior) + dx
+    return {"dx": dx, "paths": outs}
 
 
 def rel_err(got, want) -> float:

@@ -575,3 +575,56 @@ def test_planted_plane_mistakes_are_caught(mutant, monkeypatch):
     monkeypatch.setattr(oracle, "plane_linear", broken)
     with pytest.raises(AssertionError):
         test_plane_linear_loops()
+
+
+# ------------------------------------------------------------ multi-path ---
+def _two_paths(seed, M=4, d_in=6, d_out=5, r=36):
+    a, b = _tiny(seed, M, d_in, d_out, r), _tiny(seed + 100, M, d_in, d_out, r)
+    return a["x"], a["dy"], [a, b]
+
+
+def test_paths_dense_brute_force():
+    """y = x W^T and dx = dy W with W = sum_p diag(h_p) S_U,p diag(l_p) S_V,p^T diag(g_p),
+    W built element by element."""
+    x, dy, paths = _two_paths(31)
+    d_in, d_out, r = 6, 5, 36
+    W = np.zeros((d_out, d_in))
+    for p in paths:
+        for i in range(d_out):
+            for j in range(d_in):
+                W[i, j] += sum(float(p["h"][i]) * float(p["su"][i, k]) * float(p["l"][k]) * float(p["sv"][j, k])
+                               * float(p["g"][j]) for k in range(r))
+    fw = oracle.forward_paths(x, paths)
+    bw = oracle.backward_paths(x, dy, paths)
+    assert np.allclose(fw["y"], x.astype(np.float64) @ W.T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(bw["dx"], dy.astype(np.float64) @ W, rtol=1e-12, atol=1e-12)
+
+
+def test_paths_equal_one_path_of_double_rank():
+    """With shared g and h, two rank-r paths are one rank-2r path whose signs
+    and l are the two paths' side by side."""
+    x, dy, paths = _two_paths(32, r=64)
+    a, b = paths
+    b = dict(b, g=a["g"], h=a["h"])
+    cat = {k: np.concatenate([a[k], b[k]], axis=1) for k in ("su", "sv")}
+    bu, bv = oracle.pack_signs(cat["su"]), oracle.pack_signs(cat["sv"])
+    lcat = np.concatenate([a["l"], b["l"]])
+    one = oracle.forward(x, bu, bv, a["g"], lcat, a["h"])
+    two = oracle.forward_paths(x, [a, b])
+    assert np.allclose(two["y"], one["y"], rtol=1e-13, atol=1e-13)
+    onb = oracle.backward(x, dy, bu, bv, a["g"], lcat, a["h"])
+    twb = oracle.backward_paths(x, dy, [a, b])
+    assert np.allclose(twb["dx"], onb["dx"], rtol=1e-13, atol=1e-13)
+    # per-path gradients: dl splits by path, dg and dh add up over the paths
+    assert np.allclose(np.concatenate([twb["paths"][0]["dl"], twb["paths"][1]["dl"]]), onb["dl"], rtol=1e-13)
+    assert np.allclose(twb["paths"][0]["dg"] + twb["paths"][1]["dg"], onb["dg"], rtol=1e-12, atol=1e-13)
+    assert np.allclose(twb["paths"][0]["dh"] + twb["paths"][1]["dh"], onb["dh"], rtol=1e-12, atol=1e-13)
+
+
+def test_paths_priors():
+    x, dy, paths = _two_paths(33)
+    yp = np.ones((4, 5))
+    dxp = np.full((4, 6), 2.0)
+    assert np.allclose(oracle.forward_paths(x, paths, y_prior=yp)["y"], oracle.forward_paths(x, paths)["y"] + 1.0)
+    assert np.allclose(oracle.backward_paths(x, dy, paths, dx_prior=dxp)["dx"],
+                       oracle.backward_paths(x, dy, paths)["dx"] + 2.0)
