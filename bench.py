@@ -350,6 +350,7 @@ def run_gpu(args, rank, world, local_rank):
         if not args.no_sign else None
     adam = measure_adam(blr, torch.cat([dg, dl, dh]), args.steps, hbm_peak, dev)
     plane = measure_plane(blr, sets[0], args.steps, tc_peak, M, d_in, d_out, dev) if not args.no_plane else None
+    paths = measure_paths(blr, sets[0], bu, bv, g, l, h, args.steps, tc_peak, w, dev) if not args.no_paths else None
 
     # end-to-end: host buffers through the public API, copies inside the timed region
     xh = torch.from_numpy(t["x"]).pin_memory()
@@ -419,7 +420,38 @@ def run_gpu(args, rank, world, local_rank):
     result["adam"] = adam
     if plane is not None:
         result["plane_linear"] = plane
+    if paths is not None:
+        paths["vs_one_path"] = paths["us_per_step"] / (ms / args.steps * 1e3)
+        result["paths"] = paths
     return result
+
+
+def measure_paths(blr, s, bu, bv, g, l, h, steps, tc_peak, w, dev):
+    """A two-path layer (blr_forward_paths + blr_backward_paths) on the
+    workload's shape: path 0 with the step's bitmaps, path 1 with random ones;
+    its own calls after the step."""
+    import torch
+    M, d_in, d_out, r = w.M, w.d_in, w.d_out, w.r
+    gen = torch.Generator(device=dev).manual_seed(9)
+    rb = lambda rows: torch.randint(-2**31, 2**31 - 1, (rows, (r + 31) // 32), dtype=torch.int32, device=dev,  # noqa: E731
+                                    generator=gen)
+    paths = [{"bu": bu, "bv": bv, "g": g, "l": l, "h": h},
+             {"bu": rb(d_out), "bv": rb(d_in), "g": g, "l": l, "h": h}]
+    grads = [{"dg": torch.zeros(d_in, device=dev), "dl": torch.zeros(r, device=dev),
+              "dh": torch.zeros(d_out, device=dev)} for _ in paths]
+    ws = blr.alloc_paths_workspace(2, M, d_in, d_out, r, device=dev)
+
+    def call(i):
+        blr.forward_paths(s["x"], paths, s["y"], ws)
+        blr.backward_paths(s["x"], s["dy"], paths, s["dx"], grads, ws)
+
+    for i in range(3):
+        call(i)
+    ms = time_queued(call, steps)
+    flops = 2 * w.flops
+    return {"what": "two-path layer forward+backward (blr_forward_paths, blr_backward_paths), its own calls",
+            "P": 2, "us_per_step": ms * 1e3, "tokens_per_s": M / (ms * 1e-3),
+            "tflops": flops / (ms * 1e-3) / 1e12, "tensor_frac": flops / (ms * 1e-3) / 1e12 / tc_peak}
 
 
 def measure_plane(blr, s, steps, tc_peak, M, d_in, d_out, dev):
@@ -541,6 +573,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sign", action="store_true", help="skip the sign-gradient measurement")
     ap.add_argument("--no-plane", action="store_true", help="skip the plane_linear measurement")
+    ap.add_argument("--no-paths", action="store_true", help="skip the two-path layer measurement")
     ap.add_argument("--small-path", default="general", choices=["general", "fused"],
                     help="kernels for small problems: stand-alone (default) or the fused cooperative pair")
     args = ap.parse_args()

@@ -16,15 +16,20 @@ from ._binding import (  # noqa: F401
     BLR_OK,
     BlrError,
     adam,
+    alloc_paths_workspace,
     alloc_plane_workspace,
     alloc_sign_workspace,
     alloc_workspace,
     backward,
+    backward_paths,
     check_status,
     forward,
+    forward_paths,
     forward_noalloc,
     load,
     pack_signs,
+    path_workspace,
+    paths_workspace_bytes,
     plane_linear,
     plane_workspace_bytes,
     sign_grads,

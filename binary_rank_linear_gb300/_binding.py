@@ -58,6 +58,11 @@ def load() -> ctypes.CDLL:
     lib.blr_sign_workspace_bytes.restype = Z
     lib.blr_sign_grads.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, Z, P]
     lib.blr_adam.argtypes = [P, P, P, P, P, I, I, F, F, F, F, F, F, P]
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    lib.blr_paths_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.blr_paths_workspace_bytes.restype = Z
+    lib.blr_forward_paths.argtypes = [P, I, PP, PP, PP, PP, PP, P, I, I, I, I, I, P, Z, P]
+    lib.blr_backward_paths.argtypes = [P, P, I, PP, PP, PP, PP, PP, P, I, PP, PP, PP, F, I, I, I, I, P, Z, P]
     lib.blr_plane_workspace_bytes.argtypes = [I, I, I]
     lib.blr_plane_workspace_bytes.restype = Z
     lib.blr_plane_linear.argtypes = [P, P, P, I, I, F, I, I, I, P, Z, P]
@@ -67,7 +72,8 @@ def load() -> ctypes.CDLL:
     lib.blr_trace_begin.argtypes = [I]
     lib.blr_trace_read.argtypes = [I, ctypes.POINTER(ctypes.c_float)]
     lib.blr_trace_read.restype = ctypes.c_char_p
-    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_sign_grads", "blr_adam", "blr_plane_linear", "blr_check_status",
+    for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_sign_grads", "blr_adam", "blr_plane_linear", "blr_forward_paths", "blr_backward_paths",
+              "blr_check_status",
               "blr_trace_begin", "blr_trace_end", "blr_trace_count"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -168,6 +174,70 @@ def backward(x, dy, bits_u, bits_v, g, l, h, dx, dg, dl, dh, ws, gscale: float =
         _ptr(dh, "dh", torch.float32, (d_out,)), float(gscale), M, d_in, d_out, r,
         _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
     _check(code, "blr_backward")
+    return dx
+
+
+def paths_workspace_bytes(P: int, M: int, d_in: int, d_out: int, r: int) -> int:
+    return int(load().blr_paths_workspace_bytes(P, M, d_in, d_out, r))
+
+
+def alloc_paths_workspace(P: int, M: int, d_in: int, d_out: int, r: int, device=None) -> torch.Tensor:
+    n = paths_workspace_bytes(P, M, d_in, d_out, r)
+    if n == 0:
+        raise BlrError(BLR_ERR_SHAPE, "paths_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def path_workspace(ws: torch.Tensor, p: int, M: int, d_in: int, d_out: int, r: int) -> torch.Tensor:
+    """Path p's slice of a multi-path workspace (its tape, e.g. for sign_grads)."""
+    one = workspace_bytes(M, d_in, d_out, r)
+    return ws[p * one:(p + 1) * one]
+
+
+def _ptr_array(tensors, name, dtype, shape):
+    arr = (ctypes.c_void_p * len(tensors))()
+    for i, t in enumerate(tensors):
+        arr[i] = _ptr(t, f"{name}[{i}]", dtype, shape)
+    return arr
+
+
+def forward_paths(x, paths, y, ws, accumulate: bool = False, stream=None) -> torch.Tensor:
+    """y (+)= sum_p W_hat_p x; ``paths`` is a list of dicts with bu, bv, g, l, h."""
+    M, d_in = x.shape
+    d_out, r = paths[0]["h"].shape[0], paths[0]["l"].shape[0]
+    w, P = words_per_row(r), len(paths)
+    code = load().blr_forward_paths(
+        _ptr(x, "x", torch.float32, (M, d_in)), P,
+        _ptr_array([p["bu"] for p in paths], "bu", torch.int32, (d_out, w)),
+        _ptr_array([p["bv"] for p in paths], "bv", torch.int32, (d_in, w)),
+        _ptr_array([p["g"] for p in paths], "g", torch.float32, (d_in,)),
+        _ptr_array([p["l"] for p in paths], "l", torch.float32, (r,)),
+        _ptr_array([p["h"] for p in paths], "h", torch.float32, (d_out,)),
+        _ptr(y, "y", torch.float32, (M, d_out)), int(bool(accumulate)), M, d_in, d_out, r,
+        _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check(code, "blr_forward_paths")
+    return y
+
+
+def backward_paths(x, dy, paths, dx, grads, ws, gscale: float = 0.0, accumulate: bool = False,
+                   stream=None) -> torch.Tensor:
+    """dx (+)= sum_p dx_p; ``grads`` is a list of dicts with dg, dl, dh per path (always +=)."""
+    M, d_in = x.shape
+    d_out, r = paths[0]["h"].shape[0], paths[0]["l"].shape[0]
+    w, P = words_per_row(r), len(paths)
+    code = load().blr_backward_paths(
+        _ptr(x, "x", torch.float32, (M, d_in)), _ptr(dy, "dy", torch.float32, (M, d_out)), P,
+        _ptr_array([p["bu"] for p in paths], "bu", torch.int32, (d_out, w)),
+        _ptr_array([p["bv"] for p in paths], "bv", torch.int32, (d_in, w)),
+        _ptr_array([p["g"] for p in paths], "g", torch.float32, (d_in,)),
+        _ptr_array([p["l"] for p in paths], "l", torch.float32, (r,)),
+        _ptr_array([p["h"] for p in paths], "h", torch.float32, (d_out,)),
+        _ptr(dx, "dx", torch.float32, (M, d_in)), int(bool(accumulate)),
+        _ptr_array([q["dg"] for q in grads], "dg", torch.float32, (d_in,)),
+        _ptr_array([q["dl"] for q in grads], "dl", torch.float32, (r,)),
+        _ptr_array([q["dh"] for q in grads], "dh", torch.float32, (d_out,)),
+        float(gscale), M, d_in, d_out, r, _ptr(ws, "ws", torch.uint8), ws.numel(), _stream(stream))
+    _check(code, "blr_backward_paths")
     return dx
 
 

@@ -344,6 +344,27 @@ bool fused_small_enabled() {
     return v && std::strcmp(v, "fused") == 0;
 }
 
+// The per-path pointers of a multi-path call: every array present, every entry
+// non-null and 16-byte aligned.
+template <typename T>
+bool path_ptrs_ok(T *const *a, int P, int *status) {
+    if (!a) {
+        *status = BLR_ERR_ARG;
+        return false;
+    }
+    for (int p = 0; p < P; ++p) {
+        if (!a[p]) {
+            *status = BLR_ERR_ARG;
+            return false;
+        }
+        if (!aligned16(a[p])) {
+            *status = BLR_ERR_ALIGN;
+            return false;
+        }
+    }
+    return true;
+}
+
 }  // namespace blr
 
 using namespace blr;
@@ -611,6 +632,68 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     ReduceSeg sh{part_dh, dh, rows_dh, d_out};
     if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
     mark_backward_done(ws, gscale, rows_dh);
+    return BLR_OK;
+}
+
+size_t blr_paths_workspace_bytes(int P, int M, int d_in, int d_out, int r) {
+    if (P < 1 || P > 64 || !shape_ok(M, d_in, d_out, r)) return 0;
+    return (size_t)P * make_layout(M, d_in, d_out, r).total;
+}
+
+
+int blr_forward_paths(const float *x, int P, const uint32_t *const *bits_u, const uint32_t *const *bits_v,
+                      const float *const *g, const float *const *l, const float *const *h, float *y,
+                      int accumulate_y, int M, int d_in, int d_out, int r, void *ws, size_t ws_bytes,
+                      blr_stream_t stream) {
+    if (P < 1 || P > 64 || !x || !y || !ws) return BLR_ERR_ARG;
+    if (accumulate_y != 0 && accumulate_y != 1) return BLR_ERR_ARG;
+    if (!shape_ok(M, d_in, d_out, r)) return BLR_ERR_SHAPE;
+    int st = BLR_OK;
+    if (!path_ptrs_ok(bits_u, P, &st) || !path_ptrs_ok(bits_v, P, &st) || !path_ptrs_ok(g, P, &st) ||
+        !path_ptrs_ok(l, P, &st) || !path_ptrs_ok(h, P, &st))
+        return st;
+    const size_t one = make_layout(M, d_in, d_out, r).total;
+    if (ws_bytes < (size_t)P * one) return BLR_ERR_WORKSPACE;
+    for (int p = 0; p < P; ++p) {
+        st = blr_forward(x, bits_u[p], bits_v[p], g[p], l[p], h[p], y, (p > 0 || accumulate_y) ? 1 : 0, M, d_in,
+                         d_out, r, static_cast<char *>(ws) + (size_t)p * one, one, stream);
+        if (st != BLR_OK) return st;
+    }
+    return BLR_OK;
+}
+
+int blr_backward_paths(const float *x, const float *dy, int P, const uint32_t *const *bits_u,
+                       const uint32_t *const *bits_v, const float *const *g, const float *const *l,
+                       const float *const *h, float *dx, int accumulate_dx, float *const *dg, float *const *dl,
+                       float *const *dh, float gscale, int M, int d_in, int d_out, int r, void *ws,
+                       size_t ws_bytes, blr_stream_t stream) {
+    if (P < 1 || P > 64 || !x || !dy || !dx || !ws) return BLR_ERR_ARG;
+    if (accumulate_dx != 0 && accumulate_dx != 1) return BLR_ERR_ARG;
+    if (std::isnan(gscale) || (gscale > 0.0f && !pow2_positive(gscale))) return BLR_ERR_ARG;
+    if (!shape_ok(M, d_in, d_out, r)) return BLR_ERR_SHAPE;
+    int st = BLR_OK;
+    if (!path_ptrs_ok(bits_u, P, &st) || !path_ptrs_ok(bits_v, P, &st) || !path_ptrs_ok(g, P, &st) ||
+        !path_ptrs_ok(l, P, &st) || !path_ptrs_ok(h, P, &st) || !path_ptrs_ok(dg, P, &st) ||
+        !path_ptrs_ok(dl, P, &st) || !path_ptrs_ok(dh, P, &st))
+        return st;
+    const size_t one = make_layout(M, d_in, d_out, r).total;
+    if (ws_bytes < (size_t)P * one) return BLR_ERR_WORKSPACE;
+    {
+        // every path's tape must be there before any path's backward is queued
+        std::lock_guard<std::mutex> lk(g_tape_mu);
+        for (int p = 0; p < P; ++p) {
+            auto it = g_tapes.find(static_cast<char *>(ws) + (size_t)p * one);
+            if (it == g_tapes.end() || it->second.M != M || it->second.d_in != d_in || it->second.d_out != d_out ||
+                it->second.r != r)
+                return BLR_ERR_STATE;
+        }
+    }
+    for (int p = 0; p < P; ++p) {
+        st = blr_backward(x, dy, bits_u[p], bits_v[p], g[p], l[p], h[p], dx, (p > 0 || accumulate_dx) ? 1 : 0, dg[p],
+                          dl[p], dh[p], gscale, M, d_in, d_out, r, static_cast<char *>(ws) + (size_t)p * one, one,
+                          stream);
+        if (st != BLR_OK) return st;
+    }
     return BLR_OK;
 }
 

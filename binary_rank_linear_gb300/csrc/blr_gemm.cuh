@@ -511,7 +511,9 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         const int nc = (kChunks - half + kSplit - 1) / kSplit;  // this warp's chunks per tile
         uint8_t *slots = sE + ew * kNE * S::kSlotBytes;
         uint64_t *ebar = eload + ew * kNE;
-        const bool has_in = (EPI == kEpiBwd1) || (EPI == kEpiBwd2) || (EPI == kEpiFwd2 && args.accumulate);
+        // inputs: the a-tape (db) or x (dx'); y and dx accumulate by reduce-add stores
+        const bool has_in = (EPI == kEpiBwd1) || (EPI == kEpiBwd2);
+        const bool add_out = (EPI == kEpiFwd2 || EPI == kEpiBwd2) && args.accumulate;
         uint32_t pending = 0u;  // lane 0: slots with an input load not yet waited on
         uint32_t ppar = 0u;     // and that load's phase parity
         // the warp's chunk g: local tile g / nc, chunk half + kSplit * (g % nc)
@@ -628,13 +630,11 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                         s16[j * 32 + lane] = f16_bits(x * cf);
                     }
                 } else if constexpr (EPI == kEpiFwd2) {
-                    // y (+)= h.c, c saved in f16
+                    // y (+)= h.c (accumulate: the store adds), c saved in f16
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float x = __uint_as_float(v[j]);
-                        float yv = cf * x;
-                        if (has_in) yv += s32[j * 32 + lane];
-                        s32[j * 32 + lane] = yv;
+                        s32[j * 32 + lane] = cf * x;
                         s16[j * 32 + lane] = f16_bits(x);
                     }
                 } else if constexpr (EPI == kEpiBwd1) {
@@ -656,18 +656,18 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                         psum += s32[j * 32 + lane] * dxp;
                         s32[j * 32 + lane] = cf * dxp;
                     }
-                    if (args.accumulate && fvalid) {
-                        // dx += (rare mode): the prior dx of the chunk's valid tokens
-                        const int jn = M - tc < 32 ? M - tc : 32;
-                        for (int j = 0; j < jn; ++j) s32[j * 32 + lane] += args.out32[(size_t)(tc + j) * N + f];
-                    }
                 }
                 // chunk staged: one TMA store per output (rows past M and
                 // features past N are clipped; wholly outside boxes are skipped)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && tc < M && fq < N) {
-                    if constexpr (S::kHas32) tma_store_2d(&tmap_out32, s32, fq, tc);
+                    if constexpr (S::kHas32) {
+                        if (add_out)
+                            tma_reduce_add_2d(&tmap_out32, s32, fq, tc);  // y or dx += the chunk
+                        else
+                            tma_store_2d(&tmap_out32, s32, fq, tc);
+                    }
                     if constexpr (S::kHas16) tma_store_2d(&tmap_out16, s16, fq, tc);
                 }
                 if (lane == 0) bulk_commit_group();

@@ -142,6 +142,37 @@ BLR_API int blr_backward(const float *x, const float *dy,
                  int M, int d_in, int d_out, int r,
                  void *ws, size_t ws_bytes, blr_stream_t stream);
 
+/* Multi-path layers (train_mm.rs, Blr: y = sum_p W_hat_p x over P paths of
+ * the same shape; blr_forward / blr_backward loop over the paths, path 0
+ * overwriting y and dx and later paths adding, each path with its own
+ * bitmaps, g, l, h and gradients dg, dl, dh).
+ *
+ * blr_paths_workspace_bytes: P single-path workspaces side by side; path p's
+ * slice starts at p * blr_workspace_bytes(M, d_in, d_out, r) (a multiple of
+ * 256) and holds that path's tape, so blr_sign_grads(..., ws + offset_p, ...)
+ * gives path p's sign gradients after blr_backward_paths.
+ *
+ * blr_forward_paths / blr_backward_paths take host arrays of P device
+ * pointers (bits_u[p], ..., dg[p]) and run each path's kernels in turn on
+ * `stream` (path p > 0 accumulates into y and dx; accumulate_y/accumulate_dx
+ * = 1 makes path 0 accumulate too). Every argument is checked before the
+ * first launch, so an argument error changes nothing; a launch failure part
+ * way leaves the earlier paths' results in place. P in [1, 64]; the rest as
+ * blr_forward / blr_backward. */
+BLR_API size_t blr_paths_workspace_bytes(int P, int M, int d_in, int d_out, int r);
+BLR_API int blr_forward_paths(const float *x, int P,
+                              const uint32_t *const *bits_u, const uint32_t *const *bits_v,
+                              const float *const *g, const float *const *l, const float *const *h,
+                              float *y, int accumulate_y, int M, int d_in, int d_out, int r,
+                              void *ws, size_t ws_bytes, blr_stream_t stream);
+BLR_API int blr_backward_paths(const float *x, const float *dy, int P,
+                               const uint32_t *const *bits_u, const uint32_t *const *bits_v,
+                               const float *const *g, const float *const *l, const float *const *h,
+                               float *dx, int accumulate_dx,
+                               float *const *dg, float *const *dl, float *const *dh,
+                               float gscale, int M, int d_in, int d_out, int r,
+                               void *ws, size_t ws_bytes, blr_stream_t stream);
+
 /* Bytes of the second workspace blr_sign_grads needs for this shape (0 when
  * the shape violates the shape rule): the rank-side f16 operands rescaled to
  * one gradient scale, 4*M*r bytes plus a 256-byte header. */

@@ -182,6 +182,36 @@ def test_plane_linear_argument_errors(lib):
     assert _plane(lib, wsb=512) == blr.BLR_ERR_WORKSPACE
 
 
+def test_paths_argument_errors(lib):
+    import ctypes as C
+    import binary_rank_linear_gb300 as blr
+    one = lib.blr_workspace_bytes(64, 128, 128, 64)
+    assert lib.blr_paths_workspace_bytes(3, 64, 128, 128, 64) == 3 * one
+    assert lib.blr_paths_workspace_bytes(0, 64, 128, 128, 64) == 0
+    assert lib.blr_paths_workspace_bytes(65, 64, 128, 128, 64) == 0
+    arr = lambda *v: (C.c_void_p * len(v))(*v)  # noqa: E731
+    good = arr(FAKE, FAKE)
+
+    def fwd(P=2, bu=good, y=FAKE, wsb=1 << 40, r=64):
+        return lib.blr_forward_paths(FAKE, P, bu, good, good, good, good, y, 0, 64, 128, 128, r, FAKE + 16384, wsb,
+                                     None)
+
+    assert fwd(P=0) == blr.BLR_ERR_ARG
+    assert fwd(bu=None) == blr.BLR_ERR_ARG
+    assert fwd(bu=arr(FAKE, None)) == blr.BLR_ERR_ARG
+    assert fwd(bu=arr(FAKE, FAKE + 4)) == blr.BLR_ERR_ALIGN
+    assert fwd(r=40) == blr.BLR_ERR_SHAPE
+    assert fwd(wsb=one) == blr.BLR_ERR_WORKSPACE
+
+    def bwd(dl=good, gs=0.0):
+        return lib.blr_backward_paths(FAKE, FAKE, 2, good, good, good, good, good, FAKE, 0, good, dl, good, gs, 64,
+                                      128, 128, 64, FAKE + 32768, 1 << 40, None)
+
+    assert bwd(dl=arr(None, FAKE)) == blr.BLR_ERR_ARG
+    assert bwd(gs=3.0) == blr.BLR_ERR_ARG
+    assert bwd() == blr.BLR_ERR_STATE  # no forward ran on these workspace slices
+
+
 def test_pack_argument_errors(lib):
     import binary_rank_linear_gb300 as blr
     assert lib.blr_pack_signs(None, FAKE, 4, 64, None) == blr.BLR_ERR_ARG

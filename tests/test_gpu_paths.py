@@ -1,0 +1,105 @@
+"""GPU parity of multi-path layers (blr_forward_paths / blr_backward_paths)
+against the CPU f64 oracle: y and dx sum over the paths (tolerance 2e-3),
+each path keeps its own dh, dl, dg (5e-3), as the single-path calls do."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from binary_rank_linear_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import binary_rank_linear_gb300 as blr
+    blr.load()
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _run_paths(x, dy, paths, gscale=0.0, y_prior=None, dx_prior=None):
+    import binary_rank_linear_gb300 as blr
+    M, d_in = x.shape
+    d_out, r = paths[0]["su"].shape
+    dp = [{"bu": blr.pack_signs(_dev(p["su"])), "bv": blr.pack_signs(_dev(p["sv"])), "g": _dev(p["g"]),
+           "l": _dev(p["l"]), "h": _dev(p["h"])} for p in paths]
+    grads = [{"dg": torch.zeros(d_in, device="cuda"), "dl": torch.zeros(r, device="cuda"),
+              "dh": torch.zeros(d_out, device="cuda")} for _ in paths]
+    ws = blr.alloc_paths_workspace(len(paths), M, d_in, d_out, r)
+    y = _dev(y_prior) if y_prior is not None else torch.full((M, d_out), float("nan"), device="cuda")
+    dx = _dev(dx_prior) if dx_prior is not None else torch.full((M, d_in), float("nan"), device="cuda")
+    blr.forward_paths(_dev(x), dp, y, ws, accumulate=y_prior is not None)
+    blr.backward_paths(_dev(x), _dev(dy), dp, dx, grads, ws, gscale=gscale, accumulate=dx_prior is not None)
+    for p in range(len(paths)):
+        assert blr.check_status(blr.path_workspace(ws, p, M, d_in, d_out, r)) == 0
+    return y.cpu().numpy(), dx.cpu().numpy(), [{k: v.cpu().numpy() for k, v in q.items()} for q in grads], ws
+
+
+def _oracle_paths(x, dy, paths, y_prior=None, dx_prior=None):
+    op = [{"bu": oracle.pack_signs(p["su"]), "bv": oracle.pack_signs(p["sv"]), "g": p["g"], "l": p["l"],
+           "h": p["h"]} for p in paths]
+    return oracle.forward_paths(x, op, y_prior), oracle.backward_paths(x, dy, op, dx_prior)
+
+
+def _check(x, dy, paths, got, y_prior=None, dx_prior=None):
+    y, dx, grads, _ = got
+    fw, bw = _oracle_paths(x, dy, paths, y_prior, dx_prior)
+    assert oracle.rel_err(y, fw["y"]) <= 2e-3
+    assert oracle.rel_err(dx, bw["dx"]) <= 2e-3
+    for q, want in zip(grads, bw["paths"]):
+        for k in ("dg", "dl", "dh"):
+            assert oracle.rel_err(q[k], want[k]) <= 5e-3, k
+
+
+def test_pages_two_paths():
+    """The page's two-path layer: d_out 256, d_in 384, r 128, 70 tokens, gscale 1024."""
+    p0, p1 = wl.pages_case(0), wl.pages_case(1)
+    got = _run_paths(p0["x"], p0["dy"], [p0, p1], gscale=1024.0)
+    _check(p0["x"], p0["dy"], [p0, p1], got)
+
+
+@pytest.mark.parametrize("P,M,d_in,d_out,r", [(3, 300, 320, 448, 96), (2, 4600, 1024, 1568, 256),
+                                              (4, 129, 192, 96, 64)])
+def test_paths_parity(P, M, d_in, d_out, r):
+    """P paths with their own signs and vectors on one x and dy."""
+    base = wl.make_inputs(wl.WORKLOADS["small"].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    rng = np.random.default_rng(M + P)
+    paths = []
+    for _ in range(P):
+        q = dict(base)
+        q["su"] = np.where(rng.random(base["su"].shape) < 0.5, 1.0, -1.0).astype(np.float32)
+        q["sv"] = np.where(rng.random(base["sv"].shape) < 0.5, 1.0, -1.0).astype(np.float32)
+        q["g"] = (1 + 0.1 * rng.standard_normal(d_in)).astype(np.float32)
+        q["h"] = (1 + 0.1 * rng.standard_normal(d_out)).astype(np.float32)
+        q["l"] = (base["l"] * rng.uniform(0.5, 1.5, r)).astype(np.float32)
+        paths.append(q)
+    x, dy = base["x"], base["dy"]
+    _check(x, dy, paths, _run_paths(x, dy, paths))
+
+
+def test_paths_accumulate_and_sign_grads():
+    """Priors in y and dx (accumulate mode), and each path's sign gradients
+    from its slice of the workspace."""
+    import binary_rank_linear_gb300 as blr
+    p0, p1 = wl.pages_case(0), wl.pages_case(1)
+    rng = np.random.default_rng(4)
+    yp = rng.standard_normal((70, 256)).astype(np.float32)
+    dxp = rng.standard_normal((70, 384)).astype(np.float32)
+    got = _run_paths(p0["x"], p0["dy"], [p0, p1], y_prior=yp, dx_prior=dxp)
+    _check(p0["x"], p0["dy"], [p0, p1], got, y_prior=yp, dx_prior=dxp)
+    ws = got[3]
+    for p, path in enumerate((p0, p1)):
+        wsp = blr.path_workspace(ws, p, 70, 384, 256, 128)
+        sws = blr.alloc_sign_workspace(70, 384, 256, 128)
+        gu, gv = torch.empty(256, 128, device="cuda"), torch.empty(384, 128, device="cuda")
+        blr.sign_grads(_dev(p0["x"]), _dev(path["g"]), _dev(path["l"]), gu, gv, wsp, sws)
+        want = oracle.sign_grads(p0["x"], p0["dy"], oracle.pack_signs(path["su"]), oracle.pack_signs(path["sv"]),
+                                 path["g"], path["l"], path["h"])
+        assert oracle.rel_err(gu.cpu().numpy(), want["gu"]) <= 3e-3
+        assert oracle.rel_err(gv.cpu().numpy(), want["gv"]) <= 3e-3
