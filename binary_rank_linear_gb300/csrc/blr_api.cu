@@ -145,6 +145,20 @@ bool make_tmap_out_sw128(CUtensorMap *m, void *base, int rows, int cols) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows][cols] f16 with a 32 x 32 box and 64-byte swizzle (c from the
+// token-major c-product); stores are clipped to the extent.
+bool make_tmap_out16_sw64(CUtensorMap *m, void *base, int rows, int cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------ layout --------
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -195,7 +209,8 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     L.blkmax = take((size_t)L.rows_dh * 8);
     // partial rows per token tile (tiles of at least 128 tokens)
     L.rows_dl = (int)((m + 127) / 128) * epi_part_rows_per_tile(kEpiBwd1);
-    L.rows_dg = (int)((m + 127) / 128) * epi_part_rows_per_tile(kEpiBwd2);
+    // (the token-major dx'-product writes four per 128-token tile)
+    L.rows_dg = (int)((m + 127) / 128) * 4;
     L.part_dh = take((size_t)L.rows_dh * d_out * 4);
     L.part_dl = take((size_t)L.rows_dl * r * 4);
     L.part_dg = take((size_t)L.rows_dg * d_in * 4);
@@ -319,6 +334,20 @@ bool plane_mode() {
     return v && std::strcmp(v, "plane") == 0;
 }
 
+// The wide products (c: d_out outputs, dx': d_in outputs, K = r) run
+// feature-major on the sign GEMM (one thread per feature), or, with
+// BLR_WIDE=token, token-major on the dense tensor-core kernel (rows = tokens,
+// the sign plane as B: a thread owns a token row and writes it in 16-byte
+// pieces, h and g are per-column broadcasts, sigma_t a per-thread scalar, dg a
+// warp transpose-sum). Measured on GB300 the token-major form is slower on
+// every workload (attention-sized dx': 105 against 70 us; its epilogue keeps
+// one chunk of x in flight per warp, about 16 KB per SM, where the
+// feature-major one prefetches 64 KB), so it is not the default.
+bool wide_token_major() {
+    const char *v = std::getenv("BLR_WIDE");
+    return v && std::strcmp(v, "token") == 0;
+}
+
 // Grid of the fused small-M kernels: enough CTAs for the larger GEMM phase's
 // tiles (at least 16, for the staging phases), at most one per SM.
 int small_grid(const GemmPlan &p1, int N1, const GemmPlan &p2, int N2, int M, int sms) {
@@ -431,9 +460,26 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     const GemmPlan q2 = plan_gemm(M, d_out, sms);
     const bool fused = !q1.pair && !q2.pair && fused_small_enabled();
     const bool planes = !fused && plane_mode();
+    const bool dense2 = !fused && wide_token_major();
     const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : q1;
     const GemmPlan p2 = planes ? plan_gemm_plane(M, d_out, sms) : q2;
     GemmMaps m1{}, m2{};
+    DenseGemmLaunch d2{};
+    if (dense2) {
+        // c-product token-major: al16 [M][r] x S_U plane [d_out][r], both K-major
+        d2.F[0] = M;
+        d2.R = d_out;
+        d2.K = r;
+        d2.scale[0] = 1.0f;
+        d2.accumulate = accumulate_y;
+        d2.status = status;
+        d2.sms = sms;
+        d2.epm = 1;
+        d2.colv = h;
+        if (!make_tmap_act16(&d2.maps.a[0], al16, M, r, 128) || !make_tmap_act16(&d2.maps.b[0], plane_u, d_out, r, 256) ||
+            !make_tmap_out_sw128(&d2.maps.o[0], y, M, d_out) || !make_tmap_out16_sw64(&d2.maps.o16, c16, M, d_out))
+            return BLR_ERR_CUDA;
+    }
     // a-product: S_V [d_in][r] read MN-major; c-product: S_U [d_out][r] read K-major
     if (planes && (!make_tmap_act16(&m1.sgn, plane_v, d_in, r, 64) || !make_tmap_act16(&m2.sgn, plane_u, d_out, r, 128)))
         return BLR_ERR_CUDA;
@@ -455,6 +501,8 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     if (planes) {
         // both products read +-1 f16 planes in the bitmaps' own order
         pv = SignPrep{bits_v, reinterpret_cast<uint32_t *>(plane_v), d_in, r, 2, 0};
+        pu = SignPrep{bits_u, reinterpret_cast<uint32_t *>(plane_u), d_out, r, 2, 0};
+    } else if (dense2) {
         pu = SignPrep{bits_u, reinterpret_cast<uint32_t *>(plane_u), d_out, r, 2, 0};
     }
 
@@ -490,7 +538,11 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     } else {
         if (launch_fwd_prologue(pv, pu, x, g, x16, M, d_in, status, s) != cudaSuccess) return BLR_ERR_CUDA;
         if (launch_gemm(kEpiFwd1, p1, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
-        if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) return BLR_ERR_CUDA;
+        if (dense2) {
+            if (launch_dense_gemm(d2, "gemm_fwd2", s) != cudaSuccess) return BLR_ERR_CUDA;
+        } else if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) {
+            return BLR_ERR_CUDA;
+        }
     }
 
     std::lock_guard<std::mutex> lk(g_tape_mu);
@@ -544,9 +596,29 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     const GemmPlan q2 = plan_gemm(M, d_in, sms);
     const bool fused = !q1.pair && !q2.pair && small_bwd_fits(d_out) && fused_small_enabled();
     const bool planes = !fused && plane_mode();
+    const bool dense2 = !fused && wide_token_major();
     const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : q1;
     const GemmPlan p2 = planes ? plan_gemm_plane(M, d_in, sms) : q2;
     GemmMaps m1{}, m2{};
+    DenseGemmLaunch d2{};
+    if (dense2) {
+        // dx'-product token-major: db16 [M][r] x S_V plane [d_in][r], both K-major
+        d2.F[0] = M;
+        d2.R = d_in;
+        d2.K = r;
+        d2.scale[0] = 1.0f;
+        d2.accumulate = accumulate_dx;
+        d2.status = status;
+        d2.sms = sms;
+        d2.epm = 2;
+        d2.colv = g;
+        d2.row_inv = sig_inv;
+        d2.xin = x;
+        d2.part = part_dg;
+        if (!make_tmap_act16(&d2.maps.a[0], db16, M, r, 128) || !make_tmap_act16(&d2.maps.b[0], plane_v, d_in, r, 256) ||
+            !make_tmap_out_sw128(&d2.maps.o[0], dx, M, d_in))
+            return BLR_ERR_CUDA;
+    }
     // db-product: S_U [d_out][r] read MN-major; dx'-product: S_V [d_in][r] read K-major
     if (planes && (!make_tmap_act16(&m1.sgn, plane_u, d_out, r, 64) || !make_tmap_act16(&m2.sgn, plane_v, d_in, r, 128)))
         return BLR_ERR_CUDA;
@@ -561,6 +633,8 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     SignPrep pv{bits_v, bp_b2, d_in, r, 0, sign_rows(d_in)};
     if (planes) {
         pu = SignPrep{bits_u, reinterpret_cast<uint32_t *>(plane_u), d_out, r, 2, 0};
+        pv = SignPrep{bits_v, reinterpret_cast<uint32_t *>(plane_v), d_in, r, 2, 0};
+    } else if (dense2) {
         pv = SignPrep{bits_v, reinterpret_cast<uint32_t *>(plane_v), d_in, r, 2, 0};
     }
     StageDyArgs sa{};
@@ -608,7 +682,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b2.status = status;
 
     ReduceSeg sl{part_dl, dl, p1.part_rows * epi_part_rows_per_tile(kEpiBwd1), r};
-    ReduceSeg sg{part_dg, dg, p2.part_rows * epi_part_rows_per_tile(kEpiBwd2), d_in};
+    ReduceSeg sg{part_dg, dg, dense2 ? (M + 127) / 128 * 4 : p2.part_rows * epi_part_rows_per_tile(kEpiBwd2), d_in};
     if (fused) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallBwdArgs ba{};
@@ -628,7 +702,11 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     }
     if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
     if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
-    if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (dense2) {
+        if (launch_dense_gemm(d2, "gemm_bwd2", s) != cudaSuccess) return BLR_ERR_CUDA;
+    } else if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) {
+        return BLR_ERR_CUDA;
+    }
     ReduceSeg sh{part_dh, dh, rows_dh, d_out};
     if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
     mark_backward_done(ws, gscale, rows_dh);
@@ -739,8 +817,6 @@ int blr_sign_grads(const float *x, const float *g, const float *l, float *gu, fl
     DenseGemmLaunch gl{};
     gl.F[0] = d_out;
     gl.F[1] = d_in;
-    gl.out[0] = gu;
-    gl.out[1] = gv;
     gl.R = r;
     gl.K = M;  // the products sum over tokens
     gl.a_mn = gl.b_mn = true;
@@ -809,7 +885,6 @@ int blr_plane_linear(const float *x, const uint16_t *plane, float *y, int transp
     gl.F[0] = ntok;
     gl.F[1] = 0;
     gl.scale[0] = 1.0f / scale;
-    gl.out[0] = y;
     gl.R = nout;
     gl.K = kin;
     gl.accumulate = accumulate;

@@ -18,8 +18,19 @@ namespace blr {
 // x plane^T or MN-major for the transpose y = x plane).
 //
 // Warp 0 TMA producer, warp 1 MMA issuer (tcgen05 kind::f16), warps 2-5
-// epilogue: out = acc * scale (+ out), each 32 x 32 chunk staged in shared
-// memory (128-byte swizzle) and written by a TMA store.
+// epilogue (thread = one row f): each 32 x 32 chunk is staged in shared
+// memory (128-byte swizzle) and written by a TMA store, or by a TMA reduce-add
+// store in accumulate mode. Epilogue modes (EPM):
+//  0: out = acc * scale;
+//  1: the layer's c-product read token-major (rows = tokens, columns =
+//     output features, B = the S_U plane): y = h[c] * acc and c16 = f16(acc)
+//     (train_mm.rs, blr_forward: mm into cbuf, scale_acc with h);
+//  2: its dx'-product read token-major (B = the S_V plane): dx' = acc /
+//     sigma_t, dx = g[c] * dx', and the token sums of x * dx' for dg, one
+//     partial row per warp (32 tokens) of the tile (blr_backward: mm into t1,
+//     colsum_prod for dg, scale_acc with g).
+// Per-column factors are the same for every row: each thread reads the
+// chunk's 32 with eight broadcast 16-byte loads.
 //
 // Shared-memory operand tiles, as TMA writes them with the 128-byte swizzle:
 //  - K-major: rows of 64 K values (128 bytes), 8-row groups 1024 bytes apart
@@ -33,22 +44,29 @@ struct DenseGemmArgs {
     int F0, F1;                  // rows (M side) of the two products; F1 = 0: one product
     float scale0, scale1;
     const float *dscale0, *dscale1;
-    float *out0, *out1;          // [F][R] (read when accumulating)
     int R;                       // columns (N side), both products
     int K;                       // reduction length
-    int accumulate;
+    int accumulate;              // reduce-add into the output instead of storing
     uint32_t *status;
+    const float *colv;           // EPM 1, 2: per-column factor (h or g) [R]
+    const float *row_inv;        // EPM 2: per-row 1/sigma_t [F0]
+    const float *xin;            // EPM 2: x [F0][R] f32
+    float *part;                 // EPM 2: dg partial rows [row tiles * 4][R]
 };
 
 constexpr int kSgThreads = 192;
 constexpr int kSgEpi0 = 2;
 
-template <int BN>
+template <int BN, int EPM = 0>
 struct DenseGemmShape {
     static constexpr int kABytes = 2 * kMnBlockBytes;
     static constexpr int kBBytes = (BN / 64) * kMnBlockBytes;
     static constexpr int kStage = kABytes + kBBytes;
-    static constexpr int kEpiBytes = 4 * 2 * 4096;
+    // epilogue chunk slots per warp: two 4 KB f32 slots (modes 0 and 2), or
+    // one 6 KB slot of f32 y and f16 c (mode 1), which keeps four operand stages
+    static constexpr int kSlotBytes = EPM == 1 ? 6144 : 4096;
+    static constexpr int kSlots = EPM == 1 ? 1 : 2;
+    static constexpr int kEpiBytes = 4 * kSlots * kSlotBytes;
     static constexpr int kNBRaw = (227 * 1024 - 1024 - 256 - kEpiBytes) / kStage;
     static constexpr int kNB = kNBRaw > 8 ? 8 : kNBRaw;
     static constexpr int kNumBars = 2 * kNB + 4 + 1;
@@ -69,16 +87,35 @@ template <bool MN>
 constexpr uint64_t kDenseDescK = MN ? (2048u >> 4) : (32u >> 4);
 
 __device__ __forceinline__ int sw128_chunk_off(int row, int c) { return row * 128 + ((c ^ (row & 7)) << 4); }
+// 64-byte rows (32 f16) in the 64-byte swizzle: 16-byte chunk c of row r
+__device__ __forceinline__ int sw64_chunk_off(int row, int c) { return row * 64 + ((c ^ ((row >> 1) & 3)) << 4); }
 
-template <int BN, bool A_MN, bool B_MN>
+// Lane l of the warp returns sum over the 32 lanes of v[l] (a transposing
+// butterfly: 31 shuffles, each step halving the values a lane carries).
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, s);
+        }
+    }
+    return v[0];
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPM>
 __global__ void __launch_bounds__(kSgThreads, 1)
     dense_gemm_kernel(const __grid_constant__ DenseGemmMaps maps, const DenseGemmArgs args) {
-    using S = DenseGemmShape<BN>;
+    using S = DenseGemmShape<BN, EPM>;
     constexpr int NB = S::kNB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sS = smem;                          // [NB][A | B]
-    uint8_t *sE = sS + NB * S::kStage;           // [4 warps][2][32 x 32 f32]
+    uint8_t *sE = sS + NB * S::kStage;           // [4 warps][kSlots][slot]
     uint64_t *full = reinterpret_cast<uint64_t *>(sE + S::kEpiBytes);
     uint64_t *empty = full + NB;
     uint64_t *tmem_full = empty + NB;
@@ -225,7 +262,7 @@ __global__ void __launch_bounds__(kSgThreads, 1)
     } else {
         // ---- epilogue: thread = one row f of the tile ------------------------
         const int q = warp & 3;
-        uint8_t *ebuf = sE + (warp - kSgEpi0) * 2 * 4096;
+        uint8_t *ebuf = sE + (warp - kSgEpi0) * S::kSlots * S::kSlotBytes;
         int gch = 0, local = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
@@ -233,7 +270,6 @@ __global__ void __launch_bounds__(kSgThreads, 1)
             decode(tile, jb, f0, k0);
             const int jF = jb ? args.F1 : args.F0;
             const float *jds = jb ? args.dscale1 : args.dscale0;
-            float *jout = jb ? args.out1 : args.out0;
             const CUtensorMap *mo = jb ? &maps.o[1] : &maps.o[0];
             const float scale = (jb ? args.scale1 : args.scale0) * (jds ? *jds : 1.0f);
             const int acc = local & 1;
@@ -241,6 +277,16 @@ __global__ void __launch_bounds__(kSgThreads, 1)
             const int fr = f0 + q * 32;  // this warp's 32 rows
             const int f = fr + lane;
             const bool fvalid = f < jF;
+            // mode 2: this row's 1/sigma_t, and x of the tile's first chunk
+            const float ri = (EPM == 2 && fvalid) ? __ldg(args.row_inv + f) : 0.0f;
+            float4 xa[8];
+            auto load_x = [&](int kc, float4 (&xr)[8]) {
+                const bool in = fvalid && kc < args.R;
+                const float4 *src = reinterpret_cast<const float4 *>(args.xin + (size_t)f * args.R + kc);
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) xr[j4] = in ? __ldcs(src + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            };
+            if constexpr (EPM == 2) load_x(k0, xa);
             const bool got = mbar_wait(&tmem_full[acc], acc_phase, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, got)) {
                 if (lane == 0) fail(kStTimeoutEpi);
@@ -252,36 +298,86 @@ __global__ void __launch_bounds__(kSgThreads, 1)
             for (int c = 0; c < BN / 32; ++c, ++gch) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + 32 * c), v);
+                const int kc = k0 + 32 * c;  // first column of the chunk
+                float4 xn[8];
+                if constexpr (EPM == 2) {
+                    if (c + 1 < BN / 32) load_x(kc + 32, xn);  // next chunk's x, in flight meanwhile
+                }
                 tmem_wait_ld_regs(v);
                 if (c == BN / 32 - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tmem_empty[acc]);
                 }
-                const int kc = k0 + 32 * c;  // first column of the chunk
-                uint8_t *buf = ebuf + (gch & 1) * 4096;
-                if (lane == 0) bulk_wait_group_read<1>();  // the store that last used buf has read it
+                uint8_t *buf = ebuf + (gch % S::kSlots) * S::kSlotBytes;
+                // the store that last used buf has read it
+                if (lane == 0) {
+                    if constexpr (S::kSlots == 1)
+                        bulk_wait_group_read<0>();
+                    else
+                        bulk_wait_group_read<1>();
+                }
                 __syncwarp();
-                const bool accum = args.accumulate && fvalid && kc < args.R;
+                const bool cvalid = kc < args.R;
+                if constexpr (EPM == 0) {
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    float4 o = make_float4(__uint_as_float(v[4 * j4]) * scale, __uint_as_float(v[4 * j4 + 1]) * scale,
-                                           __uint_as_float(v[4 * j4 + 2]) * scale,
-                                           __uint_as_float(v[4 * j4 + 3]) * scale);
-                    if (accum) {
-                        const float4 old =
-                            *reinterpret_cast<const float4 *>(jout + (size_t)f * args.R + kc + 4 * j4);
-                        o.x += old.x;
-                        o.y += old.y;
-                        o.z += old.z;
-                        o.w += old.w;
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 o = make_float4(
+                            __uint_as_float(v[4 * j4]) * scale, __uint_as_float(v[4 * j4 + 1]) * scale,
+                            __uint_as_float(v[4 * j4 + 2]) * scale, __uint_as_float(v[4 * j4 + 3]) * scale);
+                        *reinterpret_cast<float4 *>(buf + sw128_chunk_off(lane, j4)) = o;
                     }
-                    *reinterpret_cast<float4 *>(buf + sw128_chunk_off(lane, j4)) = o;
+                } else if constexpr (EPM == 1) {
+                    // y = h * acc (f32, 128-byte swizzle), c = f16(acc) (64-byte swizzle)
+                    const float4 *h4 = reinterpret_cast<const float4 *>(args.colv + kc);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 hv = cvalid ? __ldg(h4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float4 o = make_float4(__uint_as_float(v[4 * j4]) * hv.x, __uint_as_float(v[4 * j4 + 1]) * hv.y,
+                                                     __uint_as_float(v[4 * j4 + 2]) * hv.z,
+                                                     __uint_as_float(v[4 * j4 + 3]) * hv.w);
+                        *reinterpret_cast<float4 *>(buf + sw128_chunk_off(lane, j4)) = o;
+                    }
+#pragma unroll
+                    for (int c16 = 0; c16 < 4; ++c16) {
+                        uint4 w;
+                        w.x = pack_half2(__uint_as_float(v[8 * c16]), __uint_as_float(v[8 * c16 + 1]));
+                        w.y = pack_half2(__uint_as_float(v[8 * c16 + 2]), __uint_as_float(v[8 * c16 + 3]));
+                        w.z = pack_half2(__uint_as_float(v[8 * c16 + 4]), __uint_as_float(v[8 * c16 + 5]));
+                        w.w = pack_half2(__uint_as_float(v[8 * c16 + 6]), __uint_as_float(v[8 * c16 + 7]));
+                        *reinterpret_cast<uint4 *>(buf + 4096 + sw64_chunk_off(lane, c16)) = w;
+                    }
+                } else {
+                    // dx' = acc / sigma_t; dx = g * dx'; dg partial = sum over the warp's rows of x * dx'
+                    const float4 *g4 = reinterpret_cast<const float4 *>(args.colv + kc);
+                    float prod[32];
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 gv = cvalid ? __ldg(g4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float d0 = __uint_as_float(v[4 * j4]) * ri, d1 = __uint_as_float(v[4 * j4 + 1]) * ri;
+                        const float d2 = __uint_as_float(v[4 * j4 + 2]) * ri, d3 = __uint_as_float(v[4 * j4 + 3]) * ri;
+                        prod[4 * j4] = xa[j4].x * d0;
+                        prod[4 * j4 + 1] = xa[j4].y * d1;
+                        prod[4 * j4 + 2] = xa[j4].z * d2;
+                        prod[4 * j4 + 3] = xa[j4].w * d3;
+                        *reinterpret_cast<float4 *>(buf + sw128_chunk_off(lane, j4)) =
+                            make_float4(gv.x * d0, gv.y * d1, gv.z * d2, gv.w * d3);
+                    }
+                    const float colsum = warp_transpose_sum(prod);  // lane l: column kc + l
+                    if (cvalid) args.part[((size_t)(f0 / 128) * 4 + q) * args.R + kc + lane] = colsum;
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) xa[j4] = xn[j4];
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (fr < jF && kc < args.R) tma_store_2d(mo, buf, kc, fr);
+                    if (fr < jF && cvalid) {
+                        if (args.accumulate)
+                            tma_reduce_add_2d(mo, buf, kc, fr);
+                        else
+                            tma_store_2d(mo, buf, kc, fr);
+                        if constexpr (EPM == 1) tma_store_2d(&maps.o16, buf + 4096, kc, fr);
+                    }
                     bulk_commit_group();
                 }
                 __syncwarp();
@@ -298,16 +394,17 @@ __global__ void __launch_bounds__(kSgThreads, 1)
 }
 
 // ------------------------------------------------------------ launcher ---
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, int EPM>
 static cudaError_t launch_dense_t(const DenseGemmLaunch &L, const DenseGemmArgs &ga, int grid, cudaStream_t s) {
+    using S = DenseGemmShape<BN, EPM>;
     static bool prepared = false;
     if (!prepared) {
-        const cudaError_t e = prepare_kernel(dense_gemm_kernel<BN, A_MN, B_MN>, DenseGemmShape<BN>::kSmemBytes);
+        const cudaError_t e = prepare_kernel(dense_gemm_kernel<BN, A_MN, B_MN, EPM>, S::kSmemBytes);
         if (e != cudaSuccess) return e;
         prepared = true;
     }
-    return launch_k(dense_gemm_kernel<BN, A_MN, B_MN>, dim3(grid), dim3(kSgThreads), DenseGemmShape<BN>::kSmemBytes,
-                    s, L.maps, ga);
+    return launch_k(dense_gemm_kernel<BN, A_MN, B_MN, EPM>, dim3(grid), dim3(kSgThreads), S::kSmemBytes, s, L.maps,
+                    ga);
 }
 
 cudaError_t launch_dense_gemm(const DenseGemmLaunch &L, const char *name, cudaStream_t s) {
@@ -318,26 +415,35 @@ cudaError_t launch_dense_gemm(const DenseGemmLaunch &L, const char *name, cudaSt
     ga.scale1 = L.scale[1];
     ga.dscale0 = L.dscale[0];
     ga.dscale1 = L.dscale[1];
-    ga.out0 = L.out[0];
-    ga.out1 = L.out[1];
     ga.R = L.R;
     ga.K = L.K;
     ga.accumulate = L.accumulate;
     ga.status = L.status;
-    const int bn = dense_bn(L.R);
+    ga.colv = L.colv;
+    ga.row_inv = L.row_inv;
+    ga.xin = L.xin;
+    ga.part = L.part;
+    const int bn = L.epm ? 256 : dense_bn(L.R);
     const long long tiles = (long long)(((L.F[0] + 127) / 128) + ((L.F[1] + 127) / 128)) * ((L.R + bn - 1) / bn);
     const int grid = (int)(tiles < L.sms ? tiles : L.sms);
     if (grid < 1) return cudaSuccess;
     cudaError_t e = cudaErrorInvalidValue;
     trace_before(name, s);
-    if (L.a_mn && L.b_mn)
-        e = bn == 256 ? launch_dense_t<256, true, true>(L, ga, grid, s) : launch_dense_t<128, true, true>(L, ga, grid, s);
+    if (L.epm == 1 && !L.a_mn && !L.b_mn)
+        e = launch_dense_t<256, false, false, 1>(L, ga, grid, s);
+    else if (L.epm == 2 && !L.a_mn && !L.b_mn)
+        e = launch_dense_t<256, false, false, 2>(L, ga, grid, s);
+    else if (L.epm != 0)
+        e = cudaErrorInvalidValue;
+    else if (L.a_mn && L.b_mn)
+        e = bn == 256 ? launch_dense_t<256, true, true, 0>(L, ga, grid, s)
+                      : launch_dense_t<128, true, true, 0>(L, ga, grid, s);
     else if (!L.a_mn && !L.b_mn)
-        e = bn == 256 ? launch_dense_t<256, false, false>(L, ga, grid, s)
-                      : launch_dense_t<128, false, false>(L, ga, grid, s);
+        e = bn == 256 ? launch_dense_t<256, false, false, 0>(L, ga, grid, s)
+                      : launch_dense_t<128, false, false, 0>(L, ga, grid, s);
     else if (!L.a_mn && L.b_mn)
-        e = bn == 256 ? launch_dense_t<256, false, true>(L, ga, grid, s)
-                      : launch_dense_t<128, false, true>(L, ga, grid, s);
+        e = bn == 256 ? launch_dense_t<256, false, true, 0>(L, ga, grid, s)
+                      : launch_dense_t<128, false, true, 0>(L, ga, grid, s);
     trace_after(s);
     return e;
 }

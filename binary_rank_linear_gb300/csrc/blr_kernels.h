@@ -202,24 +202,28 @@ bool small_bwd_fits(int d_out);  // the fused backward stages rows of d_out floa
 // b = the N-side operand: MN-major [K][R] (box 64 x 64) or K-major [R][K]
 //     (box 64 K x BN rows), f16, 128-byte swizzle;
 // o = the f32 output [F][R] (box 32 x 32, 128-byte swizzle).
+// o16: mode 1's f16 output c [F][R] (box 32 x 32, 64-byte swizzle).
 struct DenseGemmMaps {
-    CUtensorMap a[2], b[2], o[2];
+    CUtensorMap a[2], b[2], o[2], o16;
 };
 
 // Column tile of the dense products: 256 when R >= 256, else 128.
 inline int dense_bn(int R) { return R >= 256 ? 256 : 128; }
 
-// out_j = scale_j * dscale_j (if given) * sum_k A_j B_j, overwritten or added.
+// out_j = scale_j * dscale_j (if given) * sum_k A_j B_j, stored or (accumulate)
+// added by TMA reduce-add into the outputs the maps o describe.
 struct DenseGemmLaunch {
     DenseGemmMaps maps;
     int F[2];                      // rows of each product (F[1] = 0: one product)
     float scale[2];
     const float *dscale[2];        // device scalars or null
-    float *out[2];
     int R, K, accumulate;
     bool a_mn, b_mn;               // operand majorness (A MN-major needs B MN-major)
     uint32_t *status;
     int sms;
+    int epm;                       // epilogue mode (blr_dense.cu): 0 plain, 1 the c-product, 2 the dx'-product
+    const float *colv, *row_inv, *xin;  // modes 1, 2: h or g; 1/sigma_t; x
+    float *part;                   // mode 2: dg partial rows [ceil(F0/128) * 4][R]
 };
 cudaError_t launch_dense_gemm(const DenseGemmLaunch &L, const char *name, cudaStream_t s);
 

@@ -296,3 +296,19 @@ def test_sign_source_integer_grid_bit_exact(monkeypatch, src):
     assert out["status"] == 0
     assert np.array_equal(out["y"], fw["y"].astype(np.float32))
     assert np.array_equal(out["dx"], bw["dx"].astype(np.float32))
+
+
+@pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 4600, 1024, 1568, 1280),
+                                                 ("ragged", 127, 256, 512, 128)])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_wide_products_token_major(monkeypatch, name, M, d_in, d_out, r, accumulate):
+    """The c- and dx'-products run token-major on the dense kernel (BLR_WIDE=token)."""
+    monkeypatch.setenv("BLR_WIDE", "token")
+    w = wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r)
+    t = wl.make_inputs(w, with_priors=accumulate)
+    if accumulate:
+        out = _run(t, y_prior=t["y_prior"], dx_prior=t["dx_prior"])
+        _check_against_oracle(t, out, "(token-major, accumulate)", y_prior=t["y_prior"], dx_prior=t["dx_prior"])
+    else:
+        out = _run(t)
+        _check_against_oracle(t, out, "(token-major)")
