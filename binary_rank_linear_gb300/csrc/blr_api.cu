@@ -208,7 +208,8 @@ Layout make_layout(int M, int d_in, int d_out, int r) {
     L.rows_dh = stage_dy_blocks(M, d_out);
     L.blkmax = take((size_t)L.rows_dh * 8);
     // partial rows per token tile (tiles of at least 128 tokens)
-    L.rows_dl = (int)((m + 127) / 128) * epi_part_rows_per_tile(kEpiBwd1);
+    // (split-K db-products write one per quarter of K)
+    L.rows_dl = (int)((m + 127) / 128) * 4;
     // (the token-major dx'-product writes four per 128-token tile)
     L.rows_dg = (int)((m + 127) / 128) * 4;
     L.part_dh = take((size_t)L.rows_dh * d_out * 4);
@@ -348,6 +349,25 @@ bool wide_token_major() {
     return v && std::strcmp(v, "token") == 0;
 }
 
+// Split-K for the r-wide products (a and db, K = d_in or d_out) of problems
+// whose single-CTA tiles fill at most a quarter of the SMs: clusters of four
+// CTAs share each tile's k-steps (each at least one) and reduce over DSMEM.
+// Opt-in (BLR_SPLITK=1): measured on GB300 on the small layer (2048 tokens,
+// 1024 -> 1024, r = 256) the a-product took 18.4 us split against 12.2 us
+// whole, the db-product 20.4 against 14.2; a 32-CTA tile of 8 k-steps is
+// dominated by fixed costs (the first loads' round trip, setup, the epilogue's
+// first chunk), which the cluster launch, staging and two cluster barriers add to.
+GemmPlan plan_split(GemmPlan p, int M, int N, int K, int sms) {
+    const char *v = std::getenv("BLR_SPLITK");
+    if (!(v && std::strcmp(v, "1") == 0)) return p;
+    if (p.pair || p.plane || p.bt != 128) return p;
+    const long long tiles = (long long)((M + 127) / 128) * ((N + 127) / 128);
+    if (tiles * 4 > sms || (K + 127) / 128 < 4) return p;
+    p.split = 4;
+    p.grid = (int)(tiles * 4);
+    return p;
+}
+
 // Grid of the fused small-M kernels: enough CTAs for the larger GEMM phase's
 // tiles (at least 16, for the staging phases), at most one per SM.
 int small_grid(const GemmPlan &p1, int N1, const GemmPlan &p2, int N2, int M, int sms) {
@@ -461,7 +481,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     const bool fused = !q1.pair && !q2.pair && fused_small_enabled();
     const bool planes = !fused && plane_mode();
     const bool dense2 = !fused && wide_token_major();
-    const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : q1;
+    const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : (fused ? q1 : plan_split(q1, M, r, d_in, sms));
     const GemmPlan p2 = planes ? plan_gemm_plane(M, d_out, sms) : q2;
     GemmMaps m1{}, m2{};
     DenseGemmLaunch d2{};
@@ -597,7 +617,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     const bool fused = !q1.pair && !q2.pair && small_bwd_fits(d_out) && fused_small_enabled();
     const bool planes = !fused && plane_mode();
     const bool dense2 = !fused && wide_token_major();
-    const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : q1;
+    const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : (fused ? q1 : plan_split(q1, M, r, d_out, sms));
     const GemmPlan p2 = planes ? plan_gemm_plane(M, d_in, sms) : q2;
     GemmMaps m1{}, m2{};
     DenseGemmLaunch d2{};
@@ -681,7 +701,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     b2.accumulate = accumulate_dx;
     b2.status = status;
 
-    ReduceSeg sl{part_dl, dl, p1.part_rows * epi_part_rows_per_tile(kEpiBwd1), r};
+    ReduceSeg sl{part_dl, dl, p1.part_rows * (p1.split == 4 ? 4 : epi_part_rows_per_tile(kEpiBwd1)), r};
     ReduceSeg sg{part_dg, dg, dense2 ? (M + 127) / 128 * 4 : p2.part_rows * epi_part_rows_per_tile(kEpiBwd2), d_in};
     if (fused) {
         // small problem: the whole pass as one fused cooperative kernel

@@ -201,7 +201,14 @@ __device__ __forceinline__ uint16_t f16_bits(float v) { return __half_as_ushort(
 // (a CTA, or a CTA pair, per unit). Barriers must be initialised (and, for a
 // pair, both CTAs' barriers visible) and TMEM allocated before the call; on
 // return every load, MMA and store the phase issued has completed.
-template <int EPI, bool PAIR, int BT, bool PLANE = false>
+// SPLIT > 1 (single CTAs, one tile per CTA, clusters of SPLIT along K): CTA
+// kj of the cluster reduces k-steps [kj n / SPLIT, (kj + 1) n / SPLIT) of the
+// tile into its TMEM, stages the chunks it does not own in shared memory, and
+// after a cluster barrier adds the peers' copies of chunk kj (read over DSMEM)
+// into its TMEM; its epilogue then runs the tile's chunk kj only. For
+// problems with few tiles and long K this cuts both the k-loop and the
+// epilogue a CTA runs by SPLIT.
+template <int EPI, bool PAIR, int BT, bool PLANE = false, int SPLIT = 1>
 __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE> &L, const CUtensorMap &tmap_act,
                                            const CUtensorMap &tmap_in, const CUtensorMap &tmap_out32,
                                            const CUtensorMap &tmap_out16, const GemmArgs &args,
@@ -225,6 +232,9 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
     const int t_tiles = (M + BT - 1) / BT;
     const int num_tiles = f_tiles * t_tiles;  // feature tile varies fastest: neighbours share activations
     const int num_ks = (args.K + kStepK - 1) / kStepK;
+    static_assert(SPLIT == 1 || (!PAIR && !PLANE), "split-K runs single TMEM-expansion CTAs");
+    const int kj = SPLIT > 1 ? (int)cluster_ctarank() : 0;  // this CTA's share of K
+    const int ks0 = kj * num_ks / SPLIT, ks1 = (kj + 1) * num_ks / SPLIT;
     // the leader's copy of a barrier, as a cluster address (PAIR only)
     auto leader_bar = [&](uint64_t *bar) -> uint32_t { return mapa_shared(smem_u32(bar), 0); };
 
@@ -236,7 +246,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
                 const int t0 = (tile / f_tiles) * BT + (int)rank * S::kTokRows;  // this CTA's token rows
                 const int f0 = (tile % f_tiles) * kUnitF + (int)rank * kFM;      // this CTA's sign rows
-                for (int ks = 0; ks < num_ks; ++ks) {
+                for (int ks = ks0; ks < ks1; ++ks) {
                     if (!mbar_wait(&empty_b[sb], pb ^ 1u, abort_flag)) {
                         fail_status(args, abort_flag, kStTimeoutTma);
                         ok = false;
@@ -305,7 +315,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(acc * S::kAccCols);
                     uint32_t acc_in = 0u;
-                    for (int ks = 0; ks < num_ks; ++ks) {
+                    for (int ks = ks0; ks < ks1; ++ks) {
                         bool got = mbar_wait(&full_b[sb], pb, abort_flag);
                         if (PAIR && got) got = mbar_wait(&L.full_p[sb], pb, abort_flag);
                         if (!got) {
@@ -351,7 +361,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                 uint32_t pb = 0;
                 bool ok = true;
                 for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
-                    for (int ks = 0; ks < num_ks; ++ks) {
+                    for (int ks = ks0; ks < ks1; ++ks) {
                         if (!mbar_wait(&full_b[sb], pb, abort_flag)) {
                             fail_status(args, abort_flag, kStTimeoutMma);
                             ok = false;
@@ -391,7 +401,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * S::kAccCols);
                 uint32_t acc_in = 0u;  // the tile's first MMA overwrites the accumulator
-                for (int ks = 0; ks < num_ks; ++ks) {
+                for (int ks = ks0; ks < ks1; ++ks) {
                     if (!mbar_wait(&full_s[sa], pa, abort_flag)) {
                         fail_status(args, abort_flag, kStTimeoutMma);
                         ok = false;
@@ -452,7 +462,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         uint32_t lp = 0;  // and that slot's phase parity
         bool ok = true;
         for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
-            for (int ks = 0; ks < num_ks; ++ks) {
+            for (int ks = ks0; ks < ks1; ++ks) {
                 bool got = mbar_wait(&full_b[sb], pb, abort_flag);
                 uint32_t v[32];
                 if (got) {
@@ -508,7 +518,9 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         const int q = warp & 3;
         const int ew = warp - kWarpEpi0;
         const int half = ew / 4;
-        const int nc = (kChunks - half + kSplit - 1) / kSplit;  // this warp's chunks per tile
+        // this warp's first chunk of a tile and its chunks per tile (split-K: chunk kj only)
+        const int cb = SPLIT > 1 ? kj : half;
+        const int nc = SPLIT > 1 ? 1 : (kChunks - half + kSplit - 1) / kSplit;
         uint8_t *slots = sE + ew * kNE * S::kSlotBytes;
         uint64_t *ebar = eload + ew * kNE;
         // inputs: the a-tape (db) or x (dx'); y and dx accumulate by reduce-add stores
@@ -522,7 +534,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             const int tile = unit + lt * num_units;
             if (tile >= num_tiles) return false;
             fq = (tile % f_tiles) * kUnitF + (int)rank * kFM + q * 32;
-            tok = (tile / f_tiles) * BT + 32 * (half + kSplit * (g - lt * nc));
+            tok = (tile / f_tiles) * BT + 32 * (cb + kSplit * (g - lt * nc));
             return true;
         };
         auto load_chunk = [&](int g) {  // lane 0
@@ -540,6 +552,54 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         int g = 0;
         int local = 0;
         bool ok = true;
+        if constexpr (SPLIT > 1) {
+            // split-K: one tile per CTA. Stage the chunks other CTAs own, then sum
+            // this CTA's chunk over the cluster back into TMEM (accumulator 0).
+            // Every thread of every role passes the two cluster barriers.
+            bool got = unit < num_tiles && mbar_wait(&tmem_full[0], 0, abort_flag);
+            got = __all_sync(0xFFFFFFFFu, got);
+            if (!got && lane == 0 && unit < num_tiles) fail_status(args, abort_flag, kStTimeoutEpi);
+            tc_fence_after();
+            const uint32_t acc_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+            const int row = q * 32 + lane;  // feature row of the tile
+            float *stg = reinterpret_cast<float *>(sB);  // [kChunks][128 rows][32] f32, 16-byte groups swizzled
+            uint32_t v[32];
+            if (got) {
+                for (int c = 0; c < kChunks; ++c) {
+                    if (c == kj) continue;
+                    tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * c), v);
+                    tmem_wait_ld_regs(v);
+                    float *dst = stg + ((size_t)c * kFM + row) * 32;
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4)
+                        reinterpret_cast<float4 *>(dst)[j4 ^ (row & 7)] =
+                            make_float4(__uint_as_float(v[4 * j4]), __uint_as_float(v[4 * j4 + 1]),
+                                        __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3]));
+                }
+            }
+            cluster_sync();  // every CTA's chunks are staged
+            if (got) {
+                tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * kj), v);
+                tmem_wait_ld_regs(v);
+                const uint32_t mine = smem_u32(stg + ((size_t)kj * kFM + row) * 32);
+                for (int p = 0; p < SPLIT; ++p) {
+                    if (p == kj) continue;
+                    const uint32_t peer = mapa_shared(mine, (uint32_t)p);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 o = ld_shared_cluster_v4(peer + (uint32_t)((j4 ^ (row & 7)) * 16));
+                        v[4 * j4] = __float_as_uint(__uint_as_float(v[4 * j4]) + o.x);
+                        v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) + o.y);
+                        v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) + o.z);
+                        v[4 * j4 + 3] = __float_as_uint(__uint_as_float(v[4 * j4 + 3]) + o.w);
+                    }
+                }
+                tmem_st_32x32b_x32(acc_addr + (uint32_t)(32 * kj), v);
+                tmem_wait_st();
+            }
+            cluster_sync();  // no CTA reads a peer's staging any more
+            if (!got) ok = false;
+        }
         for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++local) {
             const int acc = local & 1;
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
@@ -552,7 +612,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             float ri_t[kMaxNc], rs_t[kMaxNc];
 #pragma unroll
             for (int i = 0; i < kMaxNc; ++i) {
-                const int tl = t0 + 32 * (half + kSplit * i) + lane;
+                const int tl = t0 + 32 * (cb + kSplit * i) + lane;
                 const bool use = i < nc && tl < M;
                 ri_t[i] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && use ? __ldg(args.row_inv + tl) : 0.0f;
                 rs_t[i] = (EPI == kEpiBwd1) && use ? __ldg(args.row_scale + tl) : 0.0f;
@@ -573,11 +633,11 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             // processed. Two warps per quarter overlap each other instead (one
             // register set keeps them within the 96 registers their 18 warps allow).
             uint32_t va[32], vb[32];
-            if constexpr (kSplit == 1) tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * half), va);
+            if constexpr (kSplit == 1) tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * cb), va);
 #pragma unroll
             for (int i = 0; i < kMaxNc; ++i) {
                 if (i >= nc) break;
-                const int c = half + kSplit * i;  // chunk of the tile
+                const int c = cb + kSplit * i;  // chunk of the tile
                 uint32_t(&v)[32] = (kSplit == 1 && (i & 1)) ? vb : va;
                 uint32_t(&vn)[32] = (kSplit == 1 && (i & 1)) ? va : vb;
                 if constexpr (kSplit == 1) {
@@ -676,7 +736,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             if (!ok) break;
             if constexpr (EPI == kEpiBwd1 || EPI == kEpiBwd2) {
                 // one partial row per (token tile, warp of the quarter)
-                if (fvalid) args.part[((size_t)tt * kSplit + half) * N + f] = psum;
+                if (fvalid) args.part[((size_t)tt * (SPLIT > 1 ? SPLIT : kSplit) + (SPLIT > 1 ? kj : half)) * N + f] = psum;
             }
         }
         // drain: stores complete, and input loads issued but not consumed have landed
@@ -687,6 +747,13 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                     atomicOr(args.status, kStTimeoutDrain);
         }
         __syncwarp();
+    }
+    if constexpr (SPLIT > 1) {
+        // the other roles, done with the tile, pass the epilogue's two cluster barriers
+        if (warp < kWarpEpi0) {
+            cluster_sync();
+            cluster_sync();
+        }
     }
 
 }
@@ -714,7 +781,7 @@ __device__ __forceinline__ uint8_t *smem_base_1024() {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 }
 
-template <int EPI, bool PAIR, int BT, bool PLANE>
+template <int EPI, bool PAIR, int BT, bool PLANE, int SPLIT>
 __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE>::kThreads, 1)
     blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ CUtensorMap tmap_in,
                     const __grid_constant__ CUtensorMap tmap_out32, const __grid_constant__ CUtensorMap tmap_out16,
@@ -748,10 +815,13 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE>::kThreads, 1)
     // setup above overlaps the previous kernel; global memory only after this
     pdl_wait();
     pdl_launch_dependents();
-    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // tile worker (CTA or pair)
-    const int num_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-    gemm_roles<EPI, PAIR, BT, PLANE>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
-                                     reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units, &tmap_sgn);
+    // tile worker: a CTA, a CTA pair, or a split-K cluster
+    const int per_unit = PAIR ? 2 : SPLIT;
+    const int unit = (int)blockIdx.x / per_unit;
+    const int num_units = (int)gridDim.x / per_unit;
+    gemm_roles<EPI, PAIR, BT, PLANE, SPLIT>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
+                                            reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units,
+                                            &tmap_sgn);
     tc_fence_before();
     if constexpr (PAIR) {
         // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it
@@ -765,12 +835,12 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE>::kThreads, 1)
     }
 }
 
-template <int EPI, bool PAIR, int BT, bool PLANE = false>
+template <int EPI, bool PAIR, int BT, bool PLANE = false, int SPLIT = 1>
 cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, cudaStream_t s) {
     using S = GemmShape<EPI, PAIR, BT, PLANE>;
     static bool attr_set = false;  // set once, outside any later stream capture
     if (!attr_set) {
-        cudaError_t e = prepare_kernel(blr_gemm_kernel<EPI, PAIR, BT, PLANE>, S::kSmemBytes);
+        cudaError_t e = prepare_kernel(blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT>, S::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -783,12 +853,12 @@ cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, 
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[1].val.clusterDim.x = PAIR ? 2 : SPLIT;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = PAIR ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, blr_gemm_kernel<EPI, PAIR, BT, PLANE>, maps.act, maps.in32, maps.out32,
+    cfg.numAttrs = (PAIR || SPLIT > 1) ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT>, maps.act, maps.in32, maps.out32,
                               maps.out16, maps.sgn, args);
 }
 
@@ -800,6 +870,9 @@ cudaError_t launch_gemm_epi(const GemmPlan &plan, const GemmMaps &maps, const Ge
         if (plan.pair && plan.bt == 256) return launch_gemm_t<EPI, true, 256, true>(maps, args, plan.grid, s);
         if (!plan.pair && plan.bt == 128) return launch_gemm_t<EPI, false, 128, true>(maps, args, plan.grid, s);
         return cudaErrorInvalidValue;
+    }
+    if constexpr (EPI == kEpiFwd1 || EPI == kEpiBwd1) {
+        if (plan.split == 4) return launch_gemm_t<EPI, false, 128, false, 4>(maps, args, plan.grid, s);
     }
     if (plan.pair && plan.bt == 192) return launch_gemm_t<EPI, true, 192>(maps, args, plan.grid, s);
     if (plan.pair && plan.bt == 160) return launch_gemm_t<EPI, true, 160>(maps, args, plan.grid, s);

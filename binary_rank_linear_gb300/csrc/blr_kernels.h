@@ -148,12 +148,15 @@ struct GemmMaps {
 // epi_part_rows_per_tile rows of partial sums per token tile).
 // plane = true: the sign operand is a +-1 f16 plane read by TMA (single CTAs,
 // bt = 128, 192 or 256); false: bitmap words expanded into TMEM.
+// split = 4: split-K over clusters of four single CTAs (one tile each; the
+// a- and db-products of problems with few tiles), grid = tiles * 4.
 struct GemmPlan {
     bool pair;
     int bt;
     int grid;
     int part_rows;
     bool plane;
+    int split;
 };
 
 GemmPlan plan_gemm(int M, int N, int sms);        // TMEM-expansion tiles

@@ -312,3 +312,29 @@ def test_wide_products_token_major(monkeypatch, name, M, d_in, d_out, r, accumul
     else:
         out = _run(t)
         _check_against_oracle(t, out, "(token-major)")
+
+
+@pytest.mark.parametrize("splitk", ["1", "0"])
+@pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 2048, 1024, 1024, 256), ("small", 333, 544, 608, 160),
+                                                 ("ragged", 129, 1056, 96, 64), ("attn", 513, 512, 640, 256)])
+def test_split_k(monkeypatch, splitk, name, M, d_in, d_out, r):
+    """The a- and db-products of problems with few tiles split K over clusters
+    of four CTAs (reduced over DSMEM); the same shapes without the split."""
+    monkeypatch.setenv("BLR_SPLITK", splitk)
+    t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    out = _run(t, gscale=0.0)
+    _check_against_oracle(t, out, f"(split-K {splitk})")
+
+
+def test_split_k_integer_grid_bit_exact(monkeypatch):
+    monkeypatch.setenv("BLR_SPLITK", "1")
+    M, d_in, d_out, r = 250, 640, 544, 96  # both r-wide products split (5 and 5 k-steps)
+    t = _integer_grid(M, d_in, d_out, r, seed=91)
+    out = _run(t, gscale=1.0)
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    fw = oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    assert out["status"] == 0
+    assert np.array_equal(out["y"], fw["y"].astype(np.float32))
+    assert np.array_equal(out["dx"], bw["dx"].astype(np.float32))
+    assert oracle.rel_err(out["dl"], bw["dl"]) == 0.0
