@@ -51,13 +51,28 @@ __global__ void unpack_signs_kernel(const uint32_t *__restrict__ bits, uint16_t 
     }
 }
 
+// Blocks [0, stage_blocks) stage; when the grid has more, the extra blocks do
+// the bitmap re-layouts alone (off the staging's critical path), otherwise
+// every block does its share of them first.
+__device__ __forceinline__ bool prologue_prep(const SignPrep &p0, const SignPrep &p1, int stage_blocks) {
+    const int extra = (int)gridDim.x - stage_blocks;
+    if (extra > 0) {
+        if ((int)blockIdx.x < stage_blocks) return false;
+        prep_share(p0, p1, (int)blockIdx.x - stage_blocks, extra);
+        return true;  // a re-layout-only block
+    }
+    prep_share(p0, p1, blockIdx.x, stage_blocks);
+    return false;
+}
+
 __global__ void __launch_bounds__(256) fwd_prologue_kernel(SignPrep p0, SignPrep p1, const float *x, const float *g,
-                                                           uint16_t *x16, int M, int d_in, uint32_t *status) {
+                                                           uint16_t *x16, int M, int d_in, uint32_t *status,
+                                                           int stage_blocks) {
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
-    prep_share(p0, p1, blockIdx.x, gridDim.x);
-    stage_x_run(x, g, x16, M, d_in, blockIdx.x, gridDim.x);
+    if (prologue_prep(p0, p1, stage_blocks)) return;
+    stage_x_run(x, g, x16, M, d_in, blockIdx.x, stage_blocks);
 }
 
 template <int GPT>
@@ -66,7 +81,7 @@ __global__ void __launch_bounds__(kStageThreads, (GPT <= 8 ? 2 : 1))
     extern __shared__ __align__(16) float smem_f[];
     pdl_wait();
     pdl_launch_dependents();
-    prep_share(p0, p1, blockIdx.x, stage_blocks);
+    if (prologue_prep(p0, p1, stage_blocks)) return;
     stage_dy_run<GPT>(a, blockIdx.x, stage_blocks, smem_f, stage_tpr(a.d_out), kStageThreads);
 }
 
@@ -77,11 +92,15 @@ int stage_dy_blocks(int M, int d_out) {
 }
 
 // ============================================================== reduce =====
-// out[f] += sum_p part[p][f]. A block of 8 warps owns 32 consecutive columns
-// of one segment; warp w sums rows w, w+8, ... and the eight warp sums are
-// added in warp order, so the result does not depend on scheduling.
-__global__ void __launch_bounds__(256) reduce_partials_kernel(ReduceSeg a, ReduceSeg b, ReduceSeg c) {
-    __shared__ float red[8][32];
+// out[f] += sum_p part[p][f]. A block of 32 warps owns 32 consecutive columns
+// of one segment; warp w sums rows w, w+32, ... (a few rows each, their loads
+// issued together: about one memory round trip for the row counts of the
+// layer's partials) and the 32 warp sums are added in warp order, so the
+// result does not depend on scheduling.
+constexpr int kReduceWarps = 32;
+
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(ReduceSeg a, ReduceSeg b, ReduceSeg c) {
+    __shared__ float red[kReduceWarps][33];
     pdl_wait();
     pdl_launch_dependents();
     const int nba = (a.n + 31) / 32, nbb = (b.n + 31) / 32;
@@ -99,15 +118,15 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(ReduceSeg a, Reduc
     const int col = col0 + lane;
     float acc = 0.0f;
     if (col < n) {
-#pragma unroll 4
-        for (int p = w; p < rows; p += 8) acc += __ldcs(part + (long long)p * n + col);
+#pragma unroll 8
+        for (int p = w; p < rows; p += kReduceWarps) acc += __ldcs(part + (long long)p * n + col);
     }
     red[w][lane] = acc;
     __syncthreads();
     if (w == 0 && col < n) {
         float t = red[0][lane];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) t += red[i][lane];
+        for (int i = 1; i < kReduceWarps; ++i) t += red[i][lane];
         out[col] += t;
     }
 }
@@ -156,8 +175,12 @@ cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const 
     }
     const long long groups = (long long)M * (d_in / 4);
     const int bs = grid_for(groups, 256 * 8, wave);
+    // re-layout-only blocks where the wave has room for them
+    const int pb = prep_blocks(p0, 256) + prep_blocks(p1, 256);
+    const int grid = bs + pb <= wave ? bs + pb : bs;
     trace_before("fwd_prologue", s);
-    cudaError_t e = launch_k(fwd_prologue_kernel, dim3(bs), dim3(256), 0, s, p0, p1, x, g, x16, M, d_in, status);
+    cudaError_t e =
+        launch_k(fwd_prologue_kernel, dim3(grid), dim3(256), 0, s, p0, p1, x, g, x16, M, d_in, status, bs);
     trace_after(s);
     return e;
 }
@@ -194,8 +217,11 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
     const int sms = cached_sms;
     int sb = stage_dy_blocks(a.M, a.d_out);
     if (sb > per_sm * sms) sb = per_sm * sms;
+    // re-layout-only blocks where the wave has room for them
+    const int pb = prep_blocks(p0, kStageThreads) + prep_blocks(p1, kStageThreads);
+    const int grid = sb + pb <= per_sm * sms ? sb + pb : sb;
     trace_before("bwd_prologue", s);
-    cudaError_t e = launch_k(bwd_prologue_kernel<GPT>, dim3(sb), dim3(kStageThreads), smem, s, p0, p1, a, sb);
+    cudaError_t e = launch_k(bwd_prologue_kernel<GPT>, dim3(grid), dim3(kStageThreads), smem, s, p0, p1, a, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;
@@ -226,7 +252,7 @@ cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaSt
         prepared = true;
     }
     trace_before("reduce_partials", s);
-    cudaError_t e = launch_k(reduce_partials_kernel, dim3(blocks), dim3(256), 0, s, a, b, c);
+    cudaError_t e = launch_k(reduce_partials_kernel, dim3(blocks), dim3(kReduceWarps * 32), 0, s, a, b, c);
     trace_after(s);
     return e;
 }
