@@ -674,6 +674,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     sa.r = r;
     int rows_dh = 0;
     sa.rows_used = &rows_dh;
+    sa.status = status;
 
     GemmArgs b1{};
     b1.M = M;

@@ -2,6 +2,9 @@
 // one-per-call re-layout of the bitmaps into the GEMMs' operand order, the
 // f32 -> f16 staging of x and dy (with the dh token sums fused into the dy
 // staging), and the fixed-order reduction of per-tile partial sums.
+#include <cstdlib>
+#include <cstring>
+
 #include "blr_device.cuh"
 #include "blr_kernels.h"
 #include "blr_stage.cuh"
@@ -83,6 +86,23 @@ __global__ void __launch_bounds__(kStageThreads, (GPT <= 8 ? 2 : 1))
     pdl_launch_dependents();
     if (prologue_prep(p0, p1, stage_blocks)) return;
     stage_dy_run<GPT>(a, blockIdx.x, stage_blocks, smem_f, stage_tpr(a.d_out), kStageThreads);
+}
+
+// Streaming form of the same prologue (rows up to kSdMaxCols wide): one block
+// per SM, a producer warp feeding row batches through a shared-memory ring.
+// Blocks past stage_blocks only do bitmap re-layouts.
+template <int Q>
+__global__ void __launch_bounds__(kSdThreads, 1)
+    bwd_stream_kernel(SignPrep p0, SignPrep p1, StageDyArgs a, int stage_blocks) {
+    extern __shared__ __align__(128) unsigned char smem_b[];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int extra = (int)gridDim.x - stage_blocks;
+    if (extra > 0 && (int)blockIdx.x >= stage_blocks) {
+        prep_share(p0, p1, (int)blockIdx.x - stage_blocks, extra);
+        return;
+    }
+    stage_dy_stream<Q>(a, blockIdx.x, stage_blocks, smem_b, p0, p1, extra > 0 ? 0 : stage_blocks);
 }
 
 int stage_dy_blocks(int M, int d_out) {
@@ -227,7 +247,52 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
     return e;
 }
 
+template <int Q>
+static cudaError_t launch_bwd_stream_t(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = prepare_kernel(bwd_stream_kernel<Q>, kSdHeadBytes + kSdRingBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const SdPlan pl = sd_plan(a.d_out);
+    int sb = (a.M + pl.ngrp - 1) / pl.ngrp;
+    if (sb > sms) sb = sms;
+    const int cap = stage_dy_blocks(a.M, a.d_out);
+    if (sb > cap) sb = cap;
+    // re-layout-only blocks on SMs the staging leaves idle
+    const int pb = prep_blocks(p0, kSdThreads) + prep_blocks(p1, kSdThreads);
+    const int grid = sb + pb <= sms ? sb + pb : sb;
+    trace_before("bwd_prologue", s);
+    cudaError_t e = launch_k(bwd_stream_kernel<Q>, dim3(grid), dim3(kSdThreads), sd_smem_bytes(a.d_out), s, p0, p1,
+                             a, sb);
+    trace_after(s);
+    if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
+    return e;
+}
+
+// BLR_DY_STAGE=rows selects the register-staged row kernel for every width
+// (the streaming kernel is used for rows up to kSdMaxCols otherwise).
+static bool dy_stage_rows_forced() {
+    const char *e = std::getenv("BLR_DY_STAGE");
+    return e && std::strcmp(e, "rows") == 0;
+}
+
 cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
+    if (sd_supported(a.d_out) && !dy_stage_rows_forced()) {
+        switch (sd_plan(a.d_out).Q) {
+            case 2: return launch_bwd_stream_t<2>(p0, p1, a, s);
+            case 4: return launch_bwd_stream_t<4>(p0, p1, a, s);
+            case 6: return launch_bwd_stream_t<6>(p0, p1, a, s);
+            default: return launch_bwd_stream_t<8>(p0, p1, a, s);
+        }
+    }
     switch (stage_gpt(a.d_out)) {
         case 1: return launch_bwd_prologue_t<1>(p0, p1, a, s);
         case 2: return launch_bwd_prologue_t<2>(p0, p1, a, s);

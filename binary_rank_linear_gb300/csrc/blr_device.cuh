@@ -20,6 +20,7 @@ enum : uint32_t {
     kStTimeoutDrain = 1u << 4,   // teardown: in-flight copies or MMAs never drained
     kStBadLaunch = 1u << 5,      // launch geometry inconsistent with the kernel
     kStTimeoutGrid = 1u << 6,    // fused small-M kernel: a grid barrier never completed
+    kStTimeoutStage = 1u << 7,   // streaming dy staging: a row batch never arrived or its slot never freed
 };
 
 // A bounded wait gives up after this much wall time (ns). Normal waits in
@@ -214,6 +215,23 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The same copy with an L2 eviction-priority hint: data read once is marked
+// to leave L2 first, so that what the next kernel reads stays there.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void bulk_load_hint(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
@@ -435,6 +453,21 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&v)[32]) {
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads:
+// every participant gets the same answer (a group-wide decision).
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ------------------------------------------------------ sign expansion -----

@@ -84,6 +84,7 @@ struct StageDyArgs {
     float gscale;          // > 0 fixed, <= 0 dynamic
     int M, d_out, r;
     int *rows_used;        // host out: dh partial rows the launch wrote
+    uint32_t *status;      // device status word (bounded waits of the streaming staging)
 };
 int stage_dy_blocks(int M, int d_out);  // dh partial rows reserved in the workspace
 cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s);

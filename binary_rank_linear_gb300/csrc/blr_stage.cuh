@@ -335,6 +335,301 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
     }
 }
 
+// ================================================ stage dy (streaming) ======
+// The same staging, as a stream of row batches that a producer warp moves
+// into a shared-memory ring with 1-D bulk copies (cp.async.bulk), so that
+// HBM sees several batches in flight per SM whatever the consumers' register
+// budget. Rows up to kSdMaxCols wide. Layout of the work:
+//  - a block owns a contiguous range of token rows;
+//  - its kSdWarps consumer warps form NGRP row groups of W warps; a group
+//    stages one row of a batch (a batch is NGRP consecutive rows, one bulk
+//    copy of dy and one of c per batch);
+//  - lane i of a group owns the float4 columns i, i + 32W, ... (Q of them)
+//    for the whole kernel, so the dh sums of its columns live in registers
+//    and are combined over the groups once, at the end, in a fixed order.
+// Per row: pass 1 over the row in shared memory gives max |dy.h| and
+// sum |dy.h| (shuffles, then a barrier of the group's warps), pass 2 writes
+// f16(dy.h.s_t) with direct 8-byte stores.
+constexpr int kSdWarps = 16;                     // consumer warps
+constexpr int kSdThreads = (kSdWarps + 1) * 32;  // + one producer warp
+constexpr int kSdMaxCols = 8191;  // wider rows: the register-staged row kernel (faster there, measured)
+constexpr int kSdRingBytes = 200 * 1024;
+constexpr int kSdHeadBytes = 1024;  // barriers, flags, reduction buffers
+
+struct SdPlan {
+    int W;        // warps per row group
+    int ngrp;     // row groups (rows per batch)
+    int Q;        // float4 columns per lane, rounded up to the kernel's template value
+    int nst;      // ring stages
+    int batch_bytes;
+};
+
+__host__ __device__ inline SdPlan sd_plan(int d_out) {
+    SdPlan p;
+    int w = d_out / 512;
+    p.W = 1;
+    while (p.W * 2 <= w && p.W < kSdWarps) p.W *= 2;
+    p.ngrp = kSdWarps / p.W;
+    const int q = (d_out / 4 + 32 * p.W - 1) / (32 * p.W);
+    p.Q = q <= 2 ? 2 : (q <= 4 ? 4 : (q <= 6 ? 6 : 8));
+    p.batch_bytes = p.ngrp * d_out * 6;
+    p.nst = kSdRingBytes / p.batch_bytes;
+    if (p.nst > 8) p.nst = 8;
+    return p;
+}
+
+__host__ __device__ inline bool sd_supported(int d_out) {
+    return d_out <= kSdMaxCols && sd_plan(d_out).nst >= 2 && (d_out / 4 + 32 * sd_plan(d_out).W - 1) /
+                                                                   (32 * sd_plan(d_out).W) <= 8;
+}
+
+// 1/2^k for a power-of-two scale 2^k, k in [-126, 127], exactly (2^-127 is subnormal).
+__device__ __forceinline__ float pow2_recip(float s) {
+    const int k = ((__float_as_int(s) >> 23) & 0xFF) - 127;
+    return k <= 126 ? __int_as_float((127 - k) << 23) : __int_as_float(1 << 22);
+}
+
+__host__ __device__ inline size_t sd_smem_bytes(int d_out) {
+    const SdPlan p = sd_plan(d_out);
+    return (size_t)kSdHeadBytes + (size_t)p.nst * p.batch_bytes;
+}
+
+// The block first does its share (1 of prep_nblocks) of the two bitmap
+// re-layouts, while the producer's first copies are in flight.
+template <int Q>
+__device__ void stage_dy_stream(const StageDyArgs &a, int block, int nblocks, unsigned char *smem,
+                                const SignPrep &p0, const SignPrep &p1, int prep_nblocks) {
+    const SdPlan pl = sd_plan(a.d_out);
+    const int G = a.d_out / 4;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);      // [8]
+    uint64_t *empty = full + 8;                                // [8]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 128);
+    float2 *red = reinterpret_cast<float2 *>(smem + 256);     // [2][kSdWarps] row sums, then block maxima
+    unsigned char *ring = smem + kSdHeadBytes;
+
+    const int row0 = (int)((long long)block * a.M / nblocks);
+    const int row1 = (int)((long long)(block + 1) * a.M / nblocks);
+    const int nbatch = (row1 - row0 + pl.ngrp - 1) / pl.ngrp;
+    const uint32_t dy_bytes = (uint32_t)pl.ngrp * a.d_out * 4;  // offset of the c part in a stage
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < pl.nst; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kSdWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ---- producer: one lane of the last warp ----
+    const bool producer = warp == kSdWarps && lane == 0;
+    uint64_t pol = 0;
+    int issued = 0;
+    auto issue = [&](int i) {
+        const int st = i % pl.nst;
+        const int r = row0 + i * pl.ngrp;
+        const int nr = row1 - r < pl.ngrp ? row1 - r : pl.ngrp;
+        unsigned char *dst = ring + (size_t)st * pl.batch_bytes;
+        mbar_arrive_expect_tx(&full[st], (uint32_t)nr * a.d_out * 6);
+        bulk_load_hint(dst, a.dy + (size_t)r * a.d_out, (uint32_t)nr * a.d_out * 4, &full[st], pol);
+        bulk_load_hint(dst + dy_bytes, a.c16 + (size_t)r * a.d_out, (uint32_t)nr * a.d_out * 2, &full[st], pol);
+        issued = i + 1;
+    };
+    if (producer) {
+        pol = l2_policy_evict_first();
+        for (int i = 0; i < nbatch && i < pl.nst; ++i) issue(i);
+    }
+    __syncwarp();
+    if (prep_nblocks > 0) prep_share(p0, p1, block, prep_nblocks);
+    if (warp == kSdWarps) {
+        if (lane != 0) return;
+        for (int i = issued; i < nbatch; ++i) {
+            const int st = i % pl.nst;
+            if (!mbar_wait(&empty[st], (uint32_t)((i / pl.nst - 1) & 1), abort_flag)) {
+                if (!*abort_flag) {
+                    *abort_flag = 1;
+                    atomicOr(a.status, kStTimeoutStage);
+                }
+                break;
+            }
+            issue(i);
+        }
+        // every issued copy lands before the block may exit
+        for (int j = issued - pl.nst < 0 ? 0 : issued - pl.nst; j < issued; ++j)
+            if (!mbar_wait(&full[j % pl.nst], (uint32_t)((j / pl.nst) & 1), abort_flag, false))
+                atomicOr(a.status, kStTimeoutDrain);
+        return;
+    }
+
+    // ---- consumers ----
+    const int grp = warp / pl.W;            // row group
+    const int ti = threadIdx.x % (32 * pl.W);  // index in the group
+    const int wg = warp % pl.W;             // warp in the group
+    const int gthreads = 32 * pl.W;
+    const bool dynamic = !(a.gscale > 0.0f);
+    const float ginv = dynamic ? 1.0f : 1.0f / a.gscale;
+    float lmax = 0.0f;
+    if (dynamic) {
+        for (int k = lane; k < a.r; k += 32) lmax = fmaxf(lmax, fabsf(__ldg(a.l + k)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+    }
+    const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
+    float4 hv[Q], dh[Q];
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+        const int col = ti + k * gthreads;
+        hv[k] = col < G ? __ldg(h4 + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+        dh[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    uint2 *o4 = reinterpret_cast<uint2 *>(a.dy16);
+    float2 mx = make_float2(0.0f, 0.0f);  // this thread's rows: max 1/s_t, max 1/sigma_t
+    bool failed = false;
+    for (int i = 0; i < nbatch; ++i) {
+        const int st = i % pl.nst;
+        bool ok = mbar_wait(&full[st], (uint32_t)((i / pl.nst) & 1), abort_flag);
+        if (!ok && !*abort_flag) {
+            *abort_flag = 1;
+            atomicOr(a.status, kStTimeoutStage);
+        }
+        const int t = row0 + i * pl.ngrp + grp;
+        const bool valid = ok && t < row1;
+        const float4 *sdy = reinterpret_cast<const float4 *>(ring + (size_t)st * pl.batch_bytes) + (size_t)grp * G;
+        const uint2 *sc = reinterpret_cast<const uint2 *>(ring + (size_t)st * pl.batch_bytes + dy_bytes) +
+                          (size_t)grp * G;
+        float amax = 0.0f, l1 = 0.0f;
+        if (valid) {
+#pragma unroll
+            for (int k = 0; k < Q; ++k) {
+                const int col = ti + k * gthreads;
+                if (col < G) {
+                    const float4 d = sdy[col];
+                    const uint2 cw = sc[col];
+                    const float2 c0 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.x));
+                    const float2 c1 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.y));
+                    dh[k].x += d.x * c0.x;
+                    dh[k].y += d.y * c0.y;
+                    dh[k].z += d.z * c1.x;
+                    dh[k].w += d.w * c1.y;
+                    const float vx = fabsf(d.x * hv[k].x), vy = fabsf(d.y * hv[k].y);
+                    const float vz = fabsf(d.z * hv[k].z), vw = fabsf(d.w * hv[k].w);
+                    amax = fmaxf(amax, fmaxf(fmaxf(vx, vy), fmaxf(vz, vw)));
+                    l1 += (vx + vy) + (vz + vw);
+                }
+            }
+        }
+        float s = a.gscale, sig = a.gscale;
+        bool counts = true;
+        if (dynamic) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+            }
+        }
+        if (pl.W > 1) {
+            // the group's warps exchange their sums and agree on whether to go on
+            if (dynamic && lane == 0) red[(i & 1) * kSdWarps + warp] = make_float2(amax, l1);
+            failed = named_bar_or(1 + grp, gthreads, !ok || *abort_flag);
+            if (dynamic) {
+                float2 r = red[(i & 1) * kSdWarps + grp * pl.W];
+                for (int q = 1; q < pl.W; ++q) {
+                    const float2 o = red[(i & 1) * kSdWarps + grp * pl.W + q];
+                    r.x = fmaxf(r.x, o.x);
+                    r.y += o.y;
+                }
+                amax = r.x;
+                l1 = r.y;
+            }
+        } else {
+            failed = !ok || *abort_flag;
+        }
+        (void)wg;
+        if (dynamic) {
+            const bool fin = amax > 0.0f && amax <= 3.402823466e38f;
+            counts = fin;
+            s = fin ? pow2i(14 - ceil_log2_pos(amax)) : 1.0f;
+            sig = s;
+            const float bound = l1 * lmax;  // bound on |db_t . l|, unscaled
+            if (fin && bound > 0.0f && bound <= 3.402823466e38f) sig = pow2i(15 - ceil_log2_pos(bound));
+        }
+        if (valid) {
+#pragma unroll
+            for (int k = 0; k < Q; ++k) {
+                const int col = ti + k * gthreads;
+                if (col < G) {
+                    const float4 d = sdy[col];  // re-read: fewer live registers than keeping dy.h
+                    const float4 v = make_float4(d.x * hv[k].x, d.y * hv[k].y, d.z * hv[k].z, d.w * hv[k].w);
+                    uint2 o;
+                    o.x = pack_half2(v.x * s, v.y * s);
+                    o.y = pack_half2(v.z * s, v.w * s);
+                    o4[(size_t)t * G + col] = o;
+                }
+            }
+            if (ti == 0) {
+                const float si = dynamic ? pow2_recip(s) : ginv, gi = dynamic ? pow2_recip(sig) : ginv;
+                a.s_inv[t] = si;
+                a.sig[t] = sig;
+                a.sig_inv[t] = gi;
+                if (counts) mx = make_float2(fmaxf(mx.x, si), fmaxf(mx.y, gi));
+            }
+        }
+        // the stage's shared memory is read: hand it back to the producer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (failed) break;
+    }
+    // ---- block end: maxima and the dh partial row, fixed order ----
+    const int cthreads = kSdWarps * 32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx.x = fmaxf(mx.x, __shfl_xor_sync(0xFFFFFFFFu, mx.x, o));
+        mx.y = fmaxf(mx.y, __shfl_xor_sync(0xFFFFFFFFu, mx.y, o));
+    }
+    if (named_bar_or(9, cthreads, *abort_flag != 0)) return;  // every consumer is done with the ring
+    if (lane == 0) red[2 * kSdWarps + warp] = mx;
+    float4 *dst = reinterpret_cast<float4 *>(a.part_dh + (size_t)block * a.d_out);
+    if (pl.ngrp == 1) {
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            const int col = ti + k * gthreads;
+            if (col < G) dst[col] = dh[k];
+        }
+    } else {
+        float4 *acc = reinterpret_cast<float4 *>(ring);  // [ngrp][G]
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            const int col = ti + k * gthreads;
+            if (col < G) acc[(size_t)grp * G + col] = dh[k];
+        }
+    }
+    named_bar_sync(9, cthreads);
+    if (threadIdx.x == 0) {
+        float2 m = red[2 * kSdWarps];
+        for (int q = 1; q < kSdWarps; ++q) {
+            m.x = fmaxf(m.x, red[2 * kSdWarps + q].x);
+            m.y = fmaxf(m.y, red[2 * kSdWarps + q].y);
+        }
+        a.blkmax[block] = m;
+    }
+    if (pl.ngrp > 1) {
+        const float4 *acc = reinterpret_cast<const float4 *>(ring);
+        for (int col = threadIdx.x; col < G; col += cthreads) {
+            float4 v = acc[col];
+            for (int q = 1; q < pl.ngrp; ++q) {
+                const float4 o = acc[(size_t)q * G + col];
+                v.x += o.x;
+                v.y += o.y;
+                v.z += o.z;
+                v.w += o.w;
+            }
+            dst[col] = v;
+        }
+    }
+}
+
 // ============================================================== reduce =====
 // out[f] += sum_p part[p][f] over three segments, 32 columns per work item:
 // warp w of the block sums rows w, w + nwarps, ... and the warp sums are

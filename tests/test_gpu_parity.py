@@ -137,6 +137,8 @@ SHAPES = [
     # small M with a wide output: the fused small-M forward, then the general
     # backward (its dy rows are too wide for the fused staging)
     ("small", 200, 128, 9216, 64),
+    # the widest rows the streaming dy staging takes (one row per batch, two stages)
+    ("small", 150, 128, 16384, 64),
 ]
 
 
@@ -338,3 +340,14 @@ def test_split_k_integer_grid_bit_exact(monkeypatch):
     assert np.array_equal(out["y"], fw["y"].astype(np.float32))
     assert np.array_equal(out["dx"], bw["dx"].astype(np.float32))
     assert oracle.rel_err(out["dl"], bw["dl"]) == 0.0
+
+
+@pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 513, 512, 4096, 256),
+                                                 ("small", 150, 128, 12288, 64)])
+def test_dy_staging_forms(monkeypatch, name, M, d_in, d_out, r):
+    """The register-staged row kernel (BLR_DY_STAGE=rows) against the oracle on
+    widths the streaming staging takes by default."""
+    monkeypatch.setenv("BLR_DY_STAGE", "rows")
+    t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    out = _run(t)
+    _check_against_oracle(t, out, "(BLR_DY_STAGE=rows)")
