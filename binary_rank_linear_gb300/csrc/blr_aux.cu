@@ -78,6 +78,18 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(SignPrep p0, SignPrep
     stage_x_run(x, g, x16, M, d_in, blockIdx.x, stage_blocks);
 }
 
+// The same prologue with x staged by rows (d_in up to kSxMaxCols).
+template <int KQ>
+__global__ void __launch_bounds__(512) fwd_prologue_rows_kernel(SignPrep p0, SignPrep p1, const float *x,
+                                                                const float *g, uint16_t *x16, int M, int d_in,
+                                                                uint32_t *status, int stage_blocks) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    if (prologue_prep(p0, p1, stage_blocks)) return;
+    stage_x_rows<KQ>(x, g, x16, M, d_in, blockIdx.x, stage_blocks);
+}
+
 template <int GPT>
 __global__ void __launch_bounds__(kStageThreads, (GPT <= 8 ? 2 : 1))
     bwd_prologue_kernel(SignPrep p0, SignPrep p1, StageDyArgs a, int stage_blocks) {
@@ -175,8 +187,57 @@ cudaError_t launch_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, i
     return e;
 }
 
+template <int KQ>
+static cudaError_t launch_fwd_prologue_rows(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16,
+                                           int M, int d_in, uint32_t *status, cudaStream_t s) {
+    static bool prepared = false;
+    if (!prepared) {
+        cudaError_t e = prepare_kernel(fwd_prologue_rows_kernel<KQ>, 0);
+        if (e != cudaSuccess) return e;
+        prepared = true;
+    }
+    const int T = sx_threads(d_in);
+    // blocks per SM for this block size, queried once per size
+    static int cached_t[8] = {0}, cached_wave[8] = {0};
+    int wave = 0;
+    for (int i = 0; i < 8; ++i)
+        if (cached_t[i] == T) wave = cached_wave[i];
+    if (wave == 0) {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_prologue_rows_kernel<KQ>, T, 0);
+        wave = (per_sm < 1 ? 1 : per_sm) * sms;
+        for (int i = 0; i < 8; ++i)
+            if (cached_t[i] == 0) {
+                cached_t[i] = T;
+                cached_wave[i] = wave;
+                break;
+            }
+    }
+    const int nchunks = (M + sx_rows(KQ) - 1) / sx_rows(KQ);
+    const int bs = nchunks < wave ? nchunks : wave;
+    const int pb = prep_blocks(p0, T) + prep_blocks(p1, T);
+    const int grid = bs + pb <= wave ? bs + pb : bs;
+    trace_before("fwd_prologue", s);
+    cudaError_t e = launch_k(fwd_prologue_rows_kernel<KQ>, dim3(grid), dim3(T), 0, s, p0, p1, x, g, x16, M, d_in,
+                             status, bs);
+    trace_after(s);
+    return e;
+}
+
 cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
                                 int d_in, uint32_t *status, cudaStream_t s) {
+    const char *form = std::getenv("BLR_X_STAGE");
+    if (d_in <= kSxMaxCols && !(form && std::strcmp(form, "flat") == 0)) {
+        switch (sx_kq(d_in)) {
+            case 1: return launch_fwd_prologue_rows<1>(p0, p1, x, g, x16, M, d_in, status, s);
+            case 2: return launch_fwd_prologue_rows<2>(p0, p1, x, g, x16, M, d_in, status, s);
+            case 4: return launch_fwd_prologue_rows<4>(p0, p1, x, g, x16, M, d_in, status, s);
+            case 6: return launch_fwd_prologue_rows<6>(p0, p1, x, g, x16, M, d_in, status, s);
+            default: return launch_fwd_prologue_rows<8>(p0, p1, x, g, x16, M, d_in, status, s);
+        }
+    }
     static bool prepared = false;
     if (!prepared) {
         cudaError_t e = prepare_kernel(fwd_prologue_kernel, 0);

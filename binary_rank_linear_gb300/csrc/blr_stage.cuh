@@ -138,6 +138,68 @@ __device__ inline void stage_x_run(const float *__restrict__ x, const float *__r
     }
 }
 
+// x staging by rows (d_in up to kSxMaxCols): a block of T threads walks
+// chunks of R consecutive rows; thread t owns the float4 columns t, t + T, ..
+// (KQ of them) and keeps their g factors in registers, so the loop is R * KQ
+// streaming loads in flight, the products and 8-byte stores.
+constexpr int kSxMaxCols = 16384;
+
+__host__ __device__ inline int sx_kq(int d_in) {
+    const int q = (d_in / 4 + 511) / 512;  // blocks of at most 512 threads
+    return q <= 2 ? q : (q <= 4 ? 4 : (q <= 6 ? 6 : 8));
+}
+
+__host__ __device__ inline int sx_threads(int d_in) {
+    const int kq = sx_kq(d_in);
+    const int t = (d_in / 4 + kq - 1) / kq;
+    return (t + 31) / 32 * 32;
+}
+
+__host__ __device__ constexpr int sx_rows(int kq) { return (8 + kq - 1) / kq; }
+
+template <int KQ>
+__device__ void stage_x_rows(const float *__restrict__ x, const float *__restrict__ g, uint16_t *__restrict__ x16,
+                             int M, int d_in, int block, int nblocks) {
+    constexpr int R = sx_rows(KQ);
+    const int G = d_in / 4;
+    const int T = blockDim.x;
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    uint2 *o = reinterpret_cast<uint2 *>(x16);
+    float4 gv[KQ];
+#pragma unroll
+    for (int k = 0; k < KQ; ++k) {
+        const int col = threadIdx.x + k * T;
+        gv[k] = col < G ? __ldg(reinterpret_cast<const float4 *>(g) + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int nchunks = (M + R - 1) / R;
+    for (int c = block; c < nchunks; c += nblocks) {
+        float4 v[R][KQ];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int row = c * R + j;
+#pragma unroll
+            for (int k = 0; k < KQ; ++k) {
+                const int col = threadIdx.x + k * T;
+                if (row < M && col < G) v[j][k] = __ldcs(x4 + (size_t)row * G + col);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int row = c * R + j;
+#pragma unroll
+            for (int k = 0; k < KQ; ++k) {
+                const int col = threadIdx.x + k * T;
+                if (row < M && col < G) {
+                    uint2 out;
+                    out.x = pack_half2(v[j][k].x * gv[k].x, v[j][k].y * gv[k].y);
+                    out.y = pack_half2(v[j][k].z * gv[k].z, v[j][k].w * gv[k].w);
+                    o[(size_t)row * G + col] = out;
+                }
+            }
+        }
+    }
+}
+
 // =========================================================== stage dy ======
 // Backward staging (train_mm.rs, `blr_backward`: cvt of dy with the column
 // factor h under the gradient scale, and `colsum_prod` of dy and c for dh).

@@ -351,3 +351,13 @@ def test_dy_staging_forms(monkeypatch, name, M, d_in, d_out, r):
     t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     out = _run(t)
     _check_against_oracle(t, out, "(BLR_DY_STAGE=rows)")
+
+
+@pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 513, 4096, 512, 256)])
+def test_x_staging_forms(monkeypatch, name, M, d_in, d_out, r):
+    """The flat grid-stride x staging (BLR_X_STAGE=flat) against the oracle on
+    widths the row-mapped staging takes by default."""
+    monkeypatch.setenv("BLR_X_STAGE", "flat")
+    t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    out = _run(t)
+    _check_against_oracle(t, out, "(BLR_X_STAGE=flat)")
