@@ -286,7 +286,7 @@ namespace blr {
 // (160 or 192: MMAs of N >= 160 run at full rate) that needs the fewest
 // token-rounds of the persistent grid; otherwise single CTAs with 128-token
 // tiles, for more tiles in flight on small problems.
-GemmPlan plan_gemm(int M, int N, int sms) {
+GemmPlan plan_gemm(int M, int N, int sms, bool allow64) {
     const int pairs = sms / 2;
     const long long fp = (N + 255) / 256;
     GemmPlan best{false, 0, 0, 0};
@@ -304,6 +304,15 @@ GemmPlan plan_gemm(int M, int N, int sms) {
     if (best.bt != 0) return best;
     const long long t_tiles = (M + 127) / 128;
     const long long tiles = t_tiles * ((N + 127) / 128);
+    // few tiles: 64-token tiles put twice as many SMs to work (a tile's time is
+    // set by its k-loop's latency at these sizes, not by its MMA time);
+    // BLR_GEMM_BT=128 keeps 128-token tiles
+    const char *v = std::getenv("BLR_GEMM_BT");
+    if (allow64 && 2 * tiles <= sms && M > 64 && !(v && std::strcmp(v, "128") == 0)) {
+        const long long t64 = (M + 63) / 64;
+        const long long tiles64 = t64 * ((N + 127) / 128);
+        return GemmPlan{false, 64, (int)(tiles64 < sms ? tiles64 : sms), (int)t64};
+    }
     return GemmPlan{false, 128, (int)(tiles < sms ? tiles : sms), (int)t_tiles};
 }
 
@@ -360,12 +369,11 @@ bool wide_token_major() {
 GemmPlan plan_split(GemmPlan p, int M, int N, int K, int sms) {
     const char *v = std::getenv("BLR_SPLITK");
     if (!(v && std::strcmp(v, "1") == 0)) return p;
-    if (p.pair || p.plane || p.bt != 128) return p;
-    const long long tiles = (long long)((M + 127) / 128) * ((N + 127) / 128);
+    if (p.pair || p.plane) return p;
+    const long long t_tiles = (M + 127) / 128;
+    const long long tiles = t_tiles * ((N + 127) / 128);
     if (tiles * 4 > sms || (K + 127) / 128 < 4) return p;
-    p.split = 4;
-    p.grid = (int)(tiles * 4);
-    return p;
+    return GemmPlan{false, 128, (int)(tiles * 4), (int)t_tiles, false, 4};
 }
 
 // Grid of the fused small-M kernels: enough CTAs for the larger GEMM phase's
@@ -476,9 +484,9 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     uint16_t *plane_u = reinterpret_cast<uint16_t *>(w + L.plane_u);
     uint16_t *plane_v = reinterpret_cast<uint16_t *>(w + L.plane_v);
     // the TMEM-expansion tiles decide what counts as a small problem (fused path)
-    const GemmPlan q1 = plan_gemm(M, r, sms);
-    const GemmPlan q2 = plan_gemm(M, d_out, sms);
-    const bool fused = !q1.pair && !q2.pair && fused_small_enabled();
+    const bool fused = !plan_gemm(M, r, sms).pair && !plan_gemm(M, d_out, sms).pair && fused_small_enabled();
+    const GemmPlan q1 = plan_gemm(M, r, sms, !fused);
+    const GemmPlan q2 = plan_gemm(M, d_out, sms, !fused);
     const bool planes = !fused && plane_mode();
     const bool dense2 = !fused && wide_token_major();
     const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : (fused ? q1 : plan_split(q1, M, r, d_in, sms));
@@ -612,9 +620,10 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
 
     uint16_t *plane_u = reinterpret_cast<uint16_t *>(w + L.plane_u);
     uint16_t *plane_v = reinterpret_cast<uint16_t *>(w + L.plane_v);
-    const GemmPlan q1 = plan_gemm(M, r, sms);
-    const GemmPlan q2 = plan_gemm(M, d_in, sms);
-    const bool fused = !q1.pair && !q2.pair && small_bwd_fits(d_out) && fused_small_enabled();
+    const bool fused =
+        !plan_gemm(M, r, sms).pair && !plan_gemm(M, d_in, sms).pair && small_bwd_fits(d_out) && fused_small_enabled();
+    const GemmPlan q1 = plan_gemm(M, r, sms, !fused);
+    const GemmPlan q2 = plan_gemm(M, d_in, sms, !fused);
     const bool planes = !fused && plane_mode();
     const bool dense2 = !fused && wide_token_major();
     const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : (fused ? q1 : plan_split(q1, M, r, d_out, sms));

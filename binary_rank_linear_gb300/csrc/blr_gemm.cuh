@@ -877,6 +877,7 @@ cudaError_t launch_gemm_epi(const GemmPlan &plan, const GemmMaps &maps, const Ge
     if (plan.pair && plan.bt == 192) return launch_gemm_t<EPI, true, 192>(maps, args, plan.grid, s);
     if (plan.pair && plan.bt == 160) return launch_gemm_t<EPI, true, 160>(maps, args, plan.grid, s);
     if (!plan.pair && plan.bt == 128) return launch_gemm_t<EPI, false, 128>(maps, args, plan.grid, s);
+    if (!plan.pair && plan.bt == 64) return launch_gemm_t<EPI, false, 64>(maps, args, plan.grid, s);
     return cudaErrorInvalidValue;
 }
 

@@ -160,7 +160,9 @@ struct GemmPlan {
     int split;
 };
 
-GemmPlan plan_gemm(int M, int N, int sms);        // TMEM-expansion tiles
+// TMEM-expansion tiles; allow64: 64-token single-CTA tiles when 128-token
+// tiles would fill at most half the SMs (the fused small-M kernels take 128)
+GemmPlan plan_gemm(int M, int N, int sms, bool allow64 = true);
 GemmPlan plan_gemm_plane(int M, int N, int sms);  // plane tiles
 
 cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
