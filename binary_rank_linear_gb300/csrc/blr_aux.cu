@@ -90,6 +90,25 @@ __global__ void __launch_bounds__(512) fwd_prologue_rows_kernel(SignPrep p0, Sig
     stage_x_rows<KQ>(x, g, x16, M, d_in, blockIdx.x, stage_blocks);
 }
 
+// The same prologue with x streamed through a shared-memory ring (one block
+// per SM; blocks past stage_blocks only do bitmap re-layouts).
+template <int KQ>
+__global__ void __launch_bounds__(kSxsThreads, 1)
+    fwd_prologue_stream_kernel(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
+                               int d_in, uint32_t *status, int stage_blocks) {
+    extern __shared__ __align__(128) unsigned char smem_b[];
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    const int extra = (int)gridDim.x - stage_blocks;
+    if (extra > 0 && (int)blockIdx.x >= stage_blocks) {
+        prep_share(p0, p1, (int)blockIdx.x - stage_blocks, extra);
+        return;
+    }
+    stage_x_stream<KQ>(x, g, x16, M, d_in, blockIdx.x, stage_blocks, smem_b, status, p0, p1,
+                       extra > 0 ? 0 : stage_blocks);
+}
+
 template <int GPT>
 __global__ void __launch_bounds__(kStageThreads, (GPT <= 8 ? 2 : 1))
     bwd_prologue_kernel(SignPrep p0, SignPrep p1, StageDyArgs a, int stage_blocks) {
@@ -226,9 +245,49 @@ static cudaError_t launch_fwd_prologue_rows(SignPrep p0, SignPrep p1, const floa
     return e;
 }
 
+template <int KQ>
+static cudaError_t launch_fwd_prologue_stream(SignPrep p0, SignPrep p1, const float *x, const float *g,
+                                             uint16_t *x16, int M, int d_in, uint32_t *status, cudaStream_t s) {
+    static bool prepared = false;
+    if (!prepared) {
+        cudaError_t e = prepare_kernel(fwd_prologue_stream_kernel<KQ>, kSxsHeadBytes + kSxsRingBytes);
+        if (e != cudaSuccess) return e;
+        prepared = true;
+    }
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const SxPlan pl = sxs_plan(d_in);
+    int sb = (M + pl.rs - 1) / pl.rs;
+    if (sb > sms) sb = sms;
+    const int pb = prep_blocks(p0, kSxsThreads) + prep_blocks(p1, kSxsThreads);
+    const int grid = sb + pb <= sms ? sb + pb : sb;
+    trace_before("fwd_prologue", s);
+    cudaError_t e = launch_k(fwd_prologue_stream_kernel<KQ>, dim3(grid), dim3(kSxsThreads), sxs_smem_bytes(d_in), s,
+                             p0, p1, x, g, x16, M, d_in, status, sb);
+    trace_after(s);
+    return e;
+}
+
 cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
                                 int d_in, uint32_t *status, cudaStream_t s) {
+    // Streaming for large x (measured on GB300: 134 MB of x 43 -> 39 us, 805 MB
+    // 233 -> 190 us), rows for small ones (8 MB: 8.2 us rows, 10.4 streamed).
+    // BLR_X_STAGE=stream|rows|flat forces a form.
     const char *form = std::getenv("BLR_X_STAGE");
+    const bool want_stream = form ? std::strcmp(form, "stream") == 0 : (long long)M * d_in * 4 >= (64ll << 20);
+    if (d_in <= kSxMaxCols && want_stream && sxs_plan(d_in).nst >= 2) {
+        switch (sx_kq(d_in)) {
+            case 1: return launch_fwd_prologue_stream<1>(p0, p1, x, g, x16, M, d_in, status, s);
+            case 2: return launch_fwd_prologue_stream<2>(p0, p1, x, g, x16, M, d_in, status, s);
+            case 4: return launch_fwd_prologue_stream<4>(p0, p1, x, g, x16, M, d_in, status, s);
+            case 6: return launch_fwd_prologue_stream<6>(p0, p1, x, g, x16, M, d_in, status, s);
+            default: return launch_fwd_prologue_stream<8>(p0, p1, x, g, x16, M, d_in, status, s);
+        }
+    }
     if (d_in <= kSxMaxCols && !(form && std::strcmp(form, "flat") == 0)) {
         switch (sx_kq(d_in)) {
             case 1: return launch_fwd_prologue_rows<1>(p0, p1, x, g, x16, M, d_in, status, s);

@@ -200,6 +200,147 @@ __device__ void stage_x_rows(const float *__restrict__ x, const float *__restric
     }
 }
 
+// x staging as a stream of row batches (d_in up to kSxMaxCols), the ring and
+// producer of the streaming dy staging below without its row reductions: a
+// producer warp bulk-copies batches of consecutive rows of x into a
+// shared-memory ring; the consumer threads form row groups of T threads (T as
+// in stage_x_rows) that own fixed float4 columns, keep their g factors in
+// registers, and write f16(x.g) with 8-byte stores.
+constexpr int kSxsWarps = 16;
+constexpr int kSxsThreads = (kSxsWarps + 1) * 32;
+constexpr int kSxsRingBytes = 200 * 1024;
+constexpr int kSxsHeadBytes = 256;
+
+struct SxPlan {
+    int T;      // threads per row group
+    int ngr;    // row groups
+    int rs;     // rows per batch (a multiple of ngr)
+    int nst;    // ring stages
+};
+
+__host__ __device__ inline SxPlan sxs_plan(int d_in) {
+    SxPlan p;
+    p.T = sx_threads(d_in);
+    p.ngr = (kSxsWarps * 32) / p.T;
+    int m = 32768 / (p.ngr * d_in * 4);
+    if (m < 1) m = 1;
+    p.rs = p.ngr * m;
+    p.nst = kSxsRingBytes / (p.rs * d_in * 4);
+    if (p.nst > 8) p.nst = 8;
+    return p;
+}
+
+__host__ __device__ inline size_t sxs_smem_bytes(int d_in) {
+    const SxPlan p = sxs_plan(d_in);
+    return (size_t)kSxsHeadBytes + (size_t)p.nst * p.rs * d_in * 4;
+}
+
+// The block first does its share (1 of prep_nblocks) of the two bitmap
+// re-layouts, while the producer's first copies are in flight.
+template <int KQ>
+__device__ void stage_x_stream(const float *__restrict__ x, const float *__restrict__ g, uint16_t *__restrict__ x16,
+                               int M, int d_in, int block, int nblocks, unsigned char *smem, uint32_t *status,
+                               const SignPrep &p0, const SignPrep &p1, int prep_nblocks) {
+    const SxPlan pl = sxs_plan(d_in);
+    const int G = d_in / 4;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [8]
+    uint64_t *empty = full + 8;                            // [8]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 128);
+    unsigned char *ring = smem + kSxsHeadBytes;
+    const uint32_t stage_bytes = (uint32_t)pl.rs * d_in * 4;
+    const int row0 = (int)((long long)block * M / nblocks);
+    const int row1 = (int)((long long)(block + 1) * M / nblocks);
+    const int nbatch = (row1 - row0 + pl.rs - 1) / pl.rs;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < pl.nst; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kSxsWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool producer = warp == kSxsWarps && lane == 0;
+    uint64_t pol = 0;
+    int issued = 0;
+    auto issue = [&](int i) {
+        const int st = i % pl.nst;
+        const int r = row0 + i * pl.rs;
+        const int nr = row1 - r < pl.rs ? row1 - r : pl.rs;
+        mbar_arrive_expect_tx(&full[st], (uint32_t)nr * d_in * 4);
+        bulk_load_hint(ring + (size_t)st * stage_bytes, x + (size_t)r * d_in, (uint32_t)nr * d_in * 4, &full[st], pol);
+        issued = i + 1;
+    };
+    if (producer) {
+        pol = l2_policy_evict_first();
+        for (int i = 0; i < nbatch && i < pl.nst; ++i) issue(i);
+    }
+    __syncwarp();
+    if (prep_nblocks > 0) prep_share(p0, p1, block, prep_nblocks);
+    if (warp == kSxsWarps) {
+        if (lane != 0) return;
+        for (int i = issued; i < nbatch; ++i) {
+            const int st = i % pl.nst;
+            if (!mbar_wait(&empty[st], (uint32_t)((i / pl.nst - 1) & 1), abort_flag)) {
+                if (!*abort_flag) {
+                    *abort_flag = 1;
+                    atomicOr(status, kStTimeoutStage);
+                }
+                break;
+            }
+            issue(i);
+        }
+        // every issued copy lands before the block may exit
+        for (int j = issued - pl.nst < 0 ? 0 : issued - pl.nst; j < issued; ++j)
+            if (!mbar_wait(&full[j % pl.nst], (uint32_t)((j / pl.nst) & 1), abort_flag, false))
+                atomicOr(status, kStTimeoutDrain);
+        return;
+    }
+    // ---- consumers ----
+    const int grp = threadIdx.x / pl.T;
+    const int ti = threadIdx.x % pl.T;
+    const bool active = grp < pl.ngr;
+    float4 gv[KQ];
+#pragma unroll
+    for (int k = 0; k < KQ; ++k) {
+        const int col = ti + k * pl.T;
+        gv[k] = active && col < G ? __ldg(reinterpret_cast<const float4 *>(g) + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    uint2 *o = reinterpret_cast<uint2 *>(x16);
+    for (int i = 0; i < nbatch; ++i) {
+        const int st = i % pl.nst;
+        if (!mbar_wait(&full[st], (uint32_t)((i / pl.nst) & 1), abort_flag)) {
+            if (!*abort_flag) {
+                *abort_flag = 1;
+                atomicOr(status, kStTimeoutStage);
+            }
+            break;
+        }
+        const int r = row0 + i * pl.rs;
+        const int nr = row1 - r < pl.rs ? row1 - r : pl.rs;
+        const float4 *sx = reinterpret_cast<const float4 *>(ring + (size_t)st * stage_bytes);
+        if (active) {
+            for (int j = grp; j < nr; j += pl.ngr) {
+#pragma unroll
+                for (int k = 0; k < KQ; ++k) {
+                    const int col = ti + k * pl.T;
+                    if (col < G) {
+                        const float4 v = sx[(size_t)j * G + col];
+                        uint2 out;
+                        out.x = pack_half2(v.x * gv[k].x, v.y * gv[k].y);
+                        out.y = pack_half2(v.z * gv[k].z, v.w * gv[k].w);
+                        o[(size_t)(r + j) * G + col] = out;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+}
+
 // =========================================================== stage dy ======
 // Backward staging (train_mm.rs, `blr_backward`: cvt of dy with the column
 // factor h under the gradient scale, and `colsum_prod` of dy and c for dh).

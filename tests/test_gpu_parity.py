@@ -353,11 +353,13 @@ def test_dy_staging_forms(monkeypatch, name, M, d_in, d_out, r):
     _check_against_oracle(t, out, "(BLR_DY_STAGE=rows)")
 
 
-@pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 513, 4096, 512, 256)])
-def test_x_staging_forms(monkeypatch, name, M, d_in, d_out, r):
-    """The flat grid-stride x staging (BLR_X_STAGE=flat) against the oracle on
-    widths the row-mapped staging takes by default."""
-    monkeypatch.setenv("BLR_X_STAGE", "flat")
+@pytest.mark.parametrize("form", ["flat", "rows", "stream"])
+@pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 513, 4096, 512, 256),
+                                                 ("small", 77, 12288, 256, 64)])
+def test_x_staging_forms(monkeypatch, form, name, M, d_in, d_out, r):
+    """Each x staging form (grid-stride, row-mapped, streamed through the
+    shared-memory ring), forced with BLR_X_STAGE, against the oracle."""
+    monkeypatch.setenv("BLR_X_STAGE", form)
     t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     out = _run(t)
-    _check_against_oracle(t, out, "(BLR_X_STAGE=flat)")
+    _check_against_oracle(t, out, f"(BLR_X_STAGE={form})")
