@@ -186,7 +186,7 @@ def job_tokens_per_s(world: int, tokens_per_rank_step: int, steps: int, ms: floa
 
 
 # ---------------------------------------------------------- CPU oracle ------
-def cpu_oracle_rate(w, budget_s: float = 12.0, max_reps: int = 50):
+def cpu_oracle_rate(w, budget_s: float = 12.0, max_reps: int = 1_000_000):
     """tokens/s of the CPU f64 oracle (as it stands) on the workload's batch,
     repeated until ``budget_s`` seconds of CPU work have run. For workloads
     whose batch would exceed the budget, a prefix of the tokens is used."""
@@ -594,8 +594,8 @@ def main():
             return
         budget = 10.0
         t0 = time.perf_counter()
-        for _ in range(args.warmup):
-            pass
+        for _ in range(args.warmup):  # untimed warm-up passes of the same sample
+            cpu_oracle_rate(w, budget_s=0.0, max_reps=1)
         per_step = []
         base = None
         for _ in range(args.steps):
