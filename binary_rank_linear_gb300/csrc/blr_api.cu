@@ -286,7 +286,7 @@ namespace blr {
 // (160 or 192: MMAs of N >= 160 run at full rate) that needs the fewest
 // token-rounds of the persistent grid; otherwise single CTAs with 128-token
 // tiles, for more tiles in flight on small problems.
-GemmPlan plan_gemm(int M, int N, int sms, bool allow64) {
+GemmPlan plan_gemm(int M, int N, int sms, bool allow64, int tile_cost) {
     const int pairs = sms / 2;
     const long long fp = (N + 255) / 256;
     GemmPlan best{false, 0, 0, 0};
@@ -295,7 +295,8 @@ GemmPlan plan_gemm(int M, int N, int sms, bool allow64) {
         const long long t_tiles = (M + bt - 1) / bt;
         const long long tiles = t_tiles * fp;
         if (tiles < pairs) continue;
-        const long long cost = ((tiles + pairs - 1) / pairs) * bt;  // rounds x MMA time per tile
+        // rounds x (a tile's fixed cost + its time per token), in tokens
+        const long long cost = ((tiles + pairs - 1) / pairs) * (bt + tile_cost);
         if (best.bt == 0 || cost < best_cost) {
             best = GemmPlan{true, bt, 2 * pairs, (int)t_tiles};
             best_cost = cost;
@@ -486,7 +487,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     // the TMEM-expansion tiles decide what counts as a small problem (fused path)
     const bool fused = !plan_gemm(M, r, sms).pair && !plan_gemm(M, d_out, sms).pair && fused_small_enabled();
     const GemmPlan q1 = plan_gemm(M, r, sms, !fused);
-    const GemmPlan q2 = plan_gemm(M, d_out, sms, !fused);
+    const GemmPlan q2 = plan_gemm(M, d_out, sms, !fused, kWideTileCost);
     const bool planes = !fused && plane_mode();
     const bool dense2 = !fused && wide_token_major();
     const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : (fused ? q1 : plan_split(q1, M, r, d_in, sms));

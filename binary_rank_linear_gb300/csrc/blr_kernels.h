@@ -162,7 +162,15 @@ struct GemmPlan {
 
 // TMEM-expansion tiles; allow64: 64-token single-CTA tiles when 128-token
 // tiles would fill at most half the SMs (the fused small-M kernels take 128)
-GemmPlan plan_gemm(int M, int N, int sms, bool allow64 = true);
+// tile_cost: a tile's fixed cost in token units (CTA-pair tile choice)
+GemmPlan plan_gemm(int M, int N, int sms, bool allow64 = true, int tile_cost = 0);
+// The c-product (K = r, output d_out wide) has a large fixed cost per tile:
+// fitted on GB300 to the attention-sized layer at 160- and 192-token pair
+// tiles, a round takes about 4.1 us + 0.0125 us per token of the tile, i.e.
+// a fixed cost worth about 330 tokens. Counting it picks 192-token tiles there
+// (67.5 -> 65.4 us; 16384 tokens, 12288 -> 4096: 124.9 -> 116.6 us). The
+// dx'-product, same shape but a heavier epilogue, measured faster at 160.
+constexpr int kWideTileCost = 330;
 GemmPlan plan_gemm_plane(int M, int N, int sms);  // plane tiles
 
 cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
