@@ -286,7 +286,7 @@ namespace blr {
 // (160 or 192: MMAs of N >= 160 run at full rate) that needs the fewest
 // token-rounds of the persistent grid; otherwise single CTAs with 128-token
 // tiles, for more tiles in flight on small problems.
-GemmPlan plan_gemm(int M, int N, int sms, bool allow64, int tile_cost) {
+GemmPlan plan_gemm(int M, int N, int sms, int min_bt, int tile_cost) {
     const int pairs = sms / 2;
     const long long fp = (N + 255) / 256;
     GemmPlan best{false, 0, 0, 0};
@@ -303,18 +303,18 @@ GemmPlan plan_gemm(int M, int N, int sms, bool allow64, int tile_cost) {
         }
     }
     if (best.bt != 0) return best;
-    const long long t_tiles = (M + 127) / 128;
-    const long long tiles = t_tiles * ((N + 127) / 128);
-    // few tiles: 64-token tiles put twice as many SMs to work (a tile's time is
-    // set by its k-loop's latency at these sizes, not by its MMA time);
-    // BLR_GEMM_BT=128 keeps 128-token tiles
+    // few tiles: halving the token tile (down to min_bt) while the tiles fill
+    // at most half the SMs puts more SMs to work (a tile's time is set by its
+    // k-loop's latency at these sizes, not by its MMA time); BLR_GEMM_BT=128
+    // keeps 128-token tiles
     const char *v = std::getenv("BLR_GEMM_BT");
-    if (allow64 && 2 * tiles <= sms && M > 64 && !(v && std::strcmp(v, "128") == 0)) {
-        const long long t64 = (M + 63) / 64;
-        const long long tiles64 = t64 * ((N + 127) / 128);
-        return GemmPlan{false, 64, (int)(tiles64 < sms ? tiles64 : sms), (int)t64};
-    }
-    return GemmPlan{false, 128, (int)(tiles < sms ? tiles : sms), (int)t_tiles};
+    if (v && std::strcmp(v, "128") == 0) min_bt = 128;
+    const long long fs = (N + 127) / 128;
+    int bt = 128;
+    while (bt > min_bt && 2 * ((M + bt - 1) / bt) * fs <= sms && M > bt / 2) bt /= 2;
+    const long long t_tiles = (M + bt - 1) / bt;
+    const long long tiles = t_tiles * fs;
+    return GemmPlan{false, bt, (int)(tiles < sms ? tiles : sms), (int)t_tiles};
 }
 
 // Plane-mode tiles: CTA pairs of 256 features x 256 tokens (each CTA loads
@@ -486,8 +486,8 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     uint16_t *plane_v = reinterpret_cast<uint16_t *>(w + L.plane_v);
     // the TMEM-expansion tiles decide what counts as a small problem (fused path)
     const bool fused = !plan_gemm(M, r, sms).pair && !plan_gemm(M, d_out, sms).pair && fused_small_enabled();
-    const GemmPlan q1 = plan_gemm(M, r, sms, !fused);
-    const GemmPlan q2 = plan_gemm(M, d_out, sms, !fused, kWideTileCost);
+    const GemmPlan q1 = plan_gemm(M, r, sms, fused ? 128 : 32);
+    const GemmPlan q2 = plan_gemm(M, d_out, sms, fused ? 128 : 64, kWideTileCost);
     const bool planes = !fused && plane_mode();
     const bool dense2 = !fused && wide_token_major();
     const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : (fused ? q1 : plan_split(q1, M, r, d_in, sms));
@@ -623,8 +623,8 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     uint16_t *plane_v = reinterpret_cast<uint16_t *>(w + L.plane_v);
     const bool fused =
         !plan_gemm(M, r, sms).pair && !plan_gemm(M, d_in, sms).pair && small_bwd_fits(d_out) && fused_small_enabled();
-    const GemmPlan q1 = plan_gemm(M, r, sms, !fused);
-    const GemmPlan q2 = plan_gemm(M, d_in, sms, !fused);
+    const GemmPlan q1 = plan_gemm(M, r, sms, fused ? 128 : 32);
+    const GemmPlan q2 = plan_gemm(M, d_in, sms, fused ? 128 : 64);
     const bool planes = !fused && plane_mode();
     const bool dense2 = !fused && wide_token_major();
     const GemmPlan p1 = planes ? plan_gemm_plane(M, r, sms) : (fused ? q1 : plan_split(q1, M, r, d_out, sms));

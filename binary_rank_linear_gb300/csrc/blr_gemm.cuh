@@ -126,7 +126,7 @@ struct GemmShape {
     static_assert(kNE >= 2, "double-buffered chunk staging");
     static constexpr int kPhaseBytes = kNB * kBBytes + kEpiBytes + kNB * kBitsBytes + kNumBars * 8;
     static constexpr int kSmemBytes = 1024 + kCtlBytes + kPhaseBytes;  // alignment slack, control block, phase
-    static_assert(BT % 32 == 0 && BT >= 64 && BT <= 256 && (!PAIR || BT % 16 == 0), "token tile");
+    static_assert(BT % 32 == 0 && BT >= 32 && BT <= 256 && (!PAIR || BT % 16 == 0), "token tile");
     static_assert(kTokRows % 8 == 0, "activation boxes hold whole 8-row swizzle groups");
     static_assert(PLANE || kNS >= 2, "at least two sign stages");
     static_assert(kNB >= 2, "at least two operand stages");
@@ -878,6 +878,9 @@ cudaError_t launch_gemm_epi(const GemmPlan &plan, const GemmMaps &maps, const Ge
     if (plan.pair && plan.bt == 160) return launch_gemm_t<EPI, true, 160>(maps, args, plan.grid, s);
     if (!plan.pair && plan.bt == 128) return launch_gemm_t<EPI, false, 128>(maps, args, plan.grid, s);
     if (!plan.pair && plan.bt == 64) return launch_gemm_t<EPI, false, 64>(maps, args, plan.grid, s);
+    if constexpr (EPI == kEpiFwd1 || EPI == kEpiBwd1) {
+        if (!plan.pair && plan.bt == 32) return launch_gemm_t<EPI, false, 32>(maps, args, plan.grid, s);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -160,10 +160,11 @@ struct GemmPlan {
     int split;
 };
 
-// TMEM-expansion tiles; allow64: 64-token single-CTA tiles when 128-token
-// tiles would fill at most half the SMs (the fused small-M kernels take 128)
-// tile_cost: a tile's fixed cost in token units (CTA-pair tile choice)
-GemmPlan plan_gemm(int M, int N, int sms, bool allow64 = true, int tile_cost = 0);
+// TMEM-expansion tiles. Single-CTA token tiles are halved from 128 down to
+// min_bt (64 or 32; the fused small-M kernels take 128) while the tiles would
+// fill at most half the SMs. tile_cost: a tile's fixed cost in token units
+// (CTA-pair tile choice).
+GemmPlan plan_gemm(int M, int N, int sms, int min_bt = 64, int tile_cost = 0);
 // The c-product (K = r, output d_out wide) has a large fixed cost per tile:
 // fitted on GB300 to the attention-sized layer at 160- and 192-token pair
 // tiles, a round takes about 4.1 us + 0.0125 us per token of the tile, i.e.

@@ -142,8 +142,8 @@ extern "C" int blr_forward_noalloc(const float *x, const uint32_t *bits_u, const
     uint16_t *c16 = reinterpret_cast<uint16_t *>(take(m * d_out * 2));
 
     // the same tile plans as blr_forward
-    const GemmPlan p1 = plan_gemm(M, r, sms);
-    const GemmPlan p2 = plan_gemm(M, d_out, sms, true, kWideTileCost);
+    const GemmPlan p1 = plan_gemm(M, r, sms, 32);
+    const GemmPlan p2 = plan_gemm(M, d_out, sms, 64, kWideTileCost);
     GemmMaps m1{}, m2{};
     const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
     if (!na_tmap(&m1.act, x16, M, d_in, 64, p1.pair ? p1.bt / 2 : p1.bt, true, CU_TENSOR_MAP_SWIZZLE_128B) ||

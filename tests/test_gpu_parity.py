@@ -368,7 +368,7 @@ def test_x_staging_forms(monkeypatch, form, name, M, d_in, d_out, r):
 @pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("small", 2048, 1024, 1024, 256)])
 def test_128_token_single_tiles(monkeypatch, name, M, d_in, d_out, r):
     """Few-tile products on 128-token single-CTA tiles (BLR_GEMM_BT=128; by
-    default they take 64-token tiles) against the oracle."""
+    default they take 64- or 32-token tiles) against the oracle."""
     monkeypatch.setenv("BLR_GEMM_BT", "128")
     t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     out = _run(t)
