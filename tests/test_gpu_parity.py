@@ -373,3 +373,12 @@ def test_128_token_single_tiles(monkeypatch, name, M, d_in, d_out, r):
     t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     out = _run(t)
     _check_against_oracle(t, out, "(BLR_GEMM_BT=128)")
+
+
+@pytest.mark.parametrize("M,d_in,d_out,r", [(33, 65536, 32768, 64), (40, 64, 64, 65536)])
+def test_maximum_widths(M, d_in, d_out, r):
+    """The widest shapes the shape rule admits (d_in and r up to 65536, d_out up
+    to 32768) with ragged token counts, against the oracle in full."""
+    t = wl.make_inputs(wl.WORKLOADS["small"].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    out = _run(t)
+    _check_against_oracle(t, out, "(maximum widths)")
