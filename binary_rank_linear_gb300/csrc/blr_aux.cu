@@ -143,42 +143,61 @@ int stage_dy_blocks(int M, int d_out) {
 }
 
 // ============================================================== reduce =====
-// out[f] += sum_p part[p][f]. A block of 32 warps owns 32 consecutive columns
-// of one segment; warp w sums rows w, w+32, ... (a few rows each, their loads
-// issued together: about one memory round trip for the row counts of the
-// layer's partials) and the 32 warp sums are added in warp order, so the
-// result does not depend on scheduling.
+// out[f] += sum_p part[p][f]. A block of 32 warps owns 128 consecutive columns
+// of one segment (a float4 per lane); warp w sums rows w, w+32, ... (their
+// loads issued together: about one memory round trip for the row counts of
+// the layer's partials) and the 32 warp sums are added in warp order, so the
+// result does not depend on scheduling. Segment widths are multiples of 32.
 constexpr int kReduceWarps = 32;
+constexpr int kReduceCols = 128;
 
 __global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(ReduceSeg a, ReduceSeg b, ReduceSeg c) {
-    __shared__ float red[kReduceWarps][33];
+    __shared__ float4 red[kReduceWarps][32];
     pdl_wait();
     pdl_launch_dependents();
-    const int nba = (a.n + 31) / 32, nbb = (b.n + 31) / 32;
+    const int nba = (a.n + kReduceCols - 1) / kReduceCols, nbb = (b.n + kReduceCols - 1) / kReduceCols;
     const float *part;
     float *out;
     int rows, n, col0;
     if ((int)blockIdx.x < nba) {
-        part = a.part, out = a.out, rows = a.rows, n = a.n, col0 = blockIdx.x * 32;
+        part = a.part, out = a.out, rows = a.rows, n = a.n, col0 = blockIdx.x * kReduceCols;
     } else if ((int)blockIdx.x < nba + nbb) {
-        part = b.part, out = b.out, rows = b.rows, n = b.n, col0 = (blockIdx.x - nba) * 32;
+        part = b.part, out = b.out, rows = b.rows, n = b.n, col0 = (blockIdx.x - nba) * kReduceCols;
     } else {
-        part = c.part, out = c.out, rows = c.rows, n = c.n, col0 = (blockIdx.x - nba - nbb) * 32;
+        part = c.part, out = c.out, rows = c.rows, n = c.n, col0 = (blockIdx.x - nba - nbb) * kReduceCols;
     }
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int col = col0 + lane;
-    float acc = 0.0f;
+    const int col = col0 + 4 * lane;  // n is a multiple of 32: a lane's float4 is wholly in or out
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (col < n) {
 #pragma unroll 8
-        for (int p = w; p < rows; p += kReduceWarps) acc += __ldcs(part + (long long)p * n + col);
+        for (int p = w; p < rows; p += kReduceWarps) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(part + (long long)p * n + col));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
     }
     red[w][lane] = acc;
     __syncthreads();
     if (w == 0 && col < n) {
-        float t = red[0][lane];
+        float4 t = red[0][lane];
 #pragma unroll
-        for (int i = 1; i < kReduceWarps; ++i) t += red[i][lane];
-        out[col] += t;
+        for (int i = 1; i < kReduceWarps; ++i) {
+            const float4 o = red[i][lane];
+            t.x += o.x;
+            t.y += o.y;
+            t.z += o.z;
+            t.w += o.w;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(out + col);
+        float4 d = *dst;
+        d.x += t.x;
+        d.y += t.y;
+        d.z += t.z;
+        d.w += t.w;
+        *dst = d;
     }
 }
 
@@ -429,7 +448,8 @@ cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, 
 }
 
 cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaStream_t s) {
-    const int blocks = (a.n + 31) / 32 + (b.n + 31) / 32 + (c.n + 31) / 32;
+    const int blocks = (a.n + kReduceCols - 1) / kReduceCols + (b.n + kReduceCols - 1) / kReduceCols +
+                       (c.n + kReduceCols - 1) / kReduceCols;
     static bool prepared = false;
     if (!prepared) {
         cudaError_t e = prepare_kernel(reduce_partials_kernel, 0);
