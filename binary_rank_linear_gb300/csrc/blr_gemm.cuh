@@ -537,13 +537,17 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             tok = (tile / f_tiles) * BT + 32 * (cb + kSplit * (g - lt * nc));
             return true;
         };
+        // L2 policy of the streams this epilogue reads or writes once (the
+        // a-tape, x, y, dx, c); the f16 operands of the next product (a.l,
+        // db.l) keep the default so that its CTAs find them in L2
+        const uint64_t once = l2_policy_evict_first();
         auto load_chunk = [&](int g) {  // lane 0
             int fq, tok;
             if (!chunk_at(g, fq, tok)) return;
             const int sl = g % kNE;
             const uint32_t par = (uint32_t)(g / kNE) & 1u;
             mbar_arrive_expect_tx(&ebar[sl], S::kSlot32);
-            tma_load_2d(slots + sl * S::kSlotBytes, &tmap_in, &ebar[sl], fq, tok);
+            tma_load_2d_hint(slots + sl * S::kSlotBytes, &tmap_in, &ebar[sl], fq, tok, once);
             pending |= 1u << sl;
             ppar = (ppar & ~(1u << sl)) | (par << sl);
         };
@@ -724,11 +728,16 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                 if (lane == 0 && tc < M && fq < N) {
                     if constexpr (S::kHas32) {
                         if (add_out)
-                            tma_reduce_add_2d(&tmap_out32, s32, fq, tc);  // y or dx += the chunk
+                            tma_reduce_add_2d_hint(&tmap_out32, s32, fq, tc, once);  // y or dx += the chunk
                         else
-                            tma_store_2d(&tmap_out32, s32, fq, tc);
+                            tma_store_2d_hint(&tmap_out32, s32, fq, tc, once);
                     }
-                    if constexpr (S::kHas16) tma_store_2d(&tmap_out16, s16, fq, tc);
+                    if constexpr (S::kHas16) {
+                        if (EPI == kEpiFwd2)
+                            tma_store_2d_hint(&tmap_out16, s16, fq, tc, once);  // c, read again by the backward only
+                        else
+                            tma_store_2d(&tmap_out16, s16, fq, tc);  // a.l or db.l: the next product's operand
+                    }
                 }
                 if (lane == 0) bulk_commit_group();
                 ++g;
