@@ -92,6 +92,26 @@ __device__ inline void prep_run(const SignPrep &p, int block, int threads) {
     }
 }
 
+// Re-layout work interleaved with a streaming kernel's consumers: a cursor
+// over this block's share of the virtual prep blocks (each `threads` wide,
+// threads = the consumer count), which a consumer warp advances by doing its
+// own part of one virtual block (its 32 threads; kind 1 is a warp-wide
+// transpose). Warps advance independently; every part is done once.
+struct PrepCursor {
+    int v, b0, b1, nblocks, threads;
+    __device__ PrepCursor(const SignPrep &p0, const SignPrep &p1, int block, int nblocks_, int threads_, bool on)
+        : v(block), b0(on ? prep_blocks(p0, threads_) : 0), b1(on ? prep_blocks(p1, threads_) : 0),
+          nblocks(nblocks_), threads(threads_) {}
+    __device__ bool done() const { return v >= b0 + b1; }
+    __device__ void step(const SignPrep &p0, const SignPrep &p1) {
+        if (v < b0)
+            prep_run(p0, v, threads);
+        else
+            prep_run(p1, v - b0, threads);
+        v += nblocks;
+    }
+};
+
 // ============================================================ stage x ======
 // train_mm.rs, `cvt_col` staging: x16 = f16(x . g), forward unscaled.
 // A thread walks float4 groups (row-major [M][d_in/4]) with a grid stride,
@@ -235,8 +255,8 @@ __host__ __device__ inline size_t sxs_smem_bytes(int d_in) {
     return (size_t)kSxsHeadBytes + (size_t)p.nst * p.rs * d_in * 4;
 }
 
-// The block first does its share (1 of prep_nblocks) of the two bitmap
-// re-layouts, while the producer's first copies are in flight.
+// The block does its share (1 of prep_nblocks) of the two bitmap re-layouts
+// while its consumers wait for data.
 template <int KQ>
 __device__ void stage_x_stream(const float *__restrict__ x, const float *__restrict__ g, uint16_t *__restrict__ x16,
                                int M, int d_in, int block, int nblocks, unsigned char *smem, uint32_t *status,
@@ -278,7 +298,6 @@ __device__ void stage_x_stream(const float *__restrict__ x, const float *__restr
         for (int i = 0; i < nbatch && i < pl.nst; ++i) issue(i);
     }
     __syncwarp();
-    if (prep_nblocks > 0) prep_share(p0, p1, block, prep_nblocks);
     if (warp == kSxsWarps) {
         if (lane != 0) return;
         for (int i = issued; i < nbatch; ++i) {
@@ -309,9 +328,13 @@ __device__ void stage_x_stream(const float *__restrict__ x, const float *__restr
         gv[k] = active && col < G ? __ldg(reinterpret_cast<const float4 *>(g) + col) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     uint2 *o = reinterpret_cast<uint2 *>(x16);
+    // the block's share of the re-layouts fills the consumers' waits for data
+    PrepCursor prep(p0, p1, block, prep_nblocks, kSxsWarps * 32, prep_nblocks > 0);
     for (int i = 0; i < nbatch; ++i) {
         const int st = i % pl.nst;
-        if (!mbar_wait(&full[st], (uint32_t)((i / pl.nst) & 1), abort_flag)) {
+        const uint32_t par = (uint32_t)((i / pl.nst) & 1);
+        while (!prep.done() && !__shfl_sync(0xFFFFFFFFu, (int)mbar_test_wait(&full[st], par), 0)) prep.step(p0, p1);
+        if (!mbar_wait(&full[st], par, abort_flag)) {
             if (!*abort_flag) {
                 *abort_flag = 1;
                 atomicOr(status, kStTimeoutStage);
@@ -339,6 +362,7 @@ __device__ void stage_x_stream(const float *__restrict__ x, const float *__restr
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
     }
+    while (!prep.done()) prep.step(p0, p1);
 }
 
 // =========================================================== stage dy ======
@@ -598,7 +622,9 @@ __host__ __device__ inline size_t sd_smem_bytes(int d_out) {
 }
 
 // The block first does its share (1 of prep_nblocks) of the two bitmap
-// re-layouts, while the producer's first copies are in flight.
+// re-layouts, while the producer's first copies are in flight (interleaving
+// it with the consumers' waits, as the x staging does, measured slower here:
+// the consumers' registers are short).
 template <int Q>
 __device__ void stage_dy_stream(const StageDyArgs &a, int block, int nblocks, unsigned char *smem,
                                 const SignPrep &p0, const SignPrep &p1, int prep_nblocks) {
