@@ -185,6 +185,13 @@ def job_tokens_per_s(world: int, tokens_per_rank_step: int, steps: int, ms: floa
     return world * tokens_per_rank_step * steps / (ms * 1e-3)
 
 
+def workload_of(args):
+    """The named workload, at --tokens tokens when given."""
+    from binary_rank_linear_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    return w.with_shape(M=args.tokens) if args.tokens else w
+
+
 # ---------------------------------------------------------- CPU oracle ------
 def cpu_oracle_rate(w, budget_s: float = 12.0, max_reps: int = 1_000_000):
     """tokens/s of the CPU f64 oracle (as it stands) on the workload's batch,
@@ -228,7 +235,7 @@ def run_gpu(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = wl.WORKLOADS[args.workload]
+    w = workload_of(args)
     M, d_in, d_out, r = w.M, w.d_in, w.d_out, w.r
     t = wl.make_inputs(w)
 
@@ -344,7 +351,8 @@ def run_gpu(args, rank, world, local_rank):
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json: bf16 burst, f16 assumed equal)" \
         if peak_src == "measured" else "fallback"
-    roof["traffic"] = stored_traffic(args.workload, dom)
+    # stored counters are for the workloads' own token counts
+    roof["traffic"] = stored_traffic(args.workload, dom) if not args.tokens else None
 
     sign = measure_sign_grads(blr, sets, g, l, args.steps, tc_peak, M, d_in, d_out, r, dev) \
         if not args.no_sign else None
@@ -398,7 +406,7 @@ def run_gpu(args, rank, world, local_rank):
         "dtype": "f16",
         "data": "synthetic",
         "config": {
-            "workload": f"{w.name}: {w.note}",
+            "workload": f"{w.name}: {w.note}" + (f" (token count set to {M})" if args.tokens else ""),
             "M": M, "d_in": d_in, "d_out": d_out, "r": r,
             "mode": "overwrite y/dx, dynamic per-token gradient scale",
             "small_path": args.small_path,
@@ -574,6 +582,9 @@ def main():
     ap.add_argument("--no-sign", action="store_true", help="skip the sign-gradient measurement")
     ap.add_argument("--no-plane", action="store_true", help="skip the plane_linear measurement")
     ap.add_argument("--no-paths", action="store_true", help="skip the two-path layer measurement")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload's shapes and distributions at this token count (a smaller case to "
+                         "profile); the bench line then is not the workload's")
     ap.add_argument("--small-path", default="general", choices=["general", "fused"],
                     help="kernels for small problems: stand-alone (default) or the fused cooperative pair")
     args = ap.parse_args()
@@ -587,7 +598,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     from binary_rank_linear_gb300 import workloads as wl
 
-    w = wl.WORKLOADS[args.workload]
+    w = workload_of(args)
 
     if args.impl == "reference":
         if rank != 0:
