@@ -269,7 +269,15 @@ BLR_API int blr_adam(float *w, const float *grad, float *m1, float *m2, const fl
  * Returns BLR_OK if no kernel recorded a failure since the last blr_forward
  * on this workspace, BLR_ERR_DEVICE_CHECK if one did (the code is written to
  * *device_code when it is not NULL), BLR_ERR_CUDA if the stream reports an
- * error. This call blocks; it is meant for tests and diagnostics. */
+ * error. This call blocks; it is meant for tests and diagnostics.
+ * Bits of the device code (each names the wait that ran out):
+ *   0x01 a product's operand loader (a ring slot never freed),
+ *   0x02 a sign expander, 0x04 an MMA issuer, 0x08 an epilogue,
+ *   0x10 the drain of copies or MMAs at a kernel's end,
+ *   0x20 a launch geometry the kernel does not accept,
+ *   0x40 a grid barrier of the fused small-problem kernels,
+ *   0x80 a streaming staging kernel (a row batch never arrived or its ring
+ *        slot never freed). */
 BLR_API int blr_check_status(const void *ws, size_t ws_bytes, blr_stream_t stream, uint32_t *device_code);
 
 /* Static description of a status code. Never NULL. */
