@@ -360,36 +360,92 @@ def run_gpu(args, rank, world, local_rank):
     plane = measure_plane(blr, sets[0], args.steps, tc_peak, M, d_in, d_out, dev) if not args.no_plane else None
     paths = measure_paths(blr, sets[0], bu, bv, g, l, h, args.steps, tc_peak, w, dev) if not args.no_paths else None
 
-    # end-to-end: host buffers through the public API, copies inside the timed region
+    # end-to-end: host buffers through the public API, copies inside the timed
+    # region. With a megabyte or more to move per step, steps are pipelined over
+    # two device buffer sets on three streams (host->device copies, the layer,
+    # device->host copies), as a training loop's data path would be: step i+1's
+    # inputs go up and step i-1's results come down while step i computes.
+    # Smaller steps run in order on one stream (there the host's launch work,
+    # not the copies, sets the pace, and the extra streams only add to it).
+    # Every step moves its own inputs and results either way.
     xh = torch.from_numpy(t["x"]).pin_memory()
     dyh = torch.from_numpy(t["dy"]).pin_memory()
-    yh = torch.empty(M, d_out).pin_memory()
-    dxh = torch.empty(M, d_in).pin_memory()
-    gh = torch.empty(d_in + r + d_out).pin_memory()
-    s0 = sets[0]
+    pipelined = 4 * M * (d_in + d_out) >= (1 << 20)
+    npipe = 2
+    pipe = []
+    for b in range(npipe):
+        pipe.append({
+            "set": sets[b % len(sets)],
+            "yh": torch.empty(M, d_out).pin_memory(),
+            "dxh": torch.empty(M, d_in).pin_memory(),
+            "gh": torch.empty(d_in + r + d_out).pin_memory(),
+            "dg": torch.zeros(d_in, device=dev), "dl": torch.zeros(r, device=dev), "dh": torch.zeros(d_out, device=dev),
+            "up": torch.cuda.Event(), "done": torch.cuda.Event(), "down": torch.cuda.Event(),
+        })
+    if pipelined:
+        s_up, s_comp, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    else:
+        s_up = s_comp = s_down = torch.cuda.current_stream(dev)
+    for b in pipe:
+        b["down"].record(s_down)  # nothing to wait for yet
 
-    def e2e_step():
+    def e2e_step_in_order(i):
+        b = pipe[0]
+        s0 = b["set"]
         s0["x"].copy_(xh, non_blocking=True)
         s0["dy"].copy_(dyh, non_blocking=True)
         blr.forward(s0["x"], bu, bv, g, l, h, s0["y"], s0["ws"])
-        blr.backward(s0["x"], s0["dy"], bu, bv, g, l, h, s0["dx"], dg, dl, dh, s0["ws"])
-        yh.copy_(s0["y"], non_blocking=True)
-        dxh.copy_(s0["dx"], non_blocking=True)
-        gh[:d_in].copy_(dg, non_blocking=True)
-        gh[d_in:d_in + r].copy_(dl, non_blocking=True)
-        gh[d_in + r:].copy_(dh, non_blocking=True)
+        blr.backward(s0["x"], s0["dy"], bu, bv, g, l, h, s0["dx"], b["dg"], b["dl"], b["dh"], s0["ws"])
+        b["yh"].copy_(s0["y"], non_blocking=True)
+        b["dxh"].copy_(s0["dx"], non_blocking=True)
+        b["gh"][:d_in].copy_(b["dg"], non_blocking=True)
+        b["gh"][d_in:d_in + r].copy_(b["dl"], non_blocking=True)
+        b["gh"][d_in + r:].copy_(b["dh"], non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    def e2e_step(i):
+        if not pipelined:
+            e2e_step_in_order(i)
+            return
+        b = pipe[i % npipe]
+        s0 = b["set"]
+        # the set's previous results are down (its y/dx and inputs are free again)
+        s_up.wait_event(b["down"])
+        with torch.cuda.stream(s_up):
+            s0["x"].copy_(xh, non_blocking=True)
+            s0["dy"].copy_(dyh, non_blocking=True)
+        b["up"].record(s_up)
+        s_comp.wait_event(b["up"])
+        with torch.cuda.stream(s_comp):
+            blr.forward(s0["x"], bu, bv, g, l, h, s0["y"], s0["ws"])
+            blr.backward(s0["x"], s0["dy"], bu, bv, g, l, h, s0["dx"], b["dg"], b["dl"], b["dh"], s0["ws"])
+        b["done"].record(s_comp)
+        s_down.wait_event(b["done"])
+        with torch.cuda.stream(s_down):
+            b["yh"].copy_(s0["y"], non_blocking=True)
+            b["dxh"].copy_(s0["dx"], non_blocking=True)
+            b["gh"][:d_in].copy_(b["dg"], non_blocking=True)
+            b["gh"][d_in:d_in + r].copy_(b["dl"], non_blocking=True)
+            b["gh"][d_in + r:].copy_(b["dh"], non_blocking=True)
+        b["down"].record(s_down)
+
+    for i in range(max(npipe, args.warmup)):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
     barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    f1.record(stream)
+    f0.record(s_up)
+    for i in range(args.steps):
+        e2e_step(i)
+    s_up.wait_stream(s_down)
+    f1.record(s_up)
+    torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = f0.elapsed_time(f1)
     e2e_ms = max_over_ranks(e2e_ms, dev)
+    for b in pipe:
+        st = blr.check_status(b["set"]["ws"])
+        if st:
+            raise RuntimeError(f"end-to-end pass: device status {st:#x}")
 
     value = job_tokens_per_s(world, M, args.steps, ms)
     result = {
@@ -421,7 +477,8 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": {"value": job_tokens_per_s(world, M, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": 4 * M * (d_in + d_out),
-                "d2h_bytes_per_step": 4 * (M * (d_in + d_out) + d_in + r + d_out)},
+                "d2h_bytes_per_step": 4 * (M * (d_in + d_out) + d_in + r + d_out),
+                "copies": "overlapped with the layer on their own streams" if pipelined else "in order on one stream"},
     }
     if sign is not None:
         result["sign_grads"] = sign
