@@ -109,14 +109,14 @@ __global__ void __launch_bounds__(kSxsThreads, 1)
                        extra > 0 ? 0 : stage_blocks);
 }
 
-template <int GPT>
-__global__ void __launch_bounds__(kStageThreads, (GPT <= 8 ? 2 : 1))
+template <int GPT, int THREADS>
+__global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
     bwd_prologue_kernel(SignPrep p0, SignPrep p1, StageDyArgs a, int stage_blocks) {
     extern __shared__ __align__(16) float smem_f[];
     pdl_wait();
     pdl_launch_dependents();
     if (prologue_prep(p0, p1, stage_blocks)) return;
-    stage_dy_run<GPT>(a, blockIdx.x, stage_blocks, smem_f, stage_tpr(a.d_out), kStageThreads);
+    stage_dy_run<GPT>(a, blockIdx.x, stage_blocks, smem_f, stage_tpr(a.d_out, THREADS), THREADS);
 }
 
 // Streaming form of the same prologue (rows up to kSdMaxCols wide): one block
@@ -344,14 +344,14 @@ cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const 
     return e;
 }
 
-template <int GPT>
+template <int GPT, int THREADS = kStageThreads>
 static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
-    const int tpr = stage_tpr(a.d_out);
-    const int rb_n = kStageThreads / tpr;
+    const int tpr = stage_tpr(a.d_out, THREADS);
+    const int rb_n = THREADS / tpr;
     const size_t smem = stage_dy_smem_bytes(a.d_out, tpr, rb_n * tpr);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = prepare_kernel(bwd_prologue_kernel<GPT>, 200 * 1024);
+        cudaError_t e = prepare_kernel(bwd_prologue_kernel<GPT, THREADS>, 200 * 1024);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -364,7 +364,7 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&cached_sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_prologue_kernel<GPT>, kStageThreads, smem);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_prologue_kernel<GPT, THREADS>, THREADS, smem);
         if (per_sm < 1) per_sm = 1;
         for (int i = 0; i < 8; ++i)
             if (cached_smem[i] == 0) {
@@ -377,10 +377,10 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
     int sb = stage_dy_blocks(a.M, a.d_out);
     if (sb > per_sm * sms) sb = per_sm * sms;
     // re-layout-only blocks where the wave has room for them
-    const int pb = prep_blocks(p0, kStageThreads) + prep_blocks(p1, kStageThreads);
+    const int pb = prep_blocks(p0, THREADS) + prep_blocks(p1, THREADS);
     const int grid = sb + pb <= per_sm * sms ? sb + pb : sb;
     trace_before("bwd_prologue", s);
-    cudaError_t e = launch_k(bwd_prologue_kernel<GPT>, dim3(grid), dim3(kStageThreads), smem, s, p0, p1, a, sb);
+    cudaError_t e = launch_k(bwd_prologue_kernel<GPT, THREADS>, dim3(grid), dim3(THREADS), smem, s, p0, p1, a, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;
@@ -443,7 +443,10 @@ cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, 
         case 8: return launch_bwd_prologue_t<8>(p0, p1, a, s);
         default: break;
     }
-    if (stage_gpt(a.d_out) <= 16) return launch_bwd_prologue_t<16>(p0, p1, a, s);
+    // rows wider than 16384: 1024-thread blocks, 8 groups per thread (measured
+    // on GB300, 4000 rows of 32768: 271 -> 228 us against 512 threads with 16;
+    // at 12288 the 512-thread blocks stay faster, 293 against 310 us)
+    if (stage_gpt(a.d_out, 1024) <= 8) return launch_bwd_prologue_t<8, 1024>(p0, p1, a, s);
     return cudaErrorInvalidValue;
 }
 

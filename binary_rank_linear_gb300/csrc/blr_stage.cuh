@@ -390,15 +390,15 @@ constexpr int kStageThreads = 512;
 constexpr int kStageRedFloats = 2 * 32 * 2;
 constexpr int kStageMaxBlocks = 2 * 160;  // partial rows reserved per call
 
-__host__ __device__ inline int stage_tpr(int d_out) {
+__host__ __device__ inline int stage_tpr(int d_out, int cap = kStageThreads) {
     const int G = d_out / 4;  // float4 groups per row
     int t = 32;
-    while (t * 8 < G && t < kStageThreads) t *= 2;  // at most 8 groups per thread when possible
+    while (t * 8 < G && t < cap) t *= 2;  // at most 8 groups per thread when possible
     return t;
 }
 
-__host__ __device__ inline int stage_gpt(int d_out) {
-    const int tpr = stage_tpr(d_out);
+__host__ __device__ inline int stage_gpt(int d_out, int cap = kStageThreads) {
+    const int tpr = stage_tpr(d_out, cap);
     return (d_out / 4 + tpr - 1) / tpr;
 }
 
