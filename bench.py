@@ -77,36 +77,43 @@ def _peaks():
 
 # ------------------------------------------------------- per-kernel work ----
 def kernel_work(name: str, M: int, d_in: int, d_out: int, r: int):
-    """Algorithmic (flops, bytes) of one launch of a kernel of the step.
+    """(flops, algorithmic bytes, staging bytes) of one launch of a kernel of the step.
 
-    Bytes count each tensor the kernel must read or write once (f32 = 4 B,
-    staged f16 = 2 B, bitmaps d*r/8 B); FLOP counts 2 per multiply-add of the
-    sign products.
+    Algorithmic bytes are the tensors the layer itself must move, attributed to
+    the kernel that moves them: x (read by the forward and again by the
+    dg sums), y, dy, dx, the f32 a tape (written, read), the f16 c tape
+    (written, read) and the bitmaps (read once per pass). The staged f16
+    operands (x16, dy16, a.l, db.l), the re-laid bitmaps and the partial-sum
+    rows are this design's own round trips: they are counted separately as
+    staging bytes and never as achieved work. FLOP counts 2 per multiply-add of
+    the four sign products.
     """
-    bits_u = d_out * r / 8
-    bits_v = d_in * r / 8
-    if name == "fwd_prologue":
-        return 0.0, 4.0 * M * d_in + 2.0 * M * d_in + 2 * (bits_u + bits_v)
-    if name == "gemm_fwd1":
-        return 2.0 * M * r * d_in, 2.0 * M * d_in + bits_v + 4.0 * M * r + 2.0 * M * r
-    if name == "gemm_fwd2":
-        return 2.0 * M * r * d_out, 2.0 * M * r + bits_u + 4.0 * M * d_out + 2.0 * M * d_out
-    if name == "bwd_prologue":
-        return 0.0, 4.0 * M * d_out + 2.0 * M * d_out + 2.0 * M * d_out + 2 * (bits_u + bits_v)
-    if name == "gemm_bwd1":
-        return 2.0 * M * r * d_out, 2.0 * M * d_out + bits_u + 4.0 * M * r + 2.0 * M * r
-    if name == "gemm_bwd2":
-        return 2.0 * M * r * d_in, 2.0 * M * r + bits_v + 4.0 * M * d_in + 4.0 * M * d_in
-    if name == "reduce_partials":
-        return 0.0, 4.0 * (d_in + d_out + r) * 2
-    if name == "small_fwd":  # fused forward of the small-M path
-        parts = [kernel_work(n, M, d_in, d_out, r) for n in ("fwd_prologue", "gemm_fwd1", "gemm_fwd2")]
-        return sum(p[0] for p in parts), 4.0 * M * d_in + 4.0 * M * r + 2.0 * M * r + 6.0 * M * d_out + bits_u + bits_v
-    if name == "small_bwd":  # fused backward of the small-M path
-        parts = [kernel_work(n, M, d_in, d_out, r) for n in ("gemm_bwd1", "gemm_bwd2")]
-        return (sum(p[0] for p in parts),
-                4.0 * M * d_out + 2.0 * M * d_out + 4.0 * M * r + 2.0 * M * r + 8.0 * M * d_in + bits_u + bits_v)
-    return 0.0, 0.0
+    words = (r + 31) // 32
+    bits_u, bits_v = 4.0 * d_out * words, 4.0 * d_in * words
+    relaid_u, relaid_v = 8.0 * sign_rows(d_out) * 2 * ((r + 127) // 128), 8.0 * sign_rows(r) * 2 * ((d_in + 127) // 128)
+    relaid_ut = 8.0 * sign_rows(r) * 2 * ((d_out + 127) // 128)
+    relaid_vd = 8.0 * sign_rows(d_in) * 2 * ((r + 127) // 128)
+    parts = 4.0 * ((M + 127) // 128) * (d_in + d_out + r)  # partial rows, about one per 128 tokens
+    table = {
+        "fwd_prologue": (0.0, 4.0 * M * d_in + bits_u + bits_v, 2.0 * M * d_in + relaid_u + relaid_v),
+        "gemm_fwd1": (2.0 * M * r * d_in, 4.0 * M * r, 2.0 * M * d_in + 2.0 * M * r + relaid_v),
+        "gemm_fwd2": (2.0 * M * r * d_out, 6.0 * M * d_out, 2.0 * M * r + relaid_u),
+        "bwd_prologue": (0.0, 6.0 * M * d_out + bits_u + bits_v, 2.0 * M * d_out + relaid_ut + relaid_vd),
+        "gemm_bwd1": (2.0 * M * r * d_out, 4.0 * M * r, 2.0 * M * d_out + 2.0 * M * r + relaid_ut + parts),
+        "gemm_bwd2": (2.0 * M * r * d_in, 8.0 * M * d_in, 2.0 * M * r + relaid_vd + parts),
+        "reduce_partials": (0.0, 8.0 * (d_in + d_out + r), parts),
+    }
+    if name == "small_fwd":
+        return tuple(sum(table[n][i] for n in ("fwd_prologue", "gemm_fwd1", "gemm_fwd2")) for i in range(3))
+    if name == "small_bwd":
+        return tuple(sum(table[n][i] for n in ("bwd_prologue", "gemm_bwd1", "gemm_bwd2", "reduce_partials"))
+                     for i in range(3))
+    return table.get(name, (0.0, 0.0, 0.0))
+
+
+def sign_rows(n: int) -> int:
+    """Rows of a re-laid bitmap (n rounded up to 256)."""
+    return (n + 255) // 256 * 256
 
 
 # --------------------------------------------------------------- clocks -----
@@ -185,101 +192,138 @@ def job_tokens_per_s(world: int, tokens_per_rank_step: int, steps: int, ms: floa
     return world * tokens_per_rank_step * steps / (ms * 1e-3)
 
 
-def workload_of(args):
-    """The named workload, at --tokens tokens when given."""
+def layers_of(args):
+    """The layers one step of the named workload runs (at --tokens tokens when given)."""
     from binary_rank_linear_gb300 import workloads as wl
-    w = wl.WORKLOADS[args.workload]
-    return w.with_shape(M=args.tokens) if args.tokens else w
+    return wl.step_layers(args.workload, args.tokens)
+
+
+def blas_threads():
+    """Threads numpy's BLAS may use, from the usual environment variables (None: the library default)."""
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            try:
+                return k, int(os.environ[k])
+            except ValueError:
+                pass
+    return None, None
 
 
 # ---------------------------------------------------------- CPU oracle ------
-def cpu_oracle_rate(w, budget_s: float = 12.0, max_reps: int = 1_000_000):
-    """tokens/s of the CPU f64 oracle (as it stands) on the workload's batch,
-    repeated until ``budget_s`` seconds of CPU work have run. For workloads
-    whose batch would exceed the budget, a prefix of the tokens is used."""
+def cpu_oracle_rate(layers, budget_s: float = 12.0, max_reps: int = 1_000_000):
+    """tokens/s of the CPU f64 oracle (as it stands) on the step's layers,
+    repeated until ``budget_s`` seconds of CPU work have run. Workloads whose
+    batch would exceed the budget run a prefix of their tokens (the seeded
+    draws of a prefix are the full batch's first rows)."""
     import oracle
     from binary_rank_linear_gb300 import workloads as wl
 
-    sample_M = w.M
-    # keep one oracle pass in the seconds range: ~4 f64 GEMMs of 2*M*r*d each
-    per_token = 4.0 * w.r * (w.d_in + w.d_out)
+    sample_M = layers[0].M
+    # keep one oracle pass in the seconds range: ~4 f64 GEMMs of 2*M*r*d each per layer
+    per_token = sum(4.0 * w.r * (w.d_in + w.d_out) for w in layers)
     while sample_M > 64 and per_token * sample_M > 3e11:
         sample_M //= 2
-    t = wl.make_inputs(w.with_shape(M=sample_M))
-    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    inputs = []
+    for w in layers:
+        t = wl.make_inputs(w.with_shape(M=sample_M))
+        inputs.append((t, oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])))
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
-        oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+        for t, bu, bv in inputs:
+            oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
+            oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= max_reps:
             break
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", cores)))
+    env, threads = blas_threads()
+    names = "+".join(w.name for w in layers)
     return {
         "value": reps * sample_M / el,
         "unit": "tokens/s",
-        "cores": min(cores, threads),
+        "cores": min(cores, threads) if threads else cores,
         "kind": "oracle",
-        "sample": f"{reps} x (forward+backward of {sample_M} tokens of {w.name}) in {el:.1f} s, numpy f64",
+        "sample": f"{reps} x (forward+backward of the first {sample_M} of {layers[0].M} tokens of {names}) in "
+                  f"{el:.1f} s, numpy f64",
+        "host_cores": cores,
+        "blas_threads": {"env": env, "value": threads} if env else "BLAS default (one per available core)",
     }
 
 
 # ------------------------------------------------------------ GPU arm -------
-def run_gpu(args, rank, world, local_rank):
+class Layer:
+    """One blr layer of the step on the device: seeded inputs, packed signs,
+    rotating buffer sets (x, dy, y, dx, workspace) and gradient vectors."""
+
+    def __init__(self, w, dev, nsets):
+        import torch
+
+        import binary_rank_linear_gb300 as blr
+        from binary_rank_linear_gb300 import workloads as wl
+        self.w, self.dev, self.blr = w, dev, blr
+        t = wl.make_inputs(w)
+        self.host = t
+
+        def d(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+        M, d_in, d_out, r = w.M, w.d_in, w.d_out, w.r
+        self.g, self.l, self.h = d(t["g"]), d(t["l"]), d(t["h"])
+        self.bu, self.bv = blr.pack_signs(d(t["su"])), blr.pack_signs(d(t["sv"]))
+        x0, dy0 = d(t["x"]), d(t["dy"])
+        self.ws_bytes = blr.workspace_bytes(M, d_in, d_out, r)
+        self.sets = []
+        for _ in range(nsets):
+            self.sets.append({
+                "x": x0.clone(), "dy": dy0.clone(),
+                "y": torch.empty(M, d_out, device=dev), "dx": torch.empty(M, d_in, device=dev),
+                "ws": torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev),
+            })
+        del x0, dy0
+        self.dg = torch.zeros(d_in, device=dev)
+        self.dl = torch.zeros(r, device=dev)
+        self.dh = torch.zeros(d_out, device=dev)
+
+    @staticmethod
+    def set_bytes(w, ws_bytes):
+        return 4 * w.M * (2 * w.d_in + 2 * w.d_out) + ws_bytes
+
+    def step(self, i, dg=None, dl=None, dh=None):
+        s = self.sets[i % len(self.sets)]
+        self.blr.forward(s["x"], self.bu, self.bv, self.g, self.l, self.h, s["y"], s["ws"])
+        self.blr.backward(s["x"], s["dy"], self.bu, self.bv, self.g, self.l, self.h, s["dx"],
+                          self.dg if dg is None else dg, self.dl if dl is None else dl,
+                          self.dh if dh is None else dh, s["ws"])
+
+    def check(self, where):
+        for s in self.sets:
+            st = self.blr.check_status(s["ws"])
+            if st:
+                raise RuntimeError(f"{where}: {self.w.name}: device status {st:#x}")
+
+
+def nsets_for(layers_w, blr):
+    """Rotating buffer sets: enough that one round of sets exceeds twice the L2."""
+    total = sum(Layer.set_bytes(w, blr.workspace_bytes(w.M, w.d_in, w.d_out, w.r)) for w in layers_w)
+    return max(2, min(64, -(-2 * L2_BYTES // total) + 1)), total
+
+
+def label(layers, li, name):
+    return name if len(layers) == 1 else f"{layers[li].w.name}/{name}"
+
+
+def time_step(layers, args, dev, clocks=None):
+    """Graph-replayed steps: W warm-up replays, then exactly K timed replays
+    between barriers, CUDA events on the launch stream. Returns (ms, graphs)."""
     import torch
-
-    import binary_rank_linear_gb300 as blr
-    from binary_rank_linear_gb300 import workloads as wl
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = workload_of(args)
-    M, d_in, d_out, r = w.M, w.d_in, w.d_out, w.r
-    t = wl.make_inputs(w)
-
-    def d(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    g, l, h = d(t["g"]), d(t["l"]), d(t["h"])
-    bu, bv = blr.pack_signs(d(t["su"])), blr.pack_signs(d(t["sv"]))
-    x0, dy0 = d(t["x"]), d(t["dy"])
-    ws_bytes = blr.workspace_bytes(M, d_in, d_out, r)
-    set_bytes = 4 * M * (2 * d_in + 2 * d_out) + ws_bytes
-    nsets = max(1, min(64, -(-2 * L2_BYTES // set_bytes) + 1))
-    sets = []
-    for _ in range(nsets):
-        sets.append({
-            "x": x0.clone(), "dy": dy0.clone(),
-            "y": torch.empty(M, d_out, device=dev), "dx": torch.empty(M, d_in, device=dev),
-            "ws": torch.empty(ws_bytes, dtype=torch.uint8, device=dev),
-        })
-    dg = torch.zeros(d_in, device=dev)
-    dl = torch.zeros(r, device=dev)
-    dh = torch.zeros(d_out, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step(i):
-        s = sets[i % nsets]
-        blr.forward(s["x"], bu, bv, g, l, h, s["y"], s["ws"])
-        blr.backward(s["x"], s["dy"], bu, bv, g, l, h, s["dx"], dg, dl, dh, s["ws"])
-
-    dist = world > 1
-    if dist:
-        import torch.distributed as tdist
-
-    def barrier():
-        if dist:
-            tdist.barrier()
-        torch.cuda.synchronize()
-
+    nsets = len(layers[0].sets)
     for i in range(max(args.warmup, nsets)):
-        step(i)
-    status = blr.check_status(sets[0]["ws"])
-    if status:
-        raise RuntimeError(f"device status {status:#x} after warm-up")
-
+        for L in layers:
+            L.step(i)
+    for L in layers:
+        L.check("warm-up")
     # one CUDA graph per buffer set: a step is replayed with no host launch cost
     graphs = []
     cap = torch.cuda.Stream(device=dev)
@@ -288,164 +332,201 @@ def run_gpu(args, rank, world, local_rank):
         for i in range(nsets):
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=cap):
-                step(i)
+                for L in layers:
+                    L.step(i)
             graphs.append(gr)
     stream.wait_stream(cap)
     for i in range(args.warmup):
         graphs[i % nsets].replay()
-
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    time.sleep(0.3)
-    barrier()
+    if clocks is not None:
+        # the sampler runs from here to the end of the timed replays; untimed
+        # replays for about half a second before them keep the GPU at its
+        # loaded clocks, so that the samples describe the timed region
+        clocks.start()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(nsets):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+        per = max(1e-6, (time.perf_counter() - t0) / nsets)
+        for i in range(min(5000, int(0.5 / per))):
+            graphs[i % nsets].replay()
+    barrier(args)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
         graphs[i % nsets].replay()
     e1.record(stream)
-    barrier()
-    ms = e0.elapsed_time(e1)
-    # kernel-level durations: an eager pass of the same steps with the library's
-    # event trace, queued behind a GPU sleep so that host launch gaps do not
-    # land inside any kernel's bracket
-    t0 = time.perf_counter()
-    step(0)
-    host_step_s = time.perf_counter() - t0
-    barrier()
-    blr.trace_begin(capacity=16 * args.steps)
-    torch.cuda._sleep(int(min(4e9, 2.5e9 * host_step_s * (args.steps + 2))))
-    for i in range(args.steps):
-        step(i)
-    barrier()
-    trace = blr.trace_end()
-    clk = clocks.stop()
-    for s in sets:
-        st = blr.check_status(s["ws"])
-        if st:
-            raise RuntimeError(f"device status {st:#x}")
+    barrier(args)
+    return e0.elapsed_time(e1), graphs
 
-    ms = max_over_ranks(ms, dev)
 
+def time_kernels(layers, args, dev):
+    """Per-kernel durations of the replayed step: the step is captured once
+    more with the library's trace on, which puts a CUDA event-record node
+    before and after every kernel of the graph; K replays are timed kernel by
+    kernel (and as whole replays). Returns ({label: [ms, ...]}, ms per replay)."""
+    import torch
+
+    import binary_rank_linear_gb300 as blr
+    stream = torch.cuda.current_stream()
+    nsets = len(layers[0].sets)
+    blr.trace_begin(capacity=nsets * 16 * len(layers) + 16)
+    graphs, ranges = [], []
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    try:
+        with torch.cuda.stream(cap):
+            for i in range(nsets):
+                gr = torch.cuda.CUDAGraph()
+                rng = []
+                with torch.cuda.graph(gr, stream=cap):
+                    for li, L in enumerate(layers):
+                        a = blr.trace_count()
+                        L.step(i)
+                        rng.append((li, a, blr.trace_count()))
+                graphs.append(gr)
+                ranges.append(rng)
+    finally:
+        blr.trace_end(read=False)
+    stream.wait_stream(cap)
     per = {}
-    for name, kms in trace:
-        per.setdefault(name, []).append(kms)
-    launches_per_step = len(trace) / max(1, args.steps)
-    peaks, peak_src = _peaks()
-    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    whole = []
+    for i in range(max(args.warmup, nsets)):
+        graphs[i % nsets].replay()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        k = i % nsets
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graphs[k].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        whole.append(e0.elapsed_time(e1))
+        for li, a, b in ranges[k]:
+            for name, ms in blr.trace_read(a, b):
+                per.setdefault(label(layers, li, name), []).append(ms)
+    del graphs
+    return per, statistics.mean(whole)
+
+
+def roofline_of(per, layers, tc_peak, hbm_peak, steps):
+    """Per-kernel figures and the roofline of the dominant kernel (largest
+    total time), from the algorithmic work of each launch."""
     kernels = {}
+    tot = sum(sum(v) for v in per.values())
     for name, lst in per.items():
-        avg = sum(lst) / len(lst)
-        fl, by = kernel_work(name, M, d_in, d_out, r)
-        kernels[name] = {"avg_us": avg * 1e3, "share": sum(lst) / sum(sum(v) for v in per.values()),
-                         "tflops": fl / (avg * 1e-3) / 1e12, "gbs": by / (avg * 1e-3) / 1e9}
+        lname = name.split("/")[-1]
+        w = next(L.w for L in layers if len(layers) == 1 or L.w.name == name.split("/")[0])
+        fl, alg, stg = kernel_work(lname, w.M, w.d_in, w.d_out, w.r)
+        avg_s = sum(lst) / len(lst) * 1e-3
+        kernels[name] = {"avg_us": avg_s * 1e6, "launches_per_step": len(lst) / steps, "share": sum(lst) / tot,
+                         "tflops": fl / avg_s / 1e12, "alg_gbs": alg / avg_s / 1e9, "staging_gbs": stg / avg_s / 1e9}
     dom = max(per, key=lambda n: sum(per[n]))
-    fl, by = kernel_work(dom, M, d_in, d_out, r)
+    lname = dom.split("/")[-1]
+    w = next(L.w for L in layers if len(layers) == 1 or L.w.name == dom.split("/")[0])
+    fl, alg, stg = kernel_work(lname, w.M, w.d_in, w.d_out, w.r)
     avg_s = kernels[dom]["avg_us"] * 1e-6
-    t_tc, t_hbm = fl / (tc_peak * 1e12), by / (hbm_peak * 1e9)
+    t_tc, t_hbm = fl / (tc_peak * 1e12), alg / (hbm_peak * 1e9)
     if t_tc >= t_hbm:
         roof = {"bound": "tensor", "achieved": fl / avg_s / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
     else:
-        roof = {"bound": "hbm", "achieved": by / avg_s / 1e9, "peak": hbm_peak, "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": alg / avg_s / 1e9, "peak": hbm_peak, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = dom
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json: bf16 burst, f16 assumed equal)" \
-        if peak_src == "measured" else "fallback"
+    roof.update({"kernel": dom, "avg_us": avg_s * 1e6, "flops_per_launch": fl, "alg_bytes_per_launch": alg,
+                 "staging_bytes_per_launch": stg})
+    return kernels, roof
+
+
+def barrier(args):
+    import torch
+    if getattr(args, "_dist", False):
+        import torch.distributed as tdist
+        tdist.barrier()
+    torch.cuda.synchronize()
+
+
+def measure_config(name, args, dev, tc_peak, hbm_peak):
+    """A compact line for one more workload: graph-timed step, per-kernel
+    durations and the dominant kernel's roofline (no side measurements)."""
+    import torch
+
+    import binary_rank_linear_gb300 as blr
+    from binary_rank_linear_gb300 import workloads as wl
+    layers_w = wl.step_layers(name)
+    nsets, set_bytes = nsets_for(layers_w, blr)
+    layers = [Layer(w, dev, nsets) for w in layers_w]
+    ms, graphs = time_step(layers, args, dev)
+    del graphs
+    per, inst_ms = time_kernels(layers, args, dev)
+    for L in layers:
+        L.check(name)
+    kernels, roof = roofline_of(per, layers, tc_peak, hbm_peak, args.steps)
+    M = layers_w[0].M
+    flops = sum(w.flops for w in layers_w)
+    canon = sum(w.canonical_bytes for w in layers_w)
+    out = {"workload": f"{name}: {wl.step_note(name)}", "value": M * args.steps / (ms * 1e-3), "unit": "tokens/s",
+           "ms_per_step": ms / args.steps, "tflops": flops * args.steps / (ms * 1e-3) / 1e12,
+           "tensor_frac": flops * args.steps / (ms * 1e-3) / 1e12 / tc_peak,
+           "hbm_frac": canon * args.steps / (ms * 1e-3) / 1e9 / hbm_peak,
+           "instrumented_ms_per_step": inst_ms, "roofline": roof,
+           "kernels": {k: {"avg_us": v["avg_us"], "share": v["share"]} for k, v in kernels.items()},
+           "l2": f"{nsets} rotating input/output/workspace sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import binary_rank_linear_gb300 as blr
+    from binary_rank_linear_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    layers_w = layers_of(args)
+    nsets, set_bytes = nsets_for(layers_w, blr)
+    layers = [Layer(w, dev, nsets) for w in layers_w]
+    M = layers_w[0].M
+    flops = sum(w.flops for w in layers_w)
+    canon = sum(w.canonical_bytes for w in layers_w)
+
+    clocks = ClockSampler(local_rank)
+    ms, graphs = time_step(layers, args, dev, clocks)
+    clk = clocks.stop()
+    del graphs
+    for L in layers:
+        L.check("timed steps")
+    ms = max_over_ranks(ms, dev)
+
+    per, inst_ms = time_kernels(layers, args, dev)
+    launches_per_step = sum(len(v) for v in per.values()) / max(1, args.steps)
+    peaks, peak_src = _peaks()
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    kernels, roof = roofline_of(per, layers, tc_peak, hbm_peak, args.steps)
+    roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json: burst; bf16 for the f16 products, the same rate "
+                           f"on this part)" if peak_src == "measured" else "fallback")
+    roof["timing"] = ("CUDA events before and after each kernel, recorded as event nodes of the replayed step "
+                      "graph (those replays run the kernels without programmatic overlap)")
     # stored counters are for the workloads' own token counts
-    roof["traffic"] = stored_traffic(args.workload, dom) if not args.tokens else None
+    roof["traffic"] = stored_traffic(args.workload, roof["kernel"]) if not args.tokens else None
 
-    sign = measure_sign_grads(blr, sets, g, l, args.steps, tc_peak, M, d_in, d_out, r, dev) \
+    L0 = layers[0]
+    w0 = L0.w
+    sign = measure_sign_grads(blr, L0.sets, L0.g, L0.l, args.steps, tc_peak, w0.M, w0.d_in, w0.d_out, w0.r, dev) \
         if not args.no_sign else None
-    adam = measure_adam(blr, torch.cat([dg, dl, dh]), args.steps, hbm_peak, dev)
-    plane = measure_plane(blr, sets[0], args.steps, tc_peak, M, d_in, d_out, dev) if not args.no_plane else None
-    paths = measure_paths(blr, sets[0], bu, bv, g, l, h, args.steps, tc_peak, w, dev) if not args.no_paths else None
+    adam = measure_adam(blr, torch.cat([L0.dg, L0.dl, L0.dh]), args.steps, hbm_peak, dev)
+    plane = measure_plane(blr, L0.sets[0], args.steps, tc_peak, w0.M, w0.d_in, w0.d_out, dev) \
+        if not args.no_plane else None
+    paths = measure_paths(blr, L0.sets[0], L0.bu, L0.bv, L0.g, L0.l, L0.h, args.steps, tc_peak, w0, dev) \
+        if not args.no_paths else None
 
-    # end-to-end: host buffers through the public API, copies inside the timed
-    # region. With a megabyte or more to move per step, steps are pipelined over
-    # two device buffer sets on three streams (host->device copies, the layer,
-    # device->host copies), as a training loop's data path would be: step i+1's
-    # inputs go up and step i-1's results come down while step i computes.
-    # Smaller steps run in order on one stream (there the host's launch work,
-    # not the copies, sets the pace, and the extra streams only add to it).
-    # Every step moves its own inputs and results either way.
-    xh = torch.from_numpy(t["x"]).pin_memory()
-    dyh = torch.from_numpy(t["dy"]).pin_memory()
-    pipelined = 4 * M * (d_in + d_out) >= (1 << 20)
-    npipe = 2
-    pipe = []
-    for b in range(npipe):
-        pipe.append({
-            "set": sets[b % len(sets)],
-            "yh": torch.empty(M, d_out).pin_memory(),
-            "dxh": torch.empty(M, d_in).pin_memory(),
-            "gh": torch.empty(d_in + r + d_out).pin_memory(),
-            "dg": torch.zeros(d_in, device=dev), "dl": torch.zeros(r, device=dev), "dh": torch.zeros(d_out, device=dev),
-            "up": torch.cuda.Event(), "done": torch.cuda.Event(), "down": torch.cuda.Event(),
-        })
-    if pipelined:
-        s_up, s_comp, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    else:
-        s_up = s_comp = s_down = torch.cuda.current_stream(dev)
-    for b in pipe:
-        b["down"].record(s_down)  # nothing to wait for yet
-
-    def e2e_step_in_order(i):
-        b = pipe[0]
-        s0 = b["set"]
-        s0["x"].copy_(xh, non_blocking=True)
-        s0["dy"].copy_(dyh, non_blocking=True)
-        blr.forward(s0["x"], bu, bv, g, l, h, s0["y"], s0["ws"])
-        blr.backward(s0["x"], s0["dy"], bu, bv, g, l, h, s0["dx"], b["dg"], b["dl"], b["dh"], s0["ws"])
-        b["yh"].copy_(s0["y"], non_blocking=True)
-        b["dxh"].copy_(s0["dx"], non_blocking=True)
-        b["gh"][:d_in].copy_(b["dg"], non_blocking=True)
-        b["gh"][d_in:d_in + r].copy_(b["dl"], non_blocking=True)
-        b["gh"][d_in + r:].copy_(b["dh"], non_blocking=True)
-
-    def e2e_step(i):
-        if not pipelined:
-            e2e_step_in_order(i)
-            return
-        b = pipe[i % npipe]
-        s0 = b["set"]
-        # the set's previous results are down (its y/dx and inputs are free again)
-        s_up.wait_event(b["down"])
-        with torch.cuda.stream(s_up):
-            s0["x"].copy_(xh, non_blocking=True)
-            s0["dy"].copy_(dyh, non_blocking=True)
-        b["up"].record(s_up)
-        s_comp.wait_event(b["up"])
-        with torch.cuda.stream(s_comp):
-            blr.forward(s0["x"], bu, bv, g, l, h, s0["y"], s0["ws"])
-            blr.backward(s0["x"], s0["dy"], bu, bv, g, l, h, s0["dx"], b["dg"], b["dl"], b["dh"], s0["ws"])
-        b["done"].record(s_comp)
-        s_down.wait_event(b["done"])
-        with torch.cuda.stream(s_down):
-            b["yh"].copy_(s0["y"], non_blocking=True)
-            b["dxh"].copy_(s0["dx"], non_blocking=True)
-            b["gh"][:d_in].copy_(b["dg"], non_blocking=True)
-            b["gh"][d_in:d_in + r].copy_(b["dl"], non_blocking=True)
-            b["gh"][d_in + r:].copy_(b["dh"], non_blocking=True)
-        b["down"].record(s_down)
-
-    for i in range(max(npipe, args.warmup)):
-        e2e_step(i)
-    torch.cuda.synchronize(dev)
-    barrier()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(s_up)
-    for i in range(args.steps):
-        e2e_step(i)
-    s_up.wait_stream(s_down)
-    f1.record(s_up)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_ms = f0.elapsed_time(f1)
+    e2e_ms, h2d, d2h, pipelined = measure_e2e(layers, args, dev)
     e2e_ms = max_over_ranks(e2e_ms, dev)
-    for b in pipe:
-        st = blr.check_status(b["set"]["ws"])
-        if st:
-            raise RuntimeError(f"end-to-end pass: device status {st:#x}")
+    for L in layers:
+        L.check("end-to-end pass")
 
     value = job_tokens_per_s(world, M, args.steps, ms)
     result = {
@@ -461,24 +542,21 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f16",
         "data": "synthetic",
-        "config": {
-            "workload": f"{w.name}: {w.note}" + (f" (token count set to {M})" if args.tokens else ""),
-            "M": M, "d_in": d_in, "d_out": d_out, "r": r,
-            "mode": "overwrite y/dx, dynamic per-token gradient scale",
-            "small_path": args.small_path,
-            "l2": f"{nsets} rotating input/output/workspace sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)",
-        },
-        "tflops": world * w.flops * args.steps / (ms * 1e-3) / 1e12,
-        "tensor_frac": (world * w.flops * args.steps / (ms * 1e-3) / 1e12) / tc_peak,
-        "hbm_frac": (w.canonical_bytes * args.steps / (ms * 1e-3) / 1e9) / hbm_peak,
+        "config": config_of(args, layers_w),
+        "small_path": args.small_path,
+        "buffer_sets": f"{nsets} rotating input/output/workspace sets ({nsets * set_bytes / 2**20:.0f} MiB)",
+        "tflops": world * flops * args.steps / (ms * 1e-3) / 1e12,
+        "tensor_frac": (world * flops * args.steps / (ms * 1e-3) / 1e12) / tc_peak,
+        "hbm_frac": (world * canon * args.steps / (ms * 1e-3) / 1e9) / hbm_peak,
         "roofline": roof,
+        "instrumented_ms_per_step": inst_ms,
         "kernels": kernels,
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clk,
         "e2e": {"value": job_tokens_per_s(world, M, args.steps, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": 4 * M * (d_in + d_out),
-                "d2h_bytes_per_step": 4 * (M * (d_in + d_out) + d_in + r + d_out),
-                "copies": "overlapped with the layer on their own streams" if pipelined else "in order on one stream"},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "overlapped with the layers on their own streams" if pipelined else
+                          "in order on one stream"},
     }
     if sign is not None:
         result["sign_grads"] = sign
@@ -486,9 +564,97 @@ def run_gpu(args, rank, world, local_rank):
     if plane is not None:
         result["plane_linear"] = plane
     if paths is not None:
-        paths["vs_one_path"] = paths["us_per_step"] / (ms / args.steps * 1e3)
+        paths["vs_one_layer_step"] = paths["us_per_step"] / (ms / args.steps * 1e3 / len(layers))
         result["paths"] = paths
+    del layers
+    torch.cuda.empty_cache()
+    if world == 1 and args.extra:
+        result["configs"] = {}
+        for name in [n for n in args.extra.split(",") if n and n != args.workload]:
+            result["configs"][name] = measure_config(name, args, dev, tc_peak, hbm_peak)
     return result
+
+
+def measure_e2e(layers, args, dev):
+    """End to end through the Python API: every step copies its inputs (x, dy
+    of every layer) from pinned host memory and its results (y, dx, dg, dl,
+    dh of every layer) back, inside the timed region. With a megabyte or more
+    to move per step, steps are pipelined over two device buffer sets on
+    three streams (host->device copies, the layers, device->host copies), as
+    a training loop's data path would be: step i+1's inputs go up and step
+    i-1's results come down while step i computes. Smaller steps run in order
+    on one stream (there the host's launch work, not the copies, sets the
+    pace). Returns (ms, h2d bytes per step, d2h bytes per step, pipelined)."""
+    import torch
+    npipe = 2
+    h2d = sum(4 * L.w.M * (L.w.d_in + L.w.d_out) for L in layers)
+    d2h = sum(4 * (L.w.M * (L.w.d_in + L.w.d_out) + L.w.d_in + L.w.r + L.w.d_out) for L in layers)
+    pipelined = h2d >= (1 << 20)
+    pipe = []
+    for b in range(npipe):
+        per_layer = []
+        for L in layers:
+            w = L.w
+            per_layer.append({
+                "set": L.sets[b % len(L.sets)],
+                "xh": torch.from_numpy(L.host["x"]).pin_memory() if b == 0 else None,
+                "dyh": torch.from_numpy(L.host["dy"]).pin_memory() if b == 0 else None,
+                "yh": torch.empty(w.M, w.d_out).pin_memory(),
+                "dxh": torch.empty(w.M, w.d_in).pin_memory(),
+                "gh": torch.empty(w.d_in + w.r + w.d_out).pin_memory(),
+                "dg": torch.zeros(w.d_in, device=dev), "dl": torch.zeros(w.r, device=dev),
+                "dh": torch.zeros(w.d_out, device=dev),
+            })
+        pipe.append({"layers": per_layer, "up": torch.cuda.Event(), "done": torch.cuda.Event(),
+                     "down": torch.cuda.Event()})
+    src = pipe[0]["layers"]
+    if pipelined:
+        s_up, s_comp, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    else:
+        s_up = s_comp = s_down = torch.cuda.current_stream(dev)
+    for b in pipe:
+        b["down"].record(s_down)  # nothing to wait for yet
+
+    def e2e_step(i):
+        b = pipe[i % npipe] if pipelined else pipe[0]
+        s_up.wait_event(b["down"])  # the set's previous results are down: its buffers are free again
+        with torch.cuda.stream(s_up):
+            for li, q in enumerate(b["layers"]):
+                q["set"]["x"].copy_(src[li]["xh"], non_blocking=True)
+                q["set"]["dy"].copy_(src[li]["dyh"], non_blocking=True)
+        b["up"].record(s_up)
+        s_comp.wait_event(b["up"])
+        with torch.cuda.stream(s_comp):
+            for L, q in zip(layers, b["layers"]):
+                s0 = q["set"]
+                L.blr.forward(s0["x"], L.bu, L.bv, L.g, L.l, L.h, s0["y"], s0["ws"])
+                L.blr.backward(s0["x"], s0["dy"], L.bu, L.bv, L.g, L.l, L.h, s0["dx"], q["dg"], q["dl"], q["dh"],
+                               s0["ws"])
+        b["done"].record(s_comp)
+        s_down.wait_event(b["done"])
+        with torch.cuda.stream(s_down):
+            for L, q in zip(layers, b["layers"]):
+                w = L.w
+                q["yh"].copy_(q["set"]["y"], non_blocking=True)
+                q["dxh"].copy_(q["set"]["dx"], non_blocking=True)
+                q["gh"][:w.d_in].copy_(q["dg"], non_blocking=True)
+                q["gh"][w.d_in:w.d_in + w.r].copy_(q["dl"], non_blocking=True)
+                q["gh"][w.d_in + w.r:].copy_(q["dh"], non_blocking=True)
+        b["down"].record(s_down)
+
+    for i in range(max(npipe, args.warmup)):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    barrier(args)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(s_up)
+    for i in range(args.steps):
+        e2e_step(i)
+    s_up.wait_stream(s_down)
+    f1.record(s_up)
+    torch.cuda.synchronize(dev)
+    barrier(args)
+    return f0.elapsed_time(f1), h2d, d2h, pipelined
 
 
 def measure_paths(blr, s, bu, bv, g, l, h, steps, tc_peak, w, dev):
@@ -628,13 +794,29 @@ def measure_sign_grads(blr, sets, g, l, steps, tc_peak, M, d_in, d_out, r, dev):
     }
 
 
+def config_of(args, layers_w):
+    """The `config` object of both arms' lines (the same keys and values)."""
+    from binary_rank_linear_gb300 import workloads as wl
+    M = layers_w[0].M
+    return {
+        "workload": f"{args.workload}: {wl.step_note(args.workload)}" + (f" (token count set to {M})" if args.tokens
+                                                                          else ""),
+        "layers": [{"name": w.name, "M": w.M, "d_in": w.d_in, "d_out": w.d_out, "r": w.r} for w in layers_w],
+        "mode": "overwrite y/dx, dynamic per-token gradient scale",
+        "l2": "buffer sets rotated between steps, their total more than twice the 129 MB L2",
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="blr", choices=["blr", "reference"])
-    ap.add_argument("--workload", default="small")
+    ap.add_argument("--workload", default="mlp",
+                    help="mlp (the SwiGLU up+down pair, default), tiny, small, attn, mlp_up, mlp_down, ragged")
+    ap.add_argument("--extra", default="tiny,small,attn,ragged",
+                    help="workloads measured after the main one (N=1 only), reported under 'configs'; '' for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sign", action="store_true", help="skip the sign-gradient measurement")
     ap.add_argument("--no-plane", action="store_true", help="skip the plane_linear measurement")
@@ -653,9 +835,8 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
-    from binary_rank_linear_gb300 import workloads as wl
-
-    w = workload_of(args)
+    layers_w = layers_of(args)
+    M = layers_w[0].M
 
     if args.impl == "reference":
         if rank != 0:
@@ -663,21 +844,20 @@ def main():
         budget = 10.0
         t0 = time.perf_counter()
         for _ in range(args.warmup):  # untimed warm-up passes of the same sample
-            cpu_oracle_rate(w, budget_s=0.0, max_reps=1)
+            cpu_oracle_rate(layers_w, budget_s=0.0, max_reps=1)
         per_step = []
         base = None
         for _ in range(args.steps):
-            base = cpu_oracle_rate(w, budget_s=min(budget, 120.0 / max(1, args.steps)), max_reps=1)
+            base = cpu_oracle_rate(layers_w, budget_s=min(budget, 120.0 / max(1, args.steps)), max_reps=1)
             per_step.append(base["value"])
         value = statistics.median(per_step)
         el = time.perf_counter() - t0
         base["value"] = value
         out = {
             "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.M / value * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": M / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": f"{w.name}: {w.note}", "M": w.M, "d_in": w.d_in,
-                                            "d_out": w.d_out, "r": w.r},
+            "data": "synthetic", "config": config_of(args, layers_w),
             "cpu_baseline": base,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": el,
@@ -685,6 +865,7 @@ def main():
         print(json.dumps(out))
         return
 
+    args._dist = world > 1
     if world > 1:
         import torch
         import torch.distributed as tdist
@@ -693,7 +874,7 @@ def main():
     res = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_oracle_rate(w)
+            res["cpu_baseline"] = cpu_oracle_rate(layers_w)
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as tdist

@@ -67,13 +67,15 @@ def load() -> ctypes.CDLL:
     lib.blr_plane_workspace_bytes.restype = Z
     lib.blr_plane_linear.argtypes = [P, P, P, I, I, F, I, I, I, P, Z, P]
     lib.blr_check_status.argtypes = [P, Z, P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.blr_noalloc_check_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.blr_workspace_release.argtypes = [P]
     lib.blr_status_string.argtypes = [I]
     lib.blr_status_string.restype = ctypes.c_char_p
     lib.blr_trace_begin.argtypes = [I]
     lib.blr_trace_read.argtypes = [I, ctypes.POINTER(ctypes.c_float)]
     lib.blr_trace_read.restype = ctypes.c_char_p
     for f in ("blr_pack_signs", "blr_unpack_signs", "blr_forward", "blr_backward", "blr_sign_grads", "blr_adam", "blr_plane_linear", "blr_forward_paths", "blr_backward_paths",
-              "blr_check_status",
+              "blr_check_status", "blr_noalloc_check_status", "blr_workspace_release",
               "blr_trace_begin", "blr_trace_end", "blr_trace_count"):
         getattr(lib, f).restype = I
     _lib = lib
@@ -314,16 +316,45 @@ def check_status(ws: torch.Tensor, stream=None) -> int:
     return int(code.value)
 
 
+def workspace_release(ws: torch.Tensor) -> None:
+    """Forget the tape record of ``ws`` (call before freeing a workspace whose
+    address may be handed out again)."""
+    _check(load().blr_workspace_release(_ptr(ws, "ws", torch.uint8)), "blr_workspace_release")
+
+
+def noalloc_check_status(stream=None) -> int:
+    """Synchronise and return the status word of the current device's
+    blr_forward_noalloc scratch array (0 = no failure)."""
+    code = ctypes.c_uint32(0)
+    rc = load().blr_noalloc_check_status(_stream(stream), ctypes.byref(code))
+    if rc not in (BLR_OK, BLR_ERR_DEVICE_CHECK):
+        raise BlrError(rc, "blr_noalloc_check_status")
+    return int(code.value)
+
+
 def trace_begin(capacity: int = 64) -> None:
     _check(load().blr_trace_begin(capacity), "blr_trace_begin")
 
 
-def trace_end() -> list:
-    """Stop tracing; return [(kernel name, ms), ...] for the kernels recorded."""
+def trace_end(read: bool = True) -> list:
+    """Stop tracing; return [(kernel name, ms), ...] for the kernels recorded
+    (nothing with read=False, e.g. when the calls were captured into a graph
+    that has not run yet: ``trace_read`` then reads each replay)."""
     lib = load()
     lib.blr_trace_end()
+    return trace_read() if read else []
+
+
+def trace_count() -> int:
+    return int(load().blr_trace_count())
+
+
+def trace_read(first: int = 0, last: int = None) -> list:
+    """[(kernel name, ms), ...] of trace entries first .. last-1 (synchronises)."""
+    lib = load()
+    last = lib.blr_trace_count() if last is None else last
     out = []
-    for i in range(lib.blr_trace_count()):
+    for i in range(first, last):
         ms = ctypes.c_float(0.0)
         name = lib.blr_trace_read(i, ctypes.byref(ms))
         if name is None:

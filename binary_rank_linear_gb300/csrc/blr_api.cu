@@ -10,6 +10,7 @@
 
 #include "../../include/blr.h"
 #include "blr_kernels.h"
+#include "blr_layout.h"
 
 namespace blr {
 cudaError_t launch_gemm_fwd(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args,
@@ -29,17 +30,28 @@ struct TraceState {
 thread_local TraceState g_trace;
 }  // namespace
 
+// A trace event on a stream that is being captured into a CUDA graph becomes
+// an event-record node of the graph (recorded at each replay), so that the
+// kernels of a replayed step can be timed one by one.
+static void trace_record(cudaEvent_t e, cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, stream, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, stream);
+}
+
 void trace_before(const char *name, cudaStream_t stream) {
     TraceState &t = g_trace;
     if (!t.on || t.n >= t.cap) return;
     t.names[t.n] = name;
-    cudaEventRecord(t.ev[2 * t.n], stream);
+    trace_record(t.ev[2 * t.n], stream);
 }
 
 void trace_after(cudaStream_t stream) {
     TraceState &t = g_trace;
     if (!t.on || t.n >= t.cap) return;
-    cudaEventRecord(t.ev[2 * t.n + 1], stream);
+    trace_record(t.ev[2 * t.n + 1], stream);
     ++t.n;
 }
 
@@ -162,63 +174,6 @@ bool make_tmap_out16_sw64(CUtensorMap *m, void *base, int rows, int cols) {
 // ------------------------------------------------------------ layout --------
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-struct Layout {
-    size_t header, bp_f1, bp_f2, bp_b1, bp_b2, plane_u, plane_v, x16, dy16, a32, al16, db16, c16, s_inv, sig,
-        sig_inv, blkmax, part_dh, part_dl, part_dg, total;
-    int rows_dh, rows_dl, rows_dg;
-};
-
-bool shape_ok(int M, int d_in, int d_out, int r) {
-    auto dim_ok = [](int d, int hi) { return d >= 64 && d <= hi && d % 32 == 0; };
-    return M >= 1 && M <= (1 << 28) && dim_ok(d_in, 65536) && dim_ok(d_out, 32768) && dim_ok(r, 65536);
-}
-
-Layout make_layout(int M, int d_in, int d_out, int r) {
-    Layout L{};
-    size_t off = 0;
-    auto take = [&](size_t bytes) {
-        size_t o = off;
-        off += align_up(bytes, 256);
-        return o;
-    };
-    const size_t m = (size_t)M;
-    L.header = take(256);
-    // re-laid bitmaps, [K blocks of 64, two per 128-deep k-step][sign_rows(N)][2]
-    // u32 (pad blocks and rows are never multiplied by anything but zero
-    // activations, or never stored)
-    auto kblocks = [](int K) { return (size_t)((K + 127) / 128) * 2; };
-    L.bp_f1 = take(kblocks(d_in) * sign_rows(r) * 8);   // forward 1: N = r, K = d_in
-    L.bp_f2 = take(kblocks(r) * sign_rows(d_out) * 8);  // forward 2: N = d_out, K = r
-    L.bp_b1 = take(kblocks(d_out) * sign_rows(r) * 8);  // backward 1: N = r, K = d_out
-    L.bp_b2 = take(kblocks(r) * sign_rows(d_in) * 8);   // backward 2: N = d_in, K = r
-    // +-1 f16 sign planes in the bitmaps' own [rows][r] order (plane-mode GEMMs)
-    L.plane_u = take((size_t)d_out * r * 2);
-    L.plane_v = take((size_t)d_in * r * 2);
-    // the f16 staging of all four products stays in place after the pass
-    // (the sign-gradient products read x16, dy16, al16 and db16 again)
-    L.x16 = take(m * d_in * 2);
-    L.dy16 = take(m * d_out * 2);
-    L.a32 = take(m * r * 4);
-    L.al16 = take(m * r * 2);
-    L.db16 = take(m * r * 2);
-    L.c16 = take(m * d_out * 2);
-    L.s_inv = take(m * 4);
-    L.sig = take(m * 4);
-    L.sig_inv = take(m * 4);
-    L.rows_dh = stage_dy_blocks(M, d_out);
-    L.blkmax = take((size_t)L.rows_dh * 8);
-    // partial rows per token tile (tiles of at least 128 tokens)
-    // (split-K db-products write one per quarter of K)
-    L.rows_dl = (int)((m + 127) / 128) * 4;
-    // (the token-major dx'-product writes four per 128-token tile)
-    L.rows_dg = (int)((m + 127) / 128) * 4;
-    L.part_dh = take((size_t)L.rows_dh * d_out * 4);
-    L.part_dl = take((size_t)L.rows_dl * r * 4);
-    L.part_dg = take((size_t)L.rows_dg * d_in * 4);
-    L.total = off;
-    return L;
-}
-
 // Second workspace of blr_sign_grads: header (the two scale maxima), then the
 // rank-side operands rescaled to one gradient scale, bu and bv [M][r] f16.
 struct SignLayout {
@@ -241,14 +196,51 @@ SignLayout make_sign_layout(int M, int r) {
 }
 
 // ------------------------------------------------------------ tape ---------
+// What the last forward on a workspace recorded there, keyed by the workspace
+// pointer: its shape and the device pointers of its inputs. A backward (and
+// the sign gradients) must name the same x and parameters as that forward,
+// so that a workspace whose address was freed and handed out again for
+// another layer of the same shape cannot pass with a stale tape.
 struct Tape {
     int M, d_in, d_out, r;
+    const void *x, *bits_u, *bits_v, *g, *l, *h;  // the forward's inputs
+    unsigned long long gen;  // forward counter when recorded (oldest first out when the registry is full)
     bool backward_done;  // a blr_backward has run on this tape (its staged dy and db are in the workspace)
     float gscale;        // that backward's gradient scale (<= 0: dynamic per-token scales)
     int stage_blocks;    // its staging blocks (entries of the per-block scale maxima)
 };
 std::mutex g_tape_mu;
 std::unordered_map<const void *, Tape> g_tapes;
+unsigned long long g_tape_gen = 0;
+// Registry bound: beyond this many live workspaces the oldest record is
+// dropped (its backward then fails with BLR_ERR_STATE).
+constexpr size_t kMaxTapes = 1u << 16;
+
+void record_tape(const void *ws, Tape t) {
+    std::lock_guard<std::mutex> lk(g_tape_mu);
+    t.gen = ++g_tape_gen;
+    g_tapes[ws] = t;
+    if (g_tapes.size() > kMaxTapes) {
+        auto oldest = g_tapes.begin();
+        for (auto it = g_tapes.begin(); it != g_tapes.end(); ++it)
+            if (it->second.gen < oldest->second.gen) oldest = it;
+        g_tapes.erase(oldest);
+    }
+}
+
+// The tape of `ws` if it was recorded by a forward of this shape on these inputs.
+bool tape_matches(const void *ws, int M, int d_in, int d_out, int r, const void *x, const void *bits_u,
+                  const void *bits_v, const void *g, const void *l, const void *h, Tape *out = nullptr) {
+    std::lock_guard<std::mutex> lk(g_tape_mu);
+    auto it = g_tapes.find(ws);
+    if (it == g_tapes.end()) return false;
+    const Tape &t = it->second;
+    if (t.M != M || t.d_in != d_in || t.d_out != d_out || t.r != r) return false;
+    if (t.x != x || t.g != g || t.l != l) return false;
+    if ((bits_u && t.bits_u != bits_u) || (bits_v && t.bits_v != bits_v) || (h && t.h != h)) return false;
+    if (out) *out = t;
+    return true;
+}
 
 void mark_backward_done(const void *ws, float gscale, int stage_blocks) {
     std::lock_guard<std::mutex> lk(g_tape_mu);
@@ -266,17 +258,17 @@ bool plane_shape_ok(int ntok, int n, int k) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool fault_injected(const char *site) {
-    const char *f = std::getenv("BLR_FAULT");
-    return f && std::strcmp(f, site) == 0;
-}
-
 bool pow2_positive(float v) {
     if (!(v > 0.0f) || !std::isfinite(v)) return false;
     int e;
     return std::frexp(v, &e) == 0.5f;
 }
 }  // namespace
+
+bool fault_injected(const char *site) {
+    const char *f = std::getenv("BLR_FAULT");
+    return f && std::strcmp(f, site) == 0;
+}
 }  // namespace blr
 
 namespace blr {
@@ -390,9 +382,6 @@ int small_grid(const GemmPlan &p1, int N1, const GemmPlan &p2, int N2, int M, in
     return tiles < sms ? tiles : sms;
 }
 
-// Word of the workspace header used as the fused kernels' grid-barrier counter.
-constexpr size_t kGridBarOffset = 64;
-
 // The fused small-M kernels (blr_small.cu) are used for small problems only
 // when BLR_SMALL_PATH=fused is set: measured on GB300 they match the
 // stand-alone kernels on per-kernel time but lose under CUDA-graph replay,
@@ -400,6 +389,22 @@ constexpr size_t kGridBarOffset = 64;
 bool fused_small_enabled() {
     const char *v = std::getenv("BLR_SMALL_PATH");
     return v && std::strcmp(v, "fused") == 0;
+}
+
+// Grid barriers of the fused small-M kernels. Their waits give up after 2 s
+// (BLR_WAIT_LIMIT_NS=<ns> sets another limit, from 1 us to 10 s). For the
+// test of that path, BLR_FAULT=grid_barrier makes every barrier expect one
+// arrival more than the grid makes, so each wait runs out: the kernels then
+// record kStTimeoutGrid in the status word, leave their remaining phases
+// early and return (their results are then meaningless).
+GridBarrier grid_barrier(unsigned int *gbar) {
+    GridBarrier b{gbar, 0u, 2000000000ull};
+    if (const char *v = std::getenv("BLR_WAIT_LIMIT_NS")) {
+        const long long ns = std::atoll(v);
+        if (ns >= 1000 && ns <= 10000000000ll) b.wait_ns = (unsigned long long)ns;
+    }
+    if (fault_injected("grid_barrier")) b.extra = 1;
+    return b;
 }
 
 // The per-path pointers of a multi-path call: every array present, every entry
@@ -432,6 +437,13 @@ extern "C" {
 size_t blr_workspace_bytes(int M, int d_in, int d_out, int r) {
     if (!shape_ok(M, d_in, d_out, r)) return 0;
     return make_layout(M, d_in, d_out, r).total;
+}
+
+int blr_workspace_release(const void *ws) {
+    if (!ws) return BLR_ERR_ARG;
+    std::lock_guard<std::mutex> lk(g_tape_mu);
+    g_tapes.erase(ws);
+    return BLR_OK;
 }
 
 int blr_pack_signs(const float *src, uint32_t *bits, int rows, int r, blr_stream_t stream) {
@@ -561,7 +573,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     if (fused) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallFwdArgs fa{pv, pu, x, g, x16, M, d_in, status,
-                        reinterpret_cast<unsigned int *>(w + L.header + kGridBarOffset), f1, f2};
+                        grid_barrier(reinterpret_cast<unsigned int *>(w + L.header + kGridBarOffset)), f1, f2};
         if (launch_small_fwd(m1, m2, fa, small_grid(p1, r, p2, d_out, M, sms), s) != cudaSuccess)
             return BLR_ERR_CUDA;
     } else {
@@ -574,8 +586,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
         }
     }
 
-    std::lock_guard<std::mutex> lk(g_tape_mu);
-    g_tapes[ws] = Tape{M, d_in, d_out, r, false, 0.0f, 0};
+    record_tape(ws, Tape{M, d_in, d_out, r, x, bits_u, bits_v, g, l, h, 0, false, 0.0f, 0});
     return BLR_OK;
 }
 
@@ -591,13 +602,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
         if (!aligned16(p)) return BLR_ERR_ALIGN;
     const Layout L = make_layout(M, d_in, d_out, r);
     if (ws_bytes < L.total) return BLR_ERR_WORKSPACE;
-    {
-        std::lock_guard<std::mutex> lk(g_tape_mu);
-        auto it = g_tapes.find(ws);
-        if (it == g_tapes.end() || it->second.M != M || it->second.d_in != d_in || it->second.d_out != d_out ||
-            it->second.r != r)
-            return BLR_ERR_STATE;
-    }
+    if (!tape_matches(ws, M, d_in, d_out, r, x, bits_u, bits_v, g, l, h)) return BLR_ERR_STATE;
     int sms;
     int st = device_info(&sms);
     if (st != BLR_OK) return st;
@@ -720,7 +725,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
         ba.pu = pu;
         ba.pv = pv;
         ba.sd = sa;
-        ba.gbar = reinterpret_cast<unsigned int *>(w + L.header + kGridBarOffset);
+        ba.gb = grid_barrier(reinterpret_cast<unsigned int *>(w + L.header + kGridBarOffset));
         ba.b1 = b1;
         ba.b2 = b2;
         ba.rh = ReduceSeg{part_dh, dh, 0, d_out};
@@ -787,16 +792,11 @@ int blr_backward_paths(const float *x, const float *dy, int P, const uint32_t *c
         return st;
     const size_t one = make_layout(M, d_in, d_out, r).total;
     if (ws_bytes < (size_t)P * one) return BLR_ERR_WORKSPACE;
-    {
-        // every path's tape must be there before any path's backward is queued
-        std::lock_guard<std::mutex> lk(g_tape_mu);
-        for (int p = 0; p < P; ++p) {
-            auto it = g_tapes.find(static_cast<char *>(ws) + (size_t)p * one);
-            if (it == g_tapes.end() || it->second.M != M || it->second.d_in != d_in || it->second.d_out != d_out ||
-                it->second.r != r)
-                return BLR_ERR_STATE;
-        }
-    }
+    // every path's tape must be there before any path's backward is queued
+    for (int p = 0; p < P; ++p)
+        if (!tape_matches(static_cast<char *>(ws) + (size_t)p * one, M, d_in, d_out, r, x, bits_u[p], bits_v[p], g[p],
+                          l[p], h[p]))
+            return BLR_ERR_STATE;
     for (int p = 0; p < P; ++p) {
         st = blr_backward(x, dy, bits_u[p], bits_v[p], g[p], l[p], h[p], dx, (p > 0 || accumulate_dx) ? 1 : 0, dg[p],
                           dl[p], dh[p], gscale, M, d_in, d_out, r, static_cast<char *>(ws) + (size_t)p * one, one,
@@ -824,14 +824,8 @@ int blr_sign_grads(const float *x, const float *g, const float *l, float *gu, fl
     const SignLayout SL = make_sign_layout(M, r);
     if (ws_bytes < L.total || sws_bytes < SL.total) return BLR_ERR_WORKSPACE;
     Tape tape{};
-    {
-        std::lock_guard<std::mutex> lk(g_tape_mu);
-        auto it = g_tapes.find(ws);
-        if (it == g_tapes.end() || !it->second.backward_done || it->second.M != M || it->second.d_in != d_in ||
-            it->second.d_out != d_out || it->second.r != r)
-            return BLR_ERR_STATE;
-        tape = it->second;
-    }
+    if (!tape_matches(ws, M, d_in, d_out, r, x, nullptr, nullptr, g, l, nullptr, &tape) || !tape.backward_done)
+        return BLR_ERR_STATE;
     int sms;
     int st = device_info(&sms);
     if (st != BLR_OK) return st;

@@ -4,6 +4,9 @@
 // staging), and the fixed-order reduction of per-tile partial sums.
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "blr_device.cuh"
 #include "blr_kernels.h"
@@ -202,6 +205,49 @@ __global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(Redu
 }
 
 // ============================================================ launchers ====
+namespace {
+std::mutex g_launch_mu;
+std::map<std::tuple<int, const void *, int, size_t>, int> g_occupancy;
+std::map<std::pair<int, const void *>, int> g_prepared;
+}  // namespace
+
+int current_device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    return n;
+}
+
+int occupancy_blocks(const void *kernel, int threads, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const auto key = std::make_tuple(dev, kernel, threads, smem);
+    std::lock_guard<std::mutex> lk(g_launch_mu);
+    auto it = g_occupancy.find(key);
+    if (it != g_occupancy.end()) return it->second;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess) per_sm = 1;
+    if (per_sm < 1) per_sm = 1;
+    g_occupancy[key] = per_sm;
+    return per_sm;
+}
+
+cudaError_t prepare_once(const void *kernel, int max_dyn_smem) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_launch_mu);
+    auto key = std::make_pair(dev, kernel);
+    auto it = g_prepared.find(key);
+    if (it != g_prepared.end() && it->second >= max_dyn_smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    g_prepared[key] = max_dyn_smem;
+    return cudaSuccess;
+}
+
 static int grid_for(long long items, int per_block, int cap = 1 << 20) {
     long long g = (items + per_block - 1) / per_block;
     if (g < 1) g = 1;
@@ -228,31 +274,11 @@ cudaError_t launch_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, i
 template <int KQ>
 static cudaError_t launch_fwd_prologue_rows(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16,
                                            int M, int d_in, uint32_t *status, cudaStream_t s) {
-    static bool prepared = false;
-    if (!prepared) {
-        cudaError_t e = prepare_kernel(fwd_prologue_rows_kernel<KQ>, 0);
-        if (e != cudaSuccess) return e;
-        prepared = true;
-    }
+    cudaError_t pe = prepare_kernel_once(fwd_prologue_rows_kernel<KQ>, 0);
+    if (pe != cudaSuccess) return pe;
     const int T = sx_threads(d_in);
-    // blocks per SM for this block size, queried once per size
-    static int cached_t[8] = {0}, cached_wave[8] = {0};
-    int wave = 0;
-    for (int i = 0; i < 8; ++i)
-        if (cached_t[i] == T) wave = cached_wave[i];
-    if (wave == 0) {
-        int dev = 0, sms = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_prologue_rows_kernel<KQ>, T, 0);
-        wave = (per_sm < 1 ? 1 : per_sm) * sms;
-        for (int i = 0; i < 8; ++i)
-            if (cached_t[i] == 0) {
-                cached_t[i] = T;
-                cached_wave[i] = wave;
-                break;
-            }
-    }
+    const int wave = occupancy_blocks(reinterpret_cast<const void *>(fwd_prologue_rows_kernel<KQ>), T, 0) *
+                     current_device_sms();
     const int nchunks = (M + sx_rows(KQ) - 1) / sx_rows(KQ);
     const int bs = nchunks < wave ? nchunks : wave;
     const int pb = prep_blocks(p0, T) + prep_blocks(p1, T);
@@ -267,18 +293,9 @@ static cudaError_t launch_fwd_prologue_rows(SignPrep p0, SignPrep p1, const floa
 template <int KQ>
 static cudaError_t launch_fwd_prologue_stream(SignPrep p0, SignPrep p1, const float *x, const float *g,
                                              uint16_t *x16, int M, int d_in, uint32_t *status, cudaStream_t s) {
-    static bool prepared = false;
-    if (!prepared) {
-        cudaError_t e = prepare_kernel(fwd_prologue_stream_kernel<KQ>, kSxsHeadBytes + kSxsRingBytes);
-        if (e != cudaSuccess) return e;
-        prepared = true;
-    }
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    cudaError_t pe = prepare_kernel_once(fwd_prologue_stream_kernel<KQ>, kSxsHeadBytes + kSxsRingBytes);
+    if (pe != cudaSuccess) return pe;
+    const int sms = current_device_sms();
     const SxPlan pl = sxs_plan(d_in);
     int sb = (M + pl.rs - 1) / pl.rs;
     if (sb > sms) sb = sms;
@@ -316,22 +333,12 @@ cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const 
             default: return launch_fwd_prologue_rows<8>(p0, p1, x, g, x16, M, d_in, status, s);
         }
     }
-    static bool prepared = false;
-    if (!prepared) {
-        cudaError_t e = prepare_kernel(fwd_prologue_kernel, 0);
-        if (e != cudaSuccess) return e;
-        prepared = true;
-    }
+    cudaError_t pe = prepare_kernel_once(fwd_prologue_kernel, 0);
+    if (pe != cudaSuccess) return pe;
     // one wave of persistent blocks (each does its share of the re-layouts, then
     // grid-strides over x), but no more blocks than 8-group shares of x
-    static int wave = 0;
-    if (wave == 0) {
-        int dev = 0, sms = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_prologue_kernel, 256, 0);
-        wave = (per_sm < 1 ? 1 : per_sm) * sms;
-    }
+    const int wave = occupancy_blocks(reinterpret_cast<const void *>(fwd_prologue_kernel), 256, 0) *
+                     current_device_sms();
     const long long groups = (long long)M * (d_in / 4);
     const int bs = grid_for(groups, 256 * 8, wave);
     // re-layout-only blocks where the wave has room for them
@@ -349,31 +356,11 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
     const int tpr = stage_tpr(a.d_out, THREADS);
     const int rb_n = THREADS / tpr;
     const size_t smem = stage_dy_smem_bytes(a.d_out, tpr, rb_n * tpr);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = prepare_kernel(bwd_prologue_kernel<GPT, THREADS>, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    // blocks per SM for this shared-memory size, queried once per size
-    static int cached_smem[8] = {0}, cached_per_sm[8] = {0}, cached_sms = 0;
-    int per_sm = 0;
-    for (int i = 0; i < 8; ++i)
-        if (cached_smem[i] == (int)smem) per_sm = cached_per_sm[i];
-    if (per_sm == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&cached_sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_prologue_kernel<GPT, THREADS>, THREADS, smem);
-        if (per_sm < 1) per_sm = 1;
-        for (int i = 0; i < 8; ++i)
-            if (cached_smem[i] == 0) {
-                cached_smem[i] = (int)smem;
-                cached_per_sm[i] = per_sm;
-                break;
-            }
-    }
-    const int sms = cached_sms;
+    cudaError_t pe = prepare_kernel_once(bwd_prologue_kernel<GPT, THREADS>, 200 * 1024);
+    if (pe != cudaSuccess) return pe;
+    const int per_sm = occupancy_blocks(reinterpret_cast<const void *>(bwd_prologue_kernel<GPT, THREADS>), THREADS,
+                                        smem);
+    const int sms = current_device_sms();
     int sb = stage_dy_blocks(a.M, a.d_out);
     if (sb > per_sm * sms) sb = per_sm * sms;
     // re-layout-only blocks where the wave has room for them
@@ -388,18 +375,9 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
 
 template <int Q>
 static cudaError_t launch_bwd_stream_t(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = prepare_kernel(bwd_stream_kernel<Q>, kSdHeadBytes + kSdRingBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    cudaError_t pe = prepare_kernel_once(bwd_stream_kernel<Q>, kSdHeadBytes + kSdRingBytes);
+    if (pe != cudaSuccess) return pe;
+    const int sms = current_device_sms();
     const SdPlan pl = sd_plan(a.d_out);
     int sb = (a.M + pl.ngrp - 1) / pl.ngrp;
     if (sb > sms) sb = sms;
@@ -453,12 +431,8 @@ cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, 
 cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaStream_t s) {
     const int blocks = (a.n + kReduceCols - 1) / kReduceCols + (b.n + kReduceCols - 1) / kReduceCols +
                        (c.n + kReduceCols - 1) / kReduceCols;
-    static bool prepared = false;
-    if (!prepared) {
-        cudaError_t e = prepare_kernel(reduce_partials_kernel, 0);
-        if (e != cudaSuccess) return e;
-        prepared = true;
-    }
+    cudaError_t pe = prepare_kernel_once(reduce_partials_kernel, 0);
+    if (pe != cudaSuccess) return pe;
     trace_before("reduce_partials", s);
     cudaError_t e = launch_k(reduce_partials_kernel, dim3(blocks), dim3(kReduceWarps * 32), 0, s, a, b, c);
     trace_after(s);

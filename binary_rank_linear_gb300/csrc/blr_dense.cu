@@ -397,12 +397,8 @@ __global__ void __launch_bounds__(kSgThreads, 1)
 template <int BN, bool A_MN, bool B_MN, int EPM>
 static cudaError_t launch_dense_t(const DenseGemmLaunch &L, const DenseGemmArgs &ga, int grid, cudaStream_t s) {
     using S = DenseGemmShape<BN, EPM>;
-    static bool prepared = false;
-    if (!prepared) {
-        const cudaError_t e = prepare_kernel(dense_gemm_kernel<BN, A_MN, B_MN, EPM>, S::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        prepared = true;
-    }
+    const cudaError_t e = prepare_kernel_once(dense_gemm_kernel<BN, A_MN, B_MN, EPM>, S::kSmemBytes);
+    if (e != cudaSuccess) return e;
     return launch_k(dense_gemm_kernel<BN, A_MN, B_MN, EPM>, dim3(grid), dim3(kSgThreads), S::kSmemBytes, s, L.maps,
                     ga);
 }

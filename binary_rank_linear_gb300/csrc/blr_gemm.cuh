@@ -847,12 +847,8 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE>::kThreads, 1)
 template <int EPI, bool PAIR, int BT, bool PLANE = false, int SPLIT = 1>
 cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, cudaStream_t s) {
     using S = GemmShape<EPI, PAIR, BT, PLANE>;
-    static bool attr_set = false;  // set once, outside any later stream capture
-    if (!attr_set) {
-        cudaError_t e = prepare_kernel(blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT>, S::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t pe = prepare_kernel_once(blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT>, S::kSmemBytes);
+    if (pe != cudaSuccess) return pe;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(S::kThreads);

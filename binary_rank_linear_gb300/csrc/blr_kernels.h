@@ -29,12 +29,17 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Sets the maximum dynamic shared memory and the carveout of `kernel` once.
+// Per-device launch facts, thread-safe (a process may drive several GPUs from
+// several threads): the current device's SM count; a kernel's resident blocks
+// per SM at a block size and shared-memory size (queried once per device and
+// configuration); and, once per (device, kernel), the kernel's maximum
+// dynamic shared memory and the maximum shared-memory carveout.
+int current_device_sms();
+int occupancy_blocks(const void *kernel, int threads, size_t smem);
+cudaError_t prepare_once(const void *kernel, int max_dyn_smem);
 template <typename... KArgs>
-cudaError_t prepare_kernel(void (*kernel)(KArgs...), int max_dyn_smem) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn_smem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+cudaError_t prepare_kernel_once(void (*kernel)(KArgs...), int max_dyn_smem) {
+    return prepare_once(reinterpret_cast<const void *>(kernel), max_dyn_smem);
 }
 
 // Optional per-kernel event tracing (see blr_trace_begin in blr.h).
@@ -178,15 +183,25 @@ cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, con
 
 // ---- fused small-M path (blr_small.cu) ---------------------------------------
 // One cooperative launch (grid = one CTA per SM) per pass; the GEMM phases use
-// single-CTA 128-token tiles (plans with pair = false, bt = 128). `gbar` is a
-// grid-barrier counter in the workspace header, zeroed by the launcher.
+// single-CTA 128-token tiles (plans with pair = false, bt = 128). `gb.gbar`
+// is a grid-barrier counter in the workspace header, zeroed by the launcher.
+//
+// Grid barrier k waits for k * grid + gb.extra arrivals, for at most
+// gb.wait_ns of wall time (extra is 0 except in the test that makes the waits
+// run out; see blr_api.cu).
+struct GridBarrier {
+    unsigned int *gbar;
+    unsigned int extra;
+    unsigned long long wait_ns;
+};
+
 struct SmallFwdArgs {
     SignPrep pv, pu;    // re-layouts of S_V (a-product) and S_U (c-product)
     const float *x, *g;
     uint16_t *x16;
     int M, d_in;
     uint32_t *status;
-    unsigned int *gbar;
+    GridBarrier gb;
     GemmArgs f1, f2;    // the a- and c-products
 };
 
@@ -196,7 +211,7 @@ struct SmallBwdArgs {
     int stage_tpr;      // threads per token row in the staging (power of two <= 256); set by the launcher
     int stage_nthr;     // staging threads per CTA (a multiple of stage_tpr); set by the launcher
     int stage_blocks;   // CTAs that stage (dh partial rows written); set by the launcher
-    unsigned int *gbar;
+    GridBarrier gb;
     GemmArgs b1, b2;    // the db- and dx'-products
     ReduceSeg rh, rl, rg;
 };

@@ -16,11 +16,14 @@
 // current) and caches it, so that first call should be made before any stream
 // capture. All calls share the one array and it keeps the last call's
 // contents; the kernels clear what must start at zero (the status word), and
-// calls that overlap on the GPU race on the array.
+// calls that overlap on the GPU race on the array. Its layout is the forward
+// part of blr_forward's workspace layout (blr_layout.h), so both entry points
+// carve the same regions for the same shape.
 #include <mutex>
 
 #include "../../include/blr.h"
 #include "blr_kernels.h"
+#include "blr_layout.h"
 
 namespace blr {
 namespace {
@@ -32,6 +35,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[BLR_NOALLOC_SCR
 std::mutex g_na_mu;
 void *g_na_ptr[64];
 int g_na_sms[64];
+bool g_na_ran[64];  // a forward has been queued on this device's array
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -65,8 +69,6 @@ bool na_tmap(CUtensorMap *m, const void *base, int rows, int cols, int box_cols,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t na_align(size_t v) { return (v + 255) / 256 * 256; }
-
 // Device address of the scratch array on the current device (looked up once
 // per device), its SM count, and whether the device is supported.
 int na_setup(void **ptr, int *sms) {
@@ -90,17 +92,6 @@ int na_setup(void **ptr, int *sms) {
     return BLR_OK;
 }
 
-// Scratch bytes a forward of this shape needs (0 if the shape is invalid).
-size_t na_scratch_bytes(int M, int d_in, int d_out, int r) {
-    if (M < 1 || d_in < 64 || d_out < 64 || r < 64 || d_in % 32 || d_out % 32 || r % 32 || d_in > 65536 ||
-        d_out > 32768 || r > 65536)
-        return 0;
-    const size_t m = (size_t)M;
-    return na_align(256) + na_align((size_t)((d_in + 127) / 128) * 2 * sign_rows(r) * 8) +
-           na_align((size_t)((r + 127) / 128) * 2 * sign_rows(d_out) * 8) +
-           na_align(m * d_in * 2) + na_align(m * r * 4) + na_align(m * r * 2) + na_align(m * d_out * 2);
-}
-
 }  // namespace
 }  // namespace blr
 
@@ -111,35 +102,29 @@ extern "C" int blr_forward_noalloc(const float *x, const uint32_t *bits_u, const
                                    int d_out, int r, blr_stream_t stream) {
     if (!x || !bits_u || !bits_v || !g || !l || !h || !y) return BLR_ERR_ARG;
     if (accumulate_y != 0 && accumulate_y != 1) return BLR_ERR_ARG;
-    const size_t need = na_scratch_bytes(M, d_in, d_out, r);
-    if (need == 0) return BLR_ERR_SHAPE;
+    if (!shape_ok(M, d_in, d_out, r)) return BLR_ERR_SHAPE;
     const void *ptrs[] = {x, bits_u, bits_v, g, l, h, y};
     for (const void *p : ptrs)
         if (reinterpret_cast<uintptr_t>(p) & 15u) return BLR_ERR_ALIGN;
-    // the shape must fit the fixed scratch array: no allocation happens here
-    if (need > (size_t)BLR_NOALLOC_SCRATCH_BYTES) return BLR_ERR_WORKSPACE;
+    // the forward regions of the workspace layout must fit the fixed scratch
+    // array: no allocation happens here
+    const Layout L = make_layout(M, d_in, d_out, r);
+    if (L.fwd_total > (size_t)BLR_NOALLOC_SCRATCH_BYTES) return BLR_ERR_WORKSPACE;
 
     void *base = nullptr;
     int sms = 0;
     int st = na_setup(&base, &sms);
     if (st != BLR_OK) return st;
+    if (fault_injected("noalloc")) return BLR_ERR_CUDA;
 
-    // scratch layout: status header, two re-laid bitmaps, x16, a (f32), a.l (f16), c (f16)
     char *w = static_cast<char *>(base);
-    size_t off = 0;
-    auto take = [&](size_t bytes) {
-        size_t o = off;
-        off += na_align(bytes);
-        return w + o;
-    };
-    const size_t m = (size_t)M;
-    uint32_t *status = reinterpret_cast<uint32_t *>(take(256));
-    uint32_t *bp_f1 = reinterpret_cast<uint32_t *>(take((size_t)((d_in + 127) / 128) * 2 * sign_rows(r) * 8));
-    uint32_t *bp_f2 = reinterpret_cast<uint32_t *>(take((size_t)((r + 127) / 128) * 2 * sign_rows(d_out) * 8));
-    uint16_t *x16 = reinterpret_cast<uint16_t *>(take(m * d_in * 2));
-    float *a32 = reinterpret_cast<float *>(take(m * r * 4));
-    uint16_t *al16 = reinterpret_cast<uint16_t *>(take(m * r * 2));
-    uint16_t *c16 = reinterpret_cast<uint16_t *>(take(m * d_out * 2));
+    uint32_t *status = reinterpret_cast<uint32_t *>(w + L.header);
+    uint32_t *bp_f1 = reinterpret_cast<uint32_t *>(w + L.bp_f1);
+    uint32_t *bp_f2 = reinterpret_cast<uint32_t *>(w + L.bp_f2);
+    uint16_t *x16 = reinterpret_cast<uint16_t *>(w + L.x16);
+    float *a32 = reinterpret_cast<float *>(w + L.a32);
+    uint16_t *al16 = reinterpret_cast<uint16_t *>(w + L.al16);
+    uint16_t *c16 = reinterpret_cast<uint16_t *>(w + L.c16);
 
     // the same tile plans as blr_forward
     const GemmPlan p1 = plan_gemm(M, r, sms, 32);
@@ -182,5 +167,28 @@ extern "C" int blr_forward_noalloc(const float *x, const uint32_t *bits_u, const
     f2.accumulate = accumulate_y;
     f2.status = status;
     if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) return BLR_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+        std::lock_guard<std::mutex> lk(g_na_mu);
+        g_na_ran[dev] = true;
+    }
     return BLR_OK;
+}
+
+extern "C" int blr_noalloc_check_status(blr_stream_t stream, uint32_t *device_code) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BLR_ERR_CUDA;
+    void *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_na_mu);
+        if (!g_na_ran[dev]) return BLR_ERR_STATE;
+        base = g_na_ptr[dev];
+    }
+    // word 0 of the array (the layout's header) is the status word
+    uint32_t code = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&code, base, sizeof(code), cudaMemcpyDeviceToHost, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (device_code) *device_code = code;
+    return code ? BLR_ERR_DEVICE_CHECK : BLR_OK;
 }

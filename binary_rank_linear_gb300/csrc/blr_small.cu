@@ -20,11 +20,14 @@ namespace blr {
 constexpr int kSmallBT = 128;
 
 // Grid barrier: one arrival per CTA on a counter in global memory that only
-// grows during a launch (zeroed before it); barrier k completes at k * grid.
-// Bounded like every other wait: on timeout the CTA records it and carries on
-// with its abort flag set, so that its remaining waits end early.
-__device__ __forceinline__ void grid_sync(unsigned int *gbar, unsigned int target, volatile int *abort_flag,
+// grows during a launch (zeroed before it); barrier k completes at k * grid
+// (+ gb.extra). Bounded like every other wait, by gb.wait_ns: on timeout the
+// CTA records it and carries on with its abort flag set, so that its
+// remaining waits end early.
+__device__ __forceinline__ void grid_sync(const GridBarrier &gb, unsigned int k, volatile int *abort_flag,
                                           uint32_t *status) {
+    unsigned int *gbar = gb.gbar;
+    const unsigned int target = k * gridDim.x + gb.extra;
     __syncthreads();
     if (threadIdx.x == 0) {
         // this CTA's TMA stores and generic writes are complete and visible
@@ -37,7 +40,7 @@ __device__ __forceinline__ void grid_sync(unsigned int *gbar, unsigned int targe
             unsigned int v;
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gbar) : "memory");
             if (v >= target) break;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > gb.wait_ns) {
                 *abort_flag = 1;
                 atomicOr(status, kStTimeoutGrid);
                 break;
@@ -97,10 +100,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
     prep_share(a.pv, a.pu, (int)blockIdx.x, (int)gridDim.x);
     stage_x_run(a.x, a.g, a.x16, a.M, a.d_in, (int)blockIdx.x, (int)gridDim.x);
-    grid_sync(a.gbar, gridDim.x, abort_flag, a.status);
+    grid_sync(a.gb, 1, abort_flag, a.status);
     // phase 2: a = x16 S_V; a (f32 tape) and a.l (f16)
     small_gemm_phase<kEpiFwd1>(smem, m1, a.f1, tmem_base, abort_flag);
-    grid_sync(a.gbar, 2 * gridDim.x, abort_flag, a.status);
+    grid_sync(a.gb, 2, abort_flag, a.status);
     // phase 3: c = (a.l) S_U^T; y (+)= h.c, c (f16)
     small_gemm_phase<kEpiFwd2>(smem, m2, a.f2, tmem_base, abort_flag);
     small_teardown(tmem_base);
@@ -119,13 +122,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if ((int)blockIdx.x < a.stage_blocks)
         stage_dy_run<GPT>(a.sd, (int)blockIdx.x, a.stage_blocks, reinterpret_cast<float *>(smem + kCtlBytes),
                           a.stage_tpr, a.stage_nthr);
-    grid_sync(a.gbar, gridDim.x, abort_flag, a.b1.status);
+    grid_sync(a.gb, 1, abort_flag, a.b1.status);
     // phase 2: db = dy16 S_U / s_t; dl partials; db.l (f16) under sigma_t
     small_gemm_phase<kEpiBwd1>(smem, m1, a.b1, tmem_base, abort_flag);
-    grid_sync(a.gbar, 2 * gridDim.x, abort_flag, a.b1.status);
+    grid_sync(a.gb, 2, abort_flag, a.b1.status);
     // phase 3: dx' = (db.l) S_V^T / sigma_t; dx (+)= g.dx'; dg partials
     small_gemm_phase<kEpiBwd2>(smem, m2, a.b2, tmem_base, abort_flag);
-    grid_sync(a.gbar, 3 * gridDim.x, abort_flag, a.b1.status);
+    grid_sync(a.gb, 3, abort_flag, a.b1.status);
     // phase 4: dh, dl, dg += fixed-order sums of the partials
     reduce_partials_run(a.rh, a.rl, a.rg, (int)blockIdx.x, (int)gridDim.x, reinterpret_cast<float *>(smem + kCtlBytes));
     small_teardown(tmem_base);
@@ -163,15 +166,11 @@ size_t small_bwd_smem(size_t stage_bytes) {
 
 cudaError_t launch_small_fwd(const GemmMaps &m1, const GemmMaps &m2, const SmallFwdArgs &a, int grid,
                              cudaStream_t s) {
-    static bool attr_set = false;
     const size_t smem = small_fwd_smem();
-    if (!attr_set) {
-        cudaError_t e = prepare_kernel(blr_small_fwd_kernel, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t pe = prepare_kernel_once(blr_small_fwd_kernel, (int)smem);
+    if (pe != cudaSuccess) return pe;
     trace_before("small_fwd", s);
-    cudaError_t e = cudaMemsetAsync(a.gbar, 0, sizeof(unsigned int), s);
+    cudaError_t e = cudaMemsetAsync(a.gb.gbar, 0, sizeof(unsigned int), s);
     if (e == cudaSuccess) e = launch_coop(blr_small_fwd_kernel, grid, smem, s, m1, m2, a);
     trace_after(s);
     return e;
@@ -180,16 +179,12 @@ cudaError_t launch_small_fwd(const GemmMaps &m1, const GemmMaps &m2, const Small
 template <int GPT>
 static cudaError_t launch_small_bwd_t(const GemmMaps &m1, const GemmMaps &m2, const SmallBwdArgs &a, int grid,
                                       cudaStream_t s) {
-    static bool attr_set = false;
     const size_t smem = small_bwd_smem(stage_dy_smem_bytes(a.sd.d_out, a.stage_tpr, a.stage_nthr));
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
-    if (!attr_set) {
-        cudaError_t e = prepare_kernel(blr_small_bwd_kernel<GPT>, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t pe = prepare_kernel_once(blr_small_bwd_kernel<GPT>, 227 * 1024);
+    if (pe != cudaSuccess) return pe;
     trace_before("small_bwd", s);
-    cudaError_t e = cudaMemsetAsync(a.gbar, 0, sizeof(unsigned int), s);
+    cudaError_t e = cudaMemsetAsync(a.gb.gbar, 0, sizeof(unsigned int), s);
     if (e == cudaSuccess) e = launch_coop(blr_small_bwd_kernel<GPT>, grid, smem, s, m1, m2, a);
     trace_after(s);
     return e;

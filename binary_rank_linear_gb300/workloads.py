@@ -87,6 +87,32 @@ WORKLOADS = {
 }
 
 
+# Steps made of several layers, each with its own seeded inputs: the SwiGLU MLP
+# pair runs the up layer's forward+backward and then the down layer's, and its
+# time is their sum.
+STEPS = {
+    "mlp": ("mlp_up", "mlp_down"),
+}
+STEP_NOTES = {
+    "mlp": "SwiGLU MLP pair: up 4096->12288 and down 12288->4096, both r=1024, M=16384 (8 windows x 2048); "
+           "one step = both layers' forward+backward on their own inputs",
+}
+
+
+def step_layers(name: str, M: int = 0) -> list:
+    """The layers one step of workload ``name`` runs (at ``M`` tokens when given)."""
+    names = STEPS.get(name, (name,))
+    out = []
+    for n in names:
+        w = WORKLOADS[n]
+        out.append(w.with_shape(M=M) if M else w)
+    return out
+
+
+def step_note(name: str) -> str:
+    return STEP_NOTES.get(name, WORKLOADS[name].note if name in WORKLOADS else name)
+
+
 def _l_vector(kind: str, r: int, rng: np.random.Generator) -> np.ndarray:
     i = np.arange(r, dtype=np.float64)
     if kind == "exp1":

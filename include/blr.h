@@ -86,6 +86,15 @@ enum {
  * shape breaks the shape rule. Pure host arithmetic; needs no GPU. */
 BLR_API size_t blr_workspace_bytes(int M, int d_in, int d_out, int r);
 
+/* The library remembers, per workspace address, what the last blr_forward
+ * on it recorded there (its shape and input pointers), so that blr_backward
+ * and blr_sign_grads can refuse a workspace that holds no matching tape. This
+ * record is host memory only; call blr_workspace_release(ws) before freeing a
+ * workspace to drop it (otherwise it is dropped when the library holds more
+ * than 65536 records, oldest first). Never touches the GPU.
+ * Errors: BLR_ERR_ARG for a null pointer. */
+BLR_API int blr_workspace_release(const void *ws);
+
 /* Pack signs into a bitmap (train_mm.rs, test helper `pack_bits`).
  *   src  [rows][r] f32, device.
  *   bits [rows][ceil(r/32)] u32, device, written in full: bit (row, k) is 1
@@ -130,9 +139,10 @@ BLR_API int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *
  *     times s_t = 2^(14 - ceil(log2 max_i |dy_ti h_i|)), and its db.l times
  *     the largest power of two that keeps the L1 bound of db_t.l under 2^15,
  *     which keeps gradients out of the f16 subnormals and never overflows.
- * Errors: as blr_forward, plus BLR_ERR_STATE when no forward of this shape
- *   preceded it on `ws` and BLR_ERR_ARG when gscale is positive but not a
- *   power of two. */
+ * Errors: as blr_forward, plus BLR_ERR_STATE when the last forward on `ws`
+ *   was not of this shape or did not take these same x, bits_u, bits_v, g,
+ *   l and h pointers (or there was none, or blr_workspace_release forgot
+ *   it), and BLR_ERR_ARG when gscale is positive but not a power of two. */
 BLR_API int blr_backward(const float *x, const float *dy,
                  const uint32_t *bits_u, const uint32_t *bits_v,
                  const float *g, const float *l, const float *h,
@@ -290,7 +300,11 @@ BLR_API const char *blr_status_string(int status);
  * returns the number of kernels recorded; blr_trace_read(i, &ms) synchronises
  * on kernel i's end event and returns its name, with its duration in
  * milliseconds in *ms (NULL if i is out of range). The events are created
- * once, on the first blr_trace_begin. Off by default; no effect on results. */
+ * once, on the first blr_trace_begin. Calls made while their stream is being
+ * captured into a CUDA graph put the events into the graph as event-record
+ * nodes: each replay records them again, and blr_trace_read after a replay
+ * reads that replay's durations (the kernel before and after such a node run
+ * without programmatic overlap). Off by default; no effect on results. */
 BLR_API int blr_trace_begin(int capacity);
 BLR_API int blr_trace_end(void);
 BLR_API int blr_trace_count(void);
@@ -315,13 +329,28 @@ BLR_API const char *blr_trace_read(int i, float *ms);
  *    kernels clear what must start at zero. Calls that overlap on the GPU
  *    (other streams, other threads) race on the array: serialise them.
  *  - The tape it leaves is not usable by blr_backward.
- * Errors: as blr_forward; BLR_ERR_WORKSPACE when the shape needs more scratch
- *   than BLR_NOALLOC_SCRATCH_BYTES (roughly M*(2 d_in + 6 r + 2 d_out) bytes
- *   plus the re-laid bitmaps). */
+ *  - Device-side failures (a bounded wait inside a kernel that ran out) are
+ *    recorded in the array's own status word, which the next call clears:
+ *    read it with blr_noalloc_check_status before that call.
+ * Errors: as blr_forward (BLR_ERR_SHAPE, BLR_ERR_ARG, BLR_ERR_ALIGN,
+ *   BLR_ERR_UNSUPPORTED_DEVICE, BLR_ERR_CUDA); BLR_ERR_WORKSPACE when the
+ *   shape needs more scratch than BLR_NOALLOC_SCRATCH_BYTES (roughly
+ *   M*(2 d_in + 6 r + 2 d_out) bytes plus the re-laid bitmaps). */
 BLR_API int blr_forward_noalloc(const float *x, const uint32_t *bits_u, const uint32_t *bits_v,
                                 const float *g, const float *l, const float *h,
                                 float *y, int accumulate_y,
                                 int M, int d_in, int d_out, int r, blr_stream_t stream);
+
+/* Synchronises `stream` and reads the status word of the current device's
+ * blr_forward_noalloc scratch array (the counterpart of blr_check_status for
+ * the entry point that has no caller workspace; the pages have none either).
+ * Returns BLR_OK when the last blr_forward_noalloc on this device recorded
+ * no failure, BLR_ERR_DEVICE_CHECK when it did (code in *device_code when not
+ * NULL, bits as for blr_check_status), BLR_ERR_STATE when no
+ * blr_forward_noalloc has run on this device yet, BLR_ERR_CUDA on a CUDA
+ * error. It copies 4 bytes to the host; it allocates nothing. Blocking; for
+ * tests and diagnostics. */
+BLR_API int blr_noalloc_check_status(blr_stream_t stream, uint32_t *device_code);
 
 #ifdef __cplusplus
 }

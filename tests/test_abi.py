@@ -228,3 +228,21 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         _binding.load()
+
+
+def test_workspace_release_host_only(lib):
+    assert lib.blr_workspace_release(None) == -1  # BLR_ERR_ARG
+    assert lib.blr_workspace_release(ctypes.c_void_p(FAKE)) == 0  # no record: nothing to drop, no GPU touched
+
+
+def test_noalloc_argument_errors(lib):
+    fn = lib.blr_forward_noalloc
+    P, I = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
+    fn.restype = I
+    f = FAKE
+    assert fn(None, f, f, f, f, f, f, 0, 64, 128, 128, 64, None) == -1      # null pointer
+    assert fn(f, f, f, f, f, f, f, 2, 64, 128, 128, 64, None) == -1         # flag not 0/1
+    assert fn(f, f, f, f, f, f, f, 0, 64, 100, 128, 64, None) == -2         # shape rule
+    assert fn(f + 4, f, f, f, f, f, f, 0, 64, 128, 128, 64, None) == -3     # alignment
+    assert fn(f, f, f, f, f, f, f, 0, 65536, 4096, 4096, 1024, None) == -4  # beyond the fixed scratch
