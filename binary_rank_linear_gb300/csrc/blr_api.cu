@@ -230,16 +230,14 @@ void record_tape(const void *ws, Tape t) {
 
 // The tape of `ws` if it was recorded by a forward of this shape on these inputs.
 bool tape_matches(const void *ws, int M, int d_in, int d_out, int r, const void *x, const void *bits_u,
-                  const void *bits_v, const void *g, const void *l, const void *h, Tape *out = nullptr) {
+                  const void *bits_v, const void *g, const void *l, const void *h) {
     std::lock_guard<std::mutex> lk(g_tape_mu);
     auto it = g_tapes.find(ws);
     if (it == g_tapes.end()) return false;
     const Tape &t = it->second;
     if (t.M != M || t.d_in != d_in || t.d_out != d_out || t.r != r) return false;
     if (t.x != x || t.g != g || t.l != l) return false;
-    if ((bits_u && t.bits_u != bits_u) || (bits_v && t.bits_v != bits_v) || (h && t.h != h)) return false;
-    if (out) *out = t;
-    return true;
+    return t.bits_u == bits_u && t.bits_v == bits_v && t.h == h;
 }
 
 void mark_backward_done(const void *ws, float gscale, int stage_blocks) {
@@ -823,9 +821,17 @@ int blr_sign_grads(const float *x, const float *g, const float *l, float *gu, fl
     const Layout L = make_layout(M, d_in, d_out, r);
     const SignLayout SL = make_sign_layout(M, r);
     if (ws_bytes < L.total || sws_bytes < SL.total) return BLR_ERR_WORKSPACE;
+    // the products read only the pass's own staging in `ws` (x.g, dy.h, a.l,
+    // db.l), so the record's shape and backward are what must match here
     Tape tape{};
-    if (!tape_matches(ws, M, d_in, d_out, r, x, nullptr, nullptr, g, l, nullptr, &tape) || !tape.backward_done)
-        return BLR_ERR_STATE;
+    {
+        std::lock_guard<std::mutex> lk(g_tape_mu);
+        auto it = g_tapes.find(ws);
+        if (it == g_tapes.end() || !it->second.backward_done || it->second.M != M || it->second.d_in != d_in ||
+            it->second.d_out != d_out || it->second.r != r)
+            return BLR_ERR_STATE;
+        tape = it->second;
+    }
     int sms;
     int st = device_info(&sms);
     if (st != BLR_OK) return st;

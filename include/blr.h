@@ -199,8 +199,9 @@ BLR_API size_t blr_sign_workspace_bytes(int M, int d_in, int d_out, int r);
  * inside the backward ("with sign"); here they are a separate call after
  * blr_backward on the same workspace `ws`, whose tape it reads: a (forward),
  * and the backward's staged f16 dy.h and db.l with their per-token powers of
- * two. So dy, h and the bitmaps are not arguments; x, g and l must be the
- * ones of that forward/backward pair.
+ * two. So dy, h and the bitmaps are not arguments; x, g and l must hold the
+ * values of that forward/backward pair (the products read only the staging
+ * in `ws`, so other buffers with those values serve as well).
  *  - Operands: the pass's own f16 staging, token-major as it is (the tensor
  *    cores read it as MN-major tiles; nothing is transposed): dy.h with x.g
  *    on the feature side, a.l and db.l on the rank side. With a fixed
