@@ -112,6 +112,17 @@ __global__ void __launch_bounds__(kSxsThreads, 1)
                        extra > 0 ? 0 : stage_blocks);
 }
 
+// Prologue of a pass whose staging runs in its first product: the status
+// word, the stagers' row counters and the two bitmap re-layouts.
+__global__ void __launch_bounds__(256) prep_kernel(SignPrep p0, SignPrep p1, uint32_t *status, unsigned int *cnt,
+                                                   int ncnt) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += gridDim.x * blockDim.x) cnt[i] = 0u;
+    prep_share(p0, p1, blockIdx.x, gridDim.x);
+}
+
 template <int GPT, int THREADS>
 __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
     bwd_prologue_kernel(SignPrep p0, SignPrep p1, StageDyArgs a, int stage_blocks) {
@@ -426,6 +437,21 @@ cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, 
     // at 12288 the 512-thread blocks stay faster, 293 against 310 us)
     if (stage_gpt(a.d_out, 1024) <= 8) return launch_bwd_prologue_t<8, 1024>(p0, p1, a, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prep(SignPrep p0, SignPrep p1, uint32_t *status, unsigned int *cnt, int ncnt, const char *name,
+                        cudaStream_t s) {
+    cudaError_t pe = prepare_kernel_once(prep_kernel, 0);
+    if (pe != cudaSuccess) return pe;
+    const int wave = occupancy_blocks(reinterpret_cast<const void *>(prep_kernel), 256, 0) * current_device_sms();
+    int grid = prep_blocks(p0, 256) + prep_blocks(p1, 256);
+    if (grid < (ncnt + 255) / 256) grid = (ncnt + 255) / 256;
+    if (grid > wave) grid = wave;
+    if (grid < 1) grid = 1;
+    trace_before(name, s);
+    cudaError_t e = launch_k(prep_kernel, dim3(grid), dim3(256), 0, s, p0, p1, status, cnt, ncnt);
+    trace_after(s);
+    return e;
 }
 
 cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaStream_t s) {

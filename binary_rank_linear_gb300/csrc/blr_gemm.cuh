@@ -58,6 +58,8 @@
 
 #include "blr_device.cuh"
 #include "blr_kernels.h"
+#include "blr_stage.cuh"
+#include "blr_stager.cuh"
 
 namespace blr {
 
@@ -87,7 +89,10 @@ static_assert(kNumExpWarps == 4 * kKB, "one expander warp per (lane quarter, 64-
 // a CTA pair each CTA loads its own 128 plane rows and half the tokens, and
 // the peer's MMA warp, idle otherwise, forwards each stage's arrival to the
 // leader (full_p) once the peer's loads have landed.
-template <int EPI, bool PAIR, int BT, bool PLANE = false>
+// STG: 0, the activation operand is staged before the launch; 1 or 2, stager
+// warps after the epilogue warps stage x (a-product) or dy (db-product) inside
+// the kernel (blr_stager.cuh). They use no shared memory beyond the control block.
+template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 struct GemmShape {
     static constexpr int kKBm = PLANE ? 1 : kKB;           // 64-wide blocks per k-step
     static constexpr int kStepKm = kKBm * kBK;             // K per k-step
@@ -104,7 +109,8 @@ struct GemmShape {
     static constexpr int kBitsBytes = PLANE ? kABlock : kKB * kBitsBlock;  // per stage: words or plane tile
     static constexpr int kEW = epi_warps(EPI);             // epilogue warps
     static constexpr int kSplit = kEW / 4;                 // epilogue warps per TMEM lane quarter
-    static constexpr int kThreads = (kEpi0 + kEW) * 32;
+    static constexpr int kStg0 = kEpi0 + kEW;              // first stager warp
+    static constexpr int kThreads = (kEpi0 + kEW + (STG ? kStgWarps : 0)) * 32;
     static constexpr bool kHas16 = EPI != kEpiBwd2;        // f16 output: a.l, c, db.l
     static constexpr bool kHas32 = EPI != kEpiBwd1;        // f32 output: a, y, dx
     static constexpr int kSlot32 = 32 * 32 * 4;            // f32 chunk: input, then output in place
@@ -114,17 +120,23 @@ struct GemmShape {
     // before has read it). dx' streams x in and dx out at HBM rate
     // (plane mode leaves more room to the operand ring, which measured faster
     // than deeper chunk buffering: no input prefetch but for dx')
-    static constexpr int kNE = PLANE ? (EPI == kEpiBwd2 ? 3 : 2)
+    // (with in-kernel staging the stager ring takes 48 KB: the a-product keeps
+    // two chunk slots, measured as fast as four for the forward products, and
+    // the db-product three, one a-tape chunk prefetched)
+    static constexpr int kNE = STG == 1 ? 2 : STG == 2 ? 3
+                             : PLANE ? (EPI == kEpiBwd2 ? 3 : 2)
                                      : (EPI == kEpiBwd2 ? 4 : (kSplit == 2 ? 2 : 4));
     static constexpr int kEpiBytes = kEW * kNE * kSlotBytes;
-    static constexpr int kBudget = (PLANE ? 224 : 221) * 1024 - kEpiBytes;
+    static constexpr int kStgBytes = STG ? kStgRingBytes : 0;
+    static constexpr int kStgSlots = STG == 1 ? kStgSlotsX : STG == 2 ? kStgSlotsDy : 0;
+    static constexpr int kBudget = (PLANE ? 224 : 221) * 1024 - kEpiBytes - kStgBytes;
     static constexpr int kNBRaw = kBudget / (kBBytes + kBitsBytes);
     static constexpr int kNB = kNBRaw > 10 ? 10 : kNBRaw;
     static constexpr int kNSMax = (kTmemCols - 2 * BT) / kSignCols;
     static constexpr int kNS = PLANE ? 0 : (kNSMax < kNB ? kNSMax : kNB);  // sign stages in TMEM
-    static constexpr int kNumBars = 2 * kNB + kNS + 2 + 2 + 1 + kEW * kNE + (PLANE && PAIR ? kNB : 0);
+    static constexpr int kNumBars = 2 * kNB + kNS + 2 + 2 + 1 + kEW * kNE + (PLANE && PAIR ? kNB : 0) + 2 * kStgSlots;
     static_assert(kNE >= 2, "double-buffered chunk staging");
-    static constexpr int kPhaseBytes = kNB * kBBytes + kEpiBytes + kNB * kBitsBytes + kNumBars * 8;
+    static constexpr int kPhaseBytes = kNB * kBBytes + kEpiBytes + kNB * kBitsBytes + kStgBytes + kNumBars * 8;
     static constexpr int kSmemBytes = 1024 + kCtlBytes + kPhaseBytes;  // alignment slack, control block, phase
     static_assert(BT % 32 == 0 && BT >= 32 && BT <= 256 && (!PAIR || BT % 16 == 0), "token tile");
     static_assert(kTokRows % 8 == 0, "activation boxes hold whole 8-row swizzle groups");
@@ -144,22 +156,25 @@ struct GemmShape {
 struct GemmCtl {
     uint32_t tmem_slot;  // TMEM base address written by tcgen05.alloc
     int abort_flag;      // set by any role whose bounded wait ran out
+    StgScratch stg;      // the stager warps' reduction buffers (STG kernels)
 };
 static_assert(sizeof(GemmCtl) <= kCtlBytes, "control block");
 
 // Shared-memory layout of one GEMM phase (from a 1024-aligned base).
-template <int EPI, bool PAIR, int BT, bool PLANE = false>
+template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 struct GemmLayout {
-    using S = GemmShape<EPI, PAIR, BT, PLANE>;
+    using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
     uint8_t *sB;       // [NB][kBBytes] activation tiles
     uint8_t *sE;       // [4 warps][kNE][slot] epilogue chunks
     uint32_t *sBits;   // [NB][2][128][2] bitmap words, or [NB][plane tile] (PLANE)
-    uint64_t *full_b, *empty_b, *full_s, *tmem_full, *tmem_empty, *drain_bar, *eload, *full_p;
+    uint8_t *sStg;     // stager ring (STG)
+    uint64_t *full_b, *empty_b, *full_s, *tmem_full, *tmem_empty, *drain_bar, *eload, *full_p, *stg_full, *stg_empty;
     __device__ explicit GemmLayout(uint8_t *base) {
         sB = base;
         sE = sB + S::kNB * S::kBBytes;
         sBits = reinterpret_cast<uint32_t *>(sE + S::kEpiBytes);
-        full_b = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sBits) + S::kNB * S::kBitsBytes);
+        sStg = reinterpret_cast<uint8_t *>(sBits) + S::kNB * S::kBitsBytes;
+        full_b = reinterpret_cast<uint64_t *>(sStg + S::kStgBytes);
         empty_b = full_b + S::kNB;
         full_s = empty_b + S::kNB;
         tmem_full = full_s + S::kNS;
@@ -167,6 +182,8 @@ struct GemmLayout {
         drain_bar = tmem_empty + 2;
         eload = drain_bar + 1;  // [epilogue warps][kNE]
         full_p = eload + S::kEW * S::kNE;  // [NB] (plane pairs: the peer's stage has landed)
+        stg_full = full_p + (PLANE && PAIR ? S::kNB : 0);  // [stager slots]
+        stg_empty = stg_full + S::kStgSlots;
     }
     // one thread: initialise every barrier of the phase
     __device__ void init_barriers() const {
@@ -183,10 +200,14 @@ struct GemmLayout {
         for (int i = 0; i < S::kEW * S::kNE; ++i) mbar_init(&eload[i], 1);
         if (PLANE && PAIR)
             for (int s = 0; s < S::kNB; ++s) mbar_init(&full_p[s], 1);
+        for (int s = 0; s < S::kStgSlots; ++s) {
+            mbar_init(&stg_full[s], 1);
+            mbar_init(&stg_empty[s], kStgWarps);
+        }
     }
     // one thread, once every role of the phase has finished with the barriers
     __device__ void inval_barriers() const {
-        for (uint64_t *b = full_b; b < eload + S::kEW * S::kNE + (PLANE && PAIR ? S::kNB : 0); ++b) mbar_inval(b);
+        for (uint64_t *b = full_b; b < stg_empty + S::kStgSlots; ++b) mbar_inval(b);
     }
 };
 
@@ -208,13 +229,15 @@ __device__ __forceinline__ uint16_t f16_bits(float v) { return __half_as_ushort(
 // into its TMEM; its epilogue then runs the tile's chunk kj only. For
 // problems with few tiles and long K this cuts both the k-loop and the
 // epilogue a CTA runs by SPLIT.
-template <int EPI, bool PAIR, int BT, bool PLANE = false, int SPLIT = 1>
-__device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE> &L, const CUtensorMap &tmap_act,
+template <int EPI, bool PAIR, int BT, bool PLANE = false, int SPLIT = 1, int STG = 0>
+__device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE, STG> &L, const CUtensorMap &tmap_act,
                                            const CUtensorMap &tmap_in, const CUtensorMap &tmap_out32,
                                            const CUtensorMap &tmap_out16, const GemmArgs &args,
                                            uint32_t tmem_base, volatile int *abort_flag, int unit, int num_units,
-                                           const CUtensorMap *tmap_sgn = nullptr) {
-    using S = GemmShape<EPI, PAIR, BT, PLANE>;
+                                           const CUtensorMap *tmap_sgn = nullptr, StgScratch *stg_scratch = nullptr) {
+    using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
+    static_assert(STG == 0 || (SPLIT == 1 && !PLANE && (STG == 1 ? EPI == kEpiFwd1 : EPI == kEpiBwd1)),
+                  "in-kernel staging: the a-product stages x, the db-product dy");
     constexpr int kKB = S::kKBm, kStepK = S::kStepKm, kWarpEpi0 = S::kEpi0;
     constexpr int NB = S::kNB, NS = S::kNS, kChunks = S::kChunks, kNE = S::kNE;
     uint8_t *sB = L.sB;
@@ -247,6 +270,23 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                 const int t0 = (tile / f_tiles) * BT + (int)rank * S::kTokRows;  // this CTA's token rows
                 const int f0 = (tile % f_tiles) * kUnitF + (int)rank * kFM;      // this CTA's sign rows
                 for (int ks = ks0; ks < ks1; ++ks) {
+                    if constexpr (STG != 0) {
+                        // the stagers publish a tile's rows per column chunk (x) or
+                        // whole (dy): acquire the count before the chunk's loads
+                        constexpr int kChunkSteps = kStgKC / kStepK;
+                        if (ks == ks0 || (STG == 1 && ks % kChunkSteps == 0)) {
+                            const int tt = tile / f_tiles;
+                            const int kc = STG == 1 ? ks / kChunkSteps : 0;
+                            const unsigned int need = (unsigned int)(M - tt * BT < BT ? M - tt * BT : BT);
+                            if (!wait_count(args.stg.cnt + (size_t)tt * stg_chunks(args.K, STG) + kc, need,
+                                            abort_flag)) {
+                                fail_status(args, abort_flag, kStTimeoutStage);
+                                ok = false;
+                                break;
+                            }
+                            fence_proxy_async_global();
+                        }
+                    }
                     if (!mbar_wait(&empty_b[sb], pb ^ 1u, abort_flag)) {
                         fail_status(args, abort_flag, kStTimeoutTma);
                         ok = false;
@@ -613,13 +653,29 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             const int t0 = tt * BT;
             // per-token scales of this warp's chunks (lane l: token 32c + l of
             // the tile), fetched before the accumulator is ready
+            if constexpr (STG == 2) {
+                // written by the stagers of this launch: acquire the tile's count
+                // first, and read them through L2 (not the read-only path)
+                const unsigned int need = (unsigned int)(M - t0 < BT ? M - t0 : BT);
+                const bool got_s = wait_count(args.stg.cnt + tt, need, abort_flag);
+                if (!__all_sync(0xFFFFFFFFu, got_s)) {
+                    if (lane == 0) fail_status(args, abort_flag, kStTimeoutStage);
+                    ok = false;
+                    break;
+                }
+            }
             float ri_t[kMaxNc], rs_t[kMaxNc];
 #pragma unroll
             for (int i = 0; i < kMaxNc; ++i) {
                 const int tl = t0 + 32 * (cb + kSplit * i) + lane;
                 const bool use = i < nc && tl < M;
-                ri_t[i] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && use ? __ldg(args.row_inv + tl) : 0.0f;
-                rs_t[i] = (EPI == kEpiBwd1) && use ? __ldg(args.row_scale + tl) : 0.0f;
+                if constexpr (STG == 2) {
+                    ri_t[i] = use ? __ldcg(args.row_inv + tl) : 0.0f;
+                    rs_t[i] = use ? __ldcg(args.row_scale + tl) : 0.0f;
+                } else {
+                    ri_t[i] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && use ? __ldg(args.row_inv + tl) : 0.0f;
+                    rs_t[i] = (EPI == kEpiBwd1) && use ? __ldg(args.row_scale + tl) : 0.0f;
+                }
             }
             const bool fvalid = f < N;
             const float cf = fvalid ? __ldg(args.colv + f) : 0.0f;
@@ -756,6 +812,16 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                     atomicOr(args.status, kStTimeoutDrain);
         }
         __syncwarp();
+    } else {
+        if constexpr (STG != 0) {
+            // ---- stagers: the activation operand of later tiles ---------------
+            const StgGeom G(M, args.K, BT, f_tiles, num_units, STG);
+            const int t = (int)threadIdx.x - S::kStg0 * 32;
+            if constexpr (STG == 1)
+                stager_x(args.stg, G, t, abort_flag, L.sStg, L.stg_full, L.stg_empty, args.status);
+            else
+                stager_dy(args.stg, G, t, abort_flag, stg_scratch, L.sStg, L.stg_full, L.stg_empty, args.status);
+        }
     }
     if constexpr (SPLIT > 1) {
         // the other roles, done with the tile, pass the epilogue's two cluster barriers
@@ -790,14 +856,14 @@ __device__ __forceinline__ uint8_t *smem_base_1024() {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 }
 
-template <int EPI, bool PAIR, int BT, bool PLANE, int SPLIT>
-__global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE>::kThreads, 1)
+template <int EPI, bool PAIR, int BT, bool PLANE, int SPLIT, int STG>
+__global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads, 1)
     blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ CUtensorMap tmap_in,
                     const __grid_constant__ CUtensorMap tmap_out32, const __grid_constant__ CUtensorMap tmap_out16,
                     const __grid_constant__ CUtensorMap tmap_sgn, const GemmArgs args) {
     uint8_t *smem = smem_base_1024();
     GemmCtl *ctl = reinterpret_cast<GemmCtl *>(smem);
-    const GemmLayout<EPI, PAIR, BT, PLANE> L(smem + kCtlBytes);
+    const GemmLayout<EPI, PAIR, BT, PLANE, STG> L(smem + kCtlBytes);
     const int warp = threadIdx.x / 32;
     if (threadIdx.x == 0) {
         L.init_barriers();
@@ -828,9 +894,9 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE>::kThreads, 1)
     const int per_unit = PAIR ? 2 : SPLIT;
     const int unit = (int)blockIdx.x / per_unit;
     const int num_units = (int)gridDim.x / per_unit;
-    gemm_roles<EPI, PAIR, BT, PLANE, SPLIT>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
-                                            reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units,
-                                            &tmap_sgn);
+    gemm_roles<EPI, PAIR, BT, PLANE, SPLIT, STG>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
+                                                 reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units,
+                                                 &tmap_sgn, &ctl->stg);
     tc_fence_before();
     if constexpr (PAIR) {
         // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it
@@ -844,10 +910,10 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE>::kThreads, 1)
     }
 }
 
-template <int EPI, bool PAIR, int BT, bool PLANE = false, int SPLIT = 1>
+template <int EPI, bool PAIR, int BT, bool PLANE = false, int SPLIT = 1, int STG = 0>
 cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, cudaStream_t s) {
-    using S = GemmShape<EPI, PAIR, BT, PLANE>;
-    cudaError_t pe = prepare_kernel_once(blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT>, S::kSmemBytes);
+    using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
+    cudaError_t pe = prepare_kernel_once(blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT, STG>, S::kSmemBytes);
     if (pe != cudaSuccess) return pe;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -863,12 +929,23 @@ cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (PAIR || SPLIT > 1) ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT>, maps.act, maps.in32, maps.out32,
-                              maps.out16, maps.sgn, args);
+    return cudaLaunchKernelEx(&cfg, blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT, STG>, maps.act, maps.in32,
+                              maps.out32, maps.out16, maps.sgn, args);
 }
 
 // Tile configurations: CTA pairs with 160 or 192 tokens per tile, single CTAs
 // with 128.
+// The same tiles with the activation operand staged inside the kernel.
+template <int EPI, int STG>
+cudaError_t launch_gemm_stg(const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s) {
+    if (plan.pair && plan.bt == 192) return launch_gemm_t<EPI, true, 192, false, 1, STG>(maps, args, plan.grid, s);
+    if (plan.pair && plan.bt == 160) return launch_gemm_t<EPI, true, 160, false, 1, STG>(maps, args, plan.grid, s);
+    if (!plan.pair && plan.bt == 128) return launch_gemm_t<EPI, false, 128, false, 1, STG>(maps, args, plan.grid, s);
+    if (!plan.pair && plan.bt == 64) return launch_gemm_t<EPI, false, 64, false, 1, STG>(maps, args, plan.grid, s);
+    if (!plan.pair && plan.bt == 32) return launch_gemm_t<EPI, false, 32, false, 1, STG>(maps, args, plan.grid, s);
+    return cudaErrorInvalidValue;
+}
+
 template <int EPI>
 cudaError_t launch_gemm_epi(const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s) {
     if (plan.plane) {

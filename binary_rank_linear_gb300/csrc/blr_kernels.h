@@ -72,6 +72,12 @@ struct SignPrep {
 cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
                                 int d_in, uint32_t *status, cudaStream_t s);
 
+// Prologue of a pass whose first product stages its own operand (GemmPlan
+// stg): re-lay two bitmaps, clear the device status word (when `status` is
+// not null: the forward) and zero the stagers' ncnt row counters.
+cudaError_t launch_prep(SignPrep p0, SignPrep p1, uint32_t *status, unsigned int *cnt, int ncnt, const char *name,
+                        cudaStream_t s);
+
 // Backward prologue, two parts in one launch: re-lay two bitmaps, and stage
 // dy16 = f16(dy.h.s_t) with per-token scales, dh partials and sigma_t.
 struct StageDyArgs {
@@ -115,6 +121,34 @@ enum GemmEpi : int { kEpiFwd1 = 0, kEpiFwd2 = 1, kEpiBwd1 = 2, kEpiBwd2 = 3 };
 __host__ __device__ constexpr int epi_warps(int epi) { return epi == kEpiBwd2 ? 8 : 4; }
 __host__ __device__ constexpr int epi_part_rows_per_tile(int epi) { return epi_warps(epi) / 4; }
 
+// In-kernel staging of the a- and db-products' activation operand (GEMM
+// template STG = 1: x16 = f16(x.g); STG = 2: dy16 = f16(dy.h.s_t) with the
+// per-token scales, the dh sums and sigma_t): stager warps of every CTA write
+// the f16 operand ahead of the MMA pipeline, in the order the persistent grid
+// consumes token tiles, and count the rows they finish per (token tile,
+// column chunk) in `cnt`; a tile's loads wait for its count (blr_stager.cuh).
+// Columns per readiness chunk of the in-kernel x staging (two 128-deep
+// k-steps); the host sizes and zeroes the counters with it.
+constexpr int kStageChunkCols = 256;
+inline int stage_counters(int M, int bt, int K, int mode) {
+    return (M + bt - 1) / bt * (mode == 1 ? (K + kStageChunkCols - 1) / kStageChunkCols : 1);
+}
+
+struct StageArgs {
+    const float *src;      // x [M][K] or dy [M][K] f32
+    const float *col;      // g [K] or h [K]
+    uint16_t *dst;         // x16 or dy16 [M][K]
+    unsigned int *cnt;     // [token tiles][column chunks] rows staged (zeroed before the launch)
+    // dy only
+    const uint16_t *c16;   // [M][K] forward c tape
+    const float *l;        // [r]
+    int r;
+    float gscale;          // > 0 fixed, <= 0 dynamic
+    float *s_inv, *sig, *sig_inv;  // [M] out
+    float *part_dh;        // [grid][K] out: one dh partial row per CTA
+    float2 *blkmax;        // [grid] out: per CTA (max 1/s_t, max 1/sigma_t) over rows with a nonzero gradient
+};
+
 struct GemmArgs {
     int M;                   // tokens
     int N;                   // features = rows of the sign operand
@@ -129,6 +163,7 @@ struct GemmArgs {
     float *part;             // BWD1 dl partials, BWD2 dg partials  [token tiles][N]
     int accumulate;          // FWD2 y +=, BWD2 dx +=
     uint32_t *status;        // device status word
+    StageArgs stg;           // in-kernel staging (STG kernels only)
 };
 
 // Rows of the re-laid bitmap of a product with N features (a multiple of the
@@ -156,6 +191,8 @@ struct GemmMaps {
 // bt = 128, 192 or 256); false: bitmap words expanded into TMEM.
 // split = 4: split-K over clusters of four single CTAs (one tile each; the
 // a- and db-products of problems with few tiles), grid = tiles * 4.
+// stg = 1 (a-product) or 2 (db-product): the activation operand is staged
+// inside the kernel (args.stg), not by a pass before it.
 struct GemmPlan {
     bool pair;
     int bt;
@@ -163,6 +200,7 @@ struct GemmPlan {
     int part_rows;
     bool plane;
     int split;
+    int stg;
 };
 
 // TMEM-expansion tiles. Single-CTA token tiles are halved from 128 down to

@@ -28,7 +28,7 @@ inline size_t relaid_bytes(int N, int K) { return (size_t)((K + 127) / 128) * 2 
 // forward pass uses come first (header .. c16, ending at fwd_total), then the
 // backward's and the optional sign planes.
 struct Layout {
-    size_t header, bp_f1, bp_f2, x16, a32, al16, c16, fwd_total;
+    size_t header, bp_f1, bp_f2, x16, a32, al16, c16, stg_cnt, fwd_total;
     size_t bp_b1, bp_b2, dy16, db16, s_inv, sig, sig_inv, blkmax, part_dh, part_dl, part_dg, plane_u, plane_v, total;
     int rows_dh, rows_dl, rows_dg;
 };
@@ -36,6 +36,10 @@ struct Layout {
 // Header words (u32 index): 0 the device status word; 16 the grid-barrier
 // counter of the fused small-M kernels.
 constexpr size_t kGridBarOffset = 64;
+
+// Largest grid of a product that stages its operand in the kernel (one dh
+// partial row per CTA is reserved for it).
+constexpr int kMaxStageGrid = 256;
 
 inline Layout make_layout(int M, int d_in, int d_out, int r) {
     Layout L{};
@@ -55,6 +59,10 @@ inline Layout make_layout(int M, int d_in, int d_out, int r) {
     L.a32 = take(m * r * 4);
     L.al16 = take(m * r * 2);
     L.c16 = take(m * d_out * 2);
+    // row counters of the in-kernel staging: one per (token tile of at least
+    // 32 tokens, column chunk of d_in) in the forward, one per token tile in
+    // the backward
+    L.stg_cnt = take((size_t)stage_counters(M, 32, d_in, 1) * 4);
     L.fwd_total = off;
     // backward: re-laid S_U (N = r, K = d_out) and S_V (N = d_in, K = r); the
     // f16 staging of all four products stays in place after the pass (the
@@ -66,7 +74,9 @@ inline Layout make_layout(int M, int d_in, int d_out, int r) {
     L.s_inv = take(m * 4);
     L.sig = take(m * 4);
     L.sig_inv = take(m * 4);
-    L.rows_dh = stage_dy_blocks(M, d_out);
+    // dh partial rows: one per staging block of the stand-alone staging, or
+    // one per CTA of the db-product when it stages dy itself
+    L.rows_dh = stage_dy_blocks(M, d_out) > kMaxStageGrid ? stage_dy_blocks(M, d_out) : kMaxStageGrid;
     L.blkmax = take((size_t)L.rows_dh * 8);
     // partial rows per token tile (tiles of at least 128 tokens; split-K
     // db-products write one per quarter of K, the token-major dx'-product four

@@ -370,8 +370,10 @@ def test_split_k_integer_grid_bit_exact(monkeypatch):
 @pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 513, 512, 4096, 256),
                                                  ("small", 150, 128, 12288, 64)])
 def test_dy_staging_forms(monkeypatch, name, M, d_in, d_out, r):
-    """The register-staged row kernel (BLR_DY_STAGE=rows) against the oracle on
-    widths the streaming staging takes by default."""
+    """The stand-alone dy staging pass (BLR_STAGE=pass) in its register-staged
+    row form (BLR_DY_STAGE=rows) against the oracle on widths the streaming
+    form takes by default."""
+    monkeypatch.setenv("BLR_STAGE", "pass")
     monkeypatch.setenv("BLR_DY_STAGE", "rows")
     t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     out = _run(t)
@@ -382,8 +384,10 @@ def test_dy_staging_forms(monkeypatch, name, M, d_in, d_out, r):
 @pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 513, 4096, 512, 256),
                                                  ("small", 77, 12288, 256, 64)])
 def test_x_staging_forms(monkeypatch, form, name, M, d_in, d_out, r):
-    """Each x staging form (grid-stride, row-mapped, streamed through the
-    shared-memory ring), forced with BLR_X_STAGE, against the oracle."""
+    """Each form of the stand-alone x staging pass (BLR_STAGE=pass):
+    grid-stride, row-mapped, streamed through the shared-memory ring, forced
+    with BLR_X_STAGE, against the oracle."""
+    monkeypatch.setenv("BLR_STAGE", "pass")
     monkeypatch.setenv("BLR_X_STAGE", form)
     t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     out = _run(t)
@@ -407,3 +411,37 @@ def test_maximum_widths(M, d_in, d_out, r):
     t = wl.make_inputs(wl.WORKLOADS["small"].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     out = _run(t)
     _check_against_oracle(t, out, "(maximum widths)")
+
+
+@pytest.mark.parametrize("stage", ["pass", "kernel"])
+@pytest.mark.parametrize("name,M,d_in,d_out,r", [("small", 300, 320, 448, 96), ("attn", 4600, 1024, 1568, 1280),
+                                                 ("ragged", 2100, 640, 4224, 256), ("small", 1, 64, 64, 64),
+                                                 ("small", 200, 128, 9216, 64), ("attn", 3001, 4096, 2048, 512)])
+@pytest.mark.parametrize("gscale", [0.0, 1024.0])
+def test_stage_forms(monkeypatch, stage, name, M, d_in, d_out, r, gscale):
+    """x and dy staged inside the a- and db-products by their stager warps
+    (default) or by stand-alone passes before them (BLR_STAGE=pass), on
+    single-CTA and CTA-pair tiles, ragged token counts and partial column
+    chunks, against the oracle."""
+    monkeypatch.setenv("BLR_STAGE", stage)
+    t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    if name == "ragged" and gscale > 0:
+        gscale = 2.0 ** 30
+    out = _run(t, gscale=gscale)
+    _check_against_oracle(t, out, f"(BLR_STAGE={stage}, gscale {gscale})")
+
+
+def test_stage_in_kernel_integer_grid_bit_exact(monkeypatch):
+    """With exact operands the in-kernel staging gives the oracle's y and dx bit
+    for bit (pair tiles, several column chunks, a ragged last token tile)."""
+    monkeypatch.setenv("BLR_STAGE", "kernel")
+    M, d_in, d_out, r = 2100, 800, 4096, 160
+    t = _integer_grid(M, d_in, d_out, r, seed=93)
+    out = _run(t, gscale=1.0)
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    fw = oracle.forward(t["x"], bu, bv, t["g"], t["l"], t["h"])
+    bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    assert out["status"] == 0
+    assert np.array_equal(out["y"], fw["y"].astype(np.float32))
+    assert np.array_equal(out["dx"], bw["dx"].astype(np.float32))
+    assert np.array_equal(out["dh"], bw["dh"].astype(np.float32))
