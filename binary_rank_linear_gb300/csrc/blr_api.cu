@@ -588,7 +588,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f2.status = status;
 
     // x staged inside the a-product (not with sign planes or split-K tiles)
-    const bool stg = !fused && !planes && p1.split == 1 && stage_in_kernel();
+    const bool stg = !fused && !planes && p1.split <= 1 && stage_in_kernel();
     if (fused) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallFwdArgs fa{pv, pu, x, g, x16, M, d_in, status,
@@ -773,7 +773,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     }
     // dy staged inside the db-product: its stager warps also form s_t, sigma_t
     // and one dh partial row per CTA
-    if (!planes && p1.split == 1 && stage_in_kernel() && p1.grid <= L.rows_dh) {
+    if (!planes && p1.split <= 1 && stage_in_kernel() && p1.grid <= L.rows_dh) {
         unsigned int *cnt = reinterpret_cast<unsigned int *>(w + L.stg_cnt);
         b1.stg.src = dy;
         b1.stg.col = h;
