@@ -102,15 +102,12 @@ def kernel_work(name: str, M: int, d_in: int, d_out: int, r: int):
         "gemm_bwd1": (2.0 * M * r * d_out, 4.0 * M * r, 2.0 * M * d_out + 2.0 * M * r + relaid_ut + parts),
         "gemm_bwd2": (2.0 * M * r * d_in, 8.0 * M * d_in, 2.0 * M * r + relaid_vd + parts),
         "reduce_partials": (0.0, 8.0 * (d_in + d_out + r), parts),
-        # passes whose staging runs in the first product: the prologue only
-        # re-lays the bitmaps, and the staging product reads x (or dy and c)
-        # itself and writes the f16 operand it then reads
+        # a forward whose x staging runs in the a-product: the prologue only
+        # re-lays the bitmaps, and the staging product reads x itself and
+        # writes the f16 operand it then reads
         "fwd_prep": (0.0, bits_u + bits_v, relaid_u + relaid_v),
         "gemm_fwd1s": (2.0 * M * r * d_in, 4.0 * M * d_in + 4.0 * M * r,
                        4.0 * M * d_in + 2.0 * M * r + relaid_v),
-        "bwd_prep": (0.0, bits_u + bits_v, relaid_ut + relaid_vd),
-        "gemm_bwd1s": (2.0 * M * r * d_out, 6.0 * M * d_out + 4.0 * M * r,
-                       4.0 * M * d_out + 2.0 * M * r + relaid_ut + parts),
     }
     if name == "small_fwd":
         return tuple(sum(table[n][i] for n in ("fwd_prologue", "gemm_fwd1", "gemm_fwd2")) for i in range(3))

@@ -56,15 +56,14 @@ void trace_after(cudaStream_t stream) {
 }
 
 cudaError_t launch_gemm_stg_fwd(const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
-cudaError_t launch_gemm_stg_bwd(const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
 
 cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s) {
     static const char *names[4] = {"gemm_fwd1", "gemm_fwd2", "gemm_bwd1", "gemm_bwd2"};
     if (plan.stg) {
-        // the a- or db-product with its activation operand staged in the kernel
-        if (!((plan.stg == 1 && epi == kEpiFwd1) || (plan.stg == 2 && epi == kEpiBwd1))) return cudaErrorInvalidValue;
-        trace_before(plan.stg == 1 ? "gemm_fwd1s" : "gemm_bwd1s", s);
-        cudaError_t e = plan.stg == 1 ? launch_gemm_stg_fwd(plan, maps, args, s) : launch_gemm_stg_bwd(plan, maps, args, s);
+        // the a-product with x staged in the kernel
+        if (plan.stg != 1 || epi != kEpiFwd1) return cudaErrorInvalidValue;
+        trace_before("gemm_fwd1s", s);
+        cudaError_t e = launch_gemm_stg_fwd(plan, maps, args, s);
         trace_after(s);
         return e;
     }
@@ -400,7 +399,7 @@ bool fused_small_enabled() {
     return v && std::strcmp(v, "fused") == 0;
 }
 
-// Where the a- and db-products' activation operand is staged: inside the
+// Where the a-product's activation operand x16 is staged: inside the
 // product's kernel by its stager warps (default), or by a stand-alone pass
 // before it when BLR_STAGE=pass (the earlier design; kept for comparison).
 bool stage_in_kernel() {
@@ -603,7 +602,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
         f1.stg.cnt = cnt;
         GemmPlan ps = p1;
         ps.stg = 1;
-        const int ncnt = stage_counters(M, p1.bt, d_in, 1);
+        const int ncnt = stage_counters(M, p1.bt, d_in);
         if (launch_prep(pv, pu, status, cnt, ncnt, "fwd_prep", s) != cudaSuccess) return BLR_ERR_CUDA;
         if (launch_gemm(kEpiFwd1, ps, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
         if (dense2) {
@@ -771,33 +770,8 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
         mark_backward_done(ws, gscale, rows_dh);
         return BLR_OK;
     }
-    // dy staged inside the db-product: its stager warps also form s_t, sigma_t
-    // and one dh partial row per CTA
-    if (!planes && p1.split <= 1 && stage_in_kernel() && p1.grid <= L.rows_dh) {
-        unsigned int *cnt = reinterpret_cast<unsigned int *>(w + L.stg_cnt);
-        b1.stg.src = dy;
-        b1.stg.col = h;
-        b1.stg.dst = dy16;
-        b1.stg.cnt = cnt;
-        b1.stg.c16 = c16;
-        b1.stg.l = l;
-        b1.stg.r = r;
-        b1.stg.gscale = gscale;
-        b1.stg.s_inv = s_inv;
-        b1.stg.sig = sig;
-        b1.stg.sig_inv = sig_inv;
-        b1.stg.part_dh = part_dh;
-        b1.stg.blkmax = sa.blkmax;
-        GemmPlan ps = p1;
-        ps.stg = 2;
-        if (launch_prep(pu, pv, nullptr, cnt, stage_counters(M, p1.bt, d_out, 2), "bwd_prep", s) != cudaSuccess)
-            return BLR_ERR_CUDA;
-        if (launch_gemm(kEpiBwd1, ps, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
-        rows_dh = p1.grid;
-    } else {
-        if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
-        if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
-    }
+    if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
     if (dense2) {
         if (launch_dense_gemm(d2, "gemm_bwd2", s) != cudaSuccess) return BLR_ERR_CUDA;
     } else if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) {

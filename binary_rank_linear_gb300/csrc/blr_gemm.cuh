@@ -89,9 +89,9 @@ static_assert(kNumExpWarps == 4 * kKB, "one expander warp per (lane quarter, 64-
 // a CTA pair each CTA loads its own 128 plane rows and half the tokens, and
 // the peer's MMA warp, idle otherwise, forwards each stage's arrival to the
 // leader (full_p) once the peer's loads have landed.
-// STG: 0, the activation operand is staged before the launch; 1 or 2, stager
-// warps after the epilogue warps stage x (a-product) or dy (db-product) inside
-// the kernel (blr_stager.cuh). They use no shared memory beyond the control block.
+// STG: 0, the activation operand is staged before the launch; 1, stager
+// warps after the epilogue warps stage x inside the a-product's kernel
+// (blr_stager.cuh), with a 48 KB ring of their own.
 template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 struct GemmShape {
     static constexpr int kKBm = PLANE ? 1 : kKB;           // 64-wide blocks per k-step
@@ -121,14 +121,13 @@ struct GemmShape {
     // (plane mode leaves more room to the operand ring, which measured faster
     // than deeper chunk buffering: no input prefetch but for dx')
     // (with in-kernel staging the stager ring takes 48 KB: the a-product keeps
-    // two chunk slots, measured as fast as four for the forward products, and
-    // the db-product three, one a-tape chunk prefetched)
-    static constexpr int kNE = STG == 1 ? 2 : STG == 2 ? 3
+    // two chunk slots, measured as fast as four for the forward products)
+    static constexpr int kNE = STG ? 2
                              : PLANE ? (EPI == kEpiBwd2 ? 3 : 2)
                                      : (EPI == kEpiBwd2 ? 4 : (kSplit == 2 ? 2 : 4));
     static constexpr int kEpiBytes = kEW * kNE * kSlotBytes;
     static constexpr int kStgBytes = STG ? kStgRingBytes : 0;
-    static constexpr int kStgSlots = STG == 1 ? kStgSlotsX : STG == 2 ? kStgSlotsDy : 0;
+    static constexpr int kStgSlots = STG ? kStgSlotsX : 0;
     static constexpr int kBudget = (PLANE ? 224 : 221) * 1024 - kEpiBytes - kStgBytes;
     static constexpr int kNBRaw = kBudget / (kBBytes + kBitsBytes);
     static constexpr int kNB = kNBRaw > 10 ? 10 : kNBRaw;
@@ -156,7 +155,6 @@ struct GemmShape {
 struct GemmCtl {
     uint32_t tmem_slot;  // TMEM base address written by tcgen05.alloc
     int abort_flag;      // set by any role whose bounded wait ran out
-    StgScratch stg;      // the stager warps' reduction buffers (STG kernels)
 };
 static_assert(sizeof(GemmCtl) <= kCtlBytes, "control block");
 
@@ -234,10 +232,10 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                                            const CUtensorMap &tmap_in, const CUtensorMap &tmap_out32,
                                            const CUtensorMap &tmap_out16, const GemmArgs &args,
                                            uint32_t tmem_base, volatile int *abort_flag, int unit, int num_units,
-                                           const CUtensorMap *tmap_sgn = nullptr, StgScratch *stg_scratch = nullptr) {
+                                           const CUtensorMap *tmap_sgn = nullptr) {
     using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
-    static_assert(STG == 0 || (SPLIT == 1 && !PLANE && (STG == 1 ? EPI == kEpiFwd1 : EPI == kEpiBwd1)),
-                  "in-kernel staging: the a-product stages x, the db-product dy");
+    static_assert(STG == 0 || (STG == 1 && SPLIT == 1 && !PLANE && EPI == kEpiFwd1),
+                  "in-kernel staging: the a-product stages x");
     constexpr int kKB = S::kKBm, kStepK = S::kStepKm, kWarpEpi0 = S::kEpi0;
     constexpr int NB = S::kNB, NS = S::kNS, kChunks = S::kChunks, kNE = S::kNE;
     uint8_t *sB = L.sB;
@@ -271,14 +269,14 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                 const int f0 = (tile % f_tiles) * kUnitF + (int)rank * kFM;      // this CTA's sign rows
                 for (int ks = ks0; ks < ks1; ++ks) {
                     if constexpr (STG != 0) {
-                        // the stagers publish a tile's rows per column chunk (x) or
-                        // whole (dy): acquire the count before the chunk's loads
+                        // the stagers publish a tile's rows per column chunk:
+                        // acquire the count before the chunk's loads
                         constexpr int kChunkSteps = kStgKC / kStepK;
-                        if (ks == ks0 || (STG == 1 && ks % kChunkSteps == 0)) {
+                        if (ks % kChunkSteps == 0) {
                             const int tt = tile / f_tiles;
-                            const int kc = STG == 1 ? ks / kChunkSteps : 0;
+                            const int kc = ks / kChunkSteps;
                             const unsigned int need = (unsigned int)(M - tt * BT < BT ? M - tt * BT : BT);
-                            if (!wait_count(args.stg.cnt + (size_t)tt * stg_chunks(args.K, STG) + kc, need,
+                            if (!wait_count(args.stg.cnt + (size_t)tt * stg_chunks(args.K) + kc, need,
                                             abort_flag)) {
                                 fail_status(args, abort_flag, kStTimeoutStage);
                                 ok = false;
@@ -653,29 +651,13 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             const int t0 = tt * BT;
             // per-token scales of this warp's chunks (lane l: token 32c + l of
             // the tile), fetched before the accumulator is ready
-            if constexpr (STG == 2) {
-                // written by the stagers of this launch: acquire the tile's count
-                // first, and read them through L2 (not the read-only path)
-                const unsigned int need = (unsigned int)(M - t0 < BT ? M - t0 : BT);
-                const bool got_s = wait_count(args.stg.cnt + tt, need, abort_flag);
-                if (!__all_sync(0xFFFFFFFFu, got_s)) {
-                    if (lane == 0) fail_status(args, abort_flag, kStTimeoutStage);
-                    ok = false;
-                    break;
-                }
-            }
             float ri_t[kMaxNc], rs_t[kMaxNc];
 #pragma unroll
             for (int i = 0; i < kMaxNc; ++i) {
                 const int tl = t0 + 32 * (cb + kSplit * i) + lane;
                 const bool use = i < nc && tl < M;
-                if constexpr (STG == 2) {
-                    ri_t[i] = use ? __ldcg(args.row_inv + tl) : 0.0f;
-                    rs_t[i] = use ? __ldcg(args.row_scale + tl) : 0.0f;
-                } else {
-                    ri_t[i] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && use ? __ldg(args.row_inv + tl) : 0.0f;
-                    rs_t[i] = (EPI == kEpiBwd1) && use ? __ldg(args.row_scale + tl) : 0.0f;
-                }
+                ri_t[i] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && use ? __ldg(args.row_inv + tl) : 0.0f;
+                rs_t[i] = (EPI == kEpiBwd1) && use ? __ldg(args.row_scale + tl) : 0.0f;
             }
             const bool fvalid = f < N;
             const float cf = fvalid ? __ldg(args.colv + f) : 0.0f;
@@ -814,13 +796,10 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         __syncwarp();
     } else {
         if constexpr (STG != 0) {
-            // ---- stagers: the activation operand of later tiles ---------------
-            const StgGeom G(M, args.K, BT, f_tiles, num_units, STG);
-            const int t = (int)threadIdx.x - S::kStg0 * 32;
-            if constexpr (STG == 1)
-                stager_x(args.stg, G, t, abort_flag, L.sStg, L.stg_full, L.stg_empty, args.status);
-            else
-                stager_dy(args.stg, G, t, abort_flag, stg_scratch, L.sStg, L.stg_full, L.stg_empty, args.status);
+            // ---- stagers: x16 of later tiles -----------------------------------
+            const StgGeom G(M, args.K, BT, f_tiles, num_units);
+            stager_x(args.stg, G, (int)threadIdx.x - S::kStg0 * 32, abort_flag, L.sStg, L.stg_full, L.stg_empty,
+                     args.status);
         }
     }
     if constexpr (SPLIT > 1) {
@@ -896,7 +875,7 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads
     const int num_units = (int)gridDim.x / per_unit;
     gemm_roles<EPI, PAIR, BT, PLANE, SPLIT, STG>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
                                                  reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units,
-                                                 &tmap_sgn, &ctl->stg);
+                                                 &tmap_sgn);
     tc_fence_before();
     if constexpr (PAIR) {
         // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it

@@ -121,32 +121,23 @@ enum GemmEpi : int { kEpiFwd1 = 0, kEpiFwd2 = 1, kEpiBwd1 = 2, kEpiBwd2 = 3 };
 __host__ __device__ constexpr int epi_warps(int epi) { return epi == kEpiBwd2 ? 8 : 4; }
 __host__ __device__ constexpr int epi_part_rows_per_tile(int epi) { return epi_warps(epi) / 4; }
 
-// In-kernel staging of the a- and db-products' activation operand (GEMM
-// template STG = 1: x16 = f16(x.g); STG = 2: dy16 = f16(dy.h.s_t) with the
-// per-token scales, the dh sums and sigma_t): stager warps of every CTA write
-// the f16 operand ahead of the MMA pipeline, in the order the persistent grid
-// consumes token tiles, and count the rows they finish per (token tile,
-// column chunk) in `cnt`; a tile's loads wait for its count (blr_stager.cuh).
-// Columns per readiness chunk of the in-kernel x staging (two 128-deep
-// k-steps); the host sizes and zeroes the counters with it.
+// In-kernel staging of the a-product's activation operand (GEMM template
+// STG = 1: x16 = f16(x.g)): stager warps of every CTA write the f16 operand
+// ahead of the MMA pipeline, in the order the persistent grid consumes token
+// tiles, and count the rows they finish per (token tile, column chunk) in
+// `cnt`; a tile's loads wait for its counts (blr_stager.cuh).
+// Columns per readiness chunk (two 128-deep k-steps); the host sizes and
+// zeroes the counters with it.
 constexpr int kStageChunkCols = 256;
-inline int stage_counters(int M, int bt, int K, int mode) {
-    return (M + bt - 1) / bt * (mode == 1 ? (K + kStageChunkCols - 1) / kStageChunkCols : 1);
+inline int stage_counters(int M, int bt, int K) {
+    return (M + bt - 1) / bt * ((K + kStageChunkCols - 1) / kStageChunkCols);
 }
 
 struct StageArgs {
-    const float *src;      // x [M][K] or dy [M][K] f32
-    const float *col;      // g [K] or h [K]
-    uint16_t *dst;         // x16 or dy16 [M][K]
+    const float *src;      // x [M][K] f32
+    const float *col;      // g [K]
+    uint16_t *dst;         // x16 [M][K]
     unsigned int *cnt;     // [token tiles][column chunks] rows staged (zeroed before the launch)
-    // dy only
-    const uint16_t *c16;   // [M][K] forward c tape
-    const float *l;        // [r]
-    int r;
-    float gscale;          // > 0 fixed, <= 0 dynamic
-    float *s_inv, *sig, *sig_inv;  // [M] out
-    float *part_dh;        // [grid][K] out: one dh partial row per CTA
-    float2 *blkmax;        // [grid] out: per CTA (max 1/s_t, max 1/sigma_t) over rows with a nonzero gradient
 };
 
 struct GemmArgs {
@@ -191,8 +182,8 @@ struct GemmMaps {
 // bt = 128, 192 or 256); false: bitmap words expanded into TMEM.
 // split = 4: split-K over clusters of four single CTAs (one tile each; the
 // a- and db-products of problems with few tiles), grid = tiles * 4.
-// stg = 1 (a-product) or 2 (db-product): the activation operand is staged
-// inside the kernel (args.stg), not by a pass before it.
+// stg = 1 (a-product only): the activation operand is staged inside the
+// kernel (args.stg), not by a pass before it.
 struct GemmPlan {
     bool pair;
     int bt;

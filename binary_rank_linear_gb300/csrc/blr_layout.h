@@ -37,9 +37,6 @@ struct Layout {
 // counter of the fused small-M kernels.
 constexpr size_t kGridBarOffset = 64;
 
-// Largest grid of a product that stages its operand in the kernel (one dh
-// partial row per CTA is reserved for it).
-constexpr int kMaxStageGrid = 256;
 
 inline Layout make_layout(int M, int d_in, int d_out, int r) {
     Layout L{};
@@ -59,10 +56,9 @@ inline Layout make_layout(int M, int d_in, int d_out, int r) {
     L.a32 = take(m * r * 4);
     L.al16 = take(m * r * 2);
     L.c16 = take(m * d_out * 2);
-    // row counters of the in-kernel staging: one per (token tile of at least
-    // 32 tokens, column chunk of d_in) in the forward, one per token tile in
-    // the backward
-    L.stg_cnt = take((size_t)stage_counters(M, 32, d_in, 1) * 4);
+    // row counters of the in-kernel x staging: one per (token tile of at
+    // least 32 tokens, column chunk of d_in)
+    L.stg_cnt = take((size_t)stage_counters(M, 32, d_in) * 4);
     L.fwd_total = off;
     // backward: re-laid S_U (N = r, K = d_out) and S_V (N = d_in, K = r); the
     // f16 staging of all four products stays in place after the pass (the
@@ -74,9 +70,7 @@ inline Layout make_layout(int M, int d_in, int d_out, int r) {
     L.s_inv = take(m * 4);
     L.sig = take(m * 4);
     L.sig_inv = take(m * 4);
-    // dh partial rows: one per staging block of the stand-alone staging, or
-    // one per CTA of the db-product when it stages dy itself
-    L.rows_dh = stage_dy_blocks(M, d_out) > kMaxStageGrid ? stage_dy_blocks(M, d_out) : kMaxStageGrid;
+    L.rows_dh = stage_dy_blocks(M, d_out);
     L.blkmax = take((size_t)L.rows_dh * 8);
     // partial rows per token tile (tiles of at least 128 tokens; split-K
     // db-products write one per quarter of K, the token-major dx'-product four
