@@ -137,6 +137,20 @@ bool make_tmap_act16(CUtensorMap *m, const void *base, int rows, int K, int box_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// x f32 [rows][cols] with a 256 x 16 box, no swizzle: the in-kernel x
+// staging's ring units (rows and columns past the extent read zero).
+bool make_tmap_x_stage(CUtensorMap *m, const void *base, int rows, int cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    cuuint32_t box[2] = {(cuuint32_t)kStageChunkCols, 16};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [rows][cols] f32 or f16 with a 32 x 32 box, no swizzle: the epilogue's
 // chunks (32 tokens x 32 features); loads read zeros out of range and stores
 // are clipped to it.
@@ -602,6 +616,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
         f1.stg.cnt = cnt;
         GemmPlan ps = p1;
         ps.stg = 1;
+        if (!make_tmap_x_stage(&m1.in32, x, M, d_in)) return BLR_ERR_CUDA;  // the a-product has no other input map
         const int ncnt = stage_counters(M, p1.bt, d_in);
         if (launch_prep(pv, pu, status, cnt, ncnt, "fwd_prep", s) != cudaSuccess) return BLR_ERR_CUDA;
         if (launch_gemm(kEpiFwd1, ps, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;

@@ -271,6 +271,15 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t byte
                  : "memory");
 }
 
+// Asynchronous L2 prefetch of one box of a tiled tensor (coordinates as in
+// tma_load_2d); nothing waits for it.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

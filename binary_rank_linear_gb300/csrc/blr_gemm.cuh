@@ -798,8 +798,9 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         if constexpr (STG != 0) {
             // ---- stagers: x16 of later tiles -----------------------------------
             const StgGeom G(M, args.K, BT, f_tiles, num_units);
-            stager_x(args.stg, G, (int)threadIdx.x - S::kStg0 * 32, abort_flag, L.sStg, L.stg_full, L.stg_empty,
-                     args.status);
+            // (the a-product has no epilogue input: its input map is x, f32, 256 x 16 boxes)
+            stager_x(args.stg, &tmap_in, G, (int)threadIdx.x - S::kStg0 * 32, abort_flag, L.sStg, L.stg_full,
+                     L.stg_empty, args.status);
         }
     }
     if constexpr (SPLIT > 1) {
@@ -813,18 +814,18 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
 }
 
 // Prefetch of a phase's tensor-map descriptors (TMA and epilogue lanes).
-template <int EPI, bool PAIR, int BT, bool PLANE = false>
+template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 __device__ __forceinline__ void gemm_prefetch_maps(const CUtensorMap &tmap_act, const CUtensorMap &tmap_in,
                                                    const CUtensorMap &tmap_out32, const CUtensorMap &tmap_out16,
                                                    const CUtensorMap *tmap_sgn = nullptr) {
-    using S = GemmShape<EPI, PAIR, BT, PLANE>;
+    using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     if (warp == kWarpTma && lane == 0) {
         tma_prefetch_desc(&tmap_act);
         if (PLANE) tma_prefetch_desc(tmap_sgn);
     }
     if (warp == S::kEpi0 && lane == 0) {
-        if (EPI != kEpiFwd1) tma_prefetch_desc(&tmap_in);
+        if (EPI != kEpiFwd1 || S::kStgSlots) tma_prefetch_desc(&tmap_in);
         if (S::kHas32) tma_prefetch_desc(&tmap_out32);
         if (S::kHas16) tma_prefetch_desc(&tmap_out16);
     }
@@ -849,7 +850,7 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads
         ctl->abort_flag = 0;
         fence_mbar_init();
     }
-    gemm_prefetch_maps<EPI, PAIR, BT, PLANE>(tmap_act, tmap_in, tmap_out32, tmap_out16, &tmap_sgn);
+    gemm_prefetch_maps<EPI, PAIR, BT, PLANE, STG>(tmap_act, tmap_in, tmap_out32, tmap_out16, &tmap_sgn);
     if constexpr (PAIR) {
         cluster_sync();  // both CTAs' barriers exist before any remote arrival
         if (warp == kWarpMma) {

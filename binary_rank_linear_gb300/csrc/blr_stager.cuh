@@ -11,11 +11,13 @@
 //    token tiles whose feature tiles the units start together), then column
 //    chunk by column chunk, then token tile and row group. CTA c stages
 //    items c, c + grid, c + 2 grid, ...
-//  - Stager thread 0 bulk-copies the items' f32 row segments into a 48 KB
-//    shared-memory ring (cp.async.bulk, full/empty mbarriers) several units
-//    ahead, and asks L2 to prefetch the units after those; the 64 stager
-//    threads convert from shared memory and write f16 with plain 8-byte
-//    stores, so the staged tiles sit in L2 when the product's TMA loads come.
+//  - Stager thread 0 loads the items' f32 tiles into a 48 KB shared-memory
+//    ring by TMA (one 256 x 16 box per unit, full/empty mbarriers) several
+//    units ahead, and asks L2 to prefetch the boxes after those; the 64
+//    stager threads convert from shared memory and write f16 with plain
+//    8-byte stores, so the staged tiles sit in L2 when the product's TMA
+//    loads come. (Measured on GB300: with one 1 KB bulk copy and one L2
+//    prefetch per row, issuing them took two thirds of thread 0's time.)
 //  - After an item, the stagers publish its rows on the counter of its
 //    (token tile, column chunk): stores, a proxy fence (the consumer reads by
 //    TMA), a barrier of the stager warps, then one release add. The TMA
@@ -48,13 +50,14 @@ constexpr int kStgBar = 8;          // named barrier of the stager warps (0 is _
 constexpr int kStgKC = kStageChunkCols;  // columns per chunk: one float4 per stager thread
 constexpr int kStgRingBytes = 48 * 1024;
 constexpr int kStgSlotsMax = 8;
-// items of 64 rows x 256 columns, ring units of 8 rows (8 KB f32)
+// items of 64 rows x 256 columns, ring units of 16 rows (16 KB f32, one TMA
+// box: x is read through a tensor map with a 256 x 16 box)
 constexpr int kStgRowsX = 64;
-constexpr int kStgUnitRows = 8;
+constexpr int kStgUnitRows = 16;
 constexpr int kStgUnitsX = kStgRowsX / kStgUnitRows;
 constexpr int kStgSlotX = kStgUnitRows * kStgKC * 4;
 constexpr int kStgSlotsX = kStgRingBytes / kStgSlotX;
-constexpr int kStgPrefetchUnits = 8;  // units prefetched into L2 beyond those in the ring
+constexpr int kStgPrefetchUnits = 6;  // units prefetched into L2 beyond those in the ring
 static_assert(kStgSlotsX >= 2 && kStgSlotsX <= kStgSlotsMax, "stager ring");
 
 __host__ __device__ constexpr int stg_chunks(int K) { return (K + kStgKC - 1) / kStgKC; }
@@ -176,8 +179,9 @@ __device__ __forceinline__ void x_cursor_next(XCursor &c, const StgGeom &G, long
     }
 }
 
-__device__ inline void stager_x(const StageArgs &a, const StgGeom &G, int t, volatile int *abort_flag,
-                                uint8_t *ring, uint64_t *full, uint64_t *empty, uint32_t *status) {
+__device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, const StgGeom &G, int t,
+                                volatile int *abort_flag, uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                uint32_t *status) {
     const int cta = blockIdx.x, nctas = gridDim.x;
     const long long n = G.items();
     const long long mine = cta < n ? (n - cta + nctas - 1) / nctas : 0;  // this CTA's items: cta + j grid
@@ -199,10 +203,9 @@ __device__ inline void stager_x(const StageArgs &a, const StgGeom &G, int t, vol
         if (u >= S && !mbar_wait(&empty[sl], (uint32_t)(((u / S) - 1) & 1), abort_flag)) return false;
         int q0, nq;
         unit_rows(ci, q0, nq);
-        mbar_arrive_expect_tx(&full[sl], (uint32_t)(nq * ci.w * 4));
-        for (int q = 0; q < nq; ++q)
-            bulk_load_hint(ring + sl * kStgSlotX + q * kStgKC * 4, a.src + (size_t)(q0 + q) * G.K + ci.c0,
-                           (uint32_t)ci.w * 4, &full[sl], once);
+        // one box of 256 columns x 16 rows (rows and columns past x read zero)
+        mbar_arrive_expect_tx(&full[sl], (uint32_t)kStgSlotX);
+        tma_load_2d_hint(ring + sl * kStgSlotX, tmap_x, &full[sl], ci.c0, q0, once);
         ++u_iss;
         x_cursor_next(ci, G, mine, cta, nctas);
         return true;
@@ -211,7 +214,7 @@ __device__ inline void stager_x(const StageArgs &a, const StgGeom &G, int t, vol
         for (; u_pf < upto && u_pf < units; ++u_pf) {
             int q0, nq;
             unit_rows(cp, q0, nq);
-            for (int q = 0; q < nq; ++q) bulk_prefetch_l2(a.src + (size_t)(q0 + q) * G.K + cp.c0, (uint32_t)cp.w * 4);
+            if (nq > 0) tma_prefetch_l2_2d(tmap_x, cp.c0, q0);
             x_cursor_next(cp, G, mine, cta, nctas);
         }
     };
