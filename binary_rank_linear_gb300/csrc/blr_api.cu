@@ -601,7 +601,8 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f2.status = status;
 
     // x staged inside the a-product (not with sign planes or split-K tiles)
-    const bool stg = !fused && !planes && p1.split <= 1 && stage_in_kernel();
+    const bool stg = !fused && !planes && p1.split <= 1 && stage_in_kernel() &&
+                     stage_fits(M, p1.bt, d_in, (r + (p1.pair ? 255 : 127)) / (p1.pair ? 256 : 128));
     if (fused) {
         // small problem: the whole pass as one fused cooperative kernel
         SmallFwdArgs fa{pv, pu, x, g, x16, M, d_in, status,

@@ -132,6 +132,13 @@ constexpr int kStageChunkCols = 256;
 inline int stage_counters(int M, int bt, int K) {
     return (M + bt - 1) / bt * ((K + kStageChunkCols - 1) / kStageChunkCols);
 }
+// The stagers index items and rounds in 32-bit arithmetic: stage in the
+// kernel only while token tiles x (feature tiles + column chunks x 3 row
+// groups) stays below 2^31 (beyond any x that fits on the device).
+inline bool stage_fits(int M, int bt, int K, int f_tiles) {
+    const long long t = (M + bt - 1) / bt;
+    return t * ((long long)f_tiles + 3ll * ((K + kStageChunkCols - 1) / kStageChunkCols)) < (1ll << 31);
+}
 
 struct StageArgs {
     const float *src;      // x [M][K] f32

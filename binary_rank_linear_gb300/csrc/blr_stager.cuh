@@ -61,7 +61,7 @@ constexpr int kStgPrefetchUnits = 6;  // units prefetched into L2 beyond those i
 static_assert(kStgSlotsX >= 2 && kStgSlotsX <= kStgSlotsMax, "stager ring");
 
 __host__ __device__ constexpr int stg_chunks(int K) { return (K + kStgKC - 1) / kStgKC; }
-static_assert(kStgKC == 4 * kStgThreads, "a chunk is one float4 per stager thread");
+static_assert(kStgKC == 8 * 32, "a chunk row is eight columns per lane of a stager warp");
 
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
     unsigned int v;
@@ -93,51 +93,57 @@ __device__ __forceinline__ bool wait_count(const unsigned int *cnt, unsigned int
     }
 }
 
-// Consumption order of the persistent GEMM grid and the stager items.
+// Consumption order of the persistent GEMM grid and the stager items (32-bit
+// arithmetic: the host stages in the kernel only while the item count and
+// token tiles x feature tiles stay below 2^31, see stage_fits).
 struct StgGeom {
-    int M, K, BT, t_tiles, f_tiles, units, n_kc, R, n_rg;
+    unsigned M, K, BT, t_tiles, f_tiles, units, n_kc, R, n_rg;
 
     __device__ StgGeom(int M_, int K_, int BT_, int f_tiles_, int units_)
         : M(M_), K(K_), BT(BT_), t_tiles((M_ + BT_ - 1) / BT_), f_tiles(f_tiles_), units(units_),
-          n_kc(stg_chunks(K_)), R(kStgRowsX), n_rg((BT_ + R - 1) / R) {}
+          n_kc(stg_chunks(K_)), R(kStgRowsX), n_rg((BT_ + kStgRowsX - 1) / kStgRowsX) {}
     // round of a token tile: the units start tiles u, u + units, ... with the
     // feature tile varying fastest, so token tile tt first appears in round
     // floor(tt * f_tiles / units)
-    __device__ int round_of(int tt) const { return (int)(((long long)tt * f_tiles) / units); }
+    __device__ unsigned round_of(unsigned tt) const { return tt * f_tiles / units; }
     // first token tile of round r: ceil(r * units / f_tiles)
-    __device__ int tt_begin(int r) const {
-        const long long v = ((long long)r * units + f_tiles - 1) / f_tiles;
-        return v < t_tiles ? (int)v : t_tiles;
+    __device__ unsigned tt_begin(unsigned r) const {
+        const unsigned v = (r * units + f_tiles - 1) / f_tiles;
+        return v < t_tiles ? v : t_tiles;
     }
-    __device__ long long items() const { return (long long)t_tiles * n_kc * n_rg; }
+    __device__ unsigned items() const { return t_tiles * n_kc * n_rg; }
     // item i -> (token tile, column chunk, row group); rounds partition the
     // token tiles in order, so the items before round r are tt_begin(r) * n_kc * n_rg
-    __device__ void item(long long i, int &tt, int &kc, int &rg) const {
-        const long long P = (long long)n_kc * n_rg;
-        const int r = round_of((int)(i / P));
-        const int lo = tt_begin(r), hi = tt_begin(r + 1);
-        const long long ii = i - (long long)lo * P;
-        const long long per_kc = (long long)(hi - lo) * n_rg;
+    __device__ void item(unsigned i, int &tt, int &kc, int &rg) const {
+        const unsigned P = n_kc * n_rg;
+        const unsigned r = round_of(i / P);
+        const unsigned lo = tt_begin(r), hi = tt_begin(r + 1);
+        const unsigned ii = i - lo * P;
+        const unsigned per_kc = (hi - lo) * n_rg;
         kc = (int)(ii / per_kc);
-        const long long rem = ii - (long long)kc * per_kc;
-        tt = lo + (int)(rem / n_rg);
+        const unsigned rem = ii - (unsigned)kc * per_kc;
+        tt = (int)(lo + rem / n_rg);
         rg = (int)(rem % n_rg);
     }
     // first row and row count of an item
     __device__ void rows(int tt, int rg, int &r0, int &nr) const {
-        r0 = tt * BT + rg * R;
-        int r1 = r0 + R;
-        if (r1 > tt * BT + BT) r1 = tt * BT + BT;
-        if (r1 > M) r1 = M;
+        r0 = tt * (int)BT + rg * (int)R;
+        int r1 = r0 + (int)R;
+        if (r1 > tt * (int)BT + (int)BT) r1 = tt * (int)BT + (int)BT;
+        if (r1 > (int)M) r1 = (int)M;
         nr = r1 > r0 ? r1 - r0 : 0;
     }
 };
 
-__device__ __forceinline__ uint2 pack4_f16(float4 v, float4 f, float s) {
-    uint2 o;
-    o.x = pack_half2(v.x * f.x * s, v.y * f.y * s);
-    o.y = pack_half2(v.z * f.z * s, v.w * f.w * s);
-    return o;
+// f16 bits of (a * b) for two f32 pairs: one paired multiply (mul.rn.f32x2,
+// each product rounded as by a plain f32 multiply) and one packed conversion
+// (round to nearest even).
+__device__ __forceinline__ uint32_t mul_pack_half2(float a0, float a1, float b0, float b1) {
+    unsigned long long a = ((unsigned long long)__float_as_uint(a1) << 32) | __float_as_uint(a0);
+    unsigned long long b = ((unsigned long long)__float_as_uint(b1) << 32) | __float_as_uint(b0);
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return pack_half2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
 }
 
 // Thread 0: wait for the copies it issued into the ring (units issued, of
@@ -157,21 +163,21 @@ __device__ __forceinline__ void stager_drain(uint64_t *full, long long done, lon
 // the consumers over the same unit sequence: the bulk copies into the ring
 // (S units ahead) and the L2 prefetches (S + kStgPrefetchUnits ahead).
 struct XCursor {
-    long long j;  // this CTA's item index (CTA item cta + j * grid)
+    unsigned j;   // this CTA's item index (CTA item cta + j * grid)
     int s;        // unit of the item
     int r0, nr, c0, w, tt, kc;
 };
 
-__device__ __forceinline__ void x_cursor_load(XCursor &c, const StgGeom &G, long long mine, int cta, int nctas) {
+__device__ __forceinline__ void x_cursor_load(XCursor &c, const StgGeom &G, unsigned mine, int cta, int nctas) {
     if (c.j >= mine) return;
     int rg;
-    G.item(cta + c.j * nctas, c.tt, c.kc, rg);
+    G.item((unsigned)cta + c.j * (unsigned)nctas, c.tt, c.kc, rg);
     G.rows(c.tt, rg, c.r0, c.nr);
     c.c0 = c.kc * kStgKC;
     c.w = G.K - c.c0 < kStgKC ? G.K - c.c0 : kStgKC;
 }
 
-__device__ __forceinline__ void x_cursor_next(XCursor &c, const StgGeom &G, long long mine, int cta, int nctas) {
+__device__ __forceinline__ void x_cursor_next(XCursor &c, const StgGeom &G, unsigned mine, int cta, int nctas) {
     if (++c.s == kStgUnitsX) {
         c.s = 0;
         ++c.j;
@@ -183,9 +189,9 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
                                 volatile int *abort_flag, uint8_t *ring, uint64_t *full, uint64_t *empty,
                                 uint32_t *status) {
     const int cta = blockIdx.x, nctas = gridDim.x;
-    const long long n = G.items();
-    const long long mine = cta < n ? (n - cta + nctas - 1) / nctas : 0;  // this CTA's items: cta + j grid
-    const long long units = mine * kStgUnitsX;
+    const unsigned n = G.items();
+    const unsigned mine = (unsigned)cta < n ? (n - cta + nctas - 1) / nctas : 0;  // this CTA's items: cta + j grid
+    const long long units = (long long)mine * kStgUnitsX;
     constexpr int S = kStgSlotsX;
     const uint64_t once = l2_policy_evict_first();
     // thread 0: the copy and prefetch cursors
@@ -231,10 +237,14 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
     XCursor cc{0, 0, 0, 0, 0, 0, 0, 0};
     x_cursor_load(cc, G, mine, cta, nctas);
     long long u = 0, first_bad = -1;  // first unit whose copy this thread did not see land
-    for (long long j = 0; j < mine; ++j) {
-        const int col = cc.c0 + 4 * t;
-        const bool cv = col < G.K;
-        const float4 gv = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // thread t converts columns 8 (t % 32) .. + 7 of the chunk in the rows
+    // t / 32, t / 32 + 2, ... of each unit, and writes them as one 16-byte store
+    const int cg = t & 31, rp = t >> 5;
+    for (unsigned j = 0; j < mine; ++j) {
+        const int col = cc.c0 + 8 * cg;
+        const bool cv = col < (int)G.K;
+        const float4 g0 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 g1 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < kStgUnitsX; ++s, ++u) {
             const int sl = (int)(u % S);
             const bool got = mbar_wait(&full[sl], (uint32_t)((u / S) & 1), abort_flag);
@@ -246,12 +256,18 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
             const int q0 = cc.r0 + kStgUnitRows * s;
             const int nq = min(kStgUnitRows, cc.r0 + cc.nr - q0);
             if (got && cv) {
-                const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + t;
+                const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + 2 * cg;
 #pragma unroll
-                for (int q = 0; q < kStgUnitRows; ++q)
-                    if (q < nq)
-                        *reinterpret_cast<uint2 *>(a.dst + (size_t)(q0 + q) * G.K + col) =
-                            pack4_f16(src[q * (kStgKC / 4)], gv, 1.0f);
+                for (int q = rp; q < kStgUnitRows; q += kStgWarps)
+                    if (q < nq) {
+                        const float4 v0 = src[q * (kStgKC / 4)], v1 = src[q * (kStgKC / 4) + 1];
+                        uint4 o;
+                        o.x = mul_pack_half2(v0.x, v0.y, g0.x, g0.y);
+                        o.y = mul_pack_half2(v0.z, v0.w, g0.z, g0.w);
+                        o.z = mul_pack_half2(v1.x, v1.y, g1.x, g1.y);
+                        o.w = mul_pack_half2(v1.z, v1.w, g1.z, g1.w);
+                        *reinterpret_cast<uint4 *>(a.dst + (size_t)(q0 + q) * G.K + col) = o;
+                    }
             }
             // the slot goes back to the producer only if the whole warp has read
             // it (a slot whose copy may still be landing is never handed back)
