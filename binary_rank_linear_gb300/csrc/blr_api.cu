@@ -137,14 +137,15 @@ bool make_tmap_act16(CUtensorMap *m, const void *base, int rows, int K, int box_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// x f32 [rows][cols] with a 256 x 16 box, no swizzle: the in-kernel x
-// staging's ring units (rows and columns past the extent read zero).
-bool make_tmap_x_stage(CUtensorMap *m, const void *base, int rows, int cols) {
+// x f32 [rows][cols] with a 256 x box_rows box, no swizzle: the in-kernel x
+// staging's ring units (16 rows) and L2 prefetches (64 rows); rows and
+// columns past the extent read zero.
+bool make_tmap_x_stage(CUtensorMap *m, const void *base, int rows, int cols, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-    cuuint32_t box[2] = {(cuuint32_t)kStageChunkCols, 16};
+    cuuint32_t box[2] = {(cuuint32_t)kStageChunkCols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -617,7 +618,9 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
         f1.stg.cnt = cnt;
         GemmPlan ps = p1;
         ps.stg = 1;
-        if (!make_tmap_x_stage(&m1.in32, x, M, d_in)) return BLR_ERR_CUDA;  // the a-product has no other input map
+        // the a-product uses neither its input map nor a sign plane: they carry x
+        if (!make_tmap_x_stage(&m1.in32, x, M, d_in, 16) || !make_tmap_x_stage(&m1.sgn, x, M, d_in, 64))
+            return BLR_ERR_CUDA;
         const int ncnt = stage_counters(M, p1.bt, d_in);
         if (launch_prep(pv, pu, status, cnt, ncnt, "fwd_prep", s) != cudaSuccess) return BLR_ERR_CUDA;
         if (launch_gemm(kEpiFwd1, ps, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;

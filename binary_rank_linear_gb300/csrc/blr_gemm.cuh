@@ -798,9 +798,11 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         if constexpr (STG != 0) {
             // ---- stagers: x16 of later tiles -----------------------------------
             const StgGeom G(M, args.K, BT, f_tiles, num_units);
-            // (the a-product has no epilogue input: its input map is x, f32, 256 x 16 boxes)
-            stager_x(args.stg, &tmap_in, G, (int)threadIdx.x - S::kStg0 * 32, abort_flag, L.sStg, L.stg_full,
-                     L.stg_empty, args.status);
+            // (the a-product has no epilogue input and no sign plane: those two
+            // maps are x, f32, in 256 x 16 boxes for the ring and 256 x 64 for
+            // the L2 prefetches)
+            stager_x(args.stg, &tmap_in, tmap_sgn, G, (int)threadIdx.x - S::kStg0 * 32, abort_flag, L.sStg,
+                     L.stg_full, L.stg_empty, args.status);
         }
     }
     if constexpr (SPLIT > 1) {
@@ -822,7 +824,7 @@ __device__ __forceinline__ void gemm_prefetch_maps(const CUtensorMap &tmap_act, 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     if (warp == kWarpTma && lane == 0) {
         tma_prefetch_desc(&tmap_act);
-        if (PLANE) tma_prefetch_desc(tmap_sgn);
+        if (PLANE || S::kStgSlots) tma_prefetch_desc(tmap_sgn);
     }
     if (warp == S::kEpi0 && lane == 0) {
         if (EPI != kEpiFwd1 || S::kStgSlots) tma_prefetch_desc(&tmap_in);

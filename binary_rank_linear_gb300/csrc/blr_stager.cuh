@@ -13,11 +13,13 @@
 //    items c, c + grid, c + 2 grid, ...
 //  - Stager thread 0 loads the items' f32 tiles into a 48 KB shared-memory
 //    ring by TMA (one 256 x 16 box per unit, full/empty mbarriers) several
-//    units ahead, and asks L2 to prefetch the boxes after those; the 64
-//    stager threads convert from shared memory and write f16 with plain
-//    8-byte stores, so the staged tiles sit in L2 when the product's TMA
-//    loads come. (Measured on GB300: with one 1 KB bulk copy and one L2
-//    prefetch per row, issuing them took two thirds of thread 0's time.)
+//    units ahead; thread 32 asks L2 to prefetch whole items (one 256 x 64
+//    box) two items ahead and publishes finished items; the 64 stager
+//    threads convert from shared memory and write f16 with 16-byte stores,
+//    so the staged tiles sit in L2 when the product's TMA loads come.
+//    (Measured on GB300 with in-kernel clock counters: one 1 KB bulk copy and
+//    one L2 prefetch per row took two thirds of thread 0's time; each TMA
+//    instruction costs its thread several hundred cycles here.)
 //  - After an item, the stagers publish its rows on the counter of its
 //    (token tile, column chunk): stores, a proxy fence (the consumer reads by
 //    TMA), a barrier of the stager warps, then one release add. The TMA
@@ -57,7 +59,7 @@ constexpr int kStgUnitRows = 16;
 constexpr int kStgUnitsX = kStgRowsX / kStgUnitRows;
 constexpr int kStgSlotX = kStgUnitRows * kStgKC * 4;
 constexpr int kStgSlotsX = kStgRingBytes / kStgSlotX;
-constexpr int kStgPrefetchUnits = 6;  // units prefetched into L2 beyond those in the ring
+constexpr int kStgPrefetchItems = 2;  // items prefetched into L2 ahead of the one being converted
 static_assert(kStgSlotsX >= 2 && kStgSlotsX <= kStgSlotsMax, "stager ring");
 
 __host__ __device__ constexpr int stg_chunks(int K) { return (K + kStgKC - 1) / kStgKC; }
@@ -185,66 +187,67 @@ __device__ __forceinline__ void x_cursor_next(XCursor &c, const StgGeom &G, unsi
     }
 }
 
-__device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, const StgGeom &G, int t,
-                                volatile int *abort_flag, uint8_t *ring, uint64_t *full, uint64_t *empty,
-                                uint32_t *status) {
+__device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, const CUtensorMap *tmap_pf,
+                                const StgGeom &G, int t, volatile int *abort_flag, uint8_t *ring, uint64_t *full,
+                                uint64_t *empty, uint32_t *status) {
     const int cta = blockIdx.x, nctas = gridDim.x;
     const unsigned n = G.items();
     const unsigned mine = (unsigned)cta < n ? (n - cta + nctas - 1) / nctas : 0;  // this CTA's items: cta + j grid
     const long long units = (long long)mine * kStgUnitsX;
     constexpr int S = kStgSlotsX;
     const uint64_t once = l2_policy_evict_first();
-    // thread 0: the copy and prefetch cursors
-    XCursor ci{0, 0, 0, 0, 0, 0, 0, 0}, cp{0, 0, 0, 0, 0, 0, 0, 0};
-    long long u_iss = 0, u_pf = 0;  // next unit to copy, to prefetch
-    auto unit_rows = [&](const XCursor &c, int &q0, int &nq) {
-        q0 = c.r0 + kStgUnitRows * c.s;
-        const int end = c.r0 + c.nr;
-        nq = end - q0 < kStgUnitRows ? end - q0 : kStgUnitRows;
-        if (nq < 0) nq = 0;
-    };
-    auto issue = [&]() -> bool {  // copy unit u_iss into slot u_iss % S
+    // roles: thread 0 (warp 0) copies ring units ahead; thread 32 (warp 1)
+    // prefetches whole items into L2 ahead and publishes finished items; all
+    // 64 threads convert
+    XCursor ci{0, 0, 0, 0, 0, 0, 0, 0};
+    long long u_iss = 0;  // next unit to copy
+    auto issue = [&]() -> bool {  // thread 0: copy unit u_iss into slot u_iss % S
         const long long u = u_iss;
         const int sl = (int)(u % S);
         if (u >= S && !mbar_wait(&empty[sl], (uint32_t)(((u / S) - 1) & 1), abort_flag)) return false;
-        int q0, nq;
-        unit_rows(ci, q0, nq);
         // one box of 256 columns x 16 rows (rows and columns past x read zero)
         mbar_arrive_expect_tx(&full[sl], (uint32_t)kStgSlotX);
-        tma_load_2d_hint(ring + sl * kStgSlotX, tmap_x, &full[sl], ci.c0, q0, once);
+        tma_load_2d_hint(ring + sl * kStgSlotX, tmap_x, &full[sl], ci.c0, ci.r0 + kStgUnitRows * ci.s, once);
         ++u_iss;
         x_cursor_next(ci, G, mine, cta, nctas);
         return true;
     };
-    auto prefetch_to = [&](long long upto) {
-        for (; u_pf < upto && u_pf < units; ++u_pf) {
-            int q0, nq;
-            unit_rows(cp, q0, nq);
-            if (nq > 0) tma_prefetch_l2_2d(tmap_x, cp.c0, q0);
-            x_cursor_next(cp, G, mine, cta, nctas);
-        }
+    auto prefetch_item = [&](unsigned j) {  // thread 32: one 256 x 64 box into L2
+        if (j >= mine) return;
+        XCursor c{j, 0, 0, 0, 0, 0, 0, 0};
+        x_cursor_load(c, G, mine, cta, nctas);
+        if (c.nr > 0) tma_prefetch_l2_2d(tmap_pf, c.c0, c.r0);
     };
     bool ok = true;
     if (t == 0) {
         x_cursor_load(ci, G, mine, cta, nctas);
-        x_cursor_load(cp, G, mine, cta, nctas);
-        // the prefetch cursor starts where the ring's first copies end
-        for (long long u = 0; u < S && u < units; ++u) x_cursor_next(cp, G, mine, cta, nctas);
-        u_pf = S < units ? S : units;
         while (ok && u_iss < units && u_iss < S) ok = issue();
-        prefetch_to(u_pf + kStgPrefetchUnits);
+    } else if (t == 32) {
+        for (unsigned j = 0; j < kStgPrefetchItems; ++j) prefetch_item(j);
     }
-    XCursor cc{0, 0, 0, 0, 0, 0, 0, 0};
-    x_cursor_load(cc, G, mine, cta, nctas);
-    long long u = 0, first_bad = -1;  // first unit whose copy this thread did not see land
     // thread t converts columns 8 (t % 32) .. + 7 of the chunk in the rows
-    // t / 32, t / 32 + 2, ... of each unit, and writes them as one 16-byte store
+    // t / 32, t / 32 + 2, ... of each unit, and writes them as one 16-byte
+    // store; the g factors of the next item are loaded a whole item ahead
     const int cg = t & 31, rp = t >> 5;
+    XCursor cc{0, 0, 0, 0, 0, 0, 0, 0}, cn{1, 0, 0, 0, 0, 0, 0, 0};
+    x_cursor_load(cc, G, mine, cta, nctas);
+    auto load_g = [&](const XCursor &c, float4 &g0, float4 &g1) {
+        const int col = c.c0 + 8 * cg;
+        const bool cv = c.j < mine && col < (int)G.K;
+        g0 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g1 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float4 g0, g1;
+    load_g(cc, g0, g1);
+    long long u = 0, first_bad = -1;  // first unit whose copy this thread did not see land
     for (unsigned j = 0; j < mine; ++j) {
+        if (t == 32) prefetch_item(j + kStgPrefetchItems);
+        cn.j = j + 1;
+        x_cursor_load(cn, G, mine, cta, nctas);
+        float4 gn0, gn1;
+        load_g(cn, gn0, gn1);
         const int col = cc.c0 + 8 * cg;
         const bool cv = col < (int)G.K;
-        const float4 g0 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 g1 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < kStgUnitsX; ++s, ++u) {
             const int sl = (int)(u % S);
             const bool got = mbar_wait(&full[sl], (uint32_t)((u / S) & 1), abort_flag);
@@ -273,18 +276,16 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
             // it (a slot whose copy may still be landing is never handed back)
             const bool warp_got = __all_sync(0xFFFFFFFFu, got);
             if (warp_got && (t & 31) == 0) mbar_arrive(&empty[sl]);
-            if (t == 0) {
-                if (ok && u_iss < units) ok = issue();
-                prefetch_to(u + 1 + S + kStgPrefetchUnits);
-            }
+            if (t == 0 && ok && u_iss < units) ok = issue();
         }
         // the item's rows are written: publish them to the TMA loads of other CTAs
         fence_proxy_async_global();
         const bool stop = named_bar_or(kStgBar, kStgThreads, !ok || *abort_flag != 0);
         if (stop) break;
-        if (t == 0 && cc.nr > 0) red_release_add_u32(a.cnt + (size_t)cc.tt * G.n_kc + cc.kc, (unsigned int)cc.nr);
-        ++cc.j;
-        x_cursor_load(cc, G, mine, cta, nctas);
+        if (t == 32 && cc.nr > 0) red_release_add_u32(a.cnt + (size_t)cc.tt * G.n_kc + cc.kc, (unsigned int)cc.nr);
+        cc = cn;
+        g0 = gn0;
+        g1 = gn1;
     }
     if (t == 0) stager_drain(full, first_bad >= 0 ? first_bad : u, u_iss, S, abort_flag, status);
 }
