@@ -259,18 +259,31 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
             const int q0 = cc.r0 + kStgUnitRows * s;
             const int nq = min(kStgUnitRows, cc.r0 + cc.nr - q0);
             if (got && cv) {
-                const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + 2 * cg;
+                // this thread's 8 rows of the unit in two batches of 4: all
+                // shared-memory loads of a batch first, then its conversions and stores
+                const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + 2 * cg +
+                                    rp * (kStgKC / 4);
+                uint16_t *dst = a.dst + (size_t)(q0 + rp) * G.K + col;
+                constexpr int kRows = kStgUnitRows / kStgWarps, kBatch = 4;
 #pragma unroll
-                for (int q = rp; q < kStgUnitRows; q += kStgWarps)
-                    if (q < nq) {
-                        const float4 v0 = src[q * (kStgKC / 4)], v1 = src[q * (kStgKC / 4) + 1];
-                        uint4 o;
-                        o.x = mul_pack_half2(v0.x, v0.y, g0.x, g0.y);
-                        o.y = mul_pack_half2(v0.z, v0.w, g0.z, g0.w);
-                        o.z = mul_pack_half2(v1.x, v1.y, g1.x, g1.y);
-                        o.w = mul_pack_half2(v1.z, v1.w, g1.z, g1.w);
-                        *reinterpret_cast<uint4 *>(a.dst + (size_t)(q0 + q) * G.K + col) = o;
+                for (int b = 0; b < kRows; b += kBatch) {
+                    float4 v[kBatch][2];
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        v[i][0] = src[(b + i) * kStgWarps * (kStgKC / 4)];
+                        v[i][1] = src[(b + i) * kStgWarps * (kStgKC / 4) + 1];
                     }
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i)
+                        if (rp + kStgWarps * (b + i) < nq) {
+                            uint4 o;
+                            o.x = mul_pack_half2(v[i][0].x, v[i][0].y, g0.x, g0.y);
+                            o.y = mul_pack_half2(v[i][0].z, v[i][0].w, g0.z, g0.w);
+                            o.z = mul_pack_half2(v[i][1].x, v[i][1].y, g1.x, g1.y);
+                            o.w = mul_pack_half2(v[i][1].z, v[i][1].w, g1.z, g1.w);
+                            *reinterpret_cast<uint4 *>(dst + (size_t)(b + i) * kStgWarps * G.K) = o;
+                        }
+                }
             }
             // the slot goes back to the producer only if the whole warp has read
             // it (a slot whose copy may still be landing is never handed back)
