@@ -15,7 +15,7 @@
 //    ring by TMA (one 256 x 16 box per unit, full/empty mbarriers) several
 //    units ahead; thread 32 asks L2 to prefetch whole items (one 256 x 64
 //    box) two items ahead and publishes finished items; the 64 stager
-//    threads convert from shared memory and write f16 with 8-byte stores,
+//    threads convert from shared memory and write f16 with 16-byte stores,
 //    so the staged tiles sit in L2 when the product's TMA loads come.
 //    (Measured on GB300 with in-kernel clock counters: one 1 KB bulk copy and
 //    one L2 prefetch per row took two thirds of thread 0's time; each TMA
@@ -63,7 +63,7 @@ constexpr int kStgPrefetchItems = 2;  // items prefetched into L2 ahead of the o
 static_assert(kStgSlotsX >= 2 && kStgSlotsX <= kStgSlotsMax, "stager ring");
 
 __host__ __device__ constexpr int stg_chunks(int K) { return (K + kStgKC - 1) / kStgKC; }
-static_assert(kStgKC == 4 * kStgThreads, "a chunk row is four columns per stager thread");
+static_assert(kStgKC == 8 * 32, "a chunk row is eight columns per lane of a stager warp");
 
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
     unsigned int v;
@@ -225,23 +225,28 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
     } else if (t == 32) {
         for (unsigned j = 0; j < kStgPrefetchItems; ++j) prefetch_item(j);
     }
-    // thread t converts columns 4 t .. 4 t + 3 of the chunk; the g factors of
-    // the next item are loaded a whole item ahead
+    // thread t converts columns 8 (t % 32) .. + 7 of the chunk in the rows
+    // t / 32, t / 32 + 2, ... of each unit, and writes them as one 16-byte
+    // store; the g factors of the next item are loaded a whole item ahead
+    const int cg = t & 31, rp = t >> 5;
     XCursor cc{0, 0, 0, 0, 0, 0, 0, 0}, cn{1, 0, 0, 0, 0, 0, 0, 0};
     x_cursor_load(cc, G, mine, cta, nctas);
-    auto load_g = [&](const XCursor &c) {
-        const int col = c.c0 + 4 * t;
+    auto load_g = [&](const XCursor &c, float4 &g0, float4 &g1) {
+        const int col = c.c0 + 8 * cg;
         const bool cv = c.j < mine && col < (int)G.K;
-        return cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g0 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g1 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
-    float4 gv = load_g(cc);
+    float4 g0, g1;
+    load_g(cc, g0, g1);
     long long u = 0, first_bad = -1;  // first unit whose copy this thread did not see land
     for (unsigned j = 0; j < mine; ++j) {
         if (t == 32) prefetch_item(j + kStgPrefetchItems);
         cn.j = j + 1;
         x_cursor_load(cn, G, mine, cta, nctas);
-        const float4 gn = load_g(cn);
-        const int col = cc.c0 + 4 * t;
+        float4 gn0, gn1;
+        load_g(cn, gn0, gn1);
+        const int col = cc.c0 + 8 * cg;
         const bool cv = col < (int)G.K;
         for (int s = 0; s < kStgUnitsX; ++s, ++u) {
             const int sl = (int)(u % S);
@@ -254,23 +259,31 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
             const int q0 = cc.r0 + kStgUnitRows * s;
             const int nq = min(kStgUnitRows, cc.r0 + cc.nr - q0);
             if (got && cv) {
-                // this thread's 4 columns in all 16 rows of the unit: the 16
-                // shared-memory loads (conflict-free: a warp reads 512
-                // consecutive bytes of a row) first, then the conversions and
-                // 8-byte stores
-                const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + t;
-                uint16_t *dst = a.dst + (size_t)q0 * G.K + col;
-                float4 v[kStgUnitRows];
+                // this thread's 8 rows of the unit in two batches of 4: all
+                // shared-memory loads of a batch first, then its conversions and stores
+                const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + 2 * cg +
+                                    rp * (kStgKC / 4);
+                uint16_t *dst = a.dst + (size_t)(q0 + rp) * G.K + col;
+                constexpr int kRows = kStgUnitRows / kStgWarps, kBatch = 4;
 #pragma unroll
-                for (int q = 0; q < kStgUnitRows; ++q) v[q] = src[q * (kStgKC / 4)];
+                for (int b = 0; b < kRows; b += kBatch) {
+                    float4 v[kBatch][2];
 #pragma unroll
-                for (int q = 0; q < kStgUnitRows; ++q)
-                    if (q < nq) {
-                        uint2 o;
-                        o.x = mul_pack_half2(v[q].x, v[q].y, gv.x, gv.y);
-                        o.y = mul_pack_half2(v[q].z, v[q].w, gv.z, gv.w);
-                        *reinterpret_cast<uint2 *>(dst + (size_t)q * G.K) = o;
+                    for (int i = 0; i < kBatch; ++i) {
+                        v[i][0] = src[(b + i) * kStgWarps * (kStgKC / 4)];
+                        v[i][1] = src[(b + i) * kStgWarps * (kStgKC / 4) + 1];
                     }
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i)
+                        if (rp + kStgWarps * (b + i) < nq) {
+                            uint4 o;
+                            o.x = mul_pack_half2(v[i][0].x, v[i][0].y, g0.x, g0.y);
+                            o.y = mul_pack_half2(v[i][0].z, v[i][0].w, g0.z, g0.w);
+                            o.z = mul_pack_half2(v[i][1].x, v[i][1].y, g1.x, g1.y);
+                            o.w = mul_pack_half2(v[i][1].z, v[i][1].w, g1.z, g1.w);
+                            *reinterpret_cast<uint4 *>(dst + (size_t)(b + i) * kStgWarps * G.K) = o;
+                        }
+                }
             }
             // the slot goes back to the producer only if the whole warp has read
             // it (a slot whose copy may still be landing is never handed back)
@@ -284,7 +297,8 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
         if (stop) break;
         if (t == 32 && cc.nr > 0) red_release_add_u32(a.cnt + (size_t)cc.tt * G.n_kc + cc.kc, (unsigned int)cc.nr);
         cc = cn;
-        gv = gn;
+        g0 = gn0;
+        g1 = gn1;
     }
     if (t == 0) stager_drain(full, first_bad >= 0 ? first_bad : u, u_iss, S, abort_flag, status);
 }
