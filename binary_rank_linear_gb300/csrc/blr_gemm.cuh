@@ -78,6 +78,7 @@ __host__ __device__ constexpr int gemm_threads(int epi) { return (kWarpEpi0 + ep
 constexpr int kGemmThreads = (kWarpEpi0 + 8) * 32;  // the fused small-M kernels' block (every phase fits)
 constexpr int kCtlBytes = 1024;   // shared-memory control block ahead of a phase's layout
 static_assert(kNumExpWarps == 4 * kKB, "one expander warp per (lane quarter, 64-wide block)");
+static_assert(kWarpExp0 % 4 == 2, "expander and epilogue warps cover the four TMEM lane quarters in turn");
 
 // PLANE selects where the sign operand comes from: false, bitmap words
 // expanded into TMEM by expander warps (above); true, a +-1 f16 sign plane
@@ -96,7 +97,12 @@ template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 struct GemmShape {
     static constexpr int kKBm = PLANE ? 1 : kKB;           // 64-wide blocks per k-step
     static constexpr int kStepKm = kKBm * kBK;             // K per k-step
-    static constexpr int kEpi0 = PLANE ? 2 : kWarpEpi0;    // first epilogue warp
+    // expander warps: one per (TMEM lane quarter, 64-wide block) of a k-step,
+    // or, in the kernels that stage x, one per lane quarter covering both
+    // blocks (the stager warps take the other four warp slots; 16 warps keep
+    // every role at 128 registers)
+    static constexpr int kNExp = PLANE ? 0 : (STG ? 4 : kNumExpWarps);
+    static constexpr int kEpi0 = PLANE ? 2 : kWarpExp0 + kNExp;  // first epilogue warp
     static constexpr bool kPlaneMN = EPI == kEpiFwd1 || EPI == kEpiBwd1;  // plane rows run along K
     static constexpr int kAccCols = BT;                    // TMEM columns of one accumulator
     static constexpr int kSignCol0 = 2 * BT;               // first sign-stage column
@@ -189,7 +195,7 @@ struct GemmLayout {
             mbar_init(&full_b[s], 1);
             mbar_init(&empty_b[s], 1);
         }
-        for (int s = 0; s < S::kNS; ++s) mbar_init(&full_s[s], PAIR ? 2 * kNumExpWarps : kNumExpWarps);
+        for (int s = 0; s < S::kNS; ++s) mbar_init(&full_s[s], PAIR ? 2 * S::kNExp : S::kNExp);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tmem_full[i], 1);
             mbar_init(&tmem_empty[i], PAIR ? 2 * S::kEW : S::kEW);
@@ -489,8 +495,9 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
     } else if (warp < kWarpEpi0) {
       if constexpr (!PLANE) {
         // ---- sign expanders: bitmap words -> +-1 f16 A operand in TMEM -----
+        constexpr int kBlocks = 4 * kKB / S::kNExp;  // 64-wide blocks of a k-step per warp
         const int quarter = warp & 3;
-        const int kk = (warp - kWarpExp0) / 4;  // which 64-wide block of the k-step
+        const int kk0 = (warp - kWarpExp0) / 4 * kBlocks;  // the warp's first 64-wide block of the k-step
         const int row = quarter * 32 + lane;    // sign row within the CTA's 128
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         int sb = 0, sa = 0;
@@ -502,15 +509,18 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
             for (int ks = ks0; ks < ks1; ++ks) {
                 bool got = mbar_wait(&full_b[sb], pb, abort_flag);
-                uint32_t v[32];
+                uint32_t v[kBlocks][32];
                 if (got) {
                     // signs first: they only need the words, not the free stage
-                    const uint2 w = reinterpret_cast<const uint2 *>(sBits + sb * (S::kBitsBytes / 4) +
-                                                                    kk * (S::kBitsBlock / 4))[row];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        v[q] = sign_pair(w.x, q);       // K 2q, 2q+1 of the block
-                        v[16 + q] = sign_pair(w.y, q);  // K 32+2q, 32+2q+1
+                    for (int b = 0; b < kBlocks; ++b) {
+                        const uint2 w = reinterpret_cast<const uint2 *>(sBits + sb * (S::kBitsBytes / 4) +
+                                                                        (kk0 + b) * (S::kBitsBlock / 4))[row];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            v[b][q] = sign_pair(w.x, q);       // K 2q, 2q+1 of the block
+                            v[b][16 + q] = sign_pair(w.y, q);  // K 32+2q, 32+2q+1
+                        }
                     }
                 }
                 if (got && lag >= 0) got = mbar_wait(&empty_b[ls], lp, abort_flag);
@@ -520,8 +530,10 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                     break;
                 }
                 tc_fence_after();
-                tmem_st_32x32b_x32(tmem_base + lane_addr + (uint32_t)(S::kSignCol0 + sa * kSignCols + kk * (kBK / 2)),
-                                   v);
+#pragma unroll
+                for (int b = 0; b < kBlocks; ++b)
+                    tmem_st_32x32b_x32(
+                        tmem_base + lane_addr + (uint32_t)(S::kSignCol0 + sa * kSignCols + (kk0 + b) * (kBK / 2)), v[b]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();

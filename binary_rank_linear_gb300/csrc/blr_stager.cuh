@@ -46,7 +46,7 @@
 
 namespace blr {
 
-constexpr int kStgWarps = 2;
+constexpr int kStgWarps = 4;
 constexpr int kStgThreads = kStgWarps * 32;
 constexpr int kStgBar = 8;          // named barrier of the stager warps (0 is __syncthreads)
 constexpr int kStgKC = kStageChunkCols;  // columns per chunk: one float4 per stager thread
