@@ -99,8 +99,8 @@ struct GemmShape {
     static constexpr int kStepKm = kKBm * kBK;             // K per k-step
     // expander warps: one per (TMEM lane quarter, 64-wide block) of a k-step,
     // or, in the kernels that stage x, one per lane quarter covering both
-    // blocks (the stager warps take the other four warp slots; 16 warps keep
-    // every role at 128 registers)
+    // blocks (the six stager warps take the freed slots: 16 warps keep every
+    // role at 128 registers)
     static constexpr int kNExp = PLANE ? 0 : (STG ? 4 : kNumExpWarps);
     static constexpr int kEpi0 = PLANE ? 2 : kWarpExp0 + kNExp;  // first epilogue warp
     static constexpr bool kPlaneMN = EPI == kEpiFwd1 || EPI == kEpiBwd1;  // plane rows run along K
@@ -161,6 +161,7 @@ struct GemmShape {
 struct GemmCtl {
     uint32_t tmem_slot;  // TMEM base address written by tcgen05.alloc
     int abort_flag;      // set by any role whose bounded wait ran out
+    unsigned int stg_done;  // items finished by the converter warps, one count per warp (STG kernels)
 };
 static_assert(sizeof(GemmCtl) <= kCtlBytes, "control block");
 
@@ -206,7 +207,7 @@ struct GemmLayout {
             for (int s = 0; s < S::kNB; ++s) mbar_init(&full_p[s], 1);
         for (int s = 0; s < S::kStgSlots; ++s) {
             mbar_init(&stg_full[s], 1);
-            mbar_init(&stg_empty[s], kStgWarps);
+            mbar_init(&stg_empty[s], kStgConvWarps);
         }
     }
     // one thread, once every role of the phase has finished with the barriers
@@ -238,7 +239,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                                            const CUtensorMap &tmap_in, const CUtensorMap &tmap_out32,
                                            const CUtensorMap &tmap_out16, const GemmArgs &args,
                                            uint32_t tmem_base, volatile int *abort_flag, int unit, int num_units,
-                                           const CUtensorMap *tmap_sgn = nullptr) {
+                                           const CUtensorMap *tmap_sgn = nullptr, unsigned int *stg_done = nullptr) {
     using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
     static_assert(STG == 0 || (STG == 1 && SPLIT == 1 && !PLANE && EPI == kEpiFwd1),
                   "in-kernel staging: the a-product stages x");
@@ -810,11 +811,18 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         if constexpr (STG != 0) {
             // ---- stagers: x16 of later tiles -----------------------------------
             const StgGeom G(M, args.K, BT, f_tiles, num_units);
+            const StgX X(args.stg, G);
+            const int t = (int)threadIdx.x - S::kStg0 * 32;
             // (the a-product has no epilogue input and no sign plane: those two
             // maps are x, f32, in 256 x 16 boxes for the ring and 256 x 64 for
             // the L2 prefetches)
-            stager_x(args.stg, &tmap_in, tmap_sgn, G, (int)threadIdx.x - S::kStg0 * 32, abort_flag, L.sStg,
-                     L.stg_full, L.stg_empty, args.status);
+            if (t < kStgConvThreads)
+                stager_x_convert(X, t, abort_flag, L.sStg, L.stg_full, L.stg_empty, stg_done, args.status);
+            else if (t == kStgConvThreads)
+                stager_x_producer(X, &tmap_in, abort_flag, L.sStg, L.stg_full, L.stg_empty, args.status);
+            else if (t == kStgConvThreads + 32)
+                stager_x_publisher(X, tmap_sgn, abort_flag, stg_done, args.status);
+            __syncwarp();
         }
     }
     if constexpr (SPLIT > 1) {
@@ -831,7 +839,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
 template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 __device__ __forceinline__ void gemm_prefetch_maps(const CUtensorMap &tmap_act, const CUtensorMap &tmap_in,
                                                    const CUtensorMap &tmap_out32, const CUtensorMap &tmap_out16,
-                                                   const CUtensorMap *tmap_sgn = nullptr) {
+                                                   const CUtensorMap *tmap_sgn = nullptr, unsigned int *stg_done = nullptr) {
     using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     if (warp == kWarpTma && lane == 0) {
@@ -862,6 +870,7 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads
     if (threadIdx.x == 0) {
         L.init_barriers();
         ctl->abort_flag = 0;
+        ctl->stg_done = 0;
         fence_mbar_init();
     }
     gemm_prefetch_maps<EPI, PAIR, BT, PLANE, STG>(tmap_act, tmap_in, tmap_out32, tmap_out16, &tmap_sgn);
@@ -890,7 +899,7 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads
     const int num_units = (int)gridDim.x / per_unit;
     gemm_roles<EPI, PAIR, BT, PLANE, SPLIT, STG>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
                                                  reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units,
-                                                 &tmap_sgn);
+                                                 &tmap_sgn, &ctl->stg_done);
     tc_fence_before();
     if constexpr (PAIR) {
         // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it

@@ -11,18 +11,19 @@
 //    token tiles whose feature tiles the units start together), then column
 //    chunk by column chunk, then token tile and row group. CTA c stages
 //    items c, c + grid, c + 2 grid, ...
-//  - Stager thread 0 loads the items' f32 tiles into a 48 KB shared-memory
+//  - One stager lane loads the items' f32 tiles into a 48 KB shared-memory
 //    ring by TMA (one 256 x 16 box per unit, full/empty mbarriers) several
-//    units ahead; thread 32 asks L2 to prefetch whole items (one 256 x 64
-//    box) two items ahead and publishes finished items; the 64 stager
-//    threads convert from shared memory and write f16 with 16-byte stores,
-//    so the staged tiles sit in L2 when the product's TMA loads come.
-//    (Measured on GB300 with in-kernel clock counters: one 1 KB bulk copy and
-//    one L2 prefetch per row took two thirds of thread 0's time; each TMA
-//    instruction costs its thread several hundred cycles here.)
+//    units ahead; another asks L2 to prefetch whole items (one 256 x 64 box)
+//    two items ahead and publishes finished items; four converter warps
+//    convert from shared memory and write f16 with 16-byte stores, so the
+//    staged tiles sit in L2 when the product's TMA loads come. (Measured on
+//    GB300 with in-kernel clock counters: converters that also issued the
+//    TMA copies and the releases spent most of their time there; each TMA
+//    instruction costs its thread several hundred cycles in this kernel.)
 //  - After an item, the stagers publish its rows on the counter of its
 //    (token tile, column chunk): stores, a proxy fence (the consumer reads by
-//    TMA), a barrier of the stager warps, then one release add. The TMA
+//    TMA), the converter warps' arrivals on a shared-memory counter, then
+//    one release add by the publisher. The TMA
 //    producer acquires the counter of each chunk of a tile before its loads
 //    (bounded wait), then fences the async proxy. A product starts as soon as
 //    the first chunk of its first round is staged.
@@ -30,7 +31,7 @@
 // Stagers never wait for another CTA: every counter completes once the
 // stagers of the grid have run (the CTAs of the persistent grid are resident
 // together). A bounded wait that runs out, or the CTA's abort flag, stops
-// them between items; thread 0 then waits for the copies it issued.
+// them; the copy producer then waits for the copies it issued.
 //
 // (The db-product's dy staging stays a stand-alone pass: its per-token scale
 // needs a row-wide maximum, and its dh sums a per-column accumulator over the
@@ -46,9 +47,10 @@
 
 namespace blr {
 
-constexpr int kStgWarps = 4;
+constexpr int kStgConvWarps = 4;                 // converter warps
+constexpr int kStgConvThreads = kStgConvWarps * 32;
+constexpr int kStgWarps = kStgConvWarps + 2;     // + the copy producer and the publisher
 constexpr int kStgThreads = kStgWarps * 32;
-constexpr int kStgBar = 8;          // named barrier of the stager warps (0 is __syncthreads)
 constexpr int kStgKC = kStageChunkCols;  // columns per chunk: one float4 per stager thread
 constexpr int kStgRingBytes = 48 * 1024;
 constexpr int kStgSlotsMax = 8;
@@ -63,7 +65,8 @@ constexpr int kStgPrefetchItems = 2;  // items prefetched into L2 ahead of the o
 static_assert(kStgSlotsX >= 2 && kStgSlotsX <= kStgSlotsMax, "stager ring");
 
 __host__ __device__ constexpr int stg_chunks(int K) { return (K + kStgKC - 1) / kStgKC; }
-static_assert(kStgKC == 8 * 32, "a chunk row is eight columns per lane of a stager warp");
+static_assert(kStgKC == 8 * 32, "a chunk row is eight columns per lane of a converter warp");
+static_assert(kStgUnitRows % kStgConvWarps == 0, "the converter warps share a unit's rows evenly");
 
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
     unsigned int v;
@@ -148,15 +151,6 @@ __device__ __forceinline__ uint32_t mul_pack_half2(float a0, float a1, float b0,
     return pack_half2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
 }
 
-// Thread 0: wait for the copies it issued into the ring (units issued, of
-// which the first `done` were consumed) before the CTA may exit.
-__device__ __forceinline__ void stager_drain(uint64_t *full, long long done, long long issued, int slots,
-                                             const volatile int *abort_flag, uint32_t *status) {
-    for (long long u = done; u < issued; ++u)
-        if (!mbar_wait(&full[u % slots], (uint32_t)((u / slots) & 1), abort_flag, false))
-            atomicOr(status, kStTimeoutDrain);
-}
-
 // ---- x: x16 = f16(x.g), items of 64 rows x 256 columns ---------------------
 // An item is kStgUnitsX ring units of 8 rows (8 KB f32 each). The consumer
 // side decodes an item once, loads its 256 g factors (one float4 per
@@ -187,71 +181,132 @@ __device__ __forceinline__ void x_cursor_next(XCursor &c, const StgGeom &G, unsi
     }
 }
 
-__device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, const CUtensorMap *tmap_pf,
-                                const StgGeom &G, int t, volatile int *abort_flag, uint8_t *ring, uint64_t *full,
-                                uint64_t *empty, uint32_t *status) {
-    const int cta = blockIdx.x, nctas = gridDim.x;
-    const unsigned n = G.items();
-    const unsigned mine = (unsigned)cta < n ? (n - cta + nctas - 1) / nctas : 0;  // this CTA's items: cta + j grid
-    const long long units = (long long)mine * kStgUnitsX;
+// Roles of the stager warps (kStgThreads threads, t = 0 ..): warps 0 ..
+// kStgConvWarps - 1 convert; the next warp's lane 0 copies ring units by TMA
+// (stager_x_producer); the last warp's lane 0 prefetches items into L2 and
+// publishes finished items (stager_x_publisher). The converters count the
+// items they finish on a shared-memory counter (one arrival per converter
+// warp and item, release at CTA scope), which the publisher acquires before
+// its release add at GPU scope; nothing in the stagers waits on a named
+// barrier, so a converter that stops early (an abort) cannot hang another.
+__device__ __forceinline__ unsigned int ld_acquire_shared_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_shared_add_u32(unsigned int *p, unsigned int v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+struct StgX {
+    const StageArgs &a;
+    const StgGeom &G;
+    unsigned mine;  // this CTA's items: cta + j * grid, j < mine
+    long long units;
+    int cta, nctas;
+    __device__ StgX(const StageArgs &a_, const StgGeom &G_) : a(a_), G(G_) {
+        cta = blockIdx.x;
+        nctas = gridDim.x;
+        const unsigned n = G.items();
+        mine = (unsigned)cta < n ? (n - cta + nctas - 1) / nctas : 0;
+        units = (long long)mine * kStgUnitsX;
+    }
+};
+
+// lane 0 of the producer warp: ring units by TMA, S ahead of the converters
+__device__ inline void stager_x_producer(const StgX &X, const CUtensorMap *tmap_x, volatile int *abort_flag,
+                                         uint8_t *ring, uint64_t *full, uint64_t *empty, uint32_t *status) {
     constexpr int S = kStgSlotsX;
     const uint64_t once = l2_policy_evict_first();
-    // roles: thread 0 (warp 0) copies ring units ahead; thread 32 (warp 1)
-    // prefetches whole items into L2 ahead and publishes finished items; all
-    // 64 threads convert
     XCursor ci{0, 0, 0, 0, 0, 0, 0, 0};
-    long long u_iss = 0;  // next unit to copy
-    auto issue = [&]() -> bool {  // thread 0: copy unit u_iss into slot u_iss % S
-        const long long u = u_iss;
+    x_cursor_load(ci, X.G, X.mine, X.cta, X.nctas);
+    long long u = 0;
+    for (; u < X.units; ++u) {
         const int sl = (int)(u % S);
-        if (u >= S && !mbar_wait(&empty[sl], (uint32_t)(((u / S) - 1) & 1), abort_flag)) return false;
+        if (u >= S && !mbar_wait(&empty[sl], (uint32_t)(((u / S) - 1) & 1), abort_flag)) break;
         // one box of 256 columns x 16 rows (rows and columns past x read zero)
         mbar_arrive_expect_tx(&full[sl], (uint32_t)kStgSlotX);
         tma_load_2d_hint(ring + sl * kStgSlotX, tmap_x, &full[sl], ci.c0, ci.r0 + kStgUnitRows * ci.s, once);
-        ++u_iss;
-        x_cursor_next(ci, G, mine, cta, nctas);
-        return true;
-    };
-    auto prefetch_item = [&](unsigned j) {  // thread 32: one 256 x 64 box into L2
-        if (j >= mine) return;
-        XCursor c{j, 0, 0, 0, 0, 0, 0, 0};
-        x_cursor_load(c, G, mine, cta, nctas);
-        if (c.nr > 0) tma_prefetch_l2_2d(tmap_pf, c.c0, c.r0);
-    };
-    bool ok = true;
-    if (t == 0) {
-        x_cursor_load(ci, G, mine, cta, nctas);
-        while (ok && u_iss < units && u_iss < S) ok = issue();
-    } else if (t == 32) {
-        for (unsigned j = 0; j < kStgPrefetchItems; ++j) prefetch_item(j);
+        x_cursor_next(ci, X.G, X.mine, X.cta, X.nctas);
     }
-    // thread t converts columns 8 (t % 32) .. + 7 of the chunk in the rows
-    // t / 32, t / 32 + 2, ... of each unit, and writes them as one 16-byte
-    // store; the g factors of the next item are loaded a whole item ahead
-    const int cg = t & 31, rp = t >> 5;
+    // every copy issued lands before the CTA may exit: for each slot, the
+    // phase of the last unit copied into it
+    for (long long v = (u > S ? u - S : 0); v < u; ++v)
+        if (!mbar_wait(&full[v % S], (uint32_t)((v / S) & 1), abort_flag, false)) atomicOr(status, kStTimeoutDrain);
+}
+
+// lane 0 of the publisher warp: L2 prefetches two items ahead, and the
+// release add of each item once every converter warp has finished it
+__device__ inline void stager_x_publisher(const StgX &X, const CUtensorMap *tmap_pf, volatile int *abort_flag,
+                                          const unsigned int *done, uint32_t *status) {
+    auto prefetch_item = [&](unsigned j) {
+        if (j >= X.mine) return;
+        XCursor c{j, 0, 0, 0, 0, 0, 0, 0};
+        x_cursor_load(c, X.G, X.mine, X.cta, X.nctas);
+        if (c.nr > 0) tma_prefetch_l2_2d(tmap_pf, c.c0, c.r0);  // one 256 x 64 box
+    };
+    for (unsigned j = 0; j < kStgPrefetchItems; ++j) prefetch_item(j);
+    for (unsigned j = 0; j < X.mine; ++j) {
+        prefetch_item(j + kStgPrefetchItems);
+        XCursor c{j, 0, 0, 0, 0, 0, 0, 0};
+        x_cursor_load(c, X.G, X.mine, X.cta, X.nctas);
+        const unsigned target = (j + 1) * kStgConvWarps;
+        if (ld_acquire_shared_u32(done) < target) {
+            const uint64_t t0 = globaltimer_ns();
+            bool ok = true;
+            for (uint32_t i = 1; ld_acquire_shared_u32(done) < target; ++i) {
+                __nanosleep(64);
+                if ((i & 15u) == 0 && (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) {
+                if (!*abort_flag) {
+                    *abort_flag = 1;
+                    atomicOr(status, kStTimeoutStage);
+                }
+                return;
+            }
+        }
+        if (c.nr > 0) red_release_add_u32(X.a.cnt + (size_t)c.tt * X.G.n_kc + c.kc, (unsigned int)c.nr);
+    }
+}
+
+// converter warps: thread t < kStgConvThreads converts columns 8 (t % 32) ..
+// + 7 of the chunk in the rows t / 32, t / 32 + kStgConvWarps, ... of each
+// unit (one 16-byte store each); the g factors of the next item are loaded a
+// whole item ahead
+__device__ inline void stager_x_convert(const StgX &X, int t, volatile int *abort_flag, uint8_t *ring,
+                                        uint64_t *full, uint64_t *empty, unsigned int *done, uint32_t *status) {
+    constexpr int S = kStgSlotsX;
+    const int cg = t & 31, rp = t >> 5, lane = t & 31;
+    const StageArgs &a = X.a;
+    const StgGeom &G = X.G;
     XCursor cc{0, 0, 0, 0, 0, 0, 0, 0}, cn{1, 0, 0, 0, 0, 0, 0, 0};
-    x_cursor_load(cc, G, mine, cta, nctas);
+    x_cursor_load(cc, G, X.mine, X.cta, X.nctas);
     auto load_g = [&](const XCursor &c, float4 &g0, float4 &g1) {
         const int col = c.c0 + 8 * cg;
-        const bool cv = c.j < mine && col < (int)G.K;
+        const bool cv = c.j < X.mine && col < (int)G.K;
         g0 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
         g1 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     float4 g0, g1;
     load_g(cc, g0, g1);
-    long long u = 0, first_bad = -1;  // first unit whose copy this thread did not see land
-    for (unsigned j = 0; j < mine; ++j) {
-        if (t == 32) prefetch_item(j + kStgPrefetchItems);
+    long long u = 0;
+    for (unsigned j = 0; j < X.mine; ++j) {
+        if (*abort_flag) break;
         cn.j = j + 1;
-        x_cursor_load(cn, G, mine, cta, nctas);
+        x_cursor_load(cn, G, X.mine, X.cta, X.nctas);
         float4 gn0, gn1;
         load_g(cn, gn0, gn1);
         const int col = cc.c0 + 8 * cg;
         const bool cv = col < (int)G.K;
+        bool ok = true;
         for (int s = 0; s < kStgUnitsX; ++s, ++u) {
             const int sl = (int)(u % S);
             const bool got = mbar_wait(&full[sl], (uint32_t)((u / S) & 1), abort_flag);
-            if (!got && first_bad < 0) first_bad = u;
             if (!got && !*abort_flag) {
                 *abort_flag = 1;
                 atomicOr(status, kStTimeoutStage);
@@ -259,48 +314,45 @@ __device__ inline void stager_x(const StageArgs &a, const CUtensorMap *tmap_x, c
             const int q0 = cc.r0 + kStgUnitRows * s;
             const int nq = min(kStgUnitRows, cc.r0 + cc.nr - q0);
             if (got && cv) {
-                // this thread's 8 rows of the unit in two batches of 4: all
-                // shared-memory loads of a batch first, then its conversions and stores
+                // this thread's rows of the unit: the shared-memory loads first,
+                // then the conversions and stores
                 const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + 2 * cg +
                                     rp * (kStgKC / 4);
                 uint16_t *dst = a.dst + (size_t)(q0 + rp) * G.K + col;
-                constexpr int kRows = kStgUnitRows / kStgWarps, kBatch = 4;
+                constexpr int kRows = kStgUnitRows / kStgConvWarps;
+                float4 v[kRows][2];
 #pragma unroll
-                for (int b = 0; b < kRows; b += kBatch) {
-                    float4 v[kBatch][2];
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        v[i][0] = src[(b + i) * kStgWarps * (kStgKC / 4)];
-                        v[i][1] = src[(b + i) * kStgWarps * (kStgKC / 4) + 1];
-                    }
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i)
-                        if (rp + kStgWarps * (b + i) < nq) {
-                            uint4 o;
-                            o.x = mul_pack_half2(v[i][0].x, v[i][0].y, g0.x, g0.y);
-                            o.y = mul_pack_half2(v[i][0].z, v[i][0].w, g0.z, g0.w);
-                            o.z = mul_pack_half2(v[i][1].x, v[i][1].y, g1.x, g1.y);
-                            o.w = mul_pack_half2(v[i][1].z, v[i][1].w, g1.z, g1.w);
-                            *reinterpret_cast<uint4 *>(dst + (size_t)(b + i) * kStgWarps * G.K) = o;
-                        }
+                for (int i = 0; i < kRows; ++i) {
+                    v[i][0] = src[i * kStgConvWarps * (kStgKC / 4)];
+                    v[i][1] = src[i * kStgConvWarps * (kStgKC / 4) + 1];
                 }
+#pragma unroll
+                for (int i = 0; i < kRows; ++i)
+                    if (rp + kStgConvWarps * i < nq) {
+                        uint4 o;
+                        o.x = mul_pack_half2(v[i][0].x, v[i][0].y, g0.x, g0.y);
+                        o.y = mul_pack_half2(v[i][0].z, v[i][0].w, g0.z, g0.w);
+                        o.z = mul_pack_half2(v[i][1].x, v[i][1].y, g1.x, g1.y);
+                        o.w = mul_pack_half2(v[i][1].z, v[i][1].w, g1.z, g1.w);
+                        *reinterpret_cast<uint4 *>(dst + (size_t)i * kStgConvWarps * G.K) = o;
+                    }
             }
             // the slot goes back to the producer only if the whole warp has read
             // it (a slot whose copy may still be landing is never handed back)
             const bool warp_got = __all_sync(0xFFFFFFFFu, got);
-            if (warp_got && (t & 31) == 0) mbar_arrive(&empty[sl]);
-            if (t == 0 && ok && u_iss < units) ok = issue();
+            if (warp_got && lane == 0) mbar_arrive(&empty[sl]);
+            ok = ok && warp_got;
         }
-        // the item's rows are written: publish them to the TMA loads of other CTAs
+        if (!ok) break;
+        // the item's rows are written: proxy fence (the TMA loads of other CTAs
+        // read them), then one arrival of this warp on the item counter
         fence_proxy_async_global();
-        const bool stop = named_bar_or(kStgBar, kStgThreads, !ok || *abort_flag != 0);
-        if (stop) break;
-        if (t == 32 && cc.nr > 0) red_release_add_u32(a.cnt + (size_t)cc.tt * G.n_kc + cc.kc, (unsigned int)cc.nr);
+        __syncwarp();
+        if (lane == 0) red_release_shared_add_u32(done, 1u);
         cc = cn;
         g0 = gn0;
         g1 = gn1;
     }
-    if (t == 0) stager_drain(full, first_bad >= 0 ? first_bad : u, u_iss, S, abort_flag, status);
 }
 
 }  // namespace blr
