@@ -415,11 +415,18 @@ bool fused_small_enabled() {
 }
 
 // Where the a-product's activation operand x16 is staged: inside the
-// product's kernel by its stager warps (default), or by a stand-alone pass
-// before it when BLR_STAGE=pass (the earlier design; kept for comparison).
-bool stage_in_kernel() {
+// product's kernel by its stager warps for x of 64 MB or more, by a
+// stand-alone pass before it otherwise. Measured on GB300 (CUDA-graph steps):
+// in the kernel, the 12288 -> 4096 MLP layer's pass and a-product take 357
+// against 460 us, the attention-sized layer's 78 against 106; for the small
+// layer (8 MB of x) the pass keeps its bitmap re-layouts hidden behind the
+// staging and the step is 50.6 against 54.0 us. BLR_STAGE=kernel or
+// BLR_STAGE=pass forces a form.
+bool stage_in_kernel(long long x_bytes) {
     const char *v = std::getenv("BLR_STAGE");
-    return !(v && std::strcmp(v, "pass") == 0);
+    if (v && std::strcmp(v, "pass") == 0) return false;
+    if (v && std::strcmp(v, "kernel") == 0) return true;
+    return x_bytes >= (64ll << 20);
 }
 
 // Grid barriers of the fused small-M kernels. Their waits give up after 2 s
@@ -602,7 +609,7 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     f2.status = status;
 
     // x staged inside the a-product (not with sign planes or split-K tiles)
-    const bool stg = !fused && !planes && p1.split <= 1 && stage_in_kernel() &&
+    const bool stg = !fused && !planes && p1.split <= 1 && stage_in_kernel((long long)M * d_in * 4) &&
                      stage_fits(M, p1.bt, d_in, (r + (p1.pair ? 255 : 127)) / (p1.pair ? 256 : 128));
     if (fused) {
         // small problem: the whole pass as one fused cooperative kernel

@@ -419,10 +419,10 @@ def test_maximum_widths(M, d_in, d_out, r):
                                                  ("small", 200, 128, 9216, 64), ("attn", 3001, 4096, 2048, 512)])
 @pytest.mark.parametrize("gscale", [0.0, 1024.0])
 def test_stage_forms(monkeypatch, stage, name, M, d_in, d_out, r, gscale):
-    """x and dy staged inside the a- and db-products by their stager warps
-    (default) or by stand-alone passes before them (BLR_STAGE=pass), on
-    single-CTA and CTA-pair tiles, ragged token counts and partial column
-    chunks, against the oracle."""
+    """x staged inside the a-product by its stager warps (BLR_STAGE=kernel,
+    the default for x of 64 MB or more) or by the stand-alone pass before it
+    (BLR_STAGE=pass), on single-CTA and CTA-pair tiles, ragged token counts
+    and partial column chunks, against the oracle."""
     monkeypatch.setenv("BLR_STAGE", stage)
     t = wl.make_inputs(wl.WORKLOADS[name].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     if name == "ragged" and gscale > 0:
