@@ -276,11 +276,13 @@ __device__ inline void stager_x_publisher(const StgX &X, const CUtensorMap *tmap
 
 // converter warps: thread t < kStgConvThreads converts columns 8 (t % 32) ..
 // + 7 of the chunk in the rows t / 32, t / 32 + kStgConvWarps, ... of each
-// unit (one 16-byte store each); the g factors of the next item are loaded a
-// whole item ahead
+// unit (one 16-byte store each). Software-pipelined over the units: the next
+// unit's shared-memory loads are in flight while the current unit converts;
+// the g factors of the next item are loaded a whole item ahead.
 __device__ inline void stager_x_convert(const StgX &X, int t, volatile int *abort_flag, uint8_t *ring,
                                         uint64_t *full, uint64_t *empty, unsigned int *done, uint32_t *status) {
     constexpr int S = kStgSlotsX;
+    constexpr int kRows = kStgUnitRows / kStgConvWarps;
     const int cg = t & 31, rp = t >> 5, lane = t & 31;
     const StageArgs &a = X.a;
     const StgGeom &G = X.G;
@@ -292,66 +294,79 @@ __device__ inline void stager_x_convert(const StgX &X, int t, volatile int *abor
         g0 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
         g1 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
-    float4 g0, g1;
-    load_g(cc, g0, g1);
-    long long u = 0;
-    for (unsigned j = 0; j < X.mine; ++j) {
-        if (*abort_flag) break;
-        cn.j = j + 1;
-        x_cursor_load(cn, G, X.mine, X.cta, X.nctas);
-        float4 gn0, gn1;
-        load_g(cn, gn0, gn1);
-        const int col = cc.c0 + 8 * cg;
-        const bool cv = col < (int)G.K;
-        bool ok = true;
-        for (int s = 0; s < kStgUnitsX; ++s, ++u) {
-            const int sl = (int)(u % S);
-            const bool got = mbar_wait(&full[sl], (uint32_t)((u / S) & 1), abort_flag);
-            if (!got && !*abort_flag) {
-                *abort_flag = 1;
-                atomicOr(status, kStTimeoutStage);
-            }
-            const int q0 = cc.r0 + kStgUnitRows * s;
-            const int nq = min(kStgUnitRows, cc.r0 + cc.nr - q0);
-            if (got && cv) {
-                // this thread's rows of the unit: the shared-memory loads first,
-                // then the conversions and stores
-                const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + 2 * cg +
-                                    rp * (kStgKC / 4);
-                uint16_t *dst = a.dst + (size_t)(q0 + rp) * G.K + col;
-                constexpr int kRows = kStgUnitRows / kStgConvWarps;
-                float4 v[kRows][2];
-#pragma unroll
-                for (int i = 0; i < kRows; ++i) {
-                    v[i][0] = src[i * kStgConvWarps * (kStgKC / 4)];
-                    v[i][1] = src[i * kStgConvWarps * (kStgKC / 4) + 1];
-                }
-#pragma unroll
-                for (int i = 0; i < kRows; ++i)
-                    if (rp + kStgConvWarps * i < nq) {
-                        uint4 o;
-                        o.x = mul_pack_half2(v[i][0].x, v[i][0].y, g0.x, g0.y);
-                        o.y = mul_pack_half2(v[i][0].z, v[i][0].w, g0.z, g0.w);
-                        o.z = mul_pack_half2(v[i][1].x, v[i][1].y, g1.x, g1.y);
-                        o.w = mul_pack_half2(v[i][1].z, v[i][1].w, g1.z, g1.w);
-                        *reinterpret_cast<uint4 *>(dst + (size_t)i * kStgConvWarps * G.K) = o;
-                    }
-            }
-            // the slot goes back to the producer only if the whole warp has read
-            // it (a slot whose copy may still be landing is never handed back)
-            const bool warp_got = __all_sync(0xFFFFFFFFu, got);
-            if (warp_got && lane == 0) mbar_arrive(&empty[sl]);
-            ok = ok && warp_got;
+    // wait for unit u's copy and load this thread's rows of it (the loads do
+    // not depend on which item the unit belongs to)
+    auto fetch = [&](long long u, float4 (&v)[kRows][2]) -> bool {
+        const int sl = (int)(u % S);
+        const bool got = mbar_wait(&full[sl], (uint32_t)((u / S) & 1), abort_flag);
+        if (!got && !*abort_flag) {
+            *abort_flag = 1;
+            atomicOr(status, kStTimeoutStage);
         }
-        if (!ok) break;
-        // the item's rows are written: proxy fence (the TMA loads of other CTAs
-        // read them), then one arrival of this warp on the item counter
-        fence_proxy_async_global();
-        __syncwarp();
-        if (lane == 0) red_release_shared_add_u32(done, 1u);
-        cc = cn;
-        g0 = gn0;
-        g1 = gn1;
+        if (got) {
+            const float4 *src = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX) + 2 * cg + rp * (kStgKC / 4);
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) {
+                v[i][0] = src[i * kStgConvWarps * (kStgKC / 4)];
+                v[i][1] = src[i * kStgConvWarps * (kStgKC / 4) + 1];
+            }
+        }
+        return got;
+    };
+    float4 g0, g1, gn0, gn1;
+    load_g(cc, g0, g1);
+    cn.j = 1;
+    x_cursor_load(cn, G, X.mine, X.cta, X.nctas);
+    load_g(cn, gn0, gn1);
+    float4 va[kRows][2], vb[kRows][2];
+    bool got_a = X.units > 0 && fetch(0, va);
+    bool ok = true;
+    for (long long u = 0; u < X.units; ++u) {
+        const int s = (int)(u % kStgUnitsX);
+        // the next unit's loads go out first
+        const bool has_next = u + 1 < X.units;
+        const bool got_b = has_next && fetch(u + 1, vb);
+        const int q0 = cc.r0 + kStgUnitRows * s;
+        const int nq = min(kStgUnitRows, cc.r0 + cc.nr - q0);
+        const int col = cc.c0 + 8 * cg;
+        if (got_a && col < (int)G.K) {
+            uint16_t *dst = a.dst + (size_t)(q0 + rp) * G.K + col;
+#pragma unroll
+            for (int i = 0; i < kRows; ++i)
+                if (rp + kStgConvWarps * i < nq) {
+                    uint4 o;
+                    o.x = mul_pack_half2(va[i][0].x, va[i][0].y, g0.x, g0.y);
+                    o.y = mul_pack_half2(va[i][0].z, va[i][0].w, g0.z, g0.w);
+                    o.z = mul_pack_half2(va[i][1].x, va[i][1].y, g1.x, g1.y);
+                    o.w = mul_pack_half2(va[i][1].z, va[i][1].w, g1.z, g1.w);
+                    *reinterpret_cast<uint4 *>(dst + (size_t)i * kStgConvWarps * G.K) = o;
+                }
+        }
+        // unit u's slot goes back to the producer once the whole warp has
+        // converted it (a slot whose copy may still be landing is never handed back)
+        const bool warp_got = __all_sync(0xFFFFFFFFu, got_a);
+        if (warp_got && lane == 0) mbar_arrive(&empty[(int)(u % S)]);
+        ok = ok && warp_got;
+        if (s == kStgUnitsX - 1) {
+            if (!ok || *abort_flag) break;
+            // the item's rows are written: proxy fence (the TMA loads of other
+            // CTAs read them), then one arrival of this warp on the item counter
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) red_release_shared_add_u32(done, 1u);
+            cc = cn;
+            g0 = gn0;
+            g1 = gn1;
+            cn.j = cc.j + 1;
+            x_cursor_load(cn, G, X.mine, X.cta, X.nctas);
+            load_g(cn, gn0, gn1);
+        }
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            va[i][0] = vb[i][0];
+            va[i][1] = vb[i][1];
+        }
+        got_a = got_b;
     }
 }
 
