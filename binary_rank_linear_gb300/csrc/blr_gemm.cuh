@@ -162,6 +162,7 @@ struct GemmCtl {
     uint32_t tmem_slot;  // TMEM base address written by tcgen05.alloc
     int abort_flag;      // set by any role whose bounded wait ran out
     unsigned int stg_done;  // items finished by the converter warps, one count per warp (STG kernels)
+    StgGeo stg_geo[kStgSlotsMax];  // geometry of the units in the stager ring (STG kernels)
 };
 static_assert(sizeof(GemmCtl) <= kCtlBytes, "control block");
 
@@ -239,7 +240,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                                            const CUtensorMap &tmap_in, const CUtensorMap &tmap_out32,
                                            const CUtensorMap &tmap_out16, const GemmArgs &args,
                                            uint32_t tmem_base, volatile int *abort_flag, int unit, int num_units,
-                                           const CUtensorMap *tmap_sgn = nullptr, unsigned int *stg_done = nullptr) {
+                                           const CUtensorMap *tmap_sgn = nullptr, GemmCtl *ctl = nullptr) {
     using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
     static_assert(STG == 0 || (STG == 1 && SPLIT == 1 && !PLANE && EPI == kEpiFwd1),
                   "in-kernel staging: the a-product stages x");
@@ -817,11 +818,13 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             // maps are x, f32, in 256 x 16 boxes for the ring and 256 x 64 for
             // the L2 prefetches)
             if (t < kStgConvThreads)
-                stager_x_convert(X, t, abort_flag, L.sStg, L.stg_full, L.stg_empty, stg_done, args.status);
+                stager_x_convert(X, t, abort_flag, L.sStg, L.stg_full, L.stg_empty, ctl->stg_geo, &ctl->stg_done,
+                                 args.status);
             else if (t == kStgConvThreads)
-                stager_x_producer(X, &tmap_in, abort_flag, L.sStg, L.stg_full, L.stg_empty, args.status);
+                stager_x_producer(X, &tmap_in, abort_flag, L.sStg, L.stg_full, L.stg_empty, ctl->stg_geo,
+                                  args.status);
             else if (t == kStgConvThreads + 32)
-                stager_x_publisher(X, tmap_sgn, abort_flag, stg_done, args.status);
+                stager_x_publisher(X, tmap_sgn, abort_flag, &ctl->stg_done, args.status);
             __syncwarp();
         }
     }
@@ -839,7 +842,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
 template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 __device__ __forceinline__ void gemm_prefetch_maps(const CUtensorMap &tmap_act, const CUtensorMap &tmap_in,
                                                    const CUtensorMap &tmap_out32, const CUtensorMap &tmap_out16,
-                                                   const CUtensorMap *tmap_sgn = nullptr, unsigned int *stg_done = nullptr) {
+                                                   const CUtensorMap *tmap_sgn = nullptr) {
     using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     if (warp == kWarpTma && lane == 0) {
@@ -899,7 +902,7 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads
     const int num_units = (int)gridDim.x / per_unit;
     gemm_roles<EPI, PAIR, BT, PLANE, SPLIT, STG>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
                                                  reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units,
-                                                 &tmap_sgn, &ctl->stg_done);
+                                                 &tmap_sgn, ctl);
     tc_fence_before();
     if constexpr (PAIR) {
         // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it

@@ -52,15 +52,17 @@ constexpr int kStgConvThreads = kStgConvWarps * 32;
 constexpr int kStgWarps = kStgConvWarps + 2;     // + the copy producer and the publisher
 constexpr int kStgThreads = kStgWarps * 32;
 constexpr int kStgKC = kStageChunkCols;  // columns per chunk: one float4 per stager thread
-constexpr int kStgRingBytes = 48 * 1024;
 constexpr int kStgSlotsMax = 8;
-// items of 64 rows x 256 columns, ring units of 16 rows (16 KB f32, one TMA
-// box: x is read through a tensor map with a 256 x 16 box)
+// items of 64 rows x 256 columns, ring units of 16 rows: a slot holds the
+// unit's f32 tile (16 KB, one TMA box: x is read through a tensor map with a
+// 256 x 16 box) and the item's 256 g factors (1 KB)
 constexpr int kStgRowsX = 64;
 constexpr int kStgUnitRows = 16;
 constexpr int kStgUnitsX = kStgRowsX / kStgUnitRows;
-constexpr int kStgSlotX = kStgUnitRows * kStgKC * 4;
-constexpr int kStgSlotsX = kStgRingBytes / kStgSlotX;
+constexpr int kStgTileBytes = kStgUnitRows * kStgKC * 4;
+constexpr int kStgSlotX = kStgTileBytes + kStgKC * 4;
+constexpr int kStgSlotsX = 3;
+constexpr int kStgRingBytes = kStgSlotsX * kStgSlotX;
 constexpr int kStgPrefetchItems = 2;  // items prefetched into L2 ahead of the one being converted
 static_assert(kStgSlotsX >= 2 && kStgSlotsX <= kStgSlotsMax, "stager ring");
 
@@ -214,9 +216,20 @@ struct StgX {
     }
 };
 
-// lane 0 of the producer warp: ring units by TMA, S ahead of the converters
+// Where a ring unit's rows go (written by the copy producer with the unit's
+// copies, read by the converters after the slot's full barrier).
+struct StgGeo {
+    int q0;  // first row
+    int nq;  // rows of x in the unit (0 .. 16)
+    int c0;  // first column
+    int pad;
+};
+
+// lane 0 of the producer warp: ring units by TMA, S ahead of the converters,
+// each with its geometry and the item's g factors
 __device__ inline void stager_x_producer(const StgX &X, const CUtensorMap *tmap_x, volatile int *abort_flag,
-                                         uint8_t *ring, uint64_t *full, uint64_t *empty, uint32_t *status) {
+                                         uint8_t *ring, uint64_t *full, uint64_t *empty, StgGeo *geo,
+                                         uint32_t *status) {
     constexpr int S = kStgSlotsX;
     const uint64_t once = l2_policy_evict_first();
     XCursor ci{0, 0, 0, 0, 0, 0, 0, 0};
@@ -225,9 +238,15 @@ __device__ inline void stager_x_producer(const StgX &X, const CUtensorMap *tmap_
     for (; u < X.units; ++u) {
         const int sl = (int)(u % S);
         if (u >= S && !mbar_wait(&empty[sl], (uint32_t)(((u / S) - 1) & 1), abort_flag)) break;
-        // one box of 256 columns x 16 rows (rows and columns past x read zero)
-        mbar_arrive_expect_tx(&full[sl], (uint32_t)kStgSlotX);
-        tma_load_2d_hint(ring + sl * kStgSlotX, tmap_x, &full[sl], ci.c0, ci.r0 + kStgUnitRows * ci.s, once);
+        const int q0 = ci.r0 + kStgUnitRows * ci.s;
+        int nq = ci.r0 + ci.nr - q0;
+        nq = nq < 0 ? 0 : (nq > kStgUnitRows ? kStgUnitRows : nq);
+        geo[sl] = StgGeo{q0, nq, ci.c0, 0};
+        // one box of 256 columns x 16 rows (rows and columns past x read
+        // zero), and the chunk's g factors
+        mbar_arrive_expect_tx(&full[sl], (uint32_t)(kStgTileBytes + ci.w * 4));
+        tma_load_2d_hint(ring + sl * kStgSlotX, tmap_x, &full[sl], ci.c0, q0, once);
+        bulk_load(ring + sl * kStgSlotX + kStgTileBytes, X.a.col + ci.c0, (uint32_t)ci.w * 4, &full[sl]);
         x_cursor_next(ci, X.G, X.mine, X.cta, X.nctas);
     }
     // every copy issued lands before the CTA may exit: for each slot, the
@@ -276,26 +295,17 @@ __device__ inline void stager_x_publisher(const StgX &X, const CUtensorMap *tmap
 
 // converter warps: thread t < kStgConvThreads converts columns 8 (t % 32) ..
 // + 7 of the chunk in the rows t / 32, t / 32 + kStgConvWarps, ... of each
-// unit (one 16-byte store each). Software-pipelined over the units: the next
-// unit's shared-memory loads are in flight while the current unit converts;
-// the g factors of the next item are loaded a whole item ahead.
+// unit (one 16-byte store each); a unit's geometry and g factors come with
+// its slot. Software-pipelined over the units: the next unit's shared-memory
+// loads are in flight while the current unit converts.
 __device__ inline void stager_x_convert(const StgX &X, int t, volatile int *abort_flag, uint8_t *ring,
-                                        uint64_t *full, uint64_t *empty, unsigned int *done, uint32_t *status) {
+                                        uint64_t *full, uint64_t *empty, const StgGeo *geo, unsigned int *done,
+                                        uint32_t *status) {
     constexpr int S = kStgSlotsX;
     constexpr int kRows = kStgUnitRows / kStgConvWarps;
     const int cg = t & 31, rp = t >> 5, lane = t & 31;
-    const StageArgs &a = X.a;
-    const StgGeom &G = X.G;
-    XCursor cc{0, 0, 0, 0, 0, 0, 0, 0}, cn{1, 0, 0, 0, 0, 0, 0, 0};
-    x_cursor_load(cc, G, X.mine, X.cta, X.nctas);
-    auto load_g = [&](const XCursor &c, float4 &g0, float4 &g1) {
-        const int col = c.c0 + 8 * cg;
-        const bool cv = c.j < X.mine && col < (int)G.K;
-        g0 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        g1 = cv ? __ldg(reinterpret_cast<const float4 *>(a.col + col) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-    };
-    // wait for unit u's copy and load this thread's rows of it (the loads do
-    // not depend on which item the unit belongs to)
+    const int K = (int)X.G.K;
+    // wait for unit u's copy and load this thread's rows of it
     auto fetch = [&](long long u, float4 (&v)[kRows][2]) -> bool {
         const int sl = (int)(u % S);
         const bool got = mbar_wait(&full[sl], (uint32_t)((u / S) & 1), abort_flag);
@@ -313,53 +323,44 @@ __device__ inline void stager_x_convert(const StgX &X, int t, volatile int *abor
         }
         return got;
     };
-    float4 g0, g1, gn0, gn1;
-    load_g(cc, g0, g1);
-    cn.j = 1;
-    x_cursor_load(cn, G, X.mine, X.cta, X.nctas);
-    load_g(cn, gn0, gn1);
     float4 va[kRows][2], vb[kRows][2];
     bool got_a = X.units > 0 && fetch(0, va);
     bool ok = true;
     for (long long u = 0; u < X.units; ++u) {
-        const int s = (int)(u % kStgUnitsX);
+        const int sl = (int)(u % S);
         // the next unit's loads go out first
-        const bool has_next = u + 1 < X.units;
-        const bool got_b = has_next && fetch(u + 1, vb);
-        const int q0 = cc.r0 + kStgUnitRows * s;
-        const int nq = min(kStgUnitRows, cc.r0 + cc.nr - q0);
-        const int col = cc.c0 + 8 * cg;
-        if (got_a && col < (int)G.K) {
-            uint16_t *dst = a.dst + (size_t)(q0 + rp) * G.K + col;
+        const bool got_b = u + 1 < X.units && fetch(u + 1, vb);
+        if (got_a) {
+            const StgGeo gq = geo[sl];
+            const int col = gq.c0 + 8 * cg;
+            if (col < K) {
+                const float4 *gs = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX + kStgTileBytes) + 2 * cg;
+                const float4 g0 = gs[0], g1 = gs[1];
+                uint16_t *dst = X.a.dst + (size_t)(gq.q0 + rp) * K + col;
 #pragma unroll
-            for (int i = 0; i < kRows; ++i)
-                if (rp + kStgConvWarps * i < nq) {
-                    uint4 o;
-                    o.x = mul_pack_half2(va[i][0].x, va[i][0].y, g0.x, g0.y);
-                    o.y = mul_pack_half2(va[i][0].z, va[i][0].w, g0.z, g0.w);
-                    o.z = mul_pack_half2(va[i][1].x, va[i][1].y, g1.x, g1.y);
-                    o.w = mul_pack_half2(va[i][1].z, va[i][1].w, g1.z, g1.w);
-                    *reinterpret_cast<uint4 *>(dst + (size_t)i * kStgConvWarps * G.K) = o;
-                }
+                for (int i = 0; i < kRows; ++i)
+                    if (rp + kStgConvWarps * i < gq.nq) {
+                        uint4 o;
+                        o.x = mul_pack_half2(va[i][0].x, va[i][0].y, g0.x, g0.y);
+                        o.y = mul_pack_half2(va[i][0].z, va[i][0].w, g0.z, g0.w);
+                        o.z = mul_pack_half2(va[i][1].x, va[i][1].y, g1.x, g1.y);
+                        o.w = mul_pack_half2(va[i][1].z, va[i][1].w, g1.z, g1.w);
+                        *reinterpret_cast<uint4 *>(dst + (size_t)i * kStgConvWarps * K) = o;
+                    }
+            }
         }
         // unit u's slot goes back to the producer once the whole warp has
         // converted it (a slot whose copy may still be landing is never handed back)
         const bool warp_got = __all_sync(0xFFFFFFFFu, got_a);
-        if (warp_got && lane == 0) mbar_arrive(&empty[(int)(u % S)]);
+        if (warp_got && lane == 0) mbar_arrive(&empty[sl]);
         ok = ok && warp_got;
-        if (s == kStgUnitsX - 1) {
+        if (u % kStgUnitsX == kStgUnitsX - 1) {
             if (!ok || *abort_flag) break;
             // the item's rows are written: proxy fence (the TMA loads of other
             // CTAs read them), then one arrival of this warp on the item counter
             fence_proxy_async_global();
             __syncwarp();
             if (lane == 0) red_release_shared_add_u32(done, 1u);
-            cc = cn;
-            g0 = gn0;
-            g1 = gn1;
-            cn.j = cc.j + 1;
-            x_cursor_load(cn, G, X.mine, X.cta, X.nctas);
-            load_g(cn, gn0, gn1);
         }
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
