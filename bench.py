@@ -1,20 +1,24 @@
 """Benchmark of the blr layer's forward+backward step on GB300.
 
-One step = blr_forward + blr_backward over one batch of synthetic tokens (every
-kernel of the hot path). Prints ONE JSON line (rank 0).
+One step = blr_forward + blr_backward of every layer of the workload over one
+batch of synthetic tokens (every kernel of the hot path); the default workload
+is the SwiGLU MLP pair (up 4096 -> 12288 and down 12288 -> 4096, r = 1024,
+16384 tokens). Prints ONE JSON line (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload small]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mlp]
   python bench.py --impl reference ...     # the CPU f64 oracle as the reference arm
 
 Timing: W untimed warm-up steps, then K timed steps between a barrier and
 cudaDeviceSynchronize on both sides, measured with CUDA events on the launch
 stream; max over ranks. L2 (129 MB) is defeated by rotating independent
-input/output/workspace sets whose total exceeds twice the L2 size. Kernel-level
-durations for the roofline come from the library's event trace over an eager
-pass of the same K steps. Steps are timed as CUDA-graph replays (one graph
-per buffer set, captured from the same library calls), so host launch cost is
-not in the device time; the end-to-end number keeps every host call. Multi-GPU: every rank runs its own batch
-(weak scaling); the path needs no collective inside a step.
+input/output/workspace sets whose total exceeds twice the L2 size. Steps are
+timed as CUDA-graph replays (one graph per buffer set, captured from the same
+library calls), so host launch cost is not in the device time; the
+end-to-end number keeps every host call. Kernel-level durations for the
+roofline come from the same graphs captured a second time with the library's
+event trace on, whose event-record nodes bracket every kernel inside the
+replays. Multi-GPU: every rank runs its own batch (weak scaling); the path
+needs no collective inside a step.
 """
 from __future__ import annotations
 

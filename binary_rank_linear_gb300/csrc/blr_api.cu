@@ -137,6 +137,35 @@ bool make_tmap_act16(CUtensorMap *m, const void *base, int rows, int K, int box_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Maps of the layer GEMMs (blr_gemm.cuh), 3-D: [planes][rows][cols] with
+// plane p `pstride` bytes after plane 0, one plane per path of a multi-path
+// launch (planes = 1 for a single path and for the tensors the paths share).
+// act: f16 activation operand, box 64 x box_rows, 128-byte swizzle, rows and
+// columns past the extent read zero. chunk: f32 or f16 epilogue chunks, box
+// 32 x 32, no swizzle; loads read zeros out of range, stores are clipped.
+bool make_gmap(CUtensorMap *m, const void *base, int rows, int cols, bool f16, int box_cols, int box_rows,
+               CUtensorMapSwizzle sw, int planes, long long pstride) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || planes < 1) return false;
+    const cuuint64_t esz = f16 ? 2 : 4;
+    const cuuint64_t plane_bytes = ((cuuint64_t)rows * cols * esz + 15) / 16 * 16;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * esz, planes > 1 ? (cuuint64_t)pstride : plane_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_gmap_act(CUtensorMap *m, const void *base, int rows, int K, int box_rows, int planes = 1,
+                   long long pstride = 0) {
+    return make_gmap(m, base, rows, K, true, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B, planes, pstride);
+}
+bool make_gmap_chunk(CUtensorMap *m, const void *base, int rows, int cols, bool f16, int planes = 1,
+                     long long pstride = 0) {
+    return make_gmap(m, base, rows, cols, f16, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE, planes, pstride);
+}
+
 // x f32 [rows][cols] with a 256 x box_rows box, no swizzle: the in-kernel x
 // staging's ring units (16 rows) and L2 prefetches (64 rows); rows and
 // columns past the extent read zero.
@@ -301,9 +330,11 @@ namespace blr {
 // (160 or 192: MMAs of N >= 160 run at full rate) that needs the fewest
 // token-rounds of the persistent grid; otherwise single CTAs with 128-token
 // tiles, for more tiles in flight on small problems.
-GemmPlan plan_gemm(int M, int N, int sms, int min_bt, int tile_cost) {
+// `paths` > 1 plans a grouped launch whose units share the tiles of that many
+// paths (the a- and db-products: tiles x paths in all).
+GemmPlan plan_gemm(int M, int N, int sms, int min_bt, int tile_cost, int paths) {
     const int pairs = sms / 2;
-    const long long fp = (N + 255) / 256;
+    const long long fp = (N + 255) / 256 * paths;
     GemmPlan best{false, 0, 0, 0};
     long long best_cost = 0;
     for (int bt : {192, 160}) {
@@ -324,7 +355,7 @@ GemmPlan plan_gemm(int M, int N, int sms, int min_bt, int tile_cost) {
     // keeps 128-token tiles
     const char *v = std::getenv("BLR_GEMM_BT");
     if (v && std::strcmp(v, "128") == 0) min_bt = 128;
-    const long long fs = (N + 127) / 128;
+    const long long fs = (N + 127) / 128 * paths;
     int bt = 128;
     while (bt > min_bt && 2 * ((M + bt - 1) / bt) * fs <= sms && M > bt / 2) bt /= 2;
     const long long t_tiles = (M + bt - 1) / bt;
@@ -447,6 +478,180 @@ GridBarrier grid_barrier(unsigned int *gbar) {
 
 // The per-path pointers of a multi-path call: every array present, every entry
 // non-null and 16-byte aligned.
+// Multi-path passes run grouped: one launch per stage of the pass for up to
+// kMaxGroupPaths paths (the prologues and the reduction with a block row per
+// path, the GEMMs with the paths in their tile sequence; y and dx receive the
+// paths' contributions in path order), unless BLR_PATHS=loop asks for the
+// paths' single-path passes in turn, or an option without a grouped form is
+// on (fused small-M kernels, sign planes, token-major wide products, split-K).
+bool paths_grouped() {
+    const char *v = std::getenv("BLR_PATHS");
+    if (v && std::strcmp(v, "loop") == 0) return false;
+    const char *k = std::getenv("BLR_SPLITK");
+    if (k && std::strcmp(k, "1") == 0) return false;
+    return !plane_mode() && !wide_token_major() && !fused_small_enabled();
+}
+
+// Forward of paths [0, n) of a multi-path layer (n <= kMaxGroupPaths), path
+// p on the workspace slice at ws0 + p * one: one prologue (x staged n times,
+// with each path's g), one a-product, one c-product.
+int forward_grouped(const float *x, int n, const uint32_t *const *bits_u, const uint32_t *const *bits_v,
+                    const float *const *g, const float *const *l, const float *const *h, float *y, int accumulate_y,
+                    int M, int d_in, int d_out, int r, char *ws0, size_t one, int sms, cudaStream_t s) {
+    const Layout L = make_layout(M, d_in, d_out, r);
+    const GemmPlan p1 = plan_gemm(M, r, sms, 32, 0, n);
+    const GemmPlan p2 = plan_gemm(M, d_out, sms, 64, kWideTileCost);
+    const long long ps = (long long)one;
+    GemmMaps m1{}, m2{};
+    if (!make_gmap_act(&m1.act, ws0 + L.x16, M, d_in, p1.pair ? p1.bt / 2 : p1.bt, n, ps) ||
+        !make_gmap_chunk(&m1.out32, ws0 + L.a32, M, r, false, n, ps) ||
+        !make_gmap_chunk(&m1.out16, ws0 + L.al16, M, r, true, n, ps) ||
+        !make_gmap_act(&m2.act, ws0 + L.al16, M, r, p2.pair ? p2.bt / 2 : p2.bt, n, ps) ||
+        !make_gmap_chunk(&m2.in32, y, M, d_out, false) || !make_gmap_chunk(&m2.out32, y, M, d_out, false) ||
+        !make_gmap_chunk(&m2.out16, ws0 + L.c16, M, d_out, true, n, ps))
+        return BLR_ERR_CUDA;
+    FwdGroup grp{};
+    grp.n = n;
+    GemmArgs f1{}, f2{};
+    for (int p = 0; p < n; ++p) {
+        char *w = ws0 + (size_t)p * one;
+        grp.e[p] = FwdPathArgs{SignPrep{bits_v[p], reinterpret_cast<uint32_t *>(w + L.bp_f1), r, d_in, 1, sign_rows(r)},
+                               SignPrep{bits_u[p], reinterpret_cast<uint32_t *>(w + L.bp_f2), d_out, r, 0,
+                                        sign_rows(d_out)},
+                               g[p], reinterpret_cast<uint16_t *>(w + L.x16), reinterpret_cast<uint32_t *>(w + L.header)};
+        f1.colv_p[p] = l[p];
+        f2.colv_p[p] = h[p];
+    }
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws0 + L.header);
+    f1.M = M;
+    f1.N = r;
+    f1.K = d_in;
+    f1.Ns = sign_rows(r);
+    f1.bsign = reinterpret_cast<const uint32_t *>(ws0 + L.bp_f1);
+    f1.out32 = reinterpret_cast<float *>(ws0 + L.a32);
+    f1.out16 = reinterpret_cast<uint16_t *>(ws0 + L.al16);
+    f1.colv = l[0];
+    f1.status = status;
+    f1.paths = n;
+    f1.pstride = ps;
+    f2.M = M;
+    f2.N = d_out;
+    f2.K = r;
+    f2.Ns = sign_rows(d_out);
+    f2.bsign = reinterpret_cast<const uint32_t *>(ws0 + L.bp_f2);
+    f2.out32 = y;
+    f2.out16 = reinterpret_cast<uint16_t *>(ws0 + L.c16);
+    f2.colv = h[0];
+    f2.accumulate = accumulate_y;
+    f2.status = status;
+    f2.paths = n;
+    f2.pstride = ps;
+    {
+        std::lock_guard<std::mutex> lk(g_tape_mu);
+        for (int p = 0; p < n; ++p) g_tapes.erase(ws0 + (size_t)p * one);
+    }
+    if (launch_fwd_prologue(grp, x, M, d_in, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiFwd1, p1, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) return BLR_ERR_CUDA;
+    for (int p = 0; p < n; ++p)
+        record_tape(ws0 + (size_t)p * one, Tape{M, d_in, d_out, r, x, bits_u[p], bits_v[p], g[p], l[p], h[p], 0, false,
+                                                0.0f, 0});
+    return BLR_OK;
+}
+
+// Backward of paths [0, n) (tapes checked by the caller): one prologue (dy
+// staged n times, with each path's h, scales and dh partials), one
+// db-product, one dx'-product, one reduction of every path's partial sums.
+int backward_grouped(const float *x, const float *dy, int n, const uint32_t *const *bits_u,
+                     const uint32_t *const *bits_v, const float *const *g, const float *const *l,
+                     const float *const *h, float *dx, int accumulate_dx, float *const *dg, float *const *dl,
+                     float *const *dh, float gscale, int M, int d_in, int d_out, int r, char *ws0, size_t one, int sms,
+                     cudaStream_t s) {
+    const Layout L = make_layout(M, d_in, d_out, r);
+    const GemmPlan p1 = plan_gemm(M, r, sms, 32, 0, n);
+    const GemmPlan p2 = plan_gemm(M, d_in, sms, 64);
+    const long long ps = (long long)one;
+    GemmMaps m1{}, m2{};
+    if (!make_gmap_act(&m1.act, ws0 + L.dy16, M, d_out, p1.pair ? p1.bt / 2 : p1.bt, n, ps) ||
+        !make_gmap_chunk(&m1.in32, ws0 + L.a32, M, r, false, n, ps) ||
+        !make_gmap_chunk(&m1.out16, ws0 + L.db16, M, r, true, n, ps) ||
+        !make_gmap_act(&m2.act, ws0 + L.db16, M, r, p2.pair ? p2.bt / 2 : p2.bt, n, ps) ||
+        !make_gmap_chunk(&m2.in32, x, M, d_in, false) || !make_gmap_chunk(&m2.out32, dx, M, d_in, false))
+        return BLR_ERR_CUDA;
+    int rows_dh = 0;
+    BwdGroup grp{};
+    grp.n = n;
+    GemmArgs b1{}, b2{};
+    for (int p = 0; p < n; ++p) {
+        char *w = ws0 + (size_t)p * one;
+        BwdPathArgs &e = grp.e[p];
+        e.p0 = SignPrep{bits_u[p], reinterpret_cast<uint32_t *>(w + L.bp_b1), r, d_out, 1, sign_rows(r)};
+        e.p1 = SignPrep{bits_v[p], reinterpret_cast<uint32_t *>(w + L.bp_b2), d_in, r, 0, sign_rows(d_in)};
+        StageDyArgs &sa = e.sd;
+        sa.dy = dy;
+        sa.h = h[p];
+        sa.c16 = reinterpret_cast<const uint16_t *>(w + L.c16);
+        sa.l = l[p];
+        sa.dy16 = reinterpret_cast<uint16_t *>(w + L.dy16);
+        sa.s_inv = reinterpret_cast<float *>(w + L.s_inv);
+        sa.sig = reinterpret_cast<float *>(w + L.sig);
+        sa.sig_inv = reinterpret_cast<float *>(w + L.sig_inv);
+        sa.part_dh = reinterpret_cast<float *>(w + L.part_dh);
+        sa.blkmax = reinterpret_cast<float2 *>(w + L.blkmax);
+        sa.gscale = gscale;
+        sa.M = M;
+        sa.d_out = d_out;
+        sa.r = r;
+        sa.rows_used = p == 0 ? &rows_dh : nullptr;
+        sa.status = reinterpret_cast<uint32_t *>(w + L.header);
+        b1.colv_p[p] = l[p];
+        b2.colv_p[p] = g[p];
+    }
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws0 + L.header);
+    b1.M = M;
+    b1.N = r;
+    b1.K = d_out;
+    b1.Ns = sign_rows(r);
+    b1.bsign = reinterpret_cast<const uint32_t *>(ws0 + L.bp_b1);
+    b1.out16 = reinterpret_cast<uint16_t *>(ws0 + L.db16);
+    b1.colv = l[0];
+    b1.row_inv = reinterpret_cast<const float *>(ws0 + L.s_inv);
+    b1.row_scale = reinterpret_cast<const float *>(ws0 + L.sig);
+    b1.part = reinterpret_cast<float *>(ws0 + L.part_dl);
+    b1.status = status;
+    b1.paths = n;
+    b1.pstride = ps;
+    b2.M = M;
+    b2.N = d_in;
+    b2.K = r;
+    b2.Ns = sign_rows(d_in);
+    b2.bsign = reinterpret_cast<const uint32_t *>(ws0 + L.bp_b2);
+    b2.out32 = dx;
+    b2.colv = g[0];
+    b2.row_inv = reinterpret_cast<const float *>(ws0 + L.sig_inv);
+    b2.part = reinterpret_cast<float *>(ws0 + L.part_dg);
+    b2.accumulate = accumulate_dx;
+    b2.status = status;
+    b2.paths = n;
+    b2.pstride = ps;
+    if (launch_bwd_prologue(grp, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) return BLR_ERR_CUDA;
+    ReduceGroup rg{};
+    rg.n = n;
+    for (int p = 0; p < n; ++p) {
+        char *w = ws0 + (size_t)p * one;
+        rg.a[p] = ReduceSeg{reinterpret_cast<const float *>(w + L.part_dh), dh[p], rows_dh, d_out};
+        rg.b[p] = ReduceSeg{reinterpret_cast<const float *>(w + L.part_dl), dl[p],
+                            p1.part_rows * epi_part_rows_per_tile(kEpiBwd1), r};
+        rg.c[p] = ReduceSeg{reinterpret_cast<const float *>(w + L.part_dg), dg[p],
+                            p2.part_rows * epi_part_rows_per_tile(kEpiBwd2), d_in};
+    }
+    if (launch_reduce_partials(rg, s) != cudaSuccess) return BLR_ERR_CUDA;
+    for (int p = 0; p < n; ++p) mark_backward_done(ws0 + (size_t)p * one, gscale, rows_dh);
+    return BLR_OK;
+}
+
 template <typename T>
 bool path_ptrs_ok(T *const *a, int P, int *status) {
     if (!a) {
@@ -562,11 +767,11 @@ int blr_forward(const float *x, const uint32_t *bits_u, const uint32_t *bits_v, 
     // a-product: S_V [d_in][r] read MN-major; c-product: S_U [d_out][r] read K-major
     if (planes && (!make_tmap_act16(&m1.sgn, plane_v, d_in, r, 64) || !make_tmap_act16(&m2.sgn, plane_u, d_out, r, 128)))
         return BLR_ERR_CUDA;
-    if (!make_tmap_act16(&m1.act, x16, M, d_in, p1.pair ? p1.bt / 2 : p1.bt) ||
-        !make_tmap_chunk(&m1.out32, a32, M, r, false) || !make_tmap_chunk(&m1.out16, al16, M, r, true) ||
-        !make_tmap_act16(&m2.act, al16, M, r, p2.pair ? p2.bt / 2 : p2.bt) ||
-        !make_tmap_chunk(&m2.in32, y, M, d_out, false) || !make_tmap_chunk(&m2.out32, y, M, d_out, false) ||
-        !make_tmap_chunk(&m2.out16, c16, M, d_out, true))
+    if (!make_gmap_act(&m1.act, x16, M, d_in, p1.pair ? p1.bt / 2 : p1.bt) ||
+        !make_gmap_chunk(&m1.out32, a32, M, r, false) || !make_gmap_chunk(&m1.out16, al16, M, r, true) ||
+        !make_gmap_act(&m2.act, al16, M, r, p2.pair ? p2.bt / 2 : p2.bt) ||
+        !make_gmap_chunk(&m2.in32, y, M, d_out, false) || !make_gmap_chunk(&m2.out32, y, M, d_out, false) ||
+        !make_gmap_chunk(&m2.out16, c16, M, d_out, true))
         return BLR_ERR_CUDA;
 
     // a new forward starts a new tape: forget the old one first
@@ -717,10 +922,10 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
     // db-product: S_U [d_out][r] read MN-major; dx'-product: S_V [d_in][r] read K-major
     if (planes && (!make_tmap_act16(&m1.sgn, plane_u, d_out, r, 64) || !make_tmap_act16(&m2.sgn, plane_v, d_in, r, 128)))
         return BLR_ERR_CUDA;
-    if (!make_tmap_act16(&m1.act, dy16, M, d_out, p1.pair ? p1.bt / 2 : p1.bt) ||
-        !make_tmap_chunk(&m1.in32, a32, M, r, false) || !make_tmap_chunk(&m1.out16, db16, M, r, true) ||
-        !make_tmap_act16(&m2.act, db16, M, r, p2.pair ? p2.bt / 2 : p2.bt) ||
-        !make_tmap_chunk(&m2.in32, x, M, d_in, false) || !make_tmap_chunk(&m2.out32, dx, M, d_in, false))
+    if (!make_gmap_act(&m1.act, dy16, M, d_out, p1.pair ? p1.bt / 2 : p1.bt) ||
+        !make_gmap_chunk(&m1.in32, a32, M, r, false) || !make_gmap_chunk(&m1.out16, db16, M, r, true) ||
+        !make_gmap_act(&m2.act, db16, M, r, p2.pair ? p2.bt / 2 : p2.bt) ||
+        !make_gmap_chunk(&m2.in32, x, M, d_in, false) || !make_gmap_chunk(&m2.out32, dx, M, d_in, false))
         return BLR_ERR_CUDA;
 
     // S_U [d_out][r/32] has its bits along r: the first product needs them along d_out
@@ -828,6 +1033,22 @@ int blr_forward_paths(const float *x, int P, const uint32_t *const *bits_u, cons
         return st;
     const size_t one = make_layout(M, d_in, d_out, r).total;
     if (ws_bytes < (size_t)P * one) return BLR_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(ws)) return BLR_ERR_ALIGN;
+    if (P > 1 && paths_grouped()) {
+        int sms;
+        st = device_info(&sms);
+        if (st != BLR_OK) return st;
+        if (fault_injected("forward")) return BLR_ERR_CUDA;
+        // groups of up to kMaxGroupPaths paths; later groups add into y
+        for (int p0 = 0; p0 < P; p0 += kMaxGroupPaths) {
+            const int n = P - p0 < kMaxGroupPaths ? P - p0 : kMaxGroupPaths;
+            st = forward_grouped(x, n, bits_u + p0, bits_v + p0, g + p0, l + p0, h + p0, y,
+                                 (p0 > 0 || accumulate_y) ? 1 : 0, M, d_in, d_out, r,
+                                 static_cast<char *>(ws) + (size_t)p0 * one, one, sms, (cudaStream_t)stream);
+            if (st != BLR_OK) return st;
+        }
+        return BLR_OK;
+    }
     for (int p = 0; p < P; ++p) {
         st = blr_forward(x, bits_u[p], bits_v[p], g[p], l[p], h[p], y, (p > 0 || accumulate_y) ? 1 : 0, M, d_in,
                          d_out, r, static_cast<char *>(ws) + (size_t)p * one, one, stream);
@@ -857,6 +1078,21 @@ int blr_backward_paths(const float *x, const float *dy, int P, const uint32_t *c
         if (!tape_matches(static_cast<char *>(ws) + (size_t)p * one, M, d_in, d_out, r, x, bits_u[p], bits_v[p], g[p],
                           l[p], h[p]))
             return BLR_ERR_STATE;
+    if (!aligned16(x) || !aligned16(dy) || !aligned16(dx) || !aligned16(ws)) return BLR_ERR_ALIGN;
+    if (P > 1 && paths_grouped()) {
+        int sms;
+        st = device_info(&sms);
+        if (st != BLR_OK) return st;
+        if (fault_injected("backward")) return BLR_ERR_CUDA;
+        for (int p0 = 0; p0 < P; p0 += kMaxGroupPaths) {
+            const int n = P - p0 < kMaxGroupPaths ? P - p0 : kMaxGroupPaths;
+            st = backward_grouped(x, dy, n, bits_u + p0, bits_v + p0, g + p0, l + p0, h + p0, dx,
+                                  (p0 > 0 || accumulate_dx) ? 1 : 0, dg + p0, dl + p0, dh + p0, gscale, M, d_in, d_out,
+                                  r, static_cast<char *>(ws) + (size_t)p0 * one, one, sms, (cudaStream_t)stream);
+            if (st != BLR_OK) return st;
+        }
+        return BLR_OK;
+    }
     for (int p = 0; p < P; ++p) {
         st = blr_backward(x, dy, bits_u[p], bits_v[p], g[p], l[p], h[p], dx, (p > 0 || accumulate_dx) ? 1 : 0, dg[p],
                           dl[p], dh[p], gscale, M, d_in, d_out, r, static_cast<char *>(ws) + (size_t)p * one, one,

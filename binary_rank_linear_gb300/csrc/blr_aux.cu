@@ -71,44 +71,46 @@ __device__ __forceinline__ bool prologue_prep(const SignPrep &p0, const SignPrep
     return false;
 }
 
-__global__ void __launch_bounds__(256) fwd_prologue_kernel(SignPrep p0, SignPrep p1, const float *x, const float *g,
-                                                           uint16_t *x16, int M, int d_in, uint32_t *status,
+// (Forward and backward prologues: block row blockIdx.y works for path
+// blockIdx.y of the group.)
+__global__ void __launch_bounds__(256) fwd_prologue_kernel(const FwdGroup grp, const float *x, int M, int d_in,
                                                            int stage_blocks) {
+    const FwdPathArgs &a = grp.e[blockIdx.y];
     pdl_wait();
     pdl_launch_dependents();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
-    if (prologue_prep(p0, p1, stage_blocks)) return;
-    stage_x_run(x, g, x16, M, d_in, blockIdx.x, stage_blocks);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+    if (prologue_prep(a.p0, a.p1, stage_blocks)) return;
+    stage_x_run(x, a.g, a.x16, M, d_in, blockIdx.x, stage_blocks);
 }
 
 // The same prologue with x staged by rows (d_in up to kSxMaxCols).
 template <int KQ>
-__global__ void __launch_bounds__(512) fwd_prologue_rows_kernel(SignPrep p0, SignPrep p1, const float *x,
-                                                                const float *g, uint16_t *x16, int M, int d_in,
-                                                                uint32_t *status, int stage_blocks) {
+__global__ void __launch_bounds__(512) fwd_prologue_rows_kernel(const FwdGroup grp, const float *x, int M,
+                                                                int d_in, int stage_blocks) {
+    const FwdPathArgs &a = grp.e[blockIdx.y];
     pdl_wait();
     pdl_launch_dependents();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
-    if (prologue_prep(p0, p1, stage_blocks)) return;
-    stage_x_rows<KQ>(x, g, x16, M, d_in, blockIdx.x, stage_blocks);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+    if (prologue_prep(a.p0, a.p1, stage_blocks)) return;
+    stage_x_rows<KQ>(x, a.g, a.x16, M, d_in, blockIdx.x, stage_blocks);
 }
 
 // The same prologue with x streamed through a shared-memory ring (one block
 // per SM; blocks past stage_blocks only do bitmap re-layouts).
 template <int KQ>
 __global__ void __launch_bounds__(kSxsThreads, 1)
-    fwd_prologue_stream_kernel(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
-                               int d_in, uint32_t *status, int stage_blocks) {
+    fwd_prologue_stream_kernel(const FwdGroup grp, const float *x, int M, int d_in, int stage_blocks) {
     extern __shared__ __align__(128) unsigned char smem_b[];
+    const FwdPathArgs &a = grp.e[blockIdx.y];
     pdl_wait();
     pdl_launch_dependents();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
     const int extra = (int)gridDim.x - stage_blocks;
     if (extra > 0 && (int)blockIdx.x >= stage_blocks) {
-        prep_share(p0, p1, (int)blockIdx.x - stage_blocks, extra);
+        prep_share(a.p0, a.p1, (int)blockIdx.x - stage_blocks, extra);
         return;
     }
-    stage_x_stream<KQ>(x, g, x16, M, d_in, blockIdx.x, stage_blocks, smem_b, status, p0, p1,
+    stage_x_stream<KQ>(x, a.g, a.x16, M, d_in, blockIdx.x, stage_blocks, smem_b, a.status, a.p0, a.p1,
                        extra > 0 ? 0 : stage_blocks);
 }
 
@@ -125,12 +127,13 @@ __global__ void __launch_bounds__(256) prep_kernel(SignPrep p0, SignPrep p1, uin
 
 template <int GPT, int THREADS>
 __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
-    bwd_prologue_kernel(SignPrep p0, SignPrep p1, StageDyArgs a, int stage_blocks) {
+    bwd_prologue_kernel(const BwdGroup grp, int stage_blocks) {
     extern __shared__ __align__(16) float smem_f[];
+    const BwdPathArgs &e = grp.e[blockIdx.y];
     pdl_wait();
     pdl_launch_dependents();
-    if (prologue_prep(p0, p1, stage_blocks)) return;
-    stage_dy_run<GPT>(a, blockIdx.x, stage_blocks, smem_f, stage_tpr(a.d_out, THREADS), THREADS);
+    if (prologue_prep(e.p0, e.p1, stage_blocks)) return;
+    stage_dy_run<GPT>(e.sd, blockIdx.x, stage_blocks, smem_f, stage_tpr(e.sd.d_out, THREADS), THREADS);
 }
 
 // Streaming form of the same prologue (rows up to kSdMaxCols wide): one block
@@ -138,16 +141,17 @@ __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
 // Blocks past stage_blocks only do bitmap re-layouts.
 template <int Q>
 __global__ void __launch_bounds__(kSdThreads, 1)
-    bwd_stream_kernel(SignPrep p0, SignPrep p1, StageDyArgs a, int stage_blocks) {
+    bwd_stream_kernel(const BwdGroup grp, int stage_blocks) {
     extern __shared__ __align__(128) unsigned char smem_b[];
+    const BwdPathArgs &e = grp.e[blockIdx.y];
     pdl_wait();
     pdl_launch_dependents();
     const int extra = (int)gridDim.x - stage_blocks;
     if (extra > 0 && (int)blockIdx.x >= stage_blocks) {
-        prep_share(p0, p1, (int)blockIdx.x - stage_blocks, extra);
+        prep_share(e.p0, e.p1, (int)blockIdx.x - stage_blocks, extra);
         return;
     }
-    stage_dy_stream<Q>(a, blockIdx.x, stage_blocks, smem_b, p0, p1, extra > 0 ? 0 : stage_blocks);
+    stage_dy_stream<Q>(e.sd, blockIdx.x, stage_blocks, smem_b, e.p0, e.p1, extra > 0 ? 0 : stage_blocks);
 }
 
 int stage_dy_blocks(int M, int d_out) {
@@ -165,8 +169,10 @@ int stage_dy_blocks(int M, int d_out) {
 constexpr int kReduceWarps = 32;
 constexpr int kReduceCols = 128;
 
-__global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(ReduceSeg a, ReduceSeg b, ReduceSeg c) {
+__global__ void __launch_bounds__(kReduceWarps * 32) reduce_partials_kernel(const ReduceGroup grp) {
     __shared__ float4 red[kReduceWarps][32];
+    // block row blockIdx.y: the segments of path blockIdx.y of the group
+    const ReduceSeg &a = grp.a[blockIdx.y], &b = grp.b[blockIdx.y], &c = grp.c[blockIdx.y];
     pdl_wait();
     pdl_launch_dependents();
     const int nba = (a.n + kReduceCols - 1) / kReduceCols, nbb = (b.n + kReduceCols - 1) / kReduceCols;
@@ -283,8 +289,7 @@ cudaError_t launch_unpack_signs(const uint32_t *bits, uint16_t *dst, int rows, i
 }
 
 template <int KQ>
-static cudaError_t launch_fwd_prologue_rows(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16,
-                                           int M, int d_in, uint32_t *status, cudaStream_t s) {
+static cudaError_t launch_fwd_prologue_rows(const FwdGroup &grp, const float *x, int M, int d_in, cudaStream_t s) {
     cudaError_t pe = prepare_kernel_once(fwd_prologue_rows_kernel<KQ>, 0);
     if (pe != cudaSuccess) return pe;
     const int T = sx_threads(d_in);
@@ -292,35 +297,33 @@ static cudaError_t launch_fwd_prologue_rows(SignPrep p0, SignPrep p1, const floa
                      current_device_sms();
     const int nchunks = (M + sx_rows(KQ) - 1) / sx_rows(KQ);
     const int bs = nchunks < wave ? nchunks : wave;
-    const int pb = prep_blocks(p0, T) + prep_blocks(p1, T);
+    const int pb = prep_blocks(grp.e[0].p0, T) + prep_blocks(grp.e[0].p1, T);
     const int grid = bs + pb <= wave ? bs + pb : bs;
     trace_before("fwd_prologue", s);
-    cudaError_t e = launch_k(fwd_prologue_rows_kernel<KQ>, dim3(grid), dim3(T), 0, s, p0, p1, x, g, x16, M, d_in,
-                             status, bs);
+    cudaError_t e = launch_k(fwd_prologue_rows_kernel<KQ>, dim3(grid, grp.n), dim3(T), 0, s, grp, x, M, d_in, bs);
     trace_after(s);
     return e;
 }
 
 template <int KQ>
-static cudaError_t launch_fwd_prologue_stream(SignPrep p0, SignPrep p1, const float *x, const float *g,
-                                             uint16_t *x16, int M, int d_in, uint32_t *status, cudaStream_t s) {
+static cudaError_t launch_fwd_prologue_stream(const FwdGroup &grp, const float *x, int M, int d_in, cudaStream_t s) {
     cudaError_t pe = prepare_kernel_once(fwd_prologue_stream_kernel<KQ>, kSxsHeadBytes + kSxsRingBytes);
     if (pe != cudaSuccess) return pe;
     const int sms = current_device_sms();
     const SxPlan pl = sxs_plan(d_in);
     int sb = (M + pl.rs - 1) / pl.rs;
     if (sb > sms) sb = sms;
-    const int pb = prep_blocks(p0, kSxsThreads) + prep_blocks(p1, kSxsThreads);
+    const int pb = prep_blocks(grp.e[0].p0, kSxsThreads) + prep_blocks(grp.e[0].p1, kSxsThreads);
     const int grid = sb + pb <= sms ? sb + pb : sb;
     trace_before("fwd_prologue", s);
-    cudaError_t e = launch_k(fwd_prologue_stream_kernel<KQ>, dim3(grid), dim3(kSxsThreads), sxs_smem_bytes(d_in), s,
-                             p0, p1, x, g, x16, M, d_in, status, sb);
+    cudaError_t e = launch_k(fwd_prologue_stream_kernel<KQ>, dim3(grid, grp.n), dim3(kSxsThreads),
+                             sxs_smem_bytes(d_in), s, grp, x, M, d_in, sb);
     trace_after(s);
     return e;
 }
 
-cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
-                                int d_in, uint32_t *status, cudaStream_t s) {
+cudaError_t launch_fwd_prologue(const FwdGroup &grp, const float *x, int M, int d_in, cudaStream_t s) {
+    if (grp.n < 1 || grp.n > kMaxGroupPaths) return cudaErrorInvalidValue;
     // Streaming for large x (measured on GB300: 134 MB of x 43 -> 39 us, 805 MB
     // 233 -> 190 us), rows for small ones (8 MB: 8.2 us rows, 10.4 streamed).
     // BLR_X_STAGE=stream|rows|flat forces a form.
@@ -328,20 +331,20 @@ cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const 
     const bool want_stream = form ? std::strcmp(form, "stream") == 0 : (long long)M * d_in * 4 >= (64ll << 20);
     if (d_in <= kSxMaxCols && want_stream && sxs_plan(d_in).nst >= 2) {
         switch (sx_kq(d_in)) {
-            case 1: return launch_fwd_prologue_stream<1>(p0, p1, x, g, x16, M, d_in, status, s);
-            case 2: return launch_fwd_prologue_stream<2>(p0, p1, x, g, x16, M, d_in, status, s);
-            case 4: return launch_fwd_prologue_stream<4>(p0, p1, x, g, x16, M, d_in, status, s);
-            case 6: return launch_fwd_prologue_stream<6>(p0, p1, x, g, x16, M, d_in, status, s);
-            default: return launch_fwd_prologue_stream<8>(p0, p1, x, g, x16, M, d_in, status, s);
+            case 1: return launch_fwd_prologue_stream<1>(grp, x, M, d_in, s);
+            case 2: return launch_fwd_prologue_stream<2>(grp, x, M, d_in, s);
+            case 4: return launch_fwd_prologue_stream<4>(grp, x, M, d_in, s);
+            case 6: return launch_fwd_prologue_stream<6>(grp, x, M, d_in, s);
+            default: return launch_fwd_prologue_stream<8>(grp, x, M, d_in, s);
         }
     }
     if (d_in <= kSxMaxCols && !(form && std::strcmp(form, "flat") == 0)) {
         switch (sx_kq(d_in)) {
-            case 1: return launch_fwd_prologue_rows<1>(p0, p1, x, g, x16, M, d_in, status, s);
-            case 2: return launch_fwd_prologue_rows<2>(p0, p1, x, g, x16, M, d_in, status, s);
-            case 4: return launch_fwd_prologue_rows<4>(p0, p1, x, g, x16, M, d_in, status, s);
-            case 6: return launch_fwd_prologue_rows<6>(p0, p1, x, g, x16, M, d_in, status, s);
-            default: return launch_fwd_prologue_rows<8>(p0, p1, x, g, x16, M, d_in, status, s);
+            case 1: return launch_fwd_prologue_rows<1>(grp, x, M, d_in, s);
+            case 2: return launch_fwd_prologue_rows<2>(grp, x, M, d_in, s);
+            case 4: return launch_fwd_prologue_rows<4>(grp, x, M, d_in, s);
+            case 6: return launch_fwd_prologue_rows<6>(grp, x, M, d_in, s);
+            default: return launch_fwd_prologue_rows<8>(grp, x, M, d_in, s);
         }
     }
     cudaError_t pe = prepare_kernel_once(fwd_prologue_kernel, 0);
@@ -353,17 +356,18 @@ cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const 
     const long long groups = (long long)M * (d_in / 4);
     const int bs = grid_for(groups, 256 * 8, wave);
     // re-layout-only blocks where the wave has room for them
-    const int pb = prep_blocks(p0, 256) + prep_blocks(p1, 256);
+    const int pb = prep_blocks(grp.e[0].p0, 256) + prep_blocks(grp.e[0].p1, 256);
     const int grid = bs + pb <= wave ? bs + pb : bs;
     trace_before("fwd_prologue", s);
-    cudaError_t e =
-        launch_k(fwd_prologue_kernel, dim3(grid), dim3(256), 0, s, p0, p1, x, g, x16, M, d_in, status, bs);
+    cudaError_t e = launch_k(fwd_prologue_kernel, dim3(grid, grp.n), dim3(256), 0, s, grp, x, M, d_in, bs);
     trace_after(s);
     return e;
 }
 
 template <int GPT, int THREADS = kStageThreads>
-static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
+static cudaError_t launch_bwd_prologue_t(const BwdGroup &grp, cudaStream_t s) {
+    const StageDyArgs &a = grp.e[0].sd;
+    const SignPrep &p0 = grp.e[0].p0, &p1 = grp.e[0].p1;
     const int tpr = stage_tpr(a.d_out, THREADS);
     const int rb_n = THREADS / tpr;
     const size_t smem = stage_dy_smem_bytes(a.d_out, tpr, rb_n * tpr);
@@ -378,14 +382,16 @@ static cudaError_t launch_bwd_prologue_t(SignPrep p0, SignPrep p1, const StageDy
     const int pb = prep_blocks(p0, THREADS) + prep_blocks(p1, THREADS);
     const int grid = sb + pb <= per_sm * sms ? sb + pb : sb;
     trace_before("bwd_prologue", s);
-    cudaError_t e = launch_k(bwd_prologue_kernel<GPT, THREADS>, dim3(grid), dim3(THREADS), smem, s, p0, p1, a, sb);
+    cudaError_t e = launch_k(bwd_prologue_kernel<GPT, THREADS>, dim3(grid, grp.n), dim3(THREADS), smem, s, grp, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;
 }
 
 template <int Q>
-static cudaError_t launch_bwd_stream_t(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
+static cudaError_t launch_bwd_stream_t(const BwdGroup &grp, cudaStream_t s) {
+    const StageDyArgs &a = grp.e[0].sd;
+    const SignPrep &p0 = grp.e[0].p0, &p1 = grp.e[0].p1;
     cudaError_t pe = prepare_kernel_once(bwd_stream_kernel<Q>, kSdHeadBytes + kSdRingBytes);
     if (pe != cudaSuccess) return pe;
     const int sms = current_device_sms();
@@ -398,8 +404,8 @@ static cudaError_t launch_bwd_stream_t(SignPrep p0, SignPrep p1, const StageDyAr
     const int pb = prep_blocks(p0, kSdThreads) + prep_blocks(p1, kSdThreads);
     const int grid = sb + pb <= sms ? sb + pb : sb;
     trace_before("bwd_prologue", s);
-    cudaError_t e = launch_k(bwd_stream_kernel<Q>, dim3(grid), dim3(kSdThreads), sd_smem_bytes(a.d_out), s, p0, p1,
-                             a, sb);
+    cudaError_t e = launch_k(bwd_stream_kernel<Q>, dim3(grid, grp.n), dim3(kSdThreads), sd_smem_bytes(a.d_out), s,
+                             grp, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;
@@ -412,30 +418,32 @@ static bool dy_stage_rows_forced() {
     return e && std::strcmp(e, "rows") == 0;
 }
 
-cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
+cudaError_t launch_bwd_prologue(const BwdGroup &grp, cudaStream_t s) {
+    if (grp.n < 1 || grp.n > kMaxGroupPaths) return cudaErrorInvalidValue;
+    const StageDyArgs &a = grp.e[0].sd;
     if (sd_supported(a.d_out) && !dy_stage_rows_forced()) {
         switch (sd_plan(a.d_out).Q) {
-            case 2: return launch_bwd_stream_t<2>(p0, p1, a, s);
-            case 4: return launch_bwd_stream_t<4>(p0, p1, a, s);
-            case 6: return launch_bwd_stream_t<6>(p0, p1, a, s);
-            default: return launch_bwd_stream_t<8>(p0, p1, a, s);
+            case 2: return launch_bwd_stream_t<2>(grp, s);
+            case 4: return launch_bwd_stream_t<4>(grp, s);
+            case 6: return launch_bwd_stream_t<6>(grp, s);
+            default: return launch_bwd_stream_t<8>(grp, s);
         }
     }
     switch (stage_gpt(a.d_out)) {
-        case 1: return launch_bwd_prologue_t<1>(p0, p1, a, s);
-        case 2: return launch_bwd_prologue_t<2>(p0, p1, a, s);
+        case 1: return launch_bwd_prologue_t<1>(grp, s);
+        case 2: return launch_bwd_prologue_t<2>(grp, s);
         case 3:
-        case 4: return launch_bwd_prologue_t<4>(p0, p1, a, s);
+        case 4: return launch_bwd_prologue_t<4>(grp, s);
         case 5:
         case 6:
         case 7:
-        case 8: return launch_bwd_prologue_t<8>(p0, p1, a, s);
+        case 8: return launch_bwd_prologue_t<8>(grp, s);
         default: break;
     }
     // rows wider than 16384: 1024-thread blocks, 8 groups per thread (measured
     // on GB300, 4000 rows of 32768: 271 -> 228 us against 512 threads with 16;
     // at 12288 the 512-thread blocks stay faster, 293 against 310 us)
-    if (stage_gpt(a.d_out, 1024) <= 8) return launch_bwd_prologue_t<8, 1024>(p0, p1, a, s);
+    if (stage_gpt(a.d_out, 1024) <= 8) return launch_bwd_prologue_t<8, 1024>(grp, s);
     return cudaErrorInvalidValue;
 }
 
@@ -454,13 +462,15 @@ cudaError_t launch_prep(SignPrep p0, SignPrep p1, uint32_t *status, unsigned int
     return e;
 }
 
-cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaStream_t s) {
+cudaError_t launch_reduce_partials(const ReduceGroup &grp, cudaStream_t s) {
+    if (grp.n < 1 || grp.n > kMaxGroupPaths) return cudaErrorInvalidValue;
+    const ReduceSeg &a = grp.a[0], &b = grp.b[0], &c = grp.c[0];
     const int blocks = (a.n + kReduceCols - 1) / kReduceCols + (b.n + kReduceCols - 1) / kReduceCols +
                        (c.n + kReduceCols - 1) / kReduceCols;
     cudaError_t pe = prepare_kernel_once(reduce_partials_kernel, 0);
     if (pe != cudaSuccess) return pe;
     trace_before("reduce_partials", s);
-    cudaError_t e = launch_k(reduce_partials_kernel, dim3(blocks), dim3(kReduceWarps * 32), 0, s, a, b, c);
+    cudaError_t e = launch_k(reduce_partials_kernel, dim3(blocks, grp.n), dim3(kReduceWarps * 32), 0, s, grp);
     trace_after(s);
     return e;
 }

@@ -29,6 +29,9 @@
 // of one of the k-step's two 64-wide blocks), warps 10-13 epilogue (warp w
 // reads lanes 32*(w%4) .. +31: each thread owns one feature of the tile and
 // walks its tokens, so the token sums dl and dg are per-thread running sums).
+// The dx'-product runs four expander warps (both blocks of a lane quarter
+// each) and eight epilogue warps (two per quarter, alternate chunks); the
+// kernels that stage x run four expander warps and six stager warps.
 // The epilogue stages each 32-token x 32-feature chunk in shared memory
 // ([token][feature], the layout of the row-major outputs) and writes it with
 // a TMA store; inputs (the a-tape, x, or y to accumulate) arrive by TMA into
@@ -74,8 +77,7 @@ constexpr int kWarpMma = 1;
 constexpr int kWarpExp0 = 2;
 constexpr int kNumExpWarps = 8;
 constexpr int kWarpEpi0 = 10;
-__host__ __device__ constexpr int gemm_threads(int epi) { return (kWarpEpi0 + epi_warps(epi)) * 32; }
-constexpr int kGemmThreads = (kWarpEpi0 + 8) * 32;  // the fused small-M kernels' block (every phase fits)
+constexpr int kGemmThreads = (kWarpEpi0 + 4) * 32;  // the fused small-M kernels' block (every phase fits)
 constexpr int kCtlBytes = 1024;   // shared-memory control block ahead of a phase's layout
 static_assert(kNumExpWarps == 4 * kKB, "one expander warp per (lane quarter, 64-wide block)");
 static_assert(kWarpExp0 % 4 == 2, "expander and epilogue warps cover the four TMEM lane quarters in turn");
@@ -92,16 +94,17 @@ static_assert(kWarpExp0 % 4 == 2, "expander and epilogue warps cover the four TM
 // leader (full_p) once the peer's loads have landed.
 // STG: 0, the activation operand is staged before the launch; 1, stager
 // warps after the epilogue warps stage x inside the a-product's kernel
-// (blr_stager.cuh), with a 48 KB ring of their own.
+// (blr_stager.cuh), with a 51 KB ring of their own.
 template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 struct GemmShape {
     static constexpr int kKBm = PLANE ? 1 : kKB;           // 64-wide blocks per k-step
     static constexpr int kStepKm = kKBm * kBK;             // K per k-step
     // expander warps: one per (TMEM lane quarter, 64-wide block) of a k-step,
-    // or, in the kernels that stage x, one per lane quarter covering both
-    // blocks (the six stager warps take the freed slots: 16 warps keep every
-    // role at 128 registers)
-    static constexpr int kNExp = PLANE ? 0 : (STG ? 4 : kNumExpWarps);
+    // or one per lane quarter covering both blocks where other roles need the
+    // warp slots: the stager warps of the kernels that stage x, the second
+    // epilogue warp of each quarter in the dx'-product (16 warps or fewer keep
+    // every role at 128 registers; more cap them at 96)
+    static constexpr int kNExp = PLANE ? 0 : ((STG || EPI == kEpiBwd2) ? 4 : kNumExpWarps);
     static constexpr int kEpi0 = PLANE ? 2 : kWarpExp0 + kNExp;  // first epilogue warp
     static constexpr bool kPlaneMN = EPI == kEpiFwd1 || EPI == kEpiBwd1;  // plane rows run along K
     static constexpr int kAccCols = BT;                    // TMEM columns of one accumulator
@@ -126,7 +129,7 @@ struct GemmShape {
     // before has read it). dx' streams x in and dx out at HBM rate
     // (plane mode leaves more room to the operand ring, which measured faster
     // than deeper chunk buffering: no input prefetch but for dx')
-    // (with in-kernel staging the stager ring takes 48 KB: the a-product keeps
+    // (with in-kernel staging the stager ring takes 51 KB: the a-product keeps
     // two chunk slots, measured as fast as four for the forward products)
     static constexpr int kNE = STG ? 2
                              : PLANE ? (EPI == kEpiBwd2 ? 3 : 2)
@@ -155,6 +158,13 @@ struct GemmShape {
     static_assert(kSlotBytes % 1024 == 0, "chunk slots stay 1024-byte aligned");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
+
+// Path p's copy of a workspace array of a multi-path launch: `stride` bytes
+// per path after path 0's.
+template <typename T>
+__device__ __forceinline__ T *path_at(T *base, int p, long long stride) {
+    return reinterpret_cast<T *>(reinterpret_cast<uintptr_t>(base) + (uintptr_t)((long long)p * stride));
+}
 
 // Shared-memory control block at the (1024-aligned) start of dynamic shared
 // memory; a GEMM phase's own layout starts kCtlBytes after it.
@@ -260,6 +270,22 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
     const int f_tiles = (N + kUnitF - 1) / kUnitF;
     const int t_tiles = (M + BT - 1) / BT;
     const int num_tiles = f_tiles * t_tiles;  // feature tile varies fastest: neighbours share activations
+    // Multi-path launches. The products that add into y or dx compute each
+    // tile for every path in turn on the same unit (local tile lt: tile
+    // unit + (lt / P) * num_units, path lt % P), so that the paths' chunks of
+    // an output tile are added in path order; the others spread the P x
+    // num_tiles (path, tile) pairs over the units, path-major. Path p's
+    // workspace arrays lie p * pstride bytes after path 0's, its TMA boxes at
+    // third coordinate p, its column factors at args.colv_p[p].
+    constexpr bool kPathMinor = EPI == kEpiFwd2 || EPI == kEpiBwd2;
+    const int P = args.paths > 1 ? args.paths : 1;
+    const int n_virt = num_tiles * P;
+    const int n_local = kPathMinor ? (unit < num_tiles ? (num_tiles - unit + num_units - 1) / num_units : 0) * P
+                                   : (unit < n_virt ? (n_virt - unit + num_units - 1) / num_units : 0);
+    auto tile_of = [&](int lt) {
+        return kPathMinor ? unit + (lt / P) * num_units : (unit + lt * num_units) % num_tiles;
+    };
+    auto path_of = [&](int lt) { return kPathMinor ? lt % P : (unit + lt * num_units) / num_tiles; };
     const int num_ks = (args.K + kStepK - 1) / kStepK;
     static_assert(SPLIT == 1 || (!PAIR && !PLANE), "split-K runs single TMEM-expansion CTAs");
     const int kj = SPLIT > 1 ? (int)cluster_ctarank() : 0;  // this CTA's share of K
@@ -272,9 +298,11 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             int sb = 0;
             uint32_t pb = 0, issued = 0, parity = 0;
             bool ok = true;
-            for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
+            for (int lt = 0; lt < n_local && ok; ++lt) {
+                const int tile = tile_of(lt), pz = path_of(lt);
                 const int t0 = (tile / f_tiles) * BT + (int)rank * S::kTokRows;  // this CTA's token rows
                 const int f0 = (tile % f_tiles) * kUnitF + (int)rank * kFM;      // this CTA's sign rows
+                const uint32_t *bsign = path_at(args.bsign, pz, args.pstride);
                 for (int ks = ks0; ks < ks1; ++ks) {
                     if constexpr (STG != 0) {
                         // the stagers publish a tile's rows per column chunk:
@@ -304,7 +332,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                         // (rows and K past the plane's extent read zero)
                         const int k0 = ks * kBK;
                         uint8_t *sa = reinterpret_cast<uint8_t *>(sBits) + sb * S::kBitsBytes;
-                        tma_load_2d(sB + sb * S::kBBytes, &tmap_act, &full_b[sb], k0, t0);
+                        tma_load_3d(sB + sb * S::kBBytes, &tmap_act, &full_b[sb], k0, t0, pz);
                         if constexpr (S::kPlaneMN) {
                             // plane [K][N]: two 64-feature blocks of 64 K rows
                             tma_load_2d(sa, tmap_sgn, &full_b[sb], f0, k0);
@@ -318,10 +346,10 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                         for (int kk = 0; kk < kKB; ++kk) {
                             // 64-wide K block; blocks past K read zero activations (and padded words)
                             const int blk = ks * kKB + kk;
-                            tma_load_2d(sB + sb * S::kBBytes + kk * S::kBBlock, &tmap_act, &full_b[sb], blk * kBK,
-                                        t0);
+                            tma_load_3d(sB + sb * S::kBBytes + kk * S::kBBlock, &tmap_act, &full_b[sb], blk * kBK,
+                                        t0, pz);
                             bulk_load(sBits + sb * (S::kBitsBytes / 4) + kk * (S::kBitsBlock / 4),
-                                      args.bsign + ((size_t)blk * args.Ns + f0) * 2, S::kBitsBlock, &full_b[sb]);
+                                      bsign + ((size_t)blk * args.Ns + f0) * 2, S::kBitsBlock, &full_b[sb]);
                         }
                     }
                     issued |= 1u << sb;
@@ -350,8 +378,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                 int sb = 0;
                 uint32_t pb = 0;
                 bool ok = true;
-                int local = 0;
-                for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++local) {
+                for (int local = 0; local < n_local && ok; ++local) {
                     const int acc = local & 1;
                     const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
                     if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, abort_flag)) {
@@ -406,7 +433,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                 int sb = 0;
                 uint32_t pb = 0;
                 bool ok = true;
-                for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
+                for (int lt = 0; lt < n_local && ok; ++lt) {
                     for (int ks = ks0; ks < ks1; ++ks) {
                         if (!mbar_wait(&full_b[sb], pb, abort_flag)) {
                             fail_status(args, abort_flag, kStTimeoutMma);
@@ -434,8 +461,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             int sa = 0, sb = 0;
             uint32_t pa = 0;
             bool ok = true;
-            int local = 0;
-            for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++local) {
+            for (int local = 0; local < n_local && ok; ++local) {
                 const int acc = local & 1;
                 const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
                 // (the peer's arrivals on tmem_empty and full_s are released at CTA
@@ -508,7 +534,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         int ls = 0;       // its activation slot
         uint32_t lp = 0;  // and that slot's phase parity
         bool ok = true;
-        for (int tile = unit; tile < num_tiles && ok; tile += num_units) {
+        for (int lt = 0; lt < n_local && ok; ++lt) {
             for (int ks = ks0; ks < ks1; ++ks) {
                 bool got = mbar_wait(&full_b[sb], pb, abort_flag);
                 uint32_t v[kBlocks][32];
@@ -577,14 +603,20 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         uint64_t *ebar = eload + ew * kNE;
         // inputs: the a-tape (db) or x (dx'); y and dx accumulate by reduce-add stores
         const bool has_in = (EPI == kEpiBwd1) || (EPI == kEpiBwd2);
-        const bool add_out = (EPI == kEpiFwd2 || EPI == kEpiBwd2) && args.accumulate;
+        // which chunk maps hold one plane per path: the a-tape in and out, and
+        // every f16 output; y, dx and x are the paths' common tensors
+        constexpr bool kIn32PerPath = EPI == kEpiBwd1, kOut32PerPath = EPI == kEpiFwd1;
+        // chunks per tile of the less busy warp of a lane quarter
+        constexpr int kMinNc = kChunks / kSplit;
+        static_assert(kMinNc >= 1, "every epilogue warp has a chunk per tile");
         uint32_t pending = 0u;  // lane 0: slots with an input load not yet waited on
         uint32_t ppar = 0u;     // and that load's phase parity
         // the warp's chunk g: local tile g / nc, chunk half + kSplit * (g % nc)
-        auto chunk_at = [&](int g, int &fq, int &tok) -> bool {
+        auto chunk_at = [&](int g, int &fq, int &tok, int &pz) -> bool {
             const int lt = g / nc;
-            const int tile = unit + lt * num_units;
-            if (tile >= num_tiles) return false;
+            if (lt >= n_local) return false;
+            const int tile = tile_of(lt);
+            pz = path_of(lt);
             fq = (tile % f_tiles) * kUnitF + (int)rank * kFM + q * 32;
             tok = (tile / f_tiles) * BT + 32 * (cb + kSplit * (g - lt * nc));
             return true;
@@ -594,12 +626,12 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
         // db.l) keep the default so that its CTAs find them in L2
         const uint64_t once = l2_policy_evict_first();
         auto load_chunk = [&](int g) {  // lane 0
-            int fq, tok;
-            if (!chunk_at(g, fq, tok)) return;
+            int fq, tok, pz;
+            if (!chunk_at(g, fq, tok, pz)) return;
             const int sl = g % kNE;
             const uint32_t par = (uint32_t)(g / kNE) & 1u;
             mbar_arrive_expect_tx(&ebar[sl], S::kSlot32);
-            tma_load_2d_hint(slots + sl * S::kSlotBytes, &tmap_in, &ebar[sl], fq, tok, once);
+            tma_load_3d_hint(slots + sl * S::kSlotBytes, &tmap_in, &ebar[sl], fq, tok, kIn32PerPath ? pz : 0, once);
             pending |= 1u << sl;
             ppar = (ppar & ~(1u << sl)) | (par << sl);
         };
@@ -656,10 +688,13 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             cluster_sync();  // no CTA reads a peer's staging any more
             if (!got) ok = false;
         }
-        for (int tile = unit; tile < num_tiles && ok; tile += num_units, ++local) {
+        for (; local < n_local && ok; ++local) {
+            const int tile = tile_of(local), pz = path_of(local);
             const int acc = local & 1;
             const uint32_t acc_phase = (uint32_t)(local >> 1) & 1u;
             const int tt = tile / f_tiles;
+            // y and dx: path 0 stores (or adds, in accumulate mode), later paths add
+            const bool add_out = (EPI == kEpiFwd2 || EPI == kEpiBwd2) && (args.accumulate || pz > 0);
             const int fq = (tile % f_tiles) * kUnitF + (int)rank * kFM + q * 32;  // this warp's 32 features
             const int f = fq + lane;
             const int t0 = tt * BT;
@@ -670,11 +705,11 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             for (int i = 0; i < kMaxNc; ++i) {
                 const int tl = t0 + 32 * (cb + kSplit * i) + lane;
                 const bool use = i < nc && tl < M;
-                ri_t[i] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && use ? __ldg(args.row_inv + tl) : 0.0f;
-                rs_t[i] = (EPI == kEpiBwd1) && use ? __ldg(args.row_scale + tl) : 0.0f;
+                ri_t[i] = (EPI == kEpiBwd1 || EPI == kEpiBwd2) && use ? __ldg(path_at(args.row_inv, pz, args.pstride) + tl) : 0.0f;
+                rs_t[i] = (EPI == kEpiBwd1) && use ? __ldg(path_at(args.row_scale, pz, args.pstride) + tl) : 0.0f;
             }
             const bool fvalid = f < N;
-            const float cf = fvalid ? __ldg(args.colv + f) : 0.0f;
+            const float cf = fvalid ? __ldg((P > 1 ? args.colv_p[pz] : args.colv) + f) : 0.0f;
             const bool got = mbar_wait(&tmem_full[acc], acc_phase, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, got)) {
                 if (lane == 0) fail_status(args, abort_flag, kStTimeoutEpi);
@@ -684,29 +719,22 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             tc_fence_after();
             float psum = 0.0f;
             const uint32_t acc_addr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * S::kAccCols);
-            // One warp per quarter: accumulator columns come in two register
-            // sets, the next chunk loaded from TMEM while the current one is
-            // processed. Two warps per quarter overlap each other instead (one
-            // register set keeps them within the 96 registers their 18 warps allow).
+            // Accumulator columns come in two register sets: the warp's next
+            // chunk is loaded from TMEM while the current one is processed.
             uint32_t va[32], vb[32];
-            if constexpr (kSplit == 1) tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * cb), va);
+            tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * cb), va);
 #pragma unroll
             for (int i = 0; i < kMaxNc; ++i) {
                 if (i >= nc) break;
                 const int c = cb + kSplit * i;  // chunk of the tile
-                uint32_t(&v)[32] = (kSplit == 1 && (i & 1)) ? vb : va;
-                uint32_t(&vn)[32] = (kSplit == 1 && (i & 1)) ? va : vb;
-                if constexpr (kSplit == 1) {
-                    tmem_wait_ld_regs(v);
-                    if (i + 1 < nc) tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * (c + kSplit)), vn);
-                } else {
-                    tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * c), v);
-                    tmem_wait_ld_regs(v);
-                }
+                uint32_t(&v)[32] = (i & 1) ? vb : va;
+                uint32_t(&vn)[32] = (i & 1) ? va : vb;
+                tmem_wait_ld_regs(v);
+                if (i + 1 < nc) tmem_ld_32x32b_x32(acc_addr + (uint32_t)(32 * (c + kSplit)), vn);
                 if (i + 1 == nc) {
                     // this warp's part of the accumulator is read: one arrival
                     // of the kEW (per CTA) that hand it back to the MMA issuer
-                    if constexpr (kSplit == 1) tmem_wait_ld_regs(vn);
+                    tmem_wait_ld_regs(vn);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -779,16 +807,23 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                 __syncwarp();
                 if (lane == 0 && tc < M && fq < N) {
                     if constexpr (S::kHas32) {
+                        const int z32 = kOut32PerPath ? pz : 0;
+                        if ((EPI == kEpiFwd2 || EPI == kEpiBwd2) && pz > 0) {
+                            // the previous path's store of this chunk was this warp's
+                            // (nc - 1)-th bulk group before this one: it must have
+                            // written y or dx before this path's add reads them
+                            bulk_wait_group<kMinNc - 1>();
+                        }
                         if (add_out)
-                            tma_reduce_add_2d_hint(&tmap_out32, s32, fq, tc, once);  // y or dx += the chunk
+                            tma_reduce_add_3d_hint(&tmap_out32, s32, fq, tc, z32, once);  // y or dx += the chunk
                         else
-                            tma_store_2d_hint(&tmap_out32, s32, fq, tc, once);
+                            tma_store_3d_hint(&tmap_out32, s32, fq, tc, z32, once);
                     }
                     if constexpr (S::kHas16) {
                         if (EPI == kEpiFwd2)
-                            tma_store_2d_hint(&tmap_out16, s16, fq, tc, once);  // c, read again by the backward only
+                            tma_store_3d_hint(&tmap_out16, s16, fq, tc, pz, once);  // c, read again by the backward only
                         else
-                            tma_store_2d(&tmap_out16, s16, fq, tc);  // a.l or db.l: the next product's operand
+                            tma_store_3d(&tmap_out16, s16, fq, tc, pz);  // a.l or db.l: the next product's operand
                     }
                 }
                 if (lane == 0) bulk_commit_group();
@@ -797,7 +832,9 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             if (!ok) break;
             if constexpr (EPI == kEpiBwd1 || EPI == kEpiBwd2) {
                 // one partial row per (token tile, warp of the quarter)
-                if (fvalid) args.part[((size_t)tt * (SPLIT > 1 ? SPLIT : kSplit) + (SPLIT > 1 ? kj : half)) * N + f] = psum;
+                if (fvalid)
+                    path_at(args.part, pz, args.pstride)[((size_t)tt * (SPLIT > 1 ? SPLIT : kSplit) + (SPLIT > 1 ? kj : half)) * N + f] =
+                        psum;
             }
         }
         // drain: stores complete, and input loads issued but not consumed have landed

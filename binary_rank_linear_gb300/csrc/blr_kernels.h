@@ -67,10 +67,32 @@ struct SignPrep {
     int Ns;    // destination row stride, sign_rows(N)
 };
 
+// Grouped launches of a multi-path layer run one stage of the pass for up to
+// kMaxGroupPaths paths of the same shape: the prologues and the reduction
+// with gridDim.y = paths (block row p takes entry p of its group), the GEMMs
+// with the path in their tile sequence (GemmArgs.paths).
+constexpr int kMaxGroupPaths = 8;
+
 // Forward prologue, one launch: clear the device status word, re-lay two
-// bitmaps and stage x16 = f16(x.g).
-cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16, int M,
-                                int d_in, uint32_t *status, cudaStream_t s);
+// bitmaps and stage x16 = f16(x.g), for each path of the group.
+struct FwdPathArgs {
+    SignPrep p0, p1;
+    const float *g;
+    uint16_t *x16;
+    uint32_t *status;
+};
+struct FwdGroup {
+    FwdPathArgs e[kMaxGroupPaths];
+    int n;
+};
+cudaError_t launch_fwd_prologue(const FwdGroup &grp, const float *x, int M, int d_in, cudaStream_t s);
+inline cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x, const float *g, uint16_t *x16,
+                                       int M, int d_in, uint32_t *status, cudaStream_t s) {
+    FwdGroup grp{};
+    grp.e[0] = FwdPathArgs{p0, p1, g, x16, status};
+    grp.n = 1;
+    return launch_fwd_prologue(grp, x, M, d_in, s);
+}
 
 // Prologue of a pass whose first product stages its own operand (GemmPlan
 // stg): re-lay two bitmaps, clear the device status word (when `status` is
@@ -98,7 +120,23 @@ struct StageDyArgs {
     uint32_t *status;      // device status word (bounded waits of the streaming staging)
 };
 int stage_dy_blocks(int M, int d_out);  // dh partial rows reserved in the workspace
-cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s);
+// per path of a group; M, d_out, r, gscale, dy and rows_used are taken from
+// entry 0 (the paths share them)
+struct BwdPathArgs {
+    SignPrep p0, p1;
+    StageDyArgs sd;
+};
+struct BwdGroup {
+    BwdPathArgs e[kMaxGroupPaths];
+    int n;
+};
+cudaError_t launch_bwd_prologue(const BwdGroup &grp, cudaStream_t s);
+inline cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
+    BwdGroup grp{};
+    grp.e[0] = BwdPathArgs{p0, p1, a};
+    grp.n = 1;
+    return launch_bwd_prologue(grp, s);
+}
 
 // out[f] += sum_p part[p][f] over three independent segments, fixed order.
 struct ReduceSeg {
@@ -107,17 +145,31 @@ struct ReduceSeg {
     int rows;
     int n;
 };
-cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaStream_t s);
+// per path of a group: its dh, dl and dg segments (same widths for every path)
+struct ReduceGroup {
+    ReduceSeg a[kMaxGroupPaths], b[kMaxGroupPaths], c[kMaxGroupPaths];
+    int n;
+};
+cudaError_t launch_reduce_partials(const ReduceGroup &grp, cudaStream_t s);
+inline cudaError_t launch_reduce_partials(ReduceSeg a, ReduceSeg b, ReduceSeg c, cudaStream_t s) {
+    ReduceGroup grp{};
+    grp.a[0] = a;
+    grp.b[0] = b;
+    grp.c[0] = c;
+    grp.n = 1;
+    return launch_reduce_partials(grp, s);
+}
 
 // ---- tcgen05 GEMMs --------------------------------------------------------
 enum GemmEpi : int { kEpiFwd1 = 0, kEpiFwd2 = 1, kEpiBwd1 = 2, kEpiBwd2 = 3 };
 
 // Epilogue warps of a product's GEMM: one per TMEM lane quarter, or two
 // (taking alternate chunks) for dx', whose epilogue (x in, dx out) outlasts its
-// short main loop. Measured on GB300, two warps per quarter also shortened the
-// c-product's epilogue only for K <= 512 and lengthened it otherwise (18 warps
-// cap every role at 96 registers). Each epilogue warp writes its own row of
-// token partial sums, so dx' has two partial rows per token tile.
+// short main loop. Measured on GB300, two warps per quarter did not shorten
+// the c-product (with eight expander warps, 18 warps at 96 registers, it
+// lengthened it for K > 512; with four, 14 warps at 128 registers, the
+// 12288-wide c-product took 316 against 308 us). Each epilogue warp writes its
+// own row of token partial sums, so dx' has two partial rows per token tile.
 __host__ __device__ constexpr int epi_warps(int epi) { return epi == kEpiBwd2 ? 8 : 4; }
 __host__ __device__ constexpr int epi_part_rows_per_tile(int epi) { return epi_warps(epi) / 4; }
 
@@ -162,6 +214,13 @@ struct GemmArgs {
     int accumulate;          // FWD2 y +=, BWD2 dx +=
     uint32_t *status;        // device status word
     StageArgs stg;           // in-kernel staging (STG kernels only)
+    // multi-path launches: `paths` paths (0 or 1: one); path p's bsign,
+    // row_inv, row_scale and part at p * pstride bytes after path 0's (its
+    // workspace slice), its colv at colv_p[p]; the activation, out16 and
+    // per-path f32 maps take the path as third coordinate
+    int paths;
+    long long pstride;
+    const float *colv_p[kMaxGroupPaths];
 };
 
 // Rows of the re-laid bitmap of a product with N features (a multiple of the
@@ -205,7 +264,7 @@ struct GemmPlan {
 // min_bt (64 or 32; the fused small-M kernels take 128) while the tiles would
 // fill at most half the SMs. tile_cost: a tile's fixed cost in token units
 // (CTA-pair tile choice).
-GemmPlan plan_gemm(int M, int N, int sms, int min_bt = 64, int tile_cost = 0);
+GemmPlan plan_gemm(int M, int N, int sms, int min_bt = 64, int tile_cost = 0, int paths = 1);
 // The c-product (K = r, output d_out wide) has a large fixed cost per tile:
 // fitted on GB300 to the attention-sized layer at 160- and 192-token pair
 // tiles, a round takes about 4.1 us + 0.0125 us per token of the tile, i.e.

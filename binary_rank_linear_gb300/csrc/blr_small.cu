@@ -18,6 +18,11 @@
 namespace blr {
 
 constexpr int kSmallBT = 128;
+static_assert(GemmShape<kEpiFwd1, false, kSmallBT>::kThreads <= kGemmThreads &&
+                  GemmShape<kEpiFwd2, false, kSmallBT>::kThreads <= kGemmThreads &&
+                  GemmShape<kEpiBwd1, false, kSmallBT>::kThreads <= kGemmThreads &&
+                  GemmShape<kEpiBwd2, false, kSmallBT>::kThreads <= kGemmThreads,
+              "every phase's warp roles fit the fused kernels' block");
 
 // Grid barrier: one arrival per CTA on a counter in global memory that only
 // grows during a launch (zeroed before it); barrier k completes at k * grid

@@ -4,19 +4,21 @@
 // a-product) is an HBM stream that leaves the tensor cores idle, while the
 // a-product it feeds (K = d_in, r outputs) leaves most of the HBM bandwidth
 // idle. Here the staging runs inside the a-product's persistent kernel, on
-// two stager warps of every CTA, ahead of the MMA pipeline:
+// six stager warps of every CTA, ahead of the MMA pipeline:
 //
 //  - Work items are blocks of 64 token rows x 256 columns of x, taken in the
 //    order the persistent grid consumes them: round by round (a round is the
 //    token tiles whose feature tiles the units start together), then column
 //    chunk by column chunk, then token tile and row group. CTA c stages
 //    items c, c + grid, c + 2 grid, ...
-//  - One stager lane loads the items' f32 tiles into a 48 KB shared-memory
-//    ring by TMA (one 256 x 16 box per unit, full/empty mbarriers) several
-//    units ahead; another asks L2 to prefetch whole items (one 256 x 64 box)
-//    two items ahead and publishes finished items; four converter warps
-//    convert from shared memory and write f16 with 16-byte stores, so the
-//    staged tiles sit in L2 when the product's TMA loads come. (Measured on
+//  - One stager lane (the copy producer) loads the items' f32 tiles into a
+//    51 KB shared-memory ring by TMA (three slots of one 256 x 16 box, a
+//    16-row unit, plus the item's 256 g factors and the unit's geometry;
+//    full/empty mbarriers); another (the publisher) asks L2 to prefetch whole
+//    items (one 256 x 64 box) two items ahead and publishes finished items;
+//    four converter warps convert from shared memory and write f16 with
+//    16-byte stores, so the staged tiles sit in L2 when the product's TMA
+//    loads come. (Measured on
 //    GB300 with in-kernel clock counters: converters that also issued the
 //    TMA copies and the releases spent most of their time there; each TMA
 //    instruction costs its thread several hundred cycles in this kernel.)

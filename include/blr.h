@@ -163,11 +163,20 @@ BLR_API int blr_backward(const float *x, const float *dy,
  * gives path p's sign gradients after blr_backward_paths.
  *
  * blr_forward_paths / blr_backward_paths take host arrays of P device
- * pointers (bits_u[p], ..., dg[p]) and run each path's kernels in turn on
- * `stream` (path p > 0 accumulates into y and dx; accumulate_y/accumulate_dx
- * = 1 makes path 0 accumulate too). Every argument is checked before the
- * first launch, so an argument error changes nothing; a launch failure part
- * way leaves the earlier paths' results in place. P in [1, 64]; the rest as
+ * pointers (bits_u[p], ..., dg[p]) and queue the pass on `stream` with one
+ * launch per stage for up to 8 paths at a time: one prologue (each path's
+ * bitmap re-layouts and staging), one launch of each product covering every
+ * path's tiles, one reduction of every path's partial sums. Path 0 overwrites
+ * y and dx and each later path adds its contribution, in path order, tile by
+ * tile (accumulate_y/accumulate_dx = 1 makes path 0 add too); the sums are
+ * the same as from P single-path calls. More than 8 paths run as groups of 8
+ * in turn. With BLR_PATHS=loop in the environment, or an option that has no
+ * grouped form (BLR_SMALL_PATH=fused, BLR_SIGN_SRC=plane, BLR_WIDE=token,
+ * BLR_SPLITK=1), each path's single-path calls run in turn instead. A
+ * grouped launch records device-side failures in path 0's status word (the
+ * first slice's header). Every argument is checked before the first launch,
+ * so an argument error changes nothing; a launch failure part way leaves
+ * the earlier groups' results in place. P in [1, 64]; the rest as
  * blr_forward / blr_backward. */
 BLR_API size_t blr_paths_workspace_bytes(int P, int M, int d_in, int d_out, int r);
 BLR_API int blr_forward_paths(const float *x, int P,

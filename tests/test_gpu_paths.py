@@ -64,9 +64,7 @@ def test_pages_two_paths():
     _check(p0["x"], p0["dy"], [p0, p1], got)
 
 
-@pytest.mark.parametrize("P,M,d_in,d_out,r", [(3, 300, 320, 448, 96), (2, 4600, 1024, 1568, 256),
-                                              (4, 129, 192, 96, 64)])
-def test_paths_parity(P, M, d_in, d_out, r):
+def _paths_inputs(P, M, d_in, d_out, r):
     """P paths with their own signs and vectors on one x and dy."""
     base = wl.make_inputs(wl.WORKLOADS["small"].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     rng = np.random.default_rng(M + P)
@@ -79,8 +77,65 @@ def test_paths_parity(P, M, d_in, d_out, r):
         q["h"] = (1 + 0.1 * rng.standard_normal(d_out)).astype(np.float32)
         q["l"] = (base["l"] * rng.uniform(0.5, 1.5, r)).astype(np.float32)
         paths.append(q)
-    x, dy = base["x"], base["dy"]
+    return base["x"], base["dy"], paths
+
+
+@pytest.mark.parametrize("P,M,d_in,d_out,r", [(3, 300, 320, 448, 96), (2, 4600, 1024, 1568, 256),
+                                              (4, 129, 192, 96, 64)])
+def test_paths_parity(P, M, d_in, d_out, r):
+    """P paths with their own signs and vectors on one x and dy."""
+    x, dy, paths = _paths_inputs(P, M, d_in, d_out, r)
     _check(x, dy, paths, _run_paths(x, dy, paths))
+
+
+@pytest.mark.parametrize("P,M,d_in,d_out,r", [(2, 300, 320, 448, 96), (3, 4600, 1024, 1568, 256),
+                                              (10, 129, 192, 96, 64), (2, 8192, 512, 4096, 128)])
+def test_grouped_paths_match_the_loop(monkeypatch, P, M, d_in, d_out, r):
+    """The grouped passes (one launch per stage for up to eight paths; ten
+    paths take two groups, the second adding into y and dx) against each
+    path's single-path calls in turn (BLR_PATHS=loop): y and dx receive the
+    same contributions in the same order, and each path's dh, dl, dg the same
+    partial sums up to their grouping; both against the oracle."""
+    x, dy, paths = _paths_inputs(P, M, d_in, d_out, r)
+    got_g = _run_paths(x, dy, paths)
+    monkeypatch.setenv("BLR_PATHS", "loop")
+    got_l = _run_paths(x, dy, paths)
+    assert oracle.rel_err(got_g[0], got_l[0]) <= 1e-6
+    assert oracle.rel_err(got_g[1], got_l[1]) <= 1e-6
+    for qg, ql in zip(got_g[2], got_l[2]):
+        for k in ("dg", "dl", "dh"):
+            assert oracle.rel_err(qg[k], ql[k]) <= 1e-5, k
+    _check(x, dy, paths, got_g)
+
+
+def test_grouped_paths_integer_grid():
+    """Bit-exact on a grid of small multiples of powers of two (every staged
+    operand exact in f16, every product and partial sum exact in f32): three
+    paths whose y and dx contributions are added by reduce-add stores in path
+    order; a contribution lost to a store that overtook an add, or added
+    twice, would show."""
+    import binary_rank_linear_gb300 as blr
+    M, d_in, d_out, r, P = 2000, 256, 1024, 128, 3
+    rng = np.random.default_rng(11)
+    x = rng.integers(-2, 3, (M, d_in)).astype(np.float32)
+    dy = rng.integers(-2, 3, (M, d_out)).astype(np.float32)
+    paths = []
+    for _ in range(P):
+        paths.append({"su": np.where(rng.random((d_out, r)) < 0.5, 1.0, -1.0).astype(np.float32),
+                      "sv": np.where(rng.random((d_in, r)) < 0.5, 1.0, -1.0).astype(np.float32),
+                      "g": rng.choice([0.5, 1.0, 2.0], d_in).astype(np.float32),
+                      "l": rng.choice([0.25, 0.5], r).astype(np.float32),
+                      "h": rng.choice([0.5, 1.0], d_out).astype(np.float32)})
+    y, dx, grads, _ = _run_paths(x, dy, paths, gscale=1.0)
+    fw, bw = _oracle_paths(x, dy, paths)
+    assert np.array_equal(y, fw["y"].astype(np.float32))
+    assert np.array_equal(dx, bw["dx"].astype(np.float32))
+    for q, want in zip(grads, bw["paths"]):
+        for k in ("dg", "dl"):
+            assert np.array_equal(q[k], want[k].astype(np.float32)), k
+        # dh reads the f16 c tape, whose larger values are rounded
+        assert oracle.rel_err(q["dh"], want["dh"]) <= 1e-3
+    del blr
 
 
 def test_paths_accumulate_and_sign_grads():
