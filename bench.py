@@ -580,7 +580,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.empty_cache()
     if world == 1 and args.extra:
         result["configs"] = {}
-        for name in [n for n in args.extra.split(",") if n and n != args.workload]:
+        for name in [n for n in args.extra.split(",") if n and n not in (args.workload, "none")]:
             result["configs"][name] = measure_config(name, args, dev, tc_peak, hbm_peak)
     return result
 
@@ -826,7 +826,7 @@ def main():
     ap.add_argument("--workload", default="mlp",
                     help="mlp (the SwiGLU up+down pair, default), tiny, small, attn, mlp_up, mlp_down, ragged")
     ap.add_argument("--extra", default="tiny,small,attn,ragged",
-                    help="workloads measured after the main one (N=1 only), reported under 'configs'; '' for none")
+                    help="workloads measured after the main one (N=1 only), reported under 'configs'; '' or none for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sign", action="store_true", help="skip the sign-gradient measurement")
     ap.add_argument("--no-plane", action="store_true", help="skip the plane_linear measurement")
