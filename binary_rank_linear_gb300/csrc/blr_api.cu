@@ -453,6 +453,20 @@ bool fused_small_enabled() {
 // layer (8 MB of x) the pass keeps its bitmap re-layouts hidden behind the
 // staging and the step is 50.6 against 54.0 us. BLR_STAGE=kernel or
 // BLR_STAGE=pass forces a form.
+// Where the backward's partial sums of dh, dl and dg are reduced: by a launch
+// of its own after the dx'-product (default), or in the dx'-product's tail
+// with BLR_REDUCE=fold (its CTAs meet at a grid barrier and share out the
+// columns; not for the token-major dx'-product). Measured on GB300 (CUDA-graph
+// steps), the folded form is slower everywhere: tiny 33.7 against 30.4 us,
+// small 54.8 against 52.6, attention-sized 349.6 against 344.8, the MLP pair
+// 2241 against 2197 (the 12288 -> 4096 dx'-product grows from 343 to 371 us
+// where the stand-alone reduction takes 11): the reduction starts only when
+// the slowest CTA arrives and runs on the product's 14 warps per CTA.
+bool reduce_folded() {
+    const char *v = std::getenv("BLR_REDUCE");
+    return v && std::strcmp(v, "fold") == 0;
+}
+
 bool stage_in_kernel(long long x_bytes) {
     const char *v = std::getenv("BLR_STAGE");
     if (v && std::strcmp(v, "pass") == 0) return false;
@@ -460,12 +474,13 @@ bool stage_in_kernel(long long x_bytes) {
     return x_bytes >= (64ll << 20);
 }
 
-// Grid barriers of the fused small-M kernels. Their waits give up after 2 s
-// (BLR_WAIT_LIMIT_NS=<ns> sets another limit, from 1 us to 10 s). For the
-// test of that path, BLR_FAULT=grid_barrier makes every barrier expect one
-// arrival more than the grid makes, so each wait runs out: the kernels then
-// record kStTimeoutGrid in the status word, leave their remaining phases
-// early and return (their results are then meaningless).
+// Grid barriers of the fused small-M kernels and of the dx'-product's folded
+// reduction. Their waits give up after 2 s (BLR_WAIT_LIMIT_NS=<ns> sets
+// another limit, from 1 us to 10 s). For the test of that path,
+// BLR_FAULT=grid_barrier makes every barrier expect one arrival more than the
+// grid makes, so each wait runs out: the kernels then record kStTimeoutGrid
+// in the status word, leave their remaining work early and return (their
+// results are then meaningless).
 GridBarrier grid_barrier(unsigned int *gbar) {
     GridBarrier b{gbar, 0u, 2000000000ull};
     if (const char *v = std::getenv("BLR_WAIT_LIMIT_NS")) {
@@ -476,8 +491,6 @@ GridBarrier grid_barrier(unsigned int *gbar) {
     return b;
 }
 
-// The per-path pointers of a multi-path call: every array present, every entry
-// non-null and 16-byte aligned.
 // Multi-path passes run grouped: one launch per stage of the pass for up to
 // kMaxGroupPaths paths (the prologues and the reduction with a block row per
 // path, the GEMMs with the paths in their tile sequence; y and dx receive the
@@ -604,6 +617,7 @@ int backward_grouped(const float *x, const float *dy, int n, const uint32_t *con
         sa.r = r;
         sa.rows_used = p == 0 ? &rows_dh : nullptr;
         sa.status = reinterpret_cast<uint32_t *>(w + L.header);
+        sa.red_cnt = nullptr;
         b1.colv_p[p] = l[p];
         b2.colv_p[p] = g[p];
     }
@@ -634,9 +648,32 @@ int backward_grouped(const float *x, const float *dy, int n, const uint32_t *con
     b2.status = status;
     b2.paths = n;
     b2.pstride = ps;
+    const bool fold = reduce_folded();
+    if (fold) grp.e[0].sd.red_cnt = reinterpret_cast<unsigned int *>(ws0 + L.header + kRedCntOffset);
     if (launch_bwd_prologue(grp, s) != cudaSuccess) return BLR_ERR_CUDA;
     if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (fold) {
+        // every path's dh, dl and dg reduced in the dx'-product's tail
+        b2.fold = 1;
+        b2.red = grid_barrier(grp.e[0].sd.red_cnt);
+        b2.red_part_h = reinterpret_cast<const float *>(ws0 + L.part_dh);
+        b2.red_part_l = reinterpret_cast<const float *>(ws0 + L.part_dl);
+        b2.red_rows_h = rows_dh;
+        b2.red_rows_l = p1.part_rows * epi_part_rows_per_tile(kEpiBwd1);
+        b2.red_rows_g = p2.part_rows * epi_part_rows_per_tile(kEpiBwd2);
+        b2.red_n_h = d_out;
+        b2.red_n_l = r;
+        for (int p = 0; p < n; ++p) {
+            b2.red_out_h[p] = dh[p];
+            b2.red_out_l[p] = dl[p];
+            b2.red_out_g[p] = dg[p];
+        }
+    }
     if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (fold) {
+        for (int p = 0; p < n; ++p) mark_backward_done(ws0 + (size_t)p * one, gscale, rows_dh);
+        return BLR_OK;
+    }
     ReduceGroup rg{};
     rg.n = n;
     for (int p = 0; p < n; ++p) {
@@ -652,6 +689,8 @@ int backward_grouped(const float *x, const float *dy, int n, const uint32_t *con
     return BLR_OK;
 }
 
+// The per-path pointers of a multi-path call: every array present, every entry
+// non-null and 16-byte aligned.
 template <typename T>
 bool path_ptrs_ok(T *const *a, int P, int *status) {
     if (!a) {
@@ -1001,15 +1040,34 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
         mark_backward_done(ws, gscale, rows_dh);
         return BLR_OK;
     }
+    const bool fold = !dense2 && reduce_folded();
+    if (fold) sa.red_cnt = reinterpret_cast<unsigned int *>(w + L.header + kRedCntOffset);
     if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
     if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (fold) {
+        // dh, dl and dg reduced in the dx'-product's tail (rows_dh is known now)
+        b2.fold = 1;
+        b2.red = grid_barrier(sa.red_cnt);
+        b2.red_part_h = part_dh;
+        b2.red_part_l = part_dl;
+        b2.red_rows_h = rows_dh;
+        b2.red_rows_l = sl.rows;
+        b2.red_rows_g = sg.rows;
+        b2.red_n_h = d_out;
+        b2.red_n_l = r;
+        b2.red_out_h[0] = dh;
+        b2.red_out_l[0] = dl;
+        b2.red_out_g[0] = dg;
+    }
     if (dense2) {
         if (launch_dense_gemm(d2, "gemm_bwd2", s) != cudaSuccess) return BLR_ERR_CUDA;
     } else if (launch_gemm(kEpiBwd2, p2, m2, b2, s) != cudaSuccess) {
         return BLR_ERR_CUDA;
     }
-    ReduceSeg sh{part_dh, dh, rows_dh, d_out};
-    if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
+    if (!fold) {
+        ReduceSeg sh{part_dh, dh, rows_dh, d_out};
+        if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
+    }
     mark_backward_done(ws, gscale, rows_dh);
     return BLR_OK;
 }

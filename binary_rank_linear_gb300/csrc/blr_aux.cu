@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
     const BwdPathArgs &e = grp.e[blockIdx.y];
     pdl_wait();
     pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && e.sd.red_cnt) *e.sd.red_cnt = 0u;
     if (prologue_prep(e.p0, e.p1, stage_blocks)) return;
     stage_dy_run<GPT>(e.sd, blockIdx.x, stage_blocks, smem_f, stage_tpr(e.sd.d_out, THREADS), THREADS);
 }
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kSdThreads, 1)
     const BwdPathArgs &e = grp.e[blockIdx.y];
     pdl_wait();
     pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && e.sd.red_cnt) *e.sd.red_cnt = 0u;
     const int extra = (int)gridDim.x - stage_blocks;
     if (extra > 0 && (int)blockIdx.x >= stage_blocks) {
         prep_share(e.p0, e.p1, (int)blockIdx.x - stage_blocks, extra);

@@ -19,7 +19,7 @@ enum : uint32_t {
     kStTimeoutEpi = 1u << 3,     // epilogue: accumulator never ready
     kStTimeoutDrain = 1u << 4,   // teardown: in-flight copies or MMAs never drained
     kStBadLaunch = 1u << 5,      // launch geometry inconsistent with the kernel
-    kStTimeoutGrid = 1u << 6,    // fused small-M kernel: a grid barrier never completed
+    kStTimeoutGrid = 1u << 6,    // a grid barrier never completed (fused small-M kernels, dx'-product's reduction)
     kStTimeoutStage = 1u << 7,   // streaming dy staging: a row batch never arrived or its slot never freed
 };
 

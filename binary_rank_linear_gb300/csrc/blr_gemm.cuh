@@ -173,6 +173,7 @@ struct GemmCtl {
     int abort_flag;      // set by any role whose bounded wait ran out
     unsigned int stg_done;  // items finished by the converter warps, one count per warp (STG kernels)
     StgGeo stg_geo[kStgSlotsMax];  // geometry of the units in the stager ring (STG kernels)
+    int red_go;          // the folded reduction's grid barrier completed (dx'-product)
 };
 static_assert(sizeof(GemmCtl) <= kCtlBytes, "control block");
 
@@ -893,6 +894,47 @@ __device__ __forceinline__ void gemm_prefetch_maps(const CUtensorMap &tmap_act, 
     }
 }
 
+// Tail of a dx'-product launch with the pass's partial-sum reduction folded
+// in (GemmArgs.fold): a grid barrier on args.red.gbar (bounded: the persistent
+// grid, at most one CTA per SM, is resident together), then each CTA adds a
+// share of the columns of every path's dh, dl and dg, each column's rows in
+// a fixed order. Called by every thread after the roles and the TMEM release;
+// the phase's shared memory is free again by then.
+__device__ __forceinline__ void gemm_fold_reduce(const GemmArgs &args, uint8_t *smem) {
+    // (the decision goes through the control block: static shared memory
+    // would push the largest phases past the per-CTA limit)
+    volatile int *go = &reinterpret_cast<GemmCtl *>(smem)->red_go;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();  // this CTA's dg partial rows (written by its epilogue warps) before the arrival
+        atomicAdd(args.red.gbar, 1u);
+        const uint64_t t0 = globaltimer_ns();
+        const unsigned int target = gridDim.x + args.red.extra;
+        bool ok = true;
+        while (ld_acquire_u32(args.red.gbar) < target) {
+            if (globaltimer_ns() - t0 > args.red.wait_ns) {
+                ok = false;
+                break;
+            }
+            __nanosleep(128);
+        }
+        if (!ok) atomicOr(args.status, kStTimeoutGrid);
+        __threadfence();
+        *go = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*go) return;
+    float *red = reinterpret_cast<float *>(smem + kCtlBytes);
+    const int P = args.paths > 1 ? args.paths : 1;
+    for (int p = 0; p < P; ++p) {
+        const ReduceSeg h{path_at(args.red_part_h, p, args.pstride), args.red_out_h[p], args.red_rows_h, args.red_n_h};
+        const ReduceSeg l{path_at(args.red_part_l, p, args.pstride), args.red_out_l[p], args.red_rows_l, args.red_n_l};
+        const ReduceSeg g{path_at(const_cast<const float *>(args.part), p, args.pstride), args.red_out_g[p],
+                          args.red_rows_g, args.N};
+        reduce_partials_run(h, l, g, (int)blockIdx.x, (int)gridDim.x, red);
+    }
+}
+
 __device__ __forceinline__ uint8_t *smem_base_1024() {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -950,6 +992,9 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads
         __syncthreads();
         tc_fence_after();
         if (warp == kWarpMma) tmem_dealloc(tmem_base, kTmemCols);
+    }
+    if constexpr (EPI == kEpiBwd2 && SPLIT == 1) {
+        if (args.fold) gemm_fold_reduce(args, smem);
     }
 }
 

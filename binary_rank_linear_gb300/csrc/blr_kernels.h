@@ -118,6 +118,7 @@ struct StageDyArgs {
     int M, d_out, r;
     int *rows_used;        // host out: dh partial rows the launch wrote
     uint32_t *status;      // device status word (bounded waits of the streaming staging)
+    unsigned int *red_cnt; // zeroed by the launch (the dx'-product's reduction counter), or null
 };
 int stage_dy_blocks(int M, int d_out);  // dh partial rows reserved in the workspace
 // per path of a group; M, d_out, r, gscale, dy and rows_used are taken from
@@ -192,6 +193,16 @@ inline bool stage_fits(int M, int bt, int K, int f_tiles) {
     return t * ((long long)f_tiles + 3ll * ((K + kStageChunkCols - 1) / kStageChunkCols)) < (1ll << 31);
 }
 
+// A grid barrier on a counter in global memory: barrier k waits for
+// k * grid + extra arrivals, for at most wait_ns of wall time (extra is 0
+// except in the test that makes the waits run out; see blr_api.cu). Used by
+// the fused small-M kernels and by the dx'-product's folded reduction.
+struct GridBarrier {
+    unsigned int *gbar;
+    unsigned int extra;
+    unsigned long long wait_ns;
+};
+
 struct StageArgs {
     const float *src;      // x [M][K] f32
     const float *col;      // g [K]
@@ -221,6 +232,20 @@ struct GemmArgs {
     int paths;
     long long pstride;
     const float *colv_p[kMaxGroupPaths];
+    // dx'-product only (fold = 1): the pass's partial-sum reduction runs in
+    // the kernel's tail. Every CTA adds its arrival to red.gbar (zeroed by the
+    // backward prologue) once its dg partial rows are written; when the whole
+    // grid has arrived (grid + red.extra arrivals, waited for at most
+    // red.wait_ns: the persistent grid is resident together), the CTAs share
+    // out the columns of every path's dh, dl and dg: out += the fixed-order
+    // sum of the partial rows, red_part_h / red_part_l / part (path p at
+    // p * pstride) with red_rows_h / red_rows_l / red_rows_g rows of d_out /
+    // r / N columns.
+    int fold;
+    GridBarrier red;
+    const float *red_part_h, *red_part_l;
+    int red_rows_h, red_rows_l, red_rows_g, red_n_h, red_n_l;
+    float *red_out_h[kMaxGroupPaths], *red_out_l[kMaxGroupPaths], *red_out_g[kMaxGroupPaths];
 };
 
 // Rows of the re-laid bitmap of a product with N features (a multiple of the
@@ -280,15 +305,6 @@ cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, con
 // One cooperative launch (grid = one CTA per SM) per pass; the GEMM phases use
 // single-CTA 128-token tiles (plans with pair = false, bt = 128). `gb.gbar`
 // is a grid-barrier counter in the workspace header, zeroed by the launcher.
-//
-// Grid barrier k waits for k * grid + gb.extra arrivals, for at most
-// gb.wait_ns of wall time (extra is 0 except in the test that makes the waits
-// run out; see blr_api.cu).
-struct GridBarrier {
-    unsigned int *gbar;
-    unsigned int extra;
-    unsigned long long wait_ns;
-};
 
 struct SmallFwdArgs {
     SignPrep pv, pu;    // re-layouts of S_V (a-product) and S_U (c-product)

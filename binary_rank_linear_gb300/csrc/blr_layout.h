@@ -34,8 +34,10 @@ struct Layout {
 };
 
 // Header words (u32 index): 0 the device status word; 16 the grid-barrier
-// counter of the fused small-M kernels.
+// counter of the fused small-M kernels; 32 the arrival counter of the
+// dx'-product's folded reduction (byte offsets below).
 constexpr size_t kGridBarOffset = 64;
+constexpr size_t kRedCntOffset = 128;
 
 
 inline Layout make_layout(int M, int d_in, int d_out, int r) {

@@ -295,7 +295,8 @@ BLR_API int blr_adam(float *w, const float *grad, float *m1, float *m2, const fl
  *   0x02 a sign expander, 0x04 an MMA issuer, 0x08 an epilogue,
  *   0x10 the drain of copies or MMAs at a kernel's end,
  *   0x20 a launch geometry the kernel does not accept,
- *   0x40 a grid barrier of the fused small-problem kernels,
+ *   0x40 a grid barrier (of the fused small-problem kernels, or before the
+ *        dx'-product's reduction of the partial sums),
  *   0x80 a streaming staging kernel (a row batch never arrived or its ring
  *        slot never freed). */
 BLR_API int blr_check_status(const void *ws, size_t ws_bytes, blr_stream_t stream, uint32_t *device_code);

@@ -203,6 +203,26 @@ def test_outputs_stay_in_bounds():
     assert torch.isfinite(ybuf[:M]).all() and torch.isfinite(dxbuf[:M]).all()
 
 
+@pytest.mark.parametrize("M,d_in,d_out,r", [(300, 256, 256, 128), (4600, 1024, 1568, 256)])
+def test_reduction_folded_and_separate(monkeypatch, M, d_in, d_out, r):
+    """dh, dl and dg reduced in the dx'-product's tail (BLR_REDUCE=fold) and
+    by a launch of their own (the default): the same partial rows summed in
+    two fixed orders, equal to rounding and both within the tolerance of the
+    oracle; y and dx do not depend on it."""
+    t = wl.make_inputs(wl.WORKLOADS["small"].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    b = _run(t)
+    monkeypatch.setenv("BLR_REDUCE", "fold")
+    a = _run(t)
+    assert a["status"] == 0 and b["status"] == 0
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["dx"], b["dx"])
+    for k in ("dh", "dl", "dg"):
+        assert oracle.rel_err(a[k], b[k]) <= 1e-5, k
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    for k in ("dh", "dl", "dg"):
+        assert oracle.rel_err(a[k], bw[k]) <= TOL_GRAD, k
+
+
 def test_deterministic():
     w = wl.WORKLOADS["small"].with_shape(M=300, d_in=256, d_out=256, r=128)
     t = wl.make_inputs(w)

@@ -1,7 +1,9 @@
 """A bounded wait that runs out on the GPU ends in a status code, not a hang.
 
-The fused small-problem kernels separate their phases with grid barriers on a
-counter in the workspace. With BLR_FAULT=grid_barrier every barrier expects
+Two grid barriers are made to run out: the fused small-problem kernels'
+(between their phases) and the general path's dx'-product's (before it
+reduces the partial sums). The fused small-problem kernels separate their
+phases with grid barriers on a counter in the workspace. With BLR_FAULT=grid_barrier every barrier expects
 one arrival more than the grid makes, so no barrier ever completes; with
 BLR_WAIT_LIMIT_NS=1000000 each wait gives up after 1 ms. The kernels must then
 record kStTimeoutGrid (0x40) in the workspace status word, leave their
@@ -54,3 +56,31 @@ def test_grid_barrier_wait_runs_out_cleanly(monkeypatch):
         assert oracle.rel_err(good[k], bw[k]) <= 5e-3
     assert np.isfinite(good["y"]).all()
     del blr
+
+
+def test_folded_reduction_barrier_runs_out_cleanly(monkeypatch):
+    """With BLR_REDUCE=fold the general path's dx'-product meets at a grid
+    barrier before it reduces the partial sums of dh, dl and dg. With
+    BLR_FAULT=grid_barrier
+    that barrier expects one arrival more than the grid makes; under a 1 ms
+    limit every CTA gives up, records kStTimeoutGrid and returns without
+    reducing. The stream then synchronises cleanly and a normal pass runs to
+    parity in the same process."""
+    from blr_gpu_run import run_layer
+    t = wl.make_inputs(wl.WORKLOADS["small"].with_shape(M=512))
+    torch.cuda.synchronize()
+    monkeypatch.setenv("BLR_REDUCE", "fold")
+    monkeypatch.setenv("BLR_FAULT", "grid_barrier")
+    monkeypatch.setenv("BLR_WAIT_LIMIT_NS", "1000000")
+    out = run_layer(t, gscale=0.0)
+    assert out["status"] & K_ST_TIMEOUT_GRID, f"status {out['status']:#x}"
+    torch.cuda.synchronize()
+    monkeypatch.delenv("BLR_FAULT")
+    monkeypatch.delenv("BLR_WAIT_LIMIT_NS")
+    good = run_layer(t, gscale=0.0)
+    assert good["status"] == 0
+    bu, bv = oracle.pack_signs(t["su"]), oracle.pack_signs(t["sv"])
+    bw = oracle.backward(t["x"], t["dy"], bu, bv, t["g"], t["l"], t["h"])
+    assert oracle.rel_err(good["dx"], bw["dx"]) <= 2e-3
+    for k in ("dh", "dl", "dg"):
+        assert oracle.rel_err(good[k], bw[k]) <= 5e-3
