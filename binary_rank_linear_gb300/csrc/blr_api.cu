@@ -507,7 +507,8 @@ bool paths_grouped() {
 
 // Forward of paths [0, n) of a multi-path layer (n <= kMaxGroupPaths), path
 // p on the workspace slice at ws0 + p * one: one prologue (x staged n times,
-// with each path's g), one a-product, one c-product.
+// with each path's g; for x of 64 MB or more only the re-layouts, the a-product
+// staging every path's x itself), one a-product, one c-product.
 int forward_grouped(const float *x, int n, const uint32_t *const *bits_u, const uint32_t *const *bits_v,
                     const float *const *g, const float *const *l, const float *const *h, float *y, int accumulate_y,
                     int M, int d_in, int d_out, int r, char *ws0, size_t one, int sms, cudaStream_t s) {
@@ -563,8 +564,29 @@ int forward_grouped(const float *x, int n, const uint32_t *const *bits_u, const 
         std::lock_guard<std::mutex> lk(g_tape_mu);
         for (int p = 0; p < n; ++p) g_tapes.erase(ws0 + (size_t)p * one);
     }
-    if (launch_fwd_prologue(grp, x, M, d_in, s) != cudaSuccess) return BLR_ERR_CUDA;
-    if (launch_gemm(kEpiFwd1, p1, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    const bool stg = p1.split <= 1 && stage_in_kernel((long long)M * d_in * 4) &&
+                     stage_fits(M, p1.bt, d_in, (r + (p1.pair ? 255 : 127)) / (p1.pair ? 256 : 128), n);
+    if (stg) {
+        // every path's x16 staged inside the a-product, path-major like its tiles
+        unsigned int *cnt0 = reinterpret_cast<unsigned int *>(ws0 + L.stg_cnt);
+        f1.stg.src = x;
+        f1.stg.col = g[0];
+        f1.stg.dst = reinterpret_cast<uint16_t *>(ws0 + L.x16);
+        f1.stg.cnt = cnt0;
+        f1.stg.paths = n;
+        f1.stg.pstride = ps;
+        for (int p = 0; p < n; ++p) f1.stg.col_p[p] = g[p];
+        GemmPlan pst = p1;
+        pst.stg = 1;
+        if (!make_tmap_x_stage(&m1.in32, x, M, d_in, 16) || !make_tmap_x_stage(&m1.sgn, x, M, d_in, 64))
+            return BLR_ERR_CUDA;
+        if (launch_prep_group(grp, cnt0, ps, stage_counters(M, p1.bt, d_in), "fwd_prep", s) != cudaSuccess)
+            return BLR_ERR_CUDA;
+        if (launch_gemm(kEpiFwd1, pst, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    } else {
+        if (launch_fwd_prologue(grp, x, M, d_in, s) != cudaSuccess) return BLR_ERR_CUDA;
+        if (launch_gemm(kEpiFwd1, p1, m1, f1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    }
     if (launch_gemm(kEpiFwd2, p2, m2, f2, s) != cudaSuccess) return BLR_ERR_CUDA;
     for (int p = 0; p < n; ++p)
         record_tape(ws0 + (size_t)p * one, Tape{M, d_in, d_out, r, x, bits_u[p], bits_v[p], g[p], l[p], h[p], 0, false,

@@ -125,6 +125,18 @@ __global__ void __launch_bounds__(256) prep_kernel(SignPrep p0, SignPrep p1, uin
     prep_share(p0, p1, blockIdx.x, gridDim.x);
 }
 
+// The same for each path of a group (block row blockIdx.y).
+__global__ void __launch_bounds__(256) prep_group_kernel(const FwdGroup grp, unsigned int *cnt0, long long pstride,
+                                                         int ncnt) {
+    const FwdPathArgs &a = grp.e[blockIdx.y];
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+    unsigned int *cnt = reinterpret_cast<unsigned int *>(reinterpret_cast<char *>(cnt0) + blockIdx.y * pstride);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += gridDim.x * blockDim.x) cnt[i] = 0u;
+    prep_share(a.p0, a.p1, blockIdx.x, gridDim.x);
+}
+
 template <int GPT, int THREADS>
 __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
     bwd_prologue_kernel(const BwdGroup grp, int stage_blocks) {
@@ -460,6 +472,23 @@ cudaError_t launch_prep(SignPrep p0, SignPrep p1, uint32_t *status, unsigned int
     if (grid < 1) grid = 1;
     trace_before(name, s);
     cudaError_t e = launch_k(prep_kernel, dim3(grid), dim3(256), 0, s, p0, p1, status, cnt, ncnt);
+    trace_after(s);
+    return e;
+}
+
+cudaError_t launch_prep_group(const FwdGroup &grp, unsigned int *cnt0, long long pstride, int ncnt, const char *name,
+                              cudaStream_t s) {
+    if (grp.n < 1 || grp.n > kMaxGroupPaths) return cudaErrorInvalidValue;
+    cudaError_t pe = prepare_kernel_once(prep_group_kernel, 0);
+    if (pe != cudaSuccess) return pe;
+    const int wave = occupancy_blocks(reinterpret_cast<const void *>(prep_group_kernel), 256, 0) *
+                     current_device_sms();
+    int grid = prep_blocks(grp.e[0].p0, 256) + prep_blocks(grp.e[0].p1, 256);
+    if (grid < (ncnt + 255) / 256) grid = (ncnt + 255) / 256;
+    if (grid * grp.n > wave) grid = (wave + grp.n - 1) / grp.n;
+    if (grid < 1) grid = 1;
+    trace_before(name, s);
+    cudaError_t e = launch_k(prep_group_kernel, dim3(grid, grp.n), dim3(256), 0, s, grp, cnt0, pstride, ncnt);
     trace_after(s);
     return e;
 }

@@ -313,8 +313,8 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                             const int tt = tile / f_tiles;
                             const int kc = ks / kChunkSteps;
                             const unsigned int need = (unsigned int)(M - tt * BT < BT ? M - tt * BT : BT);
-                            if (!wait_count(args.stg.cnt + (size_t)tt * stg_chunks(args.K) + kc, need,
-                                            abort_flag)) {
+                            if (!wait_count(path_at(args.stg.cnt, pz, args.pstride) + (size_t)tt * stg_chunks(args.K) + kc,
+                                            need, abort_flag)) {
                                 fail_status(args, abort_flag, kStTimeoutStage);
                                 ok = false;
                                 break;
@@ -849,7 +849,7 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
     } else {
         if constexpr (STG != 0) {
             // ---- stagers: x16 of later tiles -----------------------------------
-            const StgGeom G(M, args.K, BT, f_tiles, num_units);
+            const StgGeom G(M, args.K, BT, f_tiles, num_units, P);
             const StgX X(args.stg, G);
             const int t = (int)threadIdx.x - S::kStg0 * 32;
             // (the a-product has no epilogue input and no sign plane: those two

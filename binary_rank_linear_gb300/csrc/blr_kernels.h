@@ -99,6 +99,10 @@ inline cudaError_t launch_fwd_prologue(SignPrep p0, SignPrep p1, const float *x,
 // not null: the forward) and zero the stagers' ncnt row counters.
 cudaError_t launch_prep(SignPrep p0, SignPrep p1, uint32_t *status, unsigned int *cnt, int ncnt, const char *name,
                         cudaStream_t s);
+// The same for each path of a group (block row p: entry p's re-layouts and
+// status word, and the ncnt counters at cnt0 + p * pstride bytes).
+cudaError_t launch_prep_group(const FwdGroup &grp, unsigned int *cnt0, long long pstride, int ncnt, const char *name,
+                              cudaStream_t s);
 
 // Backward prologue, two parts in one launch: re-lay two bitmaps, and stage
 // dy16 = f16(dy.h.s_t) with per-token scales, dh partials and sigma_t.
@@ -188,8 +192,8 @@ inline int stage_counters(int M, int bt, int K) {
 // The stagers index items and rounds in 32-bit arithmetic: stage in the
 // kernel only while token tiles x (feature tiles + column chunks x 3 row
 // groups) stays below 2^31 (beyond any x that fits on the device).
-inline bool stage_fits(int M, int bt, int K, int f_tiles) {
-    const long long t = (M + bt - 1) / bt;
+inline bool stage_fits(int M, int bt, int K, int f_tiles, int paths = 1) {
+    const long long t = (long long)paths * ((M + bt - 1) / bt);
     return t * ((long long)f_tiles + 3ll * ((K + kStageChunkCols - 1) / kStageChunkCols)) < (1ll << 31);
 }
 
@@ -208,6 +212,12 @@ struct StageArgs {
     const float *col;      // g [K]
     uint16_t *dst;         // x16 [M][K]
     unsigned int *cnt;     // [token tiles][column chunks] rows staged (zeroed before the launch)
+    // multi-path launches (paths > 1): path p's g at col_p[p], its x16 and
+    // counters at p * pstride bytes after path 0's; the stagers take the
+    // paths' token tiles in the product's path-major order
+    int paths;
+    long long pstride;
+    const float *col_p[kMaxGroupPaths];
 };
 
 struct GemmArgs {

@@ -104,13 +104,16 @@ __device__ __forceinline__ bool wait_count(const unsigned int *cnt, unsigned int
 
 // Consumption order of the persistent GEMM grid and the stager items (32-bit
 // arithmetic: the host stages in the kernel only while the item count and
-// token tiles x feature tiles stay below 2^31, see stage_fits).
+// token tiles x feature tiles stay below 2^31, see stage_fits). With several
+// paths the grid takes the paths' tiles path-major, so the token tiles are
+// virtual: tile vt is token tile vt % t_path of path vt / t_path.
 struct StgGeom {
-    unsigned M, K, BT, t_tiles, f_tiles, units, n_kc, R, n_rg;
+    unsigned M, K, BT, t_path, t_tiles, f_tiles, units, n_kc, R, n_rg;
 
-    __device__ StgGeom(int M_, int K_, int BT_, int f_tiles_, int units_)
-        : M(M_), K(K_), BT(BT_), t_tiles((M_ + BT_ - 1) / BT_), f_tiles(f_tiles_), units(units_),
-          n_kc(stg_chunks(K_)), R(kStgRowsX), n_rg((BT_ + kStgRowsX - 1) / kStgRowsX) {}
+    __device__ StgGeom(int M_, int K_, int BT_, int f_tiles_, int units_, int paths)
+        : M(M_), K(K_), BT(BT_), t_path((M_ + BT_ - 1) / BT_), t_tiles(t_path * (unsigned)(paths > 1 ? paths : 1)),
+          f_tiles(f_tiles_), units(units_), n_kc(stg_chunks(K_)), R(kStgRowsX),
+          n_rg((BT_ + kStgRowsX - 1) / kStgRowsX) {}
     // round of a token tile: the units start tiles u, u + units, ... with the
     // feature tile varying fastest, so token tile tt first appears in round
     // floor(tt * f_tiles / units)
@@ -134,8 +137,11 @@ struct StgGeom {
         tt = (int)(lo + rem / n_rg);
         rg = (int)(rem % n_rg);
     }
-    // first row and row count of an item
-    __device__ void rows(int tt, int rg, int &r0, int &nr) const {
+    // the path and first row of x of an item, and its row count (virtual
+    // token tile vt, row group rg)
+    __device__ void rows(int vt, int rg, int &p, int &r0, int &nr) const {
+        p = vt / (int)t_path;
+        const int tt = vt - p * (int)t_path;
         r0 = tt * (int)BT + rg * (int)R;
         int r1 = r0 + (int)R;
         if (r1 > tt * (int)BT + (int)BT) r1 = tt * (int)BT + (int)BT;
@@ -165,14 +171,14 @@ __device__ __forceinline__ uint32_t mul_pack_half2(float a0, float a1, float b0,
 struct XCursor {
     unsigned j;   // this CTA's item index (CTA item cta + j * grid)
     int s;        // unit of the item
-    int r0, nr, c0, w, tt, kc;
+    int r0, nr, c0, w, tt, kc, p;  // (tt: the virtual token tile; p: the path)
 };
 
 __device__ __forceinline__ void x_cursor_load(XCursor &c, const StgGeom &G, unsigned mine, int cta, int nctas) {
     if (c.j >= mine) return;
     int rg;
     G.item((unsigned)cta + c.j * (unsigned)nctas, c.tt, c.kc, rg);
-    G.rows(c.tt, rg, c.r0, c.nr);
+    G.rows(c.tt, rg, c.p, c.r0, c.nr);
     c.c0 = c.kc * kStgKC;
     c.w = G.K - c.c0 < kStgKC ? G.K - c.c0 : kStgKC;
 }
@@ -224,7 +230,7 @@ struct StgGeo {
     int q0;  // first row
     int nq;  // rows of x in the unit (0 .. 16)
     int c0;  // first column
-    int pad;
+    int p;   // path
 };
 
 // lane 0 of the producer warp: ring units by TMA, S ahead of the converters,
@@ -234,7 +240,7 @@ __device__ inline void stager_x_producer(const StgX &X, const CUtensorMap *tmap_
                                          uint32_t *status) {
     constexpr int S = kStgSlotsX;
     const uint64_t once = l2_policy_evict_first();
-    XCursor ci{0, 0, 0, 0, 0, 0, 0, 0};
+    XCursor ci{0, 0, 0, 0, 0, 0, 0, 0, 0};
     x_cursor_load(ci, X.G, X.mine, X.cta, X.nctas);
     long long u = 0;
     for (; u < X.units; ++u) {
@@ -243,12 +249,13 @@ __device__ inline void stager_x_producer(const StgX &X, const CUtensorMap *tmap_
         const int q0 = ci.r0 + kStgUnitRows * ci.s;
         int nq = ci.r0 + ci.nr - q0;
         nq = nq < 0 ? 0 : (nq > kStgUnitRows ? kStgUnitRows : nq);
-        geo[sl] = StgGeo{q0, nq, ci.c0, 0};
+        geo[sl] = StgGeo{q0, nq, ci.c0, ci.p};
         // one box of 256 columns x 16 rows (rows and columns past x read
-        // zero), and the chunk's g factors
+        // zero), and the chunk's g factors (the unit's path's)
+        const float *g = X.a.paths > 1 ? X.a.col_p[ci.p] : X.a.col;
         mbar_arrive_expect_tx(&full[sl], (uint32_t)(kStgTileBytes + ci.w * 4));
         tma_load_2d_hint(ring + sl * kStgSlotX, tmap_x, &full[sl], ci.c0, q0, once);
-        bulk_load(ring + sl * kStgSlotX + kStgTileBytes, X.a.col + ci.c0, (uint32_t)ci.w * 4, &full[sl]);
+        bulk_load(ring + sl * kStgSlotX + kStgTileBytes, g + ci.c0, (uint32_t)ci.w * 4, &full[sl]);
         x_cursor_next(ci, X.G, X.mine, X.cta, X.nctas);
     }
     // every copy issued lands before the CTA may exit: for each slot, the
@@ -263,14 +270,14 @@ __device__ inline void stager_x_publisher(const StgX &X, const CUtensorMap *tmap
                                           const unsigned int *done, uint32_t *status) {
     auto prefetch_item = [&](unsigned j) {
         if (j >= X.mine) return;
-        XCursor c{j, 0, 0, 0, 0, 0, 0, 0};
+        XCursor c{j, 0, 0, 0, 0, 0, 0, 0, 0};
         x_cursor_load(c, X.G, X.mine, X.cta, X.nctas);
         if (c.nr > 0) tma_prefetch_l2_2d(tmap_pf, c.c0, c.r0);  // one 256 x 64 box
     };
     for (unsigned j = 0; j < kStgPrefetchItems; ++j) prefetch_item(j);
     for (unsigned j = 0; j < X.mine; ++j) {
         prefetch_item(j + kStgPrefetchItems);
-        XCursor c{j, 0, 0, 0, 0, 0, 0, 0};
+        XCursor c{j, 0, 0, 0, 0, 0, 0, 0, 0};
         x_cursor_load(c, X.G, X.mine, X.cta, X.nctas);
         const unsigned target = (j + 1) * kStgConvWarps;
         if (ld_acquire_shared_u32(done) < target) {
@@ -291,7 +298,13 @@ __device__ inline void stager_x_publisher(const StgX &X, const CUtensorMap *tmap
                 return;
             }
         }
-        if (c.nr > 0) red_release_add_u32(X.a.cnt + (size_t)c.tt * X.G.n_kc + c.kc, (unsigned int)c.nr);
+        if (c.nr > 0) {
+            // the counter of (token tile, chunk) in the item's path's slice
+            unsigned int *cnt = reinterpret_cast<unsigned int *>(reinterpret_cast<char *>(X.a.cnt) +
+                                                                 (size_t)c.p * (size_t)X.a.pstride);
+            const int tt = c.tt - c.p * (int)X.G.t_path;
+            red_release_add_u32(cnt + (size_t)tt * X.G.n_kc + c.kc, (unsigned int)c.nr);
+        }
     }
 }
 
@@ -338,7 +351,9 @@ __device__ inline void stager_x_convert(const StgX &X, int t, volatile int *abor
             if (col < K) {
                 const float4 *gs = reinterpret_cast<const float4 *>(ring + sl * kStgSlotX + kStgTileBytes) + 2 * cg;
                 const float4 g0 = gs[0], g1 = gs[1];
-                uint16_t *dst = X.a.dst + (size_t)(gq.q0 + rp) * K + col;
+                uint16_t *dst = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(X.a.dst) +
+                                                             (size_t)gq.p * (size_t)X.a.pstride) +
+                                (size_t)(gq.q0 + rp) * K + col;
 #pragma unroll
                 for (int i = 0; i < kRows; ++i)
                     if (rp + kStgConvWarps * i < gq.nq) {

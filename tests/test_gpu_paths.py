@@ -110,6 +110,24 @@ def test_grouped_paths_match_the_loop(monkeypatch, P, M, d_in, d_out, r):
     _check(x, dy, paths, got_g)
 
 
+@pytest.mark.parametrize("P,M,d_in,d_out,r", [(3, 4600, 1024, 1568, 256), (8, 129, 192, 96, 64),
+                                              (2, 2000, 2048, 512, 512)])
+def test_grouped_paths_stage_x_in_kernel(monkeypatch, P, M, d_in, d_out, r):
+    """The grouped forward with every path's x staged inside the a-product
+    (BLR_STAGE=kernel; by default for x of 64 MB or more): the stagers take
+    the paths' token tiles path-major, each with its own g, x16 and row
+    counters. Against the per-path loop with the same staging and against
+    the oracle."""
+    monkeypatch.setenv("BLR_STAGE", "kernel")
+    x, dy, paths = _paths_inputs(P, M, d_in, d_out, r)
+    got_g = _run_paths(x, dy, paths)
+    monkeypatch.setenv("BLR_PATHS", "loop")
+    got_l = _run_paths(x, dy, paths)
+    assert oracle.rel_err(got_g[0], got_l[0]) <= 1e-6
+    assert oracle.rel_err(got_g[1], got_l[1]) <= 1e-6
+    _check(x, dy, paths, got_g)
+
+
 def test_grouped_paths_integer_grid():
     """Bit-exact on a grid of small multiples of powers of two (every staged
     operand exact in f16, every product and partial sum exact in f32): three
