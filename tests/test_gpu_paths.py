@@ -90,12 +90,13 @@ def test_paths_parity(P, M, d_in, d_out, r):
 
 @pytest.mark.parametrize("P,M,d_in,d_out,r", [(2, 300, 320, 448, 96), (3, 4600, 1024, 1568, 256),
                                               (10, 129, 192, 96, 64), (2, 8192, 512, 4096, 128),
-                                              (9, 4600, 256, 1568, 256), (64, 17, 64, 96, 64), (3, 1, 64, 64, 64)])
+                                              (9, 4600, 256, 1568, 256), (64, 17, 64, 96, 64), (3, 1, 64, 64, 64),
+                                              (2, 33, 65536, 64, 64), (2, 40, 64, 32768, 128)])
 def test_grouped_paths_match_the_loop(monkeypatch, P, M, d_in, d_out, r):
     """The grouped passes (one launch per stage for up to eight paths; nine
     or ten paths take two groups, the second adding into y and dx, and the
     most paths a call takes, 64, eight groups; CTA-pair tiles at 4600 tokens;
-    a single token) against each
+    a single token; the widest d_in and d_out the shape rule admits) against each
     path's single-path calls in turn (BLR_PATHS=loop): y and dx receive the
     same contributions in the same order, and each path's dh, dl, dg the same
     partial sums up to their grouping; both against the oracle."""
