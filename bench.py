@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "blr fwd+bwd tokens/sec and TFLOP/s (% of GB300 f16 tensor peak / % HBM BW)"
 L2_BYTES = 129 * 1024 * 1024
+E2E_PIPE = 3  # device buffer sets the end-to-end measurement pipelines over
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -314,9 +315,10 @@ class Layer:
 
 
 def nsets_for(layers_w, blr):
-    """Rotating buffer sets: enough that one round of sets exceeds twice the L2."""
+    """Rotating buffer sets: enough that one round of sets exceeds twice the L2,
+    and at least E2E_PIPE (the end-to-end pipeline's depth)."""
     total = sum(Layer.set_bytes(w, blr.workspace_bytes(w.M, w.d_in, w.d_out, w.r)) for w in layers_w)
-    return max(2, min(64, -(-2 * L2_BYTES // total) + 1)), total
+    return max(E2E_PIPE, min(64, -(-2 * L2_BYTES // total) + 1)), total
 
 
 def label(layers, li, name):
@@ -565,8 +567,8 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": {"value": job_tokens_per_s(world, M, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "overlapped with the layers on their own streams" if pipelined else
-                          "in order on one stream"},
+                "copies": (f"overlapped with the layers on their own streams, {E2E_PIPE} buffer sets in flight"
+                           if pipelined else "in order on one stream")},
     }
     if sign is not None:
         result["sign_grads"] = sign
@@ -594,9 +596,14 @@ def measure_e2e(layers, args, dev):
     a training loop's data path would be: step i+1's inputs go up and step
     i-1's results come down while step i computes. Smaller steps run in order
     on one stream (there the host's launch work, not the copies, sets the
-    pace). Returns (ms, h2d bytes per step, d2h bytes per step, pipelined)."""
+    pace). Returns (ms, h2d bytes per step, d2h bytes per step, pipelined).
+
+    Three buffer sets: step i+1's inputs go up into the set whose results
+    (step i-2's) came down a step earlier, so the two directions of the host
+    link run at the same time; with two sets each upload would wait for the
+    previous download of its set, and the copies would take turns."""
     import torch
-    npipe = 2
+    npipe = E2E_PIPE
     h2d = sum(4 * L.w.M * (L.w.d_in + L.w.d_out) for L in layers)
     d2h = sum(4 * (L.w.M * (L.w.d_in + L.w.d_out) + L.w.d_in + L.w.r + L.w.d_out) for L in layers)
     pipelined = h2d >= (1 << 20)
