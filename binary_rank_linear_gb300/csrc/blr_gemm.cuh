@@ -24,14 +24,17 @@
 // tile overlaps the main loop of the next) and the remaining columns as sign
 // stages of 64 columns (one 128-deep k-step each, two f16 per column).
 //
-// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-9 sign expanders (warp w writes TMEM lanes 32*(w%4) .. +31
-// of one of the k-step's two 64-wide blocks), warps 10-13 epilogue (warp w
-// reads lanes 32*(w%4) .. +31: each thread owns one feature of the tile and
-// walks its tokens, so the token sums dl and dg are per-thread running sums).
-// The dx'-product runs four expander warps (both blocks of a lane quarter
-// each) and eight epilogue warps (two per quarter, alternate chunks); the
-// kernels that stage x run four expander warps and six stager warps.
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-5 sign expanders (warp w writes TMEM lanes 32*(w%4) .. +31
+// of both of the k-step's 64-wide blocks), warps 6-9 epilogue (warp w reads
+// lanes 32*(w%4) .. +31: each thread owns one feature of the tile and walks
+// its tokens, so the token sums dl and dg are per-thread running sums). The
+// dx'-product runs eight epilogue warps (two per quarter, alternate chunks);
+// the kernels that stage x add six stager warps. (Measured on GB300, four
+// expander warps of two blocks each against eight of one: db-product of the
+// 4096 -> 12288 MLP layer 262 against 278 us, c-product 303 against 309, the
+// attention-sized db-product 63.4 against 67.5; half as many arrivals on each
+// sign stage's barrier.)
 // The epilogue stages each 32-token x 32-feature chunk in shared memory
 // ([token][feature], the layout of the row-major outputs) and writes it with
 // a TMA store; inputs (the a-tape, x, or y to accumulate) arrive by TMA into
@@ -75,11 +78,11 @@ constexpr int kTmemCols = 512;
 constexpr int kWarpTma = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpExp0 = 2;
-constexpr int kNumExpWarps = 8;
-constexpr int kWarpEpi0 = 10;
-constexpr int kGemmThreads = (kWarpEpi0 + 4) * 32;  // the fused small-M kernels' block (every phase fits)
+constexpr int kNumExpWarps = 4;  // one per TMEM lane quarter, both 64-wide blocks of a k-step
+constexpr int kWarpEpi0 = 6;
+constexpr int kGemmThreads = (kWarpEpi0 + 8) * 32;  // the fused small-M kernels' block (every phase fits)
 constexpr int kCtlBytes = 1024;   // shared-memory control block ahead of a phase's layout
-static_assert(kNumExpWarps == 4 * kKB, "one expander warp per (lane quarter, 64-wide block)");
+static_assert(kNumExpWarps == 4, "one expander warp per TMEM lane quarter");
 static_assert(kWarpExp0 % 4 == 2, "expander and epilogue warps cover the four TMEM lane quarters in turn");
 
 // PLANE selects where the sign operand comes from: false, bitmap words
@@ -99,12 +102,11 @@ template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 struct GemmShape {
     static constexpr int kKBm = PLANE ? 1 : kKB;           // 64-wide blocks per k-step
     static constexpr int kStepKm = kKBm * kBK;             // K per k-step
-    // expander warps: one per (TMEM lane quarter, 64-wide block) of a k-step,
-    // or one per lane quarter covering both blocks where other roles need the
-    // warp slots: the stager warps of the kernels that stage x, the second
-    // epilogue warp of each quarter in the dx'-product (16 warps or fewer keep
-    // every role at 128 registers; more cap them at 96)
-    static constexpr int kNExp = PLANE ? 0 : ((STG || EPI == kEpiBwd2) ? 4 : kNumExpWarps);
+    // expander warps: one per TMEM lane quarter, covering both 64-wide blocks
+    // of a k-step (with the stager warps or the dx'-product's second epilogue
+    // warp per quarter a CTA stays at 16 warps or fewer, which keeps every
+    // role at 128 registers; more would cap them at 96)
+    static constexpr int kNExp = PLANE ? 0 : kNumExpWarps;
     static constexpr int kEpi0 = PLANE ? 2 : kWarpExp0 + kNExp;  // first epilogue warp
     static constexpr bool kPlaneMN = EPI == kEpiFwd1 || EPI == kEpiBwd1;  // plane rows run along K
     static constexpr int kAccCols = BT;                    // TMEM columns of one accumulator
