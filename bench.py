@@ -113,6 +113,13 @@ def kernel_work(name: str, M: int, d_in: int, d_out: int, r: int):
         "fwd_prep": (0.0, bits_u + bits_v, relaid_u + relaid_v),
         "gemm_fwd1s": (2.0 * M * r * d_in, 4.0 * M * d_in + 4.0 * M * r,
                        4.0 * M * d_in + 2.0 * M * r + relaid_v),
+        # a backward whose dy staging runs in the db-product: the scale pass
+        # reads dy for the per-token scales; the staging product reads c for
+        # the dh sums and reads dy again (a staging round trip, like the f16
+        # operand it writes and then reads)
+        "bwd_scales": (0.0, 4.0 * M * d_out + bits_u + bits_v, relaid_ut + relaid_vd),
+        "gemm_bwd1s": (2.0 * M * r * d_out, 4.0 * M * r + 2.0 * M * d_out,
+                       8.0 * M * d_out + 2.0 * M * r + relaid_ut + parts),
     }
     if name == "small_fwd":
         return tuple(sum(table[n][i] for n in ("fwd_prologue", "gemm_fwd1", "gemm_fwd2")) for i in range(3))

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libblr.so")
-SOURCES = ["blr_aux.cu", "blr_gemm_fwd.cu", "blr_gemm_bwd.cu", "blr_gemm_stg_fwd.cu", "blr_small.cu", "blr_sign.cu", "blr_dense.cu", "blr_plane.cu", "blr_adam.cu", "blr_api.cu", "blr_noalloc.cu"]
+SOURCES = ["blr_aux.cu", "blr_gemm_fwd.cu", "blr_gemm_bwd.cu", "blr_gemm_stg_fwd.cu", "blr_gemm_stg_bwd.cu", "blr_small.cu", "blr_sign.cu", "blr_dense.cu", "blr_plane.cu", "blr_adam.cu", "blr_api.cu", "blr_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -56,14 +56,16 @@ void trace_after(cudaStream_t stream) {
 }
 
 cudaError_t launch_gemm_stg_fwd(const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
+cudaError_t launch_gemm_stg_bwd(const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s);
 
 cudaError_t launch_gemm(int epi, const GemmPlan &plan, const GemmMaps &maps, const GemmArgs &args, cudaStream_t s) {
     static const char *names[4] = {"gemm_fwd1", "gemm_fwd2", "gemm_bwd1", "gemm_bwd2"};
     if (plan.stg) {
-        // the a-product with x staged in the kernel
-        if (plan.stg != 1 || epi != kEpiFwd1) return cudaErrorInvalidValue;
-        trace_before("gemm_fwd1s", s);
-        cudaError_t e = launch_gemm_stg_fwd(plan, maps, args, s);
+        // the a-product with x, or the db-product with dy, staged in the kernel
+        const bool fwd = plan.stg == 1 && epi == kEpiFwd1, bwd = plan.stg == 2 && epi == kEpiBwd1;
+        if (!fwd && !bwd) return cudaErrorInvalidValue;
+        trace_before(fwd ? "gemm_fwd1s" : "gemm_bwd1s", s);
+        cudaError_t e = fwd ? launch_gemm_stg_fwd(plan, maps, args, s) : launch_gemm_stg_bwd(plan, maps, args, s);
         trace_after(s);
         return e;
     }
@@ -177,6 +179,20 @@ bool make_tmap_x_stage(CUtensorMap *m, const void *base, int rows, int cols, int
     cuuint32_t box[2] = {(cuuint32_t)kStageChunkCols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The c tape [rows][cols] f16 in 256-column boxes of box_rows rows, no
+// swizzle: the db-product's dy stagers read it beside dy for the dh sums.
+bool make_tmap_c_stage(CUtensorMap *m, const void *base, int rows, int cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kStageChunkCols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -472,6 +488,19 @@ bool stage_in_kernel(long long x_bytes) {
     if (v && std::strcmp(v, "pass") == 0) return false;
     if (v && std::strcmp(v, "kernel") == 0) return true;
     return x_bytes >= (64ll << 20);
+}
+
+// dy16 staged inside the db-product (after a scale pass) with
+// BLR_DY_STAGE=kernel, wherever the db-product runs CTA-pair tiles of one
+// path; by the backward prologue otherwise (the default). Measured on GB300:
+// the 12288-wide MLP layer's scale pass, staged db-product and reduction take
+// 146 + 401 + 16 us against 307 + 264 + 12 for the prologue form, but the
+// CUDA-graph step of the MLP pair is no faster (2.207 ms at 1995 MHz against
+// 2.189 at 2010); at 4096-wide rows the prologue form is faster outright
+// (attention-sized 35 + 96 against 61 + 65 us).
+bool dy_stage_in_kernel() {
+    const char *v = std::getenv("BLR_DY_STAGE");
+    return v && std::strcmp(v, "kernel") == 0;
 }
 
 // Grid barriers of the fused small-M kernels and of the dx'-product's folded
@@ -1057,22 +1086,54 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
         ba.rh = ReduceSeg{part_dh, dh, 0, d_out};
         ba.rl = sl;
         ba.rg = sg;
-        if (launch_small_bwd(m1, m2, ba, small_grid(p1, r, p2, d_in, M, sms), L.rows_dh, s) != cudaSuccess)
+        if (launch_small_bwd(m1, m2, ba, small_grid(p1, r, p2, d_in, M, sms), stage_dy_blocks(M, d_out), s) !=
+            cudaSuccess)
             return BLR_ERR_CUDA;
         mark_backward_done(ws, gscale, rows_dh);
         return BLR_OK;
     }
     const bool fold = !dense2 && reduce_folded();
     if (fold) sa.red_cnt = reinterpret_cast<unsigned int *>(w + L.header + kRedCntOffset);
-    if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
-    if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
+    // dy staged inside the db-product (large dy, CTA-pair tiles of one
+    // path, no split-K or sign planes): a scale pass first, then the product
+    // stages dy16 and adds the dh sums into kDyPartRowsPerCta rows per CTA
+    const bool dstg = !planes && p1.pair && p1.split <= 1 && dy_stage_in_kernel() &&
+                      stage_fits(M, p1.bt, d_out, (r + 255) / 256) && p1.grid <= kDyStageMaxCtas;
+    int dh_rows = 0;
+    if (dstg) {
+        unsigned int *cnt = reinterpret_cast<unsigned int *>(w + L.stg_cnt);
+        sa.zero_cnt = cnt;
+        sa.n_cnt = stage_counters(M, p1.bt, d_out);
+        sa.zero_part = part_dh;
+        sa.n_part = (long long)p1.grid * kDyPartRowsPerCta * d_out;
+        b1.stg.src = dy;
+        b1.stg.col = h;
+        b1.stg.dst = dy16;
+        b1.stg.cnt = cnt;
+        b1.stg.row_sinv = s_inv;
+        b1.stg.part = part_dh;
+        GemmPlan ps = p1;
+        ps.stg = 2;
+        // the db-product has no f32 output and no sign plane: those maps carry
+        // dy (256 x 16 boxes for the ring, 256 x 64 for the L2 prefetches)
+        if (!make_tmap_x_stage(&m1.out32, dy, M, d_out, 16) || !make_tmap_x_stage(&m1.sgn, dy, M, d_out, 64) ||
+            !make_tmap_c_stage(&m1.aux, c16, M, d_out, 16))
+            return BLR_ERR_CUDA;
+        if (launch_bwd_scales(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
+        if (launch_gemm(kEpiBwd1, ps, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
+        dh_rows = p1.grid * kDyPartRowsPerCta;
+    } else {
+        if (launch_bwd_prologue(pu, pv, sa, s) != cudaSuccess) return BLR_ERR_CUDA;
+        if (launch_gemm(kEpiBwd1, p1, m1, b1, s) != cudaSuccess) return BLR_ERR_CUDA;
+        dh_rows = rows_dh;
+    }
     if (fold) {
-        // dh, dl and dg reduced in the dx'-product's tail (rows_dh is known now)
+        // dh, dl and dg reduced in the dx'-product's tail (the dh rows are known now)
         b2.fold = 1;
         b2.red = grid_barrier(sa.red_cnt);
         b2.red_part_h = part_dh;
         b2.red_part_l = part_dl;
-        b2.red_rows_h = rows_dh;
+        b2.red_rows_h = dh_rows;
         b2.red_rows_l = sl.rows;
         b2.red_rows_g = sg.rows;
         b2.red_n_h = d_out;
@@ -1087,7 +1148,7 @@ int blr_backward(const float *x, const float *dy, const uint32_t *bits_u, const 
         return BLR_ERR_CUDA;
     }
     if (!fold) {
-        ReduceSeg sh{part_dh, dh, rows_dh, d_out};
+        ReduceSeg sh{part_dh, dh, dh_rows, d_out};
         if (launch_reduce_partials(sh, sl, sg, s) != cudaSuccess) return BLR_ERR_CUDA;
     }
     mark_backward_done(ws, gscale, rows_dh);

@@ -137,7 +137,17 @@ __global__ void __launch_bounds__(256) prep_group_kernel(const FwdGroup grp, uns
     prep_share(a.p0, a.p1, blockIdx.x, gridDim.x);
 }
 
-template <int GPT, int THREADS>
+// The scale pass (SC) also zeroes the db-product's stager counters and dh
+// partial rows before any of its other work.
+__device__ __forceinline__ void scale_pass_zero(const StageDyArgs &a) {
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nth = (long long)gridDim.x * blockDim.x;
+    for (long long i = tid; i < a.n_cnt; i += nth) a.zero_cnt[i] = 0u;
+    float4 *p = reinterpret_cast<float4 *>(a.zero_part);
+    for (long long i = tid; i < a.n_part / 4; i += nth) p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <int GPT, int THREADS, bool SC = false>
 __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
     bwd_prologue_kernel(const BwdGroup grp, int stage_blocks) {
     extern __shared__ __align__(16) float smem_f[];
@@ -145,14 +155,108 @@ __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0 && e.sd.red_cnt) *e.sd.red_cnt = 0u;
+    if (SC) scale_pass_zero(e.sd);
     if (prologue_prep(e.p0, e.p1, stage_blocks)) return;
-    stage_dy_run<GPT>(e.sd, blockIdx.x, stage_blocks, smem_f, stage_tpr(e.sd.d_out, THREADS), THREADS);
+    stage_dy_run<GPT, SC>(e.sd, blockIdx.x, stage_blocks, smem_f, stage_tpr(e.sd.d_out, THREADS), THREADS);
+}
+
+// ============================================== scale pass (STG = 2) =======
+// Ahead of a db-product that stages dy itself: per row the scales of the
+// dy staging (s_t from max |dy.h|, sigma_t from sum |dy.h| max |l|, the same
+// rules and arithmetic per element as stage_dy_run), written as s_inv, sig,
+// sig_inv, and per block the maxima blkmax. One warp per row, 128-bit
+// streaming loads straight from global memory (four in flight per lane), no
+// shared-memory ring: nothing of the row is kept. Blocks past stage_blocks
+// do the bitmap re-layouts; every thread first zeroes its share of the
+// db-product's stager counters and dh partial rows.
+constexpr int kScaleThreads = 1024;
+__global__ void __launch_bounds__(kScaleThreads, 1) bwd_scale_kernel(const BwdGroup grp, int stage_blocks) {
+    const BwdPathArgs &e = grp.e[0];
+    const StageDyArgs &a = e.sd;
+    __shared__ float2 red[kScaleThreads / 32];
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.red_cnt) *a.red_cnt = 0u;
+    scale_pass_zero(a);
+    if (prologue_prep(e.p0, e.p1, stage_blocks)) return;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31, nw = kScaleThreads / 32;
+    const bool dynamic = !(a.gscale > 0.0f);
+    const float ginv = dynamic ? 1.0f : 1.0f / a.gscale;
+    float lmax = 0.0f;
+    if (dynamic) {
+        for (int k = lane; k < a.r; k += 32) lmax = fmaxf(lmax, fabsf(__ldg(a.l + k)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+    }
+    const int G = a.d_out / 4;
+    const float4 *dy4 = reinterpret_cast<const float4 *>(a.dy);
+    const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
+    const int row0 = (int)((long long)blockIdx.x * a.M / stage_blocks);
+    const int row1 = (int)((long long)(blockIdx.x + 1) * a.M / stage_blocks);
+    float2 mx = make_float2(0.0f, 0.0f);
+    for (int t = row0 + warp; t < row1; t += nw) {
+        const float4 *src = dy4 + (size_t)t * G;
+        float amax = 0.0f, l1 = 0.0f;
+        int c = lane;
+        for (; c + 96 < G; c += 128) {
+            float4 d[4], f[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                d[i] = __ldcs(src + c + 32 * i);
+                f[i] = __ldg(h4 + c + 32 * i);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float vx = fabsf(d[i].x * f[i].x), vy = fabsf(d[i].y * f[i].y);
+                const float vz = fabsf(d[i].z * f[i].z), vw = fabsf(d[i].w * f[i].w);
+                amax = fmaxf(amax, fmaxf(fmaxf(vx, vy), fmaxf(vz, vw)));
+                l1 += (vx + vy) + (vz + vw);
+            }
+        }
+        for (; c < G; c += 32) {
+            const float4 d = __ldcs(src + c), f = __ldg(h4 + c);
+            const float vx = fabsf(d.x * f.x), vy = fabsf(d.y * f.y), vz = fabsf(d.z * f.z), vw = fabsf(d.w * f.w);
+            amax = fmaxf(amax, fmaxf(fmaxf(vx, vy), fmaxf(vz, vw)));
+            l1 += (vx + vy) + (vz + vw);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+        }
+        if (lane == 0) {
+            float s = a.gscale, sig = a.gscale;
+            bool counts = true;
+            if (dynamic) {
+                const bool fin = amax > 0.0f && amax <= 3.402823466e38f;
+                counts = fin;
+                s = fin ? pow2i(14 - ceil_log2_pos(amax)) : 1.0f;
+                sig = s;
+                const float bound = l1 * lmax;  // bound on |db_t . l|, unscaled
+                if (fin && bound > 0.0f && bound <= 3.402823466e38f) sig = pow2i(15 - ceil_log2_pos(bound));
+            }
+            const float si = dynamic ? pow2_recip(s) : ginv, gi = dynamic ? pow2_recip(sig) : ginv;
+            a.s_inv[t] = si;
+            a.sig[t] = sig;
+            a.sig_inv[t] = gi;
+            if (counts) mx = make_float2(fmaxf(mx.x, si), fmaxf(mx.y, gi));
+        }
+    }
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 1; i < nw; ++i) {
+            mx.x = fmaxf(mx.x, red[i].x);
+            mx.y = fmaxf(mx.y, red[i].y);
+        }
+        a.blkmax[blockIdx.x] = mx;
+    }
 }
 
 // Streaming form of the same prologue (rows up to kSdMaxCols wide): one block
 // per SM, a producer warp feeding row batches through a shared-memory ring.
 // Blocks past stage_blocks only do bitmap re-layouts.
-template <int Q>
+template <int Q, bool SC = false>
 __global__ void __launch_bounds__(kSdThreads, 1)
     bwd_stream_kernel(const BwdGroup grp, int stage_blocks) {
     extern __shared__ __align__(128) unsigned char smem_b[];
@@ -160,12 +264,13 @@ __global__ void __launch_bounds__(kSdThreads, 1)
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0 && e.sd.red_cnt) *e.sd.red_cnt = 0u;
+    if (SC) scale_pass_zero(e.sd);
     const int extra = (int)gridDim.x - stage_blocks;
     if (extra > 0 && (int)blockIdx.x >= stage_blocks) {
         prep_share(e.p0, e.p1, (int)blockIdx.x - stage_blocks, extra);
         return;
     }
-    stage_dy_stream<Q>(e.sd, blockIdx.x, stage_blocks, smem_b, e.p0, e.p1, extra > 0 ? 0 : stage_blocks);
+    stage_dy_stream<Q, SC>(e.sd, blockIdx.x, stage_blocks, smem_b, e.p0, e.p1, extra > 0 ? 0 : stage_blocks);
 }
 
 int stage_dy_blocks(int M, int d_out) {
@@ -378,16 +483,16 @@ cudaError_t launch_fwd_prologue(const FwdGroup &grp, const float *x, int M, int 
     return e;
 }
 
-template <int GPT, int THREADS = kStageThreads>
+template <int GPT, int THREADS = kStageThreads, bool SC = false>
 static cudaError_t launch_bwd_prologue_t(const BwdGroup &grp, cudaStream_t s) {
     const StageDyArgs &a = grp.e[0].sd;
     const SignPrep &p0 = grp.e[0].p0, &p1 = grp.e[0].p1;
     const int tpr = stage_tpr(a.d_out, THREADS);
     const int rb_n = THREADS / tpr;
     const size_t smem = stage_dy_smem_bytes(a.d_out, tpr, rb_n * tpr);
-    cudaError_t pe = prepare_kernel_once(bwd_prologue_kernel<GPT, THREADS>, 200 * 1024);
+    cudaError_t pe = prepare_kernel_once(bwd_prologue_kernel<GPT, THREADS, SC>, 200 * 1024);
     if (pe != cudaSuccess) return pe;
-    const int per_sm = occupancy_blocks(reinterpret_cast<const void *>(bwd_prologue_kernel<GPT, THREADS>), THREADS,
+    const int per_sm = occupancy_blocks(reinterpret_cast<const void *>(bwd_prologue_kernel<GPT, THREADS, SC>), THREADS,
                                         smem);
     const int sms = current_device_sms();
     int sb = stage_dy_blocks(a.M, a.d_out);
@@ -395,18 +500,19 @@ static cudaError_t launch_bwd_prologue_t(const BwdGroup &grp, cudaStream_t s) {
     // re-layout-only blocks where the wave has room for them
     const int pb = prep_blocks(p0, THREADS) + prep_blocks(p1, THREADS);
     const int grid = sb + pb <= per_sm * sms ? sb + pb : sb;
-    trace_before("bwd_prologue", s);
-    cudaError_t e = launch_k(bwd_prologue_kernel<GPT, THREADS>, dim3(grid, grp.n), dim3(THREADS), smem, s, grp, sb);
+    trace_before(SC ? "bwd_scales" : "bwd_prologue", s);
+    cudaError_t e =
+        launch_k(bwd_prologue_kernel<GPT, THREADS, SC>, dim3(grid, grp.n), dim3(THREADS), smem, s, grp, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;
 }
 
-template <int Q>
+template <int Q, bool SC = false>
 static cudaError_t launch_bwd_stream_t(const BwdGroup &grp, cudaStream_t s) {
     const StageDyArgs &a = grp.e[0].sd;
     const SignPrep &p0 = grp.e[0].p0, &p1 = grp.e[0].p1;
-    cudaError_t pe = prepare_kernel_once(bwd_stream_kernel<Q>, kSdHeadBytes + kSdRingBytes);
+    cudaError_t pe = prepare_kernel_once(bwd_stream_kernel<Q, SC>, kSdHeadBytes + kSdRingBytes);
     if (pe != cudaSuccess) return pe;
     const int sms = current_device_sms();
     const SdPlan pl = sd_plan(a.d_out);
@@ -417,9 +523,9 @@ static cudaError_t launch_bwd_stream_t(const BwdGroup &grp, cudaStream_t s) {
     // re-layout-only blocks on SMs the staging leaves idle
     const int pb = prep_blocks(p0, kSdThreads) + prep_blocks(p1, kSdThreads);
     const int grid = sb + pb <= sms ? sb + pb : sb;
-    trace_before("bwd_prologue", s);
-    cudaError_t e = launch_k(bwd_stream_kernel<Q>, dim3(grid, grp.n), dim3(kSdThreads), sd_smem_bytes(a.d_out), s,
-                             grp, sb);
+    trace_before(SC ? "bwd_scales" : "bwd_prologue", s);
+    cudaError_t e = launch_k(bwd_stream_kernel<Q, SC>, dim3(grid, grp.n), dim3(kSdThreads), sd_smem_bytes(a.d_out),
+                             s, grp, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;
@@ -432,33 +538,57 @@ static bool dy_stage_rows_forced() {
     return e && std::strcmp(e, "rows") == 0;
 }
 
-cudaError_t launch_bwd_prologue(const BwdGroup &grp, cudaStream_t s) {
+template <bool SC>
+static cudaError_t launch_bwd_prologue_sc(const BwdGroup &grp, cudaStream_t s) {
     if (grp.n < 1 || grp.n > kMaxGroupPaths) return cudaErrorInvalidValue;
     const StageDyArgs &a = grp.e[0].sd;
     if (sd_supported(a.d_out) && !dy_stage_rows_forced()) {
         switch (sd_plan(a.d_out).Q) {
-            case 2: return launch_bwd_stream_t<2>(grp, s);
-            case 4: return launch_bwd_stream_t<4>(grp, s);
-            case 6: return launch_bwd_stream_t<6>(grp, s);
-            default: return launch_bwd_stream_t<8>(grp, s);
+            case 2: return launch_bwd_stream_t<2, SC>(grp, s);
+            case 4: return launch_bwd_stream_t<4, SC>(grp, s);
+            case 6: return launch_bwd_stream_t<6, SC>(grp, s);
+            default: return launch_bwd_stream_t<8, SC>(grp, s);
         }
     }
     switch (stage_gpt(a.d_out)) {
-        case 1: return launch_bwd_prologue_t<1>(grp, s);
-        case 2: return launch_bwd_prologue_t<2>(grp, s);
+        case 1: return launch_bwd_prologue_t<1, kStageThreads, SC>(grp, s);
+        case 2: return launch_bwd_prologue_t<2, kStageThreads, SC>(grp, s);
         case 3:
-        case 4: return launch_bwd_prologue_t<4>(grp, s);
+        case 4: return launch_bwd_prologue_t<4, kStageThreads, SC>(grp, s);
         case 5:
         case 6:
         case 7:
-        case 8: return launch_bwd_prologue_t<8>(grp, s);
+        case 8: return launch_bwd_prologue_t<8, kStageThreads, SC>(grp, s);
         default: break;
     }
     // rows wider than 16384: 1024-thread blocks, 8 groups per thread (measured
     // on GB300, 4000 rows of 32768: 271 -> 228 us against 512 threads with 16;
     // at 12288 the 512-thread blocks stay faster, 293 against 310 us)
-    if (stage_gpt(a.d_out, 1024) <= 8) return launch_bwd_prologue_t<8, 1024>(grp, s);
+    if (stage_gpt(a.d_out, 1024) <= 8) return launch_bwd_prologue_t<8, 1024, SC>(grp, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_prologue(const BwdGroup &grp, cudaStream_t s) { return launch_bwd_prologue_sc<false>(grp, s); }
+
+// The scale pass ahead of a db-product that stages dy itself (StageDyArgs
+// zero_cnt, zero_part): one block of bwd_scale_kernel per SM, plus blocks
+// for the bitmap re-layouts where the wave has room for them.
+cudaError_t launch_bwd_scales(const BwdGroup &grp, cudaStream_t s) {
+    if (grp.n != 1) return cudaErrorInvalidValue;
+    const StageDyArgs &a = grp.e[0].sd;
+    const SignPrep &p0 = grp.e[0].p0, &p1 = grp.e[0].p1;
+    const int sms = current_device_sms();
+    int sb = sms;
+    const int cap = stage_dy_blocks(a.M, a.d_out);  // blkmax rows of the workspace
+    if (sb > cap) sb = cap;
+    if (sb > a.M) sb = a.M;
+    const int pb = prep_blocks(p0, kScaleThreads) + prep_blocks(p1, kScaleThreads);
+    const int grid = sb + pb <= sms ? sb + pb : sb;
+    trace_before("bwd_scales", s);
+    cudaError_t e = launch_k(bwd_scale_kernel, dim3(grid), dim3(kScaleThreads), 0, s, grp, sb);
+    trace_after(s);
+    if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
+    return e;
 }
 
 cudaError_t launch_prep(SignPrep p0, SignPrep p1, uint32_t *status, unsigned int *cnt, int ncnt, const char *name,

@@ -97,7 +97,8 @@ static_assert(kWarpExp0 % 4 == 2, "expander and epilogue warps cover the four TM
 // leader (full_p) once the peer's loads have landed.
 // STG: 0, the activation operand is staged before the launch; 1, stager
 // warps after the epilogue warps stage x inside the a-product's kernel
-// (blr_stager.cuh), with a 51 KB ring of their own.
+// (blr_stager.cuh), with a 51 KB ring of their own; 2, the same for the
+// db-product's dy (75 KB ring: each unit also brings its c tile and scales).
 template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 struct GemmShape {
     static constexpr int kKBm = PLANE ? 1 : kKB;           // 64-wide blocks per k-step
@@ -137,8 +138,8 @@ struct GemmShape {
                              : PLANE ? (EPI == kEpiBwd2 ? 3 : 2)
                                      : (EPI == kEpiBwd2 ? 4 : (kSplit == 2 ? 2 : 4));
     static constexpr int kEpiBytes = kEW * kNE * kSlotBytes;
-    static constexpr int kStgBytes = STG ? kStgRingBytes : 0;
-    static constexpr int kStgSlots = STG ? kStgSlotsX : 0;
+    static constexpr int kStgBytes = STG == 1 ? kStgRingBytes : (STG == 2 ? kStgRingBytesDy : 0);
+    static constexpr int kStgSlots = STG == 1 ? kStgSlotsX : (STG == 2 ? kStgSlotsDy : 0);
     static constexpr int kBudget = (PLANE ? 224 : 221) * 1024 - kEpiBytes - kStgBytes;
     static constexpr int kNBRaw = kBudget / (kBBytes + kBitsBytes);
     static constexpr int kNB = kNBRaw > 10 ? 10 : kNBRaw;
@@ -253,10 +254,12 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
                                            const CUtensorMap &tmap_in, const CUtensorMap &tmap_out32,
                                            const CUtensorMap &tmap_out16, const GemmArgs &args,
                                            uint32_t tmem_base, volatile int *abort_flag, int unit, int num_units,
-                                           const CUtensorMap *tmap_sgn = nullptr, GemmCtl *ctl = nullptr) {
+                                           const CUtensorMap *tmap_sgn = nullptr, GemmCtl *ctl = nullptr,
+                                           const CUtensorMap *tmap_aux = nullptr) {
     using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
-    static_assert(STG == 0 || (STG == 1 && SPLIT == 1 && !PLANE && EPI == kEpiFwd1),
-                  "in-kernel staging: the a-product stages x");
+    static_assert(STG == 0 || (STG == 1 && SPLIT == 1 && !PLANE && EPI == kEpiFwd1) ||
+                      (STG == 2 && SPLIT == 1 && !PLANE && EPI == kEpiBwd1),
+                  "in-kernel staging: the a-product stages x, the db-product dy");
     constexpr int kKB = S::kKBm, kStepK = S::kStepKm, kWarpEpi0 = S::kEpi0;
     constexpr int NB = S::kNB, NS = S::kNS, kChunks = S::kChunks, kNE = S::kNE;
     uint8_t *sB = L.sB;
@@ -864,14 +867,24 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
             // (the a-product has no epilogue input and no sign plane: those two
             // maps are x, f32, in 256 x 16 boxes for the ring and 256 x 64 for
             // the L2 prefetches)
-            if (t < kStgConvThreads)
-                stager_x_convert(X, t, abort_flag, L.sStg, L.stg_full, L.stg_empty, ctl->stg_geo, &ctl->stg_done,
-                                 args.status);
-            else if (t == kStgConvThreads)
-                stager_x_producer(X, &tmap_in, abort_flag, L.sStg, L.stg_full, L.stg_empty, ctl->stg_geo,
-                                  args.status);
-            else if (t == kStgConvThreads + 32)
-                stager_x_publisher(X, tmap_sgn, abort_flag, &ctl->stg_done, args.status);
+            // (the db-product has no f32 output and no sign plane: those two
+            // maps are dy, f32, in 256 x 16 and 256 x 64 boxes; tmap_aux is c)
+            if constexpr (STG == 1) {
+                if (t < kStgConvThreads)
+                    stager_x_convert(X, t, abort_flag, L.sStg, L.stg_full, L.stg_empty, ctl->stg_geo,
+                                     &ctl->stg_done, args.status);
+                else if (t == kStgConvThreads)
+                    stager_x_producer(X, &tmap_in, abort_flag, L.sStg, L.stg_full, L.stg_empty, ctl->stg_geo,
+                                      args.status);
+            } else {
+                if (t < kStgConvThreads)
+                    stager_dy_convert(X, t, abort_flag, L.sStg, L.stg_full, L.stg_empty, ctl->stg_geo,
+                                      &ctl->stg_done, args.status);
+                else if (t == kStgConvThreads)
+                    stager_dy_producer(X, &tmap_out32, tmap_aux, abort_flag, L.sStg, L.stg_full, L.stg_empty,
+                                       ctl->stg_geo, args.status);
+            }
+            if (t == kStgConvThreads + 32) stager_x_publisher(X, tmap_sgn, abort_flag, &ctl->stg_done, args.status);
             __syncwarp();
         }
     }
@@ -889,12 +902,17 @@ __device__ __forceinline__ void gemm_roles(const GemmLayout<EPI, PAIR, BT, PLANE
 template <int EPI, bool PAIR, int BT, bool PLANE = false, int STG = 0>
 __device__ __forceinline__ void gemm_prefetch_maps(const CUtensorMap &tmap_act, const CUtensorMap &tmap_in,
                                                    const CUtensorMap &tmap_out32, const CUtensorMap &tmap_out16,
-                                                   const CUtensorMap *tmap_sgn = nullptr) {
+                                                   const CUtensorMap *tmap_sgn = nullptr,
+                                                   const CUtensorMap *tmap_aux = nullptr) {
     using S = GemmShape<EPI, PAIR, BT, PLANE, STG>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     if (warp == kWarpTma && lane == 0) {
         tma_prefetch_desc(&tmap_act);
         if (PLANE || S::kStgSlots) tma_prefetch_desc(tmap_sgn);
+        if (STG == 2) {
+            tma_prefetch_desc(&tmap_out32);
+            tma_prefetch_desc(tmap_aux);
+        }
     }
     if (warp == S::kEpi0 && lane == 0) {
         if (EPI != kEpiFwd1 || S::kStgSlots) tma_prefetch_desc(&tmap_in);
@@ -953,7 +971,8 @@ template <int EPI, bool PAIR, int BT, bool PLANE, int SPLIT, int STG>
 __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads, 1)
     blr_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ CUtensorMap tmap_in,
                     const __grid_constant__ CUtensorMap tmap_out32, const __grid_constant__ CUtensorMap tmap_out16,
-                    const __grid_constant__ CUtensorMap tmap_sgn, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmap_sgn, const __grid_constant__ CUtensorMap tmap_aux,
+                    const GemmArgs args) {
     uint8_t *smem = smem_base_1024();
     GemmCtl *ctl = reinterpret_cast<GemmCtl *>(smem);
     const GemmLayout<EPI, PAIR, BT, PLANE, STG> L(smem + kCtlBytes);
@@ -964,7 +983,7 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads
         ctl->stg_done = 0;
         fence_mbar_init();
     }
-    gemm_prefetch_maps<EPI, PAIR, BT, PLANE, STG>(tmap_act, tmap_in, tmap_out32, tmap_out16, &tmap_sgn);
+    gemm_prefetch_maps<EPI, PAIR, BT, PLANE, STG>(tmap_act, tmap_in, tmap_out32, tmap_out16, &tmap_sgn, &tmap_aux);
     if constexpr (PAIR) {
         cluster_sync();  // both CTAs' barriers exist before any remote arrival
         if (warp == kWarpMma) {
@@ -990,7 +1009,7 @@ __global__ void __launch_bounds__(GemmShape<EPI, PAIR, BT, PLANE, STG>::kThreads
     const int num_units = (int)gridDim.x / per_unit;
     gemm_roles<EPI, PAIR, BT, PLANE, SPLIT, STG>(L, tmap_act, tmap_in, tmap_out32, tmap_out16, args, tmem_base,
                                                  reinterpret_cast<volatile int *>(&ctl->abort_flag), unit, num_units,
-                                                 &tmap_sgn, ctl);
+                                                 &tmap_sgn, ctl, &tmap_aux);
     tc_fence_before();
     if constexpr (PAIR) {
         // neither CTA leaves while the pair's MMAs or remote arrivals may still touch it
@@ -1027,7 +1046,7 @@ cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmArgs &args, int grid, 
     cfg.attrs = attr;
     cfg.numAttrs = (PAIR || SPLIT > 1) ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, blr_gemm_kernel<EPI, PAIR, BT, PLANE, SPLIT, STG>, maps.act, maps.in32,
-                              maps.out32, maps.out16, maps.sgn, args);
+                              maps.out32, maps.out16, maps.sgn, maps.aux, args);
 }
 
 // Tile configurations: CTA pairs with 160 or 192 tokens per tile, single CTAs

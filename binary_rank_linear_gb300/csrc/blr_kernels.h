@@ -123,6 +123,14 @@ struct StageDyArgs {
     int *rows_used;        // host out: dh partial rows the launch wrote
     uint32_t *status;      // device status word (bounded waits of the streaming staging)
     unsigned int *red_cnt; // zeroed by the launch (the dx'-product's reduction counter), or null
+    // scale pass (dy staged inside the db-product, STG = 2): the launch writes
+    // only s_inv, sig, sig_inv and blkmax (no dy16, no dh sums; c16 unread),
+    // and zeroes n_cnt stager counters at zero_cnt and n_part floats of dh
+    // partial rows at zero_part
+    unsigned int *zero_cnt;
+    int n_cnt;
+    float *zero_part;
+    long long n_part;
 };
 int stage_dy_blocks(int M, int d_out);  // dh partial rows reserved in the workspace
 // per path of a group; M, d_out, r, gscale, dy and rows_used are taken from
@@ -141,6 +149,15 @@ inline cudaError_t launch_bwd_prologue(SignPrep p0, SignPrep p1, const StageDyAr
     grp.e[0] = BwdPathArgs{p0, p1, a};
     grp.n = 1;
     return launch_bwd_prologue(grp, s);
+}
+// The scale pass only (a.zero_cnt / a.zero_part set): per-row scales, block
+// maxima, the bitmap re-layouts; the db-product then stages dy itself.
+cudaError_t launch_bwd_scales(const BwdGroup &grp, cudaStream_t s);
+inline cudaError_t launch_bwd_scales(SignPrep p0, SignPrep p1, const StageDyArgs &a, cudaStream_t s) {
+    BwdGroup grp{};
+    grp.e[0] = BwdPathArgs{p0, p1, a};
+    grp.n = 1;
+    return launch_bwd_scales(grp, s);
 }
 
 // out[f] += sum_p part[p][f] over three independent segments, fixed order.
@@ -186,6 +203,10 @@ __host__ __device__ constexpr int epi_part_rows_per_tile(int epi) { return epi_w
 // Columns per readiness chunk (two 128-deep k-steps); the host sizes and
 // zeroes the counters with it.
 constexpr int kStageChunkCols = 256;
+// dh partial rows per CTA of a db-product that stages dy (one per converter warp)
+constexpr int kDyPartRowsPerCta = 4;
+// CTAs such a launch may have: the workspace reserves dh partial rows for them
+constexpr int kDyStageMaxCtas = 160;
 inline int stage_counters(int M, int bt, int K) {
     return (M + bt - 1) / bt * ((K + kStageChunkCols - 1) / kStageChunkCols);
 }
@@ -208,10 +229,17 @@ struct GridBarrier {
 };
 
 struct StageArgs {
-    const float *src;      // x [M][K] f32
-    const float *col;      // g [K]
-    uint16_t *dst;         // x16 [M][K]
+    const float *src;      // x [M][K] f32 (STG = 2: dy [M][d_out])
+    const float *col;      // g [K] (STG = 2: h [d_out])
+    uint16_t *dst;         // x16 [M][K] (STG = 2: dy16)
     unsigned int *cnt;     // [token tiles][column chunks] rows staged (zeroed before the launch)
+    // dy staged inside the db-product (STG = 2): each row's 1/s_t (written by
+    // the scale pass before the launch), and the dh partial rows,
+    // kDyPartRowsPerCta per CTA (part + (blockIdx.x * kDyPartRowsPerCta + w) * K
+    // floats for converter warp w, zeroed before the launch; each warp adds its
+    // items' column sums of dy.c into its own row)
+    const float *row_sinv;
+    float *part;
     // multi-path launches (paths > 1): path p's g at col_p[p], its x16 and
     // counters at p * pstride bytes after path 0's; the stagers take the
     // paths' token tiles in the product's path-major order
@@ -273,6 +301,7 @@ inline int sign_rows(int N) { return (N + 255) / 256 * 256; }
 // the c- and dx'-products [N][K] read K-major (box 64 K x 128 features).
 struct GemmMaps {
     CUtensorMap act, in32, out32, out16, sgn;
+    CUtensorMap aux;  // STG = 2: the c tape in 256 x 16 boxes (unused otherwise)
 };
 
 // Tile plan of one GEMM launch: CTA pairs (tcgen05 cta_group::2) with 160 or

@@ -58,9 +58,9 @@ inline Layout make_layout(int M, int d_in, int d_out, int r) {
     L.a32 = take(m * r * 4);
     L.al16 = take(m * r * 2);
     L.c16 = take(m * d_out * 2);
-    // row counters of the in-kernel x staging: one per (token tile of at
-    // least 32 tokens, column chunk of d_in)
-    L.stg_cnt = take((size_t)stage_counters(M, 32, d_in) * 4);
+    // row counters of the in-kernel x and dy staging: one per (token tile of
+    // at least 32 tokens, column chunk of d_in or d_out)
+    L.stg_cnt = take((size_t)stage_counters(M, 32, d_in > d_out ? d_in : d_out) * 4);
     L.fwd_total = off;
     // backward: re-laid S_U (N = r, K = d_out) and S_V (N = d_in, K = r); the
     // f16 staging of all four products stays in place after the pass (the
@@ -72,7 +72,10 @@ inline Layout make_layout(int M, int d_in, int d_out, int r) {
     L.s_inv = take(m * 4);
     L.sig = take(m * 4);
     L.sig_inv = take(m * 4);
+    // dh partial rows: the prologue's blocks, or the converter warps of a
+    // db-product that stages dy (kDyPartRowsPerCta per CTA)
     L.rows_dh = stage_dy_blocks(M, d_out);
+    if (L.rows_dh < kDyPartRowsPerCta * kDyStageMaxCtas) L.rows_dh = kDyPartRowsPerCta * kDyStageMaxCtas;
     L.blkmax = take((size_t)L.rows_dh * 8);
     // partial rows per token tile (tiles of at least 128 tokens; split-K
     // db-products write one per quarter of K, the token-major dx'-product four

@@ -35,10 +35,12 @@
 // together). A bounded wait that runs out, or the CTA's abort flag, stops
 // them; the copy producer then waits for the copies it issued.
 //
-// (The db-product's dy staging stays a stand-alone pass: its per-token scale
-// needs a row-wide maximum, and its dh sums a per-column accumulator over the
-// CTA's rows, which two stager warps could only keep in global memory; a
-// version that did ran latency-bound at a fraction of the pass's rate.)
+// The db-product's operand dy16 = f16(dy.h.s_t) is staged the same way
+// (GEMM template STG = 2) once a scale pass has written each row's 1/s_t:
+// a ring unit then also carries the c tape's 16 x 256 tile and the rows'
+// scales, and the converters add each item's column sums of dy.c (the dh
+// partial sums) into partial rows of their own (one per converter warp and
+// CTA), so that no two warps ever add into the same row.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -67,6 +69,18 @@ constexpr int kStgSlotsX = 3;
 constexpr int kStgRingBytes = kStgSlotsX * kStgSlotX;
 constexpr int kStgPrefetchItems = 2;  // items prefetched into L2 ahead of the one being converted
 static_assert(kStgSlotsX >= 2 && kStgSlotsX <= kStgSlotsMax, "stager ring");
+// dy items (STG = 2): a slot holds the unit's dy tile (256 x 16 f32), its c
+// tile (256 x 16 f16), the chunk's 256 h factors and the unit's 16 row scales
+// 1/s_t; slots stay 128-byte aligned for the TMA boxes
+constexpr int kStgCOff = kStgTileBytes;
+constexpr int kStgHOff = kStgCOff + kStgUnitRows * kStgKC * 2;
+constexpr int kStgSOff = kStgHOff + kStgKC * 4;
+constexpr int kStgSlotDy = kStgSOff + 128;
+constexpr int kStgSlotsDy = 3;
+constexpr int kStgRingBytesDy = kStgSlotsDy * kStgSlotDy;
+static_assert(kStgSlotDy % 128 == 0 && kStgCOff % 128 == 0, "stager slots hold TMA boxes");
+static_assert(kStgSlotsDy >= 2 && kStgSlotsDy <= kStgSlotsMax, "stager ring");
+static_assert(kStgConvWarps == kDyPartRowsPerCta, "one dh partial row per converter warp");
 
 __host__ __device__ constexpr int stg_chunks(int K) { return (K + kStgKC - 1) / kStgKC; }
 static_assert(kStgKC == 8 * 32, "a chunk row is eight columns per lane of a converter warp");
@@ -385,6 +399,149 @@ __device__ inline void stager_x_convert(const StgX &X, int t, volatile int *abor
             va[i][1] = vb[i][1];
         }
         got_a = got_b;
+    }
+}
+
+
+// ---- dy: dy16 = f16(dy.h.s_t) and the dh partial sums (STG = 2) -----------
+// lane 0 of the producer warp: ring units by TMA (the dy tile and the c tile),
+// S ahead of the converters, with the chunk's h factors and the unit's row
+// scales. Single-path launches only.
+__device__ inline void stager_dy_producer(const StgX &X, const CUtensorMap *tmap_dy, const CUtensorMap *tmap_c,
+                                          volatile int *abort_flag, uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                          StgGeo *geo, uint32_t *status) {
+    constexpr int S = kStgSlotsDy;
+    const uint64_t once = l2_policy_evict_first();
+    XCursor ci{0, 0, 0, 0, 0, 0, 0, 0, 0};
+    x_cursor_load(ci, X.G, X.mine, X.cta, X.nctas);
+    long long u = 0;
+    for (; u < X.units; ++u) {
+        const int sl = (int)(u % S);
+        if (u >= S && !mbar_wait(&empty[sl], (uint32_t)(((u / S) - 1) & 1), abort_flag)) break;
+        const int q0 = ci.r0 + kStgUnitRows * ci.s;
+        int nq = ci.r0 + ci.nr - q0;
+        nq = nq < 0 ? 0 : (nq > kStgUnitRows ? kStgUnitRows : nq);
+        geo[sl] = StgGeo{q0, nq, ci.c0, 0};
+        uint8_t *slot = ring + sl * kStgSlotDy;
+        // boxes past dy's rows read zero; a unit with no rows takes row 0's
+        // scales (never used), so that the copy stays inside the scale array
+        mbar_arrive_expect_tx(&full[sl], (uint32_t)(kStgTileBytes + kStgUnitRows * kStgKC * 2 + ci.w * 4 +
+                                                    kStgUnitRows * 4));
+        tma_load_2d_hint(slot, tmap_dy, &full[sl], ci.c0, q0, once);
+        tma_load_2d_hint(slot + kStgCOff, tmap_c, &full[sl], ci.c0, q0, once);
+        bulk_load(slot + kStgHOff, X.a.col + ci.c0, (uint32_t)ci.w * 4, &full[sl]);
+        bulk_load(slot + kStgSOff, X.a.row_sinv + (nq > 0 ? q0 : 0), kStgUnitRows * 4, &full[sl]);
+        x_cursor_next(ci, X.G, X.mine, X.cta, X.nctas);
+    }
+    // every copy issued lands before the CTA may exit
+    for (long long v = (u > S ? u - S : 0); v < u; ++v)
+        if (!mbar_wait(&full[v % S], (uint32_t)((v / S) & 1), abort_flag, false)) atomicOr(status, kStTimeoutDrain);
+}
+
+// converter warps: as for x, thread t converts columns 8 (t % 32) .. + 7 of
+// the chunk in rows t / 32, t / 32 + kStgConvWarps, ... of each unit (16-byte
+// stores), and sums dy.c of those columns over the item's rows; each warp
+// adds its sums into a partial row of its own (kStgConvWarps rows per CTA),
+// so the warp's item order fixes every column's summation order.
+__device__ inline void stager_dy_convert(const StgX &X, int t, volatile int *abort_flag, uint8_t *ring,
+                                         uint64_t *full, uint64_t *empty, const StgGeo *geo, unsigned int *done,
+                                         uint32_t *status) {
+    constexpr int S = kStgSlotsDy;
+    constexpr int kRows = kStgUnitRows / kStgConvWarps;
+    const int cg = t & 31, rp = t >> 5, lane = t & 31;
+    const int K = (int)X.G.K;
+    float *prow = X.a.part + ((size_t)blockIdx.x * kStgConvWarps + rp) * K;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    int col = 0;
+    bool ok = true;
+    for (long long u = 0; u < X.units; ++u) {
+        const int sl = (int)(u % S);
+        const bool got = mbar_wait(&full[sl], (uint32_t)((u / S) & 1), abort_flag);
+        if (!got && !*abort_flag) {
+            *abort_flag = 1;
+            atomicOr(status, kStTimeoutStage);
+        }
+        if (got) {
+            const StgGeo gq = geo[sl];
+            const uint8_t *slot = ring + sl * kStgSlotDy;
+            col = gq.c0 + 8 * cg;
+            if (col < K) {
+                const float4 *sd = reinterpret_cast<const float4 *>(slot) + 2 * cg;
+                const uint4 *sc = reinterpret_cast<const uint4 *>(slot + kStgCOff) + cg;
+                const float4 h0 = reinterpret_cast<const float4 *>(slot + kStgHOff)[2 * cg];
+                const float4 h1 = reinterpret_cast<const float4 *>(slot + kStgHOff)[2 * cg + 1];
+                const float *sv = reinterpret_cast<const float *>(slot + kStgSOff);
+                float4 d0[kRows], d1[kRows];
+                uint4 cw[kRows];
+                float sr[kRows];
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) {
+                    const int row = rp + kStgConvWarps * i;
+                    if (row < gq.nq) {
+                        d0[i] = sd[row * (kStgKC / 4)];
+                        d1[i] = sd[row * (kStgKC / 4) + 1];
+                        cw[i] = sc[row * (kStgKC / 8)];
+                        sr[i] = sv[row];
+                    }
+                }
+                uint16_t *dst = X.a.dst + (size_t)(gq.q0 + rp) * K + col;
+#pragma unroll
+                for (int i = 0; i < kRows; ++i) {
+                    if (rp + kStgConvWarps * i < gq.nq) {
+                        // f16(round(dy.h) s_t): s_t is a power of two, so the
+                        // scaling is exact and the bits match the prologue's
+                        const float s = pow2_recip(sr[i]);
+                        const float v[8] = {d0[i].x * h0.x, d0[i].y * h0.y, d0[i].z * h0.z, d0[i].w * h0.w,
+                                            d1[i].x * h1.x, d1[i].y * h1.y, d1[i].z * h1.z, d1[i].w * h1.w};
+                        uint4 o;
+                        o.x = pack_half2(v[0] * s, v[1] * s);
+                        o.y = pack_half2(v[2] * s, v[3] * s);
+                        o.z = pack_half2(v[4] * s, v[5] * s);
+                        o.w = pack_half2(v[6] * s, v[7] * s);
+                        *reinterpret_cast<uint4 *>(dst + (size_t)i * kStgConvWarps * K) = o;
+                        const uint32_t cws[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+                        const float dv[8] = {d0[i].x, d0[i].y, d0[i].z, d0[i].w, d1[i].x, d1[i].y, d1[i].z, d1[i].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 c2 = __half22float2(*reinterpret_cast<const __half2 *>(&cws[j]));
+                            acc[2 * j] += dv[2 * j] * c2.x;
+                            acc[2 * j + 1] += dv[2 * j + 1] * c2.y;
+                        }
+                    }
+                }
+            }
+        }
+        // unit u's slot goes back to the producer once the whole warp has read it
+        const bool warp_got = __all_sync(0xFFFFFFFFu, got);
+        if (warp_got && lane == 0) mbar_arrive(&empty[sl]);
+        ok = ok && warp_got;
+        if (u % kStgUnitsX == kStgUnitsX - 1) {
+            if (!ok || *abort_flag) break;
+            // the item's column sums into this warp's partial row
+            if (col < K) {
+                float4 *pr = reinterpret_cast<float4 *>(prow + col);
+                float4 a0 = pr[0], a1 = pr[1];
+                a0.x += acc[0];
+                a0.y += acc[1];
+                a0.z += acc[2];
+                a0.w += acc[3];
+                a1.x += acc[4];
+                a1.y += acc[5];
+                a1.z += acc[6];
+                a1.w += acc[7];
+                pr[0] = a0;
+                pr[1] = a1;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+            // the item's rows are written: proxy fence (other CTAs' TMA loads
+            // read them), then this warp's arrival on the item counter
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) red_release_shared_add_u32(done, 1u);
+        }
     }
 }
 

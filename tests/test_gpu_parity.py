@@ -223,6 +223,41 @@ def test_reduction_folded_and_separate(monkeypatch, M, d_in, d_out, r):
         assert oracle.rel_err(a[k], bw[k]) <= TOL_GRAD, k
 
 
+@pytest.mark.parametrize("M,d_in,d_out,r,gscale", [
+    (8192, 512, 1024, 512, 0.0),        # CTA-pair tiles of the db-product, dynamic scales
+    (8000, 256, 2048, 512, 0.0),        # a ragged last token tile
+    (8192, 512, 1024, 512, 2.0 ** 8),   # a fixed power-of-two gscale
+    (6000, 256, 8448, 512, 0.0),        # rows wider than the streaming prologue's
+])
+def test_dy_staged_in_the_db_product(monkeypatch, M, d_in, d_out, r, gscale):
+    """dy16 staged by the db-product's stager warps after a scale pass
+    (BLR_DY_STAGE=kernel) against the backward prologue's staging (=pass):
+    the same dy16, scales and tiles, so y, dx, dl and dg are bit-identical and
+    dh (summed by the stager warps in another fixed order) equal to rounding,
+    both within the oracle's tolerance; the staged product did run, and the
+    default is the prologue form."""
+    import binary_rank_linear_gb300 as blr
+    t = wl.make_inputs(wl.WORKLOADS["small"].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
+    monkeypatch.setenv("BLR_DY_STAGE", "pass")
+    b = _run(t, gscale=gscale)
+    monkeypatch.setenv("BLR_DY_STAGE", "kernel")
+    blr.trace_begin(64)
+    a = _run(t, gscale=gscale)
+    names = [n for n, _ in blr.trace_end()]
+    assert "gemm_bwd1s" in names and "bwd_scales" in names, names
+    assert a["status"] == 0 and b["status"] == 0
+    for k in ("y", "dx", "dl", "dg"):
+        assert np.array_equal(a[k], b[k]), k
+    assert oracle.rel_err(a["dh"], b["dh"]) <= 1e-5
+    _check_against_oracle(t, a)
+    monkeypatch.delenv("BLR_DY_STAGE")
+    blr.trace_begin(64)
+    c = _run(t, gscale=gscale)
+    assert "gemm_bwd1s" not in [n for n, _ in blr.trace_end()]
+    for k in ("y", "dx", "dh", "dl", "dg"):
+        assert np.array_equal(b[k], c[k]), k
+
+
 def test_deterministic():
     w = wl.WORKLOADS["small"].with_shape(M=300, d_in=256, d_out=256, r=128)
     t = wl.make_inputs(w)
