@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(256) prep_group_kernel(const FwdGroup grp, uns
     prep_share(a.p0, a.p1, blockIdx.x, gridDim.x);
 }
 
-// The scale pass (SC) also zeroes the db-product's stager counters and dh
-// partial rows before any of its other work.
+// The scale pass zeroes the db-product's stager counters and dh partial rows
+// before any of its other work.
 __device__ __forceinline__ void scale_pass_zero(const StageDyArgs &a) {
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long nth = (long long)gridDim.x * blockDim.x;
@@ -147,7 +147,7 @@ __device__ __forceinline__ void scale_pass_zero(const StageDyArgs &a) {
     for (long long i = tid; i < a.n_part / 4; i += nth) p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-template <int GPT, int THREADS, bool SC = false>
+template <int GPT, int THREADS>
 __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
     bwd_prologue_kernel(const BwdGroup grp, int stage_blocks) {
     extern __shared__ __align__(16) float smem_f[];
@@ -155,9 +155,8 @@ __global__ void __launch_bounds__(THREADS, (THREADS <= 512 && GPT <= 8 ? 2 : 1))
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0 && e.sd.red_cnt) *e.sd.red_cnt = 0u;
-    if (SC) scale_pass_zero(e.sd);
     if (prologue_prep(e.p0, e.p1, stage_blocks)) return;
-    stage_dy_run<GPT, SC>(e.sd, blockIdx.x, stage_blocks, smem_f, stage_tpr(e.sd.d_out, THREADS), THREADS);
+    stage_dy_run<GPT>(e.sd, blockIdx.x, stage_blocks, smem_f, stage_tpr(e.sd.d_out, THREADS), THREADS);
 }
 
 // ============================================== scale pass (STG = 2) =======
@@ -256,7 +255,7 @@ __global__ void __launch_bounds__(kScaleThreads, 1) bwd_scale_kernel(const BwdGr
 // Streaming form of the same prologue (rows up to kSdMaxCols wide): one block
 // per SM, a producer warp feeding row batches through a shared-memory ring.
 // Blocks past stage_blocks only do bitmap re-layouts.
-template <int Q, bool SC = false>
+template <int Q>
 __global__ void __launch_bounds__(kSdThreads, 1)
     bwd_stream_kernel(const BwdGroup grp, int stage_blocks) {
     extern __shared__ __align__(128) unsigned char smem_b[];
@@ -264,13 +263,12 @@ __global__ void __launch_bounds__(kSdThreads, 1)
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0 && e.sd.red_cnt) *e.sd.red_cnt = 0u;
-    if (SC) scale_pass_zero(e.sd);
     const int extra = (int)gridDim.x - stage_blocks;
     if (extra > 0 && (int)blockIdx.x >= stage_blocks) {
         prep_share(e.p0, e.p1, (int)blockIdx.x - stage_blocks, extra);
         return;
     }
-    stage_dy_stream<Q, SC>(e.sd, blockIdx.x, stage_blocks, smem_b, e.p0, e.p1, extra > 0 ? 0 : stage_blocks);
+    stage_dy_stream<Q>(e.sd, blockIdx.x, stage_blocks, smem_b, e.p0, e.p1, extra > 0 ? 0 : stage_blocks);
 }
 
 int stage_dy_blocks(int M, int d_out) {
@@ -483,16 +481,16 @@ cudaError_t launch_fwd_prologue(const FwdGroup &grp, const float *x, int M, int 
     return e;
 }
 
-template <int GPT, int THREADS = kStageThreads, bool SC = false>
+template <int GPT, int THREADS = kStageThreads>
 static cudaError_t launch_bwd_prologue_t(const BwdGroup &grp, cudaStream_t s) {
     const StageDyArgs &a = grp.e[0].sd;
     const SignPrep &p0 = grp.e[0].p0, &p1 = grp.e[0].p1;
     const int tpr = stage_tpr(a.d_out, THREADS);
     const int rb_n = THREADS / tpr;
     const size_t smem = stage_dy_smem_bytes(a.d_out, tpr, rb_n * tpr);
-    cudaError_t pe = prepare_kernel_once(bwd_prologue_kernel<GPT, THREADS, SC>, 200 * 1024);
+    cudaError_t pe = prepare_kernel_once(bwd_prologue_kernel<GPT, THREADS>, 200 * 1024);
     if (pe != cudaSuccess) return pe;
-    const int per_sm = occupancy_blocks(reinterpret_cast<const void *>(bwd_prologue_kernel<GPT, THREADS, SC>), THREADS,
+    const int per_sm = occupancy_blocks(reinterpret_cast<const void *>(bwd_prologue_kernel<GPT, THREADS>), THREADS,
                                         smem);
     const int sms = current_device_sms();
     int sb = stage_dy_blocks(a.M, a.d_out);
@@ -500,19 +498,18 @@ static cudaError_t launch_bwd_prologue_t(const BwdGroup &grp, cudaStream_t s) {
     // re-layout-only blocks where the wave has room for them
     const int pb = prep_blocks(p0, THREADS) + prep_blocks(p1, THREADS);
     const int grid = sb + pb <= per_sm * sms ? sb + pb : sb;
-    trace_before(SC ? "bwd_scales" : "bwd_prologue", s);
-    cudaError_t e =
-        launch_k(bwd_prologue_kernel<GPT, THREADS, SC>, dim3(grid, grp.n), dim3(THREADS), smem, s, grp, sb);
+    trace_before("bwd_prologue", s);
+    cudaError_t e = launch_k(bwd_prologue_kernel<GPT, THREADS>, dim3(grid, grp.n), dim3(THREADS), smem, s, grp, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;
 }
 
-template <int Q, bool SC = false>
+template <int Q>
 static cudaError_t launch_bwd_stream_t(const BwdGroup &grp, cudaStream_t s) {
     const StageDyArgs &a = grp.e[0].sd;
     const SignPrep &p0 = grp.e[0].p0, &p1 = grp.e[0].p1;
-    cudaError_t pe = prepare_kernel_once(bwd_stream_kernel<Q, SC>, kSdHeadBytes + kSdRingBytes);
+    cudaError_t pe = prepare_kernel_once(bwd_stream_kernel<Q>, kSdHeadBytes + kSdRingBytes);
     if (pe != cudaSuccess) return pe;
     const int sms = current_device_sms();
     const SdPlan pl = sd_plan(a.d_out);
@@ -523,9 +520,9 @@ static cudaError_t launch_bwd_stream_t(const BwdGroup &grp, cudaStream_t s) {
     // re-layout-only blocks on SMs the staging leaves idle
     const int pb = prep_blocks(p0, kSdThreads) + prep_blocks(p1, kSdThreads);
     const int grid = sb + pb <= sms ? sb + pb : sb;
-    trace_before(SC ? "bwd_scales" : "bwd_prologue", s);
-    cudaError_t e = launch_k(bwd_stream_kernel<Q, SC>, dim3(grid, grp.n), dim3(kSdThreads), sd_smem_bytes(a.d_out),
-                             s, grp, sb);
+    trace_before("bwd_prologue", s);
+    cudaError_t e = launch_k(bwd_stream_kernel<Q>, dim3(grid, grp.n), dim3(kSdThreads), sd_smem_bytes(a.d_out), s,
+                             grp, sb);
     trace_after(s);
     if (e == cudaSuccess && a.rows_used) *a.rows_used = sb;
     return e;
@@ -538,37 +535,34 @@ static bool dy_stage_rows_forced() {
     return e && std::strcmp(e, "rows") == 0;
 }
 
-template <bool SC>
-static cudaError_t launch_bwd_prologue_sc(const BwdGroup &grp, cudaStream_t s) {
+cudaError_t launch_bwd_prologue(const BwdGroup &grp, cudaStream_t s) {
     if (grp.n < 1 || grp.n > kMaxGroupPaths) return cudaErrorInvalidValue;
     const StageDyArgs &a = grp.e[0].sd;
     if (sd_supported(a.d_out) && !dy_stage_rows_forced()) {
         switch (sd_plan(a.d_out).Q) {
-            case 2: return launch_bwd_stream_t<2, SC>(grp, s);
-            case 4: return launch_bwd_stream_t<4, SC>(grp, s);
-            case 6: return launch_bwd_stream_t<6, SC>(grp, s);
-            default: return launch_bwd_stream_t<8, SC>(grp, s);
+            case 2: return launch_bwd_stream_t<2>(grp, s);
+            case 4: return launch_bwd_stream_t<4>(grp, s);
+            case 6: return launch_bwd_stream_t<6>(grp, s);
+            default: return launch_bwd_stream_t<8>(grp, s);
         }
     }
     switch (stage_gpt(a.d_out)) {
-        case 1: return launch_bwd_prologue_t<1, kStageThreads, SC>(grp, s);
-        case 2: return launch_bwd_prologue_t<2, kStageThreads, SC>(grp, s);
+        case 1: return launch_bwd_prologue_t<1>(grp, s);
+        case 2: return launch_bwd_prologue_t<2>(grp, s);
         case 3:
-        case 4: return launch_bwd_prologue_t<4, kStageThreads, SC>(grp, s);
+        case 4: return launch_bwd_prologue_t<4>(grp, s);
         case 5:
         case 6:
         case 7:
-        case 8: return launch_bwd_prologue_t<8, kStageThreads, SC>(grp, s);
+        case 8: return launch_bwd_prologue_t<8>(grp, s);
         default: break;
     }
     // rows wider than 16384: 1024-thread blocks, 8 groups per thread (measured
     // on GB300, 4000 rows of 32768: 271 -> 228 us against 512 threads with 16;
     // at 12288 the 512-thread blocks stay faster, 293 against 310 us)
-    if (stage_gpt(a.d_out, 1024) <= 8) return launch_bwd_prologue_t<8, 1024, SC>(grp, s);
+    if (stage_gpt(a.d_out, 1024) <= 8) return launch_bwd_prologue_t<8, 1024>(grp, s);
     return cudaErrorInvalidValue;
 }
-
-cudaError_t launch_bwd_prologue(const BwdGroup &grp, cudaStream_t s) { return launch_bwd_prologue_sc<false>(grp, s); }
 
 // The scale pass ahead of a db-product that stages dy itself (StageDyArgs
 // zero_cnt, zero_part): one block of bwd_scale_kernel per SM, plus blocks

@@ -419,8 +419,7 @@ __host__ __device__ inline size_t stage_dy_smem_bytes(int d_out, int tpr, int nt
     return (kStageRedFloats + (size_t)(nthr / tpr) * d_out) * sizeof(float);
 }
 
-// SC: the scale pass only (as stage_dy_stream).
-template <int GPT, bool SC = false>
+template <int GPT>
 __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float *smem, int tpr, int nthr) {
     const int rb_n = nthr / tpr;
     const int wpr = tpr / 32;  // warps per row
@@ -448,7 +447,7 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
 #pragma unroll
     for (int g = 0; g < GPT; ++g) {
         const int col = g * tpr + ti;
-        if (!SC && active && col < G) dh_s[rb * G + col] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (active && col < G) dh_s[rb * G + col] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
     const int batches = (a.M + rb_n - 1) / rb_n;
@@ -459,7 +458,7 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
         const int r0 = bt * rb_n;
         const int nr = a.M - r0 < rb_n ? a.M - r0 : rb_n;
         bulk_prefetch_l2(a.dy + (size_t)r0 * a.d_out, (uint32_t)((size_t)nr * a.d_out * 4));
-        if (!SC) bulk_prefetch_l2(a.c16 + (size_t)r0 * a.d_out, (uint32_t)((size_t)nr * a.d_out * 2));
+        bulk_prefetch_l2(a.c16 + (size_t)r0 * a.d_out, (uint32_t)((size_t)nr * a.d_out * 2));
     };
     prefetch_batch(block);
     int buf = 0;
@@ -477,19 +476,17 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
             if (valid && col < G) {
                 const long long idx = (long long)t * G + col;
                 const float4 d = __ldcs(dy4 + idx);
+                const uint2 cw = __ldcs(c4 + idx);
                 const float4 f = __ldg(h4 + col);
                 v[g] = make_float4(d.x * f.x, d.y * f.y, d.z * f.z, d.w * f.w);
-                if (!SC) {
-                    const uint2 cw = __ldcs(c4 + idx);
-                    const float2 c0 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.x));
-                    const float2 c1 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.y));
-                    float4 acc = dh_s[rb * G + col];
-                    acc.x += d.x * c0.x;
-                    acc.y += d.y * c0.y;
-                    acc.z += d.z * c1.x;
-                    acc.w += d.w * c1.y;
-                    dh_s[rb * G + col] = acc;
-                }
+                const float2 c0 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.x));
+                const float2 c1 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.y));
+                float4 acc = dh_s[rb * G + col];
+                acc.x += d.x * c0.x;
+                acc.y += d.y * c0.y;
+                acc.z += d.z * c1.x;
+                acc.w += d.w * c1.y;
+                dh_s[rb * G + col] = acc;
                 const float4 q = make_float4(fabsf(v[g].x), fabsf(v[g].y), fabsf(v[g].z), fabsf(v[g].w));
                 amax = fmaxf(amax, fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w)));
                 l1 += (q.x + q.y) + (q.z + q.w);
@@ -521,7 +518,7 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
 #pragma unroll
         for (int g = 0; g < GPT; ++g) {
             const int col = g * tpr + ti;
-            if (!SC && valid && col < G) {
+            if (valid && col < G) {
                 uint2 st;
                 st.x = pack_half2(v[g].x * s, v[g].y * s);
                 st.y = pack_half2(v[g].z * s, v[g].w * s);
@@ -551,7 +548,6 @@ __device__ void stage_dy_run(const StageDyArgs &a, int block, int nblocks, float
         a.blkmax[block] = mx;
     }
     // fixed-order combine of the row groups' dh sums into the block's partial row
-    if (SC) return;
     float4 *dst = reinterpret_cast<float4 *>(a.part_dh + (long long)block * a.d_out);
     for (int col = threadIdx.x; col < G; col += blockDim.x) {
         float4 acc = dh_s[col];
@@ -629,9 +625,7 @@ __host__ __device__ inline size_t sd_smem_bytes(int d_out) {
 // re-layouts, while the producer's first copies are in flight (interleaving
 // it with the consumers' waits, as the x staging does, measured slower here:
 // the consumers' registers are short).
-// SC: the scale pass only (per-row scales and block maxima; no c16, no dy16,
-// no dh sums).
-template <int Q, bool SC = false>
+template <int Q>
 __device__ void stage_dy_stream(const StageDyArgs &a, int block, int nblocks, unsigned char *smem,
                                 const SignPrep &p0, const SignPrep &p1, int prep_nblocks) {
     const SdPlan pl = sd_plan(a.d_out);
@@ -667,10 +661,9 @@ __device__ void stage_dy_stream(const StageDyArgs &a, int block, int nblocks, un
         const int r = row0 + i * pl.ngrp;
         const int nr = row1 - r < pl.ngrp ? row1 - r : pl.ngrp;
         unsigned char *dst = ring + (size_t)st * pl.batch_bytes;
-        mbar_arrive_expect_tx(&full[st], (uint32_t)nr * a.d_out * (SC ? 4 : 6));
+        mbar_arrive_expect_tx(&full[st], (uint32_t)nr * a.d_out * 6);
         bulk_load_hint(dst, a.dy + (size_t)r * a.d_out, (uint32_t)nr * a.d_out * 4, &full[st], pol);
-        if (!SC)
-            bulk_load_hint(dst + dy_bytes, a.c16 + (size_t)r * a.d_out, (uint32_t)nr * a.d_out * 2, &full[st], pol);
+        bulk_load_hint(dst + dy_bytes, a.c16 + (size_t)r * a.d_out, (uint32_t)nr * a.d_out * 2, &full[st], pol);
         issued = i + 1;
     };
     if (producer) {
@@ -742,15 +735,13 @@ __device__ void stage_dy_stream(const StageDyArgs &a, int block, int nblocks, un
                 const int col = ti + k * gthreads;
                 if (col < G) {
                     const float4 d = sdy[col];
-                    if (!SC) {
-                        const uint2 cw = sc[col];
-                        const float2 c0 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.x));
-                        const float2 c1 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.y));
-                        dh[k].x += d.x * c0.x;
-                        dh[k].y += d.y * c0.y;
-                        dh[k].z += d.z * c1.x;
-                        dh[k].w += d.w * c1.y;
-                    }
+                    const uint2 cw = sc[col];
+                    const float2 c0 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.x));
+                    const float2 c1 = __half22float2(*reinterpret_cast<const __half2 *>(&cw.y));
+                    dh[k].x += d.x * c0.x;
+                    dh[k].y += d.y * c0.y;
+                    dh[k].z += d.z * c1.x;
+                    dh[k].w += d.w * c1.y;
                     const float vx = fabsf(d.x * hv[k].x), vy = fabsf(d.y * hv[k].y);
                     const float vz = fabsf(d.z * hv[k].z), vw = fabsf(d.w * hv[k].w);
                     amax = fmaxf(amax, fmaxf(fmaxf(vx, vy), fmaxf(vz, vw)));
@@ -797,7 +788,7 @@ __device__ void stage_dy_stream(const StageDyArgs &a, int block, int nblocks, un
 #pragma unroll
             for (int k = 0; k < Q; ++k) {
                 const int col = ti + k * gthreads;
-                if (!SC && col < G) {
+                if (col < G) {
                     const float4 d = sdy[col];  // re-read: fewer live registers than keeping dy.h
                     const float4 v = make_float4(d.x * hv[k].x, d.y * hv[k].y, d.z * hv[k].z, d.w * hv[k].w);
                     uint2 o;
@@ -829,8 +820,7 @@ __device__ void stage_dy_stream(const StageDyArgs &a, int block, int nblocks, un
     if (named_bar_or(9, cthreads, *abort_flag != 0)) return;  // every consumer is done with the ring
     if (lane == 0) red[2 * kSdWarps + warp] = mx;
     float4 *dst = reinterpret_cast<float4 *>(a.part_dh + (size_t)block * a.d_out);
-    if (SC) {
-    } else if (pl.ngrp == 1) {
+    if (pl.ngrp == 1) {
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
             const int col = ti + k * gthreads;
@@ -853,7 +843,7 @@ __device__ void stage_dy_stream(const StageDyArgs &a, int block, int nblocks, un
         }
         a.blkmax[block] = m;
     }
-    if (!SC && pl.ngrp > 1) {
+    if (pl.ngrp > 1) {
         const float4 *acc = reinterpret_cast<const float4 *>(ring);
         for (int col = threadIdx.x; col < G; col += cthreads) {
             float4 v = acc[col];
