@@ -81,6 +81,13 @@ def _bwd(lib, **over):
                             a["wsb"], a["s"])
 
 
+def test_workspace_reserves_the_staged_dh_rows(lib):
+    """A db-product that stages dy writes four dh partial rows per CTA (up to
+    160 CTAs) into the workspace, however few tokens the layer has."""
+    for d_out in (256, 4096, 32768):
+        assert lib.blr_workspace_bytes(64, 128, d_out, 64) >= 4 * 160 * d_out * 4
+
+
 def test_forward_argument_errors(lib):
     import binary_rank_linear_gb300 as blr
     assert _fwd(lib, x=None) == blr.BLR_ERR_ARG
