@@ -233,22 +233,26 @@ def test_dy_staged_in_the_db_product(monkeypatch, M, d_in, d_out, r, gscale):
     """dy16 staged by the db-product's stager warps after a scale pass
     (BLR_DY_STAGE=kernel) against the backward prologue's staging (=pass):
     the same dy16, scales and tiles, so y, dx, dl and dg are bit-identical and
-    dh (summed by the stager warps in another fixed order) equal to rounding,
-    both within the oracle's tolerance; the staged product did run, and the
+    dh (summed by the stager warps in another fixed order) and the sign
+    gradients (read from the same dy16) equal to rounding, all within the
+    oracle's tolerance; the staged product did run, and the
     default is the prologue form."""
     import binary_rank_linear_gb300 as blr
     t = wl.make_inputs(wl.WORKLOADS["small"].with_shape(M=M, d_in=d_in, d_out=d_out, r=r))
     monkeypatch.setenv("BLR_DY_STAGE", "pass")
-    b = _run(t, gscale=gscale)
+    b = _run(t, gscale=gscale, sign=True)
     monkeypatch.setenv("BLR_DY_STAGE", "kernel")
     blr.trace_begin(64)
-    a = _run(t, gscale=gscale)
+    a = _run(t, gscale=gscale, sign=True)
     names = [n for n, _ in blr.trace_end()]
     assert "gemm_bwd1s" in names and "bwd_scales" in names, names
     assert a["status"] == 0 and b["status"] == 0
     for k in ("y", "dx", "dl", "dg"):
         assert np.array_equal(a[k], b[k]), k
     assert oracle.rel_err(a["dh"], b["dh"]) <= 1e-5
+    # the sign gradients read the staged dy16 and the scales' block maxima
+    for k in ("gu", "gv"):
+        assert oracle.rel_err(a[k], b[k]) <= 1e-5, k
     _check_against_oracle(t, a)
     monkeypatch.delenv("BLR_DY_STAGE")
     blr.trace_begin(64)
